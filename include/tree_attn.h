@@ -1,0 +1,222 @@
+/*
+ * tree_attn.h - C ABI of the GB300 (sm_103a) tree-verify attention library.
+ *
+ * The library computes the verification step of tree speculative decoding:
+ * split-KV (flash-decoding) attention of q_l draft-tree queries per head over
+ * a KV cache, with an explicit tree mask, GQA head mapping, an online softmax
+ * (running max M and running sum S) per split and a second pass that merges
+ * the per-split partials.  A second family attends over an affine-quantized
+ * (4/8-bit packed) K/V cache with optional attention sinks, a sliding window,
+ * a boolean and an additive float mask.
+ *
+ * Sources of the operations (web pages, by title and section):
+ *   [TA-M]  mlx-native 0.9.1 src/shaders/tree_attention.metal - header comment
+ *           (explicit mask, byte-identity contract), TreeAttentionParams struct,
+ *           tree_attention_impl (chunk loop, mask early exit, QK, online softmax,
+ *           PV, partial write).
+ *   [TA-R]  mlx-native 0.9.2 src/mlx_native/ops/tree_attention.rs - validate_params,
+ *           validate_buffers, tree_attention (buffer docs, two-pass dispatch),
+ *           tmp_buffer_bytes, unit tests.
+ *   [FQS]   metaltile-std 0.1.0 src/ffai/flash_quantized_sdpa.rs - module doc
+ *           (layout, mask variants) and the three kernel macros.
+ *
+ * Conventions shared by every entry point:
+ *   - Every buffer is borrowed device memory described by a ta_buf (pointer,
+ *     usable byte count, element type).  The library never allocates, frees,
+ *     copies to the host or synchronizes; all work is enqueued on `stream`
+ *     (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *   - All argument checks run before any launch, with overflow-checked size
+ *     arithmetic.  On any non-TA_OK status nothing has been launched and no
+ *     output was touched; ta_last_error() then returns a message for the
+ *     calling thread.  TA_ERR_CUDA reports a failed launch (cudaGetLastError).
+ *   - The functions are reentrant; concurrent calls must not share tmp buffers.
+ */
+#ifndef TREE_ATTN_H_
+#define TREE_ATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TA_OK = 0,
+    TA_ERR_INVALID_ARGUMENT = 1, /* bad shape, dtype, null pointer or alignment */
+    TA_ERR_BUFFER_TOO_SMALL = 2, /* a ta_buf holds fewer bytes than the shapes need */
+    TA_ERR_OVERFLOW = 3,         /* a size computation overflows 64 bits */
+    TA_ERR_UNSUPPORTED = 4,      /* valid request the kernels do not implement */
+    TA_ERR_CUDA = 5              /* the CUDA runtime reported an error */
+} ta_status;
+
+typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2, TA_U32 = 3 } ta_dtype;
+
+/* Borrowed device buffer. `bytes` is the usable size starting at `ptr`. */
+typedef struct {
+    void *ptr;
+    uint64_t bytes;
+    int32_t dtype;    /* ta_dtype */
+    int32_t reserved; /* must be 0 */
+} ta_buf;
+
+/*
+ * Tree-attention parameters, 9 x 4 bytes = 36 bytes in the field order of the
+ * GPU params struct ([TA-M] TreeAttentionParams; [TA-R] test_gpu_params_layout).
+ *   n_heads      query heads H            n_kv_heads  KV heads Hk, H % Hk == 0
+ *   head_dim     D in {128, 256, 512}     kv_seq_len  N valid KV positions, > 0
+ *   kv_capacity  C >= N, stride (in rows) between KV heads
+ *   scale        logit = (q . k) * scale + mask
+ *   nwg          number of KV splits; 0 = library's choice (tree_attn_num_splits)
+ *   q_l          L tree nodes (queries) per head, > 0
+ *   mask_stride  floats between mask rows, >= N
+ */
+typedef struct {
+    uint32_t n_heads;
+    uint32_t n_kv_heads;
+    uint32_t head_dim;
+    uint32_t kv_seq_len;
+    uint32_t kv_capacity;
+    float scale;
+    uint32_t nwg;
+    uint32_t q_l;
+    uint32_t mask_stride;
+} ta_tree_params;
+
+/*
+ * Quantized-KV attention parameters ([FQS] module doc "Layout" and the
+ * constexpr list of the kernels), as runtime values:
+ *   batch B, n_q_heads nQ, n_kv_heads nKV (nQ % nKV == 0, repeat = nQ / nKV),
+ *   dim (a multiple of 32/bits and of group_size), tokens N > 0, bits in {4, 8},
+ *   group_size G, has_sinks in {0, 1}, window_size (0 = all tokens, else the
+ *   last window_size tokens), scale (multiplies the query), nwg (splits, 0 = auto).
+ */
+typedef struct {
+    uint32_t batch;
+    uint32_t n_q_heads;
+    uint32_t n_kv_heads;
+    uint32_t dim;
+    uint32_t tokens;
+    uint32_t bits;
+    uint32_t group_size;
+    uint32_t has_sinks;
+    uint32_t window_size;
+    float scale;
+    uint32_t nwg;
+} ta_quant_params;
+
+/* ------------------------------------------------------------------ tree */
+
+/*
+ * Bytes of the per-split partial results for n_heads * q_l rows and nwg
+ * splits: rows * nwg * (head_dim + 2) * 4, saturating at SIZE_MAX
+ * ([TA-R] tmp_buffer_bytes; 16 heads, D 256, q_l 1, NWG 32 -> 528384).
+ */
+size_t tree_attn_tmp_bytes(uint32_t n_heads, uint32_t head_dim, uint32_t q_l, uint32_t nwg);
+
+/*
+ * Number of KV splits tree_attn_fwd will use for these parameters on the
+ * current device: p->nwg when non-zero, else a choice sized to the SM count.
+ * Returns 0 when the parameters are invalid or no device is visible.
+ */
+uint32_t tree_attn_num_splits(const ta_tree_params *p);
+
+/*
+ * Bytes the `tmp` buffer of tree_attn_fwd / tree_attn_reduce must hold: the
+ * partials (tree_attn_tmp_bytes at the resolved split count) plus a small
+ * per-32-key-chunk classification area and a 16-bit copy of Q for the tensor
+ * core path.  Returns SIZE_MAX on invalid parameters or overflow.
+ */
+size_t tree_attn_workspace_bytes(const ta_tree_params *p);
+
+/*
+ * Main pass ([TA-M] tree_attention_impl; [TA-R] tree_attention, first pass).
+ *   q     [n_heads, q_l, head_dim] f32
+ *   k, v  [n_kv_heads, kv_capacity, head_dim], same dtype, f32 / f16 / bf16;
+ *         only positions [0, kv_seq_len) are read.
+ *   mask  [q_l, mask_stride] f32, 0.0 = attend, -65504.0 = masked; cells at
+ *         positions >= kv_seq_len are ignored.  The mask is added to the
+ *         scaled logit.  A 32-key chunk whose cells are all <= -65504 for a
+ *         row is skipped for that row; a chunk masked for every row is not
+ *         loaded at all.  mask.ptr == NULL selects the implicit causal mask
+ *         (tree_attn_fwd_causal with window_start 0).
+ *   tmp   f32, >= tree_attn_workspace_bytes(p) bytes, 16-byte aligned.
+ *   out   [q_l, n_heads, head_dim] f32 (query-outer, head-inner: NOT Q's layout).
+ * With one split the normalized output is written to `out` here and
+ * tree_attn_reduce is a no-op; otherwise `out` is written by tree_attn_reduce.
+ * A row that attends no key produces zeros.
+ */
+ta_status tree_attn_fwd(const ta_tree_params *p, ta_buf q, ta_buf k, ta_buf v, ta_buf mask,
+                        ta_buf tmp, ta_buf out, void *stream);
+
+/*
+ * Main pass with the implicit causal / sliding-window mask of the parent
+ * kernel ([TA-M] header comment): query row i attends positions
+ * [window_start, kv_seq_len - q_l + i].  Same buffers as tree_attn_fwd minus
+ * the mask.  For a mask buffer equal to this causal mask, tree_attn_fwd
+ * produces a bit-identical output ([TA-M] byte-identity contract).
+ */
+ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, ta_buf q,
+                               ta_buf k, ta_buf v, ta_buf tmp, ta_buf out, void *stream);
+
+/*
+ * Second pass ([TA-R] tree_attention, reduce pass): merges the nwg partials
+ * of every (query, head) row with a log-sum-exp rescale:
+ *   M* = max_w M_w,  S* = sum_w S_w e^(M_w - M*),
+ *   out = sum_w O_w e^(M_w - M*) / S*   (0 when S* == 0).
+ * `p` must equal the one given to the main pass; `tmp` is its tmp buffer.
+ */
+ta_status tree_attn_reduce(const ta_tree_params *p, ta_buf tmp, ta_buf out, void *stream);
+
+/* ----------------------------------------------------------------- quant */
+
+/* Splits quant_sdpa_fwd will use (p->nwg when non-zero); 0 on invalid input. */
+uint32_t quant_sdpa_num_splits(const ta_quant_params *p);
+
+/* Bytes of the `tmp` buffer of quant_sdpa_fwd: B*nQ*nwg*(dim+2)*4, or 0 when
+ * one split is used; SIZE_MAX on invalid parameters or overflow. */
+size_t quant_sdpa_tmp_bytes(const ta_quant_params *p);
+
+/*
+ * Attention over an affine-quantized K/V cache ([FQS] all three kernel macros).
+ *   queries   [B*nQ, dim] T (T = f16 or bf16), multiplied by `scale` once
+ *   k_packed  [B*nKV, tokens, dim*bits/32] u32: element d of a token sits at
+ *             bits (d % (32/bits)) * bits of word d / (32/bits)
+ *   k_scales, k_biases  [B*nKV, tokens, dim/group_size] T:
+ *             k[d] = scale[d / group_size] * code + bias[d / group_size]
+ *   v_packed, v_scales, v_biases: same layout for V
+ *   sinks     [nQ] f32, read when has_sinks: a virtual key with logit
+ *             sinks[q % nQ] (not scaled) and value 0, counted once
+ *   mask_bool [B*nQ, tokens] u32 or ptr NULL: 0 drops the token for that query
+ *   mask_float[B*nQ, tokens] T or ptr NULL: added to the logit after the gates
+ *   tmp       f32, >= quant_sdpa_tmp_bytes(p) bytes (may be empty for 1 split)
+ *   out       [B*nQ, dim], dtype T or f32; out = o / l when l > 0, else 0
+ * Query q uses KV row q / (nQ / nKV).  Tokens outside the window are not read.
+ */
+ta_status quant_sdpa_fwd(const ta_quant_params *p, ta_buf queries, ta_buf k_packed,
+                         ta_buf k_scales, ta_buf k_biases, ta_buf v_packed, ta_buf v_scales,
+                         ta_buf v_biases, ta_buf sinks, ta_buf mask_bool, ta_buf mask_float,
+                         ta_buf tmp, ta_buf out, void *stream);
+
+/* ----------------------------------------------------------------- misc */
+
+/* Message for the calling thread's last non-TA_OK status ("" if none). */
+const char *ta_last_error(void);
+
+/* Kernels launched by this library in this process so far (host counter). */
+uint64_t ta_launch_count(void);
+
+/*
+ * Tree kernel family used by later calls: 0 = automatic (tensor cores when the
+ * KV type is f16/bf16 and a KV head serves >= 16 query rows, else CUDA-core
+ * FMA), 1 = always the CUDA-core kernel, 2 = tensor-core kernel where it
+ * applies.  Process-wide; returns the previous value, or -1 for a bad value.
+ * Meant for tests and measurements.
+ */
+int ta_set_tree_path(int path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TREE_ATTN_H_ */

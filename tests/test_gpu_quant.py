@@ -1,0 +1,96 @@
+"""GPU parity of the quantized-KV attention path against the float64 oracle,
+called through the C ABI."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import assert_close, run_quant
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import tree_masked_speculative_gb300 as m
+    return m
+
+
+def qwl(B=2, nQ=8, nKV=2, dim=128, N=300, bits=4, G=64, sinks=1, window=0, dtype="f16",
+        fmask="none", bfrac=0.0, nwg=0, seed=3):
+    return W.QuantWorkload(name="small", batch=B, n_q_heads=nQ, n_kv_heads=nKV, dim=dim, tokens=N,
+                           bits=bits, group_size=G, has_sinks=sinks, window_size=window,
+                           scale=1.0 / math.sqrt(dim), dtype=dtype, float_mask=fmask,
+                           bool_mask_frac=bfrac, nwg=nwg, seed=seed)
+
+
+QCASES = [
+    dict(),
+    dict(bits=8, dtype="bf16", sinks=0),
+    dict(dim=64, G=32, N=77, nwg=1),
+    dict(dim=96, G=32, bits=4, N=130, nwg=3),
+    dict(dim=96, G=32, bits=8, N=130, nwg=2, dtype="bf16"),
+    dict(dim=256, bits=8, window=100, N=500, fmask="alibi", bfrac=0.1, dtype="bf16", sinks=0),
+    dict(dim=512, bits=4, G=128, N=200, nwg=2),
+    dict(dim=512, bits=8, G=64, N=150, bfrac=0.3, dtype="bf16"),
+    dict(nQ=16, nKV=2, N=257, window=33),          # 8 query rows per KV row
+    dict(nQ=6, nKV=2, N=64, nwg=1),                # 3 rows per KV row
+    dict(N=31, window=500),
+]
+
+
+@pytest.mark.parametrize("kw", QCASES, ids=[str(i) for i in range(len(QCASES))])
+def test_quant_matches_oracle(ta, kw):
+    wl = qwl(**kw)
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got32, ref, what="quant f32 out %r" % (kw,))
+    gotT = run_quant(ta, wl, inp).cpu().double().numpy()
+    assert_close(gotT, ref, extra_ulp_dtype=wl.dtype, what="quant T out %r" % (kw,))
+
+
+def test_quant_no_visible_token_gives_zero_and_sink_only(ta):
+    wl = qwl(N=70, sinks=1, bfrac=0.0, nwg=2)
+    inp = W.make_quant_inputs(wl)
+    inp["mask_bool"] = torch.ones((wl.rows, wl.tokens), dtype=torch.int32)
+    inp["mask_bool"][3] = 0
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu()
+    assert torch.all(got[3] == 0.0)
+    wl0 = wl.with_(has_sinks=0)
+    got0 = run_quant(ta, wl0, inp, out_dtype=torch.float32).cpu()
+    assert torch.all(got0[3] == 0.0)
+    assert_close(got.double().numpy(), oracle.quant_oracle_for(wl, inp))
+
+
+def test_quant_split_invariance(ta):
+    wl = qwl(N=2000, bits=8, dtype="bf16")
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    outs = [run_quant(ta, wl, inp, nwg=n, out_dtype=torch.float32).cpu().double().numpy()
+            for n in (1, 3, 15)]
+    for o in outs:
+        assert_close(o, ref)
+
+
+def test_quant_b4_workload_full(ta):
+    wl = W.QUANT_B4
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp).cpu().double().numpy()
+    assert_close(got, ref, extra_ulp_dtype=wl.dtype, what="quant b4 workload")
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got32, ref, what="quant b4 workload f32")
+
+
+def test_quant_b8_masks_workload_full(ta):
+    wl = W.QUANT_B8_MASKS
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp).cpu().double().numpy()
+    assert_close(got, ref, extra_ulp_dtype=wl.dtype, what="quant b8 workload")
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got32, ref, what="quant b8 workload f32")

@@ -1,0 +1,152 @@
+"""GPU parity of the tree-verify attention path against the float64 oracle,
+called through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from helpers import assert_close, run_tree, small_tree, to_dev
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ta():
+    import tree_masked_speculative_gb300 as m
+    return m
+
+
+@pytest.fixture(params=[0, 1], ids=["auto", "fma"])
+def path(request, ta):
+    prev = ta.ta_set_tree_path(request.param)
+    yield request.param
+    ta.ta_set_tree_path(prev)
+
+
+CASES = [
+    # H, Hk, D, N, C, L, kv_dtype, nwg
+    (4, 2, 128, 256, 256, 8, "f32", 32),      # pages' PR1 reference shape
+    (4, 2, 128, 200, 256, 5, "f16", 0),       # ragged last chunk
+    (6, 3, 256, 333, 400, 7, "bf16", 3),
+    (8, 1, 512, 97, 128, 3, "f16", 2),
+    (2, 2, 128, 31, 31, 1, "f32", 1),         # one split, single partial chunk
+    (12, 4, 128, 1000, 1024, 16, "bf16", 0),  # 48 rows per KV head
+    (16, 2, 256, 517, 600, 20, "f16", 5),     # 160 rows per KV head
+    (8, 4, 512, 260, 300, 9, "bf16", 0),
+]
+
+
+@pytest.mark.parametrize("H,Hk,D,N,C,L,kvd,nwg", CASES)
+def test_tree_matches_oracle(ta, path, H, Hk, D, N, C, L, kvd, nwg):
+    wl = small_tree(H=H, Hk=Hk, D=D, N=N, C=C, L=L, kv_dtype=kvd, nwg=nwg, seed=H * 100 + N)
+    inp = W.make_tree_inputs(wl)
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    ref = oracle.tree_oracle_for(wl, inp)
+    assert_close(got, ref, what="tree %s" % (wl,))
+
+
+def test_tree_mask_stride_padding_and_tail_cells_ignored(ta, path):
+    wl = small_tree(H=4, Hk=2, D=256, N=150, C=160, L=6, stride=192, kv_dtype="f16", nwg=2)
+    inp = W.make_tree_inputs(wl)
+    inp["mask"][:, 150:] = 0.0            # cells past kv_seq_len would attend if read
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    ref = oracle.tree_oracle_for(wl, inp)
+    assert_close(got, ref)
+
+
+def test_explicit_causal_mask_bit_identical_to_implicit(ta, path):
+    """The pages' byte-identity contract, on our own two kernels."""
+    for (H, Hk, D, N, L, kvd, nwg, ws) in [(4, 2, 128, 256, 8, "f32", 32, 0),
+                                           (24, 4, 256, 700, 32, "f16", 0, 0),
+                                           (8, 2, 512, 300, 12, "bf16", 3, 0),
+                                           (4, 1, 128, 500, 4, "f16", 4, 130)]:
+        wl = small_tree(H=H, Hk=Hk, D=D, N=N, C=N, L=L, kv_dtype=kvd, nwg=nwg, topology="chain")
+        inp = W.make_tree_inputs(wl)
+        inp["mask"] = W.causal_mask(L, N, N, window_start=ws)
+        explicit = run_tree(ta, wl, inp)
+        implicit = run_tree(ta, wl, inp, causal=True, window_start=ws)
+        assert torch.equal(explicit, implicit), (H, D, kvd)
+        assert_close(explicit.cpu().numpy(),
+                     oracle.tree_oracle_for(wl, inp, mask=None, window_start=ws))
+
+
+def test_single_attended_key_returns_value_row_exactly(ta, path):
+    wl = small_tree(H=4, Hk=2, D=128, N=300, C=300, L=3, kv_dtype="bf16", nwg=4)
+    inp = W.make_tree_inputs(wl)
+    inp["mask"][:] = W.MASKED
+    keys = [5, 177, 299]
+    for i, j in enumerate(keys):
+        inp["mask"][i, j] = 0.0
+    got = run_tree(ta, wl, inp).cpu()
+    for i, j in enumerate(keys):
+        for h in range(4):
+            assert torch.equal(got[i, h], inp["v"][h // 2, j].float()), (i, h)
+
+
+def test_fully_masked_rows_and_dead_chunks(ta, path):
+    wl = small_tree(H=4, Hk=2, D=256, N=640, C=640, L=6, kv_dtype="f16", nwg=3)
+    inp = W.make_tree_inputs(wl)
+    m = inp["mask"]
+    m[2] = W.MASKED                        # row with no attended key -> zeros
+    m[:, 64:320] = W.MASKED                # chunks no row attends: never loaded
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    assert np.all(got[2] == 0.0)
+    assert_close(got, oracle.tree_oracle_for(wl, inp))
+
+
+def test_split_count_invariance(ta, path):
+    wl = small_tree(H=8, Hk=2, D=128, N=1000, C=1000, L=8, kv_dtype="f16")
+    inp = W.make_tree_inputs(wl)
+    ref = oracle.tree_oracle_for(wl, inp)
+    outs = [run_tree(ta, wl, inp, nwg=n).cpu().numpy() for n in (1, 2, 7, 32)]
+    for o in outs:
+        assert_close(o, ref)
+    assert_close(outs[0], outs[-1], atol=1e-4, rtol=1e-4)
+
+
+def test_output_guard_bytes_untouched(ta, path):
+    wl = small_tree(H=4, Hk=2, D=128, N=200, C=256, L=5, kv_dtype="f16", nwg=3)
+    inp = to_dev(W.make_tree_inputs(wl))
+    H, L, D = 4, 5, 128
+    p = ta.tree_params(H, 2, D, 200, 256, wl.scale, L, 200, 3)
+    ws = ta.tree_attn_workspace_bytes(p)
+    tmp_full = torch.full(((ws + 3) // 4 + 1024,), 7.0, device="cuda")
+    out_full = torch.full((L * H * D + 1024,), 7.0, device="cuda")
+    tmp, out = tmp_full[:(ws + 3) // 4], out_full[:L * H * D]
+    ta.tree_attn_fwd(p, inp["q"], inp["k"], inp["v"], inp["mask"], tmp, out)
+    ta.tree_attn_reduce(p, tmp, out)
+    torch.cuda.synchronize()
+    assert torch.all(tmp_full[(ws + 3) // 4:] == 7.0)
+    assert torch.all(out_full[L * H * D:] == 7.0)
+
+
+def test_pr1_reference_workload_full(ta, path):
+    wl = W.PR1_CHAIN
+    inp = W.make_tree_inputs(wl)
+    got = run_tree(ta, wl, inp)
+    assert_close(got.cpu().numpy(), oracle.tree_oracle_for(wl, inp))
+    implicit = run_tree(ta, wl, inp, causal=True)
+    assert torch.equal(got, implicit)
+
+
+def test_fixed_tree_workload_full(ta):
+    wl = W.FIXED_TREE
+    inp = W.make_tree_inputs(wl)
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    assert_close(got, oracle.tree_oracle_for(wl, inp), what="fixed tree")
+
+
+def test_dynamic_tree_workload_sampled_rows(ta):
+    wl = W.DYNAMIC_TREE
+    inp = W.make_tree_inputs(wl)
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    g = torch.Generator().manual_seed(99)
+    rows = [(int(torch.randint(0, wl.n_heads, (1,), generator=g)), int(torch.randint(0, wl.q_l, (1,), generator=g)))
+            for _ in range(48)] + [(0, 0), (wl.n_heads - 1, wl.q_l - 1)]
+    ref = oracle.tree_oracle_for(wl, inp, rows=rows)
+    sel = np.stack([got[i, h] for (h, i) in rows])
+    assert_close(sel, ref, what="dynamic tree sampled rows")
+    # properties that hold for every row: finite, bounded by the attended V range
+    v = inp["v"][:, :wl.kv_seq_len].float()
+    assert np.all(np.abs(got) <= float(v.abs().max()) + 1e-3)

@@ -1,0 +1,511 @@
+// C ABI of the tree-verify attention library: argument checks, workspace
+// layout, split-count choice and kernel dispatch.
+//
+// The checks restate mlx-native tree_attention.rs (validate_params,
+// validate_buffers with overflow-checked byte counts, tmp_buffer_bytes with
+// saturating arithmetic) for the tree path, and the shape rules of
+// metaltile-std flash_quantized_sdpa.rs (module doc "Layout", dispatch
+// invariants) for the quantized path.  Every check runs before any launch.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "ta_internal.cuh"
+#include "tree_attn.h"
+
+#define TA_EXPORT extern "C" __attribute__((visibility("default")))
+
+static_assert(sizeof(ta_tree_params) == 36, "ta_tree_params must be 9 x 4 bytes");
+
+namespace ta {
+namespace {
+
+thread_local std::string g_err;
+std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_tree_path{0};
+
+ta_status fail(ta_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return st;
+}
+
+ta_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(TA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool mul3(uint64_t a, uint64_t b, uint64_t c, uint64_t *out) {
+    uint64_t t;
+    if (__builtin_mul_overflow(a, b, &t)) return false;
+    return !__builtin_mul_overflow(t, c, out);
+}
+bool mul4(uint64_t a, uint64_t b, uint64_t c, uint64_t d, uint64_t *out) {
+    uint64_t t;
+    return mul3(a, b, c, &t) && !__builtin_mul_overflow(t, d, out);
+}
+uint64_t sat_mul(uint64_t a, uint64_t b) {
+    uint64_t r;
+    return __builtin_mul_overflow(a, b, &r) ? UINT64_MAX : r;
+}
+uint64_t align256(uint64_t x) { return (x + 255u) & ~uint64_t(255); }
+
+size_t elt_bytes(int dtype) {
+    switch (dtype) {
+        case TA_F32: return 4;
+        case TA_F16: return 2;
+        case TA_BF16: return 2;
+        case TA_U32: return 4;
+        default: return 0;
+    }
+}
+const char *dtype_name(int dtype) {
+    switch (dtype) {
+        case TA_F32: return "F32";
+        case TA_F16: return "F16";
+        case TA_BF16: return "BF16";
+        case TA_U32: return "U32";
+        default: return "unknown";
+    }
+}
+
+std::atomic<int> g_sm_count[64];   // per device, 0 = not queried yet
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return 0; }
+    if (dev >= 0 && dev < 64 && (n = g_sm_count[dev].load(std::memory_order_relaxed)) > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (dev >= 0 && dev < 64) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+// ---------------------------------------------------------------- tree params
+ta_status check_tree_params(const ta_tree_params *p, bool need_mask_stride) {
+    if (p == nullptr) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: params is NULL");
+    if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: head_dim must be 128, 256, or 512, got %u",
+                    p->head_dim);
+    if (p->n_heads == 0 || p->n_kv_heads == 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: num_heads and num_kv_heads must be > 0");
+    if (p->n_heads % p->n_kv_heads != 0)
+        return fail(TA_ERR_INVALID_ARGUMENT,
+                    "tree_attention: num_heads (%u) must be divisible by num_kv_heads (%u)", p->n_heads,
+                    p->n_kv_heads);
+    if (p->kv_seq_len == 0) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: kv_seq_len must be > 0");
+    if (p->kv_capacity < p->kv_seq_len)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: kv_capacity (%u) must be >= kv_seq_len (%u)",
+                    p->kv_capacity, p->kv_seq_len);
+    if (p->q_l == 0) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: q_l (q_seq_len) must be > 0");
+    if (need_mask_stride && p->mask_stride < p->kv_seq_len)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: mask_stride (%u) must be >= kv_seq_len (%u)",
+                    p->mask_stride, p->kv_seq_len);
+    // The kernels index with 32-bit ints and launch H * q_l reduce blocks.
+    const uint64_t nrows = (uint64_t)p->n_heads * p->q_l;
+    if (p->kv_capacity > (uint32_t)INT_MAX || p->mask_stride > (uint32_t)INT_MAX || nrows > (uint64_t)INT_MAX ||
+        p->n_kv_heads > 65535u)
+        return fail(TA_ERR_UNSUPPORTED, "tree_attention: sizes exceed the kernels' 32-bit index range");
+    if (!std::isfinite(p->scale)) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: scale is not finite");
+    return TA_OK;
+}
+
+int rows_per_kv(const ta_tree_params *p) { return (int)(p->n_heads / p->n_kv_heads * p->q_l); }
+
+uint32_t resolve_tree_nwg(const ta_tree_params *p) {
+    if (p->nwg != 0) return p->nwg;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
+    const uint64_t R = (uint64_t)rows_per_kv(p);
+    uint64_t units;
+    if (R >= 16) units = (uint64_t)p->n_kv_heads * ((R + 127) / 128) * (p->head_dim == 512 ? 2 : 1);
+    else units = (uint64_t)p->n_kv_heads * ((R + kFmaRowsPerCta - 1) / kFmaRowsPerCta);
+    uint64_t nwg = (2ull * sms + units - 1) / units;
+    if (nwg < 1) nwg = 1;
+    if (nwg > n_chunks) nwg = n_chunks;
+    if (nwg > 65535) nwg = 65535;
+    return (uint32_t)nwg;
+}
+
+bool tree_workspace(const ta_tree_params *p, uint32_t nwg, TreeWorkspace *ws) {
+    const uint64_t nrows = (uint64_t)p->n_heads * p->q_l;
+    uint64_t po, pml, q16;
+    if (!mul4(nwg, nrows, p->head_dim, 4, &po) || !mul4(nwg, nrows, 2, 4, &pml) ||
+        !mul3(nrows, p->head_dim, 2, &q16))
+        return false;
+    ws->off_part_o = 0;
+    ws->off_part_ml = po;
+    const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
+    ws->off_cls = align256(po + pml);
+    ws->off_q16 = align256(ws->off_cls + n_chunks);
+    ws->total = align256(ws->off_q16 + q16);
+    return ws->total >= ws->off_q16;
+}
+
+ta_status check_buf(const ta_buf &b, const char *name, uint64_t need_bytes, size_t align) {
+    if (b.reserved != 0) return fail(TA_ERR_INVALID_ARGUMENT, "%s: reserved field must be 0", name);
+    if (b.ptr == nullptr) return fail(TA_ERR_INVALID_ARGUMENT, "%s: NULL pointer", name);
+    if (((uintptr_t)b.ptr) % align != 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "%s: pointer must be %zu-byte aligned", name, align);
+    if (b.bytes < need_bytes)
+        return fail(TA_ERR_BUFFER_TOO_SMALL, "%s buffer too small: have %llu bytes, need >= %llu", name,
+                    (unsigned long long)b.bytes, (unsigned long long)need_bytes);
+    return TA_OK;
+}
+
+ta_status check_dtype(const ta_buf &b, const char *name, int want) {
+    if (b.dtype != want)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: %s dtype must be %s, got %s", name,
+                    dtype_name(want), dtype_name(b.dtype));
+    return TA_OK;
+}
+
+#define TA_TRY(x)                      \
+    do {                               \
+        ta_status _s = (x);            \
+        if (_s != TA_OK) return _s;    \
+    } while (0)
+
+struct TreePlan {
+    TreeArgs a;
+    int kv_type;
+    bool use_tc;
+};
+
+ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, const ta_buf *v,
+                    const ta_buf *mask, const ta_buf *tmp, const ta_buf *out, int window_start,
+                    TreePlan *plan) {
+    TA_TRY(check_tree_params(p, mask != nullptr));
+    // dtype contract (tree_attention.rs validate_buffers; bf16 K/V added)
+    TA_TRY(check_dtype(*q, "q", TA_F32));
+    if (k->dtype != v->dtype)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: k.dtype (%s) must match v.dtype (%s)",
+                    dtype_name(k->dtype), dtype_name(v->dtype));
+    if (k->dtype != TA_F32 && k->dtype != TA_F16 && k->dtype != TA_BF16)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: k/v dtype must be F32, F16 or BF16, got %s",
+                    dtype_name(k->dtype));
+    if (mask) TA_TRY(check_dtype(*mask, "tree_mask", TA_F32));
+    TA_TRY(check_dtype(*out, "output", TA_F32));
+    TA_TRY(check_dtype(*tmp, "tmp", TA_F32));
+
+    // byte-length contract, overflow-checked
+    uint64_t req_q, req_kv, req_mask = 0;
+    if (!mul4(p->n_heads, p->q_l, p->head_dim, 4, &req_q))
+        return fail(TA_ERR_OVERFLOW, "tree_attention: num_heads*q_seq_len*head_dim*4 overflows");
+    if (!mul4(p->n_kv_heads, p->kv_capacity, p->head_dim, elt_bytes(k->dtype), &req_kv))
+        return fail(TA_ERR_OVERFLOW, "tree_attention: num_kv_heads*kv_capacity*head_dim overflows");
+    if (mask && !mul3(p->q_l, p->mask_stride, 4, &req_mask))
+        return fail(TA_ERR_OVERFLOW, "tree_attention: q_seq_len*mask_stride*4 overflows");
+    const uint32_t nwg = resolve_tree_nwg(p);
+    if (nwg == 0) return fail(TA_ERR_CUDA, "tree_attention: no CUDA device to size the split count for");
+    TreeWorkspace ws;
+    if (!tree_workspace(p, nwg, &ws)) return fail(TA_ERR_OVERFLOW, "tree_attention: workspace size overflows");
+
+    TA_TRY(check_buf(*q, "tree_attention: q", req_q, 16));
+    TA_TRY(check_buf(*k, "tree_attention: k", req_kv, 16));
+    TA_TRY(check_buf(*v, "tree_attention: v", req_kv, 16));
+    if (mask) TA_TRY(check_buf(*mask, "tree_attention: tree_mask", req_mask, 4));
+    TA_TRY(check_buf(*out, "tree_attention: output", req_q, 16));
+    TA_TRY(check_buf(*tmp, "tree_attention: tmp", ws.total, 16));
+
+    TreeArgs &a = plan->a;
+    a = TreeArgs{};
+    a.q = static_cast<const float *>(q->ptr);
+    a.k = k->ptr;
+    a.v = v->ptr;
+    a.mask = mask ? static_cast<const float *>(mask->ptr) : nullptr;
+    char *t = static_cast<char *>(tmp->ptr);
+    a.part_o = reinterpret_cast<float *>(t + ws.off_part_o);
+    a.part_ml = reinterpret_cast<float *>(t + ws.off_part_ml);
+    a.cls = reinterpret_cast<uint8_t *>(t + ws.off_cls);
+    a.q16 = t + ws.off_q16;
+    a.out = static_cast<float *>(out->ptr);
+    a.H = (int)p->n_heads;
+    a.Hk = (int)p->n_kv_heads;
+    a.D = (int)p->head_dim;
+    a.N = (int)p->kv_seq_len;
+    a.C = (int)p->kv_capacity;
+    a.L = (int)p->q_l;
+    a.stride = (int)p->mask_stride;
+    a.nwg = (int)nwg;
+    a.g = a.H / a.Hk;
+    a.R = a.g * a.L;
+    a.n_chunks = (a.N + 31) / 32;
+    a.window_start = window_start;
+    a.scale = p->scale;
+    plan->kv_type = k->dtype == TA_F32 ? kKvF32 : (k->dtype == TA_F16 ? kKvF16 : kKvBF16);
+    plan->use_tc = false;
+    return TA_OK;
+}
+
+ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
+    cudaError_t e = launch_tree_classify(plan.a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attention: chunk classification launch");
+    e = launch_tree_fma(plan.a, plan.kv_type, s);
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attention: main pass launch");
+    return TA_OK;
+}
+
+// --------------------------------------------------------------- quant params
+ta_status check_quant_params(const ta_quant_params *p) {
+    if (p == nullptr) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: params is NULL");
+    if (p->batch == 0 || p->n_q_heads == 0 || p->n_kv_heads == 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: batch, n_q_heads and n_kv_heads must be > 0");
+    if (p->n_q_heads % p->n_kv_heads != 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: n_q_heads (%u) must be divisible by n_kv_heads (%u)",
+                    p->n_q_heads, p->n_kv_heads);
+    if (p->bits != 4 && p->bits != 8)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: bits must be 4 or 8, got %u", p->bits);
+    const uint32_t pf = 32 / p->bits;
+    if (p->dim == 0 || p->dim % pf != 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: dim (%u) must be a positive multiple of 32/bits (%u)",
+                    p->dim, pf);
+    if (p->group_size == 0 || p->dim % p->group_size != 0)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: dim (%u) must be a multiple of group_size (%u)", p->dim,
+                    p->group_size);
+    if (p->tokens == 0) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: tokens must be > 0");
+    if (p->has_sinks > 1) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: has_sinks must be 0 or 1");
+    if (!std::isfinite(p->scale)) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: scale is not finite");
+    if (p->group_size % pf != 0)
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: group_size must be a multiple of 32/bits");
+    if (p->dim > 512) return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: dim > 512 is not implemented");
+    if (p->n_q_heads / p->n_kv_heads > 8)
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: more than 8 query heads per KV head is not implemented");
+    const uint64_t rows = (uint64_t)p->batch * p->n_q_heads;
+    const uint64_t kvr = (uint64_t)p->batch * p->n_kv_heads;
+    uint64_t cells;
+    if (!mul3(kvr, p->tokens, p->dim, &cells) || rows > (uint64_t)INT_MAX || kvr > 65535u ||
+        p->tokens > (uint32_t)INT_MAX)
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: sizes exceed the kernels' index range");
+    return TA_OK;
+}
+
+uint32_t window_tokens(const ta_quant_params *p) {
+    return p->window_size == 0 ? p->tokens : (p->window_size < p->tokens ? p->window_size : p->tokens);
+}
+
+uint32_t resolve_quant_nwg(const ta_quant_params *p) {
+    if (p->nwg != 0) return p->nwg;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    const uint64_t kvr = (uint64_t)p->batch * p->n_kv_heads;
+    const uint64_t max_splits = (window_tokens(p) + 127u) / 128u;
+    uint64_t nwg = (4ull * sms + kvr - 1) / kvr;
+    if (nwg > max_splits) nwg = max_splits;
+    if (nwg < 1) nwg = 1;
+    if (nwg > 65535) nwg = 65535;
+    return (uint32_t)nwg;
+}
+
+bool quant_tmp(const ta_quant_params *p, uint32_t nwg, uint64_t *bytes) {
+    if (nwg <= 1) { *bytes = 0; return true; }
+    const uint64_t rows = (uint64_t)p->batch * p->n_q_heads;
+    return mul4(rows, nwg, (uint64_t)p->dim + 2, 4, bytes);
+}
+
+}  // namespace
+
+void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
+
+}  // namespace ta
+
+using namespace ta;
+
+// ============================================================== exported ABI
+TA_EXPORT size_t tree_attn_tmp_bytes(uint32_t n_heads, uint32_t head_dim, uint32_t q_l, uint32_t nwg) {
+    const uint64_t nrows = sat_mul(n_heads, q_l);
+    const uint64_t dv2 = (uint64_t)head_dim + 2;
+    const uint64_t r = sat_mul(sat_mul(sat_mul(nrows, nwg), dv2), sizeof(float));
+    return r > SIZE_MAX ? SIZE_MAX : (size_t)r;
+}
+
+TA_EXPORT uint32_t tree_attn_num_splits(const ta_tree_params *p) {
+    if (check_tree_params(p, false) != TA_OK) return 0;
+    return resolve_tree_nwg(p);
+}
+
+TA_EXPORT size_t tree_attn_workspace_bytes(const ta_tree_params *p) {
+    if (check_tree_params(p, false) != TA_OK) return SIZE_MAX;
+    const uint32_t nwg = resolve_tree_nwg(p);
+    if (nwg == 0) return SIZE_MAX;
+    TreeWorkspace ws;
+    if (!tree_workspace(p, nwg, &ws)) return SIZE_MAX;
+    return ws.total;
+}
+
+TA_EXPORT ta_status tree_attn_fwd(const ta_tree_params *p, ta_buf q, ta_buf k, ta_buf v, ta_buf mask,
+                                  ta_buf tmp, ta_buf out, void *stream) {
+    TreePlan plan;
+    const bool implicit = mask.ptr == nullptr && mask.bytes == 0;
+    TA_TRY(plan_tree(p, &q, &k, &v, implicit ? nullptr : &mask, &tmp, &out, 0, &plan));
+    return run_tree(plan, static_cast<cudaStream_t>(stream));
+}
+
+TA_EXPORT ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, ta_buf q, ta_buf k,
+                                         ta_buf v, ta_buf tmp, ta_buf out, void *stream) {
+    if (window_start > (uint32_t)INT_MAX)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: window_start out of range");
+    TreePlan plan;
+    TA_TRY(plan_tree(p, &q, &k, &v, nullptr, &tmp, &out, (int)window_start, &plan));
+    return run_tree(plan, static_cast<cudaStream_t>(stream));
+}
+
+TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, ta_buf tmp, ta_buf out, void *stream) {
+    TA_TRY(check_tree_params(p, false));
+    TA_TRY(check_dtype(tmp, "tmp", TA_F32));
+    TA_TRY(check_dtype(out, "output", TA_F32));
+    const uint32_t nwg = resolve_tree_nwg(p);
+    if (nwg == 0) return fail(TA_ERR_CUDA, "tree_attention: no CUDA device to size the split count for");
+    TreeWorkspace ws;
+    uint64_t req_out;
+    if (!tree_workspace(p, nwg, &ws) || !mul4(p->n_heads, p->q_l, p->head_dim, 4, &req_out))
+        return fail(TA_ERR_OVERFLOW, "tree_attention: size overflows");
+    TA_TRY(check_buf(tmp, "tree_attention: tmp", ws.total, 16));
+    TA_TRY(check_buf(out, "tree_attention: output", req_out, 16));
+    if (nwg == 1) return TA_OK;   // the main pass already wrote the output
+    TreeArgs a{};
+    char *t = static_cast<char *>(tmp.ptr);
+    a.part_o = reinterpret_cast<float *>(t + ws.off_part_o);
+    a.part_ml = reinterpret_cast<float *>(t + ws.off_part_ml);
+    a.out = static_cast<float *>(out.ptr);
+    a.H = (int)p->n_heads;
+    a.L = (int)p->q_l;
+    a.D = (int)p->head_dim;
+    a.nwg = (int)nwg;
+    cudaError_t e = launch_tree_reduce(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_attention: reduce launch");
+    return TA_OK;
+}
+
+TA_EXPORT uint32_t quant_sdpa_num_splits(const ta_quant_params *p) {
+    if (check_quant_params(p) != TA_OK) return 0;
+    return resolve_quant_nwg(p);
+}
+
+TA_EXPORT size_t quant_sdpa_tmp_bytes(const ta_quant_params *p) {
+    if (check_quant_params(p) != TA_OK) return SIZE_MAX;
+    const uint32_t nwg = resolve_quant_nwg(p);
+    if (nwg == 0) return SIZE_MAX;
+    uint64_t b;
+    if (!quant_tmp(p, nwg, &b)) return SIZE_MAX;
+    return (size_t)b;
+}
+
+TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, ta_buf queries, ta_buf k_packed, ta_buf k_scales,
+                                   ta_buf k_biases, ta_buf v_packed, ta_buf v_scales, ta_buf v_biases,
+                                   ta_buf sinks, ta_buf mask_bool, ta_buf mask_float, ta_buf tmp, ta_buf out,
+                                   void *stream) {
+    TA_TRY(check_quant_params(p));
+    const int T = queries.dtype;
+    if (T != TA_F16 && T != TA_BF16)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: queries dtype must be F16 or BF16, got %s",
+                    dtype_name(T));
+    const ta_buf *same_t[] = {&k_scales, &k_biases, &v_scales, &v_biases};
+    const char *same_t_names[] = {"k_scales", "k_biases", "v_scales", "v_biases"};
+    for (int i = 0; i < 4; ++i)
+        if (same_t[i]->dtype != T)
+            return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: %s dtype must equal the queries dtype (%s), got %s",
+                        same_t_names[i], dtype_name(T), dtype_name(same_t[i]->dtype));
+    if (k_packed.dtype != TA_U32 || v_packed.dtype != TA_U32)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: k_packed and v_packed dtype must be U32");
+    const bool has_bool = !(mask_bool.ptr == nullptr && mask_bool.bytes == 0);
+    const bool has_float = !(mask_float.ptr == nullptr && mask_float.bytes == 0);
+    if (has_bool && mask_bool.dtype != TA_U32)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: mask_bool dtype must be U32");
+    if (has_float && mask_float.dtype != T)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: mask_float dtype must equal the queries dtype");
+    if (out.dtype != T && out.dtype != TA_F32)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: out dtype must be the queries dtype or F32");
+    if (p->has_sinks && sinks.dtype != TA_F32)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: sinks dtype must be F32");
+
+    const uint64_t rows = (uint64_t)p->batch * p->n_q_heads;
+    const uint64_t kvr = (uint64_t)p->batch * p->n_kv_heads;
+    const uint64_t words = p->dim / (32 / p->bits);
+    const uint64_t groups = p->dim / p->group_size;
+    uint64_t req_q, req_packed, req_sb, req_mb = 0, req_mf = 0, req_out, req_tmp;
+    if (!mul3(rows, p->dim, 2, &req_q) || !mul4(kvr, p->tokens, words, 4, &req_packed) ||
+        !mul4(kvr, p->tokens, groups, 2, &req_sb) || !mul3(rows, p->tokens, 4, &req_mb) ||
+        !mul3(rows, p->tokens, 2, &req_mf) || !mul3(rows, p->dim, elt_bytes(out.dtype), &req_out))
+        return fail(TA_ERR_OVERFLOW, "quant_sdpa: buffer size overflows");
+    const uint32_t nwg = resolve_quant_nwg(p);
+    if (nwg == 0) return fail(TA_ERR_CUDA, "quant_sdpa: no CUDA device to size the split count for");
+    if (!quant_tmp(p, nwg, &req_tmp)) return fail(TA_ERR_OVERFLOW, "quant_sdpa: tmp size overflows");
+
+    TA_TRY(check_buf(queries, "quant_sdpa: queries", req_q, 2));
+    TA_TRY(check_buf(k_packed, "quant_sdpa: k_packed", req_packed, 4));
+    TA_TRY(check_buf(v_packed, "quant_sdpa: v_packed", req_packed, 4));
+    TA_TRY(check_buf(k_scales, "quant_sdpa: k_scales", req_sb, 2));
+    TA_TRY(check_buf(k_biases, "quant_sdpa: k_biases", req_sb, 2));
+    TA_TRY(check_buf(v_scales, "quant_sdpa: v_scales", req_sb, 2));
+    TA_TRY(check_buf(v_biases, "quant_sdpa: v_biases", req_sb, 2));
+    if (p->has_sinks) TA_TRY(check_buf(sinks, "quant_sdpa: sinks", (uint64_t)p->n_q_heads * 4, 4));
+    if (has_bool) TA_TRY(check_buf(mask_bool, "quant_sdpa: mask_bool", req_mb, 4));
+    if (has_float) TA_TRY(check_buf(mask_float, "quant_sdpa: mask_float", req_mf, 2));
+    TA_TRY(check_buf(out, "quant_sdpa: out", req_out, out.dtype == TA_F32 ? 4 : 2));
+    if (nwg > 1) {
+        TA_TRY(check_dtype(tmp, "tmp", TA_F32));
+        TA_TRY(check_buf(tmp, "quant_sdpa: tmp", req_tmp, 16));
+    }
+
+    QuantArgs a{};
+    a.queries = queries.ptr;
+    a.kp = static_cast<const uint32_t *>(k_packed.ptr);
+    a.vp = static_cast<const uint32_t *>(v_packed.ptr);
+    a.ks = k_scales.ptr;
+    a.kb = k_biases.ptr;
+    a.vs = v_scales.ptr;
+    a.vb = v_biases.ptr;
+    a.sinks = p->has_sinks ? static_cast<const float *>(sinks.ptr) : nullptr;
+    a.mbool = has_bool ? static_cast<const uint32_t *>(mask_bool.ptr) : nullptr;
+    a.mfloat = has_float ? mask_float.ptr : nullptr;
+    if (nwg > 1) {
+        a.part_o = static_cast<float *>(tmp.ptr);
+        a.part_ml = a.part_o + rows * nwg * p->dim;
+    }
+    a.out = out.ptr;
+    a.rows = (int)rows;
+    a.nQ = (int)p->n_q_heads;
+    a.rep = (int)(p->n_q_heads / p->n_kv_heads);
+    a.kv_rows = (int)kvr;
+    a.dim = (int)p->dim;
+    a.N = (int)p->tokens;
+    a.bits = (int)p->bits;
+    a.G = (int)p->group_size;
+    a.has_sinks = (int)p->has_sinks;
+    a.window = (int)p->window_size;
+    a.nwg = (int)nwg;
+    const uint32_t wt = window_tokens(p);
+    a.t_lo = (int)(p->tokens - wt);
+    const uint64_t per = (wt + nwg - 1) / nwg;
+    a.tps = (int)(((per + 31) / 32) * 32);
+    a.t_is_bf16 = T == TA_BF16;
+    a.out_f32 = out.dtype == TA_F32;
+    a.scale = p->scale;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_quant_fma(a, s);
+    if (e != cudaSuccess) return cuda_fail(e, "quant_sdpa: main pass launch");
+    if (nwg > 1) {
+        e = launch_quant_merge(a, s);
+        if (e != cudaSuccess) return cuda_fail(e, "quant_sdpa: merge launch");
+    }
+    return TA_OK;
+}
+
+TA_EXPORT const char *ta_last_error(void) { return g_err.c_str(); }
+
+TA_EXPORT uint64_t ta_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+TA_EXPORT int ta_set_tree_path(int path) {
+    if (path < 0 || path > 2) return -1;
+    return g_tree_path.exchange(path);
+}

@@ -1,0 +1,134 @@
+// Internal declarations of the tree-verify attention library (not installed).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <cfloat>
+
+namespace ta {
+
+// Sentinel of a masked tree-mask cell (-MAXHALF), and the running-max start
+// value of the online softmax (mlx-native tree_attention.metal, main kernel).
+constexpr float kMasked = -65504.0f;
+constexpr float kMInit = -FLT_MAX / 2;
+
+// Chunk classes written by the mask-compaction pass, one byte per 32 keys.
+enum ChunkClass : uint8_t { kChunkDead = 0, kChunkAllAttended = 1, kChunkMixed = 2 };
+
+enum KvType : int { kKvF32 = 0, kKvF16 = 1, kKvBF16 = 2 };
+
+// ------------------------------------------------------------ device helpers
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__half x) { return __half2float(x); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ float warp_max(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+
+// Expand one 16-byte vector of KV_T into floats.
+template <typename KV_T>
+struct Vec16;
+template <>
+struct Vec16<float> {
+    static constexpr int N = 4;
+    __device__ __forceinline__ static void expand(const uint4 &u, float *f) {
+        f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+        f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+    }
+};
+template <>
+struct Vec16<__half> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void expand(const uint4 &u, float *f) {
+        const __half2 *h = reinterpret_cast<const __half2 *>(&u);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) { float2 t = __half22float2(h[i]); f[2 * i] = t.x; f[2 * i + 1] = t.y; }
+    }
+};
+template <>
+struct Vec16<__nv_bfloat16> {
+    static constexpr int N = 8;
+    __device__ __forceinline__ static void expand(const uint4 &u, float *f) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            f[2 * i] = __uint_as_float(w[i] << 16);
+            f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+
+// ------------------------------------------------------------------- args
+struct TreeArgs {
+    const float *q;        // [H, L, D] f32
+    const void *k;         // [Hk, C, D] KV_T
+    const void *v;
+    const float *mask;     // [L, stride] f32; nullptr -> implicit causal
+    uint8_t *cls;          // [n_chunks] chunk classes
+    float *part_o;         // [nwg][nrows][D]
+    float *part_ml;        // [nwg][nrows][2] = (S, M)
+    float *out;            // [L, H, D]
+    void *q16;             // [H*L, D] 16-bit copy of Q (tensor-core path)
+    int H, Hk, D, N, C, L, stride, nwg, g, R, n_chunks, window_start;
+    float scale;
+};
+
+struct QuantArgs {
+    const void *queries;     // [B*nQ, dim] T
+    const uint32_t *kp, *vp; // [B*nKV, N, wpt]
+    const void *ks, *kb, *vs, *vb;  // [B*nKV, N, ng] T
+    const float *sinks;      // [nQ]
+    const uint32_t *mbool;   // [B*nQ, N] or nullptr
+    const void *mfloat;      // [B*nQ, N] T or nullptr
+    float *part_o;           // [nwg][rows][dim]
+    float *part_ml;          // [nwg][rows][2] = (S, M)
+    void *out;               // [rows, dim] T or f32
+    int rows, nQ, rep, kv_rows, dim, N, bits, G, has_sinks, window, nwg, t_lo, tps;
+    int t_is_bf16, out_f32;
+    float scale;
+};
+
+// Workspace layout inside the caller's tmp buffer (all offsets 256-aligned).
+struct TreeWorkspace {
+    size_t off_part_o, off_part_ml, off_cls, off_q16, total;
+};
+
+// ------------------------------------------------------------ host launches
+// Each returns cudaGetLastError() after enqueueing on `s`.
+cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
+cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
+cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
+cudaError_t launch_quant_fma(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s);
+
+// Rows of one CTA in the CUDA-core tree kernel.
+constexpr int kFmaRowsPerCta = 16;
+
+void count_launch(int n = 1);
+
+// Raise a kernel's dynamic shared-memory limit once per device; later calls
+// (for example while a CUDA graph is being captured) only read a flag.
+template <typename Kern>
+cudaError_t set_smem_limit_once(Kern kern, size_t bytes, unsigned long long *done_mask) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+    return e;
+}
+
+}  // namespace ta
