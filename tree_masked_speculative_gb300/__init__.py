@@ -3,7 +3,8 @@
 Every function here only marshals arguments (torch tensors -> pointer, byte
 count, dtype code; the current CUDA stream) into the C library; all work runs
 in the library's CUDA kernels.  Importing this module loads the in-tree
-``_build/libtree_attn.so`` and raises if it is missing: there is no fallback.
+``_build/libtree_attn.so`` (compiling it first when it is missing or older than
+its sources) and raises if that fails: there is no fallback.
 """
 from __future__ import annotations
 
@@ -60,10 +61,11 @@ def library_path() -> str:
 
 
 def _load() -> ctypes.CDLL:
-    path = library_path()
+    # (Re)build the in-tree library when it is missing or older than its
+    # sources; a failed build raises, so the package never imports without it.
+    path = _build_mod.build()
     if not os.path.exists(path):
-        raise ImportError("tree_masked_speculative_gb300: %s is missing; run "
-                          "tree_masked_speculative_gb300.build.build() first" % path)
+        raise ImportError("tree_masked_speculative_gb300: %s is missing" % path)
     L = ctypes.CDLL(path)
     P, B = ctypes.c_void_p, Buf
     PT, PQ = ctypes.POINTER(TreeParams), ctypes.POINTER(QuantParams)

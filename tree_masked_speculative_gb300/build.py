@@ -47,11 +47,12 @@ def _compile(src: str, extra) -> str:
     obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
     headers = sorted(glob.glob(os.path.join(CSRC, "*.cuh"))) + [os.path.join(INCLUDE, "tree_attn.h")]
     if _stale(obj, [src] + headers + [os.path.abspath(__file__)]):
-        cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-c", src, "-o", obj + ".tmp"]
+        tmp = "%s.%d.tmp" % (obj, os.getpid())
+        cmd = [nvcc()] + ARCH + NVCC_FLAGS + list(extra) + ["-c", src, "-o", tmp]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError("nvcc failed for %s:\n%s\n%s" % (src, " ".join(cmd), r.stderr[-8000:]))
-        os.replace(obj + ".tmp", obj)
+        os.replace(tmp, obj)
     return obj
 
 
