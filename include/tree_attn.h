@@ -22,9 +22,12 @@
  *
  * Conventions shared by every entry point:
  *   - Every buffer is borrowed device memory described by a ta_buf (pointer,
- *     usable byte count, element type).  The library never allocates, frees,
- *     copies to the host or synchronizes; all work is enqueued on `stream`
- *     (a cudaStream_t passed as void*, NULL = legacy default stream).
+ *     usable byte count, element type) passed by address; the ta_buf itself
+ *     is only read during the call.  An optional buffer is absent when its
+ *     ta_buf pointer is NULL (or its `ptr` is NULL with `bytes` 0).
+ *   - The library never allocates, frees, copies to the host or
+ *     synchronizes; all work is enqueued on `stream` (a cudaStream_t passed
+ *     as void*, NULL = legacy default stream).
  *   - All argument checks run before any launch, with overflow-checked size
  *     arithmetic.  On any non-TA_OK status nothing has been launched and no
  *     output was touched; ta_last_error() then returns a message for the
@@ -138,7 +141,7 @@ size_t tree_attn_workspace_bytes(const ta_tree_params *p);
  *         positions >= kv_seq_len are ignored.  The mask is added to the
  *         scaled logit.  A 32-key chunk whose cells are all <= -65504 for a
  *         row is skipped for that row; a chunk masked for every row is not
- *         loaded at all.  mask.ptr == NULL selects the implicit causal mask
+ *         loaded at all.  An absent mask selects the implicit causal mask
  *         (tree_attn_fwd_causal with window_start 0).
  *   tmp   f32, >= tree_attn_workspace_bytes(p) bytes, 16-byte aligned.
  *   out   [q_l, n_heads, head_dim] f32 (query-outer, head-inner: NOT Q's layout).
@@ -146,8 +149,8 @@ size_t tree_attn_workspace_bytes(const ta_tree_params *p);
  * tree_attn_reduce is a no-op; otherwise `out` is written by tree_attn_reduce.
  * A row that attends no key produces zeros.
  */
-ta_status tree_attn_fwd(const ta_tree_params *p, ta_buf q, ta_buf k, ta_buf v, ta_buf mask,
-                        ta_buf tmp, ta_buf out, void *stream);
+ta_status tree_attn_fwd(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, const ta_buf *v,
+                        const ta_buf *mask, const ta_buf *tmp, const ta_buf *out, void *stream);
 
 /*
  * Main pass with the implicit causal / sliding-window mask of the parent
@@ -156,8 +159,9 @@ ta_status tree_attn_fwd(const ta_tree_params *p, ta_buf q, ta_buf k, ta_buf v, t
  * the mask.  For a mask buffer equal to this causal mask, tree_attn_fwd
  * produces a bit-identical output ([TA-M] byte-identity contract).
  */
-ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, ta_buf q,
-                               ta_buf k, ta_buf v, ta_buf tmp, ta_buf out, void *stream);
+ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, const ta_buf *q,
+                               const ta_buf *k, const ta_buf *v, const ta_buf *tmp,
+                               const ta_buf *out, void *stream);
 
 /*
  * Second pass ([TA-R] tree_attention, reduce pass): merges the nwg partials
@@ -166,7 +170,8 @@ ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, t
  *   out = sum_w O_w e^(M_w - M*) / S*   (0 when S* == 0).
  * `p` must equal the one given to the main pass; `tmp` is its tmp buffer.
  */
-ta_status tree_attn_reduce(const ta_tree_params *p, ta_buf tmp, ta_buf out, void *stream);
+ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp, const ta_buf *out,
+                           void *stream);
 
 /* ----------------------------------------------------------------- quant */
 
@@ -187,16 +192,17 @@ size_t quant_sdpa_tmp_bytes(const ta_quant_params *p);
  *   v_packed, v_scales, v_biases: same layout for V
  *   sinks     [nQ] f32, read when has_sinks: a virtual key with logit
  *             sinks[q % nQ] (not scaled) and value 0, counted once
- *   mask_bool [B*nQ, tokens] u32 or ptr NULL: 0 drops the token for that query
- *   mask_float[B*nQ, tokens] T or ptr NULL: added to the logit after the gates
- *   tmp       f32, >= quant_sdpa_tmp_bytes(p) bytes (may be empty for 1 split)
+ *   mask_bool [B*nQ, tokens] u32 or absent: 0 drops the token for that query
+ *   mask_float[B*nQ, tokens] T or absent: added to the logit after the gates
+ *   tmp       f32, >= quant_sdpa_tmp_bytes(p) bytes (may be absent for 1 split)
  *   out       [B*nQ, dim], dtype T or f32; out = o / l when l > 0, else 0
  * Query q uses KV row q / (nQ / nKV).  Tokens outside the window are not read.
  */
-ta_status quant_sdpa_fwd(const ta_quant_params *p, ta_buf queries, ta_buf k_packed,
-                         ta_buf k_scales, ta_buf k_biases, ta_buf v_packed, ta_buf v_scales,
-                         ta_buf v_biases, ta_buf sinks, ta_buf mask_bool, ta_buf mask_float,
-                         ta_buf tmp, ta_buf out, void *stream);
+ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries, const ta_buf *k_packed,
+                         const ta_buf *k_scales, const ta_buf *k_biases, const ta_buf *v_packed,
+                         const ta_buf *v_scales, const ta_buf *v_biases, const ta_buf *sinks,
+                         const ta_buf *mask_bool, const ta_buf *mask_float, const ta_buf *tmp,
+                         const ta_buf *out, void *stream);
 
 /* ----------------------------------------------------------------- misc */
 

@@ -87,7 +87,8 @@ def _tree_call(ta, p, q=None, k=None, v=None, mask=None, tmp=None, out=None):
     ws = ta.tree_attn_workspace_bytes(p)
     tmp = tmp or B(ws if ws < 2 ** 63 else 0, ta.TA_F32)
     before = ta.ta_launch_count()
-    st = ta.lib.tree_attn_fwd(ctypes.byref(p), q, k, v, mask, tmp, out, None)
+    R = ctypes.byref
+    st = ta.lib.tree_attn_fwd(ctypes.byref(p), R(q), R(k), R(v), R(mask), R(tmp), R(out), None)
     assert ta.ta_launch_count() == before, "a failing call must not launch"
     return st, ta.ta_last_error()
 
@@ -177,10 +178,12 @@ def test_validate_null_misaligned_and_reserved(ta):
 def test_reduce_validates_before_launch(ta):
     p = _p(ta)
     before = ta.ta_launch_count()
-    st = ta.lib.tree_attn_reduce(ctypes.byref(p), _b(ta, 16, ta.TA_F32), _b(ta, 1 << 30, ta.TA_F32), None)
+    R = ctypes.byref
+    st = ta.lib.tree_attn_reduce(ctypes.byref(p), R(_b(ta, 16, ta.TA_F32)), R(_b(ta, 1 << 30, ta.TA_F32)),
+                                 None)
     assert st == 2 and ta.ta_launch_count() == before
-    st = ta.lib.tree_attn_reduce(ctypes.byref(_p(ta, head_dim=96)), _b(ta, 1 << 30, ta.TA_F32),
-                                 _b(ta, 1 << 30, ta.TA_F32), None)
+    st = ta.lib.tree_attn_reduce(ctypes.byref(_p(ta, head_dim=96)), R(_b(ta, 1 << 30, ta.TA_F32)),
+                                 R(_b(ta, 1 << 30, ta.TA_F32)), None)
     assert st == 1
 
 
@@ -212,7 +215,7 @@ def _quant_call(ta, p, T=None, **over):
     order = ["queries", "k_packed", "k_scales", "k_biases", "v_packed", "v_scales", "v_biases",
              "sinks", "mask_bool", "mask_float", "tmp", "out"]
     before = ta.ta_launch_count()
-    st = ta.lib.quant_sdpa_fwd(ctypes.byref(p), *[bufs[k] for k in order], None)
+    st = ta.lib.quant_sdpa_fwd(ctypes.byref(p), *[ctypes.byref(bufs[k]) for k in order], None)
     assert ta.ta_launch_count() == before
     return st, ta.ta_last_error()
 

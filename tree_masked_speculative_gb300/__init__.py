@@ -67,7 +67,7 @@ def _load() -> ctypes.CDLL:
     if not os.path.exists(path):
         raise ImportError("tree_masked_speculative_gb300: %s is missing" % path)
     L = ctypes.CDLL(path)
-    P, B = ctypes.c_void_p, Buf
+    P, B = ctypes.c_void_p, ctypes.POINTER(Buf)
     PT, PQ = ctypes.POINTER(TreeParams), ctypes.POINTER(QuantParams)
     u32 = ctypes.c_uint32
     L.tree_attn_tmp_bytes.argtypes = [u32, u32, u32, u32]
@@ -106,17 +106,18 @@ if _U32 is not None:
     _DTYPE_CODE[_U32] = TA_U32
 
 
-def buf(t: Optional[torch.Tensor], dtype_code: Optional[int] = None) -> Buf:
-    """Describe a tensor (or None = absent buffer) as a ta_buf.  int32 tensors are
-    passed as U32 (packed words, bool masks)."""
+def buf(t: Optional[torch.Tensor], dtype_code: Optional[int] = None):
+    """Describe a tensor as a ta_buf passed by reference; None = absent buffer
+    (a NULL descriptor).  int32 tensors are passed as U32 (packed words, bool
+    masks)."""
     if t is None:
-        return Buf(None, 0, TA_F32, 0)
+        return None
     if not t.is_contiguous():
         raise ValueError("tensor must be contiguous")
     code = _DTYPE_CODE.get(t.dtype) if dtype_code is None else dtype_code
     if code is None:
         raise ValueError("unsupported dtype %s" % t.dtype)
-    return Buf(t.data_ptr(), t.numel() * t.element_size(), code, 0)
+    return ctypes.byref(Buf(t.data_ptr(), t.numel() * t.element_size(), code, 0))
 
 
 def raw_buf(ptr: int, nbytes: int, dtype_code: int) -> Buf:
@@ -198,7 +199,7 @@ def quant_sdpa_fwd(p: QuantParams, queries, k_packed, k_scales, k_biases, v_pack
                    v_biases, sinks, mask_bool, mask_float, tmp, out, stream=None):
     _check(lib.quant_sdpa_fwd(ctypes.byref(p), buf(queries), buf(k_packed, TA_U32), buf(k_scales),
                               buf(k_biases), buf(v_packed, TA_U32), buf(v_scales), buf(v_biases),
-                              buf(sinks), buf(mask_bool, TA_U32) if mask_bool is not None else buf(None),
+                              buf(sinks), buf(mask_bool, TA_U32) if mask_bool is not None else None,
                               buf(mask_float), buf(tmp), buf(out), _stream(stream)))
 
 

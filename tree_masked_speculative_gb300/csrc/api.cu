@@ -151,6 +151,12 @@ bool tree_workspace(const ta_tree_params *p, uint32_t nwg, TreeWorkspace *ws) {
     return ws->total >= ws->off_q16;
 }
 
+const ta_buf kAbsent = {nullptr, 0, TA_F32, 0};
+
+// An optional buffer is absent when its descriptor is NULL or {NULL, 0}.
+bool absent(const ta_buf *b) { return b == nullptr || (b->ptr == nullptr && b->bytes == 0); }
+const ta_buf &deref(const ta_buf *b) { return b ? *b : kAbsent; }
+
 ta_status check_buf(const ta_buf &b, const char *name, uint64_t need_bytes, size_t align) {
     if (b.reserved != 0) return fail(TA_ERR_INVALID_ARGUMENT, "%s: reserved field must be 0", name);
     if (b.ptr == nullptr) return fail(TA_ERR_INVALID_ARGUMENT, "%s: NULL pointer", name);
@@ -342,24 +348,29 @@ TA_EXPORT size_t tree_attn_workspace_bytes(const ta_tree_params *p) {
     return ws.total;
 }
 
-TA_EXPORT ta_status tree_attn_fwd(const ta_tree_params *p, ta_buf q, ta_buf k, ta_buf v, ta_buf mask,
-                                  ta_buf tmp, ta_buf out, void *stream) {
+TA_EXPORT ta_status tree_attn_fwd(const ta_tree_params *p, const ta_buf *q, const ta_buf *k,
+                                  const ta_buf *v, const ta_buf *mask, const ta_buf *tmp,
+                                  const ta_buf *out, void *stream) {
     TreePlan plan;
-    const bool implicit = mask.ptr == nullptr && mask.bytes == 0;
-    TA_TRY(plan_tree(p, &q, &k, &v, implicit ? nullptr : &mask, &tmp, &out, 0, &plan));
+    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), absent(mask) ? nullptr : mask, &deref(tmp),
+                     &deref(out), 0, &plan));
     return run_tree(plan, static_cast<cudaStream_t>(stream));
 }
 
-TA_EXPORT ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, ta_buf q, ta_buf k,
-                                         ta_buf v, ta_buf tmp, ta_buf out, void *stream) {
+TA_EXPORT ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, const ta_buf *q,
+                                         const ta_buf *k, const ta_buf *v, const ta_buf *tmp,
+                                         const ta_buf *out, void *stream) {
     if (window_start > (uint32_t)INT_MAX)
         return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: window_start out of range");
     TreePlan plan;
-    TA_TRY(plan_tree(p, &q, &k, &v, nullptr, &tmp, &out, (int)window_start, &plan));
+    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out),
+                     (int)window_start, &plan));
     return run_tree(plan, static_cast<cudaStream_t>(stream));
 }
 
-TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, ta_buf tmp, ta_buf out, void *stream) {
+TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp_d, const ta_buf *out_d,
+                                     void *stream) {
+    const ta_buf &tmp = deref(tmp_d), &out = deref(out_d);
     TA_TRY(check_tree_params(p, false));
     TA_TRY(check_dtype(tmp, "tmp", TA_F32));
     TA_TRY(check_dtype(out, "output", TA_F32));
@@ -400,10 +411,15 @@ TA_EXPORT size_t quant_sdpa_tmp_bytes(const ta_quant_params *p) {
     return (size_t)b;
 }
 
-TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, ta_buf queries, ta_buf k_packed, ta_buf k_scales,
-                                   ta_buf k_biases, ta_buf v_packed, ta_buf v_scales, ta_buf v_biases,
-                                   ta_buf sinks, ta_buf mask_bool, ta_buf mask_float, ta_buf tmp, ta_buf out,
-                                   void *stream) {
+TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries_d, const ta_buf *k_packed_d,
+                                   const ta_buf *k_scales_d, const ta_buf *k_biases_d, const ta_buf *v_packed_d,
+                                   const ta_buf *v_scales_d, const ta_buf *v_biases_d, const ta_buf *sinks_d,
+                                   const ta_buf *mask_bool_d, const ta_buf *mask_float_d, const ta_buf *tmp_d,
+                                   const ta_buf *out_d, void *stream) {
+    const ta_buf &queries = deref(queries_d), &k_packed = deref(k_packed_d), &k_scales = deref(k_scales_d);
+    const ta_buf &k_biases = deref(k_biases_d), &v_packed = deref(v_packed_d), &v_scales = deref(v_scales_d);
+    const ta_buf &v_biases = deref(v_biases_d), &sinks = deref(sinks_d), &mask_bool = deref(mask_bool_d);
+    const ta_buf &mask_float = deref(mask_float_d), &tmp = deref(tmp_d), &out = deref(out_d);
     TA_TRY(check_quant_params(p));
     const int T = queries.dtype;
     if (T != TA_F16 && T != TA_BF16)
@@ -417,8 +433,8 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, ta_buf queries, ta_
                         same_t_names[i], dtype_name(T), dtype_name(same_t[i]->dtype));
     if (k_packed.dtype != TA_U32 || v_packed.dtype != TA_U32)
         return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: k_packed and v_packed dtype must be U32");
-    const bool has_bool = !(mask_bool.ptr == nullptr && mask_bool.bytes == 0);
-    const bool has_float = !(mask_float.ptr == nullptr && mask_float.bytes == 0);
+    const bool has_bool = !absent(mask_bool_d);
+    const bool has_float = !absent(mask_float_d);
     if (has_bool && mask_bool.dtype != TA_U32)
         return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: mask_bool dtype must be U32");
     if (has_float && mask_float.dtype != T)
