@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--kv-sets", type=int, default=0,
+                    help="K/V copies to rotate over (0 = enough to exceed 3x L2)")
     return ap.parse_args()
 
 
@@ -136,14 +138,14 @@ class ClockSampler:
 
 # ------------------------------------------------------------- tree arm
 class TreeBench:
-    def __init__(self, ta, wl: W.TreeWorkload, dev):
+    def __init__(self, ta, wl: W.TreeWorkload, dev, kv_sets=0):
         self.ta, self.wl, self.dev = ta, wl, dev
         inp = W.make_tree_inputs(wl)
         self.host = inp
         self.q = inp["q"].to(dev)
         self.mask = inp["mask"].to(dev)
         per_set = wl.kv_bytes + self.q.numel() * 4 + self.mask.numel() * 4
-        self.nsets = max(1, math.ceil(3 * L2_BYTES / per_set))
+        self.nsets = kv_sets or max(1, math.ceil(3 * L2_BYTES / per_set))
         k, v = inp["k"].to(dev), inp["v"].to(dev)
         self.ks = [k] + [k.clone() for _ in range(self.nsets - 1)]
         self.vs = [v] + [v.clone() for _ in range(self.nsets - 1)]
@@ -203,14 +205,14 @@ class TreeBench:
 
 # ------------------------------------------------------------ quant arm
 class QuantBench:
-    def __init__(self, ta, wl: W.QuantWorkload, dev):
+    def __init__(self, ta, wl: W.QuantWorkload, dev, kv_sets=0):
         self.ta, self.wl, self.dev = ta, wl, dev
         inp = W.make_quant_inputs(wl)
         self.host = inp
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         self.d = d
         per_set = wl.kv_bytes
-        self.nsets = max(1, math.ceil(3 * L2_BYTES / per_set))
+        self.nsets = kv_sets or max(1, math.ceil(3 * L2_BYTES / per_set))
         kv_keys = ["k_packed", "k_scales", "k_biases", "v_packed", "v_scales", "v_biases"]
         self.sets = [{k: d[k] for k in kv_keys}]
         for _ in range(self.nsets - 1):
@@ -278,9 +280,10 @@ class QuantBench:
         return list(range(self.wl.rows))
 
 
-def make_bench(ta, name, dev):
+def make_bench(ta, name, dev, kv_sets=0):
     wl = WORKLOADS[name]
-    return TreeBench(ta, wl, dev) if isinstance(wl, W.TreeWorkload) else QuantBench(ta, wl, dev)
+    cls = TreeBench if isinstance(wl, W.TreeWorkload) else QuantBench
+    return cls(ta, wl, dev, kv_sets)
 
 
 # ------------------------------------------------------------ timing
@@ -355,7 +358,7 @@ def run_ours(args):
         barrier()
     import tree_masked_speculative_gb300 as ta
 
-    bench = make_bench(ta, args.workload, dev)
+    bench = make_bench(ta, args.workload, dev, args.kv_sets)
     # warm-up (untimed): eager steps, then enough graph replays to bring clocks up
     for i in range(max(3, args.warmup)):
         bench.step(i)
