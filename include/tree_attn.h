@@ -173,6 +173,28 @@ ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, c
 ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp, const ta_buf *out,
                            void *stream);
 
+/*
+ * The whole verify step (main pass and merge, same results as tree_attn_fwd
+ * followed by tree_attn_reduce) for callers that cannot allocate device
+ * memory: engines that plan every device byte up front, plugins inside a
+ * framework that owns the allocator, decode loops that cannot afford the
+ * synchronization an allocation may cause.  The pages have no counterpart;
+ * this entry point exists for those callers only.
+ *   Instead of a caller tmp buffer it uses one static device array of
+ *   16 MiB (16777216 bytes) that every GPU loading the library holds until
+ *   process exit.  Parameters whose tree_attn_workspace_bytes exceed that
+ *   fail with TA_ERR_UNSUPPORTED (lower nwg, or use tree_attn_fwd).
+ *   The array's address is looked up on the first call made on each device
+ *   (that device current); make that first call before any stream capture.
+ *   It allocates nothing and calls no allocating routine.  All calls share the
+ *   array and it keeps the last call's contents; nothing in it has to start
+ *   at zero, but calls that overlap on the GPU race on it.
+ * Buffers as for tree_attn_fwd (an absent mask = implicit causal mask).
+ */
+ta_status tree_attn_fwd_noalloc(const ta_tree_params *p, const ta_buf *q, const ta_buf *k,
+                                const ta_buf *v, const ta_buf *mask, const ta_buf *out,
+                                void *stream);
+
 /* ----------------------------------------------------------------- quant */
 
 /* Splits quant_sdpa_fwd will use (p->nwg when non-zero); 0 on invalid input. */

@@ -19,7 +19,7 @@ from . import build as _build_mod
 __all__ = [
     "TA_OK", "TreeParams", "QuantParams", "TreeAttentionError", "lib", "library_path",
     "tree_attn_tmp_bytes", "tree_attn_num_splits", "tree_attn_workspace_bytes", "tree_attn_fwd",
-    "tree_attn_fwd_causal", "tree_attn_reduce", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
+    "tree_attn_fwd_causal", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
     "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "tree_attention",
     "quant_sdpa", "tree_params", "quant_params",
 ]
@@ -82,6 +82,8 @@ def _load() -> ctypes.CDLL:
     L.tree_attn_fwd_causal.restype = ctypes.c_int
     L.tree_attn_reduce.argtypes = [PT, B, B, P]
     L.tree_attn_reduce.restype = ctypes.c_int
+    L.tree_attn_fwd_noalloc.argtypes = [PT, B, B, B, B, B, P]
+    L.tree_attn_fwd_noalloc.restype = ctypes.c_int
     L.quant_sdpa_num_splits.argtypes = [PQ]
     L.quant_sdpa_num_splits.restype = u32
     L.quant_sdpa_tmp_bytes.argtypes = [PQ]
@@ -185,6 +187,13 @@ def tree_attn_fwd_causal(p: TreeParams, window_start: int, q, k, v, tmp, out, st
 
 def tree_attn_reduce(p: TreeParams, tmp, out, stream=None):
     _check(lib.tree_attn_reduce(ctypes.byref(p), buf(tmp), buf(out), _stream(stream)))
+
+
+def tree_attn_fwd_noalloc(p: TreeParams, q, k, v, mask, out, stream=None):
+    """Main pass + merge with the library's static scratch (no tmp buffer); for
+    callers that cannot allocate device memory.  mask=None: implicit causal."""
+    _check(lib.tree_attn_fwd_noalloc(ctypes.byref(p), buf(q), buf(k), buf(v), buf(mask), buf(out),
+                                     _stream(stream)))
 
 
 def quant_sdpa_num_splits(p: QuantParams) -> int:

@@ -322,6 +322,15 @@ bool quant_tmp(const ta_quant_params *p, uint32_t nwg, uint64_t *bytes) {
 
 void count_launch(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
+void set_last_error(const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+}
+
 }  // namespace ta
 
 using namespace ta;

@@ -117,6 +117,9 @@ constexpr int kFmaRowsPerCta = 16;
 
 void count_launch(int n = 1);
 
+// Set the calling thread's ta_last_error() message (printf format).
+void set_last_error(const char *fmt, ...);
+
 // Raise a kernel's dynamic shared-memory limit once per device; later calls
 // (for example while a CUDA graph is being captured) only read a flag.
 template <typename Kern>
