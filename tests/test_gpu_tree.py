@@ -71,28 +71,72 @@ def test_explicit_causal_mask_bit_identical_to_implicit(ta, path):
                      oracle.tree_oracle_for(wl, inp, mask=None, window_start=ws))
 
 
-def test_single_attended_key_returns_value_row_exactly(ta, path):
-    wl = small_tree(H=4, Hk=2, D=128, N=300, C=300, L=3, kv_dtype="bf16", nwg=4)
+# (H, Hk): 4/2 gives 2*L rows per KV head (CUDA-core kernel for small L),
+# 16/2 gives 8*L rows per KV head (tensor-core kernel for 16-bit K/V).
+@pytest.mark.parametrize("H,Hk,D", [(4, 2, 128), (16, 2, 128), (16, 2, 256), (8, 1, 512)])
+def test_single_attended_key_returns_value_row_exactly(ta, path, H, Hk, D):
+    wl = small_tree(H=H, Hk=Hk, D=D, N=300, C=300, L=3, kv_dtype="bf16", nwg=4)
     inp = W.make_tree_inputs(wl)
     inp["mask"][:] = W.MASKED
     keys = [5, 177, 299]
     for i, j in enumerate(keys):
         inp["mask"][i, j] = 0.0
     got = run_tree(ta, wl, inp).cpu()
+    g = H // Hk
     for i, j in enumerate(keys):
-        for h in range(4):
-            assert torch.equal(got[i, h], inp["v"][h // 2, j].float()), (i, h)
+        for h in range(H):
+            assert torch.equal(got[i, h], inp["v"][h // g, j].float()), (i, h)
 
 
-def test_fully_masked_rows_and_dead_chunks(ta, path):
-    wl = small_tree(H=4, Hk=2, D=256, N=640, C=640, L=6, kv_dtype="f16", nwg=3)
+@pytest.mark.parametrize("H,Hk,D,kvd", [(4, 2, 256, "f16"), (24, 4, 256, "f16"), (16, 2, 512, "bf16"),
+                                        (12, 1, 128, "bf16")])
+def test_fully_masked_rows_and_dead_chunks(ta, path, H, Hk, D, kvd):
+    wl = small_tree(H=H, Hk=Hk, D=D, N=640, C=640, L=6, kv_dtype=kvd, nwg=3)
     inp = W.make_tree_inputs(wl)
     m = inp["mask"]
     m[2] = W.MASKED                        # row with no attended key -> zeros
     m[:, 64:320] = W.MASKED                # chunks no row attends: never loaded
+    m[4, 330:640] = W.MASKED               # a row whose last chunks are dead for it alone
     got = run_tree(ta, wl, inp).cpu().numpy()
     assert np.all(got[2] == 0.0)
     assert_close(got, oracle.tree_oracle_for(wl, inp))
+
+
+def test_all_keys_dead_for_every_row(ta, path):
+    wl = small_tree(H=16, Hk=2, D=128, N=200, C=200, L=4, kv_dtype="f16", nwg=2)
+    inp = W.make_tree_inputs(wl)
+    inp["mask"][:] = W.MASKED
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    assert np.all(got == 0.0)
+
+
+def test_large_logits_exercise_rescaling(ta, path):
+    """Logit ranges far above the lazy-rescale slack, growing along the keys so the
+    running max moves many times."""
+    wl = small_tree(H=16, Hk=2, D=128, N=1500, C=1500, L=4, kv_dtype="bf16", nwg=2, scale=1.0)
+    inp = W.make_tree_inputs(wl)
+    ramp = torch.linspace(0.1, 3.0, wl.kv_seq_len).view(1, -1, 1)
+    inp["k"] = (inp["k"].float() * ramp).to(torch.bfloat16)
+    # quarters are exact in bf16, so the logits carry no Q-rounding error and the
+    # comparison isolates the rescaling of O and S
+    inp["q"] = torch.round(inp["q"] * 4.0) / 4.0
+    got = run_tree(ta, wl, inp).cpu().numpy()
+    assert_close(got, oracle.tree_oracle_for(wl, inp))
+
+
+def test_device_error_word_stays_zero(ta):
+    wl = small_tree(H=24, Hk=4, D=256, N=900, C=1024, L=32, kv_dtype="f16", nwg=6)
+    inp = to_dev(W.make_tree_inputs(wl))
+    p = ta.tree_params(wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.kv_seq_len, wl.kv_capacity,
+                       wl.scale, wl.q_l, wl.mask_stride, wl.nwg)
+    ws = ta.tree_attn_workspace_bytes(p)
+    tmp = torch.full(((ws + 3) // 4,), 123.0, device="cuda")
+    out = torch.empty((wl.q_l, wl.n_heads, wl.head_dim), device="cuda")
+    ta.tree_attn_fwd(p, inp["q"], inp["k"], inp["v"], inp["mask"], tmp, out)
+    ta.tree_attn_reduce(p, tmp, out)
+    torch.cuda.synchronize()
+    err_word = tmp.view(torch.int32)[(ws - 256) // 4].item()
+    assert err_word == 0
 
 
 def test_split_count_invariance(ta, path):
@@ -105,11 +149,11 @@ def test_split_count_invariance(ta, path):
     assert_close(outs[0], outs[-1], atol=1e-4, rtol=1e-4)
 
 
-def test_output_guard_bytes_untouched(ta, path):
-    wl = small_tree(H=4, Hk=2, D=128, N=200, C=256, L=5, kv_dtype="f16", nwg=3)
+@pytest.mark.parametrize("H,Hk,D,L", [(4, 2, 128, 5), (16, 2, 256, 5)])
+def test_output_guard_bytes_untouched(ta, path, H, Hk, D, L):
+    wl = small_tree(H=H, Hk=Hk, D=D, N=200, C=256, L=L, kv_dtype="f16", nwg=3)
     inp = to_dev(W.make_tree_inputs(wl))
-    H, L, D = 4, 5, 128
-    p = ta.tree_params(H, 2, D, 200, 256, wl.scale, L, 200, 3)
+    p = ta.tree_params(H, Hk, D, 200, 256, wl.scale, L, 200, 3)
     ws = ta.tree_attn_workspace_bytes(p)
     tmp_full = torch.full(((ws + 3) // 4 + 1024,), 7.0, device="cuda")
     out_full = torch.full((L * H * D + 1024,), 7.0, device="cuda")

@@ -6,11 +6,14 @@
 // saturating arithmetic) for the tree path, and the shape rules of
 // metaltile-std flash_quantized_sdpa.rs (module doc "Layout", dispatch
 // invariants) for the quantized path.  Every check runs before any launch.
+#include <cudaTypedefs.h>
+
 #include <atomic>
 #include <climits>
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <mutex>
 #include <string>
 
 #include "ta_internal.cuh"
@@ -126,12 +129,19 @@ uint32_t resolve_tree_nwg(const ta_tree_params *p) {
     if (sms <= 0) return 0;
     const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
     const uint64_t R = (uint64_t)rows_per_kv(p);
-    uint64_t units;
-    if (R >= 16) units = (uint64_t)p->n_kv_heads * ((R + 127) / 128) * (p->head_dim == 512 ? 2 : 1);
-    else units = (uint64_t)p->n_kv_heads * ((R + kFmaRowsPerCta - 1) / kFmaRowsPerCta);
-    uint64_t nwg = (2ull * sms + units - 1) / units;
+    uint64_t nwg;
+    if (R >= 16) {
+        // tensor-core kernel: one CTA per SM, CTAs = splits x row tiles x O halves x KV heads
+        const uint64_t units = (uint64_t)p->n_kv_heads * ((R + 127) / 128) * (p->head_dim == 512 ? 2 : 1);
+        nwg = (uint64_t)sms / units;
+        const uint64_t max_splits = (n_chunks + 3) / 4;      // at least one 4-chunk tile each
+        if (nwg > max_splits) nwg = max_splits;
+    } else {
+        const uint64_t units = (uint64_t)p->n_kv_heads * ((R + kFmaRowsPerCta - 1) / kFmaRowsPerCta);
+        nwg = (2ull * sms + units - 1) / units;
+        if (nwg > n_chunks) nwg = n_chunks;
+    }
     if (nwg < 1) nwg = 1;
-    if (nwg > n_chunks) nwg = n_chunks;
     if (nwg > 65535) nwg = 65535;
     return (uint32_t)nwg;
 }
@@ -147,7 +157,8 @@ bool tree_workspace(const ta_tree_params *p, uint32_t nwg, TreeWorkspace *ws) {
     const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
     ws->off_cls = align256(po + pml);
     ws->off_q16 = align256(ws->off_cls + n_chunks);
-    ws->total = align256(ws->off_q16 + q16);
+    ws->off_err = align256(ws->off_q16 + q16);
+    ws->total = ws->off_err + 256;
     return ws->total >= ws->off_q16;
 }
 
@@ -185,7 +196,34 @@ struct TreePlan {
     TreeArgs a;
     int kv_type;
     bool use_tc;
+    void *k, *v;
 };
+
+// cuTensorMapEncodeTiled from the driver, looked up once.
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+    std::call_once(g_encode_once, [] {
+        cudaDriverEntryPointQueryResult q;
+        void *fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        else
+            cudaGetLastError();
+    });
+    return g_encode != nullptr;
+}
+
+bool encode_map(CUtensorMap *m, bool bf16, void *ptr, int rank, const cuuint64_t *dims, const cuuint64_t *strides,
+                const cuuint32_t *box) {
+    const cuuint32_t es[3] = {1, 1, 1};
+    return g_encode(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, rank, ptr, dims,
+                    strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, const ta_buf *v,
                     const ta_buf *mask, const ta_buf *tmp, const ta_buf *out, int window_start,
@@ -234,6 +272,7 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     a.part_ml = reinterpret_cast<float *>(t + ws.off_part_ml);
     a.cls = reinterpret_cast<uint8_t *>(t + ws.off_cls);
     a.q16 = t + ws.off_q16;
+    a.err = reinterpret_cast<int *>(t + ws.off_err);
     a.out = static_cast<float *>(out->ptr);
     a.H = (int)p->n_heads;
     a.Hk = (int)p->n_kv_heads;
@@ -249,14 +288,37 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     a.window_start = window_start;
     a.scale = p->scale;
     plan->kv_type = k->dtype == TA_F32 ? kKvF32 : (k->dtype == TA_F16 ? kKvF16 : kKvBF16);
-    plan->use_tc = false;
+    plan->k = k->ptr;
+    plan->v = v->ptr;
+    // Tensor cores when the K/V type is 16-bit and a KV head serves >= 16 query
+    // rows (a dense contraction); otherwise the CUDA-core kernel.
+    const int path = g_tree_path.load(std::memory_order_relaxed);
+    plan->use_tc = path != 1 && plan->kv_type != kKvF32 && a.R >= 16;
+    a.q16_type = plan->use_tc ? plan->kv_type : -1;
+    if (plan->use_tc && !get_encoder())
+        return fail(TA_ERR_CUDA, "tree_attention: cuTensorMapEncodeTiled is not available");
     return TA_OK;
 }
 
 ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
+    TcMaps maps;
+    if (plan.use_tc) {
+        const TreeArgs &a = plan.a;
+        const bool bf16 = plan.kv_type == kKvBF16;
+        const cuuint64_t qdims[2] = {(cuuint64_t)a.D, (cuuint64_t)a.H * a.L};
+        const cuuint64_t qstr[1] = {(cuuint64_t)a.D * 2};
+        const cuuint32_t qbox[2] = {64, 128};
+        const cuuint64_t kdims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.N, (cuuint64_t)a.Hk};
+        const cuuint64_t kstr[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.C * a.D * 2};
+        const cuuint32_t kbox[3] = {64, 32, 1};
+        if (!encode_map(&maps.q16, bf16, a.q16, 2, qdims, qstr, qbox) ||
+            !encode_map(&maps.k, bf16, plan.k, 3, kdims, kstr, kbox) ||
+            !encode_map(&maps.v, bf16, plan.v, 3, kdims, kstr, kbox))
+            return fail(TA_ERR_CUDA, "tree_attention: TMA descriptor encoding failed");
+    }
     cudaError_t e = launch_tree_classify(plan.a, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: chunk classification launch");
-    e = launch_tree_fma(plan.a, plan.kv_type, s);
+    e = plan.use_tc ? launch_tree_tc(plan.a, maps, plan.kv_type, s) : launch_tree_fma(plan.a, plan.kv_type, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: main pass launch");
     return TA_OK;
 }

@@ -1,6 +1,7 @@
 // Internal declarations of the tree-verify attention library (not installed).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -80,8 +81,17 @@ struct TreeArgs {
     float *part_ml;        // [nwg][nrows][2] = (S, M)
     float *out;            // [L, H, D]
     void *q16;             // [H*L, D] 16-bit copy of Q (tensor-core path)
+    int *err;              // workspace error word (0 = ok), zeroed by the prep pass
     int H, Hk, D, N, C, L, stride, nwg, g, R, n_chunks, window_start;
+    int q16_type;          // -1: no 16-bit Q copy, else kKvF16 / kKvBF16
     float scale;
+};
+
+// TMA descriptors of the tensor-core tree kernel (kernel parameters).
+struct TcMaps {
+    CUtensorMap q16;   // 2D {D, H*L} 16-bit, box {64, 128}, 128-byte swizzle
+    CUtensorMap k;     // 3D {D, kv_seq_len, Hk}, box {64, 32, 1}, 128-byte swizzle
+    CUtensorMap v;
 };
 
 struct QuantArgs {
@@ -101,13 +111,14 @@ struct QuantArgs {
 
 // Workspace layout inside the caller's tmp buffer (all offsets 256-aligned).
 struct TreeWorkspace {
-    size_t off_part_o, off_part_ml, off_cls, off_q16, total;
+    size_t off_part_o, off_part_ml, off_cls, off_q16, off_err, total;
 };
 
 // ------------------------------------------------------------ host launches
 // Each returns cudaGetLastError() after enqueueing on `s`.
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
+cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_quant_fma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s);

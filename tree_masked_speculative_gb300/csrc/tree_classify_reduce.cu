@@ -14,11 +14,40 @@
 
 namespace ta {
 
-// One warp per chunk.  Class: dead if no (row, key < N) cell is attended
-// (> -65504), all-attended if every (row, key < N) cell equals 0.0, else mixed.
-__global__ void __launch_bounds__(256) tree_classify_kernel(const TreeArgs a) {
+// Prep pass, one launch: blocks [0, n_cls) classify the chunks, one warp per
+// chunk (dead if no (row, key < N) cell is attended (> -65504), all-attended if
+// every (row, key < N) cell equals 0.0, else mixed); the remaining blocks
+// write the 16-bit copy of Q for the tensor-core kernel; block 0 clears the
+// error word.
+constexpr int kPrepThreads = 256;
+constexpr int kQ16PerBlock = kPrepThreads * 8;
+
+__global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs a, int n_cls_blocks) {
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) *a.err = 0;
+    if (static_cast<int>(blockIdx.x) >= n_cls_blocks) {
+        // Q [H*L, D] f32 -> 16-bit (round to nearest), 8 elements per thread
+        const size_t total = static_cast<size_t>(a.H) * a.L * a.D;
+        const size_t i8 = (static_cast<size_t>(blockIdx.x - n_cls_blocks) * kPrepThreads + threadIdx.x) * 8;
+        if (i8 >= total) return;
+        const float4 x0 = __ldg(reinterpret_cast<const float4 *>(a.q + i8));
+        const float4 x1 = __ldg(reinterpret_cast<const float4 *>(a.q + i8) + 1);
+        uint4 o;
+        if (a.q16_type == kKvBF16) {
+            __nv_bfloat162 b0 = __floats2bfloat162_rn(x0.x, x0.y), b1 = __floats2bfloat162_rn(x0.z, x0.w);
+            __nv_bfloat162 b2 = __floats2bfloat162_rn(x1.x, x1.y), b3 = __floats2bfloat162_rn(x1.z, x1.w);
+            o = make_uint4(*reinterpret_cast<uint32_t *>(&b0), *reinterpret_cast<uint32_t *>(&b1),
+                           *reinterpret_cast<uint32_t *>(&b2), *reinterpret_cast<uint32_t *>(&b3));
+        } else {
+            __half2 h0 = __floats2half2_rn(x0.x, x0.y), h1 = __floats2half2_rn(x0.z, x0.w);
+            __half2 h2 = __floats2half2_rn(x1.x, x1.y), h3 = __floats2half2_rn(x1.z, x1.w);
+            o = make_uint4(*reinterpret_cast<uint32_t *>(&h0), *reinterpret_cast<uint32_t *>(&h1),
+                           *reinterpret_cast<uint32_t *>(&h2), *reinterpret_cast<uint32_t *>(&h3));
+        }
+        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.q16) + i8) = o;
+        return;
+    }
     const int lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int chunk = blockIdx.x * (kPrepThreads / 32) + (threadIdx.x >> 5);
     if (chunk >= a.n_chunks) return;
     const int key = chunk * 32 + lane;
     const bool valid = key < a.N;
@@ -50,8 +79,13 @@ __global__ void __launch_bounds__(256) tree_classify_kernel(const TreeArgs a) {
 }
 
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
-    dim3 grid((a.n_chunks + 7) / 8);
-    tree_classify_kernel<<<grid, 256, 0, s>>>(a);
+    const int n_cls = (a.n_chunks + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+    int n_q = 0;
+    if (a.q16_type >= 0) {
+        const size_t total = static_cast<size_t>(a.H) * a.L * a.D;
+        n_q = static_cast<int>((total + kQ16PerBlock - 1) / kQ16PerBlock);
+    }
+    tree_prep_kernel<<<n_cls + n_q, kPrepThreads, 0, s>>>(a, n_cls);
     count_launch();
     return cudaGetLastError();
 }

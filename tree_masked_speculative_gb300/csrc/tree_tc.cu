@@ -1,0 +1,507 @@
+// Tensor-core (tcgen05) tree-verify attention main pass for f16 / bf16 K/V.
+//
+// Semantics are those of mlx-native tree_attention.metal (tree_attention_impl):
+// logit = fma(qk, scale, mask); a 32-key chunk whose mask cells are all
+// <= -65504 for a row contributes nothing to that row; online softmax with a
+// running max M and sum S; partial (O, S, M) per split, merged by the reduce
+// pass (or normalized here when there is a single split).  The Metal kernel
+// walks one query row per threadgroup with CUDA-core-style dot products; here
+// all query rows of a KV head are one dense contraction for the tensor core.
+//
+// One CTA = (split, 128-row tile x O-column half, KV head).  Rows r of KV head
+// k are (head k*g + r / L, query r % L), contiguous in the 16-bit Q copy.
+//   warp 0     : TMA producer - the Q tile once, then K and V slabs
+//                ([128 keys x 64 cols] 16-bit, 128-byte swizzle) through a ring
+//                of 16 KB stages, in the order the MMA warp consumes them
+//                (K_0, K_1, V_0, K_2, V_1, ...).  A tile holds the next 4 live
+//                32-key chunks of the split; empty slots and keys past
+//                kv_seq_len are loaded out of bounds, i.e. as zeros.
+//   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
+//                TMEM, double buffered) and O += P_t V_t (M 128, N 64 per V slab,
+//                P from shared memory, V MN-major).
+//   warps 2..5 : one thread per row: mask + scale, online softmax with lazy
+//                rescaling (M only moves when a row max exceeds it by more
+//                than kRescaleSlack, so O in TMEM is rarely touched), P as
+//                16-bit into swizzled shared memory, epilogue from TMEM.
+// Every mbarrier wait is bounded; on a timeout the CTA sets the workspace
+// error word, drains its outstanding copies and MMAs, frees TMEM and exits.
+#include "sm100_ptx.cuh"
+#include "ta_internal.cuh"
+
+namespace ta {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kTcThreads = 192;
+constexpr int kSlab = 16384;                 // [128 rows][64 x 16-bit], 128-byte swizzled
+constexpr uint32_t kWaitIters = 1u << 22;
+constexpr float kRescaleSlack = 8.0f;        // P <= e^8 = 2981 fits f16 and bf16
+
+template <int D>
+struct TcCfg {
+    static constexpr int DV = D < 256 ? D : 256;     // O columns per CTA
+    static constexpr int NSK = D / 64;               // K slabs per key tile
+    static constexpr int NSV = DV / 64;              // V slabs per key tile
+    static constexpr int STAGES = D == 512 ? 4 : (D == 256 ? 8 : 10);
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_P = OFF_Q + NSK * kSlab;
+    static constexpr int OFF_RING = OFF_P + 2 * kSlab;
+    static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
+    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static_assert(SMEM <= 232448, "shared memory budget");
+};
+
+struct Bars {
+    uint64_t full[10];
+    uint64_t empty[10];
+    uint64_t q_full;
+    uint64_t s_full[2];
+    uint64_t s_free[2];
+    uint64_t p_full;
+    uint64_t o_done;
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+
+// Walk of the live 32-key chunks [lo, hi) (in live order) of this split.
+// Warp-collective: all lanes hold the same state.
+struct ChunkWalk {
+    const uint8_t *cls;
+    int n_chunks, base, left;
+    uint32_t pending;
+
+    __device__ void init(const uint8_t *c, int n, int lo, int hi) {
+        cls = c;
+        n_chunks = n;
+        left = hi > lo ? hi - lo : 0;
+        const int lane = threadIdx.x & 31;
+        int r = 0;
+        base = 0;
+        pending = 0;
+        while (base < n_chunks) {
+            const bool live = base + lane < n_chunks && cls[base + lane] != kChunkDead;
+            uint32_t m = __ballot_sync(0xffffffffu, live);
+            const int cnt = __popc(m);
+            if (r + cnt > lo) {
+                for (int skip = lo - r; skip > 0; --skip) m &= m - 1;
+                pending = m;
+                return;
+            }
+            r += cnt;
+            base += 32;
+        }
+    }
+    // Next live chunk index, or -1 when the split's range is exhausted.
+    __device__ int next() {
+        if (left <= 0) return -1;
+        const int lane = threadIdx.x & 31;
+        while (pending == 0) {
+            base += 32;
+            if (base >= n_chunks) { left = 0; return -1; }
+            pending = __ballot_sync(0xffffffffu, base + lane < n_chunks && cls[base + lane] != kChunkDead);
+        }
+        const int c = base + __ffs(pending) - 1;
+        pending &= pending - 1;
+        --left;
+        return c;
+    }
+};
+
+__device__ __forceinline__ int split_live_range(const uint8_t *cls, int n_chunks, int nwg, int split, int *lo,
+                                                int *hi) {
+    const int lane = threadIdx.x & 31;
+    int n_live = 0;
+    for (int b = 0; b < n_chunks; b += 32)
+        n_live += __popc(__ballot_sync(0xffffffffu, b + lane < n_chunks && cls[b + lane] != kChunkDead));
+    const int cps = (n_live + nwg - 1) / nwg;
+    *lo = min(n_live, split * cps);
+    *hi = min(n_live, *lo + cps);
+    return (*hi - *lo + 3) / 4;   // key tiles
+}
+
+__device__ __forceinline__ void note_abort(Bars *b, int *err, int code) {
+    b->abort_flag = 1;
+    atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code) {
+    if (b->abort_flag) return false;
+    if (mbar_wait(bar, parity, kWaitIters)) return true;
+    note_abort(b, err, code);
+    return false;
+}
+
+__device__ __forceinline__ uint32_t pack2(float lo, float hi, bool bf16) {
+    if (bf16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&v);
+    }
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ float lo16(uint32_t u, bool bf16) {
+    if (bf16) return __uint_as_float(u << 16);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(u & 0xffffu)));
+}
+__device__ __forceinline__ float hi16(uint32_t u, bool bf16) {
+    if (bf16) return __uint_as_float(u & 0xffff0000u);
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
+}
+
+template <int D, bool BF16, bool IMPLICIT>
+__global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a, const __grid_constant__ TcMaps maps) {
+    using Cfg = TcCfg<D>;
+    constexpr int DV = Cfg::DV, NSK = Cfg::NSK, NSV = Cfg::NSV, ST = Cfg::STAGES;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                                          ~static_cast<uintptr_t>(1023));
+    unsigned char *sQ = sm + Cfg::OFF_Q;
+    unsigned char *sP = sm + Cfg::OFF_P;
+    unsigned char *sRing = sm + Cfg::OFF_RING;
+    Bars *bars = reinterpret_cast<Bars *>(sm + Cfg::OFF_BAR);
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x;
+    const int n_os = D / DV;
+    const int rt = blockIdx.y / n_os, os = blockIdx.y % n_os;
+    const int kh = blockIdx.z;
+    const int n_rt = (a.R + 127) / 128;
+    const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
+    const int rows_here = min(RT, a.R - rt * RT);
+    int *err = a.err;
+
+    if (tid == 0) {
+        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], 1); }
+        mbar_init(&bars->q_full, 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 4); }
+        mbar_init(&bars->p_full, 4);
+        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 512);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tm_s[2] = {tmem, tmem + 128};
+    const uint32_t tm_o = tmem + 256;
+
+    int lo, hi;
+    const int T = split_live_range(a.cls, a.n_chunks, a.nwg, split, &lo, &hi);
+    const int n_pad = ((a.N + 31) / 32) * 32;          // a key row that is out of bounds
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        ChunkWalk walk;
+        walk.init(a.cls, a.n_chunks, lo, hi);
+        int issued = 0;                                 // ring loads issued
+        auto load_slabs = [&](const CUtensorMap *map, const int (&chunk)[4], int nslab, int x0) -> bool {
+            for (int s = 0; s < nslab; ++s) {
+                const int slot = issued % ST;
+                const uint32_t pass = static_cast<uint32_t>(issued / ST);
+                bool ok = true;
+                if (lane == 0) {
+                    ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1);
+                    if (ok) {
+                        mbar_arrive_expect_tx(&bars->full[slot], kSlab);
+                        unsigned char *dst = sRing + slot * kSlab;
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64,
+                                        chunk[c] >= 0 ? chunk[c] * 32 : n_pad, kh);
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) return false;
+                ++issued;
+            }
+            return true;
+        };
+        bool ok = true;
+        if (T > 0) {
+            if (lane == 0) {
+                tma_prefetch_desc(&maps.k);
+                tma_prefetch_desc(&maps.v);
+                mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
+                for (int s = 0; s < NSK; ++s)
+                    tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
+            }
+            int cur[4], nxt[4];
+            for (int c = 0; c < 4; ++c) nxt[c] = walk.next();
+            ok = load_slabs(&maps.k, nxt, NSK, 0);
+            for (int t = 0; t < T && ok; ++t) {
+                for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
+                if (t + 1 < T) {
+                    for (int c = 0; c < 4; ++c) nxt[c] = walk.next();
+                    ok = load_slabs(&maps.k, nxt, NSK, 0);
+                }
+                if (ok) ok = load_slabs(&maps.v, cur, NSV, os * DV);
+            }
+            // Drain: every copy issued into the ring has landed before exit.
+            if (lane == 0) {
+                if (!mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9);
+                const int first = issued > ST ? issued - ST : 0;
+                for (int n = first; n < issued; ++n)
+                    if (!mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
+                        note_abort(bars, err, 9);
+            }
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && T > 0) {
+            constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+            constexpr uint32_t id_pv = idesc_f16(128, 64, BF16 ? 1 : 0, 0, 1);
+            const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), ring_addr = smem_u32(sRing);
+            int used = 0;                                   // ring loads consumed
+            bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2);
+            auto issue_s = [&](int t) -> bool {
+                const int sb = t & 1;
+                if (!wait_or_abort(bars, &bars->s_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err, 3))
+                    return false;
+                tc_fence_after();
+                for (int s = 0; s < NSK; ++s) {
+                    const int slot = used % ST;
+                    if (!wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 4))
+                        return false;
+                    tc_fence_after();
+                    const uint32_t kb = ring_addr + slot * kSlab;
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_f16_ss(tm_s[sb], sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024),
+                                   sw128_desc(kb + kk * 32, 16, 1024), id_qk, (s | kk) != 0);
+                    mma_commit(&bars->empty[slot]);
+                    ++used;
+                }
+                mma_commit(&bars->s_full[sb]);
+                return true;
+            };
+            if (ok) ok = issue_s(0);
+            for (int t = 0; t < T && ok; ++t) {
+                if (t + 1 < T) ok = issue_s(t + 1);
+                if (!ok) break;
+                ok = wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5);
+                if (!ok) break;
+                tc_fence_after();
+                for (int s = 0; s < NSV && ok; ++s) {
+                    const int slot = used % ST;
+                    ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 6);
+                    if (!ok) break;
+                    tc_fence_after();
+                    const uint32_t vb = ring_addr + slot * kSlab;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16_ss(tm_o + s * 64, sw128_desc(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+                                   sw128_desc(vb + kk * 2048, kSlab, 1024), id_pv, (t | kk) != 0);
+                    mma_commit(&bars->empty[slot]);
+                    ++used;
+                }
+                mma_commit(&bars->o_done);
+            }
+            // Drain: all MMAs issued by this thread have completed.
+            mma_commit(&bars->drain);
+            if (!mbar_wait(&bars->drain, 0, kWaitIters)) note_abort(bars, err, 10);
+        }
+    } else {
+        // ---------------------------------------------- softmax and epilogue
+        const int quarter = warp & 3;                   // TMEM lanes 32*quarter .. +31
+        const int r = quarter * 32 + lane;              // row within the tile
+        const int rg = rt * RT + r;                     // row within the KV group
+        const bool row_ok = r < rows_here;
+        const int qi = rg % a.L;                        // query (tree node)
+        const int hj = kh * a.g + (rg / a.L);           // query head
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        const int last0 = a.N - a.L;
+        const float *mrow = IMPLICIT ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
+
+        ChunkWalk walk;
+        walk.init(a.cls, a.n_chunks, lo, hi);
+        float m_run = -INFINITY, l_run = 0.0f;
+        bool ok = true;
+        for (int t = 0; t < T && ok; ++t) {
+            int chunk[4];
+            for (int c = 0; c < 4; ++c) chunk[c] = walk.next();
+            const int sb = t & 1;
+            ok = wait_or_abort(bars, &bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, err, 7);
+            if (!ok) break;
+            tc_fence_after();
+            float s[128];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t rr[32];
+                tmem_ld32(tm_s[sb] + lane_off + c * 32, rr);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[e]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->s_free[sb]);
+
+            // mask + scale per 32-key chunk
+            float rmax = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                const int ch = chunk[c];
+                if (ch < 0) {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = -INFINITY;
+                    continue;
+                }
+                const int key0 = ch * 32;
+                const int cl = a.cls[ch];
+                bool live = false;
+                float mv[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int key = key0 + e;
+                    float v;
+                    if (key >= a.N) v = kMasked;
+                    else if (IMPLICIT) v = (key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
+                    else v = (cl == kChunkAllAttended) ? 0.0f : __ldg(mrow + key);
+                    mv[e] = v;
+                    live |= v > kMasked;
+                }
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const float lg = live ? fmaf(s[c * 32 + e], a.scale, mv[e]) : -INFINITY;
+                    s[c * 32 + e] = lg;
+                    rmax = fmaxf(rmax, lg);
+                }
+            }
+            // online softmax with lazy rescaling
+            float alpha = 1.0f;
+            if (rmax > m_run + kRescaleSlack) {
+                alpha = expf(m_run - rmax);             // 0 when m_run = -inf
+                l_run *= alpha;
+                m_run = rmax;
+            }
+            const bool row_live = m_run != -INFINITY;
+            uint32_t pk[64];
+            float psum = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 64; ++e) {
+                const float p0 = row_live ? expf(s[2 * e] - m_run) : 0.0f;
+                const float p1 = row_live ? expf(s[2 * e + 1] - m_run) : 0.0f;
+                pk[e] = pack2(p0, p1, BF16);
+                psum += lo16(pk[e], BF16) + hi16(pk[e], BF16);
+            }
+            l_run += psum;
+
+            // PV of the previous tile done: P buffer free, O stable
+            if (t > 0) {
+                ok = wait_or_abort(bars, &bars->o_done, static_cast<uint32_t>(t - 1) & 1u, err, 8);
+                if (!ok) break;
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+#pragma unroll 1
+                    for (int c = 0; c < DV / 32; ++c) {
+                        uint32_t rr[32];
+                        tmem_ld32(tm_o + lane_off + c * 32, rr);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
+                        tmem_st32(tm_o + lane_off + c * 32, rr);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // P row -> shared memory, K-major 128-byte swizzle: 16-byte unit u of
+            // row r is stored at unit u ^ (r % 8) within the row's 128 bytes.
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                const int slab = u >> 3, cu = u & 7;
+                uint4 v4 = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+                *reinterpret_cast<uint4 *>(sP + slab * kSlab + r * 128 + ((cu ^ (r & 7)) << 4)) = v4;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->p_full);
+        }
+        if (ok && T > 0) {
+            ok = wait_or_abort(bars, &bars->o_done, static_cast<uint32_t>(T - 1) & 1u, err, 8);
+            tc_fence_after();
+        }
+        // epilogue: partial (O, S, M) or, with one split, the normalized output
+        const int nrows = a.H * a.L;
+        const size_t rid = static_cast<size_t>(qi) * a.H + hj;
+        const float inv = (l_run == 0.0f) ? 0.0f : 1.0f / l_run;
+        float *dst = (a.nwg == 1) ? a.out + rid * D + os * DV
+                                  : a.part_o + (static_cast<size_t>(split) * nrows + rid) * D + os * DV;
+        const float scale_out = (a.nwg == 1) ? inv : 1.0f;
+        const bool have_o = ok && T > 0;
+#pragma unroll 1
+        for (int c = 0; c < DV / 32; ++c) {
+            uint32_t rr[32];
+            if (have_o) {
+                tmem_ld32(tm_o + lane_off + c * 32, rr);
+                tmem_wait_ld();
+            } else {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) rr[e] = 0u;
+            }
+            if (row_ok) {
+#pragma unroll
+                for (int e = 0; e < 32; e += 4) {
+                    float4 v = make_float4(__uint_as_float(rr[e]) * scale_out, __uint_as_float(rr[e + 1]) * scale_out,
+                                           __uint_as_float(rr[e + 2]) * scale_out,
+                                           __uint_as_float(rr[e + 3]) * scale_out);
+                    *reinterpret_cast<float4 *>(dst + c * 32 + e) = v;
+                }
+            }
+        }
+        if (row_ok && a.nwg > 1 && os == 0) {
+            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 0] = l_run;
+            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 1] = m_run == -INFINITY ? kMInit : m_run;
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+template <int D, bool BF16, bool IMPLICIT>
+cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
+    auto kern = tree_tc_kernel<D, BF16, IMPLICIT>;
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_limit_once(kern, TcCfg<D>::SMEM, &done);
+    if (e != cudaSuccess) return e;
+    const int n_rt = (a.R + 127) / 128;
+    dim3 grid(a.nwg, n_rt * (D / TcCfg<D>::DV), a.Hk);
+    kern<<<grid, kTcThreads, TcCfg<D>::SMEM, s>>>(a, maps);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <bool BF16>
+cudaError_t launch_tc_typed(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
+    const bool imp = a.mask == nullptr;
+    switch (a.D) {
+        case 128: return imp ? launch_tc_one<128, BF16, true>(a, maps, s) : launch_tc_one<128, BF16, false>(a, maps, s);
+        case 256: return imp ? launch_tc_one<256, BF16, true>(a, maps, s) : launch_tc_one<256, BF16, false>(a, maps, s);
+        case 512: return imp ? launch_tc_one<512, BF16, true>(a, maps, s) : launch_tc_one<512, BF16, false>(a, maps, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s) {
+    if (kv_type == kKvF16) return launch_tc_typed<false>(a, maps, s);
+    if (kv_type == kKvBF16) return launch_tc_typed<true>(a, maps, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace ta
