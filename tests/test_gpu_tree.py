@@ -121,7 +121,19 @@ def test_large_logits_exercise_rescaling(ta, path):
     # comparison isolates the rescaling of O and S
     inp["q"] = torch.round(inp["q"] * 4.0) / 4.0
     got = run_tree(ta, wl, inp).cpu().numpy()
-    assert_close(got, oracle.tree_oracle_for(wl, inp))
+    ref = oracle.tree_oracle_for(wl, inp)
+    if path == 1:
+        assert_close(got, ref)
+    else:
+        # The tensor-core kernel feeds P to the PV product in the K/V type.  With
+        # unit roundoff u of that type, out = sum(P~ v) / sum(P~) with
+        # P~ = P (1 + e), |e| <= u, so |out - ref| <= u * max_j |v_j - ref|.  This
+        # peaked-softmax input is the worst case for it; the workloads meet the
+        # plain tolerance.
+        u = 2.0 ** -8
+        vmax = float(inp["v"][:, :wl.kv_seq_len].float().abs().max())
+        assert_close(got, ref, atol=2e-3 + u * 2 * vmax)
+        assert_close(got, ref, atol=2e-3 + u * 2 * vmax, rtol=1e-3)
 
 
 def test_device_error_word_stays_zero(ta):
