@@ -132,10 +132,14 @@ uint32_t resolve_tree_nwg(const ta_tree_params *p) {
     uint64_t nwg;
     if (R >= 16) {
         // tensor-core kernel: one CTA per SM, CTAs = splits x row tiles x O halves x KV heads
+        // and each split a run of whole 4-chunk key tiles (no split gets more tiles
+        // than needed to cover the keys with at most one CTA per SM)
         const uint64_t units = (uint64_t)p->n_kv_heads * ((R + 127) / 128) * (p->head_dim == 512 ? 2 : 1);
-        nwg = (uint64_t)sms / units;
-        const uint64_t max_splits = (n_chunks + 3) / 4;      // at least one 4-chunk tile each
-        if (nwg > max_splits) nwg = max_splits;
+        const uint64_t tiles = (n_chunks + 3) / 4;
+        uint64_t most = (uint64_t)sms / units;
+        if (most < 1) most = 1;
+        const uint64_t per_split = (tiles + most - 1) / most;
+        nwg = (tiles + per_split - 1) / per_split;
     } else {
         const uint64_t units = (uint64_t)p->n_kv_heads * ((R + kFmaRowsPerCta - 1) / kFmaRowsPerCta);
         nwg = (2ull * sms + units - 1) / units;

@@ -14,15 +14,16 @@
 
 namespace ta {
 
-// Prep pass, one launch: blocks [0, n_cls) classify the chunks, one warp per
-// chunk (dead if no (row, key < N) cell is attended (> -65504), all-attended if
-// every (row, key < N) cell equals 0.0, else mixed); the remaining blocks
-// write the 16-bit copy of Q for the tensor-core kernel; block 0 clears the
-// error word.
+// Prep pass, one launch: blocks [0, n_chunks) classify one 32-key chunk each
+// (dead if no (row, key < N) cell is attended (> -65504), all-attended if every
+// (row, key < N) cell equals 0.0, else mixed; lane = key, the L rows spread
+// over the 8 warps); the remaining blocks write the 16-bit copy of Q for the
+// tensor-core kernel; block 0 clears the error word.
 constexpr int kPrepThreads = 256;
 constexpr int kQ16PerBlock = kPrepThreads * 8;
 
 __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs a, int n_cls_blocks) {
+    pdl_launch_dependents();
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) *a.err = 0;
     if (static_cast<int>(blockIdx.x) >= n_cls_blocks) {
         // Q [H*L, D] f32 -> 16-bit (round to nearest), 8 elements per thread
@@ -46,25 +47,26 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs 
         *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.q16) + i8) = o;
         return;
     }
-    const int lane = threadIdx.x & 31;
-    const int chunk = blockIdx.x * (kPrepThreads / 32) + (threadIdx.x >> 5);
-    if (chunk >= a.n_chunks) return;
+    __shared__ int s_any[kPrepThreads / 32], s_all[kPrepThreads / 32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int chunk = blockIdx.x;
     const int key = chunk * 32 + lane;
     const bool valid = key < a.N;
     bool any_att = false, all_zero = true;
     if (valid) {
         if (a.mask != nullptr) {
             const float *col = a.mask + key;
-            for (int i = 0; i < a.L; ++i) {
-                float m = __ldg(col + (size_t)i * a.stride);
+#pragma unroll 4
+            for (int i = warp; i < a.L; i += kPrepThreads / 32) {
+                const float m = __ldg(col + static_cast<size_t>(i) * a.stride);
                 any_att |= m > kMasked;
                 all_zero &= m == 0.0f;
             }
         } else {
             // implicit causal: row i attends [window_start, N - L + i]
             const int last = a.N - a.L;            // row 0's last attended key
-            for (int i = 0; i < a.L; ++i) {
-                bool att = key >= a.window_start && key <= last + i;
+            for (int i = warp; i < a.L; i += kPrepThreads / 32) {
+                const bool att = key >= a.window_start && key <= last + i;
                 any_att |= att;
                 all_zero &= att;
             }
@@ -72,56 +74,91 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs 
     }
     any_att = __any_sync(0xffffffffu, any_att);
     all_zero = __all_sync(0xffffffffu, all_zero);
-    if (lane == 0) {
-        uint8_t cl = !any_att ? kChunkDead : (all_zero ? kChunkAllAttended : kChunkMixed);
-        a.cls[chunk] = cl;
+    if (lane == 0) { s_any[warp] = any_att; s_all[warp] = all_zero; }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        bool an = false, al = true;
+        for (int w = 0; w < kPrepThreads / 32; ++w) { an |= s_any[w] != 0; al &= s_all[w] != 0; }
+        a.cls[chunk] = !an ? kChunkDead : (al ? kChunkAllAttended : kChunkMixed);
     }
 }
 
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
-    const int n_cls = (a.n_chunks + kPrepThreads / 32 - 1) / (kPrepThreads / 32);
+    const int n_cls = a.n_chunks;
     int n_q = 0;
     if (a.q16_type >= 0) {
         const size_t total = static_cast<size_t>(a.H) * a.L * a.D;
         n_q = static_cast<int>((total + kQ16PerBlock - 1) / kQ16PerBlock);
     }
-    tree_prep_kernel<<<n_cls + n_q, kPrepThreads, 0, s>>>(a, n_cls);
+    cudaError_t e = launch_pdl(tree_prep_kernel, dim3(n_cls + n_q), dim3(kPrepThreads), 0, s, a, n_cls);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
-// One CTA per output row (rid = i * H + h), D/4 threads, float4 per thread.
+// Merge: one CTA per output row (rid = i * H + h).  M* and the per-split
+// weights e^(M_w - M*) are computed once per row into shared memory (128
+// splits at a time); every thread then accumulates its float4 of O over the
+// splits with independent loads.
 __global__ void __launch_bounds__(128) tree_reduce_kernel(const TreeArgs a) {
+    pdl_wait();
+    __shared__ float s_e[128], s_se[128];
+    __shared__ float s_red[2];
     const int rid = blockIdx.x;
     const int nrows = a.H * a.L;
-    const int t = threadIdx.x;              // float4 column
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int D4 = a.D / 4;
-    float mstar = -FLT_MAX;
-    for (int w = 0; w < a.nwg; ++w)
-        mstar = fmaxf(mstar, __ldg(a.part_ml + ((size_t)w * nrows + rid) * 2 + 1));
-    float sstar = 0.0f;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int w = 0; w < a.nwg; ++w) {
-        const float sw = __ldg(a.part_ml + ((size_t)w * nrows + rid) * 2 + 0);
-        const float mw = __ldg(a.part_ml + ((size_t)w * nrows + rid) * 2 + 1);
-        const float e = expf(mw - mstar);
-        sstar += sw * e;
-        if (t < D4) {
-            float4 o = __ldg(reinterpret_cast<const float4 *>(a.part_o + ((size_t)w * nrows + rid) * a.D) + t);
-            acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
-        }
+    const float *ml = a.part_ml + static_cast<size_t>(rid) * 2;
+    const size_t ml_stride = static_cast<size_t>(nrows) * 2;
+    if (warp == 0) {
+        float m = -FLT_MAX;
+        for (int w = lane; w < a.nwg; w += 32) m = fmaxf(m, __ldg(ml + w * ml_stride + 1));
+        m = warp_max(m);
+        if (lane == 0) s_red[0] = m;
     }
+    __syncthreads();
+    const float mstar = s_red[0];
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float ssum = 0.0f;
+    const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * t;
+    const size_t po_stride = static_cast<size_t>(nrows) * a.D;
+    for (int w0 = 0; w0 < a.nwg; w0 += 128) {
+        const int n = min(128, a.nwg - w0);
+        if (t < n) {
+            const float e = expf(__ldg(ml + (w0 + t) * ml_stride + 1) - mstar);
+            s_e[t] = e;
+            s_se[t] = __ldg(ml + (w0 + t) * ml_stride) * e;
+        }
+        __syncthreads();
+        if (t < D4) {
+#pragma unroll 4
+            for (int j = 0; j < n; ++j) {
+                const float4 o = __ldg(reinterpret_cast<const float4 *>(po + (w0 + j) * po_stride));
+                const float e = s_e[j];
+                acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
+            }
+        }
+        if (warp == 0)
+            for (int j = lane; j < n; j += 32) ssum += s_se[j];
+        __syncthreads();
+    }
+    if (warp == 0) {
+        ssum = warp_sum(ssum);
+        if (lane == 0) s_red[1] = ssum;
+    }
+    __syncthreads();
+    const float sstar = s_red[1];
     const float inv = (sstar == 0.0f) ? 0.0f : 1.0f / sstar;
     if (t < D4) {
-        float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        reinterpret_cast<float4 *>(a.out + (size_t)rid * a.D)[t] = r;
+        const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+        reinterpret_cast<float4 *>(a.out + static_cast<size_t>(rid) * a.D)[t] = r;
     }
 }
 
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s) {
-    dim3 grid(a.H * a.L);
-    tree_reduce_kernel<<<grid, a.D / 4, 0, s>>>(a);
+    cudaError_t e = launch_pdl(tree_reduce_kernel, dim3(a.H * a.L), dim3(128), 0, s, a);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@ __global__ void __launch_bounds__(kThreads) tree_fma_kernel(const TreeArgs a) {
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, r0 = blockIdx.y * kRB, kh = blockIdx.z;
+    pdl_wait();                                 // chunk classes are ready
 
     // Q rows of this group: global row kh * R + r0 + rr, r = j * L + i.
     for (int idx = tid; idx < kRB * (D / 4); idx += kThreads) {
@@ -225,8 +226,9 @@ cudaError_t launch_one(const TreeArgs &a, cudaStream_t s) {
     cudaError_t e = set_smem_limit_once(kern, smem, &done);
     if (e != cudaSuccess) return e;
     dim3 grid(a.nwg, (a.R + kRB - 1) / kRB, a.Hk);
-    kern<<<grid, kThreads, smem, s>>>(a);
+    e = launch_pdl(kern, grid, dim3(kThreads), smem, s, a);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -13,15 +13,16 @@
 //   warp 0     : TMA producer - the Q tile once, then K and V slabs
 //                ([128 keys x 64 cols] 16-bit, 128-byte swizzle) through a ring
 //                of 16 KB stages, in the order the MMA warp consumes them
-//                (K_0, K_1, V_0, K_2, V_1, ...).  A tile holds the next 4 live
-//                32-key chunks of the split; empty slots and keys past
+//                (K_0, K_1, V_0, K_2, V_1, ...).  A split owns a contiguous
+//                range of 32-key chunks; a tile holds its next 4 live chunks
+//                (dead chunks are never loaded); empty slots and keys past
 //                kv_seq_len are loaded out of bounds, i.e. as zeros.
 //   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
 //                TMEM, double buffered) and O += P_t V_t (M 128, N 64 per V slab,
 //                P from shared memory, V MN-major).
 //   warps 2..5 : one thread per row: mask + scale, online softmax with lazy
 //                rescaling (M only moves when a row max exceeds it by more
-//                than kRescaleSlack, so O in TMEM is rarely touched), P as
+//                than e^8, so O in TMEM is rarely touched), P as
 //                16-bit into swizzled shared memory, epilogue from TMEM.
 // Every mbarrier wait is bounded; on a timeout the CTA sets the workspace
 // error word, drains its outstanding copies and MMAs, frees TMEM and exits.
@@ -37,7 +38,9 @@ using namespace sm100;
 constexpr int kTcThreads = 192;
 constexpr int kSlab = 16384;                 // [128 rows][64 x 16-bit], 128-byte swizzled
 constexpr uint32_t kWaitIters = 1u << 22;
-constexpr float kRescaleSlack = 8.0f;        // P <= e^8 = 2981 fits f16 and bf16
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleSlack2 = 8.0f * kLog2e;   // in log2 units: P <= e^8 = 2981 fits f16 and bf16
 
 template <int D>
 struct TcCfg {
@@ -66,60 +69,62 @@ struct Bars {
     volatile int abort_flag;
 };
 
-// Walk of the live 32-key chunks [lo, hi) (in live order) of this split.
-// Warp-collective: all lanes hold the same state.
+// Walk of the live (not dead) 32-key chunks of the chunk-index range
+// [begin, end) of this split, in order.  Warp-collective: all lanes call it
+// together and hold the same state.
 struct ChunkWalk {
     const uint8_t *cls;
-    int n_chunks, base, left;
+    int base, end, my_cls;      // my_cls: class of chunk base + lane
     uint32_t pending;
 
-    __device__ void init(const uint8_t *c, int n, int lo, int hi) {
-        cls = c;
-        n_chunks = n;
-        left = hi > lo ? hi - lo : 0;
-        const int lane = threadIdx.x & 31;
-        int r = 0;
-        base = 0;
-        pending = 0;
-        while (base < n_chunks) {
-            const bool live = base + lane < n_chunks && cls[base + lane] != kChunkDead;
-            uint32_t m = __ballot_sync(0xffffffffu, live);
-            const int cnt = __popc(m);
-            if (r + cnt > lo) {
-                for (int skip = lo - r; skip > 0; --skip) m &= m - 1;
-                pending = m;
-                return;
-            }
-            r += cnt;
-            base += 32;
-        }
+    __device__ void load(int b) {
+        const int c = b + static_cast<int>(threadIdx.x & 31);
+        my_cls = c < end ? cls[c] : kChunkDead;
+        pending = __ballot_sync(0xffffffffu, my_cls != kChunkDead);
     }
-    // Next live chunk index, or -1 when the split's range is exhausted.
-    __device__ int next() {
-        if (left <= 0) return -1;
-        const int lane = threadIdx.x & 31;
+    __device__ void init(const uint8_t *c, int begin, int end_) {
+        cls = c;
+        base = begin;
+        end = end_;
+        pending = 0u;
+        my_cls = kChunkDead;
+        if (base < end) load(base);
+    }
+    // Next live chunk index (and its class), or -1 when the range is exhausted.
+    __device__ int next(int *cl) {
         while (pending == 0) {
             base += 32;
-            if (base >= n_chunks) { left = 0; return -1; }
-            pending = __ballot_sync(0xffffffffu, base + lane < n_chunks && cls[base + lane] != kChunkDead);
+            if (base >= end) return -1;
+            load(base);
         }
-        const int c = base + __ffs(pending) - 1;
+        const int bit = __ffs(pending) - 1;
         pending &= pending - 1;
-        --left;
-        return c;
+        *cl = __shfl_sync(0xffffffffu, my_cls, bit);
+        return base + bit;
     }
 };
 
-__device__ __forceinline__ int split_live_range(const uint8_t *cls, int n_chunks, int nwg, int split, int *lo,
-                                                int *hi) {
+// Chunk-index range of a split: whole 4-chunk tiles, ceil(tiles / nwg) each.
+__device__ __forceinline__ void split_range(int n_chunks, int nwg, int split, int *begin, int *end) {
+    const int tiles = (n_chunks + 3) / 4;
+    const int cps = ((tiles + nwg - 1) / nwg) * 4;
+    *begin = min(n_chunks, split * cps);
+    *end = min(n_chunks, *begin + cps);
+}
+
+// Number of 4-chunk key tiles of the split's live chunks (warp-collective).
+__device__ __forceinline__ int count_tiles(const uint8_t *cls, int begin, int end) {
     const int lane = threadIdx.x & 31;
-    int n_live = 0;
-    for (int b = 0; b < n_chunks; b += 32)
-        n_live += __popc(__ballot_sync(0xffffffffu, b + lane < n_chunks && cls[b + lane] != kChunkDead));
-    const int cps = (n_live + nwg - 1) / nwg;
-    *lo = min(n_live, split * cps);
-    *hi = min(n_live, *lo + cps);
-    return (*hi - *lo + 3) / 4;   // key tiles
+    int n = 0;
+    for (int b = begin; b < end; b += 32)
+        n += __popc(__ballot_sync(0xffffffffu, b + lane < end && cls[b + lane] != kChunkDead));
+    return (n + 3) / 4;
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ void note_abort(Bars *b, int *err, int code) {
@@ -190,18 +195,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    pdl_wait();                                         // chunk classes and Q copy are ready
     const uint32_t tmem = bars->tmem_base;
     const uint32_t tm_s[2] = {tmem, tmem + 128};
     const uint32_t tm_o = tmem + 256;
 
-    int lo, hi;
-    const int T = split_live_range(a.cls, a.n_chunks, a.nwg, split, &lo, &hi);
+    int c_begin, c_end;
+    split_range(a.n_chunks, a.nwg, split, &c_begin, &c_end);
+    const int T = count_tiles(a.cls, c_begin, c_end);
     const int n_pad = ((a.N + 31) / 32) * 32;          // a key row that is out of bounds
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
         ChunkWalk walk;
-        walk.init(a.cls, a.n_chunks, lo, hi);
+        walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads issued
         auto load_slabs = [&](const CUtensorMap *map, const int (&chunk)[4], int nslab, int x0) -> bool {
             for (int s = 0; s < nslab; ++s) {
@@ -233,13 +240,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 for (int s = 0; s < NSK; ++s)
                     tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
             }
-            int cur[4], nxt[4];
-            for (int c = 0; c < 4; ++c) nxt[c] = walk.next();
+            int cur[4], nxt[4], cl_unused;
+            for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
             ok = load_slabs(&maps.k, nxt, NSK, 0);
             for (int t = 0; t < T && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
                 if (t + 1 < T) {
-                    for (int c = 0; c < 4; ++c) nxt[c] = walk.next();
+                    for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
                     ok = load_slabs(&maps.k, nxt, NSK, 0);
                 }
                 if (ok) ok = load_slabs(&maps.v, cur, NSV, os * DV);
@@ -321,78 +328,97 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const float *mrow = IMPLICIT ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
 
         ChunkWalk walk;
-        walk.init(a.cls, a.n_chunks, lo, hi);
-        float m_run = -INFINITY, l_run = 0.0f;
+        walk.init(a.cls, c_begin, c_end);
+        float m_run = -INFINITY, l_run = 0.0f;          // running max in log2 units
         bool ok = true;
+        const float scale2 = a.scale * kLog2e;
         for (int t = 0; t < T && ok; ++t) {
-            int chunk[4];
-            for (int c = 0; c < 4; ++c) chunk[c] = walk.next();
+            int chunk[4], ccls[4];
+            for (int c = 0; c < 4; ++c) chunk[c] = walk.next(&ccls[c]);
+            // mask of the tile's first mixed chunk, fetched before waiting for S
+            int mixed = -1;
+            float mpre[32];
+            if (!IMPLICIT) {
+#pragma unroll
+                for (int c = 3; c >= 0; --c)
+                    if (chunk[c] >= 0 && ccls[c] == kChunkMixed) mixed = c;
+                if (mixed >= 0) {
+                    const int key0 = chunk[mixed] * 32;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) mpre[e] = key0 + e < a.N ? __ldg(mrow + key0 + e) : kMasked;
+                }
+            }
             const int sb = t & 1;
             ok = wait_or_abort(bars, &bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, err, 7);
             if (!ok) break;
             tc_fence_after();
             float s[128];
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                uint32_t rr[32];
-                tmem_ld32(tm_s[sb] + lane_off + c * 32, rr);
+            {
+                uint32_t r0[32], r1[32], r2[32], r3[32];
+                tmem_ld32(tm_s[sb] + lane_off + 0, r0);
+                tmem_ld32(tm_s[sb] + lane_off + 32, r1);
+                tmem_ld32(tm_s[sb] + lane_off + 64, r2);
+                tmem_ld32(tm_s[sb] + lane_off + 96, r3);
                 tmem_wait_ld();
 #pragma unroll
-                for (int e = 0; e < 32; ++e) s[c * 32 + e] = __uint_as_float(rr[e]);
+                for (int e = 0; e < 32; ++e) {
+                    s[e] = __uint_as_float(r0[e]);
+                    s[32 + e] = __uint_as_float(r1[e]);
+                    s[64 + e] = __uint_as_float(r2[e]);
+                    s[96 + e] = __uint_as_float(r3[e]);
+                }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-            // mask + scale per 32-key chunk
+            // logits in log2 units; the chunk class is warp-uniform
             float rmax = -INFINITY;
 #pragma unroll
             for (int c = 0; c < 4; ++c) {
+                float *sc = s + c * 32;
                 const int ch = chunk[c];
-                if (ch < 0) {
-#pragma unroll
-                    for (int e = 0; e < 32; ++e) s[c * 32 + e] = -INFINITY;
-                    continue;
-                }
                 const int key0 = ch * 32;
-                const int cl = a.cls[ch];
-                bool live = false;
-                float mv[32];
+                if (ch >= 0 && ccls[c] == kChunkAllAttended && key0 + 32 <= a.N) {
+                    // every cell attended: mask 0, logit = qk * scale
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int key = key0 + e;
-                    float v;
-                    if (key >= a.N) v = kMasked;
-                    else if (IMPLICIT) v = (key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
-                    else v = (cl == kChunkAllAttended) ? 0.0f : __ldg(mrow + key);
-                    mv[e] = v;
-                    live |= v > kMasked;
-                }
+                    for (int e = 0; e < 32; ++e) {
+                        sc[e] *= scale2;
+                        rmax = fmaxf(rmax, sc[e]);
+                    }
+                } else if (ch < 0) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const float lg = live ? fmaf(s[c * 32 + e], a.scale, mv[e]) : -INFINITY;
-                    s[c * 32 + e] = lg;
-                    rmax = fmaxf(rmax, lg);
+                    for (int e = 0; e < 32; ++e) sc[e] = -INFINITY;
+                } else {
+                    float mv[32];
+                    bool live = false;
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        const int key = key0 + e;
+                        float v;
+                        if (IMPLICIT) v = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
+                        else if (ccls[c] == kChunkAllAttended) v = key < a.N ? 0.0f : kMasked;
+                        else if (c == mixed) v = mpre[e];
+                        else v = key < a.N ? __ldg(mrow + key) : kMasked;
+                        mv[e] = v;
+                        live |= v > kMasked;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) {
+                        // logit = fma(qk, scale, mask) (the pages' form), in log2 units
+                        sc[e] = live ? fmaf(sc[e], a.scale, mv[e]) * kLog2e : -INFINITY;
+                        rmax = fmaxf(rmax, sc[e]);
+                    }
                 }
             }
             // online softmax with lazy rescaling
             float alpha = 1.0f;
-            if (rmax > m_run + kRescaleSlack) {
-                alpha = expf(m_run - rmax);             // 0 when m_run = -inf
+            if (rmax > m_run + kRescaleSlack2) {
+                alpha = fast_exp2(m_run - rmax);        // 0 when m_run = -inf
                 l_run *= alpha;
                 m_run = rmax;
             }
-            const bool row_live = m_run != -INFINITY;
-            uint32_t pk[64];
-            float psum = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 64; ++e) {
-                const float p0 = row_live ? expf(s[2 * e] - m_run) : 0.0f;
-                const float p1 = row_live ? expf(s[2 * e + 1] - m_run) : 0.0f;
-                pk[e] = pack2(p0, p1, BF16);
-                psum += lo16(pk[e], BF16) + hi16(pk[e], BF16);
-            }
-            l_run += psum;
+            const float m_use = m_run == -INFINITY ? 0.0f : m_run;   // dead row: all logits -inf, P = 0
 
             // PV of the previous tile done: P buffer free, O stable
             if (t > 0) {
@@ -412,14 +438,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     tmem_wait_st();
                 }
             }
-            // P row -> shared memory, K-major 128-byte swizzle: 16-byte unit u of
-            // row r is stored at unit u ^ (r % 8) within the row's 128 bytes.
+            // P = 2^(logit - M) rounded to the K/V type, 8 per 16-byte unit, into
+            // shared memory with the K-major 128-byte swizzle: unit u of row r
+            // goes to unit u ^ (r % 8) of the row's 128 bytes.  S sums the
+            // rounded values, the ones the tensor core multiplies.
+            float psum = 0.0f;
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const float p0 = fast_exp2(s[8 * u + 2 * k] - m_use);
+                    const float p1 = fast_exp2(s[8 * u + 2 * k + 1] - m_use);
+                    w[k] = pack2(p0, p1, BF16);
+                    psum += lo16(w[k], BF16) + hi16(w[k], BF16);
+                }
                 const int slab = u >> 3, cu = u & 7;
-                uint4 v4 = make_uint4(pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-                *reinterpret_cast<uint4 *>(sP + slab * kSlab + r * 128 + ((cu ^ (r & 7)) << 4)) = v4;
+                *reinterpret_cast<uint4 *>(sP + slab * kSlab + r * 128 + ((cu ^ (r & 7)) << 4)) =
+                    make_uint4(w[0], w[1], w[2], w[3]);
             }
+            l_run += psum;
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -430,6 +468,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             tc_fence_after();
         }
         // epilogue: partial (O, S, M) or, with one split, the normalized output
+        pdl_launch_dependents();
         const int nrows = a.H * a.L;
         const size_t rid = static_cast<size_t>(qi) * a.H + hj;
         const float inv = (l_run == 0.0f) ? 0.0f : 1.0f / l_run;
@@ -459,7 +498,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         }
         if (row_ok && a.nwg > 1 && os == 0) {
             a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 0] = l_run;
-            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 1] = m_run == -INFINITY ? kMInit : m_run;
+            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 1] =
+                m_run == -INFINITY ? kMInit : m_run * kLn2;   // natural-log units
         }
     }
 
@@ -480,8 +520,9 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
     if (e != cudaSuccess) return e;
     const int n_rt = (a.R + 127) / 128;
     dim3 grid(a.nwg, n_rt * (D / TcCfg<D>::DV), a.Hk);
-    kern<<<grid, kTcThreads, TcCfg<D>::SMEM, s>>>(a, maps);
+    e = launch_pdl(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, a, maps);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
