@@ -54,6 +54,7 @@ struct TcCfg {
     static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
     static constexpr int SMEM = 1024 + OFF_BAR + 512;
     static_assert(SMEM <= 232448, "shared memory budget");
+    static_assert(128 * (DV + 4) * 4 <= OFF_BAR, "epilogue staging fits below the barriers");
 };
 
 struct Bars {
@@ -177,9 +178,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
     const int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
+    // The CTAs of one (split, KV head) - all row tiles and O halves - form one
+    // cluster when launched as such: each K slab is loaded once for the whole
+    // cluster and each V slab once per O half, shares multicast to the CTAs
+    // that use them, so every K/V byte crosses L2 -> SM once.
+    const int cs = static_cast<int>(cluster_nctarank());
+    const int crank = static_cast<int>(cluster_ctarank());
+    const int k_share = cs, k_idx = crank;             // K: all CTAs of the cluster
+    const int v_share = cs > 1 ? n_rt : 1, v_idx = cs > 1 ? rt : 0;   // V: CTAs of this O half
+    const uint16_t k_mask = static_cast<uint16_t>((1u << cs) - 1u);
+    uint16_t v_mask = 0;
+    for (int r2 = 0; r2 < n_rt; ++r2) v_mask |= static_cast<uint16_t>(1u << (r2 * n_os + os));
 
     if (tid == 0) {
-        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], 1); }
+        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cs); }
         mbar_init(&bars->q_full, 1);
         for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 4); }
         mbar_init(&bars->p_full, 4);
@@ -193,7 +205,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         tmem_relinquish();
     }
     tc_fence_before();
-    __syncthreads();
+    cluster_sync();                                     // peers' mbarriers exist before any multicast
     tc_fence_after();
     pdl_wait();                                         // chunk classes and Q copy are ready
     const uint32_t tmem = bars->tmem_base;
@@ -210,7 +222,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads issued
-        auto load_slabs = [&](const CUtensorMap *map, const int (&chunk)[4], int nslab, int x0) -> bool {
+        auto load_slabs = [&](const CUtensorMap *map, const int (&chunk)[4], int nslab, int x0, int share,
+                              int share_idx, uint16_t mask) -> bool {
             for (int s = 0; s < nslab; ++s) {
                 const int slot = issued % ST;
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
@@ -220,9 +233,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     if (ok) {
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
                         unsigned char *dst = sRing + slot * kSlab;
-                        for (int c = 0; c < 4; ++c)
-                            tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64,
-                                        chunk[c] >= 0 ? chunk[c] * 32 : n_pad, kh);
+                        for (int c = share_idx; c < 4; c += share) {
+                            const int y = chunk[c] >= 0 ? chunk[c] * 32 : n_pad;
+                            if (share > 1)
+                                tma_load_3d_mc(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh, mask);
+                            else
+                                tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
+                        }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -242,22 +259,27 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             }
             int cur[4], nxt[4], cl_unused;
             for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-            ok = load_slabs(&maps.k, nxt, NSK, 0);
+            ok = load_slabs(&maps.k, nxt, NSK, 0, k_share, k_idx, k_mask);
             for (int t = 0; t < T && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
                 if (t + 1 < T) {
                     for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-                    ok = load_slabs(&maps.k, nxt, NSK, 0);
+                    ok = load_slabs(&maps.k, nxt, NSK, 0, k_share, k_idx, k_mask);
                 }
-                if (ok) ok = load_slabs(&maps.v, cur, NSV, os * DV);
+                if (ok) ok = load_slabs(&maps.v, cur, NSV, os * DV, v_share, v_idx, v_mask);
             }
-            // Drain: every copy issued into the ring has landed before exit.
+            // Drain: every copy into this CTA's ring has landed, and every CTA
+            // of the cluster has released the last use of each slot, so no
+            // peer copy or release still targets this CTA's shared memory.
             if (lane == 0) {
                 if (!mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9);
                 const int first = issued > ST ? issued - ST : 0;
-                for (int n = first; n < issued; ++n)
+                for (int n = first; n < issued; ++n) {
                     if (!mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
                         note_abort(bars, err, 9);
+                    if (!mbar_wait(&bars->empty[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
+                        note_abort(bars, err, 9);
+                }
             }
         }
     } else if (warp == 1) {
@@ -267,6 +289,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             constexpr uint32_t id_pv = idesc_f16(128, 64, BF16 ? 1 : 0, 0, 1);
             const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), ring_addr = smem_u32(sRing);
             int used = 0;                                   // ring loads consumed
+            // a slot is free once every CTA of the cluster has consumed it
+            auto release = [&](int slot) {
+                if (cs > 1) mma_commit_mc(&bars->empty[slot], k_mask);
+                else mma_commit(&bars->empty[slot]);
+            };
             bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2);
             auto issue_s = [&](int t) -> bool {
                 const int sb = t & 1;
@@ -283,7 +310,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     for (int kk = 0; kk < 4; ++kk)
                         mma_f16_ss(tm_s[sb], sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024),
                                    sw128_desc(kb + kk * 32, 16, 1024), id_qk, (s | kk) != 0);
-                    mma_commit(&bars->empty[slot]);
+                    release(slot);
                     ++used;
                 }
                 mma_commit(&bars->s_full[sb]);
@@ -306,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     for (int kk = 0; kk < 8; ++kk)
                         mma_f16_ss(tm_o + s * 64, sw128_desc(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
                                    sw128_desc(vb + kk * 2048, kSlab, 1024), id_pv, (t | kk) != 0);
-                    mma_commit(&bars->empty[slot]);
+                    release(slot);
                     ++used;
                 }
                 mma_commit(&bars->o_done);
@@ -381,11 +408,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 const int key0 = ch * 32;
                 if (ch >= 0 && ccls[c] == kChunkAllAttended && key0 + 32 <= a.N) {
                     // every cell attended: mask 0, logit = qk * scale
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         sc[e] *= scale2;
-                        rmax = fmaxf(rmax, sc[e]);
+                        m4[e & 3] = fmaxf(m4[e & 3], sc[e]);
                     }
+                    rmax = fmaxf(rmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 } else if (ch < 0) {
 #pragma unroll
                     for (int e = 0; e < 32; ++e) sc[e] = -INFINITY;
@@ -403,12 +432,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         mv[e] = v;
                         live |= v > kMasked;
                     }
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         // logit = fma(qk, scale, mask) (the pages' form), in log2 units
                         sc[e] = live ? fmaf(sc[e], a.scale, mv[e]) * kLog2e : -INFINITY;
-                        rmax = fmaxf(rmax, sc[e]);
+                        m4[e & 3] = fmaxf(m4[e & 3], sc[e]);
                     }
+                    rmax = fmaxf(rmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 }
             }
             // online softmax with lazy rescaling
@@ -442,7 +473,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             // shared memory with the K-major 128-byte swizzle: unit u of row r
             // goes to unit u ^ (r % 8) of the row's 128 bytes.  S sums the
             // rounded values, the ones the tensor core multiplies.
-            float psum = 0.0f;
+            float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 uint32_t w[4];
@@ -451,13 +482,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     const float p0 = fast_exp2(s[8 * u + 2 * k] - m_use);
                     const float p1 = fast_exp2(s[8 * u + 2 * k + 1] - m_use);
                     w[k] = pack2(p0, p1, BF16);
-                    psum += lo16(w[k], BF16) + hi16(w[k], BF16);
+                    ps[2 * k] += lo16(w[k], BF16);
+                    ps[2 * k + 1] += hi16(w[k], BF16);
                 }
                 const int slab = u >> 3, cu = u & 7;
                 *reinterpret_cast<uint4 *>(sP + slab * kSlab + r * 128 + ((cu ^ (r & 7)) << 4)) =
                     make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l_run += psum;
+            l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
@@ -472,10 +504,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int nrows = a.H * a.L;
         const size_t rid = static_cast<size_t>(qi) * a.H + hj;
         const float inv = (l_run == 0.0f) ? 0.0f : 1.0f / l_run;
-        float *dst = (a.nwg == 1) ? a.out + rid * D + os * DV
-                                  : a.part_o + (static_cast<size_t>(split) * nrows + rid) * D + os * DV;
         const float scale_out = (a.nwg == 1) ? inv : 1.0f;
         const bool have_o = ok && T > 0;
+        // Stage the tile's O rows in shared memory (free once the last MMA is
+        // done; rows padded by 16 bytes), then store them row by row with the
+        // whole warp, so each global store instruction writes 512 contiguous bytes.
+        constexpr int SROW = DV + 4;
+        float *stage = reinterpret_cast<float *>(sm);
 #pragma unroll 1
         for (int c = 0; c < DV / 32; ++c) {
             uint32_t rr[32];
@@ -486,15 +521,20 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 #pragma unroll
                 for (int e = 0; e < 32; ++e) rr[e] = 0u;
             }
-            if (row_ok) {
 #pragma unroll
-                for (int e = 0; e < 32; e += 4) {
-                    float4 v = make_float4(__uint_as_float(rr[e]) * scale_out, __uint_as_float(rr[e + 1]) * scale_out,
-                                           __uint_as_float(rr[e + 2]) * scale_out,
-                                           __uint_as_float(rr[e + 3]) * scale_out);
-                    *reinterpret_cast<float4 *>(dst + c * 32 + e) = v;
-                }
-            }
+            for (int e = 0; e < 32; e += 4)
+                *reinterpret_cast<float4 *>(stage + r * SROW + c * 32 + e) =
+                    make_float4(__uint_as_float(rr[e]) * scale_out, __uint_as_float(rr[e + 1]) * scale_out,
+                                __uint_as_float(rr[e + 2]) * scale_out, __uint_as_float(rr[e + 3]) * scale_out);
+        }
+        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
+        for (int rr = warp - 2; rr < rows_here; rr += 4) {
+            const int rg2 = rt * RT + rr;
+            const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
+            float *dst = (a.nwg == 1) ? a.out + rid2 * D + os * DV
+                                      : a.part_o + (static_cast<size_t>(split) * nrows + rid2) * D + os * DV;
+            for (int c4 = lane; c4 < DV / 4; c4 += 32)
+                *reinterpret_cast<float4 *>(dst + 4 * c4) = *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
         }
         if (row_ok && a.nwg > 1 && os == 0) {
             a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 0] = l_run;
@@ -505,6 +545,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -519,8 +560,9 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
     cudaError_t e = set_smem_limit_once(kern, TcCfg<D>::SMEM, &done);
     if (e != cudaSuccess) return e;
     const int n_rt = (a.R + 127) / 128;
-    dim3 grid(a.nwg, n_rt * (D / TcCfg<D>::DV), a.Hk);
-    e = launch_pdl(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, a, maps);
+    const unsigned gy = static_cast<unsigned>(n_rt * (D / TcCfg<D>::DV));
+    dim3 grid(a.nwg, gy, a.Hk);
+    e = launch_pdl_cluster(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, gy <= 8 ? gy : 1u, a, maps);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
