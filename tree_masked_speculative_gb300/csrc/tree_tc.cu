@@ -35,7 +35,7 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 192;
+constexpr int kTcThreads = 320;               // producer, MMA issuer, 8 softmax warps
 constexpr int kSlab = 16384;                 // [128 rows][64 x 16-bit], 128-byte swizzled
 constexpr uint32_t kWaitIters = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -52,7 +52,7 @@ struct TcCfg {
     static constexpr int OFF_P = OFF_Q + NSK * kSlab;
     static constexpr int OFF_RING = OFF_P + 2 * kSlab;
     static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
-    static constexpr int SMEM = 1024 + OFF_BAR + 512;
+    static constexpr int SMEM = OFF_BAR + 3072;      // the dynamic base must be 1024-aligned
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(128 * (DV + 4) * 4 <= OFF_BAR, "epilogue staging fits below the barriers");
 };
@@ -68,7 +68,9 @@ struct Bars {
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
+    float xrow[2][2][128];   // per-row values exchanged by the two warps of a TMEM quarter
 };
+static_assert(sizeof(Bars) <= 3072, "barrier area");
 
 // Walk of the live (not dead) 32-key chunks of the chunk-index range
 // [begin, end) of this split, in order.  Warp-collective: all lanes call it
@@ -161,9 +163,15 @@ template <int D, bool BF16, bool IMPLICIT>
 __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a, const __grid_constant__ TcMaps maps) {
     using Cfg = TcCfg<D>;
     constexpr int DV = Cfg::DV, NSK = Cfg::NSK, NSV = Cfg::NSV, ST = Cfg::STAGES;
-    extern __shared__ unsigned char smem_raw[];
-    unsigned char *sm = reinterpret_cast<unsigned char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                                          ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    // 128-byte-swizzled TMA / MMA tiles need a 1024-byte-aligned base; every
+    // CTA has the same base, so a misaligned one stops all of them before any
+    // barrier or allocation.
+    if ((smem_u32(smem_raw) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicCAS(a.err, 0, 11);
+        return;
+    }
+    unsigned char *sm = smem_raw;
     unsigned char *sQ = sm + Cfg::OFF_Q;
     unsigned char *sP = sm + Cfg::OFF_P;
     unsigned char *sRing = sm + Cfg::OFF_RING;
@@ -193,8 +201,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cs); }
         mbar_init(&bars->q_full, 1);
-        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 4); }
-        mbar_init(&bars->p_full, 4);
+        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 8); }
+        mbar_init(&bars->p_full, 8);
         mbar_init(&bars->o_done, 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
@@ -344,7 +352,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         }
     } else {
         // ---------------------------------------------- softmax and epilogue
-        const int quarter = warp & 3;                   // TMEM lanes 32*quarter .. +31
+        // Eight warps: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and owns
+        // one 64-key half of each tile (chunks 2*half, 2*half+1) and one half of
+        // the O columns; the two warps of a quarter combine row maxima and sums
+        // through shared memory with a 64-thread named barrier.
+        const int sw = warp - 2;
+        const int half = sw >> 2;
+        const int quarter = warp & 3;
         const int r = quarter * 32 + lane;              // row within the tile
         const int rg = rt * RT + r;                     // row within the KV group
         const bool row_ok = r < rows_here;
@@ -353,182 +367,193 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int last0 = a.N - a.L;
         const float *mrow = IMPLICIT ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
+        constexpr int DVH = DV / 2;                     // O columns of this warp
+        auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
 
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
-        float m_run = -INFINITY, l_run = 0.0f;          // running max in log2 units
+        float m_run = -INFINITY, l_half = 0.0f;         // running max (log2 units), this half's sum
         bool ok = true;
         const float scale2 = a.scale * kLog2e;
-        for (int t = 0; t < T && ok; ++t) {
+        // A wait's outcome is made warp-uniform (TMEM loads/stores are warp-
+        // collective), and the named barriers run in every iteration even after
+        // a failed wait, so no softmax warp can be left at a barrier.
+        auto wait_all = [&](uint64_t *bar, uint32_t parity, int code) -> bool {
+            const bool w = ok && wait_or_abort(bars, bar, parity, err, code);
+            return __all_sync(0xffffffffu, w);
+        };
+        for (int t = 0; t < T; ++t) {
             int chunk[4], ccls[4];
             for (int c = 0; c < 4; ++c) chunk[c] = walk.next(&ccls[c]);
-            // mask of the tile's first mixed chunk, fetched before waiting for S
+            const int ch0 = half ? chunk[2] : chunk[0], ch1 = half ? chunk[3] : chunk[1];
+            const int cl0 = half ? ccls[2] : ccls[0], cl1 = half ? ccls[3] : ccls[1];
+            // mask of this half's first mixed chunk, fetched before waiting for S
             int mixed = -1;
             float mpre[32];
             if (!IMPLICIT) {
-#pragma unroll
-                for (int c = 3; c >= 0; --c)
-                    if (chunk[c] >= 0 && ccls[c] == kChunkMixed) mixed = c;
+                mixed = (ch0 >= 0 && cl0 == kChunkMixed) ? 0 : ((ch1 >= 0 && cl1 == kChunkMixed) ? 1 : -1);
                 if (mixed >= 0) {
-                    const int key0 = chunk[mixed] * 32;
+                    const int key0 = (mixed ? ch1 : ch0) * 32;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) mpre[e] = key0 + e < a.N ? __ldg(mrow + key0 + e) : kMasked;
                 }
             }
             const int sb = t & 1;
-            ok = wait_or_abort(bars, &bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, err, 7);
-            if (!ok) break;
+            ok = wait_all(&bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, 7);
             tc_fence_after();
-            float s[128];
-            {
-                uint32_t r0[32], r1[32], r2[32], r3[32];
-                tmem_ld32(tm_s[sb] + lane_off + 0, r0);
-                tmem_ld32(tm_s[sb] + lane_off + 32, r1);
-                tmem_ld32(tm_s[sb] + lane_off + 64, r2);
-                tmem_ld32(tm_s[sb] + lane_off + 96, r3);
-                tmem_wait_ld();
-#pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    s[e] = __uint_as_float(r0[e]);
-                    s[32 + e] = __uint_as_float(r1[e]);
-                    s[64 + e] = __uint_as_float(r2[e]);
-                    s[96 + e] = __uint_as_float(r3[e]);
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->s_free[sb]);
 
-            // logits in log2 units; the chunk class is warp-uniform
-            float rmax = -INFINITY;
-#pragma unroll
-            for (int c = 0; c < 4; ++c) {
-                float *sc = s + c * 32;
-                const int ch = chunk[c];
+            // pass 1: logits (log2 units) of this half's two chunks, written back
+            // over S in TMEM, and their row maximum
+            float pmax = -INFINITY;
+#pragma unroll 1
+            for (int cc = 0; cc < (ok ? 2 : 0); ++cc) {
+                const int ch = cc ? ch1 : ch0, ccl = cc ? cl1 : cl0;
+                const uint32_t col = tm_s[sb] + lane_off + (2 * half + cc) * 32;
+                uint32_t v[32];
+                tmem_ld32(col, v);
+                tmem_wait_ld();
                 const int key0 = ch * 32;
-                if (ch >= 0 && ccls[c] == kChunkAllAttended && key0 + 32 <= a.N) {
+                float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+                if (ch >= 0 && ccl == kChunkAllAttended && key0 + 32 <= a.N) {
                     // every cell attended: mask 0, logit = qk * scale
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
-                        sc[e] *= scale2;
-                        m4[e & 3] = fmaxf(m4[e & 3], sc[e]);
+                        const float lg = __uint_as_float(v[e]) * scale2;
+                        m4[e & 3] = fmaxf(m4[e & 3], lg);
+                        v[e] = __float_as_uint(lg);
                     }
-                    rmax = fmaxf(rmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 } else if (ch < 0) {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) sc[e] = -INFINITY;
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(-INFINITY);
                 } else {
                     float mv[32];
                     bool live = false;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int key = key0 + e;
-                        float v;
-                        if (IMPLICIT) v = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
-                        else if (ccls[c] == kChunkAllAttended) v = key < a.N ? 0.0f : kMasked;
-                        else if (c == mixed) v = mpre[e];
-                        else v = key < a.N ? __ldg(mrow + key) : kMasked;
-                        mv[e] = v;
-                        live |= v > kMasked;
+                        float x;
+                        if (IMPLICIT) x = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
+                        else if (ccl == kChunkAllAttended) x = key < a.N ? 0.0f : kMasked;
+                        else if (cc == mixed) x = mpre[e];
+                        else x = key < a.N ? __ldg(mrow + key) : kMasked;
+                        mv[e] = x;
+                        live |= x > kMasked;
                     }
-                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         // logit = fma(qk, scale, mask) (the pages' form), in log2 units
-                        sc[e] = live ? fmaf(sc[e], a.scale, mv[e]) * kLog2e : -INFINITY;
-                        m4[e & 3] = fmaxf(m4[e & 3], sc[e]);
+                        const float lg = live ? fmaf(__uint_as_float(v[e]), a.scale, mv[e]) * kLog2e : -INFINITY;
+                        m4[e & 3] = fmaxf(m4[e & 3], lg);
+                        v[e] = __float_as_uint(lg);
                     }
-                    rmax = fmaxf(rmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
                 }
+                pmax = fmaxf(pmax, fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])));
+                tmem_st32(col, v);
             }
-            // online softmax with lazy rescaling
+            tmem_wait_st();
+            bars->xrow[t & 1][half][r] = pmax;
+            pair_sync();
+            const float rmax = fmaxf(pmax, bars->xrow[t & 1][half ^ 1][r]);
+
+            // online softmax with lazy rescaling (same decision in both halves)
             float alpha = 1.0f;
             if (rmax > m_run + kRescaleSlack2) {
                 alpha = fast_exp2(m_run - rmax);        // 0 when m_run = -inf
-                l_run *= alpha;
+                l_half *= alpha;
                 m_run = rmax;
             }
             const float m_use = m_run == -INFINITY ? 0.0f : m_run;   // dead row: all logits -inf, P = 0
 
             // PV of the previous tile done: P buffer free, O stable
             if (t > 0) {
-                ok = wait_or_abort(bars, &bars->o_done, static_cast<uint32_t>(t - 1) & 1u, err, 8);
-                if (!ok) break;
+                ok = wait_all(&bars->o_done, static_cast<uint32_t>(t - 1) & 1u, 8);
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (ok && __any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-                    for (int c = 0; c < DV / 32; ++c) {
+                    for (int c = 0; c < DVH / 32; ++c) {
                         uint32_t rr[32];
-                        tmem_ld32(tm_o + lane_off + c * 32, rr);
+                        const uint32_t col = tm_o + lane_off + half * DVH + c * 32;
+                        tmem_ld32(col, rr);
                         tmem_wait_ld();
 #pragma unroll
                         for (int e = 0; e < 32; ++e) rr[e] = __float_as_uint(__uint_as_float(rr[e]) * alpha);
-                        tmem_st32(tm_o + lane_off + c * 32, rr);
+                        tmem_st32(col, rr);
                     }
                     tmem_wait_st();
                 }
             }
-            // P = 2^(logit - M) rounded to the K/V type, 8 per 16-byte unit, into
-            // shared memory with the K-major 128-byte swizzle: unit u of row r
-            // goes to unit u ^ (r % 8) of the row's 128 bytes.  S sums the
-            // rounded values, the ones the tensor core multiplies.
+            // pass 2: P = 2^(logit - M) rounded to the K/V type into shared memory
+            // (K-major, 128-byte swizzle: 16-byte unit u of row r sits at unit
+            // u ^ (r % 8) of the row's 128 bytes; keys 64*half.. are slab `half`).
+            // The row sum adds the rounded values, the ones the tensor core uses.
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                uint32_t w[4];
+            unsigned char *prow = sP + half * kSlab + r * 128;
+#pragma unroll 1
+            for (int cc = 0; cc < (ok ? 2 : 0); ++cc) {
+                uint32_t v[32];
+                tmem_ld32(tm_s[sb] + lane_off + (2 * half + cc) * 32, v);
+                tmem_wait_ld();
 #pragma unroll
                 for (int k = 0; k < 4; ++k) {
-                    const float p0 = fast_exp2(s[8 * u + 2 * k] - m_use);
-                    const float p1 = fast_exp2(s[8 * u + 2 * k + 1] - m_use);
-                    w[k] = pack2(p0, p1, BF16);
-                    ps[2 * k] += lo16(w[k], BF16);
-                    ps[2 * k + 1] += hi16(w[k], BF16);
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const float p0 = fast_exp2(__uint_as_float(v[8 * k + 2 * j]) - m_use);
+                        const float p1 = fast_exp2(__uint_as_float(v[8 * k + 2 * j + 1]) - m_use);
+                        w[j] = pack2(p0, p1, BF16);
+                        ps[2 * j] += lo16(w[j], BF16);
+                        ps[2 * j + 1] += hi16(w[j], BF16);
+                    }
+                    const int u = cc * 4 + k;
+                    *reinterpret_cast<uint4 *>(prow + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
                 }
-                const int slab = u >> 3, cu = u & 7;
-                *reinterpret_cast<uint4 *>(sP + slab * kSlab + r * 128 + ((cu ^ (r & 7)) << 4)) =
-                    make_uint4(w[0], w[1], w[2], w[3]);
             }
-            l_run += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
+            l_half += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->p_full);
+            if (lane == 0 && ok) {
+                mbar_arrive(&bars->s_free[sb]);
+                mbar_arrive(&bars->p_full);
+            }
         }
-        if (ok && T > 0) {
-            ok = wait_or_abort(bars, &bars->o_done, static_cast<uint32_t>(T - 1) & 1u, err, 8);
+        if (T > 0) {
+            ok = wait_all(&bars->o_done, static_cast<uint32_t>(T - 1) & 1u, 8);
             tc_fence_after();
         }
-        // epilogue: partial (O, S, M) or, with one split, the normalized output
+        // epilogue: row sum of both halves, O rows staged in shared memory (free
+        // once the last MMA is done; rows padded by 16 bytes), then stored row by
+        // row with whole warps (512 contiguous bytes per store instruction)
         pdl_launch_dependents();
+        bars->xrow[T & 1][half][r] = l_half;
+        pair_sync();
+        const float l_run = l_half + bars->xrow[T & 1][half ^ 1][r];
         const int nrows = a.H * a.L;
         const size_t rid = static_cast<size_t>(qi) * a.H + hj;
         const float inv = (l_run == 0.0f) ? 0.0f : 1.0f / l_run;
         const float scale_out = (a.nwg == 1) ? inv : 1.0f;
         const bool have_o = ok && T > 0;
-        // Stage the tile's O rows in shared memory (free once the last MMA is
-        // done; rows padded by 16 bytes), then store them row by row with the
-        // whole warp, so each global store instruction writes 512 contiguous bytes.
         constexpr int SROW = DV + 4;
         float *stage = reinterpret_cast<float *>(sm);
 #pragma unroll 1
-        for (int c = 0; c < DV / 32; ++c) {
+        for (int c = 0; c < DVH / 32; ++c) {
             uint32_t rr[32];
             if (have_o) {
-                tmem_ld32(tm_o + lane_off + c * 32, rr);
+                tmem_ld32(tm_o + lane_off + half * DVH + c * 32, rr);
                 tmem_wait_ld();
             } else {
 #pragma unroll
                 for (int e = 0; e < 32; ++e) rr[e] = 0u;
             }
+            float *srow = stage + r * SROW + half * DVH + c * 32;
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
-                *reinterpret_cast<float4 *>(stage + r * SROW + c * 32 + e) =
+                *reinterpret_cast<float4 *>(srow + e) =
                     make_float4(__uint_as_float(rr[e]) * scale_out, __uint_as_float(rr[e + 1]) * scale_out,
                                 __uint_as_float(rr[e + 2]) * scale_out, __uint_as_float(rr[e + 3]) * scale_out);
         }
-        asm volatile("bar.sync 1, 128;" ::: "memory");  // the four softmax warps
-        for (int rr = warp - 2; rr < rows_here; rr += 4) {
+        asm volatile("bar.sync 5, 256;" ::: "memory");  // the eight softmax warps
+        for (int rr = sw; rr < rows_here; rr += 8) {
             const int rg2 = rt * RT + rr;
             const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
             float *dst = (a.nwg == 1) ? a.out + rid2 * D + os * DV
@@ -536,7 +561,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             for (int c4 = lane; c4 < DV / 4; c4 += 32)
                 *reinterpret_cast<float4 *>(dst + 4 * c4) = *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
         }
-        if (row_ok && a.nwg > 1 && os == 0) {
+        if (row_ok && half == 0 && a.nwg > 1 && os == 0) {
             a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 0] = l_run;
             a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 1] =
                 m_run == -INFINITY ? kMInit : m_run * kLn2;   // natural-log units
