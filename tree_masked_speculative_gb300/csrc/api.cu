@@ -299,6 +299,14 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     const int path = g_tree_path.load(std::memory_order_relaxed);
     plan->use_tc = path != 1 && plan->kv_type != kKvF32 && a.R >= 16;
     a.q16_type = plan->use_tc ? plan->kv_type : -1;
+    // partial slots left for the merge pass (0 = the main pass writes the output)
+    a.cluster_x = 1;
+    if (plan->use_tc) {
+        int cx, cy;
+        tree_tc_cluster_shape(a, &cx, &cy);
+        a.cluster_x = cx;
+    }
+    a.n_part = a.nwg / a.cluster_x == 1 ? 0 : a.nwg / a.cluster_x;
     if (plan->use_tc && !get_encoder())
         return fail(TA_ERR_CUDA, "tree_attention: cuTensorMapEncodeTiled is not available");
     return TA_OK;
@@ -462,6 +470,7 @@ TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp_
     char *t = static_cast<char *>(tmp.ptr);
     a.part_o = reinterpret_cast<float *>(t + ws.off_part_o);
     a.part_ml = reinterpret_cast<float *>(t + ws.off_part_ml);
+    a.err = reinterpret_cast<int *>(t + ws.off_err);   // [1]: partial count the main pass left
     a.out = static_cast<float *>(out.ptr);
     a.H = (int)p->n_heads;
     a.L = (int)p->q_l;

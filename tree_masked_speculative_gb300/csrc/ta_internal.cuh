@@ -91,6 +91,8 @@ struct TreeArgs {
     int *err;              // workspace error word (0 = ok), zeroed by the prep pass
     int H, Hk, D, N, C, L, stride, nwg, g, R, n_chunks, window_start;
     int q16_type;          // -1: no 16-bit Q copy, else kKvF16 / kKvBF16
+    int n_part;            // partial slots the main pass leaves for the merge (0 = output final)
+    int cluster_x;         // tensor-core kernel: splits merged inside one cluster
     float scale;
 };
 
@@ -126,6 +128,9 @@ struct TreeWorkspace {
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
 cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s);
+// Cluster shape of the tensor-core kernel: x = splits merged in-cluster, y = the
+// row tiles and O halves that share K/V through multicast.
+void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_quant_fma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s);
@@ -154,10 +159,10 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 
-// As launch_pdl, as clusters of cluster_y CTAs along y (1 = no cluster).
+// As launch_pdl, as clusters of cluster_x x cluster_y CTAs (1 x 1 = no cluster).
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                               unsigned cluster_y, Args &&...args) {
+                               unsigned cluster_x, unsigned cluster_y, Args &&...args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -167,11 +172,11 @@ cudaError_t launch_pdl_cluster(void (*kern)(KArgs...), dim3 grid, dim3 block, si
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 1;
+    attr[1].val.clusterDim.x = cluster_x;
     attr[1].val.clusterDim.y = cluster_y;
     attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = cluster_y > 1 ? 2 : 1;
+    cfg.numAttrs = cluster_x * cluster_y > 1 ? 2 : 1;
     return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
 }
 

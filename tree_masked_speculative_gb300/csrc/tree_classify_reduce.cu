@@ -24,7 +24,10 @@ constexpr int kQ16PerBlock = kPrepThreads * 8;
 
 __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs a, int n_cls_blocks) {
     pdl_launch_dependents();
-    if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) *a.err = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) {
+        a.err[0] = 0;          // error word
+        a.err[1] = a.n_part;   // partial slots the main pass leaves for the merge
+    }
     if (static_cast<int>(blockIdx.x) >= n_cls_blocks) {
         // Q [H*L, D] f32 -> 16-bit (round to nearest), 8 elements per thread
         const size_t total = static_cast<size_t>(a.H) * a.L * a.D;
@@ -96,12 +99,15 @@ cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// Merge: one CTA per output row (rid = i * H + h).  M* and the per-split
+// Merge: one CTA per output row (rid = i * H + h) over the partial slots the
+// main pass left (workspace header; 0 = the output is already final).  M* and the per-split
 // weights e^(M_w - M*) are computed once per row into shared memory (128
 // splits at a time); every thread then accumulates its float4 of O over the
 // splits with independent loads.
 __global__ void __launch_bounds__(128) tree_reduce_kernel(const TreeArgs a) {
     pdl_wait();
+    const int nwg = a.err[1];
+    if (nwg <= 0) return;
     __shared__ float s_e[128], s_se[128];
     __shared__ float s_red[2];
     const int rid = blockIdx.x;
@@ -112,7 +118,7 @@ __global__ void __launch_bounds__(128) tree_reduce_kernel(const TreeArgs a) {
     const size_t ml_stride = static_cast<size_t>(nrows) * 2;
     if (warp == 0) {
         float m = -FLT_MAX;
-        for (int w = lane; w < a.nwg; w += 32) m = fmaxf(m, __ldg(ml + w * ml_stride + 1));
+        for (int w = lane; w < nwg; w += 32) m = fmaxf(m, __ldg(ml + w * ml_stride + 1));
         m = warp_max(m);
         if (lane == 0) s_red[0] = m;
     }
@@ -122,8 +128,8 @@ __global__ void __launch_bounds__(128) tree_reduce_kernel(const TreeArgs a) {
     float ssum = 0.0f;
     const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * t;
     const size_t po_stride = static_cast<size_t>(nrows) * a.D;
-    for (int w0 = 0; w0 < a.nwg; w0 += 128) {
-        const int n = min(128, a.nwg - w0);
+    for (int w0 = 0; w0 < nwg; w0 += 128) {
+        const int n = min(128, nwg - w0);
         if (t < n) {
             const float e = expf(__ldg(ml + (w0 + t) * ml_stride + 1) - mstar);
             s_e[t] = e;

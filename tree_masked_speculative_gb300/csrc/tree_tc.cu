@@ -54,7 +54,7 @@ struct TcCfg {
     static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
     static constexpr int SMEM = OFF_BAR + 3072;      // the dynamic base must be 1024-aligned
     static_assert(SMEM <= 232448, "shared memory budget");
-    static_assert(128 * (DV + 4) * 4 <= OFF_BAR, "epilogue staging fits below the barriers");
+    static_assert(128 * (DV + 4) * 4 + 128 * 8 <= OFF_BAR, "epilogue staging fits below the barriers");
 };
 
 struct Bars {
@@ -163,6 +163,7 @@ template <int D, bool BF16, bool IMPLICIT>
 __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a, const __grid_constant__ TcMaps maps) {
     using Cfg = TcCfg<D>;
     constexpr int DV = Cfg::DV, NSK = Cfg::NSK, NSV = Cfg::NSV, ST = Cfg::STAGES;
+    constexpr int SROW = DV + 4;                        // floats per staged O row
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 128-byte-swizzled TMA / MMA tiles need a 1024-byte-aligned base; every
     // CTA has the same base, so a misaligned one stops all of them before any
@@ -186,20 +187,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
     const int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
-    // The CTAs of one (split, KV head) - all row tiles and O halves - form one
-    // cluster when launched as such: each K slab is loaded once for the whole
-    // cluster and each V slab once per O half, shares multicast to the CTAs
-    // that use them, so every K/V byte crosses L2 -> SM once.
-    const int cs = static_cast<int>(cluster_nctarank());
-    const int crank = static_cast<int>(cluster_ctarank());
-    const int k_share = cs, k_idx = crank;             // K: all CTAs of the cluster
-    const int v_share = cs > 1 ? n_rt : 1, v_idx = cs > 1 ? rt : 0;   // V: CTAs of this O half
-    const uint16_t k_mask = static_cast<uint16_t>((1u << cs) - 1u);
-    uint16_t v_mask = 0;
-    for (int r2 = 0; r2 < n_rt; ++r2) v_mask |= static_cast<uint16_t>(1u << (r2 * n_os + os));
+    // Cluster (cx x cy): along y, the row tiles and O halves of one (split, KV
+    // head) - each K slab is loaded once for them and each V slab once per O
+    // half, the shares multicast, so every K/V byte crosses L2 -> SM once;
+    // along x, consecutive splits whose partials are merged in the cluster.
+    const int cx = static_cast<int>(cluster_nctaid_x()), cy = static_cast<int>(cluster_nctaid_y());
+    const int cxi = static_cast<int>(cluster_ctaid_x()), cyi = static_cast<int>(cluster_ctaid_y());
+    const int k_share = cy, k_idx = cyi;                            // K: every y of this split
+    const int v_share = cy > 1 ? n_rt : 1, v_idx = cy > 1 ? rt : 0;  // V: the y of this O half
+    uint16_t k_mask = 0, v_mask = 0;
+    for (int y2 = 0; y2 < cy; ++y2) k_mask |= static_cast<uint16_t>(1u << (cxi + cx * y2));
+    if (cy > 1)
+        for (int r2 = 0; r2 < n_rt; ++r2) v_mask |= static_cast<uint16_t>(1u << (cxi + cx * (r2 * n_os + os)));
 
     if (tid == 0) {
-        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cs); }
+        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cy); }
         mbar_init(&bars->q_full, 1);
         for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 8); }
         mbar_init(&bars->p_full, 8);
@@ -299,7 +301,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             int used = 0;                                   // ring loads consumed
             // a slot is free once every CTA of the cluster has consumed it
             auto release = [&](int slot) {
-                if (cs > 1) mma_commit_mc(&bars->empty[slot], k_mask);
+                if (cy > 1) mma_commit_mc(&bars->empty[slot], k_mask);
                 else mma_commit(&bars->empty[slot]);
             };
             bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2);
@@ -521,19 +523,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             ok = wait_all(&bars->o_done, static_cast<uint32_t>(T - 1) & 1u, 8);
             tc_fence_after();
         }
-        // epilogue: row sum of both halves, O rows staged in shared memory (free
-        // once the last MMA is done; rows padded by 16 bytes), then stored row by
-        // row with whole warps (512 contiguous bytes per store instruction)
+        // epilogue: row sum of both halves; the unnormalized O rows and the
+        // row's (S, M) are staged in shared memory (free once the last MMA is
+        // done; O rows padded by 16 bytes) for the store / merge phase below
         pdl_launch_dependents();
         bars->xrow[T & 1][half][r] = l_half;
         pair_sync();
         const float l_run = l_half + bars->xrow[T & 1][half ^ 1][r];
-        const int nrows = a.H * a.L;
-        const size_t rid = static_cast<size_t>(qi) * a.H + hj;
-        const float inv = (l_run == 0.0f) ? 0.0f : 1.0f / l_run;
-        const float scale_out = (a.nwg == 1) ? inv : 1.0f;
         const bool have_o = ok && T > 0;
-        constexpr int SROW = DV + 4;
         float *stage = reinterpret_cast<float *>(sm);
 #pragma unroll 1
         for (int c = 0; c < DVH / 32; ++c) {
@@ -549,34 +546,90 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
                 *reinterpret_cast<float4 *>(srow + e) =
-                    make_float4(__uint_as_float(rr[e]) * scale_out, __uint_as_float(rr[e + 1]) * scale_out,
-                                __uint_as_float(rr[e + 2]) * scale_out, __uint_as_float(rr[e + 3]) * scale_out);
+                    make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]), __uint_as_float(rr[e + 2]),
+                                __uint_as_float(rr[e + 3]));
         }
-        asm volatile("bar.sync 5, 256;" ::: "memory");  // the eight softmax warps
-        for (int rr = sw; rr < rows_here; rr += 8) {
-            const int rg2 = rt * RT + rr;
-            const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
-            float *dst = (a.nwg == 1) ? a.out + rid2 * D + os * DV
-                                      : a.part_o + (static_cast<size_t>(split) * nrows + rid2) * D + os * DV;
-            for (int c4 = lane; c4 < DV / 4; c4 += 32)
-                *reinterpret_cast<float4 *>(dst + 4 * c4) = *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
-        }
-        if (row_ok && half == 0 && a.nwg > 1 && os == 0) {
-            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 0] = l_run;
-            a.part_ml[(static_cast<size_t>(split) * nrows + rid) * 2 + 1] =
-                m_run == -INFINITY ? kMInit : m_run * kLn2;   // natural-log units
-        }
+        if (half == 0)
+            reinterpret_cast<float2 *>(stage + 128 * SROW)[r] =
+                make_float2(l_run, m_run == -INFINITY ? kMInit : m_run * kLn2);   // (S, M), natural log
     }
 
+    // ------------------------------------------------------ store or merge
+    // After the cluster barrier every CTA's staged rows are visible to its
+    // peers.  Without an x extent each CTA stores its own rows; otherwise CTA
+    // x of the cluster takes rows [x * n, (x + 1) * n) of the tile and merges
+    // them over the cx splits of the cluster (log-sum-exp weights, loads from
+    // the peers' shared memory).  With n_part == 0 the merged rows are final
+    // (normalized output); else they are partial slot split / cx.
     tc_fence_before();
     __syncthreads();
     cluster_sync();
+    if (warp >= 2) {
+        const int sw = warp - 2;
+        const int nrows = a.H * a.L;
+        const bool final_out = a.n_part == 0;
+        const float *stage = reinterpret_cast<const float *>(sm);
+        const uint32_t stage_sa = smem_u32(stage);
+        const uint32_t ml_sa = stage_sa + 128 * SROW * 4;
+        const int slot = split / cx;
+        const int rows_per = (rows_here + cx - 1) / cx;
+        const int r0 = cxi * rows_per, r1 = min(rows_here, r0 + rows_per);
+        for (int rr = r0 + sw; rr < r1; rr += 8) {
+            const int rg2 = rt * RT + rr;
+            const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
+            // split weights of this row (lane p < cx holds peer p's)
+            float mp = -FLT_MAX, wl = 0.0f, wp = 0.0f;
+            if (lane < cx) {
+                const float2 ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane + cx * cyi));
+                mp = ml.y;
+                wl = ml.x;
+            }
+            const float mstar = warp_max(mp);
+            if (lane < cx) wp = expf(mp - mstar);
+            const float sstar = warp_sum(wl * wp);
+            const float inv = (sstar == 0.0f) ? 0.0f : 1.0f / sstar;
+            float *dst = final_out ? a.out + rid2 * D + os * DV
+                                   : a.part_o + (static_cast<size_t>(slot) * nrows + rid2) * D + os * DV;
+            for (int c4 = lane; c4 < DV / 4; c4 += 32) {
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                const uint32_t off = stage_sa + (rr * SROW + 4 * c4) * 4;
+                for (int p = 0; p < cx; ++p) {
+                    const float w = __shfl_sync(0xffffffffu, wp, p);
+                    const float4 v = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p + cx * cyi))
+                                            : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
+                    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
+                }
+                if (final_out) { acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv; }
+                *reinterpret_cast<float4 *>(dst + 4 * c4) = acc;
+            }
+            if (!final_out && lane == 0 && os == 0) {
+                a.part_ml[(static_cast<size_t>(slot) * nrows + rid2) * 2 + 0] = sstar;
+                a.part_ml[(static_cast<size_t>(slot) * nrows + rid2) * 2 + 1] = mstar;
+            }
+        }
+    }
+
+    __syncthreads();
+    cluster_sync();                                     // peers are done with this CTA's shared memory
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
 }
+
+}  // namespace
+
+void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
+    const int n_rt = (a.R + 127) / 128;
+    const int gy = n_rt * (a.D == 512 ? 2 : 1);
+    *cy = gy <= 8 ? gy : 1;
+    *cx = 1;
+    for (int d = 8 / *cy; d >= 1; --d)
+        if (a.nwg % d == 0) { *cx = d; break; }
+}
+
+namespace {
 
 template <int D, bool BF16, bool IMPLICIT>
 cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
@@ -586,8 +639,11 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
     if (e != cudaSuccess) return e;
     const int n_rt = (a.R + 127) / 128;
     const unsigned gy = static_cast<unsigned>(n_rt * (D / TcCfg<D>::DV));
+    int cx, cy;
+    tree_tc_cluster_shape(a, &cx, &cy);
     dim3 grid(a.nwg, gy, a.Hk);
-    e = launch_pdl_cluster(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, gy <= 8 ? gy : 1u, a, maps);
+    e = launch_pdl_cluster(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, static_cast<unsigned>(cx),
+                           static_cast<unsigned>(cy), a, maps);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
