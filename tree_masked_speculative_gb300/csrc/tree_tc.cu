@@ -618,15 +618,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     }
 }
 
+// Clusters of `size` CTAs of this kernel that the current device can hold at
+// once (the kernel is shared-memory bound to one CTA per SM, equally for all
+// instantiations); cached per device.
+static int max_active_clusters(int size) {
+    static int cache[64][4];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return 0; }
+    const int idx = size == 1 ? 0 : (size == 2 ? 1 : (size == 4 ? 2 : 3));
+    int n = __atomic_load_n(&cache[dev][idx], __ATOMIC_ACQUIRE);
+    if (n > 0) return n;
+    auto kern = tree_tc_kernel<256, false, false>;
+    static unsigned long long done = 0;
+    if (set_smem_limit_once(kern, TcCfg<256>::SMEM, &done) != cudaSuccess) { cudaGetLastError(); return 0; }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(size, 1, 1);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = TcCfg<256>::SMEM;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = size;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) { cudaGetLastError(); n = 0; }
+    if (n > 0) __atomic_store_n(&cache[dev][idx], n, __ATOMIC_RELEASE);
+    return n;
+}
+
 }  // namespace
 
+// Largest cluster whose clusters all fit on the device at once (one wave):
+// first the row tiles / O halves along y (multicast K/V), then as many
+// consecutive splits along x as fit (in-cluster merge), at most 8 CTAs.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     const int n_rt = (a.R + 127) / 128;
     const int gy = n_rt * (a.D == 512 ? 2 : 1);
-    *cy = gy <= 8 ? gy : 1;
+    const long total = static_cast<long>(a.nwg) * gy * a.Hk;
+    auto fits = [&](int size) {
+        const int n = size == 1 ? 1 << 30 : max_active_clusters(size);
+        return n > 0 && total / size <= n;
+    };
     *cx = 1;
-    for (int d = 8 / *cy; d >= 1; --d)
-        if (a.nwg % d == 0) { *cx = d; break; }
+    *cy = 1;
+    const int y_choices[2] = {gy, 1};
+    for (int yc : y_choices) {
+        if (yc > 8 || (yc & (yc - 1)) != 0 || !fits(yc)) continue;
+        *cy = yc;
+        for (int d = 8 / yc; d >= 2; d >>= 1)
+            if (a.nwg % d == 0 && fits(d * yc)) { *cx = d; break; }
+        return;
+    }
 }
 
 namespace {
