@@ -574,33 +574,48 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int slot = split / cx;
         const int rows_per = (rows_here + cx - 1) / cx;
         const int r0 = cxi * rows_per, r1 = min(rows_here, r0 + rows_per);
+        constexpr int C4 = DV / 128;                    // float4 columns per lane
         for (int rr = r0 + sw; rr < r1; rr += 8) {
             const int rg2 = rt * RT + rr;
             const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
-            // split weights of this row (lane p < cx holds peer p's)
-            float mp = -FLT_MAX, wl = 0.0f, wp = 0.0f;
-            if (lane < cx) {
-                const float2 ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane + cx * cyi));
-                mp = ml.y;
-                wl = ml.x;
+            // every remote load of the row is issued before any is used
+            float2 ml = make_float2(0.0f, -FLT_MAX);
+            float4 v[8][C4];
+            if (lane < cx) ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane + cx * cyi));
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                if (p >= cx) break;
+#pragma unroll
+                for (int j = 0; j < C4; ++j) {
+                    const uint32_t off = stage_sa + (rr * SROW + 4 * (lane + 32 * j)) * 4;
+                    v[p][j] = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p + cx * cyi))
+                                     : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * (lane + 32 * j));
+                }
             }
-            const float mstar = warp_max(mp);
-            if (lane < cx) wp = expf(mp - mstar);
-            const float sstar = warp_sum(wl * wp);
+            const float mstar = warp_max(lane < cx ? ml.y : -FLT_MAX);
+            const float wp = lane < cx ? expf(ml.y - mstar) : 0.0f;
+            const float sstar = warp_sum(lane < cx ? ml.x * wp : 0.0f);
             const float inv = (sstar == 0.0f) ? 0.0f : 1.0f / sstar;
+            float4 acc[C4];
+#pragma unroll
+            for (int j = 0; j < C4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                if (p >= cx) break;
+                const float w = __shfl_sync(0xffffffffu, wp, p);
+#pragma unroll
+                for (int j = 0; j < C4; ++j) {
+                    acc[j].x += w * v[p][j].x; acc[j].y += w * v[p][j].y;
+                    acc[j].z += w * v[p][j].z; acc[j].w += w * v[p][j].w;
+                }
+            }
             float *dst = final_out ? a.out + rid2 * D + os * DV
                                    : a.part_o + (static_cast<size_t>(slot) * nrows + rid2) * D + os * DV;
-            for (int c4 = lane; c4 < DV / 4; c4 += 32) {
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                const uint32_t off = stage_sa + (rr * SROW + 4 * c4) * 4;
-                for (int p = 0; p < cx; ++p) {
-                    const float w = __shfl_sync(0xffffffffu, wp, p);
-                    const float4 v = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p + cx * cyi))
-                                            : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
-                    acc.x += w * v.x; acc.y += w * v.y; acc.z += w * v.z; acc.w += w * v.w;
-                }
-                if (final_out) { acc.x *= inv; acc.y *= inv; acc.z *= inv; acc.w *= inv; }
-                *reinterpret_cast<float4 *>(dst + 4 * c4) = acc;
+#pragma unroll
+            for (int j = 0; j < C4; ++j) {
+                float4 o = acc[j];
+                if (final_out) { o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv; }
+                *reinterpret_cast<float4 *>(dst + 4 * (lane + 32 * j)) = o;
             }
             if (!final_out && lane == 0 && os == 0) {
                 a.part_ml[(static_cast<size_t>(slot) * nrows + rid2) * 2 + 0] = sstar;
