@@ -666,8 +666,10 @@ static int max_active_clusters(int size) {
 }  // namespace
 
 // Largest cluster whose clusters all fit on the device at once (one wave):
-// first the row tiles / O halves along y (multicast K/V), then as many
-// consecutive splits along x as fit (in-cluster merge), at most 8 CTAs.
+// first the row tiles / O halves along y (multicast K/V); then all splits
+// along x when they fit in the cluster, so the merge completes inside it and
+// no partials are written (a partial in-cluster merge costs more in remote
+// loads than it saves in partial traffic); at most 8 CTAs.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     const int n_rt = (a.R + 127) / 128;
     const int gy = n_rt * (a.D == 512 ? 2 : 1);
@@ -682,8 +684,7 @@ void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     for (int yc : y_choices) {
         if (yc > 8 || (yc & (yc - 1)) != 0 || !fits(yc)) continue;
         *cy = yc;
-        for (int d = 8 / yc; d >= 2; d >>= 1)
-            if (a.nwg % d == 0 && fits(d * yc)) { *cx = d; break; }
+        if (a.nwg > 1 && a.nwg * yc <= 8 && fits(a.nwg * yc)) *cx = a.nwg;
         return;
     }
 }
