@@ -355,8 +355,9 @@ ta_status check_quant_params(const ta_quant_params *p) {
     if (p->tokens == 0) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: tokens must be > 0");
     if (p->has_sinks > 1) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: has_sinks must be 0 or 1");
     if (!std::isfinite(p->scale)) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: scale is not finite");
-    if (p->group_size % pf != 0)
-        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: group_size must be a multiple of 32/bits");
+    if (p->group_size % (4 * pf) != 0)
+        return fail(TA_ERR_UNSUPPORTED,
+                    "quant_sdpa: group_size must be a multiple of 4 * 32/bits (whole 16-byte word groups)");
     if (p->dim > 512) return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: dim > 512 is not implemented");
     if (p->n_q_heads / p->n_kv_heads > 8)
         return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: more than 8 query heads per KV head is not implemented");
@@ -542,7 +543,7 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     if (!quant_tmp(p, nwg, &req_tmp)) return fail(TA_ERR_OVERFLOW, "quant_sdpa: tmp size overflows");
 
     TA_TRY(check_buf(queries, "quant_sdpa: queries", req_q, 2));
-    TA_TRY(check_buf(k_packed, "quant_sdpa: k_packed", req_packed, 4));
+    TA_TRY(check_buf(k_packed, "quant_sdpa: k_packed", req_packed, 16));
     TA_TRY(check_buf(v_packed, "quant_sdpa: v_packed", req_packed, 4));
     TA_TRY(check_buf(k_scales, "quant_sdpa: k_scales", req_sb, 2));
     TA_TRY(check_buf(k_biases, "quant_sdpa: k_biases", req_sb, 2));

@@ -48,15 +48,29 @@ __device__ __forceinline__ float code_to_f32(uint32_t code) {
     return __uint_as_float(0x4B000000u | code) - 8388608.0f;
 }
 
+// Shared memory of one CTA: scale * q as [dim][REP] (all rows of one element
+// in one vector load), the per-group sums of scale * q (bias term of the
+// factored dequant), per warp a double-buffered [32 tokens][WPT + 4] tile of
+// packed K words (padded so per-token 16-byte reads are conflict-free) and the
+// chunk's softmax weights, and the cross-warp combine area.
 template <int REP>
 struct QuantSmem {
-    static size_t bytes(int dim) {
-        return sizeof(float) * ((size_t)REP * dim          // sQ
-                                + kWarps * 32 * REP        // sP
-                                + (size_t)kWarps * REP * dim  // sRed
-                                + kWarps * REP * 2);       // per-warp (M, S)
+    static size_t qv_floats(int dim, int ng) { return (size_t)REP * dim + (size_t)REP * ng; }
+    static size_t bytes(int dim, int ng, int wpt) {
+        return sizeof(float) * (qv_floats(dim, ng) + kWarps * 32 * REP + (size_t)kWarps * REP * dim +
+                                kWarps * REP * 2) +
+               sizeof(uint32_t) * (size_t)kWarps * 2 * 32 * (wpt + 4) + 16;
     }
 };
+
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, bool pred) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(pred ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <int BITS, typename T, int REP, int WPL>
 __global__ void __launch_bounds__(kThreads) quant_fma_kernel(const QuantArgs a) {
@@ -65,22 +79,33 @@ __global__ void __launch_bounds__(kThreads) quant_fma_kernel(const QuantArgs a) 
     constexpr int EPL = WPL * PF;               // output elements per lane
     extern __shared__ __align__(16) float qsm[];
     const int dim = a.dim;
-    float *sQ = qsm;                            // [REP][dim], scale * q
-    float *sP = sQ + REP * dim;                 // [warp][token][REP]
+    const int WPT = dim / PF;                   // packed words per token (a multiple of 4)
+    const int NG = dim / a.G;
+    const int WPG = a.G / PF;                   // words per group
+    const int WPS = WPT + 4;                    // padded words per staged token
+    float *sQ = qsm;                            // [dim][REP], scale * q
+    float *sQg = sQ + REP * dim;                // [REP][NG], per-group sum of scale * q
+    float *sP = sQg + REP * NG;                 // [warp][token][REP]
     float *sRed = sP + kWarps * 32 * REP;       // [warp][REP][dim]
     float *sMS = sRed + kWarps * REP * dim;     // [warp][REP][2]
+    uint32_t *sK = reinterpret_cast<uint32_t *>(
+        (reinterpret_cast<uintptr_t>(sMS + kWarps * REP * 2) + 15) & ~static_cast<uintptr_t>(15));
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int split = blockIdx.x, kv = blockIdx.y;
     const int q0 = kv * a.rep;
     const int N = a.N;
-    const int WPT = dim / PF;                   // packed words per token
-    const int NG = dim / a.G;
-    const int WPG = a.G / PF;                   // words per group
 
     for (int idx = tid; idx < REP * dim; idx += kThreads) {
-        const int rr = idx / dim, d = idx % dim;
+        const int d = idx / REP, rr = idx % REP;
         sQ[idx] = rr < a.rep ? a.scale * ld_t<T>(a.queries, (size_t)(q0 + rr) * dim + d) : 0.0f;
+    }
+    __syncthreads();
+    for (int idx = tid; idx < REP * NG; idx += kThreads) {
+        const int rr = idx / NG, g = idx % NG;
+        float acc = 0.0f;
+        for (int d = g * a.G; d < (g + 1) * a.G; ++d) acc += sQ[d * REP + rr];
+        sQg[idx] = acc;
     }
     __syncthreads();
 
@@ -91,61 +116,101 @@ __global__ void __launch_bounds__(kThreads) quant_fma_kernel(const QuantArgs a) 
     const int my_slot = lane % wpt_eff;
     const bool pv_lane = my_to < tpi;
 
-    float M[REP], S[REP], O[REP][EPL];
+    float M[REP], S[REP], O[REP][EPL], OB[REP][WPL];   // OB: per-word bias term sum_t p * b
 #pragma unroll
     for (int rr = 0; rr < REP; ++rr) {
         M[rr] = kMInit;
         S[rr] = 0.0f;
 #pragma unroll
         for (int e = 0; e < EPL; ++e) O[rr][e] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < WPL; ++u) OB[rr][u] = 0.0f;
     }
 
     const int t_begin = a.t_lo + split * a.tps;
     const int t_end = min(N, t_begin + a.tps);
     float *myP = sP + warp * 32 * REP;
+    uint32_t *myK = sK + (size_t)warp * 2 * 32 * WPS;
+    const uint32_t *kp_row = a.kp + (size_t)kv * N * WPT;
 
-    for (int c0 = t_begin + warp * 32; c0 < t_end; c0 += kWarps * 32) {
+    // stage the packed K words of the warp's chunk starting at c0 into buffer b
+    auto stage_k = [&](int c0, int b) {
+        uint32_t *dst = myK + b * 32 * WPS;
+        const int pieces = 32 * (WPT / 4);
+        for (int i = lane; i < pieces; i += 32) {
+            const int tk = i / (WPT / 4), j = i % (WPT / 4);
+            const bool ok = c0 + tk < t_end;
+            cp_async16(dst + tk * WPS + 4 * j, kp_row + (size_t)(ok ? c0 + tk : t_begin) * WPT + 4 * j, ok);
+        }
+        cp_async_commit();
+    };
+
+    int c0 = t_begin + warp * 32;
+    int buf = 0;
+    if (c0 < t_end) stage_k(c0, 0);
+    for (; c0 < t_end; c0 += kWarps * 32, buf ^= 1) {
+        const int cn = c0 + kWarps * 32;
+        if (cn < t_end) {
+            stage_k(cn, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
         // ---- logits: lane = token
         const int t = c0 + lane;
+        const bool valid = t < t_end;
         bool gate[REP];
         bool any_gate = false;
 #pragma unroll
         for (int rr = 0; rr < REP; ++rr) {
-            bool g = (t < t_end) && (rr < a.rep);
+            bool g = valid && (rr < a.rep);
             if (g && a.mbool != nullptr) g = __ldg(a.mbool + (size_t)(q0 + rr) * N + t) != 0u;
             gate[rr] = g;
             any_gate |= g;
         }
-        if (!__any_sync(0xffffffffu, any_gate)) continue;
+        float fm[REP];
+#pragma unroll
+        for (int rr = 0; rr < REP; ++rr)
+            fm[rr] = (a.mfloat != nullptr && gate[rr]) ? ld_t<T>(a.mfloat, (size_t)(q0 + rr) * N + t) : 0.0f;
         float logit[REP];
 #pragma unroll
         for (int rr = 0; rr < REP; ++rr) logit[rr] = -INFINITY;
-        if (any_gate) {
+        if (__any_sync(0xffffffffu, any_gate)) {
             float acc[REP];
 #pragma unroll
             for (int rr = 0; rr < REP; ++rr) acc[rr] = 0.0f;
-            const size_t tok = (size_t)kv * N + t;
-            const uint32_t *kw = a.kp + tok * WPT;
-            for (int g = 0; g < NG; ++g) {
-                const float s = ld_t<T>(a.ks, tok * NG + g);
-                const float b = ld_t<T>(a.kb, tok * NG + g);
-                for (int wi = g * WPG; wi < (g + 1) * WPG; ++wi) {
-                    const uint32_t w = __ldg(kw + wi);
+            if (any_gate) {
+                const size_t tok = (size_t)kv * N + t;
+                const uint32_t *kw = myK + buf * 32 * WPS + lane * WPS;
+                for (int g = 0; g < NG; ++g) {
+                    // q . k over group g = s * sum(q_d * code_d) + b * sum(q_d)
+                    float part[REP];
 #pragma unroll
-                    for (int e = 0; e < PF; ++e) {
-                        const float kval = fmaf(s, code_to_f32((w >> (e * BITS)) & CMASK), b);
-                        const float *qd = sQ + wi * PF + e;
+                    for (int rr = 0; rr < REP; ++rr) part[rr] = 0.0f;
+                    for (int wi = g * WPG; wi < (g + 1) * WPG; wi += 4) {
+                        const uint4 w4 = *reinterpret_cast<const uint4 *>(kw + wi);
+                        const uint32_t ws[4] = {w4.x, w4.y, w4.z, w4.w};
 #pragma unroll
-                        for (int rr = 0; rr < REP; ++rr) acc[rr] = fmaf(qd[rr * dim], kval, acc[rr]);
+                        for (int x = 0; x < 4; ++x) {
+#pragma unroll
+                            for (int e = 0; e < PF; ++e) {
+                                const float cf = code_to_f32((ws[x] >> (e * BITS)) & CMASK);
+                                const float *qd = sQ + ((wi + x) * PF + e) * REP;
+#pragma unroll
+                                for (int rr = 0; rr < REP; ++rr) part[rr] = fmaf(qd[rr], cf, part[rr]);
+                            }
+                        }
                     }
+                    const float sc = ld_t<T>(a.ks, tok * NG + g);
+                    const float bi = ld_t<T>(a.kb, tok * NG + g);
+#pragma unroll
+                    for (int rr = 0; rr < REP; ++rr)
+                        acc[rr] = fmaf(sc, part[rr], fmaf(bi, sQg[rr * NG + g], acc[rr]));
                 }
             }
 #pragma unroll
-            for (int rr = 0; rr < REP; ++rr) {
-                float l = acc[rr];
-                if (a.mfloat != nullptr && gate[rr]) l += ld_t<T>(a.mfloat, (size_t)(q0 + rr) * N + t);
-                logit[rr] = gate[rr] ? l : -INFINITY;
-            }
+            for (int rr = 0; rr < REP; ++rr) logit[rr] = gate[rr] ? acc[rr] + fm[rr] : -INFINITY;
         }
         // ---- online softmax over the 32 tokens, per row
 #pragma unroll
@@ -160,12 +225,15 @@ __global__ void __launch_bounds__(kThreads) quant_fma_kernel(const QuantArgs a) 
                 M[rr] = m_new;
 #pragma unroll
                 for (int e = 0; e < EPL; ++e) O[rr][e] *= alpha;
+#pragma unroll
+                for (int u = 0; u < WPL; ++u) OB[rr][u] *= alpha;
             }
             myP[lane * REP + rr] = p;
         }
         __syncwarp();
-        // ---- O += p * v: lane = packed word
+        // ---- O += p * v = (p * s) * code + p * b: lane = packed word
         if (pv_lane) {
+#pragma unroll 2
             for (int tt = 0; tt < 32; tt += tpi) {
                 const int to = tt + my_to;
                 const int tk = c0 + to;
@@ -176,25 +244,41 @@ __global__ void __launch_bounds__(kThreads) quant_fma_kernel(const QuantArgs a) 
                 for (int rr = 0; rr < REP; ++rr) { pw[rr] = myP[to * REP + rr]; any_p |= pw[rr] != 0.0f; }
                 if (!any_p) continue;
                 const size_t tok = (size_t)kv * N + tk;
+                uint32_t wv[WPL];
+                float sv[WPL], bv[WPL];
 #pragma unroll
                 for (int u = 0; u < WPL; ++u) {
                     const int wi = my_slot + 32 * u;
-                    if (wi >= WPT) break;
-                    const uint32_t w = __ldg(a.vp + tok * WPT + wi);
-                    const int g = wi / WPG;
-                    const float s = ld_t<T>(a.vs, tok * NG + g);
-                    const float b = ld_t<T>(a.vb, tok * NG + g);
+                    const bool in = wi < WPT;
+                    wv[u] = in ? __ldg(a.vp + tok * WPT + wi) : 0u;
+                    sv[u] = in ? ld_t<T>(a.vs, tok * NG + wi / WPG) : 0.0f;
+                    bv[u] = in ? ld_t<T>(a.vb, tok * NG + wi / WPG) : 0.0f;
+                }
+#pragma unroll
+                for (int u = 0; u < WPL; ++u) {
+                    float ps[REP];
+#pragma unroll
+                    for (int rr = 0; rr < REP; ++rr) {
+                        ps[rr] = pw[rr] * sv[u];
+                        OB[rr][u] = fmaf(pw[rr], bv[u], OB[rr][u]);
+                    }
 #pragma unroll
                     for (int e = 0; e < PF; ++e) {
-                        const float vval = fmaf(s, code_to_f32((w >> (e * BITS)) & CMASK), b);
+                        const float cf = code_to_f32((wv[u] >> (e * BITS)) & CMASK);
 #pragma unroll
-                        for (int rr = 0; rr < REP; ++rr) O[rr][u * PF + e] = fmaf(pw[rr], vval, O[rr][u * PF + e]);
+                        for (int rr = 0; rr < REP; ++rr) O[rr][u * PF + e] = fmaf(ps[rr], cf, O[rr][u * PF + e]);
                     }
                 }
             }
         }
         __syncwarp();
     }
+#pragma unroll
+    for (int rr = 0; rr < REP; ++rr)
+#pragma unroll
+        for (int u = 0; u < WPL; ++u)
+#pragma unroll
+            for (int e = 0; e < PF; ++e) O[rr][u * PF + e] += OB[rr][u];
 
     // ---- lanes sharing a word slot hold the same state: sum them
     for (int k = 1; k < tpi; ++k) {
@@ -295,7 +379,7 @@ __global__ void __launch_bounds__(128) quant_merge_kernel(const QuantArgs a) {
 template <int BITS, typename T, int REP, int WPL>
 cudaError_t launch_q(const QuantArgs &a, cudaStream_t s) {
     auto kern = quant_fma_kernel<BITS, T, REP, WPL>;
-    const size_t smem = QuantSmem<REP>::bytes(a.dim);
+    const size_t smem = QuantSmem<REP>::bytes(a.dim, a.dim / a.G, a.dim * BITS / 32);
     static unsigned long long done = 0;
     cudaError_t e = set_smem_limit_once(kern, smem, &done);
     if (e != cudaSuccess) return e;
