@@ -37,6 +37,9 @@ QCASES = [
     dict(dim=512, bits=4, G=128, N=200, nwg=2),
     dict(dim=512, bits=8, G=64, N=150, bfrac=0.3, dtype="bf16"),
     dict(nQ=16, nKV=2, N=257, window=33),          # 8 query rows per KV row
+    dict(nQ=32, nKV=2, N=129, bits=8, dtype="bf16", fmask="alibi", bfrac=0.2),   # 16 rows, 4 row groups
+    dict(nQ=4, nKV=4, N=100, dim=128, nwg=2),      # 1 row per KV row
+    dict(dim=128, G=32, bits=8, N=333, window=200, fmask="alibi", bfrac=0.1, sinks=1, dtype="bf16"),
     dict(nQ=6, nKV=2, N=64, nwg=1),                # 3 rows per KV row
     dict(N=31, window=500),
 ]

@@ -359,8 +359,6 @@ ta_status check_quant_params(const ta_quant_params *p) {
         return fail(TA_ERR_UNSUPPORTED,
                     "quant_sdpa: group_size must be a multiple of 4 * 32/bits (whole 16-byte word groups)");
     if (p->dim > 512) return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: dim > 512 is not implemented");
-    if (p->n_q_heads / p->n_kv_heads > 8)
-        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: more than 8 query heads per KV head is not implemented");
     const uint64_t rows = (uint64_t)p->batch * p->n_q_heads;
     const uint64_t kvr = (uint64_t)p->batch * p->n_kv_heads;
     uint64_t cells;
@@ -374,14 +372,30 @@ uint32_t window_tokens(const ta_quant_params *p) {
     return p->window_size == 0 ? p->tokens : (p->window_size < p->tokens ? p->window_size : p->tokens);
 }
 
+// 32-token chunks of one KV row inside the window (chunks start at multiples
+// of 32 tokens).
+uint32_t quant_chunks(const ta_quant_params *p) {
+    const uint32_t t_lo = p->tokens - window_tokens(p);
+    return (p->tokens + 31u) / 32u - t_lo / 32u;
+}
+
+uint32_t quant_row_groups(const ta_quant_params *p) {
+    const uint32_t rep = p->n_q_heads / p->n_kv_heads;
+    return (rep + (uint32_t)kQuantRowsPerCta - 1) / (uint32_t)kQuantRowsPerCta;
+}
+
+// Token splits: as many as fill every SM's resident one-warp CTAs in one wave
+// (kv rows x row groups x splits), at most one per chunk.
 uint32_t resolve_quant_nwg(const ta_quant_params *p) {
     if (p->nwg != 0) return p->nwg;
     const int sms = sm_count();
     if (sms <= 0) return 0;
-    const uint64_t kvr = (uint64_t)p->batch * p->n_kv_heads;
-    const uint64_t max_splits = (window_tokens(p) + 127u) / 128u;
-    uint64_t nwg = (4ull * sms + kvr - 1) / kvr;
-    if (nwg > max_splits) nwg = max_splits;
+    const int per_sm = quant_ctas_per_sm((int)p->bits, (int)p->dim, (int)(p->dim / p->group_size));
+    if (per_sm <= 0) return 0;
+    const uint64_t units = (uint64_t)p->batch * p->n_kv_heads * quant_row_groups(p);
+    uint64_t nwg = ((uint64_t)sms * (uint64_t)per_sm) / units;
+    const uint64_t nch = quant_chunks(p);
+    if (nwg > nch) nwg = nch;
     if (nwg < 1) nwg = 1;
     if (nwg > 65535) nwg = 65535;
     return (uint32_t)nwg;
@@ -544,7 +558,7 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
 
     TA_TRY(check_buf(queries, "quant_sdpa: queries", req_q, 2));
     TA_TRY(check_buf(k_packed, "quant_sdpa: k_packed", req_packed, 16));
-    TA_TRY(check_buf(v_packed, "quant_sdpa: v_packed", req_packed, 4));
+    TA_TRY(check_buf(v_packed, "quant_sdpa: v_packed", req_packed, 16));
     TA_TRY(check_buf(k_scales, "quant_sdpa: k_scales", req_sb, 2));
     TA_TRY(check_buf(k_biases, "quant_sdpa: k_biases", req_sb, 2));
     TA_TRY(check_buf(v_scales, "quant_sdpa: v_scales", req_sb, 2));
@@ -585,10 +599,18 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     a.has_sinks = (int)p->has_sinks;
     a.window = (int)p->window_size;
     a.nwg = (int)nwg;
-    const uint32_t wt = window_tokens(p);
-    a.t_lo = (int)(p->tokens - wt);
-    const uint64_t per = (wt + nwg - 1) / nwg;
-    a.tps = (int)(((per + 31) / 32) * 32);
+    a.wpt = (int)(p->dim * p->bits / 32);
+    a.ng = (int)(p->dim / p->group_size);
+    a.n_rg = (int)quant_row_groups(p);
+    a.t_lo = (int)(p->tokens - window_tokens(p));
+    a.c_lo = a.t_lo / 32;
+    a.nch = (int)quant_chunks(p);
+    const auto al16 = [](const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; };
+    a.al_sb = al16(k_scales.ptr) && al16(k_biases.ptr) && al16(v_scales.ptr) && al16(v_biases.ptr) &&
+              ((uint64_t)p->tokens * a.ng * 2) % 16 == 0;
+    a.al_mf = has_float && al16(mask_float.ptr) && p->tokens % 8 == 0;
+    if ((uint64_t)a.nwg * a.n_rg > (uint64_t)INT_MAX)
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: too many splits x row groups");
     a.t_is_bf16 = T == TA_BF16;
     a.out_f32 = out.dtype == TA_F32;
     a.scale = p->scale;

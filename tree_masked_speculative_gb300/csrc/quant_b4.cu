@@ -1,0 +1,7 @@
+// 4-bit instances of the quantized-KV kernel.
+#include "quant_kernel.cuh"
+
+namespace ta {
+cudaError_t launch_quant_b4(const QuantArgs &a, cudaStream_t s) { return quant::launch_bits<4>(a, s); }
+int quant_ctas_per_sm_b4(int dim, int ng) { return quant::occupancy_bits<4>(dim, ng); }
+}  // namespace ta

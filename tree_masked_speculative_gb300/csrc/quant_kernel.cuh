@@ -1,0 +1,567 @@
+// Attention over an affine-quantized K/V cache on the CUDA cores (one warp
+// per CTA).  Included by quant_b4.cu and quant_b8.cu, which instantiate it.
+//
+// What it computes follows metaltile-std flash_quantized_sdpa.rs (base,
+// bool-mask and float-mask kernels): q is multiplied by `scale` before the dot;
+// K and V element d of a token is scale[d / G] * code_d + bias[d / G], code_d
+// at bits (d % pf) * bits of word d / pf; a token takes part when it lies in
+// the sliding window and its bool-mask slot is non-zero; the float mask is
+// added to the logit; the sink is a virtual key with logit sinks[q % nQ] and
+// value 0 (added by the finalisation or the merge); out = o / l, or o when
+// l = 0.  Both masks applied in one pass is the chained composition the
+// module doc describes.
+//
+// GB300 design (not the pages' one-simdgroup-per-query token loop):
+//  * one warp = one CTA owns a (KV row, row group of 4 query rows, token
+//    split); the split count fills every SM's resident-warp slots in one wave;
+//  * every 32-token chunk is staged in shared memory by cp.async in two
+//    groups (K words + scales + masks, then V words) so that one chunk's loads
+//    overlap the previous chunk's arithmetic;
+//  * scores: each lane keeps scale * log2(e) * q for 16 dimensions of the 4
+//    rows in registers (so no shared-memory broadcast of q per dimension),
+//    decodes its part of each token with byte permutes, scales the codes with
+//    one packed FMA (s * (2^23 + c) - 2^23 * s = s * c) and accumulates with
+//    packed f32x2 FMAs; the per-token partial sums of the lanes are combined
+//    by a transposed butterfly (reduce-scatter), which leaves each lane one
+//    (token, row) score per batch; the bias term sum_g b_g * sum_{d in g} q_d
+//    is added once per (token, row) after the reduction;
+//  * online softmax in log2 units per row; P is kept in shared memory;
+//  * values: lane = packed-word slot; O += p * (s * c) with the same decode
+//    and packed FMAs, and the bias part sum_t p_t * b_t is accumulated per
+//    (row, group) once per chunk.
+#pragma once
+
+#include <type_traits>
+
+#include "ta_internal.cuh"
+
+namespace ta {
+namespace quant {
+
+constexpr int REP = kQuantRowsPerCta;   // query rows of one row group
+constexpr int DPL = 16;                 // score pass: dimensions per lane (q regs = DPL * REP)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kTwo23 = 8388608.0f;   // 2^23: the float whose low mantissa bits hold a code
+
+template <int BITS, int DIMC>
+struct Shape {
+    static constexpr int PF = 32 / BITS;                   // codes per packed word
+    static constexpr int LPT = DIMC / DPL;                 // score lanes per token (4..32)
+    static constexpr int TPP = 32 / LPT;                   // tokens per score pass
+    static constexpr int B = LPT / REP;                    // score passes per reduction batch
+    static constexpr int WPQ = DPL / PF;                   // words per lane per token (scores)
+    static constexpr int WPTC = DIMC * BITS / 32;          // words per token at capacity
+    static constexpr int WPL = WPTC >= 32 ? WPTC / 32 : 1; // words per lane (values)
+    static constexpr int LPV = WPTC / WPL;                 // value lanes per token
+    static constexpr int TPV = 32 / LPV;                   // tokens per value pass
+    static constexpr int EPL = WPL * PF;                   // output dimensions per lane
+    static_assert(LPT >= REP && LPT <= 32, "score lanes per token");
+    static_assert(B * REP == LPT, "one reduced score per lane per batch");
+    static_assert(REP == 4, "the value pass reads the weights of four rows");
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// cp.async of 16 bytes (zero-filled beyond src_bytes) and of 4 bytes.
+__device__ __forceinline__ void cp16(void *dst, const void *src, int src_bytes) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp4(void *dst, const void *src, int src_bytes) {
+    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+
+template <typename T>
+__device__ __forceinline__ float t2f(uint16_t bits) {
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) return __uint_as_float(static_cast<uint32_t>(bits) << 16);
+    else return __half2float(__ushort_as_half(bits));
+}
+
+template <typename T>
+__device__ __forceinline__ void st_out(void *p, size_t i, float x, int out_f32) {
+    if (out_f32) reinterpret_cast<float *>(p)[i] = x;
+    else if constexpr (std::is_same<T, __half>::value) reinterpret_cast<__half *>(p)[i] = __float2half_rn(x);
+    else reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
+}
+
+// Codes (2k, 2k+1) of a packed word as the floats {2^23 + c0, 2^23 + c1}: the
+// code byte is permuted into the low mantissa byte under the exponent of 2^23.
+template <int BITS>
+struct Codes;
+template <>
+struct Codes<8> {
+    uint32_t w;
+    __device__ __forceinline__ explicit Codes(uint32_t word) : w(word) {}
+    __device__ __forceinline__ float2 pair(int k) const {
+        return make_float2(__uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | (2 * k))),
+                           __uint_as_float(__byte_perm(w, 0x4B000000u, 0x7440u | (2 * k + 1))));
+    }
+};
+template <>
+struct Codes<4> {
+    uint32_t lo, hi;   // even / odd nibbles, one per byte
+    __device__ __forceinline__ explicit Codes(uint32_t w) : lo(w & 0x0F0F0F0Fu), hi((w >> 4) & 0x0F0F0F0Fu) {}
+    __device__ __forceinline__ float2 pair(int k) const {
+        return make_float2(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440u | k)),
+                           __uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440u | k)));
+    }
+};
+
+// Reduce-scatter over groups of N lanes (xor 1 .. N/2): on return lane l holds
+// the sum over its group of value index (l % N).
+template <int N>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+    for (int s = 0; (1 << s) < N; ++s) {
+        const int m = 1 << s;
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < (N >> s) / 2; ++k) {
+            const float send = upper ? v[2 * k] : v[2 * k + 1];
+            const float keep = upper ? v[2 * k + 1] : v[2 * k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+        }
+    }
+    return v[0];
+}
+
+template <typename T, int WPL>
+__device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&w)[WPL]) {
+    if constexpr (WPL == 4) {
+        const uint4 x = *reinterpret_cast<const uint4 *>(p);
+        w[0] = x.x; w[1] = x.y; w[2] = x.z; w[3] = x.w;
+    } else if constexpr (WPL == 2) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(p);
+        w[0] = x.x; w[1] = x.y;
+    } else {
+#pragma unroll
+        for (int u = 0; u < WPL; ++u) w[u] = p[u];
+    }
+}
+
+template <int BITS, typename T, int DIMC>
+__global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const QuantArgs a) {
+    using S = Shape<BITS, DIMC>;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x;
+    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
+    const int q0 = kv * a.rep + rg * REP;
+    const int nrow = min(REP, a.rep - rg * REP);
+    const int N = a.N, WPT = a.wpt, NG = a.ng, G = a.G, dim = a.dim;
+    const QuantLayout L = quant_layout(WPT, NG);
+    uint32_t *sK = reinterpret_cast<uint32_t *>(smem + L.k);
+    uint32_t *sV = reinterpret_cast<uint32_t *>(smem + L.v);
+    uint16_t *sKs = reinterpret_cast<uint16_t *>(smem + L.ks);
+    uint16_t *sKb = reinterpret_cast<uint16_t *>(smem + L.kb);
+    uint16_t *sVs = reinterpret_cast<uint16_t *>(smem + L.vs);
+    uint16_t *sVb = reinterpret_cast<uint16_t *>(smem + L.vb);
+    uint32_t *sMb = reinterpret_cast<uint32_t *>(smem + L.mb);
+    uint16_t *sMf = reinterpret_cast<uint16_t *>(smem + L.mf);
+    float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
+    float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
+    float2 *sP2 = reinterpret_cast<float2 *>(smem + L.p2);     // [token][row] {p, p}
+    float *sOB = reinterpret_cast<float *>(smem + L.ob);       // [row][group] sum_t p * b
+    float *sQS = reinterpret_cast<float *>(smem + L.qs);       // [row][group] sum_{d in g} q'
+
+    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
+    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
+
+    // score-pass roles: lane = (token in pass tp, dimension slice j)
+    const int tp = lane / S::LPT, j = lane % S::LPT;
+    const int d0 = j * DPL;
+    const bool qk_live = d0 < dim;
+    const int g_qk = qk_live ? d0 / G : 0;
+    const int r_l = j % REP;   // row of the lane's reduced scores
+    const int pb_l = j / REP;  // pass (within a batch) of the lane's reduced scores
+    // value-pass roles: lane = (token in pass tv, word slot wl)
+    const int tv = lane / S::LPV, wl = lane % S::LPV;
+    const bool pv_live = wl * S::WPL < WPT;
+    const int g_v = pv_live ? (wl * S::WPL * S::PF) / G : 0;
+
+    // q' = scale * log2(e) * q for the lane's 16 dimensions of every row
+    const float qscale = a.scale * kLog2e;
+    float2 q2[REP][DPL / 2];
+    {
+        const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.queries);
+#pragma unroll
+        for (int r = 0; r < REP; ++r)
+#pragma unroll
+            for (int k = 0; k < DPL / 2; ++k) {
+                float2 x = make_float2(0.0f, 0.0f);
+                if (qk_live && r < nrow) {
+                    const size_t i = static_cast<size_t>(q0 + r) * dim + d0 + 2 * k;
+                    x = make_float2(qscale * t2f<T>(qg[i]), qscale * t2f<T>(qg[i + 1]));
+                }
+                q2[r][k] = x;
+            }
+    }
+    // per-(row, group) sums of q' (bias term), via the lanes' partial sums
+    {
+        float *sQP = reinterpret_cast<float *>(sP2);   // [row][LPT], free until the first chunk
+        if (tp == 0) {
+#pragma unroll
+            for (int r = 0; r < REP; ++r) {
+                float s = 0.0f;
+#pragma unroll
+                for (int k = 0; k < DPL / 2; ++k) s += q2[r][k].x + q2[r][k].y;
+                sQP[r * S::LPT + j] = s;
+            }
+        }
+        __syncwarp();
+        const int lpg = G / DPL;   // lanes per group
+        for (int idx = lane; idx < REP * NG; idx += 32) {
+            const int r = idx / NG, g = idx % NG;
+            float s = 0.0f;
+            for (int jj = g * lpg; jj < (g + 1) * lpg; ++jj) s += sQP[r * S::LPT + jj];
+            sQS[idx] = s;
+        }
+        for (int idx = lane; idx < REP * NG; idx += 32) sOB[idx] = 0.0f;
+        __syncwarp();
+    }
+
+    // ---- chunk staging
+    auto copy_sb = [&](uint16_t *dst, const void *src_v, size_t e0, int valid_e) {
+        const uint16_t *src = static_cast<const uint16_t *>(src_v) + e0;
+        const int E = 32 * NG;
+        if (a.al_sb) {
+            for (int p = lane; p < E / 8; p += 32) {
+                const int b = min(16, max(0, (valid_e - 8 * p) * 2));
+                cp16(dst + 8 * p, b > 0 ? src + 8 * p : src, b);
+            }
+        } else {
+            for (int e = lane; e < E; e += 32) dst[e] = e < valid_e ? src[e] : static_cast<uint16_t>(0);
+        }
+    };
+    auto issue_a = [&](int c) {
+        const int t0 = c * 32;
+        const int tval = min(32, N - t0);
+        const uint32_t *kg = a.kp + (static_cast<size_t>(kv) * N + t0) * WPT;
+        const int kvalid = tval * WPT / 4;
+        for (int p = lane; p < 8 * WPT; p += 32) cp16(sK + 4 * p, p < kvalid ? kg + 4 * p : kg, p < kvalid ? 16 : 0);
+        const size_t e0 = (static_cast<size_t>(kv) * N + t0) * NG;
+        copy_sb(sKs, a.ks, e0, tval * NG);
+        copy_sb(sKb, a.kb, e0, tval * NG);
+        copy_sb(sVs, a.vs, e0, tval * NG);
+        copy_sb(sVb, a.vb, e0, tval * NG);
+        if (a.mbool != nullptr) {
+#pragma unroll
+            for (int r = 0; r < REP; ++r) {
+                const bool ok = r < nrow && lane < tval;
+                const uint32_t *src = a.mbool + static_cast<size_t>(q0 + (r < nrow ? r : 0)) * N + t0;
+                cp4(sMb + r * 32 + lane, ok ? src + lane : src, ok ? 4 : 0);
+            }
+        }
+        if (a.mfloat != nullptr) {
+            const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
+            if (a.al_mf) {
+                if (lane < 4 * REP) {
+                    const int r = lane / 4, p = lane % 4;
+                    const uint16_t *src = mf + static_cast<size_t>(q0 + (r < nrow ? r : 0)) * N + t0;
+                    const int b = r < nrow ? min(16, max(0, (tval - 8 * p) * 2)) : 0;
+                    cp16(sMf + r * 32 + 8 * p, b > 0 ? src + 8 * p : src, b);
+                }
+            } else {
+#pragma unroll
+                for (int r = 0; r < REP; ++r) {
+                    const bool ok = r < nrow && lane < tval;
+                    sMf[r * 32 + lane] = ok ? mf[static_cast<size_t>(q0 + r) * N + t0 + lane] : static_cast<uint16_t>(0);
+                }
+            }
+        }
+    };
+    auto issue_b = [&](int c) {
+        const int t0 = c * 32;
+        const int tval = min(32, N - t0);
+        const uint32_t *vg = a.vp + (static_cast<size_t>(kv) * N + t0) * WPT;
+        const int vvalid = tval * WPT / 4;
+        for (int p = lane; p < 8 * WPT; p += 32) cp16(sV + 4 * p, p < vvalid ? vg + 4 * p : vg, p < vvalid ? 16 : 0);
+    };
+
+    float M = -INFINITY, Ssum = 0.0f;   // online-softmax state of row r_l (log2 units)
+    float2 O2[REP][S::EPL / 2];
+#pragma unroll
+    for (int r = 0; r < REP; ++r)
+#pragma unroll
+        for (int k = 0; k < S::EPL / 2; ++k) O2[r][k] = make_float2(0.0f, 0.0f);
+
+    if (c_begin < c_end) issue_a(c_begin);
+    cp_commit();
+    if (c_begin < c_end) issue_b(c_begin);
+    cp_commit();
+
+    for (int c = c_begin; c < c_end; ++c) {
+        cp_wait<1>();   // group A of chunk c (K, scales, masks)
+        __syncwarp();
+        const int t0 = c * 32;
+        for (int idx = lane; idx < 32 * NG; idx += 32) {
+            const float s = t2f<T>(sKs[idx]);
+            sKS4[idx] = make_float4(s, s, -kTwo23 * s, -kTwo23 * s);
+            const float sv = t2f<T>(sVs[idx]);
+            sVS4[idx] = make_float4(sv, sv, -kTwo23 * sv, -kTwo23 * sv);
+        }
+        // gates of the lane's (token, row) score slots
+        bool live[REP];
+        int tk[REP];
+        bool any = false;
+#pragma unroll
+        for (int bb = 0; bb < REP; ++bb) {
+            tk[bb] = (bb * S::B + pb_l) * S::TPP + tp;
+            const int t = t0 + tk[bb];
+            bool g = r_l < nrow && t >= a.t_lo && t < N;
+            if (g && a.mbool != nullptr) g = sMb[r_l * 32 + tk[bb]] != 0u;
+            live[bb] = g;
+            any |= g;
+        }
+        __syncwarp();
+        const bool chunk_live = __any_sync(0xffffffffu, any);
+
+        float lg[REP];
+#pragma unroll
+        for (int bb = 0; bb < REP; ++bb) lg[bb] = -INFINITY;
+        if (chunk_live) {
+            // ---- scores: partial dot products, reduce-scattered over the token's lanes
+#pragma unroll
+            for (int bb = 0; bb < REP; ++bb) {
+                float v[S::B * REP];
+#pragma unroll
+                for (int pb = 0; pb < S::B; ++pb) {
+                    const int t = (bb * S::B + pb) * S::TPP + tp;
+                    float2 acc[REP];
+#pragma unroll
+                    for (int r = 0; r < REP; ++r) acc[r] = make_float2(0.0f, 0.0f);
+                    if (qk_live) {
+                        uint32_t w[S::WPQ];
+                        load_words<T, S::WPQ>(sK + t * WPT + d0 / S::PF, w);
+                        const float4 sm = sKS4[t * NG + g_qk];
+                        const float2 s2 = make_float2(sm.x, sm.y), m2 = make_float2(sm.z, sm.w);
+#pragma unroll
+                        for (int u = 0; u < S::WPQ; ++u) {
+                            const Codes<BITS> cd(w[u]);
+#pragma unroll
+                            for (int k = 0; k < S::PF / 2; ++k) {
+                                const float2 sc = __ffma2_rn(cd.pair(k), s2, m2);   // s * code, rounded once
+#pragma unroll
+                                for (int r = 0; r < REP; ++r)
+                                    acc[r] = __ffma2_rn(q2[r][u * (S::PF / 2) + k], sc, acc[r]);
+                            }
+                        }
+                    }
+#pragma unroll
+                    for (int r = 0; r < REP; ++r) v[pb * REP + r] = acc[r].x + acc[r].y;
+                }
+                const float dot = reduce_scatter<S::B * REP>(v, lane);
+                if (live[bb]) {
+                    // + sum_g b_g * sum_{d in g} q'_d, + log2(e) * float mask
+                    float bias = 0.0f;
+                    for (int g = 0; g < NG; ++g) bias = fmaf(t2f<T>(sKb[tk[bb] * NG + g]), sQS[r_l * NG + g], bias);
+                    float fm = 0.0f;
+                    if (a.mfloat != nullptr) fm = kLog2e * t2f<T>(sMf[r_l * 32 + tk[bb]]);
+                    lg[bb] = dot + bias + fm;
+                }
+            }
+        }
+
+        // ---- online softmax of row r_l over the chunk (log2 units)
+        float cmax = lg[0];
+#pragma unroll
+        for (int bb = 1; bb < REP; ++bb) cmax = fmaxf(cmax, lg[bb]);
+#pragma unroll
+        for (int m = REP; m < 32; m <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, m));
+        const float m_new = fmaxf(M, cmax);
+        float alpha = 1.0f;
+        float p[REP];
+        if (m_new == -INFINITY) {
+#pragma unroll
+            for (int bb = 0; bb < REP; ++bb) p[bb] = 0.0f;
+        } else {
+            alpha = ex2(M - m_new);   // 0 while M = -inf
+#pragma unroll
+            for (int bb = 0; bb < REP; ++bb) p[bb] = ex2(lg[bb] - m_new);
+        }
+        float psum = 0.0f;
+#pragma unroll
+        for (int bb = 0; bb < REP; ++bb) psum += p[bb];
+#pragma unroll
+        for (int m = REP; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
+        Ssum = Ssum * alpha + psum;
+        M = m_new;
+#pragma unroll
+        for (int bb = 0; bb < REP; ++bb) sP2[tk[bb] * REP + r_l] = make_float2(p[bb], p[bb]);
+        // bias part of O: sum_t p_t * b_{t,g} per (row, group)
+        if (chunk_live) {
+            for (int g = 0; g < NG; ++g) {
+                float s = 0.0f;
+#pragma unroll
+                for (int bb = 0; bb < REP; ++bb) s = fmaf(p[bb], t2f<T>(sVb[tk[bb] * NG + g]), s);
+#pragma unroll
+                for (int m = REP; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+                if (lane < REP) sOB[lane * NG + g] = sOB[lane * NG + g] * alpha + s;
+            }
+        }   // otherwise every p is 0 and alpha is 1
+        // rescale O when some row's running max grew
+        float al[REP];
+        bool rescale = false;
+#pragma unroll
+        for (int r = 0; r < REP; ++r) {
+            al[r] = __shfl_sync(0xffffffffu, alpha, r);
+            rescale |= al[r] != 1.0f;
+        }
+        if (rescale) {
+#pragma unroll
+            for (int r = 0; r < REP; ++r)
+#pragma unroll
+                for (int k = 0; k < S::EPL / 2; ++k) {
+                    O2[r][k].x *= al[r];
+                    O2[r][k].y *= al[r];
+                }
+        }
+        __syncwarp();
+        if (c + 1 < c_end) issue_a(c + 1);   // K / scale / mask buffers are free
+        cp_commit();
+        cp_wait<1>();   // group B of chunk c (V)
+        __syncwarp();
+
+        // ---- values: O += p * (s * code); lane = packed-word slot
+        if (chunk_live && pv_live) {
+#pragma unroll 2
+            for (int ps = 0; ps < 32 / S::TPV; ++ps) {
+                const int t = ps * S::TPV + tv;
+                uint32_t w[S::WPL];
+                load_words<T, S::WPL>(sV + t * WPT + wl * S::WPL, w);
+                const float4 sm = sVS4[t * NG + g_v];
+                const float2 s2 = make_float2(sm.x, sm.y), m2 = make_float2(sm.z, sm.w);
+                const float4 pa = *reinterpret_cast<const float4 *>(sP2 + t * REP);
+                const float4 pc = *reinterpret_cast<const float4 *>(sP2 + t * REP + 2);
+                const float2 pp[REP] = {make_float2(pa.x, pa.y), make_float2(pa.z, pa.w), make_float2(pc.x, pc.y),
+                                        make_float2(pc.z, pc.w)};
+#pragma unroll
+                for (int u = 0; u < S::WPL; ++u) {
+                    const Codes<BITS> cd(w[u]);
+#pragma unroll
+                    for (int k = 0; k < S::PF / 2; ++k) {
+                        const float2 sc = __ffma2_rn(cd.pair(k), s2, m2);
+#pragma unroll
+                        for (int r = 0; r < REP; ++r)
+                            O2[r][u * (S::PF / 2) + k] = __ffma2_rn(pp[r], sc, O2[r][u * (S::PF / 2) + k]);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+        if (c + 1 < c_end) issue_b(c + 1);   // V buffer is free
+        cp_commit();
+    }
+    cp_wait<0>();
+    __syncwarp();
+
+    // ---- lanes that share word slots hold sums over different tokens
+#pragma unroll
+    for (int m = S::LPV; m < 32; m <<= 1)
+#pragma unroll
+        for (int r = 0; r < REP; ++r)
+#pragma unroll
+            for (int k = 0; k < S::EPL / 2; ++k) {
+                O2[r][k].x += __shfl_xor_sync(0xffffffffu, O2[r][k].x, m);
+                O2[r][k].y += __shfl_xor_sync(0xffffffffu, O2[r][k].y, m);
+            }
+    float Mr[REP], Sr[REP];
+#pragma unroll
+    for (int r = 0; r < REP; ++r) {
+        Mr[r] = __shfl_sync(0xffffffffu, M, r);
+        Sr[r] = __shfl_sync(0xffffffffu, Ssum, r);
+    }
+    if (tv == 0 && pv_live) {
+        const int dl = wl * S::EPL;   // first output dimension of the lane
+#pragma unroll
+        for (int r = 0; r < REP; ++r) {
+            if (r >= nrow) break;
+            const int q = q0 + r;
+            const float ob = sOB[r * NG + g_v];
+            if (a.nwg == 1) {
+                float c = 1.0f, sf = Sr[r];
+                if (a.has_sinks) {
+                    const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
+                    const float mf = fmaxf(Mr[r], sk);
+                    c = Mr[r] == -INFINITY ? 0.0f : ex2(Mr[r] - mf);
+                    sf = Sr[r] * c + ex2(sk - mf);
+                }
+                const float f = sf > 0.0f ? c / sf : 0.0f;
+#pragma unroll
+                for (int k = 0; k < S::EPL / 2; ++k) {
+                    st_out<T>(a.out, static_cast<size_t>(q) * dim + dl + 2 * k, (O2[r][k].x + ob) * f, a.out_f32);
+                    st_out<T>(a.out, static_cast<size_t>(q) * dim + dl + 2 * k + 1, (O2[r][k].y + ob) * f, a.out_f32);
+                }
+            } else {
+                float2 *po = reinterpret_cast<float2 *>(a.part_o + (static_cast<size_t>(split) * a.rows + q) * dim + dl);
+#pragma unroll
+                for (int k = 0; k < S::EPL / 2; ++k) po[k] = make_float2(O2[r][k].x + ob, O2[r][k].y + ob);
+            }
+        }
+    }
+    if (a.nwg > 1 && lane < nrow)
+        reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] = make_float2(Ssum, M);
+}
+
+template <int BITS, typename T, int DIMC>
+cudaError_t launch_one(const QuantArgs &a, cudaStream_t s) {
+    auto kern = quant_kernel<BITS, T, DIMC>;
+    const size_t smem = quant_layout(a.wpt, a.ng).total;
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(a.nwg * a.n_rg, a.kv_rows), 32, smem, s>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int BITS, typename T, int DIMC>
+int occupancy_one(size_t smem) {
+    auto kern = quant_kernel<BITS, T, DIMC>;
+    static unsigned long long done = 0;
+    if (set_smem_limit_once(kern, kQuantMaxSmem, &done) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, smem) != cudaSuccess) return 0;
+    return n;
+}
+
+template <int BITS>
+cudaError_t launch_bits(const QuantArgs &a, cudaStream_t s) {
+    const int dimc = quant_dim_capacity(a.dim);
+    if (a.t_is_bf16) {
+        if (dimc == 64) return launch_one<BITS, __nv_bfloat16, 64>(a, s);
+        if (dimc == 128) return launch_one<BITS, __nv_bfloat16, 128>(a, s);
+        if (dimc == 256) return launch_one<BITS, __nv_bfloat16, 256>(a, s);
+        return launch_one<BITS, __nv_bfloat16, 512>(a, s);
+    }
+    if (dimc == 64) return launch_one<BITS, __half, 64>(a, s);
+    if (dimc == 128) return launch_one<BITS, __half, 128>(a, s);
+    if (dimc == 256) return launch_one<BITS, __half, 256>(a, s);
+    return launch_one<BITS, __half, 512>(a, s);
+}
+
+template <int BITS, typename T>
+int occupancy_t(int dimc, size_t smem) {
+    if (dimc == 64) return occupancy_one<BITS, T, 64>(smem);
+    if (dimc == 128) return occupancy_one<BITS, T, 128>(smem);
+    if (dimc == 256) return occupancy_one<BITS, T, 256>(smem);
+    return occupancy_one<BITS, T, 512>(smem);
+}
+
+template <int BITS>
+int occupancy_bits(int dim, int ng) {
+    const int dimc = quant_dim_capacity(dim);
+    const size_t smem = quant_layout(dim * BITS / 32, ng).total;
+    const int a = occupancy_t<BITS, __half>(dimc, smem), b = occupancy_t<BITS, __nv_bfloat16>(dimc, smem);
+    return a < b ? a : b;
+}
+
+}  // namespace quant
+}  // namespace ta

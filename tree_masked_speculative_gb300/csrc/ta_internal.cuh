@@ -111,12 +111,59 @@ struct QuantArgs {
     const uint32_t *mbool;   // [B*nQ, N] or nullptr
     const void *mfloat;      // [B*nQ, N] T or nullptr
     float *part_o;           // [nwg][rows][dim]
-    float *part_ml;          // [nwg][rows][2] = (S, M)
+    float *part_ml;          // [nwg][rows][2] = (S, M), M in log2 units
     void *out;               // [rows, dim] T or f32
-    int rows, nQ, rep, kv_rows, dim, N, bits, G, has_sinks, window, nwg, t_lo, tps;
+    int rows, nQ, rep, kv_rows, dim, N, bits, G, has_sinks, window, nwg;
+    int wpt, ng;             // packed words and scale groups per token
+    int n_rg;                // row groups of kQuantRowsPerCta query rows per KV row
+    int t_lo;                // first token of the window
+    int c_lo, nch;           // first 32-token chunk of the window, chunks per KV row
+    int al_sb;               // scale/bias chunks start on 16-byte boundaries
+    int al_mf;               // float-mask chunks start on 16-byte boundaries
     int t_is_bf16, out_f32;
     float scale;
 };
+
+// Query rows served by one CTA of the quantized-KV kernel (a row group).
+constexpr int kQuantRowsPerCta = 4;
+// Dynamic shared-memory limit requested for the quantized-KV kernels.
+constexpr size_t kQuantMaxSmem = 227 * 1024;
+
+// Per-warp shared-memory layout of the quantized-KV kernel for one 32-token
+// chunk (byte offsets, 16-aligned): packed K and V words, raw scale / bias
+// copies, bool and float mask rows, the scales as {s, s, -2^23 s, -2^23 s},
+// the weights {p, p} per (token, row), the bias accumulators and q-group sums.
+struct QuantLayout {
+    int k, v, ks, kb, vs, vb, mb, mf, ks4, vs4, p2, ob, qs, total;
+};
+__host__ __device__ inline int quant_take(int *o, int bytes) {
+    const int r = *o;
+    *o += (bytes + 15) & ~15;
+    return r;
+}
+__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng) {
+    QuantLayout L;
+    int o = 0;
+    L.k = quant_take(&o, 32 * wpt * 4);
+    L.v = quant_take(&o, 32 * wpt * 4);
+    L.ks = quant_take(&o, 32 * ng * 2);
+    L.kb = quant_take(&o, 32 * ng * 2);
+    L.vs = quant_take(&o, 32 * ng * 2);
+    L.vb = quant_take(&o, 32 * ng * 2);
+    L.mb = quant_take(&o, kQuantRowsPerCta * 32 * 4);
+    L.mf = quant_take(&o, kQuantRowsPerCta * 32 * 2);
+    L.ks4 = quant_take(&o, 32 * ng * 16);
+    L.vs4 = quant_take(&o, 32 * ng * 16);
+    L.p2 = quant_take(&o, 32 * kQuantRowsPerCta * 8);
+    L.ob = quant_take(&o, kQuantRowsPerCta * ng * 4);
+    L.qs = quant_take(&o, kQuantRowsPerCta * ng * 4);
+    L.total = o;
+    return L;
+}
+// Head-dimension capacity of the kernel instance serving `dim` (64..512).
+__host__ __device__ inline int quant_dim_capacity(int dim) {
+    return dim <= 64 ? 64 : (dim <= 128 ? 128 : (dim <= 256 ? 256 : 512));
+}
 
 // Workspace layout inside the caller's tmp buffer (all offsets 256-aligned).
 struct TreeWorkspace {
@@ -134,6 +181,13 @@ void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_quant_fma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_b4(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_b8(const QuantArgs &a, cudaStream_t s);
+// Resident CTAs (warps) per SM of the quantized-KV kernel for (bits, dim,
+// groups per token); 0 if it cannot be determined.
+int quant_ctas_per_sm(int bits, int dim, int ng);
+int quant_ctas_per_sm_b4(int dim, int ng);
+int quant_ctas_per_sm_b8(int dim, int ng);
 
 // Rows of one CTA in the CUDA-core tree kernel.
 constexpr int kFmaRowsPerCta = 16;
