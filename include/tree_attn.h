@@ -200,8 +200,9 @@ ta_status tree_attn_fwd_noalloc(const ta_tree_params *p, const ta_buf *q, const 
 /* Splits quant_sdpa_fwd will use (p->nwg when non-zero); 0 on invalid input. */
 uint32_t quant_sdpa_num_splits(const ta_quant_params *p);
 
-/* Bytes of the `tmp` buffer of quant_sdpa_fwd: B*nQ*nwg*(dim+2)*4, or 0 when
- * one split is used; SIZE_MAX on invalid parameters or overflow. */
+/* Bytes of the `tmp` buffer of quant_sdpa_fwd: 256 (error word region) plus,
+ * with more than one split, B*nQ*nwg*(dim+2)*4 for the split partials;
+ * SIZE_MAX on invalid parameters or overflow. */
 size_t quant_sdpa_tmp_bytes(const ta_quant_params *p);
 
 /*
@@ -216,9 +217,14 @@ size_t quant_sdpa_tmp_bytes(const ta_quant_params *p);
  *             sinks[q % nQ] (not scaled) and value 0, counted once
  *   mask_bool [B*nQ, tokens] u32 or absent: 0 drops the token for that query
  *   mask_float[B*nQ, tokens] T or absent: added to the logit after the gates
- *   tmp       f32, >= quant_sdpa_tmp_bytes(p) bytes (may be absent for 1 split)
+ *   tmp       f32, >= quant_sdpa_tmp_bytes(p) bytes, 16-byte aligned.  Its
+ *             first 32-bit word is an error word: the kernel ORs in 1 when a
+ *             copy of K/V into shared memory did not complete within its
+ *             wait bound (the output is then not valid).  The library never
+ *             clears it; a caller that wants to check it zeroes it first.
  *   out       [B*nQ, dim], dtype T or f32; out = o / l when l > 0, else 0
  * Query q uses KV row q / (nQ / nKV).  Tokens outside the window are not read.
+ * k_packed and v_packed must be 16-byte aligned.
  */
 ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries, const ta_buf *k_packed,
                          const ta_buf *k_scales, const ta_buf *k_biases, const ta_buf *v_packed,

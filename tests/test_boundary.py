@@ -223,8 +223,8 @@ def _quant_call(ta, p, T=None, **over):
 def test_quant_tmp_bytes(ta):
     p = _qp(ta)
     assert ta.quant_sdpa_num_splits(p) == 3
-    assert ta.quant_sdpa_tmp_bytes(p) == 16 * 3 * (128 + 2) * 4
-    assert ta.quant_sdpa_tmp_bytes(_qp(ta, nwg=1)) == 0
+    assert ta.quant_sdpa_tmp_bytes(p) == 256 + 16 * 3 * (128 + 2) * 4
+    assert ta.quant_sdpa_tmp_bytes(_qp(ta, nwg=1)) == 256
 
 
 @pytest.mark.parametrize("kw,st_want,frag", [

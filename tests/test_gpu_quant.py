@@ -69,6 +69,24 @@ def test_quant_no_visible_token_gives_zero_and_sink_only(ta):
     assert_close(got.double().numpy(), oracle.quant_oracle_for(wl, inp))
 
 
+def test_quant_error_word_stays_clear(ta):
+    wl = qwl(N=700, bits=8, dtype="bf16", fmask="alibi", bfrac=0.1, window=300)
+    inp = W.make_quant_inputs(wl)
+    p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits,
+                        wl.group_size, wl.has_sinks, wl.window_size, wl.scale, 0)
+    nb = ta.quant_sdpa_tmp_bytes(p)
+    assert nb >= 256
+    tmp = torch.zeros((nb + 3) // 4, dtype=torch.float32, device="cuda")
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    out = ta.quant_sdpa(d, batch=wl.batch, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads,
+                        dim=wl.dim, tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size,
+                        has_sinks=wl.has_sinks, window_size=wl.window_size, scale=wl.scale,
+                        out_dtype=torch.float32, tmp=tmp)
+    torch.cuda.synchronize()
+    assert int(tmp[:1].view(torch.int32).item()) == 0
+    assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp))
+
+
 def test_quant_split_invariance(ta):
     wl = qwl(N=2000, bits=8, dtype="bf16")
     inp = W.make_quant_inputs(wl)

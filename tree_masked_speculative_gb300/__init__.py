@@ -251,7 +251,7 @@ def quant_sdpa(inputs: dict, *, batch: int, n_q_heads: int, n_kv_heads: int, dim
         nb = quant_sdpa_tmp_bytes(p)
         if nb >= 2 ** 63:
             raise TreeAttentionError(1, "invalid quantized-SDPA parameters")
-        tmp = torch.empty(max(1, (nb + 3) // 4), dtype=torch.float32, device=dev)
+        tmp = torch.zeros(max(1, (nb + 3) // 4), dtype=torch.float32, device=dev)   # error word = 0
     if out is None:
         out = torch.empty((batch * n_q_heads, dim), dtype=out_dtype or inputs["queries"].dtype,
                           device=dev)

@@ -372,11 +372,12 @@ uint32_t window_tokens(const ta_quant_params *p) {
     return p->window_size == 0 ? p->tokens : (p->window_size < p->tokens ? p->window_size : p->tokens);
 }
 
-// 32-token chunks of one KV row inside the window (chunks start at multiples
-// of 32 tokens).
+// Chunks of one KV row inside the window (chunks start at multiples of the
+// kernel instance's chunk length).
 uint32_t quant_chunks(const ta_quant_params *p) {
     const uint32_t t_lo = p->tokens - window_tokens(p);
-    return (p->tokens + 31u) / 32u - t_lo / 32u;
+    const uint32_t c = (uint32_t)quant_chunk_tokens((int)p->dim, (int)p->bits);
+    return (p->tokens + c - 1u) / c - t_lo / c;
 }
 
 uint32_t quant_row_groups(const ta_quant_params *p) {
@@ -401,10 +402,14 @@ uint32_t resolve_quant_nwg(const ta_quant_params *p) {
     return (uint32_t)nwg;
 }
 
+// tmp = [error word region][split partials O (f32) then (S, M) pairs].
 bool quant_tmp(const ta_quant_params *p, uint32_t nwg, uint64_t *bytes) {
-    if (nwg <= 1) { *bytes = 0; return true; }
+    if (nwg <= 1) { *bytes = kQuantErrBytes; return true; }
     const uint64_t rows = (uint64_t)p->batch * p->n_q_heads;
-    return mul4(rows, nwg, (uint64_t)p->dim + 2, 4, bytes);
+    uint64_t part;
+    if (!mul4(rows, nwg, (uint64_t)p->dim + 2, 4, &part)) return false;
+    *bytes = part + kQuantErrBytes;
+    return true;
 }
 
 }  // namespace
@@ -567,10 +572,8 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     if (has_bool) TA_TRY(check_buf(mask_bool, "quant_sdpa: mask_bool", req_mb, 4));
     if (has_float) TA_TRY(check_buf(mask_float, "quant_sdpa: mask_float", req_mf, 2));
     TA_TRY(check_buf(out, "quant_sdpa: out", req_out, out.dtype == TA_F32 ? 4 : 2));
-    if (nwg > 1) {
-        TA_TRY(check_dtype(tmp, "tmp", TA_F32));
-        TA_TRY(check_buf(tmp, "quant_sdpa: tmp", req_tmp, 16));
-    }
+    TA_TRY(check_dtype(tmp, "tmp", TA_F32));
+    TA_TRY(check_buf(tmp, "quant_sdpa: tmp", req_tmp, 16));
 
     QuantArgs a{};
     a.queries = queries.ptr;
@@ -583,8 +586,9 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     a.sinks = p->has_sinks ? static_cast<const float *>(sinks.ptr) : nullptr;
     a.mbool = has_bool ? static_cast<const uint32_t *>(mask_bool.ptr) : nullptr;
     a.mfloat = has_float ? mask_float.ptr : nullptr;
+    a.err = static_cast<int *>(tmp.ptr);
     if (nwg > 1) {
-        a.part_o = static_cast<float *>(tmp.ptr);
+        a.part_o = reinterpret_cast<float *>(static_cast<unsigned char *>(tmp.ptr) + kQuantErrBytes);
         a.part_ml = a.part_o + rows * nwg * p->dim;
     }
     a.out = out.ptr;
@@ -603,11 +607,12 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     a.ng = (int)(p->dim / p->group_size);
     a.n_rg = (int)quant_row_groups(p);
     a.t_lo = (int)(p->tokens - window_tokens(p));
-    a.c_lo = a.t_lo / 32;
+    a.c_lo = a.t_lo / quant_chunk_tokens(a.dim, a.bits);
     a.nch = (int)quant_chunks(p);
     const auto al16 = [](const void *ptr) { return ((uintptr_t)ptr & 15u) == 0; };
     a.al_sb = al16(k_scales.ptr) && al16(k_biases.ptr) && al16(v_scales.ptr) && al16(v_biases.ptr) &&
               ((uint64_t)p->tokens * a.ng * 2) % 16 == 0;
+    a.al_mb = has_bool && al16(mask_bool.ptr) && p->tokens % 4 == 0;
     a.al_mf = has_float && al16(mask_float.ptr) && p->tokens % 8 == 0;
     if ((uint64_t)a.nwg * a.n_rg > (uint64_t)INT_MAX)
         return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: too many splits x row groups");

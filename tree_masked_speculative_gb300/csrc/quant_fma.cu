@@ -23,11 +23,16 @@ __device__ __forceinline__ void store_out(void *p, size_t i, float x, int out_f3
     else reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
 }
 
-// One CTA per query row; the per-split weights are computed once into shared
-// memory (128 splits at a time), then every thread sums its dimensions.
+// One CTA per query row.  Thread t sums the float4 column (t % D4) of the
+// splits w = t / D4 (mod groups) with independent loads; the groups are then
+// added in shared memory.  Launched as a programmatic dependent of the main
+// pass.
+constexpr int kMergeThreads = 256;
+
 template <typename T>
-__global__ void __launch_bounds__(128) quant_merge_kernel(const QuantArgs a) {
-    __shared__ float s_w[128];
+__global__ void __launch_bounds__(kMergeThreads) quant_merge_kernel(const QuantArgs a) {
+    pdl_wait();
+    __shared__ float4 s_acc[kMergeThreads];
     __shared__ float s_red[2];
     const int q = blockIdx.x;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -52,30 +57,38 @@ __global__ void __launch_bounds__(128) quant_merge_kernel(const QuantArgs a) {
     }
     __syncthreads();
     const float mstar = s_red[0], sstar = s_red[1];
-    const float inv = sstar > 0.0f ? 1.0f / sstar : 0.0f;
-    float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};   // dims t, t + 128, t + 256, t + 384
-    for (int w0 = 0; w0 < a.nwg; w0 += 128) {
-        const int n = min(128, a.nwg - w0);
-        __syncthreads();
-        if (t < n) {
-            const float mw = __ldg(&ml[static_cast<size_t>(w0 + t) * a.rows + q].y);
-            s_w[t] = (mw == -INFINITY || mstar == -INFINITY) ? 0.0f : exp2f(mw - mstar);
-        }
-        __syncthreads();
-        for (int j = 0; j < n; ++j) {
-            const float wj = s_w[j];
-            const float *po = a.part_o + (static_cast<size_t>(w0 + j) * a.rows + q) * a.dim;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int d = t + 128 * k;
-                if (d < a.dim) acc[k] = fmaf(__ldg(po + d), wj, acc[k]);
-            }
+    const int D4 = a.dim / 4;
+    const int groups = kMergeThreads / D4;
+    const int g = t / D4, i = t % D4;
+    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (g < groups && mstar != -INFINITY) {
+        const size_t stride = static_cast<size_t>(a.rows) * a.dim;
+        const float *po = a.part_o + static_cast<size_t>(q) * a.dim + 4 * i;
+#pragma unroll 4
+        for (int w = g; w < a.nwg; w += groups) {
+            const float mw = __ldg(&ml[static_cast<size_t>(w) * a.rows + q].y);
+            const float4 o = __ldg(reinterpret_cast<const float4 *>(po + w * stride));
+            const float e = mw == -INFINITY ? 0.0f : exp2f(mw - mstar);
+            acc.x = fmaf(o.x, e, acc.x);
+            acc.y = fmaf(o.y, e, acc.y);
+            acc.z = fmaf(o.z, e, acc.z);
+            acc.w = fmaf(o.w, e, acc.w);
         }
     }
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const int d = t + 128 * k;
-        if (d < a.dim) store_out<T>(a.out, static_cast<size_t>(q) * a.dim + d, acc[k] * inv, a.out_f32);
+    s_acc[t] = acc;
+    __syncthreads();
+    if (t < D4) {
+        float4 r = s_acc[t];
+        for (int k = 1; k < groups; ++k) {
+            const float4 x = s_acc[k * D4 + t];
+            r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
+        }
+        const float inv = sstar > 0.0f ? 1.0f / sstar : 0.0f;
+        const size_t o = static_cast<size_t>(q) * a.dim + 4 * t;
+        store_out<T>(a.out, o + 0, r.x * inv, a.out_f32);
+        store_out<T>(a.out, o + 1, r.y * inv, a.out_f32);
+        store_out<T>(a.out, o + 2, r.z * inv, a.out_f32);
+        store_out<T>(a.out, o + 3, r.w * inv, a.out_f32);
     }
 }
 
@@ -94,10 +107,10 @@ int quant_ctas_per_sm(int bits, int dim, int ng) {
 }
 
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s) {
-    dim3 grid(a.rows);
-    if (a.t_is_bf16) quant_merge_kernel<__nv_bfloat16><<<grid, 128, 0, s>>>(a);
-    else quant_merge_kernel<__half><<<grid, 128, 0, s>>>(a);
+    cudaError_t e = a.t_is_bf16 ? launch_pdl(quant_merge_kernel<__nv_bfloat16>, dim3(a.rows), dim3(kMergeThreads), 0, s, a)
+                                : launch_pdl(quant_merge_kernel<__half>, dim3(a.rows), dim3(kMergeThreads), 0, s, a);
     count_launch();
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 

@@ -14,16 +14,17 @@
 // GB300 design (not the pages' one-simdgroup-per-query token loop):
 //  * one warp = one CTA owns a (KV row, row group of 4 query rows, token
 //    split); the split count fills every SM's resident-warp slots in one wave;
-//  * every 32-token chunk is staged in shared memory by cp.async in two
-//    groups (K words + scales + masks, then V words) so that one chunk's loads
-//    overlap the previous chunk's arithmetic;
+//  * every chunk (32 tokens, or 16 when a token has more than 32 packed
+//    words) is staged in shared memory by TMA bulk copies in two groups (K
+//    words + scales + masks, then V words), each double-buffered and issued
+//    two chunks ahead, completing on mbarriers;
 //  * scores: each lane keeps scale * log2(e) * q for 16 dimensions of the 4
 //    rows in registers (so no shared-memory broadcast of q per dimension),
 //    decodes its part of each token with byte permutes, scales the codes with
 //    one packed FMA (s * (2^23 + c) - 2^23 * s = s * c) and accumulates with
 //    packed f32x2 FMAs; the per-token partial sums of the lanes are combined
 //    by a transposed butterfly (reduce-scatter), which leaves each lane one
-//    (token, row) score per batch; the bias term sum_g b_g * sum_{d in g} q_d
+//    (token, row) score per batch of passes; the bias term sum_g b_g * sum_{d in g} q_d
 //    is added once per (token, row) after the reduction;
 //  * online softmax in log2 units per row; P is kept in shared memory;
 //  * values: lane = packed-word slot; O += p * (s * c) with the same decode
@@ -33,18 +34,24 @@
 
 #include <type_traits>
 
+#include "sm100_ptx.cuh"
 #include "ta_internal.cuh"
 
 namespace ta {
 namespace quant {
 
+using namespace ta::sm100;
+
 constexpr int REP = kQuantRowsPerCta;   // query rows of one row group
 constexpr int DPL = 16;                 // score pass: dimensions per lane (q regs = DPL * REP)
+constexpr uint32_t kWaitPolls = 1u << 22;   // bound of every mbarrier wait
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwo23 = 8388608.0f;   // 2^23: the float whose low mantissa bits hold a code
 
 template <int BITS, int DIMC>
 struct Shape {
+    static constexpr int CH = DIMC * BITS / 32 <= 32 ? 32 : 16;   // tokens per chunk
+    static constexpr int NB = CH * REP / 32;               // score slots (token, row) per lane
     static constexpr int PF = 32 / BITS;                   // codes per packed word
     static constexpr int LPT = DIMC / DPL;                 // score lanes per token (4..32)
     static constexpr int TPP = 32 / LPT;                   // tokens per score pass
@@ -58,6 +65,8 @@ struct Shape {
     static_assert(LPT >= REP && LPT <= 32, "score lanes per token");
     static_assert(B * REP == LPT, "one reduced score per lane per batch");
     static_assert(REP == 4, "the value pass reads the weights of four rows");
+    static_assert(NB * B * TPP == CH && CH % TPV == 0, "chunk tiling");
+    static_assert(CH == 32 || CH == 16, "chunk length");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -66,18 +75,10 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// cp.async of 16 bytes (zero-filled beyond src_bytes) and of 4 bytes.
-__device__ __forceinline__ void cp16(void *dst, const void *src, int src_bytes) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+// Bounded wait of every lane on an mbarrier phase; the result is uniform.
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitPolls));
 }
-__device__ __forceinline__ void cp4(void *dst, const void *src, int src_bytes) {
-    const uint32_t d = static_cast<uint32_t>(__cvta_generic_to_shared(dst));
-    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
-}
-__device__ __forceinline__ void cp_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
 
 template <typename T>
 __device__ __forceinline__ float t2f(uint16_t bits) {
@@ -150,29 +151,24 @@ __device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&w)[WPL]
 template <int BITS, typename T, int DIMC>
 __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const QuantArgs a) {
     using S = Shape<BITS, DIMC>;
-    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int CH = S::CH, NB = S::NB;
+    extern __shared__ __align__(128) unsigned char smem[];
     const int lane = threadIdx.x;
     const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
     const int q0 = kv * a.rep + rg * REP;
     const int nrow = min(REP, a.rep - rg * REP);
     const int N = a.N, WPT = a.wpt, NG = a.ng, G = a.G, dim = a.dim;
-    const QuantLayout L = quant_layout(WPT, NG);
-    uint32_t *sK = reinterpret_cast<uint32_t *>(smem + L.k);
-    uint32_t *sV = reinterpret_cast<uint32_t *>(smem + L.v);
-    uint16_t *sKs = reinterpret_cast<uint16_t *>(smem + L.ks);
-    uint16_t *sKb = reinterpret_cast<uint16_t *>(smem + L.kb);
-    uint16_t *sVs = reinterpret_cast<uint16_t *>(smem + L.vs);
-    uint16_t *sVb = reinterpret_cast<uint16_t *>(smem + L.vb);
-    uint32_t *sMb = reinterpret_cast<uint32_t *>(smem + L.mb);
-    uint16_t *sMf = reinterpret_cast<uint16_t *>(smem + L.mf);
+    const QuantLayout L = quant_layout(WPT, NG, CH);
     float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
     float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
     float2 *sP2 = reinterpret_cast<float2 *>(smem + L.p2);     // [token][row] {p, p}
     float *sOB = reinterpret_cast<float *>(smem + L.ob);       // [row][group] sum_t p * b
     float *sQS = reinterpret_cast<float *>(smem + L.qs);       // [row][group] sum_{d in g} q'
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);   // A stage 0/1, B stage 0/1
 
     const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
     const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
+    const int nc = c_end - c_begin;
 
     // score-pass roles: lane = (token in pass tp, dimension slice j)
     const int tp = lane / S::LPT, j = lane % S::LPT;
@@ -185,6 +181,88 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     const int tv = lane / S::LPV, wl = lane % S::LPV;
     const bool pv_live = wl * S::WPL < WPT;
     const int g_v = pv_live ? (wl * S::WPL * S::PF) / G : 0;
+
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    // ---- chunk staging: lane 0 issues the bulk copies; tail chunks and
+    // unaligned rows are filled by all lanes with plain loads (zero beyond N)
+    auto fill_sb = [&](uint16_t *dst, const void *src_v, size_t e0, int valid_e) {
+        const uint16_t *src = static_cast<const uint16_t *>(src_v) + e0;
+        for (int e = lane; e < CH * NG; e += 32) dst[e] = e < valid_e ? src[e] : static_cast<uint16_t>(0);
+    };
+    auto issue_a = [&](int c, int b) {
+        unsigned char *st = smem + L.a0 + b * L.a_stage;
+        const int t0 = c * CH, tval = min(CH, N - t0);
+        const bool full = tval == CH;
+        const size_t tok0 = static_cast<size_t>(kv) * N + t0;
+        const bool sb_bulk = a.al_sb && full;
+        const bool mb_bulk = a.mbool != nullptr && a.al_mb && full;
+        const bool mf_bulk = a.mfloat != nullptr && a.al_mf && full;
+        if (!sb_bulk) {
+            fill_sb(reinterpret_cast<uint16_t *>(st + L.ks), a.ks, tok0 * NG, tval * NG);
+            fill_sb(reinterpret_cast<uint16_t *>(st + L.kb), a.kb, tok0 * NG, tval * NG);
+            fill_sb(reinterpret_cast<uint16_t *>(st + L.vs), a.vs, tok0 * NG, tval * NG);
+            fill_sb(reinterpret_cast<uint16_t *>(st + L.vb), a.vb, tok0 * NG, tval * NG);
+        }
+        if (a.mbool != nullptr && !mb_bulk) {
+            uint32_t *dst = reinterpret_cast<uint32_t *>(st + L.mb);
+            for (int i = lane; i < REP * CH; i += 32) {
+                const int r = i / CH, t = i % CH;
+                dst[i] = (r < nrow && t < tval) ? a.mbool[static_cast<size_t>(q0 + r) * N + t0 + t] : 0u;
+            }
+        }
+        if (a.mfloat != nullptr && !mf_bulk) {
+            const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
+            uint16_t *dst = reinterpret_cast<uint16_t *>(st + L.mf);
+            for (int i = lane; i < REP * CH; i += 32) {
+                const int r = i / CH, t = i % CH;
+                dst[i] = (r < nrow && t < tval) ? mf[static_cast<size_t>(q0 + r) * N + t0 + t] : static_cast<uint16_t>(0);
+            }
+        }
+        if (lane == 0) {
+            const uint32_t kbytes = static_cast<uint32_t>(tval * WPT * 4);
+            const uint32_t sbytes = static_cast<uint32_t>(CH * NG * 2);
+            uint32_t total = kbytes;
+            if (sb_bulk) total += 4 * sbytes;
+            if (mb_bulk) total += static_cast<uint32_t>(nrow * CH * 4);
+            if (mf_bulk) total += static_cast<uint32_t>(nrow * CH * 2);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[b], total);
+            bulk_load(st + L.k, a.kp + tok0 * WPT, kbytes, &bars[b]);
+            if (sb_bulk) {
+                const size_t e0 = tok0 * NG;
+                bulk_load(st + L.ks, static_cast<const uint16_t *>(a.ks) + e0, sbytes, &bars[b]);
+                bulk_load(st + L.kb, static_cast<const uint16_t *>(a.kb) + e0, sbytes, &bars[b]);
+                bulk_load(st + L.vs, static_cast<const uint16_t *>(a.vs) + e0, sbytes, &bars[b]);
+                bulk_load(st + L.vb, static_cast<const uint16_t *>(a.vb) + e0, sbytes, &bars[b]);
+            }
+            if (mb_bulk)
+                for (int r = 0; r < nrow; ++r)
+                    bulk_load(st + L.mb + r * CH * 4, a.mbool + static_cast<size_t>(q0 + r) * N + t0, CH * 4, &bars[b]);
+            if (mf_bulk)
+                for (int r = 0; r < nrow; ++r)
+                    bulk_load(st + L.mf + r * CH * 2,
+                              static_cast<const uint16_t *>(a.mfloat) + static_cast<size_t>(q0 + r) * N + t0, CH * 2,
+                              &bars[b]);
+        }
+    };
+    auto issue_b = [&](int c, int b) {
+        if (lane == 0) {
+            const int t0 = c * CH, tval = min(CH, N - t0);
+            const uint32_t bytes = static_cast<uint32_t>(tval * WPT * 4);
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bars[2 + b], bytes);
+            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, bytes, &bars[2 + b]);
+        }
+    };
+    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
+    for (; a_issued < 2 && a_issued < nc; ++a_issued) issue_a(c_begin + a_issued, a_issued & 1);
+    for (; b_issued < 2 && b_issued < nc; ++b_issued) issue_b(c_begin + b_issued, b_issued & 1);
 
     // q' = scale * log2(e) * q for the lane's 16 dimensions of every row
     const float qscale = a.scale * kLog2e;
@@ -227,64 +305,6 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
         __syncwarp();
     }
 
-    // ---- chunk staging
-    auto copy_sb = [&](uint16_t *dst, const void *src_v, size_t e0, int valid_e) {
-        const uint16_t *src = static_cast<const uint16_t *>(src_v) + e0;
-        const int E = 32 * NG;
-        if (a.al_sb) {
-            for (int p = lane; p < E / 8; p += 32) {
-                const int b = min(16, max(0, (valid_e - 8 * p) * 2));
-                cp16(dst + 8 * p, b > 0 ? src + 8 * p : src, b);
-            }
-        } else {
-            for (int e = lane; e < E; e += 32) dst[e] = e < valid_e ? src[e] : static_cast<uint16_t>(0);
-        }
-    };
-    auto issue_a = [&](int c) {
-        const int t0 = c * 32;
-        const int tval = min(32, N - t0);
-        const uint32_t *kg = a.kp + (static_cast<size_t>(kv) * N + t0) * WPT;
-        const int kvalid = tval * WPT / 4;
-        for (int p = lane; p < 8 * WPT; p += 32) cp16(sK + 4 * p, p < kvalid ? kg + 4 * p : kg, p < kvalid ? 16 : 0);
-        const size_t e0 = (static_cast<size_t>(kv) * N + t0) * NG;
-        copy_sb(sKs, a.ks, e0, tval * NG);
-        copy_sb(sKb, a.kb, e0, tval * NG);
-        copy_sb(sVs, a.vs, e0, tval * NG);
-        copy_sb(sVb, a.vb, e0, tval * NG);
-        if (a.mbool != nullptr) {
-#pragma unroll
-            for (int r = 0; r < REP; ++r) {
-                const bool ok = r < nrow && lane < tval;
-                const uint32_t *src = a.mbool + static_cast<size_t>(q0 + (r < nrow ? r : 0)) * N + t0;
-                cp4(sMb + r * 32 + lane, ok ? src + lane : src, ok ? 4 : 0);
-            }
-        }
-        if (a.mfloat != nullptr) {
-            const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
-            if (a.al_mf) {
-                if (lane < 4 * REP) {
-                    const int r = lane / 4, p = lane % 4;
-                    const uint16_t *src = mf + static_cast<size_t>(q0 + (r < nrow ? r : 0)) * N + t0;
-                    const int b = r < nrow ? min(16, max(0, (tval - 8 * p) * 2)) : 0;
-                    cp16(sMf + r * 32 + 8 * p, b > 0 ? src + 8 * p : src, b);
-                }
-            } else {
-#pragma unroll
-                for (int r = 0; r < REP; ++r) {
-                    const bool ok = r < nrow && lane < tval;
-                    sMf[r * 32 + lane] = ok ? mf[static_cast<size_t>(q0 + r) * N + t0 + lane] : static_cast<uint16_t>(0);
-                }
-            }
-        }
-    };
-    auto issue_b = [&](int c) {
-        const int t0 = c * 32;
-        const int tval = min(32, N - t0);
-        const uint32_t *vg = a.vp + (static_cast<size_t>(kv) * N + t0) * WPT;
-        const int vvalid = tval * WPT / 4;
-        for (int p = lane; p < 8 * WPT; p += 32) cp16(sV + 4 * p, p < vvalid ? vg + 4 * p : vg, p < vvalid ? 16 : 0);
-    };
-
     float M = -INFINITY, Ssum = 0.0f;   // online-softmax state of row r_l (log2 units)
     float2 O2[REP][S::EPL / 2];
 #pragma unroll
@@ -292,44 +312,52 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
 #pragma unroll
         for (int k = 0; k < S::EPL / 2; ++k) O2[r][k] = make_float2(0.0f, 0.0f);
 
-    if (c_begin < c_end) issue_a(c_begin);
-    cp_commit();
-    if (c_begin < c_end) issue_b(c_begin);
-    cp_commit();
-
-    for (int c = c_begin; c < c_end; ++c) {
-        cp_wait<1>();   // group A of chunk c (K, scales, masks)
+    bool ok = true;
+    for (int i = 0; i < nc; ++i) {
+        const int c = c_begin + i, b = i & 1;
+        const uint32_t par = static_cast<uint32_t>(i >> 1) & 1u;
+        if (!wait_warp(&bars[b], par)) { ok = false; break; }   // group A of chunk c
+        ++a_done;
         __syncwarp();
-        const int t0 = c * 32;
-        for (int idx = lane; idx < 32 * NG; idx += 32) {
+        const unsigned char *st = smem + L.a0 + b * L.a_stage;
+        const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
+        const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + L.ks);
+        const uint16_t *sKb = reinterpret_cast<const uint16_t *>(st + L.kb);
+        const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + L.vs);
+        const uint16_t *sVb = reinterpret_cast<const uint16_t *>(st + L.vb);
+        const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
+        const uint16_t *sMf = reinterpret_cast<const uint16_t *>(st + L.mf);
+        const uint32_t *sV = reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage);
+        const int t0 = c * CH;
+        for (int idx = lane; idx < CH * NG; idx += 32) {
             const float s = t2f<T>(sKs[idx]);
             sKS4[idx] = make_float4(s, s, -kTwo23 * s, -kTwo23 * s);
             const float sv = t2f<T>(sVs[idx]);
             sVS4[idx] = make_float4(sv, sv, -kTwo23 * sv, -kTwo23 * sv);
         }
         // gates of the lane's (token, row) score slots
-        bool live[REP];
-        int tk[REP];
+        bool live[NB];
+        int tk[NB];
         bool any = false;
 #pragma unroll
-        for (int bb = 0; bb < REP; ++bb) {
+        for (int bb = 0; bb < NB; ++bb) {
             tk[bb] = (bb * S::B + pb_l) * S::TPP + tp;
             const int t = t0 + tk[bb];
             bool g = r_l < nrow && t >= a.t_lo && t < N;
-            if (g && a.mbool != nullptr) g = sMb[r_l * 32 + tk[bb]] != 0u;
+            if (g && a.mbool != nullptr) g = sMb[r_l * CH + tk[bb]] != 0u;
             live[bb] = g;
             any |= g;
         }
         __syncwarp();
         const bool chunk_live = __any_sync(0xffffffffu, any);
 
-        float lg[REP];
+        float lg[NB];
 #pragma unroll
-        for (int bb = 0; bb < REP; ++bb) lg[bb] = -INFINITY;
+        for (int bb = 0; bb < NB; ++bb) lg[bb] = -INFINITY;
         if (chunk_live) {
             // ---- scores: partial dot products, reduce-scattered over the token's lanes
 #pragma unroll
-            for (int bb = 0; bb < REP; ++bb) {
+            for (int bb = 0; bb < NB; ++bb) {
                 float v[S::B * REP];
 #pragma unroll
                 for (int pb = 0; pb < S::B; ++pb) {
@@ -363,7 +391,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
                     float bias = 0.0f;
                     for (int g = 0; g < NG; ++g) bias = fmaf(t2f<T>(sKb[tk[bb] * NG + g]), sQS[r_l * NG + g], bias);
                     float fm = 0.0f;
-                    if (a.mfloat != nullptr) fm = kLog2e * t2f<T>(sMf[r_l * 32 + tk[bb]]);
+                    if (a.mfloat != nullptr) fm = kLog2e * t2f<T>(sMf[r_l * CH + tk[bb]]);
                     lg[bb] = dot + bias + fm;
                 }
             }
@@ -372,35 +400,35 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
         // ---- online softmax of row r_l over the chunk (log2 units)
         float cmax = lg[0];
 #pragma unroll
-        for (int bb = 1; bb < REP; ++bb) cmax = fmaxf(cmax, lg[bb]);
+        for (int bb = 1; bb < NB; ++bb) cmax = fmaxf(cmax, lg[bb]);
 #pragma unroll
         for (int m = REP; m < 32; m <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, m));
         const float m_new = fmaxf(M, cmax);
         float alpha = 1.0f;
-        float p[REP];
+        float p[NB];
         if (m_new == -INFINITY) {
 #pragma unroll
-            for (int bb = 0; bb < REP; ++bb) p[bb] = 0.0f;
+            for (int bb = 0; bb < NB; ++bb) p[bb] = 0.0f;
         } else {
             alpha = ex2(M - m_new);   // 0 while M = -inf
 #pragma unroll
-            for (int bb = 0; bb < REP; ++bb) p[bb] = ex2(lg[bb] - m_new);
+            for (int bb = 0; bb < NB; ++bb) p[bb] = ex2(lg[bb] - m_new);
         }
         float psum = 0.0f;
 #pragma unroll
-        for (int bb = 0; bb < REP; ++bb) psum += p[bb];
+        for (int bb = 0; bb < NB; ++bb) psum += p[bb];
 #pragma unroll
         for (int m = REP; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
         Ssum = Ssum * alpha + psum;
         M = m_new;
 #pragma unroll
-        for (int bb = 0; bb < REP; ++bb) sP2[tk[bb] * REP + r_l] = make_float2(p[bb], p[bb]);
+        for (int bb = 0; bb < NB; ++bb) sP2[tk[bb] * REP + r_l] = make_float2(p[bb], p[bb]);
         // bias part of O: sum_t p_t * b_{t,g} per (row, group)
         if (chunk_live) {
             for (int g = 0; g < NG; ++g) {
                 float s = 0.0f;
 #pragma unroll
-                for (int bb = 0; bb < REP; ++bb) s = fmaf(p[bb], t2f<T>(sVb[tk[bb] * NG + g]), s);
+                for (int bb = 0; bb < NB; ++bb) s = fmaf(p[bb], t2f<T>(sVb[tk[bb] * NG + g]), s);
 #pragma unroll
                 for (int m = REP; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
                 if (lane < REP) sOB[lane * NG + g] = sOB[lane * NG + g] * alpha + s;
@@ -424,15 +452,15 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
                 }
         }
         __syncwarp();
-        if (c + 1 < c_end) issue_a(c + 1);   // K / scale / mask buffers are free
-        cp_commit();
-        cp_wait<1>();   // group B of chunk c (V)
+        if (a_issued < nc) { issue_a(c_begin + a_issued, a_issued & 1); ++a_issued; }   // stage b is free
+        if (!wait_warp(&bars[2 + b], par)) { ok = false; break; }   // group B of chunk c
+        ++b_done;
         __syncwarp();
 
         // ---- values: O += p * (s * code); lane = packed-word slot
         if (chunk_live && pv_live) {
 #pragma unroll 2
-            for (int ps = 0; ps < 32 / S::TPV; ++ps) {
+            for (int ps = 0; ps < CH / S::TPV; ++ps) {
                 const int t = ps * S::TPV + tv;
                 uint32_t w[S::WPL];
                 load_words<T, S::WPL>(sV + t * WPT + wl * S::WPL, w);
@@ -456,11 +484,16 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
             }
         }
         __syncwarp();
-        if (c + 1 < c_end) issue_b(c + 1);   // V buffer is free
-        cp_commit();
+        if (b_issued < nc) { issue_b(c_begin + b_issued, b_issued & 1); ++b_issued; }
     }
-    cp_wait<0>();
-    __syncwarp();
+    pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
+    if (!ok) {
+        // a copy never completed: report it, let the issued copies land (bounded) and leave
+        if (lane == 0 && a.err != nullptr) atomicOr(a.err, 1);
+        for (; a_done < a_issued; ++a_done) wait_warp(&bars[a_done & 1], static_cast<uint32_t>(a_done >> 1) & 1u);
+        for (; b_done < b_issued; ++b_done) wait_warp(&bars[2 + (b_done & 1)], static_cast<uint32_t>(b_done >> 1) & 1u);
+        return;
+    }
 
     // ---- lanes that share word slots hold sums over different tokens
 #pragma unroll
@@ -513,7 +546,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
 template <int BITS, typename T, int DIMC>
 cudaError_t launch_one(const QuantArgs &a, cudaStream_t s) {
     auto kern = quant_kernel<BITS, T, DIMC>;
-    const size_t smem = quant_layout(a.wpt, a.ng).total;
+    const size_t smem = quant_layout(a.wpt, a.ng, Shape<BITS, DIMC>::CH).total;
     static unsigned long long done = 0;
     cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
     if (e != cudaSuccess) return e;
@@ -558,7 +591,7 @@ int occupancy_t(int dimc, size_t smem) {
 template <int BITS>
 int occupancy_bits(int dim, int ng) {
     const int dimc = quant_dim_capacity(dim);
-    const size_t smem = quant_layout(dim * BITS / 32, ng).total;
+    const size_t smem = quant_layout(dim * BITS / 32, ng, quant_chunk_tokens(dim, BITS)).total;
     const int a = occupancy_t<BITS, __half>(dimc, smem), b = occupancy_t<BITS, __nv_bfloat16>(dimc, smem);
     return a < b ? a : b;
 }

@@ -117,9 +117,11 @@ struct QuantArgs {
     int wpt, ng;             // packed words and scale groups per token
     int n_rg;                // row groups of kQuantRowsPerCta query rows per KV row
     int t_lo;                // first token of the window
-    int c_lo, nch;           // first 32-token chunk of the window, chunks per KV row
+    int c_lo, nch;           // first chunk of the window, chunks per KV row
     int al_sb;               // scale/bias chunks start on 16-byte boundaries
+    int al_mb;               // bool-mask chunks start on 16-byte boundaries
     int al_mf;               // float-mask chunks start on 16-byte boundaries
+    int *err;                // error word (bit 0: a copy wait timed out), never cleared here
     int t_is_bf16, out_f32;
     float scale;
 };
@@ -128,41 +130,58 @@ struct QuantArgs {
 constexpr int kQuantRowsPerCta = 4;
 // Dynamic shared-memory limit requested for the quantized-KV kernels.
 constexpr size_t kQuantMaxSmem = 227 * 1024;
+// Bytes at the start of the quantized path's tmp buffer holding its error
+// word (the split partials follow).
+constexpr size_t kQuantErrBytes = 256;
 
-// Per-warp shared-memory layout of the quantized-KV kernel for one 32-token
-// chunk (byte offsets, 16-aligned): packed K and V words, raw scale / bias
-// copies, bool and float mask rows, the scales as {s, s, -2^23 s, -2^23 s},
-// the weights {p, p} per (token, row), the bias accumulators and q-group sums.
+// Per-warp shared-memory layout of the quantized-KV kernel (byte offsets,
+// 16-aligned).  Group A of a chunk (packed K words, raw scale / bias copies,
+// bool and float mask rows) and group B (packed V words) are double-buffered;
+// then the scales as {s, s, -2^23 s, -2^23 s}, the weights {p, p} per
+// (token, row), the bias accumulators, the q-group sums and four mbarriers.
 struct QuantLayout {
-    int k, v, ks, kb, vs, vb, mb, mf, ks4, vs4, p2, ob, qs, total;
+    int a0, a_stage;                    // group-A stage b at a0 + b * a_stage
+    int k, ks, kb, vs, vb, mb, mf;      // offsets inside a group-A stage
+    int v0, v_stage;                    // group-B stage b at v0 + b * v_stage
+    int ks4, vs4, p2, ob, qs, bars, total;
 };
 __host__ __device__ inline int quant_take(int *o, int bytes) {
     const int r = *o;
     *o += (bytes + 15) & ~15;
     return r;
 }
-__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng) {
+__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
+    constexpr int R = kQuantRowsPerCta;
     QuantLayout L;
-    int o = 0;
-    L.k = quant_take(&o, 32 * wpt * 4);
-    L.v = quant_take(&o, 32 * wpt * 4);
-    L.ks = quant_take(&o, 32 * ng * 2);
-    L.kb = quant_take(&o, 32 * ng * 2);
-    L.vs = quant_take(&o, 32 * ng * 2);
-    L.vb = quant_take(&o, 32 * ng * 2);
-    L.mb = quant_take(&o, kQuantRowsPerCta * 32 * 4);
-    L.mf = quant_take(&o, kQuantRowsPerCta * 32 * 2);
-    L.ks4 = quant_take(&o, 32 * ng * 16);
-    L.vs4 = quant_take(&o, 32 * ng * 16);
-    L.p2 = quant_take(&o, 32 * kQuantRowsPerCta * 8);
-    L.ob = quant_take(&o, kQuantRowsPerCta * ng * 4);
-    L.qs = quant_take(&o, kQuantRowsPerCta * ng * 4);
+    int o = 0;   // inside a group-A stage
+    L.k = quant_take(&o, ch * wpt * 4);
+    L.ks = quant_take(&o, ch * ng * 2);
+    L.kb = quant_take(&o, ch * ng * 2);
+    L.vs = quant_take(&o, ch * ng * 2);
+    L.vb = quant_take(&o, ch * ng * 2);
+    L.mb = quant_take(&o, R * ch * 4);
+    L.mf = quant_take(&o, R * ch * 2);
+    L.a_stage = o;
+    o = 0;
+    L.a0 = quant_take(&o, 2 * L.a_stage);
+    L.v_stage = (ch * wpt * 4 + 15) & ~15;
+    L.v0 = quant_take(&o, 2 * L.v_stage);
+    L.ks4 = quant_take(&o, ch * ng * 16);
+    L.vs4 = quant_take(&o, ch * ng * 16);
+    L.p2 = quant_take(&o, (ch > 32 ? ch : 32) * R * 8);   // also holds [row][32] q sums
+    L.ob = quant_take(&o, R * ng * 4);
+    L.qs = quant_take(&o, R * ng * 4);
+    L.bars = quant_take(&o, 4 * 8);
     L.total = o;
     return L;
 }
-// Head-dimension capacity of the kernel instance serving `dim` (64..512).
+// Head-dimension capacity of the kernel instance serving `dim` (64..512), and
+// its chunk length in tokens (32 when a token has at most 32 packed words).
 __host__ __device__ inline int quant_dim_capacity(int dim) {
     return dim <= 64 ? 64 : (dim <= 128 ? 128 : (dim <= 256 ? 256 : 512));
+}
+__host__ __device__ inline int quant_chunk_tokens(int dim, int bits) {
+    return quant_dim_capacity(dim) * bits / 32 <= 32 ? 32 : 16;
 }
 
 // Workspace layout inside the caller's tmp buffer (all offsets 256-aligned).
