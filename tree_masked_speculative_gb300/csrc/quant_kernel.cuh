@@ -148,7 +148,10 @@ __device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&w)[WPL]
     }
 }
 
-template <int BITS, typename T, int DIMC>
+// GC > 0: exact-shape instance (dim == DIMC, group size GC, both compile-time
+// so that shared-memory addressing folds into immediates); GC == 0: any
+// dim <= DIMC and group size, read at run time.
+template <int BITS, typename T, int DIMC, int GC>
 __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const QuantArgs a) {
     using S = Shape<BITS, DIMC>;
     constexpr int CH = S::CH, NB = S::NB;
@@ -157,7 +160,11 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
     const int q0 = kv * a.rep + rg * REP;
     const int nrow = min(REP, a.rep - rg * REP);
-    const int N = a.N, WPT = a.wpt, NG = a.ng, G = a.G, dim = a.dim;
+    const int N = a.N;
+    const int WPT = GC > 0 ? DIMC * BITS / 32 : a.wpt;
+    const int NG = GC > 0 ? DIMC / (GC > 0 ? GC : 1) : a.ng;
+    const int G = GC > 0 ? GC : a.G;
+    const int dim = GC > 0 ? DIMC : a.dim;
     const QuantLayout L = quant_layout(WPT, NG, CH);
     float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
     float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
@@ -459,7 +466,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
 
         // ---- values: O += p * (s * code); lane = packed-word slot
         if (chunk_live && pv_live) {
-#pragma unroll 2
+#pragma unroll 4
             for (int ps = 0; ps < CH / S::TPV; ++ps) {
                 const int t = ps * S::TPV + tv;
                 uint32_t w[S::WPL];
@@ -543,9 +550,9 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
         reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] = make_float2(Ssum, M);
 }
 
-template <int BITS, typename T, int DIMC>
+template <int BITS, typename T, int DIMC, int GC>
 cudaError_t launch_one(const QuantArgs &a, cudaStream_t s) {
-    auto kern = quant_kernel<BITS, T, DIMC>;
+    auto kern = quant_kernel<BITS, T, DIMC, GC>;
     const size_t smem = quant_layout(a.wpt, a.ng, Shape<BITS, DIMC>::CH).total;
     static unsigned long long done = 0;
     cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
@@ -555,9 +562,9 @@ cudaError_t launch_one(const QuantArgs &a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-template <int BITS, typename T, int DIMC>
+template <int BITS, typename T, int DIMC, int GC>
 int occupancy_one(size_t smem) {
-    auto kern = quant_kernel<BITS, T, DIMC>;
+    auto kern = quant_kernel<BITS, T, DIMC, GC>;
     static unsigned long long done = 0;
     if (set_smem_limit_once(kern, kQuantMaxSmem, &done) != cudaSuccess) return 0;
     int n = 0;
@@ -565,34 +572,48 @@ int occupancy_one(size_t smem) {
     return n;
 }
 
-template <int BITS>
-cudaError_t launch_bits(const QuantArgs &a, cudaStream_t s) {
-    const int dimc = quant_dim_capacity(a.dim);
-    if (a.t_is_bf16) {
-        if (dimc == 64) return launch_one<BITS, __nv_bfloat16, 64>(a, s);
-        if (dimc == 128) return launch_one<BITS, __nv_bfloat16, 128>(a, s);
-        if (dimc == 256) return launch_one<BITS, __nv_bfloat16, 256>(a, s);
-        return launch_one<BITS, __nv_bfloat16, 512>(a, s);
-    }
-    if (dimc == 64) return launch_one<BITS, __half, 64>(a, s);
-    if (dimc == 128) return launch_one<BITS, __half, 128>(a, s);
-    if (dimc == 256) return launch_one<BITS, __half, 256>(a, s);
-    return launch_one<BITS, __half, 512>(a, s);
+// Exact-shape instances exist for group size 64 at every capacity.
+inline bool quant_exact(int dim, int G) { return G == 64 && dim == quant_dim_capacity(dim); }
+
+template <int BITS, typename T, int DIMC>
+cudaError_t launch_dimc(const QuantArgs &a, cudaStream_t s) {
+    if (quant_exact(a.dim, a.G)) return launch_one<BITS, T, DIMC, 64>(a, s);
+    return launch_one<BITS, T, DIMC, 0>(a, s);
 }
 
 template <int BITS, typename T>
-int occupancy_t(int dimc, size_t smem) {
-    if (dimc == 64) return occupancy_one<BITS, T, 64>(smem);
-    if (dimc == 128) return occupancy_one<BITS, T, 128>(smem);
-    if (dimc == 256) return occupancy_one<BITS, T, 256>(smem);
-    return occupancy_one<BITS, T, 512>(smem);
+cudaError_t launch_t(const QuantArgs &a, cudaStream_t s) {
+    const int dimc = quant_dim_capacity(a.dim);
+    if (dimc == 64) return launch_dimc<BITS, T, 64>(a, s);
+    if (dimc == 128) return launch_dimc<BITS, T, 128>(a, s);
+    if (dimc == 256) return launch_dimc<BITS, T, 256>(a, s);
+    return launch_dimc<BITS, T, 512>(a, s);
+}
+
+template <int BITS>
+cudaError_t launch_bits(const QuantArgs &a, cudaStream_t s) {
+    return a.t_is_bf16 ? launch_t<BITS, __nv_bfloat16>(a, s) : launch_t<BITS, __half>(a, s);
+}
+
+template <int BITS, typename T, int DIMC>
+int occupancy_dimc(bool exact, size_t smem) {
+    return exact ? occupancy_one<BITS, T, DIMC, 64>(smem) : occupancy_one<BITS, T, DIMC, 0>(smem);
+}
+
+template <int BITS, typename T>
+int occupancy_t(int dimc, bool exact, size_t smem) {
+    if (dimc == 64) return occupancy_dimc<BITS, T, 64>(exact, smem);
+    if (dimc == 128) return occupancy_dimc<BITS, T, 128>(exact, smem);
+    if (dimc == 256) return occupancy_dimc<BITS, T, 256>(exact, smem);
+    return occupancy_dimc<BITS, T, 512>(exact, smem);
 }
 
 template <int BITS>
 int occupancy_bits(int dim, int ng) {
     const int dimc = quant_dim_capacity(dim);
+    const bool exact = quant_exact(dim, dim / ng);
     const size_t smem = quant_layout(dim * BITS / 32, ng, quant_chunk_tokens(dim, BITS)).total;
-    const int a = occupancy_t<BITS, __half>(dimc, smem), b = occupancy_t<BITS, __nv_bfloat16>(dimc, smem);
+    const int a = occupancy_t<BITS, __half>(dimc, exact, smem), b = occupancy_t<BITS, __nv_bfloat16>(dimc, exact, smem);
     return a < b ? a : b;
 }
 
