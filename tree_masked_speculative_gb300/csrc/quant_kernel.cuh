@@ -45,6 +45,7 @@ using namespace ta::sm100;
 constexpr int REP = kQuantRowsPerCta;   // query rows of one row group
 constexpr int DPL = 16;                 // score pass: dimensions per lane (q regs = DPL * REP)
 constexpr uint32_t kWaitPolls = 1u << 22;   // bound of every mbarrier wait
+constexpr float kSlack = 8.0f;              // lazy-max slack (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwo23 = 8388608.0f;   // 2^23: the float whose low mantissa bits hold a code
 
@@ -169,7 +170,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
     float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
     float2 *sP2 = reinterpret_cast<float2 *>(smem + L.p2);     // [token][row] {p, p}
-    float *sOB = reinterpret_cast<float *>(smem + L.ob);       // [row][group] sum_t p * b
+    float *sOBl = reinterpret_cast<float *>(smem + L.ob);      // [group][lane] sum_t p * b (lane's slots)
     float *sQS = reinterpret_cast<float *>(smem + L.qs);       // [row][group] sum_{d in g} q'
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);   // A stage 0/1, B stage 0/1
 
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
             for (int jj = g * lpg; jj < (g + 1) * lpg; ++jj) s += sQP[r * S::LPT + jj];
             sQS[idx] = s;
         }
-        for (int idx = lane; idx < REP * NG; idx += 32) sOB[idx] = 0.0f;
+        for (int idx = lane; idx < 32 * NG; idx += 32) sOBl[idx] = 0.0f;
         __syncwarp();
     }
 
@@ -404,52 +405,27 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
             }
         }
 
-        // ---- online softmax of row r_l over the chunk (log2 units)
-        float cmax = lg[0];
+        // ---- online softmax of row r_l (log2 units).  The running max M only
+        // moves when a score exceeds it by more than kSlack (then every row is
+        // rescaled); otherwise the weights 2^(s - M) <= 2^kSlack are used as
+        // they are.  S and the V-bias sums stay per lane until the end.
+        bool grow = false;
 #pragma unroll
-        for (int bb = 1; bb < NB; ++bb) cmax = fmaxf(cmax, lg[bb]);
+        for (int bb = 0; bb < NB; ++bb) grow |= lg[bb] > M + kSlack;
+        if (__any_sync(0xffffffffu, grow)) {
+            float cmax = lg[0];
 #pragma unroll
-        for (int m = REP; m < 32; m <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, m));
-        const float m_new = fmaxf(M, cmax);
-        float alpha = 1.0f;
-        float p[NB];
-        if (m_new == -INFINITY) {
+            for (int bb = 1; bb < NB; ++bb) cmax = fmaxf(cmax, lg[bb]);
 #pragma unroll
-            for (int bb = 0; bb < NB; ++bb) p[bb] = 0.0f;
-        } else {
-            alpha = ex2(M - m_new);   // 0 while M = -inf
+            for (int m = REP; m < 32; m <<= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, m));
+            const float m_new = fmaxf(M, cmax);
+            const float alpha = m_new == M ? 1.0f : ex2(M - m_new);   // 0 while M = -inf
+            M = m_new;
+            Ssum *= alpha;
+            for (int g = 0; g < NG; ++g) sOBl[g * 32 + lane] *= alpha;
+            float al[REP];
 #pragma unroll
-            for (int bb = 0; bb < NB; ++bb) p[bb] = ex2(lg[bb] - m_new);
-        }
-        float psum = 0.0f;
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) psum += p[bb];
-#pragma unroll
-        for (int m = REP; m < 32; m <<= 1) psum += __shfl_xor_sync(0xffffffffu, psum, m);
-        Ssum = Ssum * alpha + psum;
-        M = m_new;
-#pragma unroll
-        for (int bb = 0; bb < NB; ++bb) sP2[tk[bb] * REP + r_l] = make_float2(p[bb], p[bb]);
-        // bias part of O: sum_t p_t * b_{t,g} per (row, group)
-        if (chunk_live) {
-            for (int g = 0; g < NG; ++g) {
-                float s = 0.0f;
-#pragma unroll
-                for (int bb = 0; bb < NB; ++bb) s = fmaf(p[bb], t2f<T>(sVb[tk[bb] * NG + g]), s);
-#pragma unroll
-                for (int m = REP; m < 32; m <<= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
-                if (lane < REP) sOB[lane * NG + g] = sOB[lane * NG + g] * alpha + s;
-            }
-        }   // otherwise every p is 0 and alpha is 1
-        // rescale O when some row's running max grew
-        float al[REP];
-        bool rescale = false;
-#pragma unroll
-        for (int r = 0; r < REP; ++r) {
-            al[r] = __shfl_sync(0xffffffffu, alpha, r);
-            rescale |= al[r] != 1.0f;
-        }
-        if (rescale) {
+            for (int r = 0; r < REP; ++r) al[r] = __shfl_sync(0xffffffffu, alpha, r);
 #pragma unroll
             for (int r = 0; r < REP; ++r)
 #pragma unroll
@@ -457,6 +433,22 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
                     O2[r][k].x *= al[r];
                     O2[r][k].y *= al[r];
                 }
+        }
+        if (chunk_live) {
+            float p[NB];
+#pragma unroll
+            for (int bb = 0; bb < NB; ++bb) {
+                p[bb] = M == -INFINITY ? 0.0f : ex2(lg[bb] - M);
+                Ssum += p[bb];
+                sP2[tk[bb] * REP + r_l] = make_float2(p[bb], p[bb]);
+            }
+            // bias part of O: sum_t p_t * b_{t,g}, this lane's slots, per group
+            for (int g = 0; g < NG; ++g) {
+                float x = sOBl[g * 32 + lane];
+#pragma unroll
+                for (int bb = 0; bb < NB; ++bb) x = fmaf(p[bb], t2f<T>(sVb[tk[bb] * NG + g]), x);
+                sOBl[g * 32 + lane] = x;
+            }
         }
         __syncwarp();
         if (a_issued < nc) { issue_a(c_begin + a_issued, a_issued & 1); ++a_issued; }   // stage b is free
@@ -512,6 +504,18 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
                 O2[r][k].x += __shfl_xor_sync(0xffffffffu, O2[r][k].x, m);
                 O2[r][k].y += __shfl_xor_sync(0xffffffffu, O2[r][k].y, m);
             }
+    // row sums and V-bias sums over the lanes of each row
+#pragma unroll
+    for (int m = REP; m < 32; m <<= 1) Ssum += __shfl_xor_sync(0xffffffffu, Ssum, m);
+    float *sOB = sQS;   // [row][group] totals (the q-group sums are no longer needed)
+    __syncwarp();
+    for (int g = 0; g < NG; ++g) {
+        float x = sOBl[g * 32 + lane];
+#pragma unroll
+        for (int m = REP; m < 32; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+        if (lane < REP) sOB[lane * NG + g] = x;
+    }
+    __syncwarp();
     float Mr[REP], Sr[REP];
 #pragma unroll
     for (int r = 0; r < REP; ++r) {

@@ -138,7 +138,8 @@ constexpr size_t kQuantErrBytes = 256;
 // 16-aligned).  Group A of a chunk (packed K words, raw scale / bias copies,
 // bool and float mask rows) and group B (packed V words) are double-buffered;
 // then the scales as {s, s, -2^23 s, -2^23 s}, the weights {p, p} per
-// (token, row), the bias accumulators, the q-group sums and four mbarriers.
+// (token, row), the per-lane V-bias accumulators, the q-group sums and four
+// mbarriers.
 struct QuantLayout {
     int a0, a_stage;                    // group-A stage b at a0 + b * a_stage
     int k, ks, kb, vs, vb, mb, mf;      // offsets inside a group-A stage
@@ -169,7 +170,7 @@ __host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
     L.ks4 = quant_take(&o, ch * ng * 16);
     L.vs4 = quant_take(&o, ch * ng * 16);
     L.p2 = quant_take(&o, (ch > 32 ? ch : 32) * R * 8);   // also holds [row][32] q sums
-    L.ob = quant_take(&o, R * ng * 4);
+    L.ob = quant_take(&o, 32 * ng * 4);
     L.qs = quant_take(&o, R * ng * 4);
     L.bars = quant_take(&o, 4 * 8);
     L.total = o;
