@@ -15,9 +15,10 @@
 //  * one warp = one CTA owns a (KV row, row group of 4 query rows, token
 //    split); the split count fills every SM's resident-warp slots in one wave;
 //  * every chunk (32 tokens, or 16 when a token has more than 32 packed
-//    words) is staged in shared memory by TMA bulk copies in two groups (K
-//    words + scales + masks, then V words), each double-buffered and issued
-//    two chunks ahead, completing on mbarriers;
+//    words) is staged in shared memory in two groups (K words + scales +
+//    masks, then V words), each double-buffered and issued two chunks ahead:
+//    the K and V tiles by TMA bulk copies, the small scale and mask runs by
+//    per-lane cp.async, all completing on mbarriers;
 //  * scores: each lane keeps scale * log2(e) * q for 16 dimensions of the 4
 //    rows in registers (so no shared-memory broadcast of q per dimension),
 //    decodes its part of each token with byte permutes, scales the codes with
@@ -74,6 +75,21 @@ __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
+}
+
+// cp.async of 16 bytes (zero-filled beyond src_bytes) and of 4 bytes; the
+// thread's prior cp.async copies arrive on an mbarrier once they have landed
+// (.noinc: the barrier's expected count includes these arrivals).
+__device__ __forceinline__ void cp16(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp4(void *dst, const void *src, int src_bytes) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(src_bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Bounded wait of every lane on an mbarrier phase; the result is uniform.
@@ -191,79 +207,89 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     const int g_v = pv_live ? (wl * S::WPL * S::PF) / G : 0;
 
     if (lane == 0) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mbar_init(&bars[i], 1);
+        mbar_init(&bars[0], 33);   // group A: lane 0's expect-tx arrive + one cp.async arrive per lane
+        mbar_init(&bars[1], 33);
+        mbar_init(&bars[2], 1);    // group B: lane 0's expect-tx arrive
+        mbar_init(&bars[3], 1);
         fence_mbar_init();
     }
     __syncwarp();
 
-    // ---- chunk staging: lane 0 issues the bulk copies; tail chunks and
-    // unaligned rows are filled by all lanes with plain loads (zero beyond N)
-    auto fill_sb = [&](uint16_t *dst, const void *src_v, size_t e0, int valid_e) {
-        const uint16_t *src = static_cast<const uint16_t *>(src_v) + e0;
-        for (int e = lane; e < CH * NG; e += 32) dst[e] = e < valid_e ? src[e] : static_cast<uint16_t>(0);
-    };
+    // ---- chunk staging.  Group A: lane 0 copies the K tile with one bulk copy
+    // (mbarrier transaction bytes); the scale / bias runs and mask rows are
+    // copied by all lanes with 16- or 4-byte cp.async that arrive on the same
+    // mbarrier (count 1 + 32); tail chunks and unaligned rows are filled with
+    // plain loads (zero beyond N).  Group B: lane 0 copies the V tile.
     auto issue_a = [&](int c, int b) {
         unsigned char *st = smem + L.a0 + b * L.a_stage;
         const int t0 = c * CH, tval = min(CH, N - t0);
         const bool full = tval == CH;
         const size_t tok0 = static_cast<size_t>(kv) * N + t0;
-        const bool sb_bulk = a.al_sb && full;
-        const bool mb_bulk = a.mbool != nullptr && a.al_mb && full;
-        const bool mf_bulk = a.mfloat != nullptr && a.al_mf && full;
-        if (!sb_bulk) {
-            fill_sb(reinterpret_cast<uint16_t *>(st + L.ks), a.ks, tok0 * NG, tval * NG);
-            fill_sb(reinterpret_cast<uint16_t *>(st + L.kb), a.kb, tok0 * NG, tval * NG);
-            fill_sb(reinterpret_cast<uint16_t *>(st + L.vs), a.vs, tok0 * NG, tval * NG);
-            fill_sb(reinterpret_cast<uint16_t *>(st + L.vb), a.vb, tok0 * NG, tval * NG);
-        }
-        if (a.mbool != nullptr && !mb_bulk) {
-            uint32_t *dst = reinterpret_cast<uint32_t *>(st + L.mb);
-            for (int i = lane; i < REP * CH; i += 32) {
-                const int r = i / CH, t = i % CH;
-                dst[i] = (r < nrow && t < tval) ? a.mbool[static_cast<size_t>(q0 + r) * N + t0 + t] : 0u;
-            }
-        }
-        if (a.mfloat != nullptr && !mf_bulk) {
-            const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
-            uint16_t *dst = reinterpret_cast<uint16_t *>(st + L.mf);
-            for (int i = lane; i < REP * CH; i += 32) {
-                const int r = i / CH, t = i % CH;
-                dst[i] = (r < nrow && t < tval) ? mf[static_cast<size_t>(q0 + r) * N + t0 + t] : static_cast<uint16_t>(0);
-            }
-        }
         if (lane == 0) {
             const uint32_t kbytes = static_cast<uint32_t>(tval * WPT * 4);
-            const uint32_t sbytes = static_cast<uint32_t>(CH * NG * 2);
-            uint32_t total = kbytes;
-            if (sb_bulk) total += 4 * sbytes;
-            if (mb_bulk) total += static_cast<uint32_t>(nrow * CH * 4);
-            if (mf_bulk) total += static_cast<uint32_t>(nrow * CH * 2);
-            fence_proxy_async_smem();
-            mbar_arrive_expect_tx(&bars[b], total);
+            mbar_arrive_expect_tx(&bars[b], kbytes);
             bulk_load(st + L.k, a.kp + tok0 * WPT, kbytes, &bars[b]);
-            if (sb_bulk) {
-                const size_t e0 = tok0 * NG;
-                bulk_load(st + L.ks, static_cast<const uint16_t *>(a.ks) + e0, sbytes, &bars[b]);
-                bulk_load(st + L.kb, static_cast<const uint16_t *>(a.kb) + e0, sbytes, &bars[b]);
-                bulk_load(st + L.vs, static_cast<const uint16_t *>(a.vs) + e0, sbytes, &bars[b]);
-                bulk_load(st + L.vb, static_cast<const uint16_t *>(a.vb) + e0, sbytes, &bars[b]);
-            }
-            if (mb_bulk)
-                for (int r = 0; r < nrow; ++r)
-                    bulk_load(st + L.mb + r * CH * 4, a.mbool + static_cast<size_t>(q0 + r) * N + t0, CH * 4, &bars[b]);
-            if (mf_bulk)
-                for (int r = 0; r < nrow; ++r)
-                    bulk_load(st + L.mf + r * CH * 2,
-                              static_cast<const uint16_t *>(a.mfloat) + static_cast<size_t>(q0 + r) * N + t0, CH * 2,
-                              &bars[b]);
         }
+        // scale / bias runs: [4 arrays][CH * NG] T
+        {
+            const int per = CH * NG;   // elements per array
+            if (a.al_sb && full) {
+                const int pieces = per / 8;
+                for (int i = lane; i < 4 * pieces; i += 32) {
+                    const int arr = i / pieces, pc = i % pieces;
+                    const void *base = arr == 0 ? a.ks : arr == 1 ? a.kb : arr == 2 ? a.vs : a.vb;
+                    const int off = arr == 0 ? L.ks : arr == 1 ? L.kb : arr == 2 ? L.vs : L.vb;
+                    cp16(st + off + 16 * pc, static_cast<const uint16_t *>(base) + tok0 * NG + 8 * pc, 16);
+                }
+            } else {
+                const int valid = tval * NG;
+                for (int i = lane; i < 4 * per; i += 32) {
+                    const int arr = i / per, e = i % per;
+                    const void *base = arr == 0 ? a.ks : arr == 1 ? a.kb : arr == 2 ? a.vs : a.vb;
+                    const int off = arr == 0 ? L.ks : arr == 1 ? L.kb : arr == 2 ? L.vs : L.vb;
+                    reinterpret_cast<uint16_t *>(st + off)[e] =
+                        e < valid ? static_cast<const uint16_t *>(base)[tok0 * NG + e] : static_cast<uint16_t>(0);
+                }
+            }
+        }
+        // bool-mask rows [REP][CH] u32 (rows beyond nrow are never read)
+        if (a.mbool != nullptr) {
+            uint32_t *dst = reinterpret_cast<uint32_t *>(st + L.mb);
+            if (a.al_mb && full) {
+                for (int i = lane; i < nrow * CH / 4; i += 32) {
+                    const int r = i / (CH / 4), pc = i % (CH / 4);
+                    cp16(dst + r * CH + 4 * pc, a.mbool + static_cast<size_t>(q0 + r) * N + t0 + 4 * pc, 16);
+                }
+            } else {
+                for (int i = lane; i < nrow * CH; i += 32) {
+                    const int r = i / CH, t = i % CH;
+                    const uint32_t *src = a.mbool + static_cast<size_t>(q0 + r) * N + t0;
+                    cp4(dst + i, t < tval ? src + t : src, t < tval ? 4 : 0);
+                }
+            }
+        }
+        // float-mask rows [REP][CH] T
+        if (a.mfloat != nullptr) {
+            const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
+            uint16_t *dst = reinterpret_cast<uint16_t *>(st + L.mf);
+            if (a.al_mf && full) {
+                for (int i = lane; i < nrow * CH / 8; i += 32) {
+                    const int r = i / (CH / 8), pc = i % (CH / 8);
+                    cp16(dst + r * CH + 8 * pc, mf + static_cast<size_t>(q0 + r) * N + t0 + 8 * pc, 16);
+                }
+            } else {
+                for (int i = lane; i < nrow * CH; i += 32) {
+                    const int r = i / CH, t = i % CH;
+                    dst[i] = t < tval ? mf[static_cast<size_t>(q0 + r) * N + t0 + t] : static_cast<uint16_t>(0);
+                }
+            }
+        }
+        cp_arrive_noinc(&bars[b]);
     };
     auto issue_b = [&](int c, int b) {
         if (lane == 0) {
             const int t0 = c * CH, tval = min(CH, N - t0);
             const uint32_t bytes = static_cast<uint32_t>(tval * WPT * 4);
-            fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bars[2 + b], bytes);
             bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, bytes, &bars[2 + b]);
         }
