@@ -23,65 +23,61 @@ __device__ __forceinline__ void store_out(void *p, size_t i, float x, int out_f3
     else reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(x);
 }
 
-// One CTA per query row.  Thread t sums the float4 column (t % D4) of the
-// splits w = t / D4 (mod groups) with independent loads; the groups are then
-// added in shared memory.  Launched as a programmatic dependent of the main
-// pass.
+// One CTA per query row.  Thread t takes float4 column (t % D4) of the splits
+// w = t / D4 (mod groups): its (S, M) and O loads are issued together and
+// merged against the thread's own running max (log2 units); the groups, and
+// the sink, are combined in shared memory.  Launched as a programmatic
+// dependent of the main pass.
 constexpr int kMergeThreads = 256;
 
 template <typename T>
 __global__ void __launch_bounds__(kMergeThreads) quant_merge_kernel(const QuantArgs a) {
     pdl_wait();
     __shared__ float4 s_acc[kMergeThreads];
-    __shared__ float s_red[2];
+    __shared__ float2 s_ms[kMergeThreads];
     const int q = blockIdx.x;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
-    const float sink = a.has_sinks ? kLog2eM * __ldg(a.sinks + (q % a.nQ)) : -INFINITY;
-    if (warp == 0) {
-        float m = sink;
-        for (int w = lane; w < a.nwg; w += 32) m = fmaxf(m, __ldg(&ml[static_cast<size_t>(w) * a.rows + q].y));
-        m = warp_max(m);
-        float s = 0.0f;
-        if (m != -INFINITY) {
-            for (int w = lane; w < a.nwg; w += 32) {
-                const float2 sm = __ldg(&ml[static_cast<size_t>(w) * a.rows + q]);
-                if (sm.y != -INFINITY) s += sm.x * exp2f(sm.y - m);
-            }
-        }
-        s = warp_sum(s);
-        if (lane == 0) {
-            s_red[0] = m;
-            s_red[1] = (a.has_sinks && m != -INFINITY) ? s + exp2f(sink - m) : s;
-        }
-    }
-    __syncthreads();
-    const float mstar = s_red[0], sstar = s_red[1];
+    const int t = threadIdx.x;
     const int D4 = a.dim / 4;
     const int groups = kMergeThreads / D4;
     const int g = t / D4, i = t % D4;
+    const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml) + q;   // (S, M), stride rows
+    float m = -INFINITY, ssum = 0.0f;
     float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-    if (g < groups && mstar != -INFINITY) {
+    if (g < groups) {
         const size_t stride = static_cast<size_t>(a.rows) * a.dim;
         const float *po = a.part_o + static_cast<size_t>(q) * a.dim + 4 * i;
 #pragma unroll 4
         for (int w = g; w < a.nwg; w += groups) {
-            const float mw = __ldg(&ml[static_cast<size_t>(w) * a.rows + q].y);
+            const float2 sm = __ldg(ml + static_cast<size_t>(w) * a.rows);
             const float4 o = __ldg(reinterpret_cast<const float4 *>(po + w * stride));
-            const float e = mw == -INFINITY ? 0.0f : exp2f(mw - mstar);
-            acc.x = fmaf(o.x, e, acc.x);
-            acc.y = fmaf(o.y, e, acc.y);
-            acc.z = fmaf(o.z, e, acc.z);
-            acc.w = fmaf(o.w, e, acc.w);
+            if (sm.y == -INFINITY) continue;   // a split that saw no token
+            const float mn = fmaxf(m, sm.y);
+            const float c = exp2f(m - mn), e = exp2f(sm.y - mn);   // c = 0 while m = -inf
+            m = mn;
+            ssum = ssum * c + sm.x * e;
+            acc.x = acc.x * c + o.x * e; acc.y = acc.y * c + o.y * e;
+            acc.z = acc.z * c + o.z * e; acc.w = acc.w * c + o.w * e;
         }
     }
     s_acc[t] = acc;
+    s_ms[t] = make_float2(m, ssum);
     __syncthreads();
     if (t < D4) {
-        float4 r = s_acc[t];
-        for (int k = 1; k < groups; ++k) {
-            const float4 x = s_acc[k * D4 + t];
-            r.x += x.x; r.y += x.y; r.z += x.z; r.w += x.w;
+        const float sink = a.has_sinks ? kLog2eM * __ldg(a.sinks + (q % a.nQ)) : -INFINITY;
+        float mstar = sink;
+        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_ms[k * D4 + t].x);
+        float sstar = 0.0f;
+        float4 r = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        if (mstar != -INFINITY) {
+            if (a.has_sinks) sstar = exp2f(sink - mstar);
+            for (int k = 0; k < groups; ++k) {
+                const float2 ms = s_ms[k * D4 + t];
+                if (ms.x == -INFINITY) continue;
+                const float w = exp2f(ms.x - mstar);
+                const float4 x = s_acc[k * D4 + t];
+                sstar += ms.y * w;
+                r.x += x.x * w; r.y += x.y * w; r.z += x.z * w; r.w += x.w * w;
+            }
         }
         const float inv = sstar > 0.0f ? 1.0f / sstar : 0.0f;
         const size_t o = static_cast<size_t>(q) * a.dim + 4 * t;

@@ -100,69 +100,66 @@ cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
 }
 
 // Merge: one CTA per output row (rid = i * H + h) over the partial slots the
-// main pass left (workspace header; 0 = the output is already final).  M* and the per-split
-// weights e^(M_w - M*) are computed once per row into shared memory (128
-// splits at a time); every thread then accumulates its float4 of O over the
-// splits with independent loads.
-__global__ void __launch_bounds__(128) tree_reduce_kernel(const TreeArgs a) {
+// main pass left (workspace header; 0 = the output is already final).  Thread
+// t takes float4 column (t % D4) of the slots w = t / D4 (mod groups): all its
+// (S, M) and O loads are issued together and merged against the thread's own
+// running max; the groups are then combined in shared memory with the
+// log-sum-exp weights e^(m_g - M*).  One round trip to memory.
+constexpr int kReduceThreads = 256;
+
+__global__ void __launch_bounds__(kReduceThreads) tree_reduce_kernel(const TreeArgs a) {
     pdl_wait();
     const int nwg = a.err[1];
     if (nwg <= 0) return;
-    __shared__ float s_e[128], s_se[128];
-    __shared__ float s_red[2];
+    __shared__ float4 s_acc[kReduceThreads];
+    __shared__ float2 s_ms[kReduceThreads];   // (m_g, s_g) per thread
     const int rid = blockIdx.x;
     const int nrows = a.H * a.L;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int t = threadIdx.x;
     const int D4 = a.D / 4;
-    const float *ml = a.part_ml + static_cast<size_t>(rid) * 2;
-    const size_t ml_stride = static_cast<size_t>(nrows) * 2;
-    if (warp == 0) {
-        float m = -FLT_MAX;
-        for (int w = lane; w < nwg; w += 32) m = fmaxf(m, __ldg(ml + w * ml_stride + 1));
-        m = warp_max(m);
-        if (lane == 0) s_red[0] = m;
-    }
-    __syncthreads();
-    const float mstar = s_red[0];
+    const int groups = kReduceThreads / D4;
+    const int g = t / D4, i = t % D4;
+    const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml) + rid;   // (S, M), stride nrows
+    float m = -FLT_MAX, ssum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float ssum = 0.0f;
-    const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * t;
-    const size_t po_stride = static_cast<size_t>(nrows) * a.D;
-    for (int w0 = 0; w0 < nwg; w0 += 128) {
-        const int n = min(128, nwg - w0);
-        if (t < n) {
-            const float e = expf(__ldg(ml + (w0 + t) * ml_stride + 1) - mstar);
-            s_e[t] = e;
-            s_se[t] = __ldg(ml + (w0 + t) * ml_stride) * e;
-        }
-        __syncthreads();
-        if (t < D4) {
+    if (g < groups) {
+        const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * i;
+        const size_t po_stride = static_cast<size_t>(nrows) * a.D;
 #pragma unroll 4
-            for (int j = 0; j < n; ++j) {
-                const float4 o = __ldg(reinterpret_cast<const float4 *>(po + (w0 + j) * po_stride));
-                const float e = s_e[j];
-                acc.x += o.x * e; acc.y += o.y * e; acc.z += o.z * e; acc.w += o.w * e;
-            }
+        for (int w = g; w < nwg; w += groups) {
+            const float2 sm = __ldg(ml + static_cast<size_t>(w) * nrows);
+            const float4 o = __ldg(reinterpret_cast<const float4 *>(po + w * po_stride));
+            const float mn = fmaxf(m, sm.y);
+            const float c = expf(m - mn), e = expf(sm.y - mn);
+            m = mn;
+            ssum = ssum * c + sm.x * e;
+            acc.x = acc.x * c + o.x * e; acc.y = acc.y * c + o.y * e;
+            acc.z = acc.z * c + o.z * e; acc.w = acc.w * c + o.w * e;
         }
-        if (warp == 0)
-            for (int j = lane; j < n; j += 32) ssum += s_se[j];
-        __syncthreads();
     }
-    if (warp == 0) {
-        ssum = warp_sum(ssum);
-        if (lane == 0) s_red[1] = ssum;
-    }
+    s_acc[t] = acc;
+    s_ms[t] = make_float2(m, ssum);
     __syncthreads();
-    const float sstar = s_red[1];
-    const float inv = (sstar == 0.0f) ? 0.0f : 1.0f / sstar;
     if (t < D4) {
-        const float4 r = make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
-        reinterpret_cast<float4 *>(a.out + static_cast<size_t>(rid) * a.D)[t] = r;
+        float mstar = -FLT_MAX;
+        for (int k = 0; k < groups; ++k) mstar = fmaxf(mstar, s_ms[k * D4 + t].x);
+        float sstar = 0.0f;
+        float4 r = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int k = 0; k < groups; ++k) {
+            const float2 ms = s_ms[k * D4 + t];
+            const float w = expf(ms.x - mstar);
+            const float4 x = s_acc[k * D4 + t];
+            sstar += ms.y * w;
+            r.x += x.x * w; r.y += x.y * w; r.z += x.z * w; r.w += x.w * w;
+        }
+        const float inv = (sstar == 0.0f) ? 0.0f : 1.0f / sstar;
+        reinterpret_cast<float4 *>(a.out + static_cast<size_t>(rid) * a.D)[t] =
+            make_float4(r.x * inv, r.y * inv, r.z * inv, r.w * inv);
     }
 }
 
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s) {
-    cudaError_t e = launch_pdl(tree_reduce_kernel, dim3(a.H * a.L), dim3(128), 0, s, a);
+    cudaError_t e = launch_pdl(tree_reduce_kernel, dim3(a.H * a.L), dim3(kReduceThreads), 0, s, a);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
