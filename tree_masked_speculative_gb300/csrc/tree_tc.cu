@@ -564,7 +564,39 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     tc_fence_before();
     __syncthreads();
     cluster_sync();
-    if (warp >= 2) {
+    if (warp >= 2 && cx == 1) {
+        // No merge in the cluster: the 256 softmax threads copy the staged rows
+        // out with independent float4 loads and stores (normalized when the
+        // output is final, else as partial slot `split` with its (S, M)).
+        constexpr int F4 = DV / 4;                      // float4 per row
+        const int t2 = tid - 64;
+        const int nrows = a.H * a.L;
+        const bool final_out = a.n_part == 0;
+        const float *stage = reinterpret_cast<const float *>(sm);
+        const float2 *stage_ml = reinterpret_cast<const float2 *>(stage + 128 * SROW);
+        for (int idx = t2; idx < rows_here * F4; idx += 256) {
+            const int rr = idx / F4, c4 = idx % F4;
+            const int rg2 = rt * RT + rr;
+            const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
+            float4 o = *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
+            float *dst;
+            if (final_out) {
+                const float sl = stage_ml[rr].x;
+                const float inv = sl == 0.0f ? 0.0f : 1.0f / sl;
+                o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
+                dst = a.out + rid2 * D + os * DV;
+            } else {
+                dst = a.part_o + (static_cast<size_t>(split) * nrows + rid2) * D + os * DV;
+            }
+            *reinterpret_cast<float4 *>(dst + 4 * c4) = o;
+        }
+        if (!final_out && os == 0)
+            for (int rr = t2; rr < rows_here; rr += 256) {
+                const int rg2 = rt * RT + rr;
+                const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
+                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * nrows + rid2] = stage_ml[rr];
+            }
+    } else if (warp >= 2) {
         const int sw = warp - 2;
         const int nrows = a.H * a.L;
         const bool final_out = a.n_part == 0;
