@@ -19,11 +19,12 @@
 //                kv_seq_len are loaded out of bounds, i.e. as zeros.
 //   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
 //                TMEM, double buffered) and O += P_t V_t (M 128, N 64 per V slab,
-//                P from shared memory, V MN-major).
+//                P read from TMEM where the softmax left it over S_t, V MN-major);
+//                a buffer is released for S_t+2 when PV_t completes.
 //   warps 2..5 : one thread per row: mask + scale, online softmax with lazy
 //                rescaling (M only moves when a row max exceeds it by more
 //                than e^8, so O in TMEM is rarely touched), P as
-//                16-bit into swizzled shared memory, epilogue from TMEM.
+//                16-bit pairs back into TMEM, epilogue from TMEM.
 // Every mbarrier wait is bounded; on a timeout the CTA sets the workspace
 // error word, drains its outstanding copies and MMAs, frees TMEM and exits.
 #include "sm100_ptx.cuh"
@@ -47,10 +48,9 @@ struct TcCfg {
     static constexpr int DV = D < 256 ? D : 256;     // O columns per CTA
     static constexpr int NSK = D / 64;               // K slabs per key tile
     static constexpr int NSV = DV / 64;              // V slabs per key tile
-    static constexpr int STAGES = D == 512 ? 4 : (D == 256 ? 8 : 10);
+    static constexpr int STAGES = D == 512 ? 6 : (D == 256 ? 10 : 12);
     static constexpr int OFF_Q = 0;
-    static constexpr int OFF_P = OFF_Q + NSK * kSlab;
-    static constexpr int OFF_RING = OFF_P + 2 * kSlab;
+    static constexpr int OFF_RING = OFF_Q + NSK * kSlab;
     static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
     static constexpr int SMEM = OFF_BAR + 3072;      // the dynamic base must be 1024-aligned
     static_assert(SMEM <= 232448, "shared memory budget");
@@ -58,13 +58,13 @@ struct TcCfg {
 };
 
 struct Bars {
-    uint64_t full[10];
-    uint64_t empty[10];
+    uint64_t full[12];
+    uint64_t empty[12];
     uint64_t q_full;
     uint64_t s_full[2];
     uint64_t s_free[2];
     uint64_t p_full;
-    uint64_t o_done;
+    uint64_t o_done[2];   // PV of tiles t = b (mod 2) done
     uint64_t drain;
     uint32_t tmem_base;
     volatile int abort_flag;
@@ -174,7 +174,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     }
     unsigned char *sm = smem_raw;
     unsigned char *sQ = sm + Cfg::OFF_Q;
-    unsigned char *sP = sm + Cfg::OFF_P;
     unsigned char *sRing = sm + Cfg::OFF_RING;
     Bars *bars = reinterpret_cast<Bars *>(sm + Cfg::OFF_BAR);
 
@@ -203,9 +202,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cy); }
         mbar_init(&bars->q_full, 1);
-        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 8); }
+        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 1); }
         mbar_init(&bars->p_full, 8);
-        mbar_init(&bars->o_done, 1);
+        mbar_init(&bars->o_done[0], 1);
+        mbar_init(&bars->o_done[1], 1);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -297,7 +297,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         if (lane == 0 && T > 0) {
             constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
             constexpr uint32_t id_pv = idesc_f16(128, 64, BF16 ? 1 : 0, 0, 1);
-            const uint32_t q_addr = smem_u32(sQ), p_addr = smem_u32(sP), ring_addr = smem_u32(sRing);
+            const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
             int used = 0;                                   // ring loads consumed
             // a slot is free once every CTA of the cluster has consumed it
             auto release = [&](int slot) {
@@ -339,14 +339,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t vb = ring_addr + slot * kSlab;
+                    // P_t sits in TMEM over S_t: keys 64h.. of the tile in columns
+                    // 64h + [0, 32) of the buffer, two 16-bit keys per column
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tm_o + s * 64, sw128_desc(p_addr + (kk >> 2) * kSlab + (kk & 3) * 32, 16, 1024),
+                        mma_f16_ts(tm_o + s * 64, tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3),
                                    sw128_desc(vb + kk * 2048, kSlab, 1024), id_pv, (t | kk) != 0);
                     release(slot);
                     ++used;
                 }
-                mma_commit(&bars->o_done);
+                mma_commit(&bars->o_done[t & 1]);
+                mma_commit(&bars->s_free[t & 1]);   // S_t / P_t buffer free once PV_t is done
             }
             // Drain: all MMAs issued by this thread have completed.
             mma_commit(&bars->drain);
@@ -466,11 +469,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             }
             const float m_use = m_run == -INFINITY ? 0.0f : m_run;   // dead row: all logits -inf, P = 0
 
-            // PV of the previous tile done: P buffer free, O stable
-            if (t > 0) {
-                ok = wait_all(&bars->o_done, static_cast<uint32_t>(t - 1) & 1u, 8);
+            // A rescale needs O stable: wait for PV of the previous tile (only
+            // then; P_t has a TMEM buffer of its own).  Waiting for tile t-1 on
+            // o_done[(t-1) % 2] is unambiguous: S_t was issued after PV_t-2 was
+            // done, so that barrier's phase is the one of tile t-1.
+            if (t > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                ok = wait_all(&bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, 8);
                 tc_fence_after();
-                if (ok && __any_sync(0xffffffffu, alpha != 1.0f)) {
+                if (ok) {
 #pragma unroll 1
                     for (int c = 0; c < DVH / 32; ++c) {
                         uint32_t rr[32];
@@ -484,43 +490,44 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     tmem_wait_st();
                 }
             }
-            // pass 2: P = 2^(logit - M) rounded to the K/V type into shared memory
-            // (K-major, 128-byte swizzle: 16-byte unit u of row r sits at unit
-            // u ^ (r % 8) of the row's 128 bytes; keys 64*half.. are slab `half`).
-            // The row sum adds the rounded values, the ones the tensor core uses.
+            // pass 2: P = 2^(logit - M) rounded to the K/V type, written back into
+            // TMEM over this half's logits (columns 64 * half + [0, 32): two keys
+            // per column, the lower key in the low 16 bits), where PV reads it as
+            // the A operand.  The row sum adds the rounded values, the ones the
+            // tensor core uses.
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            unsigned char *prow = sP + half * kSlab + r * 128;
-#pragma unroll 1
-            for (int cc = 0; cc < (ok ? 2 : 0); ++cc) {
+            uint32_t pw[32];
+#pragma unroll
+            for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
-                tmem_ld32(tm_s[sb] + lane_off + (2 * half + cc) * 32, v);
-                tmem_wait_ld();
+                if (ok) {
+                    tmem_ld32(tm_s[sb] + lane_off + (2 * half + cc) * 32, v);
+                    tmem_wait_ld();
+                } else {
 #pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    uint32_t w[4];
+                    for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(-INFINITY);
+                }
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const float p0 = fast_exp2(__uint_as_float(v[8 * k + 2 * j]) - m_use);
-                        const float p1 = fast_exp2(__uint_as_float(v[8 * k + 2 * j + 1]) - m_use);
-                        w[j] = pack2(p0, p1, BF16);
-                        ps[2 * j] += lo16(w[j], BF16);
-                        ps[2 * j + 1] += hi16(w[j], BF16);
-                    }
-                    const int u = cc * 4 + k;
-                    *reinterpret_cast<uint4 *>(prow + ((u ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = fast_exp2(__uint_as_float(v[2 * j]) - m_use);
+                    const float p1 = fast_exp2(__uint_as_float(v[2 * j + 1]) - m_use);
+                    const uint32_t w = pack2(p0, p1, BF16);
+                    pw[cc * 16 + j] = w;
+                    ps[(2 * j) & 7] += lo16(w, BF16);
+                    ps[(2 * j + 1) & 7] += hi16(w, BF16);
                 }
             }
+            if (ok) {
+                tmem_st32(tm_s[sb] + lane_off + 64 * half, pw);
+                tmem_wait_st();
+            }
             l_half += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
-            fence_proxy_async_smem();
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok) {
-                mbar_arrive(&bars->s_free[sb]);
-                mbar_arrive(&bars->p_full);
-            }
+            if (lane == 0 && ok) mbar_arrive(&bars->p_full);
         }
         if (T > 0) {
-            ok = wait_all(&bars->o_done, static_cast<uint32_t>(T - 1) & 1u, 8);
+            ok = wait_all(&bars->o_done[(T - 1) & 1], (static_cast<uint32_t>(T - 1) >> 1) & 1u, 8);
             tc_fence_after();
         }
         // epilogue: row sum of both halves; the unnormalized O rows and the
