@@ -62,6 +62,40 @@ def dist_env():
     return ws, rank, local
 
 
+# ------------------------------------------------------------ multi-rank helpers
+# One process per GPU, each running its own independent step stream (weak
+# scaling: the verify step needs no data-path exchange).  The only collectives
+# are a barrier around the timed region and the max over ranks of the times.
+
+def rank_barrier(ws):
+    """A barrier over the ranks (a no-op for one rank)."""
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(values, ws, device=None):
+    """Element-wise maximum over the ranks of a list of floats (identity for
+    one rank); every rank receives the result."""
+    if ws <= 1:
+        return [float(v) for v in values]
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def job_rate(ws, bytes_per_step, steps, ms):
+    """Whole-job throughput in GB/s: every rank processed `steps` steps of
+    `bytes_per_step` K/V bytes within the slowest rank's `ms` milliseconds."""
+    return ws * bytes_per_step * steps / (ms * 1e-3) / 1e9
+
+
+def prints(rank):
+    """Rank 0 alone prints the JSON line."""
+    return rank == 0
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -193,8 +227,9 @@ class TreeBench:
         s = i % self.nsets
         self.q.copy_(self.h_q, non_blocking=True)
         self.mask.copy_(self.h_mask, non_blocking=True)
-        self.ks[s][:, :N].copy_(self.h_k, non_blocking=True)
-        self.vs[s][:, :N].copy_(self.h_v, non_blocking=True)
+        for h in range(self.wl.n_kv_heads):   # contiguous [N, D] runs, one copy each
+            self.ks[s][h, :N].copy_(self.h_k[h], non_blocking=True)
+            self.vs[s][h, :N].copy_(self.h_v[h], non_blocking=True)
         self.step(i)
         self.h_out.copy_(self.out, non_blocking=True)
 
@@ -350,9 +385,7 @@ def run_ours(args):
     if ws > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        barrier = lambda: dist.barrier()
-    else:
-        barrier = lambda: None
+    barrier = lambda: rank_barrier(ws)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     from tree_masked_speculative_gb300 import build as b
@@ -386,11 +419,7 @@ def run_ours(args):
     ms_fwd, _ = timed_graph_steps(lambda i: bench.step(i, fwd_only=True), args.steps, 0, barrier)
     clocks = sampler.stop()
 
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms, ms_fwd], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, ms_fwd = float(t[0]), float(t[1])
+    ms, ms_fwd = max_over_ranks([ms, ms_fwd], ws, dev)
 
     # end to end: host buffers in, output back, every step
     bench.e2e_setup()
@@ -409,20 +438,16 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
-    if ws > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms_e2e], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_e2e = float(t[0])
+    ms_e2e = max_over_ranks([ms_e2e], ws, dev)[0]
 
-    if rank != 0:
+    if not prints(rank):
         if ws > 1:
             import torch.distributed as dist
             dist.destroy_process_group()
         return
     peak, peak_kind = load_peaks()
     us_step = ms * 1e3 / args.steps
-    value = ws * bench.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
+    value = job_rate(ws, bench.bytes_per_step, args.steps, ms)
     achieved = bench.bytes_per_step * args.steps / (ms_fwd * 1e-3) / 1e9
     traffic = committed_traffic(bench.name)
     line = {
@@ -435,7 +460,7 @@ def run_ours(args):
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": bench.fwd_label + ", timed alone",
                      "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs)"},
-        "e2e": {"value": round(ws * bench.bytes_per_step * e2e_steps / (ms_e2e * 1e-3) / 1e9, 2),
+        "e2e": {"value": round(job_rate(ws, bench.bytes_per_step, e2e_steps, ms_e2e), 2),
                 "unit": "GB/s", "h2d_bytes_per_step": bench.e2e_h2d,
                 "d2h_bytes_per_step": bench.e2e_d2h, "steps": e2e_steps,
                 "us_per_step": round(ms_e2e * 1e3 / e2e_steps, 3)},
@@ -476,8 +501,8 @@ def run_reference(args):
     """The float64 CPU oracle as it stands, on this machine's host cores: each step
     computes a bounded sample of the workload's query rows."""
     ws, rank, _ = dist_env()
-    if rank != 0:
-        return
+    if not prints(rank):
+        return                       # the other ranks exit 0 without work
     import oracle
     oracle.build()
 
