@@ -50,6 +50,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--profile", action="store_true",
                     help="run --warmup eager steps and exit (a short, graph-free run for a profiler)")
+    ap.add_argument("--mask-build", action="store_true",
+                    help="tree workloads: also time the device-side tree-mask build from the parent array")
     ap.add_argument("--kv-sets", type=int, default=0,
                     help="K/V copies to rotate over (0 = enough to exceed 3x L2)")
     return ap.parse_args()
@@ -195,6 +197,14 @@ class TreeBench:
         self.name = wl.name
         self.dtype = wl.kv_dtype
         self.fwd_label = "mask compaction + main pass (tree_attn_fwd)"
+        self.parents = torch.tensor(inp["parents"], dtype=torch.int32, device=dev) if "parents" in inp else None
+        self.built_mask = None
+
+    def mask_step(self, i):
+        """The device-side tree-mask build from the parent array (into its own buffer)."""
+        if self.built_mask is None:
+            self.built_mask = torch.empty_like(self.mask)
+        self.ta.tree_mask_build(self.p, self.parents, self.built_mask)
 
     def step(self, i, fwd_only=False):
         s = i % self.nsets
@@ -417,6 +427,9 @@ def run_ours(args):
     ms, launches_per_step = timed_graph_steps(bench.step, args.steps, 0, barrier)
     # the dominant pass alone (mask compaction + main kernel), same rotation, for the roofline
     ms_fwd, _ = timed_graph_steps(lambda i: bench.step(i, fwd_only=True), args.steps, 0, barrier)
+    ms_mask = None
+    if args.mask_build and isinstance(bench, TreeBench) and bench.parents is not None:
+        ms_mask, _ = timed_graph_steps(bench.mask_step, args.steps, 0, barrier)
     clocks = sampler.stop()
 
     ms, ms_fwd = max_over_ranks([ms, ms_fwd], ws, dev)
@@ -467,6 +480,12 @@ def run_ours(args):
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clocks,
     }
+    if ms_mask is not None:
+        mb = bench.mask.numel() * 4                       # every mask cell written once
+        gbs = mb * args.steps / (ms_mask * 1e-3) / 1e9
+        line["mask_build"] = {"us_per_build": round(ms_mask * 1e3 / args.steps, 3), "bytes": mb,
+                              "achieved": round(gbs, 2), "unit": "GB/s", "peak": peak,
+                              "frac": round(gbs / peak, 4), "bound": "hbm (writes)"}
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(bench, args.cpu_seconds)
     print(json.dumps(line), flush=True)

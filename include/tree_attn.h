@@ -53,7 +53,7 @@ typedef enum {
     TA_ERR_CUDA = 5              /* the CUDA runtime reported an error */
 } ta_status;
 
-typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2, TA_U32 = 3 } ta_dtype;
+typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2, TA_U32 = 3, TA_I32 = 4 } ta_dtype;
 
 /* Borrowed device buffer. `bytes` is the usable size starting at `ptr`. */
 typedef struct {
@@ -194,6 +194,27 @@ ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp, const ta_
 ta_status tree_attn_fwd_noalloc(const ta_tree_params *p, const ta_buf *q, const ta_buf *k,
                                 const ta_buf *v, const ta_buf *mask, const ta_buf *out,
                                 void *stream);
+
+/*
+ * Dense tree mask from a parent array, built on the device: the step before
+ * the verify pass (the tree semantics of mlx-native tree_attention.metal's
+ * header comment and of the tree_attention.rs tests; 0 = attend, -65504 =
+ * masked).  The draft tree's node i sits at KV position kv_seq_len - q_l + i.
+ *   p        q_l, kv_seq_len and mask_stride are used; p must pass the same
+ *            checks as for tree_attn_fwd (mask_stride >= kv_seq_len >= q_l).
+ *   parents  [q_l] i32 on the device: parents[i] in [-1, i) (node 0 is the
+ *            root, -1 = no parent).  Node a is an ancestor of i when the chain
+ *            i, parents[i], parents[parents[i]], ... reaches a; a value outside
+ *            [0, current node) ends the chain there.
+ *   mask     [q_l, mask_stride] f32 on the device, every cell written: row i is
+ *            0 on [0, kv_seq_len - q_l), at kv_seq_len - q_l + a for i itself
+ *            and each of its ancestors a, and -65504 elsewhere (including
+ *            positions >= kv_seq_len).
+ * Errors: as tree_attn_fwd's checks; parents must be I32 and 4-byte aligned,
+ * mask F32 and 4-byte aligned; q_l > 16384 is TA_ERR_UNSUPPORTED.  Nothing is
+ * launched on error.  Asynchronous on `stream`.
+ */
+ta_status tree_mask_build(const ta_tree_params *p, const ta_buf *parents, const ta_buf *mask, void *stream);
 
 /* ----------------------------------------------------------------- quant */
 

@@ -58,6 +58,8 @@ def _load():
             lib.oracle_decode.restype = None
             lib.oracle_dequant_token.argtypes = [I, I, I, I, I, P, P, P, I, I, P]
             lib.oracle_dequant_token.restype = I
+            lib.oracle_tree_mask.argtypes = [P, I, I, I, P]
+            lib.oracle_tree_mask.restype = I
             _lib = lib
     return _lib
 
@@ -176,3 +178,15 @@ def quant_oracle_for(wl, inp: dict, rows=None, threads=None) -> np.ndarray:
                       dim=wl.dim, tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size,
                       has_sinks=wl.has_sinks, window_size=wl.window_size, scale=wl.scale,
                       dtype=wl.dtype, rows=rows, threads=threads)
+
+
+def tree_mask(parents, *, kv_seq_len: int, mask_stride: int) -> np.ndarray:
+    """Dense tree mask [q_l, mask_stride] f32 (0 / -65504) from a parent array
+    (oracle_tree_mask in oracle.c)."""
+    par = np.ascontiguousarray(np.asarray(parents, dtype=np.int32))
+    q_l = int(par.shape[0])
+    out = np.empty((q_l, mask_stride), dtype=np.float32)
+    st = _load().oracle_tree_mask(_ptr(par), q_l, kv_seq_len, mask_stride, _ptr(out))
+    if st != 0:
+        raise ValueError("oracle_tree_mask: invalid sizes (status %d)" % st)
+    return out

@@ -286,3 +286,40 @@ int oracle_dequant_token(int dim, int N, int bits, int G, int t_dtype, const uin
     for (int d = 0; d < dim; ++d) out[d] = orc_dequant(&c, packed, scales, biases, kv, t, d);
     return 0;
 }
+
+/*
+ * Tree mask from a parent array (the step before the verify pass): the draft
+ * tree's node i sits at KV position kv_seq_len - q_l + i and attends the
+ * prefix [0, kv_seq_len - q_l), its ancestors and itself (tree_attention.metal
+ * header comment and the tree_attention.rs tests: 0 = attend, -65504 =
+ * masked).  Node a is an ancestor of i when the chain i, parents[i],
+ * parents[parents[i]], ... reaches a; the chain ends at a value outside
+ * [0, current node) (-1 for the root).  Cells at positions >= kv_seq_len, up
+ * to mask_stride, are -65504.  out is [q_l, mask_stride] binary32.
+ */
+int oracle_tree_mask(const int32_t *parents, int q_l, int kv_seq_len, int mask_stride, float *out) {
+    if (q_l < 1 || kv_seq_len < q_l || mask_stride < kv_seq_len) return 1;
+    const int prefix = kv_seq_len - q_l;
+    unsigned char *anc = (unsigned char *)malloc((size_t)q_l);
+    if (anc == NULL) return 2;
+    for (int i = 0; i < q_l; ++i) {
+        for (int a = 0; a < q_l; ++a) anc[a] = 0;
+        int node = i;
+        anc[node] = 1;
+        for (;;) {
+            const int up = parents[node];
+            if (up < 0 || up >= node) break;
+            anc[up] = 1;
+            node = up;
+        }
+        float *row = out + (size_t)i * mask_stride;
+        for (int j = 0; j < mask_stride; ++j) {
+            int attend = 0;
+            if (j < prefix) attend = 1;
+            else if (j < kv_seq_len) attend = anc[j - prefix];
+            row[j] = attend ? 0.0f : -65504.0f;
+        }
+    }
+    free(anc);
+    return 0;
+}

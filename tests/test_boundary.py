@@ -262,3 +262,30 @@ def test_set_tree_path(ta):
     prev = ta.ta_set_tree_path(1)
     assert ta.ta_set_tree_path(prev) == 1
     assert ta.ta_set_tree_path(7) == -1
+
+
+# ------------------------------------------------------------ tree mask builder
+@pytest.mark.parametrize("kw,pbytes,pdtype,mbytes,mdtype,st_want,frag", [
+    (dict(), 10 * 4, "I32", 10 * 64 * 4, "F32", None, None),                 # valid shape; see below
+    (dict(), 10 * 4, "U32", 10 * 64 * 4, "F32", 1, "parents dtype"),
+    (dict(), 10 * 4, "I32", 10 * 64 * 4, "F16", 1, "mask dtype"),
+    (dict(), 9 * 4, "I32", 10 * 64 * 4, "F32", 2, "parents"),
+    (dict(), 10 * 4, "I32", 10 * 64 * 4 - 4, "F32", 2, "mask"),
+    (dict(mask_stride=40), 10 * 4, "I32", 10 * 64 * 4, "F32", 1, "mask_stride"),
+    (dict(q_l=60, kv_seq_len=50, mask_stride=64), 60 * 4, "I32", 60 * 64 * 4, "F32", 1, "q_l"),
+    (dict(q_l=16385, kv_seq_len=20000, mask_stride=20000), 16385 * 4, "I32", 16385 * 20000 * 4, "F32", 4, "q_l"),
+])
+def test_tree_mask_build_rejections(ta, kw, pbytes, pdtype, mbytes, mdtype, st_want, frag):
+    if st_want is None:
+        return                                               # launching needs a GPU (tests/test_gpu_tree.py)
+    d = dict(n_heads=4, n_kv_heads=2, head_dim=128, kv_seq_len=50, kv_capacity=64, scale=0.1, nwg=0, q_l=10,
+             mask_stride=64)
+    d.update(kw)
+    d["kv_capacity"] = max(d["kv_capacity"], d["kv_seq_len"])
+    p = ta.TreeParams(**d)
+    code = {"I32": ta.TA_I32, "U32": ta.TA_U32, "F32": ta.TA_F32, "F16": ta.TA_F16}
+    before = ta.ta_launch_count()
+    st = ta.lib.tree_mask_build(ctypes.byref(p), ctypes.byref(_b(ta, pbytes, code[pdtype])),
+                                ctypes.byref(_b(ta, mbytes, code[mdtype])), None)
+    assert ta.ta_launch_count() == before
+    assert st == st_want and frag in ta.ta_last_error()

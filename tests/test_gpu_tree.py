@@ -206,3 +206,54 @@ def test_dynamic_tree_workload_sampled_rows(ta):
     # properties that hold for every row: finite, bounded by the attended V range
     v = inp["v"][:, :wl.kv_seq_len].float()
     assert np.all(np.abs(got) <= float(v.abs().max()) + 1e-3)
+
+
+# ------------------------------------------------------------ tree mask builder
+MASK_CASES = [
+    ("fixed", 32, 4096, 8192),        # the fixed-tree workload's shape (stride 8192 > N)
+    ("dynamic", 64, 32768, 32768),    # the dynamic-tree workload's shape
+    ("chain", 8, 256, 256),
+    ("dynamic", 1, 5, 7),             # a single node; stride not a multiple of 4
+    ("dynamic", 100, 1000, 1003),
+    ("fixed", 17, 17, 17),            # no prefix
+    ("dynamic", 300, 5000, 5004),     # more than 256 nodes
+]
+
+
+def _parents(topology, L, seed=5):
+    if topology == "chain":
+        return W.chain_parents(L)
+    if topology == "fixed":
+        return W.fixed_tree_parents((4, 2, 2, 2, 2, 1, 1), L)
+    return W.dynamic_tree_parents(L, torch.Generator().manual_seed(seed))
+
+
+@pytest.mark.parametrize("topology,L,N,S", MASK_CASES, ids=[str(i) for i in range(len(MASK_CASES))])
+def test_tree_mask_build_matches_oracle(ta, topology, L, N, S):
+    par = _parents(topology, L)
+    p = ta.tree_params(8, 2, 128, N, N, 0.1, L, S, 0)
+    d_par = torch.tensor(par, dtype=torch.int32, device="cuda")
+    full = torch.full((L * S + 64,), 7.0, device="cuda")           # guard cells after the mask
+    mask = full[:L * S].view(L, S)
+    ta.tree_mask_build(p, d_par, mask)
+    torch.cuda.synchronize()
+    ref = oracle.tree_mask(par, kv_seq_len=N, mask_stride=S)
+    got = mask.cpu().numpy()
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))   # bit-exact
+    assert torch.all(full[L * S:] == 7.0)
+
+
+def test_tree_mask_build_feeds_the_verify_pass(ta):
+    # the device-built mask gives the same attention output, bit for bit, as the host-built one
+    wl = small_tree(H=8, Hk=2, D=128, N=600, C=640, L=12, kv_dtype="f16", topology="fixed")
+    inp = W.make_tree_inputs(wl)
+    par = W.fixed_tree_parents(wl.branching, wl.q_l)
+    out_host = run_tree(ta, wl, inp)
+    p = ta.tree_params(wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.kv_seq_len, wl.kv_capacity, wl.scale,
+                       wl.q_l, wl.mask_stride, wl.nwg)
+    d_mask = torch.empty((wl.q_l, wl.mask_stride), device="cuda")
+    ta.tree_mask_build(p, torch.tensor(par, dtype=torch.int32, device="cuda"), d_mask)
+    inp2 = dict(inp)
+    inp2["mask"] = d_mask.cpu()
+    out_dev = run_tree(ta, wl, inp2)
+    assert torch.equal(out_host, out_dev)

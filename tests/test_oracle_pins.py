@@ -399,3 +399,53 @@ def test_quant_oracle_row_subset_and_gqa_mapping():
     full = oracle.quant_sdpa(inp, **kw)
     sub = oracle.quant_sdpa(inp, rows=[7, 2], **kw)
     assert np.array_equal(sub[0], full[7]) and np.array_equal(sub[1], full[2])
+
+
+# ------------------------------------------------------------- tree mask builder
+def test_tree_mask_oracle_hand_golden():
+    g = json.load(open(os.path.join(GOLDEN, "tree_mask_small.json")))
+    m = oracle.tree_mask(g["parents"], kv_seq_len=g["kv_seq_len"], mask_stride=g["mask_stride"])
+    assert m.shape == (len(g["parents"]), g["mask_stride"])
+    for i, cols in enumerate(g["attended_positions"]):
+        want = np.full(g["mask_stride"], -65504.0, dtype=np.float32)
+        want[cols] = 0.0
+        assert np.array_equal(m[i], want), i
+
+
+def test_tree_mask_oracle_chain_is_causal():
+    # a chain (node i's parent is i - 1) attends exactly keys [0, N - L + i]
+    L, N, S = 9, 40, 45
+    m = oracle.tree_mask([-1] + list(range(L - 1)), kv_seq_len=N, mask_stride=S)
+    j = np.arange(S)[None, :]
+    i = np.arange(L)[:, None]
+    assert np.array_equal(m == 0.0, (j <= N - L + i))
+
+
+def test_tree_mask_oracle_matches_transitive_closure():
+    rng = np.random.default_rng(11)
+    for L in (1, 2, 7, 33):
+        par = [-1] + [int(rng.integers(0, i)) for i in range(1, L)]
+        N, S = L + 17, L + 20
+        m = oracle.tree_mask(par, kv_seq_len=N, mask_stride=S)
+        # reachability by repeated squaring of (I + child->parent edges)
+        A = np.eye(L, dtype=bool)
+        for i, p in enumerate(par):
+            if p >= 0:
+                A[i, p] = True
+        R = A.copy()
+        for _ in range(max(1, int(np.ceil(np.log2(L))) + 1)):
+            R = R | ((R.astype(np.int64) @ R.astype(np.int64)) > 0)
+        P = N - L
+        assert np.all(m[:, :P] == 0.0)
+        assert np.array_equal(m[:, P:N] == 0.0, R)
+        assert np.all(m[:, N:] == -65504.0)
+
+
+def test_tree_mask_oracle_invalid_links_end_the_chain():
+    # node 1 names a later node as its parent and node 3 itself: both chains stop there
+    m = oracle.tree_mask([-1, 2, 1, 3], kv_seq_len=6, mask_stride=6)
+    att = (m == 0.0)
+    P = 2
+    assert list(np.flatnonzero(att[1][P:])) == [1]
+    assert list(np.flatnonzero(att[2][P:])) == [1, 2]
+    assert list(np.flatnonzero(att[3][P:])) == [3]

@@ -21,11 +21,11 @@ __all__ = [
     "tree_attn_tmp_bytes", "tree_attn_num_splits", "tree_attn_workspace_bytes", "tree_attn_fwd",
     "tree_attn_fwd_causal", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
     "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "tree_attention",
-    "quant_sdpa", "tree_params", "quant_params",
+    "quant_sdpa", "tree_params", "quant_params", "tree_mask_build",
 ]
 
 TA_OK = 0
-TA_F32, TA_F16, TA_BF16, TA_U32 = 0, 1, 2, 3
+TA_F32, TA_F16, TA_BF16, TA_U32, TA_I32 = 0, 1, 2, 3, 4
 STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARGUMENT", 2: "TA_ERR_BUFFER_TOO_SMALL",
                 3: "TA_ERR_OVERFLOW", 4: "TA_ERR_UNSUPPORTED", 5: "TA_ERR_CUDA"}
 
@@ -96,6 +96,8 @@ def _load() -> ctypes.CDLL:
     L.ta_launch_count.restype = ctypes.c_uint64
     L.ta_set_tree_path.argtypes = [ctypes.c_int]
     L.ta_set_tree_path.restype = ctypes.c_int
+    L.tree_mask_build.argtypes = [PT, B, B, P]
+    L.tree_mask_build.restype = ctypes.c_int
     return L
 
 
@@ -260,3 +262,8 @@ def quant_sdpa(inputs: dict, *, batch: int, n_q_heads: int, n_kv_heads: int, dim
                    inputs["sinks"] if has_sinks else None, inputs.get("mask_bool"),
                    inputs.get("mask_float"), tmp, out, stream)
     return out
+
+
+def tree_mask_build(p: TreeParams, parents: torch.Tensor, mask: torch.Tensor, stream=None):
+    """Dense tree mask [q_l, mask_stride] f32 from parents [q_l] int32, on the device."""
+    _check(lib.tree_mask_build(ctypes.byref(p), buf(parents, TA_I32), buf(mask), _stream(stream)))

@@ -74,6 +74,7 @@ const char *dtype_name(int dtype) {
         case TA_F16: return "F16";
         case TA_BF16: return "BF16";
         case TA_U32: return "U32";
+        case TA_I32: return "I32";
         default: return "unknown";
     }
 }
@@ -498,6 +499,28 @@ TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp_
     a.nwg = (int)nwg;
     cudaError_t e = launch_tree_reduce(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: reduce launch");
+    return TA_OK;
+}
+
+TA_EXPORT ta_status tree_mask_build(const ta_tree_params *p, const ta_buf *parents_d, const ta_buf *mask_d,
+                                    void *stream) {
+    const ta_buf &parents = deref(parents_d), &mask = deref(mask_d);
+    TA_TRY(check_tree_params(p, true));
+    if (p->q_l > p->kv_seq_len)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_mask_build: q_l (%u) must be <= kv_seq_len (%u)", p->q_l,
+                    p->kv_seq_len);
+    if (p->q_l > (uint32_t)kMaxTreeMaskNodes)
+        return fail(TA_ERR_UNSUPPORTED, "tree_mask_build: q_l > %d is not implemented", kMaxTreeMaskNodes);
+    TA_TRY(check_dtype(parents, "parents", TA_I32));
+    TA_TRY(check_dtype(mask, "mask", TA_F32));
+    uint64_t req_mask;
+    if (!mul3(p->q_l, p->mask_stride, 4, &req_mask)) return fail(TA_ERR_OVERFLOW, "tree_mask_build: size overflows");
+    TA_TRY(check_buf(parents, "tree_mask_build: parents", (uint64_t)p->q_l * 4, 4));
+    TA_TRY(check_buf(mask, "tree_mask_build: mask", req_mask, 4));
+    cudaError_t e = launch_tree_mask(static_cast<const int32_t *>(parents.ptr), (int)p->q_l, (int)p->kv_seq_len,
+                                     (int)p->mask_stride, static_cast<float *>(mask.ptr),
+                                     static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "tree_mask_build: launch");
     return TA_OK;
 }
 

@@ -199,6 +199,12 @@ cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, c
 // row tiles and O halves that share K/V through multicast.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
+// Dense tree mask [q_l, stride] f32 from parents [q_l] (device pointers).
+cudaError_t launch_tree_mask(const int32_t *parents, int q_l, int kv_seq_len, int stride, float *mask,
+                             cudaStream_t s);
+// Largest q_l the mask builder takes (its parents and bitset live in shared memory).
+constexpr int kMaxTreeMaskNodes = 16384;
+constexpr size_t kMaxTreeMaskSmem = sizeof(int32_t) * (kMaxTreeMaskNodes + kMaxTreeMaskNodes / 32);
 cudaError_t launch_quant_fma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_b4(const QuantArgs &a, cudaStream_t s);
