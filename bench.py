@@ -33,7 +33,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "tree-verify attention KV GB/s and % of HBM roofline; μs per verify step"
 WORKLOADS = {"pr1_chain": W.PR1_CHAIN, "fixed_tree": W.FIXED_TREE, "dynamic_tree": W.DYNAMIC_TREE,
-             "quant_b4": W.QUANT_B4, "quant_b8_masks": W.QUANT_B8_MASKS}
+             "quant_b4": W.QUANT_B4, "quant_b8_masks": W.QUANT_B8_MASKS, "quant_tree": W.QUANT_TREE}
 L2_BYTES = 129 * 1024 * 1024
 GRAPH_STEPS = 500
 

@@ -115,3 +115,27 @@ def test_quant_b8_masks_workload_full(ta):
     assert_close(got, ref, extra_ulp_dtype=wl.dtype, what="quant b8 workload")
     got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
     assert_close(got32, ref, what="quant b8 workload f32")
+
+
+@pytest.mark.parametrize("bits,dtype", [(4, "f16"), (8, "bf16")])
+def test_quant_cache_verified_with_a_tree_mask(ta, bits, dtype):
+    """q_l draft-tree nodes per head verified against a quantized cache through
+    the same call: the nodes are extra query rows (n_q_heads * q_l of them,
+    ordered (batch, head, node), so each KV row serves heads_per_kv * q_l rows)
+    and each row's tree mask is its additive float mask (0 / -65504)."""
+    B, nQ, nKV, q_l, N = 2, 4, 2, 6, 300
+    wl = qwl(B=B, nQ=nQ * q_l, nKV=nKV, dim=128, N=N, bits=bits, G=64, sinks=0, dtype=dtype)
+    inp = W.make_quant_inputs(wl)
+    par = W.fixed_tree_parents((2, 2, 1), q_l)
+    tm = oracle.tree_mask(par, kv_seq_len=N, mask_stride=N)             # [q_l, N]
+    T = torch.float16 if dtype == "f16" else torch.bfloat16
+    inp["mask_float"] = torch.from_numpy(np.tile(tm, (B * nQ, 1))).to(T)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got, ref, what="quant cache x tree mask")
+    # the same token sets given as a bool mask instead of an additive one
+    inp_b = dict(inp)
+    del inp_b["mask_float"]
+    inp_b["mask_bool"] = torch.from_numpy(np.tile((tm == 0.0).astype(np.int32), (B * nQ, 1)))
+    got_b = run_quant(ta, wl, inp_b, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got_b, ref, what="quant cache x tree mask as a bool mask")

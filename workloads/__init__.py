@@ -206,7 +206,8 @@ class QuantWorkload:
     window_size: int
     scale: float
     dtype: str                  # T: "f16" | "bf16"
-    float_mask: str = "none"    # "none" | "alibi"
+    float_mask: str = "none"    # "none" | "alibi" | "tree<q_l>": n_q_heads = heads x q_l draft
+                                # nodes (rows (batch, head, node)), each row's fixed-tree mask
     bool_mask_frac: float = 0.0  # 0 = no bool mask
     nwg: int = 0
     seed: int = 0
@@ -289,6 +290,10 @@ def make_quant_inputs(wl: QuantWorkload) -> dict:
     mask_float = None
     if wl.float_mask == "alibi":
         mask_float = alibi_mask(rows, wl.n_q_heads, N, T)
+    elif wl.float_mask.startswith("tree"):
+        q_l = int(wl.float_mask[len("tree"):])
+        tm = tree_mask(fixed_tree_parents((4, 2, 2, 1, 1), q_l), N, N)      # [q_l, N]
+        mask_float = tm.repeat(rows // q_l, 1).to(T)
     return {"queries": queries, "k_packed": k_packed, "k_scales": k_scales,
             "k_biases": k_biases, "v_packed": v_packed, "v_scales": v_scales,
             "v_biases": v_biases, "sinks": sinks, "mask_bool": mask_bool,
@@ -306,5 +311,12 @@ QUANT_B8_MASKS = QuantWorkload(
     window_size=4096, scale=1.0 / math.sqrt(256), dtype="bf16", float_mask="alibi",
     bool_mask_frac=0.1, seed=1005)
 
+# A draft tree verified on a quantized cache: 32 heads x 8 fixed-tree nodes as
+# query rows over 8 KV heads (32 rows per KV row), 4-bit d128 cache.
+QUANT_TREE = QuantWorkload(
+    name="quant_tree_B1_h32xq8_kv8_d128_n16384_4bit_f16", batch=1, n_q_heads=256, n_kv_heads=8,
+    dim=128, tokens=16384, bits=4, group_size=64, has_sinks=0, window_size=0,
+    scale=1.0 / math.sqrt(128), dtype="f16", float_mask="tree8", seed=1006)
+
 TREE_WORKLOADS = {w.name: w for w in (PR1_CHAIN, FIXED_TREE, DYNAMIC_TREE)}
-QUANT_WORKLOADS = {w.name: w for w in (QUANT_B4, QUANT_B8_MASKS)}
+QUANT_WORKLOADS = {w.name: w for w in (QUANT_B4, QUANT_B8_MASKS, QUANT_TREE)}
