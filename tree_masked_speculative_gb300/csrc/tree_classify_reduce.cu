@@ -22,8 +22,7 @@ namespace ta {
 constexpr int kPrepThreads = 256;
 constexpr int kQ16PerBlock = kPrepThreads * 8;
 
-__global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs a, int n_cls_blocks) {
-    pdl_launch_dependents();
+__device__ __forceinline__ void prep_body(const TreeArgs &a, int n_cls_blocks) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) {
         a.err[0] = 0;          // error word
         a.err[1] = a.n_part;   // partial slots the main pass leaves for the merge
@@ -86,6 +85,16 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs 
     }
 }
 
+// Launched as a programmatic dependent: the main pass that follows may start
+// launching at once (it waits for this grid), and this grid waits for its own
+// predecessor - the previous merge, or whatever kernel wrote Q and the mask -
+// before it reads anything or touches the workspace.
+__global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs a, int n_cls_blocks) {
+    pdl_launch_dependents();
+    pdl_wait();
+    prep_body(a, n_cls_blocks);
+}
+
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
     const int n_cls = a.n_chunks;
     int n_q = 0;
@@ -109,6 +118,9 @@ constexpr int kReduceThreads = 256;
 
 __global__ void __launch_bounds__(kReduceThreads) tree_reduce_kernel(const TreeArgs a) {
     pdl_wait();
+    // The next prep pass may start launching; it waits for this grid to finish
+    // before it rewrites the workspace.
+    pdl_launch_dependents();
     const int nwg = a.err[1];
     if (nwg <= 0) return;
     __shared__ float4 s_acc[kReduceThreads];
