@@ -52,6 +52,9 @@ def parse():
                     help="run --warmup eager steps and exit (a short, graph-free run for a profiler)")
     ap.add_argument("--mask-build", action="store_true",
                     help="tree workloads: also time the device-side tree-mask build from the parent array")
+    ap.add_argument("--quant-path", type=int, default=0, choices=[0, 1, 2],
+                    help="quantized workloads: 0 automatic, 1 CUDA-core kernel, 2 tensor-core kernel "
+                         "where the shape allows it")
     ap.add_argument("--kv-sets", type=int, default=0,
                     help="K/V copies to rotate over (0 = enough to exceed 3x L2)")
     return ap.parse_args()
@@ -274,7 +277,9 @@ class QuantBench:
         self.bytes_per_step = wl.kv_bytes
         self.name = wl.name
         self.dtype = "u%d" % wl.bits
-        self.fwd_label = "main pass + split merge (quant_sdpa_fwd, one call)"
+        self.tc = ta.quant_sdpa_uses_tensor_cores(self.p) == 1
+        kern = "quant_tc_kernel (tensor cores)" if self.tc else "quant_kernel (CUDA cores)"
+        self.fwd_label = "main pass (%s) + split merge (quant_sdpa_fwd, one call)" % kern
 
     def step(self, i, fwd_only=False):
         s = self.sets[i % self.nsets]
@@ -289,6 +294,7 @@ class QuantBench:
         return {"workload": wl.name, "batch": wl.batch, "n_q_heads": wl.n_q_heads,
                 "n_kv_heads": wl.n_kv_heads, "dim": wl.dim, "tokens": wl.tokens, "bits": wl.bits,
                 "group_size": wl.group_size, "window_size": wl.window_size, "splits": self.nwg,
+                "kernel": "tensor cores" if self.tc else "CUDA cores",
                 "l2": "rotating %d K/V sets, %.0f MB read per rotation (> 3x L2)" % (
                     self.nsets, self.nsets * self.bytes_per_step / 1e6)}
 
@@ -405,6 +411,7 @@ def run_ours(args):
         barrier()
     import tree_masked_speculative_gb300 as ta
 
+    ta.ta_set_quant_path(args.quant_path)
     bench = make_bench(ta, args.workload, dev, args.kv_sets)
     if args.profile:
         for i in range(max(1, args.warmup)):

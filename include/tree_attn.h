@@ -270,6 +270,32 @@ uint64_t ta_launch_count(void);
  */
 int ta_set_tree_path(int path);
 
+/*
+ * Quantized-KV kernel family used by later calls: 0 = automatic (the
+ * tensor-core kernel when the shape allows it and a KV row serves >= 16 query
+ * rows, e.g. draft-tree nodes as rows, else the CUDA-core kernel), 2 = the
+ * tensor-core kernel wherever the shape allows it, 1 = always the CUDA-core
+ * kernel.  Process-wide; returns the previous value, or
+ * -1 for a bad value.  The split count and tmp size depend on the family, so
+ * size tmp (quant_sdpa_tmp_bytes) after setting it.  Meant for tests and
+ * measurements.
+ *
+ * The tensor-core kernel serves head dimensions 64, 128 and 256 when TMEM
+ * holds O (dim f32 columns) and two score buffers (dim / group_size groups x
+ * 16 or 32 query rows each).  It feeds the tensor core the exact integer codes
+ * of K (the per-group scales and biases are applied to the f32 scores), V
+ * dequantized once to f16 (s * code + b, one rounding) and the weights P in
+ * f16; Q is scaled per row by a power of two into f16 (exact for f16 and bf16
+ * queries).  Dequantized V values are assumed to lie within the f16 range
+ * (|v| <= 65504); the CUDA-core kernel has no such limit.
+ */
+int ta_set_quant_path(int path);
+
+/* 1 if quant_sdpa_fwd with these params takes the tensor-core kernel under the
+ * current ta_set_quant_path setting, 0 if the CUDA-core kernel, -1 for invalid
+ * params.  No device work. */
+int quant_sdpa_uses_tensor_cores(const ta_quant_params *p);
+
 #ifdef __cplusplus
 }
 #endif

@@ -262,6 +262,9 @@ def test_set_tree_path(ta):
     prev = ta.ta_set_tree_path(1)
     assert ta.ta_set_tree_path(prev) == 1
     assert ta.ta_set_tree_path(7) == -1
+    prev = ta.ta_set_quant_path(1)
+    assert ta.ta_set_quant_path(prev) == 1
+    assert ta.ta_set_quant_path(-1) == -1
 
 
 # ------------------------------------------------------------ tree mask builder
@@ -289,3 +292,26 @@ def test_tree_mask_build_rejections(ta, kw, pbytes, pdtype, mbytes, mdtype, st_w
                                 ctypes.byref(_b(ta, mbytes, code[mdtype])), None)
     assert ta.ta_launch_count() == before
     assert st == st_want and frag in ta.ta_last_error()
+
+
+def test_quant_kernel_family_choice(ta):
+    """Which quantized kernel a shape takes (no device work)."""
+    def p(dim, G=64, nQ=32, nKV=8, bits=4):
+        return ta.quant_params(1, nQ, nKV, dim, 1000, bits, G, 0, 0, 0.1, 0)
+    prev = ta.ta_set_quant_path(0)
+    try:
+        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0            # 4 rows per KV row: CUDA cores
+        assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128)) == 1    # 16 rows per KV row
+        assert ta.quant_sdpa_uses_tensor_cores(p(512, nQ=256)) == 0
+        ta.ta_set_quant_path(2)
+        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 1
+        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8)) == 1
+        assert ta.quant_sdpa_uses_tensor_cores(p(64, G=32)) == 1
+        assert ta.quant_sdpa_uses_tensor_cores(p(512)) == 0            # O alone fills TMEM
+        assert ta.quant_sdpa_uses_tensor_cores(p(96, G=32)) == 0       # not a multiple of 64
+        assert ta.quant_sdpa_uses_tensor_cores(p(256, G=16, nQ=256, bits=8)) == 0   # 16 groups x 32 rows
+        assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1           # invalid params
+        ta.ta_set_quant_path(1)
+        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0
+    finally:
+        ta.ta_set_quant_path(prev)

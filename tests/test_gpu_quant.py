@@ -13,10 +13,14 @@ from helpers import assert_close, run_quant
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module")
-def ta():
+@pytest.fixture(scope="module", params=[2, 1], ids=["tensor_cores", "cuda_cores"])
+def ta(request):
+    """Every test runs on both kernel families: the tensor-core kernel (where
+    the shape allows it; others fall back to CUDA cores) and the CUDA-core one."""
     import tree_masked_speculative_gb300 as m
-    return m
+    prev = m.ta_set_quant_path(request.param)
+    yield m
+    m.ta_set_quant_path(prev)
 
 
 def qwl(B=2, nQ=8, nKV=2, dim=128, N=300, bits=4, G=64, sinks=1, window=0, dtype="f16",
@@ -139,3 +143,26 @@ def test_quant_cache_verified_with_a_tree_mask(ta, bits, dtype):
     inp_b["mask_bool"] = torch.from_numpy(np.tile((tm == 0.0).astype(np.int32), (B * nQ, 1)))
     got_b = run_quant(ta, wl, inp_b, out_dtype=torch.float32).cpu().double().numpy()
     assert_close(got_b, ref, what="quant cache x tree mask as a bool mask")
+
+
+def test_quant_many_rows_per_kv_row(ta):
+    """48 query rows per KV row: two row blocks of the tensor-core kernel, a
+    ragged last tile, a window that starts inside a tile, both masks."""
+    wl = qwl(B=1, nQ=48, nKV=1, dim=128, N=777, bits=4, G=32, sinks=1, window=600, fmask="alibi",
+             bfrac=0.2, dtype="bf16")
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got, ref, what="48 rows per KV row")
+    gotT = run_quant(ta, wl, inp).cpu().double().numpy()
+    assert_close(gotT, ref, extra_ulp_dtype=wl.dtype, what="48 rows per KV row, T out")
+
+
+def test_quant_tree_workload_full(ta):
+    """The draft-tree workload on a quantized cache at full size (256 rows over
+    8 KV rows, 16384 tokens, per-row tree masks)."""
+    wl = W.QUANT_TREE
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got, ref, what="quant tree workload f32")

@@ -20,7 +20,8 @@ __all__ = [
     "TA_OK", "TreeParams", "QuantParams", "TreeAttentionError", "lib", "library_path",
     "tree_attn_tmp_bytes", "tree_attn_num_splits", "tree_attn_workspace_bytes", "tree_attn_fwd",
     "tree_attn_fwd_causal", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
-    "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "tree_attention",
+    "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "ta_set_quant_path",
+    "quant_sdpa_uses_tensor_cores", "tree_attention",
     "quant_sdpa", "tree_params", "quant_params", "tree_mask_build",
 ]
 
@@ -96,6 +97,10 @@ def _load() -> ctypes.CDLL:
     L.ta_launch_count.restype = ctypes.c_uint64
     L.ta_set_tree_path.argtypes = [ctypes.c_int]
     L.ta_set_tree_path.restype = ctypes.c_int
+    L.ta_set_quant_path.argtypes = [ctypes.c_int]
+    L.ta_set_quant_path.restype = ctypes.c_int
+    L.quant_sdpa_uses_tensor_cores.argtypes = [PQ]
+    L.quant_sdpa_uses_tensor_cores.restype = ctypes.c_int
     L.tree_mask_build.argtypes = [PT, B, B, P]
     L.tree_mask_build.restype = ctypes.c_int
     return L
@@ -151,6 +156,14 @@ def ta_launch_count() -> int:
 
 def ta_set_tree_path(path: int) -> int:
     return int(lib.ta_set_tree_path(path))
+
+
+def ta_set_quant_path(path: int) -> int:
+    return int(lib.ta_set_quant_path(path))
+
+
+def quant_sdpa_uses_tensor_cores(p: QuantParams) -> int:
+    return int(lib.quant_sdpa_uses_tensor_cores(ctypes.byref(p)))
 
 
 def tree_params(n_heads, n_kv_heads, head_dim, kv_seq_len, kv_capacity, scale, q_l, mask_stride,

@@ -29,6 +29,8 @@ namespace {
 thread_local std::string g_err;
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_tree_path{0};
+std::atomic<int> g_quant_path{0};   // 0 auto, 1 CUDA cores, 2 tensor cores where the shape allows
+constexpr int kQuantTcMinRows = 16;  // automatic choice: tensor cores from this many rows per KV row
 
 ta_status fail(ta_status st, const char *fmt, ...) {
     char buf[512];
@@ -386,12 +388,85 @@ uint32_t quant_row_groups(const ta_quant_params *p) {
     return (rep + (uint32_t)kQuantRowsPerCta - 1) / (uint32_t)kQuantRowsPerCta;
 }
 
+// Tensor-core quantized kernel: shape rules (params only, so that the split
+// count and tmp size do not depend on which masks a call passes): head
+// dimension 64, 128 or 256; TMEM for O (dim columns) and two score buffers
+// (groups x rows per CTA each) within 512 columns; the worst-case shared-memory
+// layout (both masks, shallowest rings) within the per-CTA limit.
+struct QtcShape {
+    int rr, rp, n_rb, cols;   // rows per CTA, MMA N (max(16, rr)), row blocks, TMEM columns
+};
+bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
+    const int path = g_quant_path.load(std::memory_order_relaxed);
+    if (path == 1) return false;
+    if (p->dim != 64 && p->dim != 128 && p->dim != 256) return false;
+    const int rep = (int)(p->n_q_heads / p->n_kv_heads);
+    // automatic choice: the tensor-core kernel from 16 query rows per KV row
+    // (draft-tree verification), where the CUDA-core kernel's per-row work dominates
+    if (path == 0 && rep < kQuantTcMinRows) return false;
+    const int ng = (int)(p->dim / p->group_size);
+    const int wpt = (int)(p->dim * p->bits / 32);
+    if (wpt % 4 != 0 || p->group_size % 16 != 0) return false;
+    sh->rr = rep <= 4 ? 4 : rep <= 8 ? 8 : rep <= 16 ? 16 : 32;
+    sh->rp = sh->rr < 16 ? 16 : sh->rr;
+    sh->n_rb = (rep + sh->rr - 1) / sh->rr;
+    const int need = (int)p->dim + 2 * ng * sh->rp;
+    if (need > 512) return false;
+    int cols = 32;
+    while (cols < need) cols <<= 1;
+    sh->cols = cols;
+    const QtcLayout L = qtc_layout(sh->rp, (int)p->dim, wpt, ng, 2, 2, 2, true, true);
+    return (size_t)L.total <= kQuantMaxSmem;
+}
+
+// Ring depths for the masks a call passes: four decoded chunks (two when
+// shared memory is short) and the deepest packed-K / packed-V rings (2..6)
+// that fit; the size is padded so that one CTA runs per SM (the TMEM budget
+// assumes it).
+struct QtcPlan {
+    int nd, nk, nv;
+    size_t smem;
+};
+bool quant_tc_plan(const ta_quant_params *p, const QtcShape &sh, bool has_mb, bool has_mf, QtcPlan *pl) {
+    const int ng = (int)(p->dim / p->group_size);
+    const int wpt = (int)(p->dim * p->bits / 32);
+    for (int nd = 4; nd >= 2; nd -= 2)
+        for (int n = 6; n >= 2; --n) {
+            const QtcLayout L = qtc_layout(sh.rp, (int)p->dim, wpt, ng, nd, n, n, has_mb, has_mf);
+            if ((size_t)L.total > kQuantMaxSmem) continue;
+            pl->nd = nd;
+            pl->nk = pl->nv = n;
+            pl->smem = (size_t)L.total < 120 * 1024 ? 120 * 1024 : (size_t)L.total;
+            return true;
+        }
+    return false;
+}
+
+uint32_t window_tiles(const ta_quant_params *p, uint32_t *j_lo) {
+    const uint32_t t_lo = p->tokens - window_tokens(p);
+    *j_lo = t_lo / 128u;
+    return (p->tokens + 127u) / 128u - *j_lo;
+}
+
 // Token splits: as many as fill every SM's resident one-warp CTAs in one wave
-// (kv rows x row groups x splits), at most one per chunk.
+// (kv rows x row groups x splits), at most one per chunk; for the tensor-core
+// kernel, one CTA per SM over (kv rows x row blocks x splits), at most one
+// split per 128-token tile.
 uint32_t resolve_quant_nwg(const ta_quant_params *p) {
     if (p->nwg != 0) return p->nwg;
     const int sms = sm_count();
     if (sms <= 0) return 0;
+    QtcShape sh;
+    if (quant_tc_shape(p, &sh)) {
+        const uint64_t units = (uint64_t)p->batch * p->n_kv_heads * (uint64_t)sh.n_rb;
+        uint64_t nwg = (uint64_t)sms / units;
+        uint32_t j_lo;
+        const uint64_t nt = window_tiles(p, &j_lo);
+        if (nwg > nt) nwg = nt;
+        if (nwg < 1) nwg = 1;
+        if (nwg > 65535) nwg = 65535;
+        return (uint32_t)nwg;
+    }
     const int per_sm = quant_ctas_per_sm((int)p->bits, (int)p->dim, (int)(p->dim / p->group_size));
     if (per_sm <= 0) return 0;
     const uint64_t units = (uint64_t)p->batch * p->n_kv_heads * quant_row_groups(p);
@@ -643,7 +718,26 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     a.out_f32 = out.dtype == TA_F32;
     a.scale = p->scale;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = launch_quant_fma(a, s);
+    cudaError_t e;
+    QtcShape sh;
+    QtcPlan pl;
+    if (quant_tc_shape(p, &sh) && quant_tc_plan(p, sh, has_bool, has_float, &pl)) {
+        uint32_t j_lo;
+        a.ntile = (int)window_tiles(p, &j_lo);
+        a.j_lo = (int)j_lo;
+        a.rp = sh.rr;
+        a.n_rb = sh.n_rb;
+        a.tc_cols = sh.cols;
+        a.tc_nd = pl.nd;
+        a.tc_nk = pl.nk;
+        a.tc_nv = pl.nv;
+        a.al_out = al16(out.ptr);
+        if ((uint64_t)kvr * (uint64_t)sh.n_rb > 65535u)
+            return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: too many KV rows x row blocks for one launch");
+        e = launch_quant_tc(a, pl.smem, s);
+    } else {
+        e = launch_quant_fma(a, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "quant_sdpa: main pass launch");
     if (nwg > 1) {
         e = launch_quant_merge(a, s);
@@ -659,4 +753,15 @@ TA_EXPORT uint64_t ta_launch_count(void) { return g_launches.load(std::memory_or
 TA_EXPORT int ta_set_tree_path(int path) {
     if (path < 0 || path > 2) return -1;
     return g_tree_path.exchange(path);
+}
+
+TA_EXPORT int ta_set_quant_path(int path) {
+    if (path < 0 || path > 2) return -1;
+    return g_quant_path.exchange(path);
+}
+
+TA_EXPORT int quant_sdpa_uses_tensor_cores(const ta_quant_params *p) {
+    if (check_quant_params(p) != TA_OK) return -1;
+    QtcShape sh;
+    return quant_tc_shape(p, &sh) ? 1 : 0;
 }

@@ -102,6 +102,18 @@ int quant_ctas_per_sm(int bits, int dim, int ng) {
     return 0;
 }
 
+int quant_tc_ctas_per_sm(int bits, int rp, size_t smem) {
+    if (bits == 4) return quant_tc_ctas_per_sm_b4(rp, smem);
+    if (bits == 8) return quant_tc_ctas_per_sm_b8(rp, smem);
+    return 0;
+}
+
+cudaError_t launch_quant_tc(const QuantArgs &a, size_t smem, cudaStream_t s) {
+    if (a.bits == 4) return launch_quant_tc_b4(a, smem, s);
+    if (a.bits == 8) return launch_quant_tc_b8(a, smem, s);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_quant_merge(const QuantArgs &a, cudaStream_t s) {
     cudaError_t e = a.t_is_bf16 ? launch_pdl(quant_merge_kernel<__nv_bfloat16>, dim3(a.rows), dim3(kMergeThreads), 0, s, a)
                                 : launch_pdl(quant_merge_kernel<__half>, dim3(a.rows), dim3(kMergeThreads), 0, s, a);

@@ -1,0 +1,742 @@
+// Attention over an affine-quantized K/V cache on the tensor cores (tcgen05).
+// Included by quant_tc_b4.cu and quant_tc_b8.cu, which instantiate it.
+//
+// What it computes is what the CUDA-core kernel computes (metaltile-std
+// flash_quantized_sdpa.rs: base, bool-mask and float-mask kernels): element d
+// of a K or V token is scale[d / G] * code_d + bias[d / G]; q is scaled by
+// `scale` before the dot; window and bool-mask gates; the float mask added to
+// the logit; a sink as a virtual key of value 0 (finalisation or merge).
+//
+// GB300 design.  One CTA = (token split, block of up to RR = 4, 8, 16 or 32
+// query rows of one KV row); the token range is walked in 128-token tiles.
+//   warp 0     : producer.  Per tile, the packed K words (one bulk copy) into
+//                the K ring; the packed V words, the four scale / bias runs
+//                (bulk copies, or plain loads for a ragged or unaligned tile)
+//                and the rows' bool / float mask runs (per-lane cp.async) into
+//                the V ring.
+//   warps 2..5 : decoders.  Packed codes become 16-bit operands in a ring of
+//                16 KB chunks ([128 tokens][64 dims], 128-byte swizzled): K as
+//                the exact integer codes (byte permutes under the f16 exponent
+//                of 1024, minus 1024), V as s * code + b rounded once to f16.
+//                Order: K_0, then K_t+1 before V_t, the MMA warp's order.
+//   warp 1     : TMEM owner and MMA issuer.  Scores transposed, tokens on the
+//                M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M 128
+//                tokens, N rp rows, one f32 accumulator per group, double
+//                buffered); O += P V (M 128 with rows 0..rp-1 real, N 64 per V
+//                chunk, V MN-major, P from shared memory).
+//   warps 6..9 : softmax, one thread per token (TMEM lane): logit of each row
+//                = 2^e_r * scale * log2(e) * sum_g s_g S^T_g + sum_g b_g *
+//                scale * log2(e) * sum_{d in g} q_d (+ log2(e) * float mask),
+//                (the sum accumulated in units of 2^e_r * scale * log2(e)),
+//                row maxima by a warp reduce-scatter and a four-warp exchange,
+//                lazy running max (moves only by more than 2^8), P in f16 into
+//                the A operand of PV, per-lane row sums; the warp on TMEM lanes
+//                0..31 rescales O when a max moves and writes the rows out.
+// Q is staged once as f16 after scaling each row by a power of two (2^-e_r,
+// max |q'| in [2^14, 2^15)), exact for f16 and bf16 queries; K codes enter
+// the MMA exactly, so the scores carry only f32 accumulation error; V values
+// and P carry one f16 rounding each.  For 4-bit codes the decoded dimensions
+// of every 8-dimension word sit in the order 0,4,1,5,2,6,3,7 (one mask-and-or
+// per pair); Q follows the same order and O columns are put back on output.
+// Every mbarrier wait is bounded; on a timeout the CTA sets bit 0 of the
+// error word, drains its copies and MMAs, frees TMEM and exits.
+#pragma once
+
+#include <type_traits>
+
+#include "sm100_ptx.cuh"
+#include "ta_internal.cuh"
+
+namespace ta {
+namespace qtc {
+
+using namespace ta::sm100;
+
+constexpr int kThreads = 320;
+constexpr uint32_t kPolls = 1u << 22;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kSlack = 8.0f;      // lazy-max slack (log2 units): P <= 256
+constexpr int kMaxRing = 8;
+
+struct Bars {
+    uint64_t kfull[kMaxRing], kempty[kMaxRing];
+    uint64_t vfull[kMaxRing], vempty[kMaxRing];
+    uint64_t dfull[kMaxRing], dempty[kMaxRing];
+    uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_done[2];   // per tile parity
+    uint64_t drain;
+    uint32_t tmem_base;
+    volatile int abort_flag;
+};
+static_assert(sizeof(Bars) <= kQtcBarBytes, "barrier area");
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float t2f(uint16_t bits, bool bf16) {
+    return bf16 ? __uint_as_float(static_cast<uint32_t>(bits) << 16) : __half2float(__ushort_as_half(bits));
+}
+__device__ __forceinline__ __half t2h(uint16_t bits, bool bf16) {
+    return bf16 ? __float2half_rn(__uint_as_float(static_cast<uint32_t>(bits) << 16)) : __ushort_as_half(bits);
+}
+__device__ __forceinline__ void cp16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void note_abort(Bars *b, int *err) {
+    b->abort_flag = 1;
+    atomicOr(err, 1);
+}
+// Bounded wait of one thread; false (and the CTA marked aborted) on timeout.
+__device__ __forceinline__ bool wait1(Bars *b, uint64_t *bar, uint32_t parity, int *err) {
+    if (b->abort_flag) return false;
+    if (mbar_wait(bar, parity, kPolls)) return true;
+    note_abort(b, err);
+    return false;
+}
+// Bounded wait of a whole warp: lane 0 polls (32 polling lanes per warp would
+// crowd the shared-memory pipe the working warps use), the warp barrier then
+// orders the other lanes after its acquire.  The result is warp-uniform.
+__device__ __forceinline__ bool waitw(Bars *b, uint64_t *bar, uint32_t parity, int *err) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait1(b, bar, parity, err);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok;
+}
+
+// Position of dimension k (0..7) of a 4-bit word in its decoded 8-dimension
+// piece (the decode leaves the pairs (c0, c4), (c1, c5), (c2, c6), (c3, c7)).
+__device__ __forceinline__ int pos4(int k) { return ((k & 3) << 1) | (k >> 2); }
+
+template <int N>
+__device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ldn<4>(uint32_t taddr, uint32_t (&r)[4]) { tmem_ld4(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_ldn<8>(uint32_t taddr, uint32_t (&r)[8]) { tmem_ld8(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_ldn<16>(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld16(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_ldn<32>(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld32(taddr, r); }
+
+// Reduce-scatter over groups of N lanes (xor 1 .. N/2): lane l returns the
+// max (or sum) over its group of value index l % N.  Destroys v.
+template <int N, bool MAX>
+__device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
+#pragma unroll
+    for (int s = 0; (1 << s) < N; ++s) {
+        const int m = 1 << s;
+        const bool upper = (lane & m) != 0;
+#pragma unroll
+        for (int k = 0; k < (N >> s) / 2; ++k) {
+            const float send = upper ? v[2 * k] : v[2 * k + 1];
+            const float keep = upper ? v[2 * k + 1] : v[2 * k];
+            const float got = __shfl_xor_sync(0xffffffffu, send, m);
+            v[k] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+    }
+    return v[0];
+}
+
+// Decode chunk c (dimensions [64c, 64c + 64)) of a tile's packed words into a
+// [128 tokens][64 x f16] 128-byte-swizzled operand chunk: the codes (K) or
+// s * code + b (V).  128 threads; a 16-byte item is four words of a token.
+template <int BITS>
+__device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int c, unsigned char *dst, int dtid,
+                                             bool is_v, const uint16_t *vs, const uint16_t *vb, int ng, int G,
+                                             bool bf16) {
+    constexpr int DPW = 32 / BITS;          // dimensions per word
+    constexpr int IPT = 64 / (4 * DPW);     // items per token and chunk (2 or 4)
+    constexpr int PPI = 4 * DPW / 8;        // 16-byte output pieces per item (4 or 2)
+    const __half2 k1024 = __float2half2_rn(1024.0f);
+#pragma unroll
+    for (int i = 0; i < IPT; ++i) {
+        const int it = dtid + 128 * i;
+        const int tok = it / IPT, h = it % IPT;
+        const uint4 w4 = *reinterpret_cast<const uint4 *>(words + tok * wpt + c * (64 / DPW) + h * 4);
+        const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
+        __half2 s2 = k1024, b2 = k1024;
+        if (is_v) {
+            const int g = (c * 64 + h * 4 * DPW) / G;
+            s2 = __half2half2(t2h(vs[tok * ng + g], bf16));
+            b2 = __half2half2(t2h(vb[tok * ng + g], bf16));
+        }
+        constexpr int NO = BITS == 4 ? 16 : 8;   // f16 pairs per item
+        uint32_t out[NO];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if constexpr (BITS == 4) {
+#pragma unroll
+                for (int k = 0; k < 4; ++k) out[u * 4 + k] = ((w[u] >> (4 * k)) & 0x000F000Fu) | 0x64006400u;
+            } else {
+                out[u * 2 + 0] = __byte_perm(w[u], 0x64646464u, 0x5140u);
+                out[u * 2 + 1] = __byte_perm(w[u], 0x64646464u, 0x5342u);
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < NO; ++e) {
+            __half2 x = __hsub2(*reinterpret_cast<__half2 *>(&out[e]), k1024);   // exact code
+            if (is_v) x = __hfma2(x, s2, b2);                                   // s * c + b, rounded once
+            out[e] = *reinterpret_cast<uint32_t *>(&x);
+        }
+#pragma unroll
+        for (int p = 0; p < PPI; ++p) {
+            const int j = h * PPI + p;
+            *reinterpret_cast<uint4 *>(dst + tok * 128 + ((j ^ (tok & 7)) << 4)) =
+                make_uint4(out[4 * p], out[4 * p + 1], out[4 * p + 2], out[4 * p + 3]);
+        }
+    }
+}
+
+// RR: query rows of a CTA (4, 8, 16 or 32); the score MMA's N (and the Q and
+// score-buffer layout) is RP = max(16, RR), its extra rows zero.
+template <int BITS, int RR>
+__global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a) {
+    constexpr int RP = RR < 16 ? 16 : RR;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    // 128-byte-swizzled operands need a 1024-byte-aligned base (the same for
+    // every CTA, so a misaligned one stops all of them before any barrier)
+    if ((smem_u32(smem) & 1023u) != 0) {
+        if (threadIdx.x == 0) atomicOr(a.err, 1);
+        return;
+    }
+    const bool has_mb = a.mbool != nullptr, has_mf = a.mfloat != nullptr;
+    const int NG = a.ng, DIM = a.dim, WPT = a.wpt, G = a.G, N = a.N;
+    const int ND = a.tc_nd, NK = a.tc_nk, NV = a.tc_nv;
+    const QtcLayout L = qtc_layout(RP, DIM, WPT, NG, ND, NK, NV, has_mb, has_mf);
+    Bars *bars = reinterpret_cast<Bars *>(smem + L.bars);
+    float *sF = reinterpret_cast<float *>(smem + L.rc);      // [RP] 2^e_r * scale * log2(e)
+    float *sQG = sF + RP;                                     // [NG][RP] 2^-e_r * sum_{d in g} q_d
+    float *sRed = reinterpret_cast<float *>(smem + L.red);   // [3][4][32] softmax exchange
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int split = blockIdx.x, rb = blockIdx.y % a.n_rb, kv = blockIdx.y / a.n_rb;
+    const int q0 = kv * a.rep + rb * RR;
+    const int rows_here = min(RR, a.rep - rb * RR);
+    const int j0 = a.j_lo + static_cast<int>((static_cast<long long>(split) * a.ntile) / a.nwg);
+    const int j1 = a.j_lo + static_cast<int>((static_cast<long long>(split + 1) * a.ntile) / a.nwg);
+    const int T = j1 - j0;
+    const int NCH = DIM / 64;
+    const bool bf16 = a.t_is_bf16 != 0;
+    int *err = a.err;
+
+    if (tid == 0) {
+        for (int i = 0; i < NK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 4); }
+        // V slot: the producer's expect-tx arrive, 32 cp.async arrivals, 32 plain arrivals
+        for (int i = 0; i < NV; ++i) { mbar_init(&bars->vfull[i], 65); mbar_init(&bars->vempty[i], 8); }
+        for (int i = 0; i < ND; ++i) { mbar_init(&bars->dfull[i], 4); mbar_init(&bars->dempty[i], 1); }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bars->s_full[i], 1);
+            mbar_init(&bars->s_free[i], 4);
+            mbar_init(&bars->p_full[i], 4);
+            mbar_init(&bars->p_free[i], 1);
+            mbar_init(&bars->o_done[i], 1);
+        }
+        mbar_init(&bars->drain, 1);
+        bars->abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, static_cast<uint32_t>(a.tc_cols));
+        tmem_relinquish();
+    }
+
+    // ---- Q operand (f16, rows scaled by 2^-e_r) and per-row constants
+    {
+        const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
+        const int E = DIM / 32;                 // dimensions per lane (2, 4 or 8)
+        const float qs = a.scale * kLog2e;
+        for (int r = warp; r < RP; r += kThreads / 32) {
+            const bool live = r < rows_here;
+            float x[8];
+            float amax = 0.0f, gs = 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                x[e] = 0.0f;
+                if (e < E && live) x[e] = t2f(qg[static_cast<size_t>(q0 + r) * DIM + lane * E + e], bf16);
+                amax = fmaxf(amax, fabsf(x[e]));
+                gs += x[e];
+            }
+            amax = warp_max(amax);
+            const int ex = amax > 0.0f ? ilogbf(amax) - 14 : 0;
+            const int lpg = G / E;              // lanes per scale group (power of two <= 32)
+            for (int m = 1; m < lpg; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
+            // the bias term in units of the row factor: sum_g b_g * 2^-e_r * sum_{d in g} q_d
+            if (lane % lpg == 0) sQG[(lane * E / G) * RP + r] = live ? ldexpf(gs, -ex) : 0.0f;
+            if (lane == 0) sF[r] = live ? ldexpf(qs, ex) : 0.0f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                if (e >= E) break;
+                const int d = lane * E + e;
+                const int pos = BITS == 4 ? ((d & ~7) | pos4(d & 7)) : d;
+                const int blk = pos >> 6, pc = (pos & 63) >> 3;
+                *reinterpret_cast<__half *>(smem + L.q0 + blk * RP * 128 + r * 128 + ((pc ^ (r & 7)) << 4) +
+                                            (pos & 7) * 2) = __float2half_rn(ldexpf(x[e], -ex));
+            }
+        }
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+    const uint32_t tm_o = tmem;
+    auto tm_s = [&](int sb) { return tmem + static_cast<uint32_t>(DIM + sb * NG * RP); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        int kn = 0, vn = 0;
+        const size_t row0 = static_cast<size_t>(kv) * N;
+        // scale / bias run k (0..3: K scales, K biases, V scales, V biases): source and slot offset
+        auto sb_src = [&](int k) {
+            return static_cast<const uint16_t *>(k == 0 ? a.ks : k == 1 ? a.kb : k == 2 ? a.vs : a.vb);
+        };
+        auto sb_off = [&](int k) { return k == 0 ? L.vks : k == 1 ? L.vkb : k == 2 ? L.vvs : L.vvb; };
+        for (int t = 0; t < T; ++t) {
+            const int t0 = (j0 + t) * 128;
+            const int tval = min(128, N - t0);
+            const bool full = tval == 128;
+            bool ok = true;
+            {
+                const int slot = kn % NK;
+                if (lane == 0) {
+                    ok = wait1(bars, &bars->kempty[slot], (static_cast<uint32_t>(kn / NK) & 1u) ^ 1u, err);
+                    if (ok) {
+                        const uint32_t bytes = static_cast<uint32_t>(tval * WPT * 4);
+                        mbar_arrive_expect_tx(&bars->kfull[slot], bytes);
+                        bulk_load(smem + L.k0 + slot * L.kslot, a.kp + (row0 + t0) * WPT, bytes, &bars->kfull[slot]);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                ++kn;
+            }
+            {
+                const int slot = vn % NV;
+                unsigned char *st = smem + L.v0 + slot * L.vslot;
+                const bool sb_bulk = a.al_sb && full;
+                const uint32_t sbb = static_cast<uint32_t>(128 * NG * 2);
+                if (lane == 0) {
+                    ok = wait1(bars, &bars->vempty[slot], (static_cast<uint32_t>(vn / NV) & 1u) ^ 1u, err);
+                    if (ok) {
+                        const uint32_t vbytes = static_cast<uint32_t>(tval * WPT * 4);
+                        mbar_arrive_expect_tx(&bars->vfull[slot], vbytes + (sb_bulk ? 4 * sbb : 0u));
+                        bulk_load(st + L.vw, a.vp + (row0 + t0) * WPT, vbytes, &bars->vfull[slot]);
+                        if (sb_bulk)
+                            for (int k = 0; k < 4; ++k)
+                                bulk_load(st + sb_off(k), sb_src(k) + (row0 + t0) * NG, sbb, &bars->vfull[slot]);
+                    }
+                }
+                if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                ++vn;
+                if (!sb_bulk) {
+                    const int per = 128 * NG, valid = tval * NG;
+                    for (int i = lane; i < 4 * per; i += 32) {
+                        const int k = i / per, e = i % per;
+                        reinterpret_cast<uint16_t *>(st + sb_off(k))[e] =
+                            e < valid ? sb_src(k)[(row0 + t0) * NG + e] : static_cast<uint16_t>(0);
+                    }
+                }
+                if (has_mb) {
+                    uint32_t *dst = reinterpret_cast<uint32_t *>(st + L.vmb);
+                    if (a.al_mb && full) {
+                        for (int i = lane; i < rows_here * 32; i += 32) {
+                            const int r = i >> 5, pc = i & 31;
+                            cp16(dst + r * 128 + 4 * pc, a.mbool + static_cast<size_t>(q0 + r) * N + t0 + 4 * pc);
+                        }
+                    } else {
+                        for (int i = lane; i < rows_here * 128; i += 32) {
+                            const int r = i >> 7, k = i & 127;
+                            dst[i] = k < tval ? a.mbool[static_cast<size_t>(q0 + r) * N + t0 + k] : 0u;
+                        }
+                    }
+                }
+                if (has_mf) {
+                    uint16_t *dst = reinterpret_cast<uint16_t *>(st + L.vmf);
+                    const uint16_t *mf = static_cast<const uint16_t *>(a.mfloat);
+                    if (a.al_mf && full) {
+                        for (int i = lane; i < rows_here * 16; i += 32) {
+                            const int r = i >> 4, pc = i & 15;
+                            cp16(dst + r * 128 + 8 * pc, mf + static_cast<size_t>(q0 + r) * N + t0 + 8 * pc);
+                        }
+                    } else {
+                        for (int i = lane; i < rows_here * 128; i += 32) {
+                            const int r = i >> 7, k = i & 127;
+                            dst[i] = k < tval ? mf[static_cast<size_t>(q0 + r) * N + t0 + k] : static_cast<uint16_t>(0);
+                        }
+                    }
+                }
+                cp_arrive_noinc(&bars->vfull[slot]);   // when this lane's cp.async copies have landed
+                mbar_arrive(&bars->vfull[slot]);       // after this lane's plain stores (release)
+            }
+        }
+        // Drain: every copy issued into this CTA's rings has landed.
+        if (lane == 0) {
+            for (int n = kn > NK ? kn - NK : 0; n < kn; ++n)
+                if (!mbar_wait(&bars->kfull[n % NK], static_cast<uint32_t>(n / NK) & 1u, kPolls)) note_abort(bars, err);
+            for (int n = vn > NV ? vn - NV : 0; n < vn; ++n)
+                if (!mbar_wait(&bars->vfull[n % NV], static_cast<uint32_t>(n / NV) & 1u, kPolls)) note_abort(bars, err);
+        }
+    } else if (warp == 1) {
+        // ---------------------------------------------------------- MMA issuer
+        if (lane == 0 && T > 0) {
+            const uint32_t id_s = idesc_f16(128, RP, 0, 0, 0);
+            const uint32_t id_pv = idesc_f16(128, 64, 0, 0, 1);
+            const uint32_t q_addr = smem_u32(smem + L.q0), d_addr = smem_u32(smem + L.d0);
+            const uint32_t p_addr = smem_u32(smem + L.p0);
+            int dn = 0;
+            auto take = [&](uint32_t *ca) -> bool {
+                const int slot = dn % ND;
+                if (!wait1(bars, &bars->dfull[slot], static_cast<uint32_t>(dn / ND) & 1u, err)) return false;
+                tc_fence_after();
+                *ca = d_addr + slot * kQtcChunk;
+                return true;
+            };
+            auto give = [&]() {
+                mma_commit(&bars->dempty[dn % ND]);
+                ++dn;
+            };
+            auto issue_s = [&](int t) -> bool {
+                const int sb = t & 1;
+                if (!wait1(bars, &bars->s_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err)) return false;
+                tc_fence_after();
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t ca;
+                    if (!take(&ca)) return false;
+#pragma unroll
+                    for (int k4 = 0; k4 < 4; ++k4) {
+                        const int d0 = c * 64 + k4 * 16;    // first dimension of the k-step
+                        mma_f16_ss(tm_s(sb) + static_cast<uint32_t>((d0 / G) * RP),
+                                   sw128_desc(ca + k4 * 32, 16, 1024),
+                                   sw128_desc(q_addr + c * RP * 128 + k4 * 32, 16, 1024), id_s, (d0 % G) != 0);
+                    }
+                    give();
+                }
+                mma_commit(&bars->s_full[sb]);
+                return true;
+            };
+            auto issue_pv = [&](int t) -> bool {
+                if (!wait1(bars, &bars->p_full[t & 1], (static_cast<uint32_t>(t) >> 1) & 1u, err)) return false;
+                tc_fence_after();
+                const uint32_t pa = p_addr + (t & 1) * 2 * L.pkb;
+                for (int c = 0; c < NCH; ++c) {
+                    uint32_t ca;
+                    if (!take(&ca)) return false;
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_f16_ss(tm_o + c * 64, sw128_desc(pa + (kk >> 2) * L.pkb + (kk & 3) * 32, 16, 1024),
+                                   sw128_desc(ca + kk * 2048, kQtcChunk, 1024), id_pv, (t | kk) != 0);
+                    give();
+                }
+                mma_commit(&bars->o_done[t & 1]);
+                mma_commit(&bars->p_free[t & 1]);   // P_t buffer free once PV_t is done
+                return true;
+            };
+            bool ok = issue_s(0);
+            for (int t = 0; t < T && ok; ++t) {
+                if (t + 1 < T) ok = issue_s(t + 1);
+                if (ok) ok = issue_pv(t);
+            }
+            // Drain: all MMAs issued by this thread have completed.
+            mma_commit(&bars->drain);
+            if (!mbar_wait(&bars->drain, 0, kPolls)) note_abort(bars, err);
+        }
+    } else if (warp < 6) {
+        // ------------------------------------------------------------ decoders
+        const int dtid = tid - 64;
+        int dn = 0;
+        auto put = [&](const uint32_t *words, int c, bool is_v, const uint16_t *vs, const uint16_t *vb) -> bool {
+            const int slot = dn % ND;
+            if (!waitw(bars, &bars->dempty[slot], (static_cast<uint32_t>(dn / ND) & 1u) ^ 1u, err)) return false;
+            decode_chunk<BITS>(words, WPT, c, smem + L.d0 + slot * kQtcChunk, dtid, is_v, vs, vb, NG, G, bf16);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->dfull[slot]);
+            ++dn;
+            return true;
+        };
+        auto do_k = [&](int t) -> bool {
+            const int slot = t % NK;
+            if (!waitw(bars, &bars->kfull[slot], static_cast<uint32_t>(t / NK) & 1u, err)) return false;
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(smem + L.k0 + slot * L.kslot);
+            for (int c = 0; c < NCH; ++c)
+                if (!put(words, c, false, nullptr, nullptr)) return false;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->kempty[slot]);
+            return true;
+        };
+        auto do_v = [&](int t) -> bool {
+            const int slot = t % NV;
+            if (!waitw(bars, &bars->vfull[slot], static_cast<uint32_t>(t / NV) & 1u, err)) return false;
+            const unsigned char *st = smem + L.v0 + slot * L.vslot;
+            const uint32_t *words = reinterpret_cast<const uint32_t *>(st + L.vw);
+            const uint16_t *vs = reinterpret_cast<const uint16_t *>(st + L.vvs);
+            const uint16_t *vb = reinterpret_cast<const uint16_t *>(st + L.vvb);
+            for (int c = 0; c < NCH; ++c)
+                if (!put(words, c, true, vs, vb)) return false;
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->vempty[slot]);
+            return true;
+        };
+        bool ok = T > 0 ? do_k(0) : true;
+        for (int t = 0; t < T && ok; ++t) {
+            if (t + 1 < T) ok = do_k(t + 1);
+            if (ok) ok = do_v(t);
+        }
+    } else {
+        // -------------------------------------------- softmax and epilogue
+        const int quarter = warp & 3;
+        const int tl = quarter * 32 + lane;                 // token of the tile = TMEM lane
+        const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
+        auto group_sync = [&]() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
+        float lsum[RR];
+#pragma unroll
+        for (int r = 0; r < RR; ++r) lsum[r] = 0.0f;
+        float m_row = -INFINITY;                            // running max (log2 units) of row lane % RR
+        bool ok = true;
+        for (int t = 0; t < T; ++t) {
+            const int sb = t & 1;
+            const int vslot = t % NV;
+            const int tok = (j0 + t) * 128 + tl;
+            const bool tok_ok = tok >= a.t_lo && tok < N;
+            ok = ok && waitw(bars, &bars->vfull[vslot], static_cast<uint32_t>(t / NV) & 1u, err);
+            ok = ok && waitw(bars, &bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, err);
+            tc_fence_after();
+            const unsigned char *st = smem + L.v0 + vslot * L.vslot;
+            const uint16_t *ks = reinterpret_cast<const uint16_t *>(st + L.vks);
+            const uint16_t *kb = reinterpret_cast<const uint16_t *>(st + L.vkb);
+            float acc[RR];   // sum_g s_g S^T_g + b_g * 2^-e_r * sum_{d in g} q_d
+#pragma unroll
+            for (int r = 0; r < RR; ++r) acc[r] = 0.0f;
+            if (ok) {
+#pragma unroll 1
+                for (int g = 0; g < NG; ++g) {
+                    uint32_t d[RR];
+                    tmem_ldn<RR>(tm_s(sb) + lane_off + static_cast<uint32_t>(g * RP), d);
+                    tmem_wait_ld();
+                    const float s = t2f(ks[tl * NG + g], bf16), b = t2f(kb[tl * NG + g], bf16);
+                    const float4 *qg4 = reinterpret_cast<const float4 *>(sQG + g * RP);
+#pragma unroll
+                    for (int r4 = 0; r4 < RR / 4; ++r4) {
+                        const float4 qv = qg4[r4];
+                        acc[4 * r4 + 0] = fmaf(s, __uint_as_float(d[4 * r4 + 0]), fmaf(b, qv.x, acc[4 * r4 + 0]));
+                        acc[4 * r4 + 1] = fmaf(s, __uint_as_float(d[4 * r4 + 1]), fmaf(b, qv.y, acc[4 * r4 + 1]));
+                        acc[4 * r4 + 2] = fmaf(s, __uint_as_float(d[4 * r4 + 2]), fmaf(b, qv.z, acc[4 * r4 + 2]));
+                        acc[4 * r4 + 3] = fmaf(s, __uint_as_float(d[4 * r4 + 3]), fmaf(b, qv.w, acc[4 * r4 + 3]));
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&bars->s_free[sb]);   // S_t read out of TMEM
+            float (&lg)[RR] = acc;   // logits (log2 units), in place
+            const bool live_tok = ok && tok_ok;
+#pragma unroll
+            for (int r = 0; r < RR; ++r) lg[r] = (live_tok && r < rows_here) ? acc[r] * sF[r] : -INFINITY;
+            if (has_mf) {
+                const uint16_t *mf = reinterpret_cast<const uint16_t *>(st + L.vmf) + tl;
+#pragma unroll
+                for (int r = 0; r < RR; ++r)
+                    if (r < rows_here) lg[r] = fmaf(kLog2e, t2f(mf[r * 128], bf16), lg[r]);
+            }
+            if (has_mb) {
+                const uint32_t *mb = reinterpret_cast<const uint32_t *>(st + L.vmb) + tl;
+#pragma unroll
+                for (int r = 0; r < RR; ++r)
+                    if (r < rows_here && mb[r * 128] == 0u) lg[r] = -INFINITY;
+            }
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&bars->vempty[vslot]);   // scales and masks read
+
+            // row maxima of the tile: warp reduce-scatter, then the four warps
+            float tmp[RR];
+#pragma unroll
+            for (int r = 0; r < RR; ++r) tmp[r] = lg[r];
+            float wm = reduce_scatter<RR, true>(tmp, lane);
+#pragma unroll
+            for (int m = RR; m < 32; m <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, m));
+            sRed[(sb * 4 + quarter) * 32 + lane] = wm;
+            group_sync();
+            const float tmax = fmaxf(fmaxf(sRed[(sb * 4 + 0) * 32 + lane], sRed[(sb * 4 + 1) * 32 + lane]),
+                                     fmaxf(sRed[(sb * 4 + 2) * 32 + lane], sRed[(sb * 4 + 3) * 32 + lane]));
+            float alpha = 1.0f;
+            if (tmax > m_row + kSlack) {
+                alpha = m_row == -INFINITY ? 0.0f : ex2(m_row - tmax);
+                m_row = tmax;
+            }
+            const bool need = __any_sync(0xffffffffu, alpha != 1.0f);   // same in the four warps
+            if (need) {
+#pragma unroll
+                for (int r = 0; r < RR; ++r) lsum[r] *= __shfl_sync(0xffffffffu, alpha, r);
+            }
+            // the P buffer of this tile is free once PV of tile t - 2 is done
+            ok = ok && waitw(bars, &bars->p_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err);
+            if (quarter == 0 && need && t > 0) {
+                // rows moved their max: rescale O (rows = TMEM lanes 0..31) once
+                // PV of the previous tile is done
+                ok = ok && waitw(bars, &bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, err);
+                tc_fence_after();
+                if (ok) {
+#pragma unroll 1
+                    for (int c = 0; c < DIM / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_ld32(tm_o + c * 32, v);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        tmem_st32(tm_o + c * 32, v);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            unsigned char *pb = smem + L.p0 + sb * 2 * L.pkb + (tl >> 6) * L.pkb;
+            const int tc = tl & 63;
+#pragma unroll
+            for (int r = 0; r < RR; ++r) {
+                const float m = __shfl_sync(0xffffffffu, m_row, r);
+                const __half ph = __float2half_rn(ex2(lg[r] - (m == -INFINITY ? 0.0f : m)));
+                lsum[r] += __half2float(ph);
+                if (r < rows_here)
+                    *reinterpret_cast<__half *>(pb + r * 128 + (((tc >> 3) ^ (r & 7)) << 4) + (tc & 7) * 2) = ph;
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && ok) mbar_arrive(&bars->p_full[sb]);
+        }
+        pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
+        if (T > 0) {
+            ok = ok && waitw(bars, &bars->o_done[(T - 1) & 1], (static_cast<uint32_t>(T - 1) >> 1) & 1u, err);
+            tc_fence_after();
+        }
+        // row sums over the four warps' tokens
+        float ls = reduce_scatter<RR, false>(lsum, lane);
+#pragma unroll
+        for (int m = RR; m < 32; m <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
+        sRed[(8 + quarter) * 32 + lane] = ls;
+        group_sync();
+        if (quarter == 0 && ok) {
+            const float l_tot = (sRed[8 * 32 + lane] + sRed[9 * 32 + lane]) + (sRed[10 * 32 + lane] + sRed[11 * 32 + lane]);
+            const int r = lane;                              // O row = TMEM lane
+            const bool live = r < rows_here;
+            const int q = q0 + r;
+            float f = 1.0f;
+            if (a.nwg == 1 && live) {
+                float cf = 1.0f, sf = l_tot;
+                if (a.has_sinks) {
+                    const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
+                    const float mx = fmaxf(m_row, sk);
+                    cf = m_row == -INFINITY ? 0.0f : ex2(m_row - mx);
+                    sf = l_tot * cf + ex2(sk - mx);
+                }
+                f = sf > 0.0f ? cf / sf : 0.0f;
+            }
+#pragma unroll 1
+            for (int c = 0; c < DIM / 32; ++c) {
+                uint32_t v[32];
+                if (T > 0) {
+                    tmem_ld32(tm_o + c * 32, v);
+                    tmem_wait_ld();
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                }
+                if (!live) continue;
+#pragma unroll
+                for (int g8 = 0; g8 < 4; ++g8) {
+                    float o[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)   // for 4-bit codes dimension k of the word sits at column pos4(k)
+                        o[k] = __uint_as_float(v[8 * g8 + (BITS == 4 ? pos4(k) : k)]) * f;
+                    const size_t base = static_cast<size_t>(q) * DIM + c * 32 + g8 * 8;
+                    if (a.nwg > 1) {
+                        float4 *po = reinterpret_cast<float4 *>(a.part_o + static_cast<size_t>(split) * a.rows * DIM + base);
+                        po[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        po[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    } else if (!a.al_out) {
+#pragma unroll
+                        for (int k = 0; k < 8; ++k) {
+                            if (a.out_f32) static_cast<float *>(a.out)[base + k] = o[k];
+                            else if (bf16) static_cast<__nv_bfloat16 *>(a.out)[base + k] = __float2bfloat16_rn(o[k]);
+                            else static_cast<__half *>(a.out)[base + k] = __float2half_rn(o[k]);
+                        }
+                    } else if (a.out_f32) {
+                        float4 *po = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + base);
+                        po[0] = make_float4(o[0], o[1], o[2], o[3]);
+                        po[1] = make_float4(o[4], o[5], o[6], o[7]);
+                    } else {
+                        uint32_t pk[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            if (bf16) {
+                                __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
+                                pk[e] = *reinterpret_cast<uint32_t *>(&h);
+                            } else {
+                                __half2 h = __floats2half2_rn(o[2 * e], o[2 * e + 1]);
+                                pk[e] = *reinterpret_cast<uint32_t *>(&h);
+                            }
+                        }
+                        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + base) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    }
+                }
+            }
+            if (a.nwg > 1 && live)
+                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q] = make_float2(l_tot, m_row);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, static_cast<uint32_t>(a.tc_cols));
+    }
+}
+
+template <int BITS, int RR>
+cudaError_t launch_rr(const QuantArgs &a, size_t smem, cudaStream_t s) {
+    auto kern = quant_tc_kernel<BITS, RR>;
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(a.nwg, a.kv_rows * a.n_rb), kThreads, smem, s>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int BITS>
+cudaError_t launch_bits(const QuantArgs &a, size_t smem, cudaStream_t s) {
+    switch (a.rp) {
+        case 4: return launch_rr<BITS, 4>(a, smem, s);
+        case 8: return launch_rr<BITS, 8>(a, smem, s);
+        case 16: return launch_rr<BITS, 16>(a, smem, s);
+        case 32: return launch_rr<BITS, 32>(a, smem, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int BITS, int RR>
+int occupancy_rr(size_t smem) {
+    auto kern = quant_tc_kernel<BITS, RR>;
+    static unsigned long long done = 0;
+    if (set_smem_limit_once(kern, kQuantMaxSmem, &done) != cudaSuccess) { cudaGetLastError(); return 0; }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return n;
+}
+
+template <int BITS>
+int occupancy_bits(int rp, size_t smem) {
+    return rp <= 4 ? occupancy_rr<BITS, 4>(smem) : rp <= 8 ? occupancy_rr<BITS, 8>(smem)
+         : rp <= 16 ? occupancy_rr<BITS, 16>(smem) : occupancy_rr<BITS, 32>(smem);
+}
+
+}  // namespace qtc
+}  // namespace ta

@@ -124,6 +124,11 @@ struct QuantArgs {
     int *err;                // error word (bit 0: a copy wait timed out), never cleared here
     int t_is_bf16, out_f32;
     float scale;
+    // tensor-core kernel only: rows per CTA (4, 8, 16 or 32), row blocks per KV row,
+    // first 128-token tile and tile count of the window, ring depths (decoded
+    // chunks, packed-K slots, packed-V slots) and TMEM columns
+    int rp, n_rb, j_lo, ntile, tc_nd, tc_nk, tc_nv, tc_cols;
+    int al_out;              // out starts on a 16-byte boundary
 };
 
 // Query rows served by one CTA of the quantized-KV kernel (a row group).
@@ -176,6 +181,61 @@ __host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
     L.total = o;
     return L;
 }
+// Shared-memory layout of the tensor-core quantized-KV kernel (byte offsets).
+// Two P buffers (A operand of PV: [128 rows][128 tokens] 16-bit, 128-byte
+// swizzled, only the first rp rows written; the MMA's reads of the other rows
+// stay inside the CTA's shared memory), the 16-bit Q operand ([rp][dim],
+// 64-dimension blocks), the ring of decoded 16 KB chunks ([128 tokens][64
+// dims] f16), the packed-K ring, the packed-V ring (V words, K and V scale /
+// bias runs, bool and float mask rows), per-row constants, the softmax
+// exchange area and the mbarriers.
+struct QtcLayout {
+    int pkb;                              // bytes of a 64-token k-block of a P buffer (rp x 128 B)
+    int p0, q0, d0, k0, kslot, v0, vslot;
+    int vw, vks, vkb, vvs, vvb, vmb, vmf;  // inside a packed-V slot
+    int rc, red, bars, total;
+};
+constexpr int kQtcChunk = 16384;
+constexpr int kQtcBarBytes = 1024;
+__host__ __device__ inline int qtc_align(int o, int a) { return (o + a - 1) / a * a; }
+__host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng, int nd, int nk, int nv,
+                                                bool has_mb, bool has_mf) {
+    QtcLayout L;
+    L.pkb = rp * 128;
+    int o = 0;
+    L.p0 = o;
+    o += 4 * L.pkb;
+    o = qtc_align(o, 1024);
+    L.q0 = o;
+    o += (dim / 64) * rp * 128;
+    o = qtc_align(o, 1024);
+    L.d0 = o;
+    o += nd * kQtcChunk;
+    L.kslot = qtc_align(128 * wpt * 4, 16);
+    L.k0 = o;
+    o += nk * L.kslot;
+    int v = 0;
+    L.vw = v;  v = qtc_align(v + 128 * wpt * 4, 16);
+    L.vks = v; v = qtc_align(v + 128 * ng * 2, 16);
+    L.vkb = v; v = qtc_align(v + 128 * ng * 2, 16);
+    L.vvs = v; v = qtc_align(v + 128 * ng * 2, 16);
+    L.vvb = v; v = qtc_align(v + 128 * ng * 2, 16);
+    L.vmb = v; if (has_mb) v = qtc_align(v + rp * 128 * 4, 16);
+    L.vmf = v; if (has_mf) v = qtc_align(v + rp * 128 * 2, 16);
+    L.vslot = v;
+    L.v0 = o;
+    o += nv * L.vslot;
+    L.rc = o;
+    o = qtc_align(o + (rp + ng * rp) * 4, 16);
+    L.red = o;
+    o = qtc_align(o + 3 * 4 * 32 * 4, 16);
+    o = qtc_align(o, 8);
+    L.bars = o;
+    o += kQtcBarBytes;
+    L.total = o;
+    return L;
+}
+
 // Head-dimension capacity of the kernel instance serving `dim` (64..512), and
 // its chunk length in tokens (32 when a token has at most 32 packed words).
 __host__ __device__ inline int quant_dim_capacity(int dim) {
@@ -214,6 +274,14 @@ cudaError_t launch_quant_b8(const QuantArgs &a, cudaStream_t s);
 int quant_ctas_per_sm(int bits, int dim, int ng);
 int quant_ctas_per_sm_b4(int dim, int ng);
 int quant_ctas_per_sm_b8(int dim, int ng);
+// Tensor-core quantized-KV kernel (rows on the N side of the score MMA):
+// launch, and resident CTAs per SM for a dynamic shared-memory size.
+cudaError_t launch_quant_tc(const QuantArgs &a, size_t smem, cudaStream_t s);
+cudaError_t launch_quant_tc_b4(const QuantArgs &a, size_t smem, cudaStream_t s);
+cudaError_t launch_quant_tc_b8(const QuantArgs &a, size_t smem, cudaStream_t s);
+int quant_tc_ctas_per_sm(int bits, int rp, size_t smem);
+int quant_tc_ctas_per_sm_b4(int rp, size_t smem);
+int quant_tc_ctas_per_sm_b8(int rp, size_t smem);
 
 // Rows of one CTA in the CUDA-core tree kernel.
 constexpr int kFmaRowsPerCta = 16;
