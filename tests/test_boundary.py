@@ -305,7 +305,8 @@ def test_quant_kernel_family_choice(ta):
         assert ta.quant_sdpa_uses_tensor_cores(p(512, nQ=256)) == 0
         ta.ta_set_quant_path(2)
         assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 1
-        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8)) == 1
+        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=4)) == 1
+        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8)) == 0       # rings exceed shared memory
         assert ta.quant_sdpa_uses_tensor_cores(p(64, G=32)) == 1
         assert ta.quant_sdpa_uses_tensor_cores(p(512)) == 0            # O alone fills TMEM
         assert ta.quant_sdpa_uses_tensor_cores(p(96, G=32)) == 0       # not a multiple of 64

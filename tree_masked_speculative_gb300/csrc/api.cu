@@ -415,14 +415,15 @@ bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
     int cols = 32;
     while (cols < need) cols <<= 1;
     sh->cols = cols;
-    const QtcLayout L = qtc_layout(sh->rp, (int)p->dim, wpt, ng, 2, 2, 2, true, true);
+    const QtcLayout L = qtc_layout(sh->rp, (int)p->dim, wpt, ng, (int)p->dim / 64, 2, 2, true, true);
     return (size_t)L.total <= kQuantMaxSmem;
 }
 
-// Ring depths for the masks a call passes: four decoded chunks (two when
-// shared memory is short) and the deepest packed-K / packed-V rings (2..6)
-// that fit; the size is padded so that one CTA runs per SM (the TMEM budget
-// assumes it).
+// Ring depths for the masks a call passes: the decoded-chunk ring holds up to
+// four K or V tile parts (dim / 64 chunks each) so that the decoders run ahead
+// of the MMA warp, the packed-K / packed-V rings three or two tiles; the
+// deepest combination that fits.  The size is padded so that one CTA runs per
+// SM (the TMEM budget assumes it).
 struct QtcPlan {
     int nd, nk, nv;
     size_t smem;
@@ -430,8 +431,11 @@ struct QtcPlan {
 bool quant_tc_plan(const ta_quant_params *p, const QtcShape &sh, bool has_mb, bool has_mf, QtcPlan *pl) {
     const int ng = (int)(p->dim / p->group_size);
     const int wpt = (int)(p->dim * p->bits / 32);
-    for (int nd = 4; nd >= 2; nd -= 2)
-        for (int n = 6; n >= 2; --n) {
+    const int nch = (int)p->dim / 64;
+    for (int parts = 4; parts >= 1; --parts)
+        for (int n = 3; n >= 2; --n) {
+            const int nd = parts * nch;
+            if (nd > kQuantTcMaxRing) continue;
             const QtcLayout L = qtc_layout(sh.rp, (int)p->dim, wpt, ng, nd, n, n, has_mb, has_mf);
             if ((size_t)L.total > kQuantMaxSmem) continue;
             pl->nd = nd;

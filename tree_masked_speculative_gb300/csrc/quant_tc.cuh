@@ -9,29 +9,29 @@
 //
 // GB300 design.  One CTA = (token split, block of up to RR = 4, 8, 16 or 32
 // query rows of one KV row); the token range is walked in 128-token tiles.
-//   warp 0     : producer.  Per tile, the packed K words (one bulk copy) into
-//                the K ring; the packed V words, the four scale / bias runs
-//                (bulk copies, or plain loads for a ragged or unaligned tile)
-//                and the rows' bool / float mask runs (per-lane cp.async) into
-//                the V ring.
-//   warps 2..5 : decoders.  Packed codes become 16-bit operands in a ring of
-//                16 KB chunks ([128 tokens][64 dims], 128-byte swizzled): K as
-//                the exact integer codes (byte permutes under the f16 exponent
-//                of 1024, minus 1024), V as s * code + b rounded once to f16.
-//                Order: K_0, then K_t+1 before V_t, the MMA warp's order.
-//   warp 1     : TMEM owner and MMA issuer.  Scores transposed, tokens on the
-//                M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M 128
-//                tokens, N rp rows, one f32 accumulator per group, double
-//                buffered); O += P V (M 128 with rows 0..rp-1 real, N 64 per V
-//                chunk, V MN-major, P from shared memory).
-//   warps 6..9 : softmax, one thread per token (TMEM lane): logit of each row
-//                = 2^e_r * scale * log2(e) * sum_g s_g S^T_g + sum_g b_g *
-//                scale * log2(e) * sum_{d in g} q_d (+ log2(e) * float mask),
-//                (the sum accumulated in units of 2^e_r * scale * log2(e)),
-//                row maxima by a warp reduce-scatter and a four-warp exchange,
-//                lazy running max (moves only by more than 2^8), P in f16 into
-//                the A operand of PV, per-lane row sums; the warp on TMEM lanes
-//                0..31 rescales O when a max moves and writes the rows out.
+//   warp 0      : producer.  Per tile, the packed K words (one bulk copy) into
+//                 the K ring; the packed V words, the four scale / bias runs
+//                 (bulk copies, or plain loads for a ragged or unaligned tile)
+//                 and the rows' bool / float mask runs (per-lane cp.async) into
+//                 the V ring.
+//   warps 2..9  : decoders.  Packed codes become 16-bit operands in a ring of
+//                 16 KB chunks ([128 tokens][64 dims], 128-byte swizzled): K as
+//                 the exact integer codes (byte permutes under the f16 exponent
+//                 of 1024, minus 1024), V as s * code + b rounded once to f16.
+//                 Order: K_0, then K_t+1 before V_t, the MMA warp's order.
+//   warp 1      : TMEM owner and MMA issuer.  Scores transposed, tokens on the
+//                 M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M 128
+//                 tokens, N = max(16, RR) rows, one f32 accumulator per group,
+//                 double buffered); O += P V (M 128 with rows 0..RR-1 real, N 64
+//                 per V chunk, V MN-major, P from shared memory).
+//   warps 10..17: softmax, one thread per (token, half of the rows): logit =
+//                 2^e_r * scale * log2(e) * (sum_g s_g S^T_g + b_g * 2^-e_r *
+//                 sum_{d in g} q_d) (+ log2(e) * float mask); row maxima by a
+//                 warp reduce-scatter and an exchange among the four warps of a
+//                 half; lazy running max (moves only by more than 2^8); P in f16
+//                 into the A operand of PV; per-lane row sums.  The warp on TMEM
+//                 lanes 0..31 of the first half rescales O when a max moves and
+//                 writes the rows out.  These warps also stage Q at the start.
 // Q is staged once as f16 after scaling each row by a power of two (2^-e_r,
 // max |q'| in [2^14, 2^15)), exact for f16 and bf16 queries; K codes enter
 // the MMA exactly, so the scores carry only f32 accumulation error; V values
@@ -52,18 +52,21 @@ namespace qtc {
 
 using namespace ta::sm100;
 
-constexpr int kThreads = 320;
-constexpr uint32_t kPolls = 1u << 22;
+constexpr int kDecWarps = 8;      // decoders
+constexpr int kSmWarps = 8;       // softmax: two per TMEM lane quarter, each half of the rows
+constexpr int kThreads = 32 * (2 + kDecWarps + kSmWarps);
+constexpr uint32_t kPolls = 1u << 21;     // bound of every wait: tries of up to kSleepNs each
+constexpr uint32_t kSleepNs = 1000;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kSlack = 8.0f;      // lazy-max slack (log2 units): P <= 256
-constexpr int kMaxRing = 8;
+constexpr int kMaxRing = kQuantTcMaxRing;
 
 struct Bars {
     uint64_t kfull[kMaxRing], kempty[kMaxRing];
     uint64_t vfull[kMaxRing], vempty[kMaxRing];
     uint64_t dfull[kMaxRing], dempty[kMaxRing];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_done[2];   // per tile parity
-    uint64_t drain;
+    uint64_t q_ready, drain;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -93,8 +96,9 @@ __device__ __forceinline__ void note_abort(Bars *b, int *err) {
 }
 // Bounded wait of one thread; false (and the CTA marked aborted) on timeout.
 __device__ __forceinline__ bool wait1(Bars *b, uint64_t *bar, uint32_t parity, int *err) {
+    if (mbar_try_wait(bar, parity)) return true;      // the common case: the phase is already complete
     if (b->abort_flag) return false;
-    if (mbar_wait(bar, parity, kPolls)) return true;
+    if (mbar_wait_sleep(bar, parity, kPolls, kSleepNs)) return true;
     note_abort(b, err);
     return false;
 }
@@ -115,6 +119,8 @@ __device__ __forceinline__ int pos4(int k) { return ((k & 3) << 1) | (k >> 2); }
 
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_ldn<2>(uint32_t taddr, uint32_t (&r)[2]) { tmem_ld2(taddr, r); }
 template <>
 __device__ __forceinline__ void tmem_ldn<4>(uint32_t taddr, uint32_t (&r)[4]) { tmem_ld4(taddr, r); }
 template <>
@@ -145,7 +151,8 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 
 // Decode chunk c (dimensions [64c, 64c + 64)) of a tile's packed words into a
 // [128 tokens][64 x f16] 128-byte-swizzled operand chunk: the codes (K) or
-// s * code + b (V).  128 threads; a 16-byte item is four words of a token.
+// s * code + b (V).  kDecWarps * 32 threads; a 16-byte item is four words of
+// a token.
 template <int BITS>
 __device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int c, unsigned char *dst, int dtid,
                                              bool is_v, const uint16_t *vs, const uint16_t *vb, int ng, int G,
@@ -154,9 +161,10 @@ __device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int
     constexpr int IPT = 64 / (4 * DPW);     // items per token and chunk (2 or 4)
     constexpr int PPI = 4 * DPW / 8;        // 16-byte output pieces per item (4 or 2)
     const __half2 k1024 = __float2half2_rn(1024.0f);
+    constexpr int NIT = 128 * IPT / (kDecWarps * 32);   // items per thread
 #pragma unroll
-    for (int i = 0; i < IPT; ++i) {
-        const int it = dtid + 128 * i;
+    for (int i = 0; i < NIT; ++i) {
+        const int it = dtid + kDecWarps * 32 * i;
         const int tok = it / IPT, h = it % IPT;
         const uint4 w4 = *reinterpret_cast<const uint4 *>(words + tok * wpt + c * (64 / DPW) + h * 4);
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -193,11 +201,13 @@ __device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int
     }
 }
 
-// RR: query rows of a CTA (4, 8, 16 or 32); the score MMA's N (and the Q and
-// score-buffer layout) is RP = max(16, RR), its extra rows zero.
+// RR: query rows of a CTA (4, 8, 16 or 32); each softmax lane handles RH =
+// RR / 2 of them (two warps per TMEM lane quarter).  The score MMA's N (and
+// the Q and score-buffer layout) is RP = max(16, RR), its extra rows zero.
 template <int BITS, int RR>
 __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a) {
     constexpr int RP = RR < 16 ? 16 : RR;
+    constexpr int RH = RR / 2;
     extern __shared__ __align__(1024) unsigned char smem[];
     // 128-byte-swizzled operands need a 1024-byte-aligned base (the same for
     // every CTA, so a misaligned one stops all of them before any barrier)
@@ -212,7 +222,14 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     Bars *bars = reinterpret_cast<Bars *>(smem + L.bars);
     float *sF = reinterpret_cast<float *>(smem + L.rc);      // [RP] 2^e_r * scale * log2(e)
     float *sQG = sF + RP;                                     // [NG][RP] 2^-e_r * sum_{d in g} q_d
-    float *sRed = reinterpret_cast<float *>(smem + L.red);   // [3][4][32] softmax exchange
+    // softmax exchange: row maxima [parity][half][quarter][32], row sums
+    // [half][quarter][32], rescale factors [parity][32], flags [parity][half],
+    // final row maxima [32]
+    float *sMax = reinterpret_cast<float *>(smem + L.red);
+    float *sSum = sMax + 512;
+    float *sAlpha = sSum + 256;
+    int *sNeed = reinterpret_cast<int *>(sAlpha + 64);
+    float *sMrow = reinterpret_cast<float *>(sNeed + 4);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, rb = blockIdx.y % a.n_rb, kv = blockIdx.y / a.n_rb;
     const int q0 = kv * a.rep + rb * RR;
@@ -225,17 +242,27 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     int *err = a.err;
 
     if (tid == 0) {
-        for (int i = 0; i < NK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 4); }
+        for (int i = 0; i < NK; ++i) {
+            mbar_init(&bars->kfull[i], 1);
+            mbar_init(&bars->kempty[i], kDecWarps);
+        }
         // V slot: the producer's expect-tx arrive, 32 cp.async arrivals, 32 plain arrivals
-        for (int i = 0; i < NV; ++i) { mbar_init(&bars->vfull[i], 65); mbar_init(&bars->vempty[i], 8); }
-        for (int i = 0; i < ND; ++i) { mbar_init(&bars->dfull[i], 4); mbar_init(&bars->dempty[i], 1); }
+        for (int i = 0; i < NV; ++i) {
+            mbar_init(&bars->vfull[i], 65);
+            mbar_init(&bars->vempty[i], kDecWarps + kSmWarps);
+        }
+        for (int i = 0; i < ND; ++i) {
+            mbar_init(&bars->dfull[i], kDecWarps);
+            mbar_init(&bars->dempty[i], 1);
+        }
         for (int i = 0; i < 2; ++i) {
             mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_free[i], 4);
-            mbar_init(&bars->p_full[i], 4);
+            mbar_init(&bars->s_free[i], kSmWarps);
+            mbar_init(&bars->p_full[i], kSmWarps);
             mbar_init(&bars->p_free[i], 1);
             mbar_init(&bars->o_done[i], 1);
         }
+        mbar_init(&bars->q_ready, kSmWarps);
         mbar_init(&bars->drain, 1);
         bars->abort_flag = 0;
         fence_mbar_init();
@@ -244,42 +271,6 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         tmem_alloc(&bars->tmem_base, static_cast<uint32_t>(a.tc_cols));
         tmem_relinquish();
     }
-
-    // ---- Q operand (f16, rows scaled by 2^-e_r) and per-row constants
-    {
-        const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
-        const int E = DIM / 32;                 // dimensions per lane (2, 4 or 8)
-        const float qs = a.scale * kLog2e;
-        for (int r = warp; r < RP; r += kThreads / 32) {
-            const bool live = r < rows_here;
-            float x[8];
-            float amax = 0.0f, gs = 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                x[e] = 0.0f;
-                if (e < E && live) x[e] = t2f(qg[static_cast<size_t>(q0 + r) * DIM + lane * E + e], bf16);
-                amax = fmaxf(amax, fabsf(x[e]));
-                gs += x[e];
-            }
-            amax = warp_max(amax);
-            const int ex = amax > 0.0f ? ilogbf(amax) - 14 : 0;
-            const int lpg = G / E;              // lanes per scale group (power of two <= 32)
-            for (int m = 1; m < lpg; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
-            // the bias term in units of the row factor: sum_g b_g * 2^-e_r * sum_{d in g} q_d
-            if (lane % lpg == 0) sQG[(lane * E / G) * RP + r] = live ? ldexpf(gs, -ex) : 0.0f;
-            if (lane == 0) sF[r] = live ? ldexpf(qs, ex) : 0.0f;
-#pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                if (e >= E) break;
-                const int d = lane * E + e;
-                const int pos = BITS == 4 ? ((d & ~7) | pos4(d & 7)) : d;
-                const int blk = pos >> 6, pc = (pos & 63) >> 3;
-                *reinterpret_cast<__half *>(smem + L.q0 + blk * RP * 128 + r * 128 + ((pc ^ (r & 7)) << 4) +
-                                            (pos & 7) * 2) = __float2half_rn(ldexpf(x[e], -ex));
-            }
-        }
-    }
-    fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -376,9 +367,9 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         // Drain: every copy issued into this CTA's rings has landed.
         if (lane == 0) {
             for (int n = kn > NK ? kn - NK : 0; n < kn; ++n)
-                if (!mbar_wait(&bars->kfull[n % NK], static_cast<uint32_t>(n / NK) & 1u, kPolls)) note_abort(bars, err);
+                if (!mbar_wait_sleep(&bars->kfull[n % NK], static_cast<uint32_t>(n / NK) & 1u, kPolls, kSleepNs)) note_abort(bars, err);
             for (int n = vn > NV ? vn - NV : 0; n < vn; ++n)
-                if (!mbar_wait(&bars->vfull[n % NV], static_cast<uint32_t>(n / NV) & 1u, kPolls)) note_abort(bars, err);
+                if (!mbar_wait_sleep(&bars->vfull[n % NV], static_cast<uint32_t>(n / NV) & 1u, kPolls, kSleepNs)) note_abort(bars, err);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
@@ -387,6 +378,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             const uint32_t id_pv = idesc_f16(128, 64, 0, 0, 1);
             const uint32_t q_addr = smem_u32(smem + L.q0), d_addr = smem_u32(smem + L.d0);
             const uint32_t p_addr = smem_u32(smem + L.p0);
+            const uint64_t kmaj = sw128_desc_hi(16, 1024);          // K-major operands
+            const uint64_t vmn = sw128_desc_hi(kQtcChunk, 1024);    // V chunk, MN-major
             int dn = 0;
             auto take = [&](uint32_t *ca) -> bool {
                 const int slot = dn % ND;
@@ -409,9 +402,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
                         const int d0 = c * 64 + k4 * 16;    // first dimension of the k-step
-                        mma_f16_ss(tm_s(sb) + static_cast<uint32_t>((d0 / G) * RP),
-                                   sw128_desc(ca + k4 * 32, 16, 1024),
-                                   sw128_desc(q_addr + c * RP * 128 + k4 * 32, 16, 1024), id_s, (d0 % G) != 0);
+                        mma_f16_ss(tm_s(sb) + static_cast<uint32_t>((d0 / G) * RP), sw128_desc_at(kmaj, ca + k4 * 32),
+                                   sw128_desc_at(kmaj, q_addr + c * RP * 128 + k4 * 32), id_s, (d0 % G) != 0);
                     }
                     give();
                 }
@@ -427,24 +419,26 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                     if (!take(&ca)) return false;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tm_o + c * 64, sw128_desc(pa + (kk >> 2) * L.pkb + (kk & 3) * 32, 16, 1024),
-                                   sw128_desc(ca + kk * 2048, kQtcChunk, 1024), id_pv, (t | kk) != 0);
+                        mma_f16_ss(tm_o + c * 64, sw128_desc_at(kmaj, pa + (kk >> 2) * L.pkb + (kk & 3) * 32),
+                                   sw128_desc_at(vmn, ca + kk * 2048), id_pv, (t | kk) != 0);
                     give();
                 }
                 mma_commit(&bars->o_done[t & 1]);
                 mma_commit(&bars->p_free[t & 1]);   // P_t buffer free once PV_t is done
                 return true;
             };
-            bool ok = issue_s(0);
+            bool ok = wait1(bars, &bars->q_ready, 0, err);   // Q operand staged
+            tc_fence_after();
+            if (ok) ok = issue_s(0);
             for (int t = 0; t < T && ok; ++t) {
                 if (t + 1 < T) ok = issue_s(t + 1);
                 if (ok) ok = issue_pv(t);
             }
             // Drain: all MMAs issued by this thread have completed.
             mma_commit(&bars->drain);
-            if (!mbar_wait(&bars->drain, 0, kPolls)) note_abort(bars, err);
+            if (!mbar_wait_sleep(&bars->drain, 0, kPolls, kSleepNs)) note_abort(bars, err);
         }
-    } else if (warp < 6) {
+    } else if (warp < 2 + kDecWarps) {
         // ------------------------------------------------------------ decoders
         const int dtid = tid - 64;
         int dn = 0;
@@ -458,45 +452,91 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             ++dn;
             return true;
         };
-        auto do_k = [&](int t) -> bool {
-            const int slot = t % NK;
-            if (!waitw(bars, &bars->kfull[slot], static_cast<uint32_t>(t / NK) & 1u, err)) return false;
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(smem + L.k0 + slot * L.kslot);
+        // one part = the K or V tile of a token tile, decoded chunk by chunk
+        auto part = [&](int t, bool is_v) -> bool {
+            const int slot = is_v ? t % NV : t % NK;
+            uint64_t *full = is_v ? &bars->vfull[slot] : &bars->kfull[slot];
+            if (!waitw(bars, full, static_cast<uint32_t>(t / (is_v ? NV : NK)) & 1u, err)) return false;
+            const unsigned char *st = is_v ? smem + L.v0 + slot * L.vslot + L.vw : smem + L.k0 + slot * L.kslot;
+            const unsigned char *vst = smem + L.v0 + slot * L.vslot;
+            const uint16_t *vs = reinterpret_cast<const uint16_t *>(vst + L.vvs);
+            const uint16_t *vb = reinterpret_cast<const uint16_t *>(vst + L.vvb);
+#pragma unroll 1
             for (int c = 0; c < NCH; ++c)
-                if (!put(words, c, false, nullptr, nullptr)) return false;
+                if (!put(reinterpret_cast<const uint32_t *>(st), c, is_v, vs, vb)) return false;
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->kempty[slot]);
+            if (lane == 0) mbar_arrive(is_v ? &bars->vempty[slot] : &bars->kempty[slot]);
             return true;
         };
-        auto do_v = [&](int t) -> bool {
-            const int slot = t % NV;
-            if (!waitw(bars, &bars->vfull[slot], static_cast<uint32_t>(t / NV) & 1u, err)) return false;
-            const unsigned char *st = smem + L.v0 + slot * L.vslot;
-            const uint32_t *words = reinterpret_cast<const uint32_t *>(st + L.vw);
-            const uint16_t *vs = reinterpret_cast<const uint16_t *>(st + L.vvs);
-            const uint16_t *vb = reinterpret_cast<const uint16_t *>(st + L.vvb);
-            for (int c = 0; c < NCH; ++c)
-                if (!put(words, c, true, vs, vb)) return false;
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->vempty[slot]);
-            return true;
-        };
-        bool ok = T > 0 ? do_k(0) : true;
+        bool ok = T > 0 ? part(0, false) : true;
+#pragma unroll 1
         for (int t = 0; t < T && ok; ++t) {
-            if (t + 1 < T) ok = do_k(t + 1);
-            if (ok) ok = do_v(t);
+            if (t + 1 < T) ok = part(t + 1, false);
+            if (ok) ok = part(t, true);
         }
     } else {
         // -------------------------------------------- softmax and epilogue
+        const int sw = warp - 2 - kDecWarps;                // 0..7
+        const int half = sw >> 2;                           // rows [half * RH, half * RH + RH)
         const int quarter = warp & 3;
         const int tl = quarter * 32 + lane;                 // token of the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
-        auto group_sync = [&]() { asm volatile("bar.sync 1, 128;" ::: "memory"); };
-        float lsum[RR];
+        const int hr0 = half * RH;
+        const bool o_warp = half == 0 && quarter == 0;      // owns O (TMEM lanes 0..31 = rows)
+        auto half_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory"); };
+        auto all_sync = [&]() { asm volatile("bar.sync 3, 256;" ::: "memory"); };
+
+        // ---- Q operand (f16, rows scaled by 2^-e_r) and per-row constants:
+        // every load of this warp's rows is issued before any is used
+        {
+            const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
+            const int E = DIM / 32;                         // dimensions per lane (2, 4 or 8)
+            const float qs = a.scale * kLog2e;
+            constexpr int RPW = RP / kSmWarps;              // rows per warp (2 or 4)
+            float x[RPW][8];
 #pragma unroll
-        for (int r = 0; r < RR; ++r) lsum[r] = 0.0f;
-        float m_row = -INFINITY;                            // running max (log2 units) of row lane % RR
-        bool ok = true;
+            for (int i = 0; i < RPW; ++i) {
+                const int r = sw + kSmWarps * i;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[i][e] = (e < E && r < rows_here) ? t2f(qg[static_cast<size_t>(q0 + r) * DIM + lane * E + e], bf16)
+                                                       : 0.0f;
+            }
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const int r = sw + kSmWarps * i;
+                const bool live = r < rows_here;
+                float amax = 0.0f, gs = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) { amax = fmaxf(amax, fabsf(x[i][e])); gs += x[i][e]; }
+                amax = warp_max(amax);
+                const int ex = amax > 0.0f ? ilogbf(amax) - 14 : 0;
+                const int lpg = G / E;                      // lanes per scale group (power of two <= 32)
+                for (int m = 1; m < lpg; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
+                // the bias term in units of the row factor: sum_g b_g * 2^-e_r * sum_{d in g} q_d
+                if (lane % lpg == 0) sQG[(lane * E / G) * RP + r] = live ? ldexpf(gs, -ex) : 0.0f;
+                if (lane == 0) sF[r] = live ? ldexpf(qs, ex) : 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    if (e >= E) break;
+                    const int d = lane * E + e;
+                    const int pos = BITS == 4 ? ((d & ~7) | pos4(d & 7)) : d;
+                    const int blk = pos >> 6, pc = (pos & 63) >> 3;
+                    *reinterpret_cast<__half *>(smem + L.q0 + blk * RP * 128 + r * 128 + ((pc ^ (r & 7)) << 4) +
+                                                (pos & 7) * 2) = __float2half_rn(ldexpf(x[i][e], -ex));
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->q_ready);
+        }
+        bool ok = waitw(bars, &bars->q_ready, 0, err);      // every warp's rows (sF, sQG)
+
+        float lsum[RH];
+#pragma unroll
+        for (int r = 0; r < RH; ++r) lsum[r] = 0.0f;
+        float m_row = -INFINITY;                            // running max (log2 units) of row hr0 + lane % RH
+#pragma unroll 1
         for (int t = 0; t < T; ++t) {
             const int sb = t & 1;
             const int vslot = t % NV;
@@ -508,75 +548,75 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             const unsigned char *st = smem + L.v0 + vslot * L.vslot;
             const uint16_t *ks = reinterpret_cast<const uint16_t *>(st + L.vks);
             const uint16_t *kb = reinterpret_cast<const uint16_t *>(st + L.vkb);
-            float acc[RR];   // sum_g s_g S^T_g + b_g * 2^-e_r * sum_{d in g} q_d
+            float acc[RH];   // sum_g s_g S^T_g + b_g * 2^-e_r * sum_{d in g} q_d
 #pragma unroll
-            for (int r = 0; r < RR; ++r) acc[r] = 0.0f;
+            for (int r = 0; r < RH; ++r) acc[r] = 0.0f;
             if (ok) {
 #pragma unroll 1
                 for (int g = 0; g < NG; ++g) {
-                    uint32_t d[RR];
-                    tmem_ldn<RR>(tm_s(sb) + lane_off + static_cast<uint32_t>(g * RP), d);
+                    uint32_t d[RH];
+                    tmem_ldn<RH>(tm_s(sb) + lane_off + static_cast<uint32_t>(g * RP + hr0), d);
                     tmem_wait_ld();
                     const float s = t2f(ks[tl * NG + g], bf16), b = t2f(kb[tl * NG + g], bf16);
-                    const float4 *qg4 = reinterpret_cast<const float4 *>(sQG + g * RP);
+                    const float *qg = sQG + g * RP + hr0;
 #pragma unroll
-                    for (int r4 = 0; r4 < RR / 4; ++r4) {
-                        const float4 qv = qg4[r4];
-                        acc[4 * r4 + 0] = fmaf(s, __uint_as_float(d[4 * r4 + 0]), fmaf(b, qv.x, acc[4 * r4 + 0]));
-                        acc[4 * r4 + 1] = fmaf(s, __uint_as_float(d[4 * r4 + 1]), fmaf(b, qv.y, acc[4 * r4 + 1]));
-                        acc[4 * r4 + 2] = fmaf(s, __uint_as_float(d[4 * r4 + 2]), fmaf(b, qv.z, acc[4 * r4 + 2]));
-                        acc[4 * r4 + 3] = fmaf(s, __uint_as_float(d[4 * r4 + 3]), fmaf(b, qv.w, acc[4 * r4 + 3]));
-                    }
+                    for (int r = 0; r < RH; ++r) acc[r] = fmaf(s, __uint_as_float(d[r]), fmaf(b, qg[r], acc[r]));
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(&bars->s_free[sb]);   // S_t read out of TMEM
-            float (&lg)[RR] = acc;   // logits (log2 units), in place
+            float (&lg)[RH] = acc;   // logits (log2 units), in place
             const bool live_tok = ok && tok_ok;
 #pragma unroll
-            for (int r = 0; r < RR; ++r) lg[r] = (live_tok && r < rows_here) ? acc[r] * sF[r] : -INFINITY;
+            for (int r = 0; r < RH; ++r) lg[r] = (live_tok && hr0 + r < rows_here) ? acc[r] * sF[hr0 + r] : -INFINITY;
             if (has_mf) {
                 const uint16_t *mf = reinterpret_cast<const uint16_t *>(st + L.vmf) + tl;
 #pragma unroll
-                for (int r = 0; r < RR; ++r)
-                    if (r < rows_here) lg[r] = fmaf(kLog2e, t2f(mf[r * 128], bf16), lg[r]);
+                for (int r = 0; r < RH; ++r)
+                    if (hr0 + r < rows_here) lg[r] = fmaf(kLog2e, t2f(mf[(hr0 + r) * 128], bf16), lg[r]);
             }
             if (has_mb) {
                 const uint32_t *mb = reinterpret_cast<const uint32_t *>(st + L.vmb) + tl;
 #pragma unroll
-                for (int r = 0; r < RR; ++r)
-                    if (r < rows_here && mb[r * 128] == 0u) lg[r] = -INFINITY;
+                for (int r = 0; r < RH; ++r)
+                    if (hr0 + r < rows_here && mb[(hr0 + r) * 128] == 0u) lg[r] = -INFINITY;
             }
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(&bars->vempty[vslot]);   // scales and masks read
 
-            // row maxima of the tile: warp reduce-scatter, then the four warps
-            float tmp[RR];
+            // row maxima of the tile: warp reduce-scatter, then the half's four warps
+            float tmp[RH];
 #pragma unroll
-            for (int r = 0; r < RR; ++r) tmp[r] = lg[r];
-            float wm = reduce_scatter<RR, true>(tmp, lane);
+            for (int r = 0; r < RH; ++r) tmp[r] = lg[r];
+            float wm = reduce_scatter<RH, true>(tmp, lane);
 #pragma unroll
-            for (int m = RR; m < 32; m <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, m));
-            sRed[(sb * 4 + quarter) * 32 + lane] = wm;
-            group_sync();
-            const float tmax = fmaxf(fmaxf(sRed[(sb * 4 + 0) * 32 + lane], sRed[(sb * 4 + 1) * 32 + lane]),
-                                     fmaxf(sRed[(sb * 4 + 2) * 32 + lane], sRed[(sb * 4 + 3) * 32 + lane]));
+            for (int m = RH; m < 32; m <<= 1) wm = fmaxf(wm, __shfl_xor_sync(0xffffffffu, wm, m));
+            float *mx = sMax + (sb * 2 + half) * 128;
+            mx[quarter * 32 + lane] = wm;
+            half_sync();
+            const float tmax = fmaxf(fmaxf(mx[lane], mx[32 + lane]), fmaxf(mx[64 + lane], mx[96 + lane]));
             float alpha = 1.0f;
             if (tmax > m_row + kSlack) {
                 alpha = m_row == -INFINITY ? 0.0f : ex2(m_row - tmax);
                 m_row = tmax;
             }
-            const bool need = __any_sync(0xffffffffu, alpha != 1.0f);   // same in the four warps
+            const bool need = __any_sync(0xffffffffu, alpha != 1.0f);   // same in the half's four warps
             if (need) {
 #pragma unroll
-                for (int r = 0; r < RR; ++r) lsum[r] *= __shfl_sync(0xffffffffu, alpha, r);
+                for (int r = 0; r < RH; ++r) lsum[r] *= __shfl_sync(0xffffffffu, alpha, r);
             }
+            if (quarter == 0) {
+                if (lane < RH) sAlpha[sb * 32 + hr0 + lane] = alpha;
+                if (lane == 0) sNeed[sb * 2 + half] = need ? 1 : 0;
+            }
+            all_sync();
             // the P buffer of this tile is free once PV of tile t - 2 is done
             ok = ok && waitw(bars, &bars->p_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err);
-            if (quarter == 0 && need && t > 0) {
-                // rows moved their max: rescale O (rows = TMEM lanes 0..31) once
-                // PV of the previous tile is done
+            if (o_warp && t > 0 && (sNeed[sb * 2] | sNeed[sb * 2 + 1]) != 0) {
+                // rows moved their max: rescale O (rows = TMEM lanes) once PV of
+                // the previous tile is done
+                const float al = lane < RR ? sAlpha[sb * 32 + lane] : 1.0f;
                 ok = ok && waitw(bars, &bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, err);
                 tc_fence_after();
                 if (ok) {
@@ -586,7 +626,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                         tmem_ld32(tm_o + c * 32, v);
                         tmem_wait_ld();
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * al);
                         tmem_st32(tm_o + c * 32, v);
                     }
                     tmem_wait_st();
@@ -595,12 +635,13 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             unsigned char *pb = smem + L.p0 + sb * 2 * L.pkb + (tl >> 6) * L.pkb;
             const int tc = tl & 63;
 #pragma unroll
-            for (int r = 0; r < RR; ++r) {
+            for (int r = 0; r < RH; ++r) {
+                const int row = hr0 + r;
                 const float m = __shfl_sync(0xffffffffu, m_row, r);
                 const __half ph = __float2half_rn(ex2(lg[r] - (m == -INFINITY ? 0.0f : m)));
                 lsum[r] += __half2float(ph);
-                if (r < rows_here)
-                    *reinterpret_cast<__half *>(pb + r * 128 + (((tc >> 3) ^ (r & 7)) << 4) + (tc & 7) * 2) = ph;
+                if (row < rows_here)
+                    *reinterpret_cast<__half *>(pb + row * 128 + (((tc >> 3) ^ (row & 7)) << 4) + (tc & 7) * 2) = ph;
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -608,28 +649,34 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             if (lane == 0 && ok) mbar_arrive(&bars->p_full[sb]);
         }
         pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
-        if (T > 0) {
+        if (T > 0 && o_warp) {
             ok = ok && waitw(bars, &bars->o_done[(T - 1) & 1], (static_cast<uint32_t>(T - 1) >> 1) & 1u, err);
             tc_fence_after();
         }
-        // row sums over the four warps' tokens
-        float ls = reduce_scatter<RR, false>(lsum, lane);
+        // row sums over the tokens of the half's four warps; final row maxima
+        float ls = reduce_scatter<RH, false>(lsum, lane);
 #pragma unroll
-        for (int m = RR; m < 32; m <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
-        sRed[(8 + quarter) * 32 + lane] = ls;
-        group_sync();
-        if (quarter == 0 && ok) {
-            const float l_tot = (sRed[8 * 32 + lane] + sRed[9 * 32 + lane]) + (sRed[10 * 32 + lane] + sRed[11 * 32 + lane]);
+        for (int m = RH; m < 32; m <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, m);
+        sSum[(half * 4 + quarter) * 32 + lane] = ls;
+        if (quarter == 0 && lane < RH) sMrow[hr0 + lane] = m_row;
+        all_sync();
+        if (o_warp && ok) {
             const int r = lane;                              // O row = TMEM lane
             const bool live = r < rows_here;
             const int q = q0 + r;
+            float l_tot = 0.0f, m_fin = -INFINITY;
+            if (r < RR) {
+                const float *sh = sSum + (r / RH) * 128 + (r % RH);
+                l_tot = (sh[0] + sh[32]) + (sh[64] + sh[96]);
+                m_fin = sMrow[r];
+            }
             float f = 1.0f;
             if (a.nwg == 1 && live) {
                 float cf = 1.0f, sf = l_tot;
                 if (a.has_sinks) {
                     const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
-                    const float mx = fmaxf(m_row, sk);
-                    cf = m_row == -INFINITY ? 0.0f : ex2(m_row - mx);
+                    const float mx = fmaxf(m_fin, sk);
+                    cf = m_fin == -INFINITY ? 0.0f : ex2(m_fin - mx);
                     sf = l_tot * cf + ex2(sk - mx);
                 }
                 f = sf > 0.0f ? cf / sf : 0.0f;
@@ -684,7 +731,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 }
             }
             if (a.nwg > 1 && live)
-                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q] = make_float2(l_tot, m_row);
+                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q] = make_float2(l_tot, m_fin);
         }
     }
 

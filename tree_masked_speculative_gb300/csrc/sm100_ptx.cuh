@@ -39,6 +39,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, letting the thread sleep up to hint_ns until the phase
+// completes instead of returning at once (a waiting warp then takes no issue
+// slots from the working ones).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+// Bounded sleeping wait: at most max_iters tries of up to hint_ns each.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t max_iters, uint32_t hint_ns) {
+    for (uint32_t i = 0; i < max_iters; ++i)
+        if (mbar_try_wait_sleep(bar, parity, hint_ns)) return true;
+    return false;
+}
 // Wait for the phase with the given parity to complete; gives up (returns
 // false) after max_iters polls so that no wait can hang the GPU.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t max_iters) {
@@ -223,7 +243,10 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
           "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
         : "r"(taddr));
 }
-// 4 / 8 / 16 consecutive f32 columns of this thread's TMEM lane.
+// 2 / 4 / 8 / 16 consecutive f32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld2(uint32_t taddr, uint32_t (&r)[2]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x2.b32 {%0, %1}, [%2];" : "=r"(r[0]), "=r"(r[1]) : "r"(taddr));
+}
 __device__ __forceinline__ void tmem_ld4(uint32_t taddr, uint32_t (&r)[4]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
@@ -272,6 +295,13 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uin
     d |= static_cast<uint64_t>(1) << 46;
     d |= static_cast<uint64_t>(2) << 61;
     return d;
+}
+
+// The same descriptor split into its constant part (hi: offsets, version,
+// layout) and the start-address field added per use.
+__device__ __forceinline__ uint64_t sw128_desc_hi(uint32_t lbo, uint32_t sbo) { return sw128_desc(0, lbo, sbo); }
+__device__ __forceinline__ uint64_t sw128_desc_at(uint64_t hi, uint32_t saddr) {
+    return hi | static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
 }
 
 // Instruction descriptor of tcgen05.mma kind::f16: f32 accumulator, A and B

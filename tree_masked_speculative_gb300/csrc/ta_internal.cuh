@@ -196,7 +196,9 @@ struct QtcLayout {
     int rc, red, bars, total;
 };
 constexpr int kQtcChunk = 16384;
-constexpr int kQtcBarBytes = 1024;
+constexpr int kQuantTcMaxRing = 16;   // deepest ring of the tensor-core quantized kernel
+constexpr int kQtcRedBytes = 4096;   // softmax exchange area (row maxima, sums, rescale factors)
+constexpr int kQtcBarBytes = 1280;
 __host__ __device__ inline int qtc_align(int o, int a) { return (o + a - 1) / a * a; }
 __host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng, int nd, int nk, int nv,
                                                 bool has_mb, bool has_mf) {
@@ -228,7 +230,7 @@ __host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng
     L.rc = o;
     o = qtc_align(o + (rp + ng * rp) * 4, 16);
     L.red = o;
-    o = qtc_align(o + 3 * 4 * 32 * 4, 16);
+    o = qtc_align(o + kQtcRedBytes, 16);
     o = qtc_align(o, 8);
     L.bars = o;
     o += kQtcBarBytes;

@@ -137,7 +137,9 @@ __device__ __forceinline__ void note_abort(Bars *b, int *err, int code) {
 
 __device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code) {
     if (b->abort_flag) return false;
-    if (mbar_wait(bar, parity, kWaitIters)) return true;
+    // a waiting warp sleeps on the barrier (taking no issue slots from the
+    // MMA issuer and the softmax) for at most 2^21 tries of 1 us
+    if (mbar_try_wait(bar, parity) || mbar_wait_sleep(bar, parity, 1u << 21, 1000)) return true;
     note_abort(b, err, code);
     return false;
 }
