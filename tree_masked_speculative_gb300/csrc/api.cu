@@ -415,13 +415,13 @@ bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
     int cols = 32;
     while (cols < need) cols <<= 1;
     sh->cols = cols;
-    const QtcLayout L = qtc_layout(sh->rp, (int)p->dim, wpt, ng, (int)p->dim / 64, 2, 2, true, true);
+    const QtcLayout L = qtc_layout(sh->rp, (int)p->dim, wpt, ng, 4, 2, 2, true, true);
     return (size_t)L.total <= kQuantMaxSmem;
 }
 
-// Ring depths for the masks a call passes: the decoded-chunk ring holds up to
-// four K or V tile parts (dim / 64 chunks each) so that the decoders run ahead
-// of the MMA warp, the packed-K / packed-V rings three or two tiles; the
+// Ring depths for the masks a call passes: the decoded K and V rings hold two
+// tile parts (dim / 64 chunks each) each where shared memory allows, else one,
+// else two chunks; the packed-K / packed-V rings three or two tiles; the
 // deepest combination that fits.  The size is padded so that one CTA runs per
 // SM (the TMEM budget assumes it).
 struct QtcPlan {
@@ -432,9 +432,12 @@ bool quant_tc_plan(const ta_quant_params *p, const QtcShape &sh, bool has_mb, bo
     const int ng = (int)(p->dim / p->group_size);
     const int wpt = (int)(p->dim * p->bits / 32);
     const int nch = (int)p->dim / 64;
-    for (int parts = 4; parts >= 1; --parts)
+    // decoded chunks per ring (K and V each): two tile parts, one, or two chunks
+    const int per_ring[3] = {2 * nch, nch, 2};
+    for (int i = 0; i < 3; ++i)
         for (int n = 3; n >= 2; --n) {
-            const int nd = parts * nch;
+            if (i > 0 && per_ring[i] >= per_ring[i - 1]) continue;
+            const int nd = 2 * per_ring[i];
             if (nd > kQuantTcMaxRing) continue;
             const QtcLayout L = qtc_layout(sh.rp, (int)p->dim, wpt, ng, nd, n, n, has_mb, has_mf);
             if ((size_t)L.total > kQuantMaxSmem) continue;

@@ -14,11 +14,11 @@
 //                 (bulk copies, or plain loads for a ragged or unaligned tile)
 //                 and the rows' bool / float mask runs (per-lane cp.async) into
 //                 the V ring.
-//   warps 2..9  : decoders.  Packed codes become 16-bit operands in a ring of
-//                 16 KB chunks ([128 tokens][64 dims], 128-byte swizzled): K as
-//                 the exact integer codes (byte permutes under the f16 exponent
-//                 of 1024, minus 1024), V as s * code + b rounded once to f16.
-//                 Order: K_0, then K_t+1 before V_t, the MMA warp's order.
+//   warps 2..9  : decoders, four for K and four for V, each group filling its
+//                 own ring of 16 KB chunks ([128 tokens][64 dims], 128-byte
+//                 swizzled) in tile order: K as the exact integer codes (byte
+//                 permutes under the f16 exponent of 1024, minus 1024), V as
+//                 s * code + b rounded once to f16.
 //   warp 1      : TMEM owner and MMA issuer.  Scores transposed, tokens on the
 //                 M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M 128
 //                 tokens, N = max(16, RR) rows, one f32 accumulator per group,
@@ -52,7 +52,8 @@ namespace qtc {
 
 using namespace ta::sm100;
 
-constexpr int kDecWarps = 8;      // decoders
+constexpr int kDecWarps = 8;      // decoders: four for K, four for V
+constexpr int kDecGroup = 4;
 constexpr int kSmWarps = 8;       // softmax: two per TMEM lane quarter, each half of the rows
 constexpr int kThreads = 32 * (2 + kDecWarps + kSmWarps);
 constexpr uint32_t kPolls = 1u << 21;     // bound of every wait: tries of up to kSleepNs each
@@ -151,7 +152,7 @@ __device__ __forceinline__ float reduce_scatter(float (&v)[N], int lane) {
 
 // Decode chunk c (dimensions [64c, 64c + 64)) of a tile's packed words into a
 // [128 tokens][64 x f16] 128-byte-swizzled operand chunk: the codes (K) or
-// s * code + b (V).  kDecWarps * 32 threads; a 16-byte item is four words of
+// s * code + b (V).  kDecGroup * 32 threads; a 16-byte item is four words of
 // a token.
 template <int BITS>
 __device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int c, unsigned char *dst, int dtid,
@@ -161,10 +162,10 @@ __device__ __forceinline__ void decode_chunk(const uint32_t *words, int wpt, int
     constexpr int IPT = 64 / (4 * DPW);     // items per token and chunk (2 or 4)
     constexpr int PPI = 4 * DPW / 8;        // 16-byte output pieces per item (4 or 2)
     const __half2 k1024 = __float2half2_rn(1024.0f);
-    constexpr int NIT = 128 * IPT / (kDecWarps * 32);   // items per thread
+    constexpr int NIT = 128 * IPT / (kDecGroup * 32);   // items per thread
 #pragma unroll
     for (int i = 0; i < NIT; ++i) {
-        const int it = dtid + kDecWarps * 32 * i;
+        const int it = dtid + kDecGroup * 32 * i;
         const int tok = it / IPT, h = it % IPT;
         const uint4 w4 = *reinterpret_cast<const uint4 *>(words + tok * wpt + c * (64 / DPW) + h * 4);
         const uint32_t w[4] = {w4.x, w4.y, w4.z, w4.w};
@@ -244,15 +245,15 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     if (tid == 0) {
         for (int i = 0; i < NK; ++i) {
             mbar_init(&bars->kfull[i], 1);
-            mbar_init(&bars->kempty[i], kDecWarps);
+            mbar_init(&bars->kempty[i], kDecGroup);
         }
         // V slot: the producer's expect-tx arrive, 32 cp.async arrivals, 32 plain arrivals
         for (int i = 0; i < NV; ++i) {
             mbar_init(&bars->vfull[i], 65);
-            mbar_init(&bars->vempty[i], kDecWarps + kSmWarps);
+            mbar_init(&bars->vempty[i], kDecGroup + kSmWarps);
         }
         for (int i = 0; i < ND; ++i) {
-            mbar_init(&bars->dfull[i], kDecWarps);
+            mbar_init(&bars->dfull[i], kDecGroup);
             mbar_init(&bars->dempty[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
@@ -380,32 +381,40 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             const uint32_t p_addr = smem_u32(smem + L.p0);
             const uint64_t kmaj = sw128_desc_hi(16, 1024);          // K-major operands
             const uint64_t vmn = sw128_desc_hi(kQtcChunk, 1024);    // V chunk, MN-major
-            int dn = 0;
-            auto take = [&](uint32_t *ca) -> bool {
-                const int slot = dn % ND;
-                if (!wait1(bars, &bars->dfull[slot], static_cast<uint32_t>(dn / ND) & 1u, err)) return false;
+            // decoded chunks: K in slots [0, ND/2), V in [ND/2, ND), each ring in
+            // order; slot and phase kept as running counters (this thread is on
+            // the critical path: no divisions in its loop)
+            const int NDH = ND / 2;
+            int dslot[2] = {0, NDH};
+            uint32_t dph[2] = {0u, 0u};
+            auto take = [&](int ring, uint32_t *ca) -> bool {
+                if (!wait1(bars, &bars->dfull[dslot[ring]], dph[ring], err)) return false;
                 tc_fence_after();
-                *ca = d_addr + slot * kQtcChunk;
+                *ca = d_addr + static_cast<uint32_t>(dslot[ring]) * kQtcChunk;
                 return true;
             };
-            auto give = [&]() {
-                mma_commit(&bars->dempty[dn % ND]);
-                ++dn;
+            auto give = [&](int ring) {
+                mma_commit(&bars->dempty[dslot[ring]]);
+                if (++dslot[ring] == (ring + 1) * NDH) { dslot[ring] = ring * NDH; dph[ring] ^= 1u; }
             };
+            const int ksg = G / 16;   // k-steps per scale group
             auto issue_s = [&](int t) -> bool {
                 const int sb = t & 1;
                 if (!wait1(bars, &bars->s_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err)) return false;
                 tc_fence_after();
+                uint32_t acc_col = tm_s(sb), qa = q_addr;
+                int kig = 0;                                // k-step within the scale group
                 for (int c = 0; c < NCH; ++c) {
                     uint32_t ca;
-                    if (!take(&ca)) return false;
+                    if (!take(0, &ca)) return false;
 #pragma unroll
                     for (int k4 = 0; k4 < 4; ++k4) {
-                        const int d0 = c * 64 + k4 * 16;    // first dimension of the k-step
-                        mma_f16_ss(tm_s(sb) + static_cast<uint32_t>((d0 / G) * RP), sw128_desc_at(kmaj, ca + k4 * 32),
-                                   sw128_desc_at(kmaj, q_addr + c * RP * 128 + k4 * 32), id_s, (d0 % G) != 0);
+                        mma_f16_ss(acc_col, sw128_desc_at(kmaj, ca + k4 * 32), sw128_desc_at(kmaj, qa + k4 * 32), id_s,
+                                   kig != 0);
+                        if (++kig == ksg) { kig = 0; acc_col += RP; }
                     }
-                    give();
+                    qa += RP * 128;
+                    give(0);
                 }
                 mma_commit(&bars->s_full[sb]);
                 return true;
@@ -416,12 +425,12 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 const uint32_t pa = p_addr + (t & 1) * 2 * L.pkb;
                 for (int c = 0; c < NCH; ++c) {
                     uint32_t ca;
-                    if (!take(&ca)) return false;
+                    if (!take(1, &ca)) return false;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
                         mma_f16_ss(tm_o + c * 64, sw128_desc_at(kmaj, pa + (kk >> 2) * L.pkb + (kk & 3) * 32),
                                    sw128_desc_at(vmn, ca + kk * 2048), id_pv, (t | kk) != 0);
-                    give();
+                    give(1);
                 }
                 mma_commit(&bars->o_done[t & 1]);
                 mma_commit(&bars->p_free[t & 1]);   // P_t buffer free once PV_t is done
@@ -440,39 +449,38 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         }
     } else if (warp < 2 + kDecWarps) {
         // ------------------------------------------------------------ decoders
-        const int dtid = tid - 64;
-        int dn = 0;
-        auto put = [&](const uint32_t *words, int c, bool is_v, const uint16_t *vs, const uint16_t *vb) -> bool {
-            const int slot = dn % ND;
-            if (!waitw(bars, &bars->dempty[slot], (static_cast<uint32_t>(dn / ND) & 1u) ^ 1u, err)) return false;
-            decode_chunk<BITS>(words, WPT, c, smem + L.d0 + slot * kQtcChunk, dtid, is_v, vs, vb, NG, G, bf16);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bars->dfull[slot]);
-            ++dn;
-            return true;
-        };
-        // one part = the K or V tile of a token tile, decoded chunk by chunk
-        auto part = [&](int t, bool is_v) -> bool {
+        // warps 2..5 decode K tiles into the first half of the decoded ring,
+        // warps 6..9 V tiles into the second; each group runs ahead on its own
+        const bool is_v = warp >= 2 + kDecGroup;
+        const int dtid = tid - 64 - (is_v ? 32 * kDecGroup : 0);
+        const int NDH = ND / 2;
+        const int ds0 = is_v ? NDH : 0;
+        int ds = ds0;                                       // ring slot and its pass parity
+        uint32_t dph = 0u;
+        bool ok = true;
+#pragma unroll 1
+        for (int t = 0; t < T && ok; ++t) {
             const int slot = is_v ? t % NV : t % NK;
             uint64_t *full = is_v ? &bars->vfull[slot] : &bars->kfull[slot];
-            if (!waitw(bars, full, static_cast<uint32_t>(t / (is_v ? NV : NK)) & 1u, err)) return false;
-            const unsigned char *st = is_v ? smem + L.v0 + slot * L.vslot + L.vw : smem + L.k0 + slot * L.kslot;
+            ok = waitw(bars, full, static_cast<uint32_t>(t / (is_v ? NV : NK)) & 1u, err);
+            if (!ok) break;
+            const unsigned char *words = is_v ? smem + L.v0 + slot * L.vslot + L.vw : smem + L.k0 + slot * L.kslot;
             const unsigned char *vst = smem + L.v0 + slot * L.vslot;
             const uint16_t *vs = reinterpret_cast<const uint16_t *>(vst + L.vvs);
             const uint16_t *vb = reinterpret_cast<const uint16_t *>(vst + L.vvb);
 #pragma unroll 1
-            for (int c = 0; c < NCH; ++c)
-                if (!put(reinterpret_cast<const uint32_t *>(st), c, is_v, vs, vb)) return false;
+            for (int c = 0; c < NCH && ok; ++c) {
+                ok = waitw(bars, &bars->dempty[ds], dph ^ 1u, err);
+                if (!ok) break;
+                decode_chunk<BITS>(reinterpret_cast<const uint32_t *>(words), WPT, c, smem + L.d0 + ds * kQtcChunk, dtid,
+                                   is_v, vs, vb, NG, G, bf16);
+                fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bars->dfull[ds]);
+                if (++ds == ds0 + NDH) { ds = ds0; dph ^= 1u; }
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(is_v ? &bars->vempty[slot] : &bars->kempty[slot]);
-            return true;
-        };
-        bool ok = T > 0 ? part(0, false) : true;
-#pragma unroll 1
-        for (int t = 0; t < T && ok; ++t) {
-            if (t + 1 < T) ok = part(t + 1, false);
-            if (ok) ok = part(t, true);
+            if (lane == 0 && ok) mbar_arrive(is_v ? &bars->vempty[slot] : &bars->kempty[slot]);
         }
     } else {
         // -------------------------------------------- softmax and epilogue
