@@ -540,6 +540,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         pair_sync();
         const float l_run = l_half + bars->xrow[T & 1][half ^ 1][r];
         const bool have_o = ok && T > 0;
+        // a final row stored straight from the stage (no merge in the cluster)
+        // is normalized here
+        const float row_sc = (cx == 1 && a.n_part == 0) ? (l_run == 0.0f ? 0.0f : 1.0f / l_run) : 1.0f;
         float *stage = reinterpret_cast<float *>(sm);
 #pragma unroll 1
         for (int c = 0; c < DVH / 32; ++c) {
@@ -555,12 +558,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 #pragma unroll
             for (int e = 0; e < 32; e += 4)
                 *reinterpret_cast<float4 *>(srow + e) =
-                    make_float4(__uint_as_float(rr[e]), __uint_as_float(rr[e + 1]), __uint_as_float(rr[e + 2]),
-                                __uint_as_float(rr[e + 3]));
+                    make_float4(__uint_as_float(rr[e]) * row_sc, __uint_as_float(rr[e + 1]) * row_sc,
+                                __uint_as_float(rr[e + 2]) * row_sc, __uint_as_float(rr[e + 3]) * row_sc);
         }
         if (half == 0)
             reinterpret_cast<float2 *>(stage + 128 * SROW)[r] =
                 make_float2(l_run, m_run == -INFINITY ? kMInit : m_run * kLn2);   // (S, M), natural log
+        fence_proxy_async_smem();   // the staged rows may leave by bulk copy
     }
 
     // ------------------------------------------------------ store or merge
@@ -574,30 +578,36 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     __syncthreads();
     cluster_sync();
     if (warp >= 2 && cx == 1) {
-        // No merge in the cluster: the 256 softmax threads copy the staged rows
-        // out with independent float4 loads and stores (normalized when the
-        // output is final, else as partial slot `split` with its (S, M)).
+        // No merge in the cluster: each staged row (final and normalized, or
+        // partial slot `split` with its (S, M)) leaves by one bulk copy issued
+        // by its own thread; a destination off a 16-byte boundary is written
+        // with plain stores instead.
         constexpr int F4 = DV / 4;                      // float4 per row
         const int t2 = tid - 64;
         const int nrows = a.H * a.L;
         const bool final_out = a.n_part == 0;
         const float *stage = reinterpret_cast<const float *>(sm);
         const float2 *stage_ml = reinterpret_cast<const float2 *>(stage + 128 * SROW);
-        for (int idx = t2; idx < rows_here * F4; idx += 256) {
-            const int rr = idx / F4, c4 = idx % F4;
+        bool issued = false;
+        for (int rr = t2; rr < rows_here; rr += 256) {
             const int rg2 = rt * RT + rr;
             const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
-            float4 o = *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * c4);
-            float *dst;
-            if (final_out) {
-                const float sl = stage_ml[rr].x;
-                const float inv = sl == 0.0f ? 0.0f : 1.0f / sl;
-                o.x *= inv; o.y *= inv; o.z *= inv; o.w *= inv;
-                dst = a.out + rid2 * D + os * DV;
+            float *dst = final_out ? a.out + rid2 * D + os * DV
+                                   : a.part_o + (static_cast<size_t>(split) * nrows + rid2) * D + os * DV;
+            const float *src = stage + rr * SROW;
+            if ((reinterpret_cast<uintptr_t>(dst) & 15u) == 0) {
+                bulk_store(dst, src, DV * 4);
+                issued = true;
             } else {
-                dst = a.part_o + (static_cast<size_t>(split) * nrows + rid2) * D + os * DV;
+                for (int c4 = 0; c4 < F4; ++c4) {
+                    const float4 o = *reinterpret_cast<const float4 *>(src + 4 * c4);
+                    dst[4 * c4] = o.x; dst[4 * c4 + 1] = o.y; dst[4 * c4 + 2] = o.z; dst[4 * c4 + 3] = o.w;
+                }
             }
-            *reinterpret_cast<float4 *>(dst + 4 * c4) = o;
+        }
+        if (issued) {
+            bulk_commit();
+            bulk_wait_all();   // the stage is read and the rows written before the CTA moves on
         }
         if (!final_out && os == 0)
             for (int rr = t2; rr < rows_here; rr += 256) {
