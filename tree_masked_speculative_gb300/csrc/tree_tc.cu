@@ -568,15 +568,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     }
 
     // ------------------------------------------------------ store or merge
-    // After the cluster barrier every CTA's staged rows are visible to its
-    // peers.  Without an x extent each CTA stores its own rows; otherwise CTA
+    // With an x extent, after the cluster barrier every CTA's staged rows are
+    // visible to its peers.  Without one each CTA stores its own rows; otherwise CTA
     // x of the cluster takes rows [x * n, (x + 1) * n) of the tile and merges
     // them over the cx splits of the cluster (log-sum-exp weights, loads from
     // the peers' shared memory).  With n_part == 0 the merged rows are final
     // (normalized output); else they are partial slot split / cx.
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
+    if (cx > 1) cluster_sync();   // the merge reads the peers' staged rows (cx is uniform in a cluster)
     if (warp >= 2 && cx == 1) {
         // No merge in the cluster: each staged row (final and normalized, or
         // partial slot `split` with its (S, M)) leaves by one bulk copy issued
