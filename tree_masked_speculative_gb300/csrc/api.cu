@@ -410,7 +410,10 @@ bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
     sh->rr = rep <= 4 ? 4 : rep <= 8 ? 8 : rep <= 16 ? 16 : 32;
     sh->rp = sh->rr < 16 ? 16 : sh->rr;
     sh->n_rb = (rep + sh->rr - 1) / sh->rr;
-    const int need = (int)p->dim + 2 * ng * sh->rp;
+    // TMEM: O^T (dimensions on lanes) takes rows-per-CTA columns per 128
+    // dimensions, then the two score buffers
+    const int ob = p->dim >= 128 ? (int)p->dim / 128 : 1;
+    const int need = ob * sh->rp + 2 * ng * sh->rp;
     if (need > 512) return false;
     int cols = 32;
     while (cols < need) cols <<= 1;

@@ -120,6 +120,12 @@ __device__ __forceinline__ int pos4(int k) { return ((k & 3) << 1) | (k >> 2); }
 
 template <int N>
 __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]);
+template <int N>
+__device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]);
+template <>
+__device__ __forceinline__ void tmem_stn<16>(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_stn<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
 template <>
 __device__ __forceinline__ void tmem_ldn<2>(uint32_t taddr, uint32_t (&r)[2]) { tmem_ld2(taddr, r); }
 template <>
@@ -242,31 +248,50 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     const bool bf16 = a.t_is_bf16 != 0;
     int *err = a.err;
 
-    if (tid == 0) {
-        for (int i = 0; i < NK; ++i) {
-            mbar_init(&bars->kfull[i], 1);
-            mbar_init(&bars->kempty[i], kDecGroup);
+    if (warp == 0) {
+        // the barriers, initialized by the lanes of warp 0 in parallel
+        if (lane < NK) {
+            mbar_init(&bars->kfull[lane], 1);
+            mbar_init(&bars->kempty[lane], kDecGroup);
         }
         // V slot: the producer's expect-tx arrive, 32 cp.async arrivals, 32 plain arrivals
-        for (int i = 0; i < NV; ++i) {
-            mbar_init(&bars->vfull[i], 65);
-            mbar_init(&bars->vempty[i], kDecGroup + kSmWarps);
+        if (lane < NV) {
+            mbar_init(&bars->vfull[lane], 65);
+            mbar_init(&bars->vempty[lane], kDecGroup + kSmWarps);
         }
-        for (int i = 0; i < ND; ++i) {
-            mbar_init(&bars->dfull[i], kDecGroup);
-            mbar_init(&bars->dempty[i], 1);
+        if (lane < ND) {
+            mbar_init(&bars->dfull[lane], kDecGroup);
+            mbar_init(&bars->dempty[lane], 1);
         }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(&bars->s_full[i], 1);
-            mbar_init(&bars->s_free[i], kSmWarps);
-            mbar_init(&bars->p_full[i], kSmWarps);
-            mbar_init(&bars->p_free[i], 1);
-            mbar_init(&bars->o_done[i], 1);
+        if (lane < 2) {
+            mbar_init(&bars->s_full[lane], 1);
+            mbar_init(&bars->s_free[lane], kSmWarps);
+            mbar_init(&bars->p_full[lane], kSmWarps);
+            mbar_init(&bars->p_free[lane], 1);
+            mbar_init(&bars->o_done[lane], 1);
         }
-        mbar_init(&bars->q_ready, kSmWarps);
-        mbar_init(&bars->drain, 1);
-        bars->abort_flag = 0;
+        if (lane == 31) {
+            mbar_init(&bars->q_ready, kSmWarps);
+            mbar_init(&bars->drain, 1);
+            bars->abort_flag = 0;
+        }
         fence_mbar_init();
+    }
+    // the softmax warps fetch their Q rows now, to use them once the barriers exist
+    constexpr int RPW = RP / kSmWarps;                  // Q rows staged per softmax warp (2 or 4)
+    const int sw = warp - 2 - kDecWarps;                // softmax warp index (0..7 for those warps)
+    const int E = DIM / 32;                             // Q elements per lane (2, 4 or 8)
+    float qx[RPW][8];
+    if (sw >= 0) {
+        const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const int r = sw + kSmWarps * i;
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                qx[i][e] = (e < E && r < rows_here) ? t2f(qg[static_cast<size_t>(q0 + r) * DIM + lane * E + e], bf16)
+                                                    : 0.0f;
+        }
     }
     if (warp == 1) {
         tmem_alloc(&bars->tmem_base, static_cast<uint32_t>(a.tc_cols));
@@ -276,8 +301,11 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
+    // TMEM: O^T (lanes = dimensions of a 128-dimension block, columns = rows),
+    // RP columns per block, then the two score buffers
+    const int OB = DIM >= 128 ? DIM / 128 : 1;
     const uint32_t tm_o = tmem;
-    auto tm_s = [&](int sb) { return tmem + static_cast<uint32_t>(DIM + sb * NG * RP); };
+    auto tm_s = [&](int sb) { return tmem + static_cast<uint32_t>(OB * RP + sb * NG * RP); };
 
     if (warp == 0) {
         // ------------------------------------------------------------ producer
@@ -376,11 +404,12 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0 && T > 0) {
             const uint32_t id_s = idesc_f16(128, RP, 0, 0, 0);
-            const uint32_t id_pv = idesc_f16(128, 64, 0, 0, 1);
+            const uint32_t id_pv = idesc_f16(128, RP, 0, 1, 0);   // A = V (MN-major), B = P (K-major)
             const uint32_t q_addr = smem_u32(smem + L.q0), d_addr = smem_u32(smem + L.d0);
             const uint32_t p_addr = smem_u32(smem + L.p0);
             const uint64_t kmaj = sw128_desc_hi(16, 1024);          // K-major operands
-            const uint64_t vmn = sw128_desc_hi(kQtcChunk, 1024);    // V chunk, MN-major
+            // V chunks as the MN-major A operand: 64-dimension atoms one chunk apart
+            const uint64_t vmn = sw128_desc_hi(kQtcChunk, 1024);
             // decoded chunks: K in slots [0, ND/2), V in [ND/2, ND), each ring in
             // order; slot and phase kept as running counters (this thread is on
             // the critical path: no divisions in its loop)
@@ -391,6 +420,13 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 if (!wait1(bars, &bars->dfull[dslot[ring]], dph[ring], err)) return false;
                 tc_fence_after();
                 *ca = d_addr + static_cast<uint32_t>(dslot[ring]) * kQtcChunk;
+                return true;
+            };
+            // the chunk after the current one (the second half of a V pair: same
+            // ring pass, since a pair starts on an even slot of an even ring)
+            auto take_next = [&](int ring) -> bool {
+                if (!wait1(bars, &bars->dfull[dslot[ring] + 1], dph[ring], err)) return false;
+                tc_fence_after();
                 return true;
             };
             auto give = [&](int ring) {
@@ -423,14 +459,19 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 if (!wait1(bars, &bars->p_full[t & 1], (static_cast<uint32_t>(t) >> 1) & 1u, err)) return false;
                 tc_fence_after();
                 const uint32_t pa = p_addr + (t & 1) * 2 * L.pkb;
-                for (int c = 0; c < NCH; ++c) {
+                // O^T[128 dims][rows] += V^T P^T per 128-dimension block: its two
+                // 64-dimension chunks sit in adjacent ring slots (the V ring holds
+                // an even number of chunks and a tile part starts on an even one)
+                for (int mb = 0; mb < OB; ++mb) {
                     uint32_t ca;
                     if (!take(1, &ca)) return false;
+                    if (NCH > 1 && !take_next(1)) return false;
 #pragma unroll
                     for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tm_o + c * 64, sw128_desc_at(kmaj, pa + (kk >> 2) * L.pkb + (kk & 3) * 32),
-                                   sw128_desc_at(vmn, ca + kk * 2048), id_pv, (t | kk) != 0);
+                        mma_f16_ss(tm_o + static_cast<uint32_t>(mb * RP), sw128_desc_at(vmn, ca + kk * 2048),
+                                   sw128_desc_at(kmaj, pa + (kk >> 2) * L.pkb + (kk & 3) * 32), id_pv, (t | kk) != 0);
                     give(1);
+                    if (NCH > 1) give(1);
                 }
                 mma_commit(&bars->o_done[t & 1]);
                 mma_commit(&bars->p_free[t & 1]);   // P_t buffer free once PV_t is done
@@ -484,32 +525,20 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         }
     } else {
         // -------------------------------------------- softmax and epilogue
-        const int sw = warp - 2 - kDecWarps;                // 0..7
         const int half = sw >> 2;                           // rows [half * RH, half * RH + RH)
         const int quarter = warp & 3;
         const int tl = quarter * 32 + lane;                 // token of the tile = TMEM lane
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int hr0 = half * RH;
-        const bool o_warp = half == 0 && quarter == 0;      // owns O (TMEM lanes 0..31 = rows)
+        const bool o_warp = half == 0;                      // the first half's warps own O^T (all lanes)
         auto half_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + half) : "memory"); };
         auto all_sync = [&]() { asm volatile("bar.sync 3, 256;" ::: "memory"); };
 
-        // ---- Q operand (f16, rows scaled by 2^-e_r) and per-row constants:
-        // every load of this warp's rows is issued before any is used
+        // ---- Q operand (f16, rows scaled by 2^-e_r) and per-row constants from
+        // the rows fetched at the start
         {
-            const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
-            const int E = DIM / 32;                         // dimensions per lane (2, 4 or 8)
             const float qs = a.scale * kLog2e;
-            constexpr int RPW = RP / kSmWarps;              // rows per warp (2 or 4)
-            float x[RPW][8];
-#pragma unroll
-            for (int i = 0; i < RPW; ++i) {
-                const int r = sw + kSmWarps * i;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    x[i][e] = (e < E && r < rows_here) ? t2f(qg[static_cast<size_t>(q0 + r) * DIM + lane * E + e], bf16)
-                                                       : 0.0f;
-            }
+            auto &x = qx;
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
                 const int r = sw + kSmWarps * i;
@@ -518,12 +547,18 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
 #pragma unroll
                 for (int e = 0; e < 8; ++e) { amax = fmaxf(amax, fabsf(x[i][e])); gs += x[i][e]; }
                 amax = warp_max(amax);
-                const int ex = amax > 0.0f ? ilogbf(amax) - 14 : 0;
+                // 2^ex with max |q'| = max |q| * 2^-ex in [2^14, 2^15): the exponent
+                // field of amax, clamped so that both 2^ex and 2^-ex are normal
+                // floats (a row whose entries are all below 2^-100 scales to zeros)
+                int ex = amax > 0.0f ? static_cast<int>((__float_as_uint(amax) >> 23) & 0xFFu) - 127 - 14 : 0;
+                ex = max(-100, min(100, ex));
+                const float up = __uint_as_float(static_cast<uint32_t>(127 + ex) << 23);     // 2^ex
+                const float down = __uint_as_float(static_cast<uint32_t>(127 - ex) << 23);   // 2^-ex
                 const int lpg = G / E;                      // lanes per scale group (power of two <= 32)
                 for (int m = 1; m < lpg; m <<= 1) gs += __shfl_xor_sync(0xffffffffu, gs, m);
                 // the bias term in units of the row factor: sum_g b_g * 2^-e_r * sum_{d in g} q_d
-                if (lane % lpg == 0) sQG[(lane * E / G) * RP + r] = live ? ldexpf(gs, -ex) : 0.0f;
-                if (lane == 0) sF[r] = live ? ldexpf(qs, ex) : 0.0f;
+                if (lane % lpg == 0) sQG[(lane * E / G) * RP + r] = live ? gs * down : 0.0f;
+                if (lane == 0) sF[r] = live ? qs * up : 0.0f;
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     if (e >= E) break;
@@ -531,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                     const int pos = BITS == 4 ? ((d & ~7) | pos4(d & 7)) : d;
                     const int blk = pos >> 6, pc = (pos & 63) >> 3;
                     *reinterpret_cast<__half *>(smem + L.q0 + blk * RP * 128 + r * 128 + ((pc ^ (r & 7)) << 4) +
-                                                (pos & 7) * 2) = __float2half_rn(ldexpf(x[i][e], -ex));
+                                                (pos & 7) * 2) = __float2half_rn(x[i][e] * down);
                 }
             }
             fence_proxy_async_smem();
@@ -622,20 +657,22 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             // the P buffer of this tile is free once PV of tile t - 2 is done
             ok = ok && waitw(bars, &bars->p_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err);
             if (o_warp && t > 0 && (sNeed[sb * 2] | sNeed[sb * 2 + 1]) != 0) {
-                // rows moved their max: rescale O (rows = TMEM lanes) once PV of
-                // the previous tile is done
-                const float al = lane < RR ? sAlpha[sb * 32 + lane] : 1.0f;
+                // rows moved their max: rescale their columns of O^T (all lanes)
+                // once PV of the previous tile is done
                 ok = ok && waitw(bars, &bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, err);
                 tc_fence_after();
                 if (ok) {
+                    // 16 columns (rows) at a time: few registers on this rare path
 #pragma unroll 1
-                    for (int c = 0; c < DIM / 32; ++c) {
-                        uint32_t v[32];
-                        tmem_ld32(tm_o + c * 32, v);
+                    for (int c16 = 0; c16 < OB * RP; c16 += 16) {
+                        uint32_t v[16];
+                        tmem_ld16(tm_o + lane_off + static_cast<uint32_t>(c16), v);
                         tmem_wait_ld();
+                        const int r0 = c16 % RP;                    // row of the first column
 #pragma unroll
-                        for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * al);
-                        tmem_st32(tm_o + c * 32, v);
+                        for (int j = 0; j < 16; ++j)
+                            if (r0 + j < RR) v[j] = __float_as_uint(__uint_as_float(v[j]) * sAlpha[sb * 32 + r0 + j]);
+                        tmem_st16(tm_o + lane_off + static_cast<uint32_t>(c16), v);
                     }
                     tmem_wait_st();
                 }
@@ -669,77 +706,55 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         if (quarter == 0 && lane < RH) sMrow[hr0 + lane] = m_row;
         all_sync();
         if (o_warp && ok) {
-            const int r = lane;                              // O row = TMEM lane
-            const bool live = r < rows_here;
-            const int q = q0 + r;
-            float l_tot = 0.0f, m_fin = -INFINITY;
-            if (r < RR) {
+            // the first half's four warps: lane = a dimension position of each
+            // 128-dimension block (TMEM lane quarter * 32 + lane), column = row
+            const int pos = quarter * 32 + lane;             // 0..127
+            // dimension held at that position (4-bit words decode to positions 0,4,1,5,2,6,3,7)
+            const int p8 = pos & 7;
+            const int dpos = (pos & ~7) | (BITS == 4 ? ((p8 >> 1) | ((p8 & 1) << 2)) : p8);
+            // output factor of row r: 1 for a partial, else 1 / (l + sink term)
+            auto row_factor = [&](int r) -> float {
+                if (a.nwg > 1) return 1.0f;
                 const float *sh = sSum + (r / RH) * 128 + (r % RH);
-                l_tot = (sh[0] + sh[32]) + (sh[64] + sh[96]);
-                m_fin = sMrow[r];
-            }
-            float f = 1.0f;
-            if (a.nwg == 1 && live) {
+                const float l_tot = (sh[0] + sh[32]) + (sh[64] + sh[96]);
+                const float m_fin = sMrow[r];
                 float cf = 1.0f, sf = l_tot;
                 if (a.has_sinks) {
-                    const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
+                    const float sk = kLog2e * __ldg(a.sinks + ((q0 + r) % a.nQ));
                     const float mx = fmaxf(m_fin, sk);
                     cf = m_fin == -INFINITY ? 0.0f : ex2(m_fin - mx);
                     sf = l_tot * cf + ex2(sk - mx);
                 }
-                f = sf > 0.0f ? cf / sf : 0.0f;
-            }
+                return sf > 0.0f ? cf / sf : 0.0f;
+            };
 #pragma unroll 1
-            for (int c = 0; c < DIM / 32; ++c) {
-                uint32_t v[32];
+            for (int mb = 0; mb < OB; ++mb) {
+                uint32_t v[RP];
                 if (T > 0) {
-                    tmem_ld32(tm_o + c * 32, v);
+                    tmem_ldn<RP>(tm_o + lane_off + static_cast<uint32_t>(mb * RP), v);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) v[e] = 0u;
+                    for (int j = 0; j < RP; ++j) v[j] = 0u;
                 }
-                if (!live) continue;
+                const int d = mb * 128 + dpos;
+                if (d >= DIM) continue;
 #pragma unroll
-                for (int g8 = 0; g8 < 4; ++g8) {
-                    float o[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)   // for 4-bit codes dimension k of the word sits at column pos4(k)
-                        o[k] = __uint_as_float(v[8 * g8 + (BITS == 4 ? pos4(k) : k)]) * f;
-                    const size_t base = static_cast<size_t>(q) * DIM + c * 32 + g8 * 8;
-                    if (a.nwg > 1) {
-                        float4 *po = reinterpret_cast<float4 *>(a.part_o + static_cast<size_t>(split) * a.rows * DIM + base);
-                        po[0] = make_float4(o[0], o[1], o[2], o[3]);
-                        po[1] = make_float4(o[4], o[5], o[6], o[7]);
-                    } else if (!a.al_out) {
-#pragma unroll
-                        for (int k = 0; k < 8; ++k) {
-                            if (a.out_f32) static_cast<float *>(a.out)[base + k] = o[k];
-                            else if (bf16) static_cast<__nv_bfloat16 *>(a.out)[base + k] = __float2bfloat16_rn(o[k]);
-                            else static_cast<__half *>(a.out)[base + k] = __float2half_rn(o[k]);
-                        }
-                    } else if (a.out_f32) {
-                        float4 *po = reinterpret_cast<float4 *>(static_cast<float *>(a.out) + base);
-                        po[0] = make_float4(o[0], o[1], o[2], o[3]);
-                        po[1] = make_float4(o[4], o[5], o[6], o[7]);
-                    } else {
-                        uint32_t pk[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            if (bf16) {
-                                __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * e], o[2 * e + 1]);
-                                pk[e] = *reinterpret_cast<uint32_t *>(&h);
-                            } else {
-                                __half2 h = __floats2half2_rn(o[2 * e], o[2 * e + 1]);
-                                pk[e] = *reinterpret_cast<uint32_t *>(&h);
-                            }
-                        }
-                        *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.out) + base) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    }
+                for (int r = 0; r < RR; ++r) {
+                    if (r >= rows_here) break;
+                    const float o = __uint_as_float(v[r]) * row_factor(r);
+                    const size_t idx = static_cast<size_t>(q0 + r) * DIM + d;
+                    if (a.nwg > 1) a.part_o[static_cast<size_t>(split) * a.rows * DIM + idx] = o;
+                    else if (a.out_f32) static_cast<float *>(a.out)[idx] = o;
+                    else if (bf16) static_cast<__nv_bfloat16 *>(a.out)[idx] = __float2bfloat16_rn(o);
+                    else static_cast<__half *>(a.out)[idx] = __float2half_rn(o);
                 }
             }
-            if (a.nwg > 1 && live)
-                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q] = make_float2(l_tot, m_fin);
+            if (a.nwg > 1 && quarter == 0 && lane < rows_here) {
+                const float *sh = sSum + (lane / RH) * 128 + (lane % RH);
+                reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] =
+                    make_float2((sh[0] + sh[32]) + (sh[64] + sh[96]), sMrow[lane]);
+            }
         }
     }
 

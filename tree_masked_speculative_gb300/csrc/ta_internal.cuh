@@ -213,6 +213,9 @@ __host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng
     o = qtc_align(o, 1024);
     L.d0 = o;
     o += nd * kQtcChunk;
+    // a 64-dimension V chunk is read as the first half of a 128-dimension MMA
+    // operand: keep the chunk-sized read past the ring inside the allocation
+    if (dim < 128) o += kQtcChunk;
     L.kslot = qtc_align(128 * wpt * 4, 16);
     L.k0 = o;
     o += nk * L.kslot;
