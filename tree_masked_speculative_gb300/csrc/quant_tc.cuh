@@ -123,6 +123,12 @@ __device__ __forceinline__ void tmem_ldn(uint32_t taddr, uint32_t (&r)[N]);
 template <int N>
 __device__ __forceinline__ void tmem_stn(uint32_t taddr, const uint32_t (&r)[N]);
 template <>
+__device__ __forceinline__ void tmem_stn<2>(uint32_t taddr, const uint32_t (&r)[2]) { tmem_st2(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_stn<4>(uint32_t taddr, const uint32_t (&r)[4]) { tmem_st4(taddr, r); }
+template <>
+__device__ __forceinline__ void tmem_stn<8>(uint32_t taddr, const uint32_t (&r)[8]) { tmem_st8(taddr, r); }
+template <>
 __device__ __forceinline__ void tmem_stn<16>(uint32_t taddr, const uint32_t (&r)[16]) { tmem_st16(taddr, r); }
 template <>
 __device__ __forceinline__ void tmem_stn<32>(uint32_t taddr, const uint32_t (&r)[32]) { tmem_st32(taddr, r); }
@@ -230,13 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     float *sF = reinterpret_cast<float *>(smem + L.rc);      // [RP] 2^e_r * scale * log2(e)
     float *sQG = sF + RP;                                     // [NG][RP] 2^-e_r * sum_{d in g} q_d
     // softmax exchange: row maxima [parity][half][quarter][32], row sums
-    // [half][quarter][32], rescale factors [parity][32], flags [parity][half],
-    // final row maxima [32]
+    // [half][quarter][32], final row maxima [32]
     float *sMax = reinterpret_cast<float *>(smem + L.red);
     float *sSum = sMax + 512;
-    float *sAlpha = sSum + 256;
-    int *sNeed = reinterpret_cast<int *>(sAlpha + 64);
-    float *sMrow = reinterpret_cast<float *>(sNeed + 4);
+    float *sMrow = sSum + 256;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, rb = blockIdx.y % a.n_rb, kv = blockIdx.y / a.n_rb;
     const int q0 = kv * a.rep + rb * RR;
@@ -649,30 +652,25 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
 #pragma unroll
                 for (int r = 0; r < RH; ++r) lsum[r] *= __shfl_sync(0xffffffffu, alpha, r);
             }
-            if (quarter == 0) {
-                if (lane < RH) sAlpha[sb * 32 + hr0 + lane] = alpha;
-                if (lane == 0) sNeed[sb * 2 + half] = need ? 1 : 0;
-            }
-            all_sync();
             // the P buffer of this tile is free once PV of tile t - 2 is done
             ok = ok && waitw(bars, &bars->p_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err);
-            if (o_warp && t > 0 && (sNeed[sb * 2] | sNeed[sb * 2 + 1]) != 0) {
-                // rows moved their max: rescale their columns of O^T (all lanes)
-                // once PV of the previous tile is done
+            if (need && t > 0) {
+                // this half's rows moved their max: the half's four warps rescale
+                // the rows' columns of O^T (their lanes) once PV of the previous
+                // tile is done; the other half's columns are its own business
                 ok = ok && waitw(bars, &bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, err);
                 tc_fence_after();
                 if (ok) {
-                    // 16 columns (rows) at a time: few registers on this rare path
 #pragma unroll 1
-                    for (int c16 = 0; c16 < OB * RP; c16 += 16) {
-                        uint32_t v[16];
-                        tmem_ld16(tm_o + lane_off + static_cast<uint32_t>(c16), v);
+                    for (int mb = 0; mb < OB; ++mb) {
+                        const uint32_t col = tm_o + lane_off + static_cast<uint32_t>(mb * RP + hr0);
+                        uint32_t v[RH];
+                        tmem_ldn<RH>(col, v);
                         tmem_wait_ld();
-                        const int r0 = c16 % RP;                    // row of the first column
 #pragma unroll
-                        for (int j = 0; j < 16; ++j)
-                            if (r0 + j < RR) v[j] = __float_as_uint(__uint_as_float(v[j]) * sAlpha[sb * 32 + r0 + j]);
-                        tmem_st16(tm_o + lane_off + static_cast<uint32_t>(c16), v);
+                        for (int r = 0; r < RH; ++r)
+                            v[r] = __float_as_uint(__uint_as_float(v[r]) * __shfl_sync(0xffffffffu, alpha, r));
+                        tmem_stn<RH>(col, v);
                     }
                     tmem_wait_st();
                 }
