@@ -166,3 +166,13 @@ def test_quant_tree_workload_full(ta):
     ref = oracle.quant_oracle_for(wl, inp)
     got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
     assert_close(got, ref, what="quant tree workload f32")
+
+
+def test_quant_more_splits_than_tiles(ta):
+    """A forced split count above the number of 128-token tiles: the splits
+    without a token leave an empty partial (S = 0) that the merge skips."""
+    wl = qwl(N=200, nwg=5, sinks=1, dtype="bf16")
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, nwg=5, out_dtype=torch.float32).cpu().double().numpy()
+    assert_close(got, ref, what="more splits than tiles")

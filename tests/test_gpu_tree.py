@@ -34,6 +34,8 @@ CASES = [
     (12, 4, 128, 1000, 1024, 16, "bf16", 0),  # 48 rows per KV head
     (16, 2, 256, 517, 600, 20, "f16", 5),     # 160 rows per KV head
     (8, 4, 512, 260, 300, 9, "bf16", 0),
+    (4, 2, 256, 150, 160, 4, "f32", 2),       # f32 K/V at each head dimension (CUDA-core kernel)
+    (4, 2, 512, 100, 128, 3, "f32", 0),
 ]
 
 
