@@ -741,7 +741,6 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
         a.tc_nd = pl.nd;
         a.tc_nk = pl.nk;
         a.tc_nv = pl.nv;
-        a.al_out = al16(out.ptr);
         if ((uint64_t)kvr * (uint64_t)sh.n_rb > 65535u)
             return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: too many KV rows x row blocks for one launch");
         e = launch_quant_tc(a, pl.smem, s);

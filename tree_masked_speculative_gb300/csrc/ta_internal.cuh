@@ -128,7 +128,6 @@ struct QuantArgs {
     // first 128-token tile and tile count of the window, ring depths (decoded
     // chunks, packed-K slots, packed-V slots) and TMEM columns
     int rp, n_rb, j_lo, ntile, tc_nd, tc_nk, tc_nv, tc_cols;
-    int al_out;              // out starts on a 16-byte boundary
 };
 
 // Query rows served by one CTA of the quantized-KV kernel (a row group).
@@ -182,13 +181,14 @@ __host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
     return L;
 }
 // Shared-memory layout of the tensor-core quantized-KV kernel (byte offsets).
-// Two P buffers (A operand of PV: [128 rows][128 tokens] 16-bit, 128-byte
-// swizzled, only the first rp rows written; the MMA's reads of the other rows
-// stay inside the CTA's shared memory), the 16-bit Q operand ([rp][dim],
-// 64-dimension blocks), the ring of decoded 16 KB chunks ([128 tokens][64
-// dims] f16), the packed-K ring, the packed-V ring (V words, K and V scale /
-// bias runs, bool and float mask rows), per-row constants, the softmax
-// exchange area and the mbarriers.
+// Two P buffers (the PV operand P^T: [rp rows][128 tokens] 16-bit, 128-byte
+// swizzled, two 64-token k-blocks of rp * 128 bytes; rows past the CTA's
+// query rows are never written and only feed O^T columns that are never
+// read), the 16-bit Q operand ([rp][dim], 64-dimension blocks), the ring of
+// decoded 16 KB chunks ([128 tokens][64 dims] f16: K half, V half), the
+// packed-K ring, the packed-V ring (V words, K and V scale / bias runs, bool
+// and float mask rows), per-row constants, the softmax exchange area and the
+// mbarriers.
 struct QtcLayout {
     int pkb;                              // bytes of a 64-token k-block of a P buffer (rp x 128 B)
     int p0, q0, d0, k0, kslot, v0, vslot;
@@ -197,7 +197,7 @@ struct QtcLayout {
 };
 constexpr int kQtcChunk = 16384;
 constexpr int kQuantTcMaxRing = 16;   // deepest ring of the tensor-core quantized kernel
-constexpr int kQtcRedBytes = 4096;   // softmax exchange area (row maxima, sums, rescale factors)
+constexpr int kQtcRedBytes = 4096;   // softmax exchange area (row maxima, row sums, final maxima)
 constexpr int kQtcBarBytes = 1280;
 __host__ __device__ inline int qtc_align(int o, int a) { return (o + a - 1) / a * a; }
 __host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng, int nd, int nk, int nv,
