@@ -164,6 +164,27 @@ ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, c
                                const ta_buf *out, void *stream);
 
 /*
+ * Main pass with the tree mask given compactly as a parent array instead of
+ * a dense [q_l, mask_stride] f32 mask (the tree semantics of [TA-M]'s header
+ * comment: node i of the draft tree sits at KV position kv_seq_len - q_l + i
+ * and attends the prefix [0, kv_seq_len - q_l), its ancestors and itself).
+ * The result is bit-identical to tree_attn_fwd given the mask
+ * tree_mask_build writes for the same parents; no dense mask
+ * is read or written (a per-row ancestor bitset of (q_l + 31) / 32 words is
+ * built in `tmp` by one extra launch).
+ *   parents  [q_l] i32 on the device, the rule of tree_mask_build: a chain
+ *            i, parents[i], ... ends at a value outside [0, current node).
+ *   q, k, v, tmp, out  as for tree_attn_fwd; p->mask_stride is not used.
+ * Errors: as tree_attn_fwd's checks; parents I32, >= 4*q_l bytes, 4-byte
+ * aligned; q_l <= kv_seq_len; q_l > 256 is TA_ERR_UNSUPPORTED (use
+ * tree_mask_build and tree_attn_fwd).  Nothing is launched on error.
+ * tree_attn_reduce merges its partials as for tree_attn_fwd.
+ */
+ta_status tree_attn_fwd_parents(const ta_tree_params *p, const ta_buf *parents, const ta_buf *q,
+                                const ta_buf *k, const ta_buf *v, const ta_buf *tmp, const ta_buf *out,
+                                void *stream);
+
+/*
  * Second pass ([TA-R] tree_attention, reduce pass): merges the nwg partials
  * of every (query, head) row with a log-sum-exp rescale:
  *   M* = max_w M_w,  S* = sum_w S_w e^(M_w - M*),

@@ -187,6 +187,38 @@ def test_reduce_validates_before_launch(ta):
     assert st == 1
 
 
+@pytest.mark.parametrize("kw,pbytes,pdtype,st_want,frag", [
+    (dict(q_l=10), 10 * 4, "U32", 1, "parents dtype"),
+    (dict(q_l=10), None, None, 1, "parents dtype"),                    # no parent array at all
+    (dict(q_l=10), 9 * 4, "I32", 2, "parents"),
+    (dict(q_l=120), 120 * 4, "I32", 1, "q_l"),                          # more nodes than keys
+    (dict(q_l=257, kv_seq_len=1000, mask_stride=1000), 257 * 4, "I32", 4, "q_l <= 256"),
+    (dict(q_l=10, head_dim=96), 10 * 4, "I32", 1, "head_dim"),
+])
+def test_tree_parents_rejections(ta, kw, pbytes, pdtype, st_want, frag):
+    p = _p(ta, **kw)
+    H, L, D = p.n_heads, p.q_l, p.head_dim
+    B = lambda n, c: _b(ta, n, c)
+    q, out = B(H * L * D * 4, ta.TA_F32), B(H * L * D * 4, ta.TA_F32)
+    k = v = B(p.n_kv_heads * p.kv_capacity * D * 2, ta.TA_F16)
+    ws = ta.tree_attn_workspace_bytes(p)
+    tmp = B(ws if ws < 2 ** 63 else 0, ta.TA_F32)
+    code = {"I32": ta.TA_I32, "U32": ta.TA_U32}
+    R = ctypes.byref
+    par = R(_b(ta, pbytes, code[pdtype])) if pbytes is not None else None
+    before = ta.ta_launch_count()
+    st = ta.lib.tree_attn_fwd_parents(R(p), par, R(q), R(k), R(v), R(tmp), R(out), None)
+    assert ta.ta_launch_count() == before, "a failing call must not launch"
+    assert st == st_want and frag in ta.ta_last_error()
+
+
+def test_workspace_holds_ancestor_bitsets(ta):
+    # a parent-array tree mask keeps q_l * ceil(q_l / 32) words of ancestor bits in tmp
+    small = ta.tree_attn_workspace_bytes(_p(ta, q_l=32, kv_seq_len=1000, mask_stride=1000))
+    large = ta.tree_attn_workspace_bytes(_p(ta, q_l=256, kv_seq_len=1000, mask_stride=1000))
+    assert large - small >= 256 * 8 * 4 - 32 * 4
+
+
 # ------------------------------------------------------------------- quant
 def _qp(ta, **kw):
     d = dict(batch=2, n_q_heads=8, n_kv_heads=2, dim=128, tokens=100, bits=4, group_size=64,

@@ -36,6 +36,8 @@ CASES = [
     (8, 4, 512, 260, 300, 9, "bf16", 0),
     (4, 2, 256, 150, 160, 4, "f32", 2),       # f32 K/V at each head dimension (CUDA-core kernel)
     (4, 2, 512, 100, 128, 3, "f32", 0),
+    (16, 2, 512, 700, 700, 20, "bf16", 3),    # 160 rows: two row tiles per O half
+    (20, 1, 512, 400, 416, 15, "f16", 2),     # 300 rows: three row tiles
 ]
 
 
@@ -259,3 +261,69 @@ def test_tree_mask_build_feeds_the_verify_pass(ta):
     inp2["mask"] = d_mask.cpu()
     out_dev = run_tree(ta, wl, inp2)
     assert torch.equal(out_host, out_dev)
+
+
+# ------------------------------------------------- tree mask as a parent array
+def _run_parents(ta, wl, inp, parents, nwg=None):
+    d = to_dev(inp)
+    par = torch.tensor(parents, dtype=torch.int32, device="cuda")
+    out = ta.tree_attention(d["q"], d["k"], d["v"], None, n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads,
+                            kv_seq_len=wl.kv_seq_len, scale=wl.scale, mask_stride=wl.mask_stride,
+                            nwg=wl.nwg if nwg is None else nwg, parents=par)
+    torch.cuda.synchronize()
+    return out
+
+
+PARENT_CASES = [
+    # H, Hk, D, N, C, L, kv_dtype, topology, nwg
+    (24, 4, 256, 1000, 1024, 32, "f16", "fixed", 0),     # tensor cores, two row tiles
+    (16, 2, 512, 700, 700, 20, "bf16", "dynamic", 3),    # D 512, two O halves
+    (8, 2, 128, 300, 320, 13, "f16", "chain", 2),
+    (4, 2, 128, 256, 256, 8, "f32", "chain", 32),        # CUDA cores (f32 K/V)
+    (4, 4, 256, 90, 96, 3, "bf16", "dynamic", 0),        # CUDA cores (R = 3)
+    (2, 1, 128, 40, 40, 1, "f16", "dynamic", 1),         # a single node, one split
+    (8, 2, 128, 64, 64, 64, "f16", "dynamic", 0),        # no prefix: every key is a tree node
+    (2, 1, 128, 600, 600, 256, "f16", "chain", 0),       # the largest tree, a 256-deep chain
+    (4, 1, 256, 900, 900, 200, "bf16", "dynamic", 4),    # 800 rows, bitsets of 7 words
+]
+
+
+@pytest.mark.parametrize("H,Hk,D,N,C,L,kvd,topo,nwg", PARENT_CASES, ids=[str(i) for i in range(len(PARENT_CASES))])
+def test_parent_array_mask_bit_identical_to_dense(ta, path, H, Hk, D, N, C, L, kvd, topo, nwg):
+    """The parent-array entry gives, bit for bit, what the dense-mask entry gives
+    for the mask the device builder writes from the same parents; both match
+    the oracle on the host-built mask."""
+    wl = small_tree(H=H, Hk=Hk, D=D, N=N, C=C, L=L, kv_dtype=kvd, topology="chain", nwg=nwg, seed=N + L)
+    inp = W.make_tree_inputs(wl)
+    par = _parents(topo, L, seed=N)
+    inp["mask"] = W.tree_mask(par, N, N)
+    got = _run_parents(ta, wl, inp, par)
+    p = ta.tree_params(H, Hk, D, N, C, wl.scale, L, N, nwg)
+    d_mask = torch.empty((L, N), device="cuda")
+    ta.tree_mask_build(p, torch.tensor(par, dtype=torch.int32, device="cuda"), d_mask)
+    inp_dev = dict(inp)
+    inp_dev["mask"] = d_mask.cpu()
+    dense = run_tree(ta, wl, inp_dev)
+    assert torch.equal(got, dense)
+    assert_close(got.cpu().numpy(), oracle.tree_oracle_for(wl, inp), what="parents %s" % topo)
+
+
+def test_parent_array_out_of_range_values_end_chains(ta):
+    """Values outside [-1, i) end a node's chain there, as in the mask builder."""
+    wl = small_tree(H=16, Hk=2, D=128, N=400, C=400, L=12, kv_dtype="f16", nwg=2)
+    inp = W.make_tree_inputs(wl)
+    par = [-1, 0, 0, 7, 1, -5, 3, 2, 100, 4, 9, 8]    # 3 -> 7 (not smaller), 5 -> -5, 8 -> 100
+    ref_par = [-1, 0, 0, -1, 1, -1, 3, 2, -1, 4, 9, 8]
+    inp["mask"] = W.tree_mask(ref_par, wl.kv_seq_len, wl.mask_stride)
+    got = _run_parents(ta, wl, inp, par).cpu().numpy()
+    assert_close(got, oracle.tree_oracle_for(wl, inp))
+
+
+def test_parent_array_dynamic_tree_workload(ta):
+    """The dynamic-tree workload at full size: the parent-array entry equals the
+    dense-mask entry bit for bit on every output."""
+    wl = W.DYNAMIC_TREE
+    inp = W.make_tree_inputs(wl)
+    dense = run_tree(ta, wl, inp)
+    got = _run_parents(ta, wl, inp, inp["parents"])
+    assert torch.equal(got, dense)

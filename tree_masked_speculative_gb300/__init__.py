@@ -19,7 +19,7 @@ from . import build as _build_mod
 __all__ = [
     "TA_OK", "TreeParams", "QuantParams", "TreeAttentionError", "lib", "library_path",
     "tree_attn_tmp_bytes", "tree_attn_num_splits", "tree_attn_workspace_bytes", "tree_attn_fwd",
-    "tree_attn_fwd_causal", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
+    "tree_attn_fwd_causal", "tree_attn_fwd_parents", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
     "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "ta_set_quant_path",
     "quant_sdpa_uses_tensor_cores", "tree_attention",
     "quant_sdpa", "tree_params", "quant_params", "tree_mask_build",
@@ -81,6 +81,8 @@ def _load() -> ctypes.CDLL:
     L.tree_attn_fwd.restype = ctypes.c_int
     L.tree_attn_fwd_causal.argtypes = [PT, u32, B, B, B, B, B, P]
     L.tree_attn_fwd_causal.restype = ctypes.c_int
+    L.tree_attn_fwd_parents.argtypes = [PT, B, B, B, B, B, B, P]
+    L.tree_attn_fwd_parents.restype = ctypes.c_int
     L.tree_attn_reduce.argtypes = [PT, B, B, P]
     L.tree_attn_reduce.restype = ctypes.c_int
     L.tree_attn_fwd_noalloc.argtypes = [PT, B, B, B, B, B, P]
@@ -195,6 +197,11 @@ def tree_attn_fwd(p: TreeParams, q, k, v, mask, tmp, out, stream=None):
                              buf(out), _stream(stream)))
 
 
+def tree_attn_fwd_parents(p: TreeParams, parents, q, k, v, tmp, out, stream=None):
+    _check(lib.tree_attn_fwd_parents(ctypes.byref(p), buf(parents, TA_I32), buf(q), buf(k), buf(v), buf(tmp),
+                                     buf(out), _stream(stream)))
+
+
 def tree_attn_fwd_causal(p: TreeParams, window_start: int, q, k, v, tmp, out, stream=None):
     _check(lib.tree_attn_fwd_causal(ctypes.byref(p), window_start, buf(q), buf(k), buf(v),
                                     buf(tmp), buf(out), _stream(stream)))
@@ -232,9 +239,11 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
                    *, n_heads: int, n_kv_heads: int, kv_seq_len: int, scale: float,
                    mask_stride: Optional[int] = None, nwg: int = 0, window_start: int = 0,
                    tmp: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-                   stream=None) -> torch.Tensor:
+                   parents: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
     """One verify step (main pass + reduce) on device tensors.  mask=None uses the
-    implicit causal mask starting at window_start.  Returns out [q_l, n_heads, D]."""
+    implicit causal mask starting at window_start, or, with `parents` (int32
+    [q_l] on the device), the tree mask of that parent array.  Returns out
+    [q_l, n_heads, D]."""
     H, L, D = q.shape
     C = k.shape[1]
     stride = mask_stride if mask_stride is not None else (mask.shape[1] if mask is not None else kv_seq_len)
@@ -246,7 +255,11 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
         tmp = torch.empty((ws + 3) // 4, dtype=torch.float32, device=q.device)
     if out is None:
         out = torch.empty((L, n_heads, D), dtype=torch.float32, device=q.device)
-    if mask is None:
+    if parents is not None:
+        if mask is not None:
+            raise ValueError("give either a dense mask or a parent array, not both")
+        tree_attn_fwd_parents(p, parents, q, k, v, tmp, out, stream)
+    elif mask is None:
         tree_attn_fwd_causal(p, window_start, q, k, v, tmp, out, stream)
     else:
         tree_attn_fwd(p, q, k, v, mask, tmp, out, stream)

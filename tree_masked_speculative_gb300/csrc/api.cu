@@ -164,7 +164,10 @@ bool tree_workspace(const ta_tree_params *p, uint32_t nwg, TreeWorkspace *ws) {
     const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
     ws->off_cls = align256(po + pml);
     ws->off_q16 = align256(ws->off_cls + n_chunks);
-    ws->off_err = align256(ws->off_q16 + q16);
+    // ancestor bitsets of a parent-array tree mask (trees of up to kMaxTreeBitsNodes nodes)
+    const uint64_t anc = p->q_l <= (uint32_t)kMaxTreeBitsNodes ? (uint64_t)p->q_l * ((p->q_l + 31u) / 32u) * 4u : 0u;
+    ws->off_anc = align256(ws->off_q16 + q16);
+    ws->off_err = align256(ws->off_anc + anc);
     ws->total = ws->off_err + 256;
     return ws->total >= ws->off_q16;
 }
@@ -204,6 +207,7 @@ struct TreePlan {
     int kv_type;
     bool use_tc;
     void *k, *v;
+    const int32_t *parents;   // tree mask as a parent array (ancestor bitsets built first), or nullptr
 };
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -234,8 +238,17 @@ bool encode_map(CUtensorMap *m, bool bf16, void *ptr, int rank, const cuuint64_t
 
 ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, const ta_buf *v,
                     const ta_buf *mask, const ta_buf *tmp, const ta_buf *out, int window_start,
-                    TreePlan *plan) {
+                    TreePlan *plan, const ta_buf *parents = nullptr) {
     TA_TRY(check_tree_params(p, mask != nullptr));
+    if (parents) {
+        TA_TRY(check_dtype(*parents, "parents", TA_I32));
+        if (p->q_l > p->kv_seq_len)
+            return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: q_l (%u) must be <= kv_seq_len (%u)", p->q_l,
+                        p->kv_seq_len);
+        if (p->q_l > (uint32_t)kMaxTreeBitsNodes)
+            return fail(TA_ERR_UNSUPPORTED, "tree_attention: a parent-array mask takes q_l <= %d (got %u); "
+                        "build a dense mask with tree_mask_build instead", kMaxTreeBitsNodes, p->q_l);
+    }
     // dtype contract (tree_attention.rs validate_buffers; bf16 K/V added)
     TA_TRY(check_dtype(*q, "q", TA_F32));
     if (k->dtype != v->dtype)
@@ -265,6 +278,7 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     TA_TRY(check_buf(*k, "tree_attention: k", req_kv, 16));
     TA_TRY(check_buf(*v, "tree_attention: v", req_kv, 16));
     if (mask) TA_TRY(check_buf(*mask, "tree_attention: tree_mask", req_mask, 4));
+    if (parents) TA_TRY(check_buf(*parents, "tree_attention: parents", (uint64_t)p->q_l * 4u, 4));
     TA_TRY(check_buf(*out, "tree_attention: output", req_q, 16));
     TA_TRY(check_buf(*tmp, "tree_attention: tmp", ws.total, 16));
 
@@ -275,6 +289,11 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     a.v = v->ptr;
     a.mask = mask ? static_cast<const float *>(mask->ptr) : nullptr;
     char *t = static_cast<char *>(tmp->ptr);
+    plan->parents = parents ? static_cast<const int32_t *>(parents->ptr) : nullptr;
+    if (parents) {
+        a.anc = reinterpret_cast<const uint32_t *>(t + ws.off_anc);
+        a.anc_words = (int)((p->q_l + 31u) / 32u);
+    }
     a.part_o = reinterpret_cast<float *>(t + ws.off_part_o);
     a.part_ml = reinterpret_cast<float *>(t + ws.off_part_ml);
     a.cls = reinterpret_cast<uint8_t *>(t + ws.off_cls);
@@ -331,7 +350,12 @@ ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
             !encode_map(&maps.v, bf16, plan.v, 3, kdims, kstr, kbox))
             return fail(TA_ERR_CUDA, "tree_attention: TMA descriptor encoding failed");
     }
-    cudaError_t e = launch_tree_classify(plan.a, s);
+    cudaError_t e = cudaSuccess;
+    if (plan.parents) {
+        e = launch_tree_anc(plan.a, plan.parents, s);
+        if (e != cudaSuccess) return cuda_fail(e, "tree_attention: ancestor bitset launch");
+    }
+    e = launch_tree_classify(plan.a, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: chunk classification launch");
     e = plan.use_tc ? launch_tree_tc(plan.a, maps, plan.kv_type, s) : launch_tree_fma(plan.a, plan.kv_type, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: main pass launch");
@@ -554,6 +578,15 @@ TA_EXPORT ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t windo
     TreePlan plan;
     TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out),
                      (int)window_start, &plan));
+    return run_tree(plan, static_cast<cudaStream_t>(stream));
+}
+
+TA_EXPORT ta_status tree_attn_fwd_parents(const ta_tree_params *p, const ta_buf *parents, const ta_buf *q,
+                                          const ta_buf *k, const ta_buf *v, const ta_buf *tmp, const ta_buf *out,
+                                          void *stream) {
+    TreePlan plan;
+    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out), 0, &plan,
+                     &deref(parents)));
     return run_tree(plan, static_cast<cudaStream_t>(stream));
 }
 

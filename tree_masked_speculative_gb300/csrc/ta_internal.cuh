@@ -19,6 +19,10 @@ constexpr float kMInit = -FLT_MAX / 2;
 // Chunk classes written by the mask-compaction pass, one byte per 32 keys.
 enum ChunkClass : uint8_t { kChunkDead = 0, kChunkAllAttended = 1, kChunkMixed = 2 };
 
+// Largest draft tree (q_l) whose mask may be given as a parent array: its
+// per-row ancestor bitsets ((q_l + 31) / 32 words a row) live in the workspace.
+constexpr int kMaxTreeBitsNodes = 256;
+
 enum KvType : int { kKvF32 = 0, kKvF16 = 1, kKvBF16 = 2 };
 
 // ------------------------------------------------------------ device helpers
@@ -82,7 +86,9 @@ struct TreeArgs {
     const float *q;        // [H, L, D] f32
     const void *k;         // [Hk, C, D] KV_T
     const void *v;
-    const float *mask;     // [L, stride] f32; nullptr -> implicit causal
+    const float *mask;     // [L, stride] f32; nullptr (and no anc) -> implicit causal
+    const uint32_t *anc;   // [L][anc_words] ancestor bitsets of a parent array, or nullptr
+    int anc_words;         // (L + 31) / 32
     uint8_t *cls;          // [n_chunks] chunk classes
     float *part_o;         // [nwg][nrows][D]
     float *part_ml;        // [nwg][nrows][2] = (S, M)
@@ -95,6 +101,19 @@ struct TreeArgs {
     int cluster_x;         // tensor-core kernel: splits merged inside one cluster
     float scale;
 };
+
+// Cell (query row qi, key < N) of an explicit tree mask: the dense mask row
+// `mrow`, or, when the mask came as a parent array, 0 on the prefix
+// [0, N - L) and at the tree positions N - L + a for a in qi's ancestor
+// bitset (itself included), -65504 elsewhere - the cells tree_mask_build
+// writes for the same parents.
+__device__ __forceinline__ float explicit_cell(const TreeArgs &a, const float *mrow, int qi, int key) {
+    if (a.anc == nullptr) return __ldg(mrow + key);
+    const int rel = key - (a.N - a.L);
+    if (rel < 0) return 0.0f;
+    const uint32_t w = __ldg(a.anc + static_cast<size_t>(qi) * a.anc_words + (rel >> 5));
+    return ((w >> (rel & 31)) & 1u) ? 0.0f : kMasked;
+}
 
 // TMA descriptors of the tensor-core tree kernel (kernel parameters).
 struct TcMaps {
@@ -252,7 +271,7 @@ __host__ __device__ inline int quant_chunk_tokens(int dim, int bits) {
 
 // Workspace layout inside the caller's tmp buffer (all offsets 256-aligned).
 struct TreeWorkspace {
-    size_t off_part_o, off_part_ml, off_cls, off_q16, off_err, total;
+    size_t off_part_o, off_part_ml, off_cls, off_q16, off_anc, off_err, total;
 };
 
 // ------------------------------------------------------------ host launches
@@ -264,6 +283,8 @@ cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, c
 // row tiles and O halves that share K/V through multicast.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
+// Ancestor bitsets a.anc of the parent array `parents` [a.L] (device pointer).
+cudaError_t launch_tree_anc(const TreeArgs &a, const int32_t *parents, cudaStream_t s);
 // Dense tree mask [q_l, stride] f32 from parents [q_l] (device pointers).
 cudaError_t launch_tree_mask(const int32_t *parents, int q_l, int kv_seq_len, int stride, float *mask,
                              cudaStream_t s);

@@ -64,6 +64,13 @@ __device__ __forceinline__ void prep_body(const TreeArgs &a, int n_cls_blocks) {
                 any_att |= m > kMasked;
                 all_zero &= m == 0.0f;
             }
+        } else if (a.anc != nullptr) {
+            // tree mask of a parent array: the same cells, from the bitsets
+            for (int i = warp; i < a.L; i += kPrepThreads / 32) {
+                const float m = explicit_cell(a, nullptr, i, key);
+                any_att |= m > kMasked;
+                all_zero &= m == 0.0f;
+            }
         } else {
             // implicit causal: row i attends [window_start, N - L + i]
             const int last = a.N - a.L;            // row 0's last attended key
@@ -93,6 +100,49 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs 
     pdl_launch_dependents();
     pdl_wait();
     prep_body(a, n_cls_blocks);
+}
+
+// Ancestor bitsets of a parent array, one launch of one CTA before the prep
+// pass (q_l <= kMaxTreeBitsNodes): thread i walks node i's chain i,
+// parents[i], ... in shared memory - a value outside [0, current node) ends
+// it, the rule of the dense mask builder - and writes row i's words.
+constexpr int kAncThreads = kMaxTreeBitsNodes;
+static_assert(kMaxTreeBitsNodes % 32 == 0, "whole bitset words per row");
+
+__global__ void __launch_bounds__(kAncThreads) tree_anc_kernel(const TreeArgs a, const int32_t *parents) {
+    pdl_launch_dependents();
+    pdl_wait();   // parents may come from the kernel before; the previous call's passes are done
+    __shared__ int32_t s_par[kMaxTreeBitsNodes];
+    const int L = a.L, i = threadIdx.x;
+    if (i < L) s_par[i] = __ldg(parents + i);
+    __syncthreads();
+    if (i >= L) return;
+    uint32_t w[kMaxTreeBitsNodes / 32];
+#pragma unroll
+    for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k) w[k] = 0u;
+    auto set = [&](int n) {
+#pragma unroll
+        for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k)
+            if (k == (n >> 5)) w[k] |= 1u << (n & 31);
+    };
+    set(i);
+    for (int node = i;;) {   // at most i steps: each step goes to a smaller node
+        const int up = s_par[node];
+        if (up < 0 || up >= node) break;
+        set(up);
+        node = up;
+    }
+    uint32_t *row = const_cast<uint32_t *>(a.anc) + static_cast<size_t>(i) * a.anc_words;
+#pragma unroll
+    for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k)
+        if (k < a.anc_words) row[k] = w[k];
+}
+
+cudaError_t launch_tree_anc(const TreeArgs &a, const int32_t *parents, cudaStream_t s) {
+    cudaError_t e = launch_pdl(tree_anc_kernel, dim3(1), dim3(kAncThreads), 0, s, a, parents);
+    count_launch();
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
 }
 
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {

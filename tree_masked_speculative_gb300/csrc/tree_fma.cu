@@ -171,8 +171,10 @@ __global__ void __launch_bounds__(kThreads) tree_fma_kernel(const TreeArgs a) {
                 } else if (IMPLICIT) {
                     mv = (key >= a.window_start && key <= last0 + row_i[rr]) ? 0.0f : kMasked;
                 } else {
-                    mv = (ccls == kChunkAllAttended) ? 0.0f
-                                                     : __ldg(a.mask + (size_t)row_i[rr] * a.stride + key);
+                    mv = (ccls == kChunkAllAttended)
+                             ? 0.0f
+                             : explicit_cell(a, a.mask == nullptr ? nullptr : a.mask + (size_t)row_i[rr] * a.stride,
+                                             row_i[rr], key);
                 }
                 if (!__any_sync(0xffffffffu, mv > kMasked)) continue;   // chunk dead for this row
                 const float s = fmaf(acc[rr], a.scale, mv);
@@ -234,7 +236,7 @@ cudaError_t launch_one(const TreeArgs &a, cudaStream_t s) {
 
 template <typename KV_T>
 cudaError_t launch_typed(const TreeArgs &a, cudaStream_t s) {
-    const bool imp = a.mask == nullptr;
+    const bool imp = a.mask == nullptr && a.anc == nullptr;
     switch (a.D) {
         case 128: return imp ? launch_one<128, KV_T, true>(a, s) : launch_one<128, KV_T, false>(a, s);
         case 256: return imp ? launch_one<256, KV_T, true>(a, s) : launch_one<256, KV_T, false>(a, s);

@@ -181,25 +181,29 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x;
-    const int n_os = D / DV;
-    const int rt = blockIdx.y / n_os, os = blockIdx.y % n_os;
-    const int kh = blockIdx.z;
     const int n_rt = (a.R + 127) / 128;
+    const int os = blockIdx.y / n_rt, rt = blockIdx.y % n_rt;   // y = O half * row tiles + row tile
+    const int kh = blockIdx.z;
     const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
     const int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
-    // Cluster (cx x cy): along y, the row tiles and O halves of one (split, KV
-    // head) - each K slab is loaded once for them and each V slab once per O
-    // half, the shares multicast, so every K/V byte crosses L2 -> SM once;
-    // along x, consecutive splits whose partials are merged in the cluster.
+    // Cluster (cx x cy): along y, CTAs of one (split, KV head): 1, the row
+    // tiles of one O half (cy = n_rt), or the row tiles of both halves.  Each
+    // K slab is loaded once for the cluster and each V slab once for the row
+    // tiles of an O half, the shares multicast; along x, consecutive splits
+    // whose partials are merged in the cluster.
     const int cx = static_cast<int>(cluster_nctaid_x()), cy = static_cast<int>(cluster_nctaid_y());
     const int cxi = static_cast<int>(cluster_ctaid_x()), cyi = static_cast<int>(cluster_ctaid_y());
-    const int k_share = cy, k_idx = cyi;                            // K: every y of this split
-    const int v_share = cy > 1 ? n_rt : 1, v_idx = cy > 1 ? rt : 0;  // V: the y of this O half
+    const int k_share = cy, k_idx = cyi;                            // K: every y of the cluster
+    const bool v_shared = n_rt > 1 && cy >= n_rt;                   // V: the row tiles of this O half
+    const int v_share = v_shared ? n_rt : 1, v_idx = v_shared ? rt : 0;
     uint16_t k_mask = 0, v_mask = 0;
     for (int y2 = 0; y2 < cy; ++y2) k_mask |= static_cast<uint16_t>(1u << (cxi + cx * y2));
-    if (cy > 1)
-        for (int r2 = 0; r2 < n_rt; ++r2) v_mask |= static_cast<uint16_t>(1u << (cxi + cx * (r2 * n_os + os)));
+    if (v_shared) {
+        const int y0 = static_cast<int>(blockIdx.y) - cyi;          // first y of the cluster
+        for (int r2 = 0; r2 < n_rt; ++r2)
+            v_mask |= static_cast<uint16_t>(1u << (cxi + cx * (os * n_rt + r2 - y0)));
+    }
 
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cy); }
@@ -373,7 +377,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int hj = kh * a.g + (rg / a.L);           // query head
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int last0 = a.N - a.L;
-        const float *mrow = IMPLICIT ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
+        const float *mrow = (IMPLICIT || a.mask == nullptr) ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
         constexpr int DVH = DV / 2;                     // O columns of this warp
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
 
@@ -402,7 +406,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 if (mixed >= 0) {
                     const int key0 = (mixed ? ch1 : ch0) * 32;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) mpre[e] = key0 + e < a.N ? __ldg(mrow + key0 + e) : kMasked;
+                    for (int e = 0; e < 32; ++e)
+                        mpre[e] = key0 + e < a.N ? explicit_cell(a, mrow, qi, key0 + e) : kMasked;
                 }
             }
             const int sb = t & 1;
@@ -442,7 +447,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         if (IMPLICIT) x = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
                         else if (ccl == kChunkAllAttended) x = key < a.N ? 0.0f : kMasked;
                         else if (cc == mixed) x = mpre[e];
-                        else x = key < a.N ? __ldg(mrow + key) : kMasked;
+                        else x = key < a.N ? explicit_cell(a, mrow, qi, key) : kMasked;
                         mv[e] = x;
                         live |= x > kMasked;
                     }
@@ -731,7 +736,11 @@ void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     };
     *cx = 1;
     *cy = 1;
-    const int y_choices[2] = {gy, 1};
+    // With two O halves the cluster holds the row tiles of one half: K slabs
+    // are then shared by n_rt CTAs rather than by all of them, so a ring slot
+    // waits on fewer consumers (the other half reads K again from L2).
+    const int y_pref = (gy > n_rt && n_rt > 1) ? n_rt : gy;
+    const int y_choices[2] = {y_pref, 1};
     for (int yc : y_choices) {
         if (yc > 8 || (yc & (yc - 1)) != 0 || !fits(yc)) continue;
         *cy = yc;
@@ -762,7 +771,7 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
 
 template <bool BF16>
 cudaError_t launch_tc_typed(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
-    const bool imp = a.mask == nullptr;
+    const bool imp = a.mask == nullptr && a.anc == nullptr;
     switch (a.D) {
         case 128: return imp ? launch_tc_one<128, BF16, true>(a, maps, s) : launch_tc_one<128, BF16, false>(a, maps, s);
         case 256: return imp ? launch_tc_one<256, BF16, true>(a, maps, s) : launch_tc_one<256, BF16, false>(a, maps, s);
