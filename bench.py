@@ -55,6 +55,9 @@ def parse():
     ap.add_argument("--quant-path", type=int, default=0, choices=[0, 1, 2],
                     help="quantized workloads: 0 automatic, 1 CUDA-core kernel, 2 tensor-core kernel "
                          "where the shape allows it")
+    ap.add_argument("--tree-mask", default="dense", choices=["dense", "parents"],
+                    help="tree workloads: the mask as the dense f32 array (tree_attn_fwd) or as the "
+                         "parent array (tree_attn_fwd_parents)")
     ap.add_argument("--kv-sets", type=int, default=0,
                     help="K/V copies to rotate over (0 = enough to exceed 3x L2)")
     return ap.parse_args()
@@ -179,7 +182,7 @@ class ClockSampler:
 
 # ------------------------------------------------------------- tree arm
 class TreeBench:
-    def __init__(self, ta, wl: W.TreeWorkload, dev, kv_sets=0):
+    def __init__(self, ta, wl: W.TreeWorkload, dev, kv_sets=0, tree_mask="dense"):
         self.ta, self.wl, self.dev = ta, wl, dev
         inp = W.make_tree_inputs(wl)
         self.host = inp
@@ -199,8 +202,10 @@ class TreeBench:
         self.bytes_per_step = wl.kv_bytes
         self.name = wl.name
         self.dtype = wl.kv_dtype
-        self.fwd_label = "mask compaction + main pass (tree_attn_fwd)"
         self.parents = torch.tensor(inp["parents"], dtype=torch.int32, device=dev) if "parents" in inp else None
+        self.use_parents = tree_mask == "parents"
+        self.fwd_label = ("ancestor bitsets + mask compaction + main pass (tree_attn_fwd_parents)"
+                          if self.use_parents else "mask compaction + main pass (tree_attn_fwd)")
         self.built_mask = None
 
     def mask_step(self, i):
@@ -211,7 +216,10 @@ class TreeBench:
 
     def step(self, i, fwd_only=False):
         s = i % self.nsets
-        self.ta.tree_attn_fwd(self.p, self.q, self.ks[s], self.vs[s], self.mask, self.tmp, self.out)
+        if self.use_parents:
+            self.ta.tree_attn_fwd_parents(self.p, self.parents, self.q, self.ks[s], self.vs[s], self.tmp, self.out)
+        else:
+            self.ta.tree_attn_fwd(self.p, self.q, self.ks[s], self.vs[s], self.mask, self.tmp, self.out)
         if not fwd_only:
             self.ta.tree_attn_reduce(self.p, self.tmp, self.out)
 
@@ -220,6 +228,7 @@ class TreeBench:
         return {"workload": wl.name, "n_heads": wl.n_heads, "n_kv_heads": wl.n_kv_heads,
                 "head_dim": wl.head_dim, "kv_seq_len": wl.kv_seq_len, "kv_capacity": wl.kv_capacity,
                 "q_l": wl.q_l, "kv_dtype": wl.kv_dtype, "splits": self.nwg,
+                "tree_mask": "parent array" if self.use_parents else "dense f32",
                 "l2": "rotating %d K/V sets, %.0f MB read per rotation (> 3x L2)" % (
                     self.nsets, self.nsets * self.bytes_per_step / 1e6)}
 
@@ -228,7 +237,8 @@ class TreeBench:
         wl = self.wl
         N = wl.kv_seq_len
         self.h_q = self.host["q"].pin_memory()
-        self.h_mask = self.host["mask"].pin_memory()
+        self.h_mask = (torch.tensor(self.host["parents"], dtype=torch.int32) if self.use_parents
+                       else self.host["mask"]).pin_memory()
         self.h_k = self.host["k"][:, :N].contiguous().pin_memory()
         self.h_v = self.host["v"][:, :N].contiguous().pin_memory()
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
@@ -239,7 +249,7 @@ class TreeBench:
         N = self.wl.kv_seq_len
         s = i % self.nsets
         self.q.copy_(self.h_q, non_blocking=True)
-        self.mask.copy_(self.h_mask, non_blocking=True)
+        (self.parents if self.use_parents else self.mask).copy_(self.h_mask, non_blocking=True)
         for h in range(self.wl.n_kv_heads):   # contiguous [N, D] runs, one copy each
             self.ks[s][h, :N].copy_(self.h_k[h], non_blocking=True)
             self.vs[s][h, :N].copy_(self.h_v[h], non_blocking=True)
@@ -335,10 +345,11 @@ class QuantBench:
         return list(range(self.wl.rows))
 
 
-def make_bench(ta, name, dev, kv_sets=0):
+def make_bench(ta, name, dev, kv_sets=0, tree_mask="dense"):
     wl = WORKLOADS[name]
-    cls = TreeBench if isinstance(wl, W.TreeWorkload) else QuantBench
-    return cls(ta, wl, dev, kv_sets)
+    if isinstance(wl, W.TreeWorkload):
+        return TreeBench(ta, wl, dev, kv_sets, tree_mask)
+    return QuantBench(ta, wl, dev, kv_sets)
 
 
 # ------------------------------------------------------------ timing
@@ -412,7 +423,7 @@ def run_ours(args):
     import tree_masked_speculative_gb300 as ta
 
     ta.ta_set_quant_path(args.quant_path)
-    bench = make_bench(ta, args.workload, dev, args.kv_sets)
+    bench = make_bench(ta, args.workload, dev, args.kv_sets, args.tree_mask)
     if args.profile:
         for i in range(max(1, args.warmup)):
             bench.step(i)

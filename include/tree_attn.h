@@ -170,8 +170,8 @@ ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, c
  * and attends the prefix [0, kv_seq_len - q_l), its ancestors and itself).
  * The result is bit-identical to tree_attn_fwd given the mask
  * tree_mask_build writes for the same parents; no dense mask
- * is read or written (a per-row ancestor bitset of (q_l + 31) / 32 words is
- * built in `tmp` by one extra launch).
+ * is read or written (the mask-compaction pass builds a per-row ancestor
+ * bitset of (q_l + 31) / 32 words in `tmp`; no extra launch).
  *   parents  [q_l] i32 on the device, the rule of tree_mask_build: a chain
  *            i, parents[i], ... ends at a value outside [0, current node).
  *   q, k, v, tmp, out  as for tree_attn_fwd; p->mask_stride is not used.

@@ -207,7 +207,6 @@ struct TreePlan {
     int kv_type;
     bool use_tc;
     void *k, *v;
-    const int32_t *parents;   // tree mask as a parent array (ancestor bitsets built first), or nullptr
 };
 
 // cuTensorMapEncodeTiled from the driver, looked up once.
@@ -289,8 +288,8 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     a.v = v->ptr;
     a.mask = mask ? static_cast<const float *>(mask->ptr) : nullptr;
     char *t = static_cast<char *>(tmp->ptr);
-    plan->parents = parents ? static_cast<const int32_t *>(parents->ptr) : nullptr;
     if (parents) {
+        a.parents = static_cast<const int32_t *>(parents->ptr);
         a.anc = reinterpret_cast<const uint32_t *>(t + ws.off_anc);
         a.anc_words = (int)((p->q_l + 31u) / 32u);
     }
@@ -350,12 +349,7 @@ ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
             !encode_map(&maps.v, bf16, plan.v, 3, kdims, kstr, kbox))
             return fail(TA_ERR_CUDA, "tree_attention: TMA descriptor encoding failed");
     }
-    cudaError_t e = cudaSuccess;
-    if (plan.parents) {
-        e = launch_tree_anc(plan.a, plan.parents, s);
-        if (e != cudaSuccess) return cuda_fail(e, "tree_attention: ancestor bitset launch");
-    }
-    e = launch_tree_classify(plan.a, s);
+    cudaError_t e = launch_tree_classify(plan.a, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: chunk classification launch");
     e = plan.use_tc ? launch_tree_tc(plan.a, maps, plan.kv_type, s) : launch_tree_fma(plan.a, plan.kv_type, s);
     if (e != cudaSuccess) return cuda_fail(e, "tree_attention: main pass launch");

@@ -87,7 +87,9 @@ struct TreeArgs {
     const void *k;         // [Hk, C, D] KV_T
     const void *v;
     const float *mask;     // [L, stride] f32; nullptr (and no anc) -> implicit causal
-    const uint32_t *anc;   // [L][anc_words] ancestor bitsets of a parent array, or nullptr
+    const uint32_t *anc;   // [L][anc_words] ancestor bitsets of a parent array (written by
+                           // the prep pass), or nullptr
+    const int32_t *parents;  // [L] the parent array (device), with anc
     int anc_words;         // (L + 31) / 32
     uint8_t *cls;          // [n_chunks] chunk classes
     float *part_o;         // [nwg][nrows][D]
@@ -113,6 +115,29 @@ __device__ __forceinline__ float explicit_cell(const TreeArgs &a, const float *m
     if (rel < 0) return 0.0f;
     const uint32_t w = __ldg(a.anc + static_cast<size_t>(qi) * a.anc_words + (rel >> 5));
     return ((w >> (rel & 31)) & 1u) ? 0.0f : kMasked;
+}
+
+// The 32 explicit-mask cells of row qi for keys key0 .. key0 + 31 (masked at
+// keys >= N), the mask's kind decided once for the chunk.
+__device__ __forceinline__ void explicit_chunk(const TreeArgs &a, const float *mrow, int qi, int key0,
+                                               float (&x)[32]) {
+    if (a.anc == nullptr) {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) x[e] = key0 + e < a.N ? __ldg(mrow + key0 + e) : kMasked;
+    } else {
+        // the chunk's tree positions span at most two bitset words of the row
+        const int rel0 = key0 - (a.N - a.L);
+        const uint32_t *row = a.anc + static_cast<size_t>(qi) * a.anc_words;
+        const int w0 = rel0 >> 5;   // arithmetic shift: -1 for a chunk that starts in the prefix
+        const uint32_t lo = w0 >= 0 && w0 < a.anc_words ? __ldg(row + w0) : 0u;
+        const uint32_t hi = w0 + 1 >= 0 && w0 + 1 < a.anc_words ? __ldg(row + w0 + 1) : 0u;
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+            const int rel = rel0 + e;
+            const uint32_t w = (rel >> 5) == w0 ? lo : hi;
+            x[e] = key0 + e >= a.N ? kMasked : (rel < 0 ? 0.0f : (((w >> (rel & 31)) & 1u) ? 0.0f : kMasked));
+        }
+    }
 }
 
 // TMA descriptors of the tensor-core tree kernel (kernel parameters).
@@ -283,8 +308,6 @@ cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, c
 // row tiles and O halves that share K/V through multicast.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
-// Ancestor bitsets a.anc of the parent array `parents` [a.L] (device pointer).
-cudaError_t launch_tree_anc(const TreeArgs &a, const int32_t *parents, cudaStream_t s);
 // Dense tree mask [q_l, stride] f32 from parents [q_l] (device pointers).
 cudaError_t launch_tree_mask(const int32_t *parents, int q_l, int kv_seq_len, int stride, float *mask,
                              cudaStream_t s);

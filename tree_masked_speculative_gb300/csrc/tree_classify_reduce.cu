@@ -22,6 +22,63 @@ namespace ta {
 constexpr int kPrepThreads = 256;
 constexpr int kQ16PerBlock = kPrepThreads * 8;
 
+// Classification of one chunk for a tree mask given as a parent array (and,
+// by the last chunk's block, the per-row ancestor bitsets the main pass
+// reads).  The cells are those of the dense builder: row i attends the prefix
+// [0, N - L) and the tree positions N - L + a of itself and its ancestors.  A
+// chunk wholly in the prefix is all-attended; a chunk over tree positions
+// first builds every row's bitset in shared memory - thread i walks node i's
+// chain i, parents[i], ..., which a value outside [0, current node) ends -
+// and classifies from it.
+static_assert(kPrepThreads >= kMaxTreeBitsNodes, "one thread per tree node");
+
+__device__ __forceinline__ void classify_parents(const TreeArgs &a, int chunk) {
+    __shared__ int32_t s_par[kMaxTreeBitsNodes];
+    __shared__ uint32_t s_bits[kMaxTreeBitsNodes * (kMaxTreeBitsNodes / 32)];
+    __shared__ int s_any[kPrepThreads / 32], s_all[kPrepThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int prefix = a.N - a.L, W = a.anc_words;
+    if (chunk * 32 + 32 <= prefix) {
+        if (t == 0) a.cls[chunk] = kChunkAllAttended;
+        return;
+    }
+    if (t < a.L) s_par[t] = __ldg(a.parents + t);
+    __syncthreads();
+    if (t < a.L) {
+        uint32_t *row = s_bits + t * W;
+        for (int k = 0; k < W; ++k) row[k] = 0u;
+        row[t >> 5] |= 1u << (t & 31);
+        for (int node = t;;) {                     // at most t steps: each goes to a smaller node
+            const int up = s_par[node];
+            if (up < 0 || up >= node) break;
+            row[up >> 5] |= 1u << (up & 31);
+            node = up;
+        }
+    }
+    __syncthreads();
+    if (chunk == a.n_chunks - 1)                    // one block publishes the bitsets
+        for (int k = t; k < a.L * W; k += kPrepThreads) const_cast<uint32_t *>(a.anc)[k] = s_bits[k];
+    const int key = chunk * 32 + lane;
+    bool any_att = false, all_zero = true;
+    if (key < a.N) {
+        const int rel = key - prefix;
+        for (int i = warp; i < a.L; i += kPrepThreads / 32) {
+            const bool att = rel < 0 || ((s_bits[i * W + (rel >> 5)] >> (rel & 31)) & 1u);
+            any_att |= att;
+            all_zero &= att;
+        }
+    }
+    any_att = __any_sync(0xffffffffu, any_att);
+    all_zero = __all_sync(0xffffffffu, all_zero);
+    if (lane == 0) { s_any[warp] = any_att; s_all[warp] = all_zero; }
+    __syncthreads();
+    if (t == 0) {
+        bool an = false, al = true;
+        for (int w = 0; w < kPrepThreads / 32; ++w) { an |= s_any[w] != 0; al &= s_all[w] != 0; }
+        a.cls[chunk] = !an ? kChunkDead : (al ? kChunkAllAttended : kChunkMixed);
+    }
+}
+
 __device__ __forceinline__ void prep_body(const TreeArgs &a, int n_cls_blocks) {
     if (blockIdx.x == 0 && threadIdx.x == 0 && a.err != nullptr) {
         a.err[0] = 0;          // error word
@@ -49,6 +106,10 @@ __device__ __forceinline__ void prep_body(const TreeArgs &a, int n_cls_blocks) {
         *reinterpret_cast<uint4 *>(static_cast<uint16_t *>(a.q16) + i8) = o;
         return;
     }
+    if (a.anc != nullptr) {
+        classify_parents(a, static_cast<int>(blockIdx.x));
+        return;
+    }
     __shared__ int s_any[kPrepThreads / 32], s_all[kPrepThreads / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int chunk = blockIdx.x;
@@ -61,13 +122,6 @@ __device__ __forceinline__ void prep_body(const TreeArgs &a, int n_cls_blocks) {
 #pragma unroll 4
             for (int i = warp; i < a.L; i += kPrepThreads / 32) {
                 const float m = __ldg(col + static_cast<size_t>(i) * a.stride);
-                any_att |= m > kMasked;
-                all_zero &= m == 0.0f;
-            }
-        } else if (a.anc != nullptr) {
-            // tree mask of a parent array: the same cells, from the bitsets
-            for (int i = warp; i < a.L; i += kPrepThreads / 32) {
-                const float m = explicit_cell(a, nullptr, i, key);
                 any_att |= m > kMasked;
                 all_zero &= m == 0.0f;
             }
@@ -102,49 +156,6 @@ __global__ void __launch_bounds__(kPrepThreads) tree_prep_kernel(const TreeArgs 
     prep_body(a, n_cls_blocks);
 }
 
-// Ancestor bitsets of a parent array, one launch of one CTA before the prep
-// pass (q_l <= kMaxTreeBitsNodes): thread i walks node i's chain i,
-// parents[i], ... in shared memory - a value outside [0, current node) ends
-// it, the rule of the dense mask builder - and writes row i's words.
-constexpr int kAncThreads = kMaxTreeBitsNodes;
-static_assert(kMaxTreeBitsNodes % 32 == 0, "whole bitset words per row");
-
-__global__ void __launch_bounds__(kAncThreads) tree_anc_kernel(const TreeArgs a, const int32_t *parents) {
-    pdl_launch_dependents();
-    pdl_wait();   // parents may come from the kernel before; the previous call's passes are done
-    __shared__ int32_t s_par[kMaxTreeBitsNodes];
-    const int L = a.L, i = threadIdx.x;
-    if (i < L) s_par[i] = __ldg(parents + i);
-    __syncthreads();
-    if (i >= L) return;
-    uint32_t w[kMaxTreeBitsNodes / 32];
-#pragma unroll
-    for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k) w[k] = 0u;
-    auto set = [&](int n) {
-#pragma unroll
-        for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k)
-            if (k == (n >> 5)) w[k] |= 1u << (n & 31);
-    };
-    set(i);
-    for (int node = i;;) {   // at most i steps: each step goes to a smaller node
-        const int up = s_par[node];
-        if (up < 0 || up >= node) break;
-        set(up);
-        node = up;
-    }
-    uint32_t *row = const_cast<uint32_t *>(a.anc) + static_cast<size_t>(i) * a.anc_words;
-#pragma unroll
-    for (int k = 0; k < kMaxTreeBitsNodes / 32; ++k)
-        if (k < a.anc_words) row[k] = w[k];
-}
-
-cudaError_t launch_tree_anc(const TreeArgs &a, const int32_t *parents, cudaStream_t s) {
-    cudaError_t e = launch_pdl(tree_anc_kernel, dim3(1), dim3(kAncThreads), 0, s, a, parents);
-    count_launch();
-    if (e != cudaSuccess) return e;
-    return cudaGetLastError();
-}
-
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s) {
     const int n_cls = a.n_chunks;
     int n_q = 0;
@@ -171,8 +182,6 @@ __global__ void __launch_bounds__(kReduceThreads) tree_reduce_kernel(const TreeA
     // The next prep pass may start launching; it waits for this grid to finish
     // before it rewrites the workspace.
     pdl_launch_dependents();
-    const int nwg = a.err[1];
-    if (nwg <= 0) return;
     __shared__ float4 s_acc[kReduceThreads];
     __shared__ float2 s_ms[kReduceThreads];   // (m_g, s_g) per thread
     const int rid = blockIdx.x;
@@ -182,22 +191,42 @@ __global__ void __launch_bounds__(kReduceThreads) tree_reduce_kernel(const TreeA
     const int groups = kReduceThreads / D4;
     const int g = t / D4, i = t % D4;
     const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml) + rid;   // (S, M), stride nrows
+    const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * i;
+    const size_t po_stride = static_cast<size_t>(nrows) * a.D;
+    // The thread's first kPre slots (of the a.nwg the workspace holds) are
+    // loaded together with the slot count the main pass published, so the
+    // count costs no round trip of its own; slots past the count are ignored.
+    constexpr int kPre = 4;
+    float2 sm_pre[kPre];
+    float4 o_pre[kPre];
+#pragma unroll
+    for (int k = 0; k < kPre; ++k) {
+        const int w = g + k * groups;
+        if (g < groups && w < a.nwg) {
+            sm_pre[k] = __ldg(ml + static_cast<size_t>(w) * nrows);
+            o_pre[k] = __ldg(reinterpret_cast<const float4 *>(po + w * po_stride));
+        }
+    }
+    const int nwg = a.err[1];
+    if (nwg <= 0) return;
     float m = -FLT_MAX, ssum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    auto merge = [&](float2 sm, float4 o) {
+        const float mn = fmaxf(m, sm.y);
+        const float c = expf(m - mn), e = expf(sm.y - mn);
+        m = mn;
+        ssum = ssum * c + sm.x * e;
+        acc.x = acc.x * c + o.x * e; acc.y = acc.y * c + o.y * e;
+        acc.z = acc.z * c + o.z * e; acc.w = acc.w * c + o.w * e;
+    };
     if (g < groups) {
-        const float *po = a.part_o + static_cast<size_t>(rid) * a.D + 4 * i;
-        const size_t po_stride = static_cast<size_t>(nrows) * a.D;
+#pragma unroll
+        for (int k = 0; k < kPre; ++k)
+            if (g + k * groups < nwg) merge(sm_pre[k], o_pre[k]);
 #pragma unroll 4
-        for (int w = g; w < nwg; w += groups) {
-            const float2 sm = __ldg(ml + static_cast<size_t>(w) * nrows);
-            const float4 o = __ldg(reinterpret_cast<const float4 *>(po + w * po_stride));
-            const float mn = fmaxf(m, sm.y);
-            const float c = expf(m - mn), e = expf(sm.y - mn);
-            m = mn;
-            ssum = ssum * c + sm.x * e;
-            acc.x = acc.x * c + o.x * e; acc.y = acc.y * c + o.y * e;
-            acc.z = acc.z * c + o.z * e; acc.w = acc.w * c + o.w * e;
-        }
+        for (int w = g + kPre * groups; w < nwg; w += groups)
+            merge(__ldg(ml + static_cast<size_t>(w) * nrows),
+                  __ldg(reinterpret_cast<const float4 *>(po + w * po_stride)));
     }
     s_acc[t] = acc;
     s_ms[t] = make_float2(m, ssum);

@@ -403,12 +403,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             float mpre[32];
             if (!IMPLICIT) {
                 mixed = (ch0 >= 0 && cl0 == kChunkMixed) ? 0 : ((ch1 >= 0 && cl1 == kChunkMixed) ? 1 : -1);
-                if (mixed >= 0) {
-                    const int key0 = (mixed ? ch1 : ch0) * 32;
-#pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        mpre[e] = key0 + e < a.N ? explicit_cell(a, mrow, qi, key0 + e) : kMasked;
-                }
+                if (mixed >= 0) explicit_chunk(a, mrow, qi, (mixed ? ch1 : ch0) * 32, mpre);
             }
             const int sb = t & 1;
             ok = wait_all(&bars->s_full[sb], (static_cast<uint32_t>(t) >> 1) & 1u, 7);
@@ -439,18 +434,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(-INFINITY);
                 } else {
                     float mv[32];
+                    if (IMPLICIT) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) {
+                            const int key = key0 + e;
+                            mv[e] = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
+                        }
+                    } else if (ccl == kChunkAllAttended) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mv[e] = key0 + e < a.N ? 0.0f : kMasked;
+                    } else if (cc == mixed) {
+#pragma unroll
+                        for (int e = 0; e < 32; ++e) mv[e] = mpre[e];
+                    } else {
+                        explicit_chunk(a, mrow, qi, key0, mv);
+                    }
                     bool live = false;
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
-                        const int key = key0 + e;
-                        float x;
-                        if (IMPLICIT) x = (key < a.N && key >= a.window_start && key <= last0 + qi) ? 0.0f : kMasked;
-                        else if (ccl == kChunkAllAttended) x = key < a.N ? 0.0f : kMasked;
-                        else if (cc == mixed) x = mpre[e];
-                        else x = key < a.N ? explicit_cell(a, mrow, qi, key) : kMasked;
-                        mv[e] = x;
-                        live |= x > kMasked;
-                    }
+                    for (int e = 0; e < 32; ++e) live |= mv[e] > kMasked;
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         // logit = fma(qk, scale, mask) (the pages' form), in log2 units
