@@ -143,8 +143,10 @@ __device__ __forceinline__ void explicit_chunk(const TreeArgs &a, const float *m
 // TMA descriptors of the tensor-core tree kernel (kernel parameters).
 struct TcMaps {
     CUtensorMap q16;   // 2D {D, H*L} 16-bit, box {64, 128}, 128-byte swizzle
-    CUtensorMap k;     // 3D {D, kv_seq_len, Hk}, box {64, 32, 1}, 128-byte swizzle
+    CUtensorMap k;     // 3D {D, kv_seq_len, Hk}, box {64, 32, 1}, 128-byte swizzle (one chunk)
     CUtensorMap v;
+    CUtensorMap k64;   // the same tensors, box {64, 64, 1}: two consecutive chunks
+    CUtensorMap v64;
 };
 
 struct QuantArgs {

@@ -238,8 +238,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads issued
-        auto load_slabs = [&](const CUtensorMap *map, const int (&chunk)[4], int nslab, int x0, int share,
-                              int share_idx, uint16_t mask) -> bool {
+        // A slab's 4 chunks go as 32-key boxes split over the CTAs of the share
+        // group.  With D = 512, where chunks 0-1 and 2-3 are consecutive pairs,
+        // they go as two 64-key boxes instead (one per CTA with a share of 2,
+        // both with 1): half the boxes to issue for the twelve slabs of a key
+        // tile (measured faster there; with D <= 256 the 32-key boxes were).
+        auto load_slabs = [&](const CUtensorMap *map, const CUtensorMap *map64, const int (&chunk)[4], int nslab,
+                              int x0, int share, int share_idx, uint16_t mask) -> bool {
+            const bool pairs = D == 512 && share <= 2 && chunk[0] >= 0 && chunk[1] == chunk[0] + 1 &&
+                               chunk[2] >= 0 && chunk[3] == chunk[2] + 1;
             for (int s = 0; s < nslab; ++s) {
                 const int slot = issued % ST;
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
@@ -249,12 +256,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     if (ok) {
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
                         unsigned char *dst = sRing + slot * kSlab;
-                        for (int c = share_idx; c < 4; c += share) {
-                            const int y = chunk[c] >= 0 ? chunk[c] * 32 : n_pad;
-                            if (share > 1)
-                                tma_load_3d_mc(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh, mask);
-                            else
-                                tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
+                        if (pairs) {
+                            for (int c = 2 * share_idx; c < 4; c += 2 * share) {
+                                if (share > 1)
+                                    tma_load_3d_mc(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32,
+                                                   kh, mask);
+                                else
+                                    tma_load_3d(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32, kh);
+                            }
+                        } else {
+                            for (int c = share_idx; c < 4; c += share) {
+                                const int y = chunk[c] >= 0 ? chunk[c] * 32 : n_pad;
+                                if (share > 1)
+                                    tma_load_3d_mc(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh, mask);
+                                else
+                                    tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
+                            }
                         }
                     }
                 }
@@ -269,20 +286,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             if (lane == 0) {
                 tma_prefetch_desc(&maps.k);
                 tma_prefetch_desc(&maps.v);
+                tma_prefetch_desc(&maps.k64);
+                tma_prefetch_desc(&maps.v64);
                 mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
                 for (int s = 0; s < NSK; ++s)
                     tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
             }
             int cur[4], nxt[4], cl_unused;
             for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-            ok = load_slabs(&maps.k, nxt, NSK, 0, k_share, k_idx, k_mask);
+            ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0, k_share, k_idx, k_mask);
             for (int t = 0; t < T && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
                 if (t + 1 < T) {
                     for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-                    ok = load_slabs(&maps.k, nxt, NSK, 0, k_share, k_idx, k_mask);
+                    ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0, k_share, k_idx, k_mask);
                 }
-                if (ok) ok = load_slabs(&maps.v, cur, NSV, os * DV, v_share, v_idx, v_mask);
+                if (ok) ok = load_slabs(&maps.v, &maps.v64, cur, NSV, os * DV, v_share, v_idx, v_mask);
             }
             // Drain: every copy into this CTA's ring has landed, and every CTA
             // of the cluster has released the last use of each slot, so no
