@@ -244,16 +244,28 @@ class TreeBench:
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
         self.e2e_h2d = sum(t.numel() * t.element_size() for t in (self.h_q, self.h_mask, self.h_k, self.h_v))
         self.e2e_d2h = self.h_out.numel() * 4
+        # two device input sets: step i + 1's inputs land in one while step i reads the other
+        m = self.parents if self.use_parents else self.mask
+        k1 = self.ks[1] if self.nsets > 1 else self.ks[0].clone()
+        v1 = self.vs[1] if self.nsets > 1 else self.vs[0].clone()
+        self.e2e_sets = [(self.q, m, self.ks[0], self.vs[0]), (self.q.clone(), m.clone(), k1, v1)]
 
-    def e2e_step(self, i):
+    def e2e_copy_in(self, i):
         N = self.wl.kv_seq_len
-        s = i % self.nsets
-        self.q.copy_(self.h_q, non_blocking=True)
-        (self.parents if self.use_parents else self.mask).copy_(self.h_mask, non_blocking=True)
+        q, m, k, v = self.e2e_sets[i % 2]
+        q.copy_(self.h_q, non_blocking=True)
+        m.copy_(self.h_mask, non_blocking=True)
         for h in range(self.wl.n_kv_heads):   # contiguous [N, D] runs, one copy each
-            self.ks[s][h, :N].copy_(self.h_k[h], non_blocking=True)
-            self.vs[s][h, :N].copy_(self.h_v[h], non_blocking=True)
-        self.step(i)
+            k[h, :N].copy_(self.h_k[h], non_blocking=True)
+            v[h, :N].copy_(self.h_v[h], non_blocking=True)
+
+    def e2e_compute(self, i):
+        q, m, k, v = self.e2e_sets[i % 2]
+        if self.use_parents:
+            self.ta.tree_attn_fwd_parents(self.p, m, q, k, v, self.tmp, self.out)
+        else:
+            self.ta.tree_attn_fwd(self.p, q, k, v, m, self.tmp, self.out)
+        self.ta.tree_attn_reduce(self.p, self.tmp, self.out)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_reference(self, rows, threads):
@@ -323,18 +335,31 @@ class QuantBench:
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
         self.e2e_h2d = sum(t.numel() * t.element_size() for t in self.h.values())
         self.e2e_d2h = self.h_out.numel() * self.h_out.element_size()
+        # two device input sets: step i + 1's inputs land in one while step i reads the other
+        first = dict(self.d)
+        first.update(self.sets[0])
+        kv = set(self.sets[0])
+        second = {k: (v.clone() if isinstance(v, torch.Tensor) and k not in kv else v) for k, v in self.d.items()}
+        second.update(self.sets[1] if self.nsets > 1 else {k: v.clone() for k, v in self.sets[0].items()})
+        self.e2e_sets = [first, second]
 
-    def e2e_step(self, i):
+    def e2e_copy_in(self, i):
         wl = self.wl
         lo = wl.tokens - wl.window_tokens
-        s = self.sets[i % self.nsets]
-        self.d["queries"].copy_(self.h["queries"], non_blocking=True)
+        e = self.e2e_sets[i % 2]
+        e["queries"].copy_(self.h["queries"], non_blocking=True)
         for k in ("k_packed", "k_scales", "k_biases", "v_packed", "v_scales", "v_biases"):
-            s[k][:, lo:].copy_(self.h[k], non_blocking=True)
+            e[k][:, lo:].copy_(self.h[k], non_blocking=True)
         for k in ("mask_bool", "mask_float"):
             if k in self.h:
-                self.d[k][:, lo:].copy_(self.h[k], non_blocking=True)
-        self.step(i)
+                e[k][:, lo:].copy_(self.h[k], non_blocking=True)
+
+    def e2e_compute(self, i):
+        e = self.e2e_sets[i % 2]
+        self.ta.quant_sdpa_fwd(self.p, e["queries"], e["k_packed"], e["k_scales"], e["k_biases"],
+                               e["v_packed"], e["v_scales"], e["v_biases"],
+                               e["sinks"] if self.wl.has_sinks else None, e.get("mask_bool"),
+                               e.get("mask_float"), self.tmp, self.out)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def cpu_reference(self, rows, threads):
@@ -452,22 +477,51 @@ def run_ours(args):
 
     ms, ms_fwd = max_over_ranks([ms, ms_fwd], ws, dev)
 
-    # end to end: host buffers in, output back, every step
+    # end to end: every step's inputs from pinned host memory and its output back, through the
+    # public API; step i + 1's copies (second stream, second device input set) overlap step i.
+    # The steps are captured in a CUDA graph (as a serving loop would), so the host's per-call
+    # work is not timed; every copy still runs in every step.
     bench.e2e_setup()
-    e2e_steps = max(1, min(args.e2e_steps, args.steps))
-    for i in range(3):
-        bench.e2e_step(i)
-    torch.cuda.synchronize()
     s = torch.cuda.current_stream()
+    copy_s = torch.cuda.Stream()
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_run(n):
+        cur = torch.cuda.current_stream()
+        for b in range(2):
+            free[b].record(cur)
+        for i in range(n):
+            b = i % 2
+            copy_s.wait_event(free[b])         # step i - 2 is done reading input set b
+            with torch.cuda.stream(copy_s):
+                bench.e2e_copy_in(i)
+                ready[b].record(copy_s)
+            cur.wait_event(ready[b])
+            bench.e2e_compute(i)
+            free[b].record(cur)
+        cur.wait_stream(copy_s)
+
+    e2e_run(3)
+    torch.cuda.synchronize()
+    per_graph = max(2, min(50, args.e2e_steps))
+    replays = max(1, -(-args.e2e_steps // per_graph))
+    e2e_steps = per_graph * replays
+    ge = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(ge):
+        e2e_run(per_graph)
+    ge.replay()
+    torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(s)
-    for i in range(e2e_steps):
-        bench.e2e_step(i)
-    e1.record(s)
+    for _ in range(replays):
+        ge.replay()
+    e1.record(s)                               # after the last output copy
     torch.cuda.synchronize()
     barrier()
+    del ge
     ms_e2e = e0.elapsed_time(e1)
     ms_e2e = max_over_ranks([ms_e2e], ws, dev)[0]
 
@@ -494,7 +548,9 @@ def run_ours(args):
         "e2e": {"value": round(job_rate(ws, bench.bytes_per_step, e2e_steps, ms_e2e), 2),
                 "unit": "GB/s", "h2d_bytes_per_step": bench.e2e_h2d,
                 "d2h_bytes_per_step": bench.e2e_d2h, "steps": e2e_steps,
-                "us_per_step": round(ms_e2e * 1e3 / e2e_steps, 3)},
+                "us_per_step": round(ms_e2e * 1e3 / e2e_steps, 3),
+                "overlap": "step i+1's host-to-device copies on a second stream during step i",
+                "launch": "CUDA graphs of %d steps" % per_graph},
         "gpu_launches": int(round(launches_per_step * args.steps)),
         "clocks": clocks,
     }
