@@ -46,18 +46,34 @@ __global__ void __launch_bounds__(kMergeThreads) quant_merge_kernel(const QuantA
     if (g < groups) {
         const size_t stride = static_cast<size_t>(a.rows) * a.dim;
         const float *po = a.part_o + static_cast<size_t>(q) * a.dim + 4 * i;
-#pragma unroll 4
-        for (int w = g; w < a.nwg; w += groups) {
-            const float2 sm = __ldg(ml + static_cast<size_t>(w) * a.rows);
-            const float4 o = __ldg(reinterpret_cast<const float4 *>(po + w * stride));
-            if (sm.y == -INFINITY) continue;   // a split that saw no token
+        auto merge = [&](float2 sm, float4 o) {
+            if (sm.y == -INFINITY) return;   // a split that saw no token
             const float mn = fmaxf(m, sm.y);
             const float c = exp2f(m - mn), e = exp2f(sm.y - mn);   // c = 0 while m = -inf
             m = mn;
             ssum = ssum * c + sm.x * e;
             acc.x = acc.x * c + o.x * e; acc.y = acc.y * c + o.y * e;
             acc.z = acc.z * c + o.z * e; acc.w = acc.w * c + o.w * e;
+        };
+        // the thread's first kPre slots are all loaded before any is merged (one round
+        // trip for up to kPre * groups splits), the rest four at a time
+        constexpr int kPre = 8;
+        float2 sm_pre[kPre];
+        float4 o_pre[kPre];
+#pragma unroll
+        for (int k = 0; k < kPre; ++k) {
+            const int w = g + k * groups;
+            if (w < a.nwg) {
+                sm_pre[k] = __ldg(ml + static_cast<size_t>(w) * a.rows);
+                o_pre[k] = __ldg(reinterpret_cast<const float4 *>(po + w * stride));
+            }
         }
+#pragma unroll
+        for (int k = 0; k < kPre; ++k)
+            if (g + k * groups < a.nwg) merge(sm_pre[k], o_pre[k]);
+#pragma unroll 4
+        for (int w = g + kPre * groups; w < a.nwg; w += groups)
+            merge(__ldg(ml + static_cast<size_t>(w) * a.rows), __ldg(reinterpret_cast<const float4 *>(po + w * stride)));
     }
     s_acc[t] = acc;
     s_ms[t] = make_float2(m, ssum);
