@@ -1,8 +1,8 @@
 #!/usr/bin/env python3
 """Benchmark of the tree-verify attention step (and the quantized-KV variant).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload fixed_tree|pr1_chain|dynamic_tree|quant_b4|quant_b8_masks]
+    python bench.py [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload dynamic_tree|fixed_tree|pr1_chain|quant_b4|quant_b8_masks|quant_tree]
 
 A step is one verify pass over one batch of synthetic inputs: mask compaction
 + main pass + split merge (tree), or main pass + merge (quantized).  The
@@ -10,7 +10,13 @@ headline is KV-cache bytes streamed per second (K and V of positions
 [0, kv_seq_len), once per KV head) over the device-timed region.  Inputs are
 resident in HBM; K/V rotate over enough copies that the bytes read per pass of
 the rotation exceed 3x the L2 size, so every step reads cold K/V.  Prints one
-JSON line (rank 0).
+JSON line.  The default workload is the largest single-GPU one, the dynamic
+asymmetric tree (537 MB of K/V per step).
+
+One GPU per process: the verify step of one sequence never needs more, and
+the library has no multi-GPU path, so --gpus > 1 (or a multi-rank launch) is
+refused with an error.  The reference arm (--impl reference, the float64 CPU
+oracle) runs on rank 0 alone; other ranks exit at once.
 """
 from __future__ import annotations
 
@@ -44,7 +50,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=200)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="fixed_tree", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="dynamic_tree", choices=sorted(WORKLOADS))
     ap.add_argument("--e2e-steps", type=int, default=300)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
@@ -52,9 +58,9 @@ def parse():
                     help="run --warmup eager steps and exit (a short, graph-free run for a profiler)")
     ap.add_argument("--mask-build", action="store_true",
                     help="tree workloads: also time the device-side tree-mask build from the parent array")
-    ap.add_argument("--quant-path", type=int, default=0, choices=[0, 1, 2],
-                    help="quantized workloads: 0 automatic, 1 CUDA-core kernel, 2 tensor-core kernel "
-                         "where the shape allows it")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="kernel family of the main pass: 0 automatic, 1 CUDA cores, 2 tensor cores "
+                         "where the shape allows them")
     ap.add_argument("--tree-mask", default="dense", choices=["dense", "parents"],
                     help="tree workloads: the mask as the dense f32 array (tree_attn_fwd) or as the "
                          "parent array (tree_attn_fwd_parents)")
@@ -70,38 +76,13 @@ def dist_env():
     return ws, rank, local
 
 
-# ------------------------------------------------------------ multi-rank helpers
-# One process per GPU, each running its own independent step stream (weak
-# scaling: the verify step needs no data-path exchange).  The only collectives
-# are a barrier around the timed region and the max over ranks of the times.
-
-def rank_barrier(ws):
-    """A barrier over the ranks (a no-op for one rank)."""
-    if ws > 1:
-        import torch.distributed as dist
-        dist.barrier()
-
-
-def max_over_ranks(values, ws, device=None):
-    """Element-wise maximum over the ranks of a list of floats (identity for
-    one rank); every rank receives the result."""
-    if ws <= 1:
-        return [float(v) for v in values]
-    import torch.distributed as dist
-    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return [float(x) for x in t.cpu()]
-
-
-def job_rate(ws, bytes_per_step, steps, ms):
-    """Whole-job throughput in GB/s: every rank processed `steps` steps of
-    `bytes_per_step` K/V bytes within the slowest rank's `ms` milliseconds."""
-    return ws * bytes_per_step * steps / (ms * 1e-3) / 1e9
-
-
-def prints(rank):
-    """Rank 0 alone prints the JSON line."""
-    return rank == 0
+def refuse_multi_gpu(args, ws):
+    """This bench (and the library) runs one GPU per process; a request for more
+    is an error, not a silently smaller run."""
+    if args.gpus != 1 or ws != 1:
+        sys.stderr.write("bench.py: one GPU per process (got --gpus %d, WORLD_SIZE %d); the library has no "
+                         "multi-GPU path\n" % (args.gpus, ws))
+        sys.exit(2)
 
 
 def load_peaks():
@@ -182,8 +163,9 @@ class ClockSampler:
 
 # ------------------------------------------------------------- tree arm
 class TreeBench:
-    def __init__(self, ta, wl: W.TreeWorkload, dev, kv_sets=0, tree_mask="dense"):
+    def __init__(self, ta, wl: W.TreeWorkload, dev, kv_sets=0, tree_mask="dense", kernel=0):
         self.ta, self.wl, self.dev = ta, wl, dev
+        self.kernel = kernel
         inp = W.make_tree_inputs(wl)
         self.host = inp
         self.q = inp["q"].to(dev)
@@ -214,14 +196,21 @@ class TreeBench:
             self.built_mask = torch.empty_like(self.mask)
         self.ta.tree_mask_build(self.p, self.parents, self.built_mask)
 
+    def _fwd(self, q, m, k, v):
+        ta = self.ta
+        kind = ta.MASK_PARENTS if self.use_parents else ta.MASK_DENSE
+        ta.tree_attn_fwd_ex(self.p, self.kernel, kind, 0, q, k, v, m, self.tmp, self.out)
+
     def step(self, i, fwd_only=False):
         s = i % self.nsets
-        if self.use_parents:
-            self.ta.tree_attn_fwd_parents(self.p, self.parents, self.q, self.ks[s], self.vs[s], self.tmp, self.out)
-        else:
-            self.ta.tree_attn_fwd(self.p, self.q, self.ks[s], self.vs[s], self.mask, self.tmp, self.out)
+        self._fwd(self.q, self.parents if self.use_parents else self.mask, self.ks[s], self.vs[s])
         if not fwd_only:
             self.ta.tree_attn_reduce(self.p, self.tmp, self.out)
+
+    def status_word(self):
+        """The device status word of the last main pass (0 = every bounded wait completed)."""
+        off = self.ta.tree_attn_status_offset(self.p)
+        return int(self.tmp.view(torch.int32)[off // 4].item())
 
     def config(self):
         wl = self.wl
@@ -261,10 +250,7 @@ class TreeBench:
 
     def e2e_compute(self, i):
         q, m, k, v = self.e2e_sets[i % 2]
-        if self.use_parents:
-            self.ta.tree_attn_fwd_parents(self.p, m, q, k, v, self.tmp, self.out)
-        else:
-            self.ta.tree_attn_fwd(self.p, q, k, v, m, self.tmp, self.out)
+        self._fwd(q, m, k, v)
         self.ta.tree_attn_reduce(self.p, self.tmp, self.out)
         self.h_out.copy_(self.out, non_blocking=True)
 
@@ -278,7 +264,7 @@ class TreeBench:
 
 # ------------------------------------------------------------ quant arm
 class QuantBench:
-    def __init__(self, ta, wl: W.QuantWorkload, dev, kv_sets=0):
+    def __init__(self, ta, wl: W.QuantWorkload, dev, kv_sets=0, kernel=0):
         self.ta, self.wl, self.dev = ta, wl, dev
         inp = W.make_quant_inputs(wl)
         self.host = inp
@@ -291,10 +277,11 @@ class QuantBench:
         for _ in range(self.nsets - 1):
             self.sets.append({k: d[k].clone() for k in kv_keys})
         self.p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits,
-                                 wl.group_size, wl.has_sinks, wl.window_size, wl.scale, wl.nwg)
+                                 wl.group_size, wl.has_sinks, wl.window_size, wl.scale, wl.nwg, kernel)
         self.nwg = ta.quant_sdpa_num_splits(self.p)
         nb = ta.quant_sdpa_tmp_bytes(self.p)
-        self.tmp = torch.empty(max(1, (nb + 3) // 4), dtype=torch.float32, device=dev)
+        # the status word (tmp's first 32-bit word) is sticky: zeroed here, ORed by the kernel
+        self.tmp = torch.zeros(max(1, (nb + 3) // 4), dtype=torch.float32, device=dev)
         self.out = torch.empty((wl.rows, wl.dim), dtype=d["queries"].dtype, device=dev)
         self.bytes_per_step = wl.kv_bytes
         self.name = wl.name
@@ -362,6 +349,10 @@ class QuantBench:
                                e.get("mask_float"), self.tmp, self.out)
         self.h_out.copy_(self.out, non_blocking=True)
 
+    def status_word(self):
+        """ORed device status of every call since tmp was zeroed (0 = every bounded wait completed)."""
+        return int(self.tmp[:1].view(torch.int32).item())
+
     def cpu_reference(self, rows, threads):
         import oracle
         return oracle.quant_oracle_for(self.wl, self.host, rows=rows, threads=threads)
@@ -370,11 +361,11 @@ class QuantBench:
         return list(range(self.wl.rows))
 
 
-def make_bench(ta, name, dev, kv_sets=0, tree_mask="dense"):
+def make_bench(ta, name, dev, kv_sets=0, tree_mask="dense", kernel=0):
     wl = WORKLOADS[name]
     if isinstance(wl, W.TreeWorkload):
-        return TreeBench(ta, wl, dev, kv_sets, tree_mask)
-    return QuantBench(ta, wl, dev, kv_sets)
+        return TreeBench(ta, wl, dev, kv_sets, tree_mask, kernel)
+    return QuantBench(ta, wl, dev, kv_sets, kernel)
 
 
 # ------------------------------------------------------------ timing
@@ -386,7 +377,7 @@ def capture(fn, n, start):
     return g
 
 
-def timed_graph_steps(fn, steps, start, barrier):
+def timed_graph_steps(fn, steps, start):
     """Time exactly `steps` calls of fn on the device; returns (ms_total, launches_per_step)."""
     import tree_masked_speculative_gb300 as ta
     full, rem = divmod(steps, GRAPH_STEPS)
@@ -400,7 +391,6 @@ def timed_graph_steps(fn, steps, start, barrier):
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize()
     e0.record(s)
     for _ in range(full):
@@ -409,7 +399,6 @@ def timed_graph_steps(fn, steps, start, barrier):
         gr.replay()
     e1.record(s)
     torch.cuda.synchronize()
-    barrier()
     return e0.elapsed_time(e1), per_step
 
 
@@ -432,27 +421,30 @@ def cpu_baseline(bench, seconds):
                       "scaled to a full step" % (len(sample), len(rows), threads, dt)}
 
 
+def check_status(bench, where):
+    """Every bounded wait of the timed kernels completed (a timed-out wait would
+    have left the output invalid)."""
+    st = bench.status_word()
+    if st != 0:
+        raise RuntimeError("device status word %#x after the %s: a bounded wait gave up" % (st, where))
+    return st
+
+
 def run_ours(args):
     ws, rank, local = dist_env()
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    barrier = lambda: rank_barrier(ws)
+    refuse_multi_gpu(args, ws)
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     from tree_masked_speculative_gb300 import build as b
-    if rank == 0 or ws == 1:
-        b.build()
-    if ws > 1:
-        barrier()
+    b.build()
     import tree_masked_speculative_gb300 as ta
 
-    ta.ta_set_quant_path(args.quant_path)
-    bench = make_bench(ta, args.workload, dev, args.kv_sets, args.tree_mask)
+    bench = make_bench(ta, args.workload, dev, args.kv_sets, args.tree_mask, args.kernel)
     if args.profile:
         for i in range(max(1, args.warmup)):
             bench.step(i)
         torch.cuda.synchronize()
+        check_status(bench, "profile steps")
         print(json.dumps({"profile_run": bench.name, "eager_steps": max(1, args.warmup)}), flush=True)
         return
     # warm-up (untimed): eager steps, then enough graph replays to bring clocks up
@@ -467,15 +459,14 @@ def run_ours(args):
         g.replay()
         torch.cuda.synchronize()
     del g
-    ms, launches_per_step = timed_graph_steps(bench.step, args.steps, 0, barrier)
+    ms, launches_per_step = timed_graph_steps(bench.step, args.steps, 0)
+    check_status(bench, "timed steps")
     # the dominant pass alone (mask compaction + main kernel), same rotation, for the roofline
-    ms_fwd, _ = timed_graph_steps(lambda i: bench.step(i, fwd_only=True), args.steps, 0, barrier)
+    ms_fwd, _ = timed_graph_steps(lambda i: bench.step(i, fwd_only=True), args.steps, 0)
     ms_mask = None
     if args.mask_build and isinstance(bench, TreeBench) and bench.parents is not None:
-        ms_mask, _ = timed_graph_steps(bench.mask_step, args.steps, 0, barrier)
+        ms_mask, _ = timed_graph_steps(bench.mask_step, args.steps, 0)
     clocks = sampler.stop()
-
-    ms, ms_fwd = max_over_ranks([ms, ms_fwd], ws, dev)
 
     # end to end: every step's inputs from pinned host memory and its output back, through the
     # public API; step i + 1's copies (second stream, second device input set) overlap step i.
@@ -513,45 +504,39 @@ def run_ours(args):
     ge.replay()
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
     torch.cuda.synchronize()
     e0.record(s)
     for _ in range(replays):
         ge.replay()
     e1.record(s)                               # after the last output copy
     torch.cuda.synchronize()
-    barrier()
     del ge
     ms_e2e = e0.elapsed_time(e1)
-    ms_e2e = max_over_ranks([ms_e2e], ws, dev)[0]
+    status = check_status(bench, "end-to-end steps")
 
-    if not prints(rank):
-        if ws > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
-        return
     peak, peak_kind = load_peaks()
     us_step = ms * 1e3 / args.steps
-    value = job_rate(ws, bench.bytes_per_step, args.steps, ms)
+    value = bench.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
     achieved = bench.bytes_per_step * args.steps / (ms_fwd * 1e-3) / 1e9
     traffic = committed_traffic(bench.name)
     line = {
-        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": ws,
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
-        "us_per_step": round(us_step, 3), "pct_of_hbm_peak": round(100 * value / ws / peak, 1),
+        "us_per_step": round(us_step, 3), "pct_of_hbm_peak": round(100 * value / peak, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": bench.dtype,
         "data": "synthetic (seeded, shapes of the named workload)", "config": bench.config(),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": bench.fwd_label + ", timed alone",
                      "peak_kind": peak_kind + " (MEASURED_PEAKS hbm_gbs)"},
-        "e2e": {"value": round(job_rate(ws, bench.bytes_per_step, e2e_steps, ms_e2e), 2),
+        "e2e": {"value": round(bench.bytes_per_step * e2e_steps / (ms_e2e * 1e-3) / 1e9, 2),
                 "unit": "GB/s", "h2d_bytes_per_step": bench.e2e_h2d,
                 "d2h_bytes_per_step": bench.e2e_d2h, "steps": e2e_steps,
                 "us_per_step": round(ms_e2e * 1e3 / e2e_steps, 3),
                 "overlap": "step i+1's host-to-device copies on a second stream during step i",
                 "launch": "CUDA graphs of %d steps" % per_graph},
         "gpu_launches": int(round(launches_per_step * args.steps)),
+        "device_status": status,
         "clocks": clocks,
     }
     if ms_mask is not None:
@@ -563,9 +548,6 @@ def run_ours(args):
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(bench, args.cpu_seconds)
     print(json.dumps(line), flush=True)
-    if ws > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
 
 
 def committed_traffic(name):
@@ -594,7 +576,7 @@ def run_reference(args):
     """The float64 CPU oracle as it stands, on this machine's host cores: each step
     computes a bounded sample of the workload's query rows."""
     ws, rank, _ = dist_env()
-    if not prints(rank):
+    if rank != 0:
         return                       # the other ranks exit 0 without work
     import oracle
     oracle.build()

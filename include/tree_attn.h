@@ -55,6 +55,18 @@ typedef enum {
 
 typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2, TA_U32 = 3, TA_I32 = 4 } ta_dtype;
 
+/*
+ * Kernel family of a call (ta_tree_options.kernel, ta_quant_params.kernel).
+ * TA_KERNEL_AUTO is the library's choice; the others force a family, for
+ * tests and measurements.  The choice travels with the call: there is no
+ * process-wide setting, so concurrent callers cannot affect one another.
+ */
+typedef enum {
+    TA_KERNEL_AUTO = 0,         /* tensor cores where the shape makes a dense contraction */
+    TA_KERNEL_CUDA_CORES = 1,   /* always the CUDA-core kernel */
+    TA_KERNEL_TENSOR_CORES = 2  /* the tensor-core kernel wherever its shape rules allow it */
+} ta_kernel;
+
 /* Borrowed device buffer. `bytes` is the usable size starting at `ptr`. */
 typedef struct {
     void *ptr;
@@ -92,7 +104,8 @@ typedef struct {
  *   batch B, n_q_heads nQ, n_kv_heads nKV (nQ % nKV == 0, repeat = nQ / nKV),
  *   dim (a multiple of 32/bits and of group_size), tokens N > 0, bits in {4, 8},
  *   group_size G, has_sinks in {0, 1}, window_size (0 = all tokens, else the
- *   last window_size tokens), scale (multiplies the query), nwg (splits, 0 = auto).
+ *   last window_size tokens), scale (multiplies the query), nwg (splits, 0 = auto),
+ *   kernel (ta_kernel; not from the pages).
  */
 typedef struct {
     uint32_t batch;
@@ -106,7 +119,24 @@ typedef struct {
     uint32_t window_size;
     float scale;
     uint32_t nwg;
+    uint32_t kernel;   /* ta_kernel; the split count and tmp size follow the family chosen */
 } ta_quant_params;
+
+/* Mask forms of tree_attn_fwd_ex. */
+typedef enum {
+    TA_MASK_DENSE = 0,    /* `mask` is the [q_l, mask_stride] f32 mask (tree_attn_fwd) */
+    TA_MASK_CAUSAL = 1,   /* implicit causal / sliding window; `mask` unused (tree_attn_fwd_causal) */
+    TA_MASK_PARENTS = 2   /* `mask` is the [q_l] i32 parent array (tree_attn_fwd_parents) */
+} ta_mask_kind;
+
+/* Per-call options of tree_attn_fwd_ex (the pages' 36-byte params struct
+ * stays as it is). */
+typedef struct {
+    int32_t kernel;         /* ta_kernel */
+    int32_t mask_kind;      /* ta_mask_kind */
+    uint32_t window_start;  /* TA_MASK_CAUSAL: first attended position */
+    int32_t reserved;       /* must be 0 */
+} ta_tree_options;
 
 /* ------------------------------------------------------------------ tree */
 
@@ -185,6 +215,31 @@ ta_status tree_attn_fwd_parents(const ta_tree_params *p, const ta_buf *parents, 
                                 void *stream);
 
 /*
+ * The main pass of tree_attn_fwd, tree_attn_fwd_causal or tree_attn_fwd_parents
+ * (chosen by o->mask_kind; `mask` is then the dense mask, unused, or the
+ * parent array) with the kernel family of o->kernel.  Same buffers, checks,
+ * workspace and results as those calls, which are this call with
+ * TA_KERNEL_AUTO.  The workspace size and split count do not depend on the
+ * family.  Errors: TA_ERR_INVALID_ARGUMENT for a NULL `o`, an unknown kernel
+ * or mask kind, reserved != 0, or a missing mask / parent array.
+ */
+ta_status tree_attn_fwd_ex(const ta_tree_params *p, const ta_tree_options *o, const ta_buf *q,
+                           const ta_buf *k, const ta_buf *v, const ta_buf *mask, const ta_buf *tmp,
+                           const ta_buf *out, void *stream);
+
+/*
+ * Byte offset, inside the `tmp` buffer of the tree main pass, of the call's
+ * 32-bit device status word (an int32).  The mask-compaction pass of every
+ * main-pass call sets it to 0; the tensor-core main pass writes a non-zero
+ * code there when one of its bounded waits (a K/V copy or an MMA that did not
+ * complete within about two seconds) gave up, and the output of that call is
+ * then not valid.  The library never reads it back: a caller that wants to
+ * check copies the word to the host after the call (same stream) and tests it
+ * for 0.  SIZE_MAX on invalid parameters.
+ */
+size_t tree_attn_status_offset(const ta_tree_params *p);
+
+/*
  * Second pass ([TA-R] tree_attention, reduce pass): merges the nwg partials
  * of every (query, head) row with a log-sum-exp rescale:
  *   M* = max_w M_w,  S* = sum_w S_w e^(M_w - M*),
@@ -205,8 +260,10 @@ ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp, const ta_
  *   16 MiB (16777216 bytes) that every GPU loading the library holds until
  *   process exit.  Parameters whose tree_attn_workspace_bytes exceed that
  *   fail with TA_ERR_UNSUPPORTED (lower nwg, or use tree_attn_fwd).
- *   The array's address is looked up on the first call made on each device
- *   (that device current); make that first call before any stream capture.
+ *   The array's device address is looked up on every call (it belongs to the
+ *   CUDA context, which a cudaDeviceReset replaces); the first call in a
+ *   context also loads the library's module there, so make that first call
+ *   before any stream capture.
  *   It allocates nothing and calls no allocating routine.  All calls share the
  *   array and it keeps the last call's contents; nothing in it has to start
  *   at zero, but calls that overlap on the GPU race on it.
@@ -283,39 +340,40 @@ const char *ta_last_error(void);
 uint64_t ta_launch_count(void);
 
 /*
- * Tree kernel family used by later calls: 0 = automatic (tensor cores when the
- * KV type is f16/bf16 and a KV head serves >= 16 query rows, else CUDA-core
- * FMA), 1 = always the CUDA-core kernel, 2 = tensor-core kernel where it
- * applies.  Process-wide; returns the previous value, or -1 for a bad value.
- * Meant for tests and measurements.
- */
-int ta_set_tree_path(int path);
-
-/*
- * Quantized-KV kernel family used by later calls: 0 = automatic (the
- * tensor-core kernel when the shape allows it and a KV row serves >= 16 query
- * rows, e.g. draft-tree nodes as rows, else the CUDA-core kernel), 2 = the
- * tensor-core kernel wherever the shape allows it, 1 = always the CUDA-core
- * kernel.  Process-wide; returns the previous value, or
- * -1 for a bad value.  The split count and tmp size depend on the family, so
- * size tmp (quant_sdpa_tmp_bytes) after setting it.  Meant for tests and
- * measurements.
+ * 1 if quant_sdpa_fwd with these params (p->kernel included) takes the
+ * tensor-core kernel, 0 if the CUDA-core kernel, -1 for invalid params.  No
+ * device work.
  *
  * The tensor-core kernel serves head dimensions 64, 128 and 256 when TMEM
  * holds O (dim f32 columns) and two score buffers (dim / group_size groups x
- * 16 or 32 query rows each).  It feeds the tensor core the exact integer codes
- * of K (the per-group scales and biases are applied to the f32 scores), V
- * dequantized once to f16 (s * code + b, one rounding) and the weights P in
- * f16; Q is scaled per row by a power of two into f16 (exact for f16 and bf16
- * queries).  Dequantized V values are assumed to lie within the f16 range
- * (|v| <= 65504); the CUDA-core kernel has no such limit.
+ * 16 or 32 query rows each) and its shared-memory layout fits.  With
+ * TA_KERNEL_AUTO it is chosen from 16 query rows per KV row (e.g. draft-tree
+ * nodes as rows).  It feeds the tensor core the exact integer codes of K (the
+ * per-group scales and biases are applied to the f32 scores), V dequantized
+ * once to f16 (s * code + b, one rounding) and the weights P as two f16 terms
+ * (P_hi + P_lo); Q is scaled per row by a power of two into f16 (exact for
+ * f16 and bf16 queries).  Dequantized V values are assumed to lie within the
+ * f16 range (|v| <= 65504); the CUDA-core kernel has no such limit.
  */
-int ta_set_quant_path(int path);
-
-/* 1 if quant_sdpa_fwd with these params takes the tensor-core kernel under the
- * current ta_set_quant_path setting, 0 if the CUDA-core kernel, -1 for invalid
- * params.  No device work. */
 int quant_sdpa_uses_tensor_cores(const ta_quant_params *p);
+
+/*
+ * Test hook, not for production use: quant_sdpa_fwd on the CUDA-core kernel
+ * (p->kernel must resolve to it, else TA_ERR_UNSUPPORTED) with the first K/V
+ * copy wait of every CTA bounded by `first_wait_polls` polls instead of the
+ * normal bound; 0 makes that wait give up at once.  It exercises the failure
+ * path of the kernel's bounded waits without any fault: the CTA ORs 1 into the
+ * status word (tmp's first 32-bit word), waits (with the normal bound) until
+ * every copy it issued has landed, and returns.  The output is then not valid.
+ * Same buffers and checks as quant_sdpa_fwd.
+ */
+ta_status ta_test_quant_sdpa_fwd_wait_limit(uint32_t first_wait_polls, const ta_quant_params *p,
+                                            const ta_buf *queries, const ta_buf *k_packed,
+                                            const ta_buf *k_scales, const ta_buf *k_biases,
+                                            const ta_buf *v_packed, const ta_buf *v_scales,
+                                            const ta_buf *v_biases, const ta_buf *sinks,
+                                            const ta_buf *mask_bool, const ta_buf *mask_float,
+                                            const ta_buf *tmp, const ta_buf *out, void *stream);
 
 #ifdef __cplusplus
 }

@@ -44,22 +44,22 @@ def to_dev(inp: dict, dev="cuda"):
     return {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
 
 
-def run_tree(ta, wl: W.TreeWorkload, inp: dict, *, causal=False, window_start=0, nwg=None):
+def run_tree(ta, wl: W.TreeWorkload, inp: dict, *, causal=False, window_start=0, nwg=None, kernel=0):
     d = to_dev(inp)
     out = ta.tree_attention(d["q"], d["k"], d["v"], None if causal else d["mask"],
                             n_heads=wl.n_heads, n_kv_heads=wl.n_kv_heads, kv_seq_len=wl.kv_seq_len,
                             scale=wl.scale, mask_stride=wl.mask_stride,
-                            nwg=wl.nwg if nwg is None else nwg, window_start=window_start)
+                            nwg=wl.nwg if nwg is None else nwg, window_start=window_start, kernel=kernel)
     torch.cuda.synchronize()
     return out
 
 
-def run_quant(ta, wl: W.QuantWorkload, inp: dict, *, nwg=None, out_dtype=None):
+def run_quant(ta, wl: W.QuantWorkload, inp: dict, *, nwg=None, out_dtype=None, kernel=0):
     d = to_dev(inp)
     out = ta.quant_sdpa(d, batch=wl.batch, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads,
                         dim=wl.dim, tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size,
                         has_sinks=wl.has_sinks, window_size=wl.window_size, scale=wl.scale,
-                        nwg=wl.nwg if nwg is None else nwg, out_dtype=out_dtype)
+                        nwg=wl.nwg if nwg is None else nwg, out_dtype=out_dtype, kernel=kernel)
     torch.cuda.synchronize()
     return out
 

@@ -94,3 +94,29 @@ def test_peak_lookup(tmp_path, monkeypatch):
     assert bench.load_peaks() == (6800.0, "fallback")
     _write(os.path.join(str(tmp_path), "MEASURED_PEAKS.json"), json.dumps({"hbm_gbs": 6696.5}))
     assert bench.load_peaks() == (6696.5, "measured")
+
+
+def test_bench_refuses_more_than_one_gpu():
+    """One GPU per process: --gpus 2, or a multi-rank launch, is an error (exit 2),
+    not a silently smaller run.  The refusal comes before any device work."""
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2"], env=env,
+                       capture_output=True, text=True, timeout=300)
+    assert r.returncode == 2 and "one GPU per process" in r.stderr
+    env.update(WORLD_SIZE="2", RANK="0")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py")], env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 2 and "one GPU per process" in r.stderr
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = dict(os.environ, WORLD_SIZE="2", RANK="1", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--gpus", "2"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""

@@ -189,7 +189,7 @@ def test_reduce_validates_before_launch(ta):
 
 @pytest.mark.parametrize("kw,pbytes,pdtype,st_want,frag", [
     (dict(q_l=10), 10 * 4, "U32", 1, "parents dtype"),
-    (dict(q_l=10), None, None, 1, "parents dtype"),                    # no parent array at all
+    (dict(q_l=10), None, None, 1, "parents is NULL"),                  # no parent array at all
     (dict(q_l=10), 9 * 4, "I32", 2, "parents"),
     (dict(q_l=120), 120 * 4, "I32", 1, "q_l"),                          # more nodes than keys
     (dict(q_l=257, kv_seq_len=1000, mask_stride=1000), 257 * 4, "I32", 4, "q_l <= 256"),
@@ -290,13 +290,39 @@ def test_quant_dtype_and_size_rejections(ta):
     assert st == 2 and "tmp" in msg
 
 
-def test_set_tree_path(ta):
-    prev = ta.ta_set_tree_path(1)
-    assert ta.ta_set_tree_path(prev) == 1
-    assert ta.ta_set_tree_path(7) == -1
-    prev = ta.ta_set_quant_path(1)
-    assert ta.ta_set_quant_path(prev) == 1
-    assert ta.ta_set_quant_path(-1) == -1
+def test_kernel_choice_is_per_call(ta):
+    """The kernel family travels with each call (no process-wide switch): an
+    invalid choice is rejected before any launch, a valid one changes nothing
+    for other calls."""
+    d = dict(n_heads=4, n_kv_heads=2, head_dim=128, kv_seq_len=50, kv_capacity=64, scale=0.1, nwg=0, q_l=10,
+             mask_stride=64)
+    p = ta.TreeParams(**d)
+    b = ctypes.byref(_b(ta, 1 << 30, ta.TA_F32))
+    before = ta.ta_launch_count()
+    for kernel, kind, frag in [(3, 0, "kernel"), (-1, 0, "kernel"), (0, 7, "mask_kind")]:
+        o = ta.TreeOptions(kernel, kind, 0, 0)
+        st = ta.lib.tree_attn_fwd_ex(ctypes.byref(p), ctypes.byref(o), b, b, b, b, b, b, None)
+        assert st == 1 and frag in ta.ta_last_error()
+    o = ta.TreeOptions(0, 0, 0, 5)
+    assert ta.lib.tree_attn_fwd_ex(ctypes.byref(p), ctypes.byref(o), b, b, b, b, b, b, None) == 1
+    assert "reserved" in ta.ta_last_error()
+    assert ta.lib.tree_attn_fwd_ex(ctypes.byref(p), None, b, b, b, b, b, b, None) == 1
+    o = ta.TreeOptions(0, ta.MASK_DENSE, 0, 0)
+    assert ta.lib.tree_attn_fwd_ex(ctypes.byref(p), ctypes.byref(o), b, b, b, None, b, b, None) == 1
+    assert "needs a mask" in ta.ta_last_error()
+    q = ta.quant_params(1, 8, 2, 128, 100, 4, 64, 0, 0, 0.1, 0, 3)
+    assert ta.quant_sdpa_uses_tensor_cores(q) == -1
+    assert ta.quant_sdpa_tmp_bytes(q) == 2 ** 64 - 1
+    assert ta.ta_launch_count() == before
+
+
+def test_status_offset_is_the_workspace_header(ta):
+    p = ta.tree_params(24, 4, 256, 4096, 8192, 1 / 16, 32, 4096, 5)
+    ws = ta.tree_attn_workspace_bytes(p)
+    off = ta.tree_attn_status_offset(p)
+    assert off == ws - 256 and off % 256 == 0
+    bad = ta.tree_params(24, 4, 100, 4096, 8192, 1 / 16, 32, 4096, 5)
+    assert ta.tree_attn_status_offset(bad) == 2 ** 64 - 1
 
 
 # ------------------------------------------------------------ tree mask builder
@@ -328,23 +354,17 @@ def test_tree_mask_build_rejections(ta, kw, pbytes, pdtype, mbytes, mdtype, st_w
 
 def test_quant_kernel_family_choice(ta):
     """Which quantized kernel a shape takes (no device work)."""
-    def p(dim, G=64, nQ=32, nKV=8, bits=4):
-        return ta.quant_params(1, nQ, nKV, dim, 1000, bits, G, 0, 0, 0.1, 0)
-    prev = ta.ta_set_quant_path(0)
-    try:
-        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0            # 4 rows per KV row: CUDA cores
-        assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128)) == 1    # 16 rows per KV row
-        assert ta.quant_sdpa_uses_tensor_cores(p(512, nQ=256)) == 0
-        ta.ta_set_quant_path(2)
-        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 1
-        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=4)) == 1
-        assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8)) == 0       # rings exceed shared memory
-        assert ta.quant_sdpa_uses_tensor_cores(p(64, G=32)) == 1
-        assert ta.quant_sdpa_uses_tensor_cores(p(512)) == 0            # O alone fills TMEM
-        assert ta.quant_sdpa_uses_tensor_cores(p(96, G=32)) == 0       # not a multiple of 64
-        assert ta.quant_sdpa_uses_tensor_cores(p(256, G=16, nQ=256, bits=8)) == 0   # 16 groups x 32 rows
-        assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1           # invalid params
-        ta.ta_set_quant_path(1)
-        assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0
-    finally:
-        ta.ta_set_quant_path(prev)
+    def p(dim, G=64, nQ=32, nKV=8, bits=4, kernel=0):
+        return ta.quant_params(1, nQ, nKV, dim, 1000, bits, G, 0, 0, 0.1, 0, kernel)
+    assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0            # 4 rows per KV row: CUDA cores
+    assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128)) == 1    # 16 rows per KV row
+    assert ta.quant_sdpa_uses_tensor_cores(p(512, nQ=256)) == 0
+    assert ta.quant_sdpa_uses_tensor_cores(p(128, kernel=2)) == 1
+    assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=4, kernel=2)) == 1
+    assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8, kernel=2)) == 0       # rings exceed shared memory
+    assert ta.quant_sdpa_uses_tensor_cores(p(64, G=32, kernel=2)) == 1
+    assert ta.quant_sdpa_uses_tensor_cores(p(512, kernel=2)) == 0            # O alone fills TMEM
+    assert ta.quant_sdpa_uses_tensor_cores(p(96, G=32, kernel=2)) == 0       # not a multiple of 64
+    assert ta.quant_sdpa_uses_tensor_cores(p(256, G=16, nQ=256, bits=8, kernel=2)) == 0   # 16 groups x 32 rows
+    assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1           # invalid params
+    assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128, kernel=1)) == 0

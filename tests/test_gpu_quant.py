@@ -13,14 +13,17 @@ from helpers import assert_close, run_quant
 pytestmark = pytest.mark.gpu
 
 
-@pytest.fixture(scope="module", params=[2, 1], ids=["tensor_cores", "cuda_cores"])
-def ta(request):
+@pytest.fixture(scope="module")
+def ta():
+    import tree_masked_speculative_gb300 as m
+    return m
+
+
+@pytest.fixture(params=[2, 1], ids=["tensor_cores", "cuda_cores"])
+def kern(request):
     """Every test runs on both kernel families: the tensor-core kernel (where
     the shape allows it; others fall back to CUDA cores) and the CUDA-core one."""
-    import tree_masked_speculative_gb300 as m
-    prev = m.ta_set_quant_path(request.param)
-    yield m
-    m.ta_set_quant_path(prev)
+    return request.param
 
 
 def qwl(B=2, nQ=8, nKV=2, dim=128, N=300, bits=4, G=64, sinks=1, window=0, dtype="f16",
@@ -50,34 +53,34 @@ QCASES = [
 
 
 @pytest.mark.parametrize("kw", QCASES, ids=[str(i) for i in range(len(QCASES))])
-def test_quant_matches_oracle(ta, kw):
+def test_quant_matches_oracle(ta, kern, kw):
     wl = qwl(**kw)
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got32, ref, what="quant f32 out %r" % (kw,))
-    gotT = run_quant(ta, wl, inp).cpu().double().numpy()
+    gotT = run_quant(ta, wl, inp, kernel=kern).cpu().double().numpy()
     assert_close(gotT, ref, extra_ulp_dtype=wl.dtype, what="quant T out %r" % (kw,))
 
 
-def test_quant_no_visible_token_gives_zero_and_sink_only(ta):
+def test_quant_no_visible_token_gives_zero_and_sink_only(ta, kern):
     wl = qwl(N=70, sinks=1, bfrac=0.0, nwg=2)
     inp = W.make_quant_inputs(wl)
     inp["mask_bool"] = torch.ones((wl.rows, wl.tokens), dtype=torch.int32)
     inp["mask_bool"][3] = 0
-    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu()
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu()
     assert torch.all(got[3] == 0.0)
     wl0 = wl.with_(has_sinks=0)
-    got0 = run_quant(ta, wl0, inp, out_dtype=torch.float32).cpu()
+    got0 = run_quant(ta, wl0, inp, out_dtype=torch.float32, kernel=kern).cpu()
     assert torch.all(got0[3] == 0.0)
     assert_close(got.double().numpy(), oracle.quant_oracle_for(wl, inp))
 
 
-def test_quant_error_word_stays_clear(ta):
+def test_quant_error_word_stays_clear(ta, kern):
     wl = qwl(N=700, bits=8, dtype="bf16", fmask="alibi", bfrac=0.1, window=300)
     inp = W.make_quant_inputs(wl)
     p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits,
-                        wl.group_size, wl.has_sinks, wl.window_size, wl.scale, 0)
+                        wl.group_size, wl.has_sinks, wl.window_size, wl.scale, 0, kern)
     nb = ta.quant_sdpa_tmp_bytes(p)
     assert nb >= 256
     tmp = torch.zeros((nb + 3) // 4, dtype=torch.float32, device="cuda")
@@ -85,44 +88,44 @@ def test_quant_error_word_stays_clear(ta):
     out = ta.quant_sdpa(d, batch=wl.batch, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads,
                         dim=wl.dim, tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size,
                         has_sinks=wl.has_sinks, window_size=wl.window_size, scale=wl.scale,
-                        out_dtype=torch.float32, tmp=tmp)
+                        out_dtype=torch.float32, tmp=tmp, kernel=kern)
     torch.cuda.synchronize()
     assert int(tmp[:1].view(torch.int32).item()) == 0
     assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp))
 
 
-def test_quant_split_invariance(ta):
+def test_quant_split_invariance(ta, kern):
     wl = qwl(N=2000, bits=8, dtype="bf16")
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    outs = [run_quant(ta, wl, inp, nwg=n, out_dtype=torch.float32).cpu().double().numpy()
+    outs = [run_quant(ta, wl, inp, nwg=n, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
             for n in (1, 3, 15)]
     for o in outs:
         assert_close(o, ref)
 
 
-def test_quant_b4_workload_full(ta):
+def test_quant_b4_workload_full(ta, kern):
     wl = W.QUANT_B4
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, extra_ulp_dtype=wl.dtype, what="quant b4 workload")
-    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got32, ref, what="quant b4 workload f32")
 
 
-def test_quant_b8_masks_workload_full(ta):
+def test_quant_b8_masks_workload_full(ta, kern):
     wl = W.QUANT_B8_MASKS
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, extra_ulp_dtype=wl.dtype, what="quant b8 workload")
-    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got32 = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got32, ref, what="quant b8 workload f32")
 
 
 @pytest.mark.parametrize("bits,dtype", [(4, "f16"), (8, "bf16")])
-def test_quant_cache_verified_with_a_tree_mask(ta, bits, dtype):
+def test_quant_cache_verified_with_a_tree_mask(ta, kern, bits, dtype):
     """q_l draft-tree nodes per head verified against a quantized cache through
     the same call: the nodes are extra query rows (n_q_heads * q_l of them,
     ordered (batch, head, node), so each KV row serves heads_per_kv * q_l rows)
@@ -135,44 +138,95 @@ def test_quant_cache_verified_with_a_tree_mask(ta, bits, dtype):
     T = torch.float16 if dtype == "f16" else torch.bfloat16
     inp["mask_float"] = torch.from_numpy(np.tile(tm, (B * nQ, 1))).to(T)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, what="quant cache x tree mask")
     # the same token sets given as a bool mask instead of an additive one
     inp_b = dict(inp)
     del inp_b["mask_float"]
     inp_b["mask_bool"] = torch.from_numpy(np.tile((tm == 0.0).astype(np.int32), (B * nQ, 1)))
-    got_b = run_quant(ta, wl, inp_b, out_dtype=torch.float32).cpu().double().numpy()
+    got_b = run_quant(ta, wl, inp_b, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got_b, ref, what="quant cache x tree mask as a bool mask")
 
 
-def test_quant_many_rows_per_kv_row(ta):
+def test_quant_many_rows_per_kv_row(ta, kern):
     """48 query rows per KV row: two row blocks of the tensor-core kernel, a
     ragged last tile, a window that starts inside a tile, both masks."""
     wl = qwl(B=1, nQ=48, nKV=1, dim=128, N=777, bits=4, G=32, sinks=1, window=600, fmask="alibi",
              bfrac=0.2, dtype="bf16")
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, what="48 rows per KV row")
-    gotT = run_quant(ta, wl, inp).cpu().double().numpy()
+    gotT = run_quant(ta, wl, inp, kernel=kern).cpu().double().numpy()
     assert_close(gotT, ref, extra_ulp_dtype=wl.dtype, what="48 rows per KV row, T out")
 
 
-def test_quant_tree_workload_full(ta):
+def test_quant_tree_workload_full(ta, kern):
     """The draft-tree workload on a quantized cache at full size (256 rows over
     8 KV rows, 16384 tokens, per-row tree masks)."""
     wl = W.QUANT_TREE
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, what="quant tree workload f32")
 
 
-def test_quant_more_splits_than_tiles(ta):
+def test_quant_more_splits_than_tiles(ta, kern):
     """A forced split count above the number of 128-token tiles: the splits
     without a token leave an empty partial (S = 0) that the merge skips."""
     wl = qwl(N=200, nwg=5, sinks=1, dtype="bf16")
     inp = W.make_quant_inputs(wl)
     ref = oracle.quant_oracle_for(wl, inp)
-    got = run_quant(ta, wl, inp, nwg=5, out_dtype=torch.float32).cpu().double().numpy()
+    got = run_quant(ta, wl, inp, nwg=5, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
     assert_close(got, ref, what="more splits than tiles")
+
+
+@pytest.mark.parametrize("bits,dtype", [(8, "bf16"), (4, "f16")])
+def test_quant_peaked_softmax_plain_tolerance(ta, kern, bits, dtype):
+    """A peaked softmax with a running max that moves many times: 16 rows per KV
+    row (the tensor-core kernel's shape), queries scaled by 4 (exact in f16 /
+    bf16) and a large attention scale.  A single f16 P would move the output by
+    up to 2^-11 of the attended V spread (8-bit codes: V up to about 13); the
+    kernels are held to the plain tolerance."""
+    wl = qwl(B=1, nQ=32, nKV=2, dim=128, N=1200, bits=bits, G=64, sinks=1, dtype=dtype)
+    wl = wl.with_(scale=1.5)
+    inp = W.make_quant_inputs(wl)
+    inp["queries"] = inp["queries"] * 4.0
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern).cpu().double().numpy()
+    assert_close(got, ref, what="quant peaked softmax")
+
+
+def test_bounded_wait_timeout_sets_status_and_returns(ta):
+    """The failure path of the bounded waits, exercised without any fault: the
+    test hook gives every CTA's first K/V copy wait a bound of zero polls, so
+    it gives up at once.  Each CTA then ORs 1 into the status word, lets its
+    issued copies land (normal bound) and returns; the call completes, the
+    status is set, and the context stays usable for a normal call."""
+    wl = qwl(B=2, nQ=8, nKV=2, dim=128, N=2000, bits=4, G=64, sinks=1, dtype="f16")
+    inp = W.make_quant_inputs(wl)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    for nwg in (1, 0):
+        p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits, wl.group_size,
+                            wl.has_sinks, wl.window_size, wl.scale, nwg, 1)
+        nb = ta.quant_sdpa_tmp_bytes(p)
+        tmp = torch.zeros((nb + 3) // 4, dtype=torch.float32, device="cuda")
+        out = torch.zeros((wl.rows, wl.dim), dtype=torch.float32, device="cuda")
+        args = (d["queries"], d["k_packed"], d["k_scales"], d["k_biases"], d["v_packed"], d["v_scales"],
+                d["v_biases"], d["sinks"], None, None, tmp, out)
+        ta.ta_test_quant_sdpa_fwd_wait_limit(0, p, *args)
+        torch.cuda.synchronize()
+        assert int(tmp[:1].view(torch.int32).item()) & 1 == 1
+        tmp.zero_()
+        ta.quant_sdpa_fwd(p, *args)
+        torch.cuda.synchronize()
+        assert int(tmp[:1].view(torch.int32).item()) == 0
+        assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp), what="after a timeout")
+    # the hook refuses the tensor-core kernel
+    p2 = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits, wl.group_size,
+                         wl.has_sinks, wl.window_size, wl.scale, 0, 2)
+    tmp2 = torch.zeros((ta.quant_sdpa_tmp_bytes(p2) + 3) // 4, dtype=torch.float32, device="cuda")
+    before = ta.ta_launch_count()
+    with pytest.raises(ta.TreeAttentionError, match="CUDA-core kernel only"):
+        ta.ta_test_quant_sdpa_fwd_wait_limit(0, p2, *args[:-2], tmp2, out)
+    assert ta.ta_launch_count() == before

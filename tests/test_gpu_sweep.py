@@ -69,15 +69,11 @@ QUANT_SWEEP = [_quant_case(random.Random(2000 + i)) for i in range(18)]
 @pytest.mark.parametrize("path", [2, 1], ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("kw", QUANT_SWEEP, ids=[str(i) for i in range(len(QUANT_SWEEP))])
 def test_quant_sweep(ta, kw, path):
-    prev = ta.ta_set_quant_path(path)
-    try:
-        wl = W.QuantWorkload(name="sweep", scale=1.0 / math.sqrt(kw["dim"]), **kw)
-        inp = W.make_quant_inputs(wl)
-        ref = oracle.quant_oracle_for(wl, inp)
-        got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
-        assert_close(got, ref, what="quant sweep %r" % (kw,))
-    finally:
-        ta.ta_set_quant_path(prev)
+    wl = W.QuantWorkload(name="sweep", scale=1.0 / math.sqrt(kw["dim"]), **kw)
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=path).cpu().double().numpy()
+    assert_close(got, ref, what="quant sweep %r" % (kw,))
 
 
 def _layout_case(rng):
@@ -122,12 +118,8 @@ DRAFT_SWEEP = [_draft_tree_case(random.Random(4000 + i)) for i in range(10)]
 @pytest.mark.parametrize("path", [2, 1], ids=["tensor_cores", "cuda_cores"])
 @pytest.mark.parametrize("kw", DRAFT_SWEEP, ids=[str(i) for i in range(len(DRAFT_SWEEP))])
 def test_quant_draft_tree_sweep(ta, kw, path):
-    prev = ta.ta_set_quant_path(path)
-    try:
-        wl = W.QuantWorkload(name="sweep", scale=1.0 / math.sqrt(kw["dim"]), **kw)
-        inp = W.make_quant_inputs(wl)
-        ref = oracle.quant_oracle_for(wl, inp)
-        got = run_quant(ta, wl, inp, out_dtype=torch.float32).cpu().double().numpy()
-        assert_close(got, ref, what="quant draft-tree sweep %r" % (kw,))
-    finally:
-        ta.ta_set_quant_path(prev)
+    wl = W.QuantWorkload(name="sweep", scale=1.0 / math.sqrt(kw["dim"]), **kw)
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    got = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=path).cpu().double().numpy()
+    assert_close(got, ref, what="quant draft-tree sweep %r" % (kw,))

@@ -75,6 +75,40 @@ def test_tree_oracle_matches_torch_sdpa(kv_dtype, H, Hk, L):
     np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
 
 
+@pytest.mark.parametrize("kv_dtype", ["f32", "f16", "bf16"])
+@pytest.mark.parametrize("H,Hk,L", [(4, 2, 3), (6, 3, 5), (8, 1, 4)])
+def test_tree_oracle_additive_mask_matches_torch_sdpa_float_mask(kv_dtype, H, Hk, L):
+    """The mask is added to the scaled logit (mlx-native tree_attention.metal,
+    tree_attention_impl: logit = fma(qk, scale, mask)): finite, non-binary
+    cells shift the logits, cells <= -65504 drop the key.  torch SDPA with a
+    float attn_mask (the cell where attended, -inf where masked) computes the
+    same softmax; a 0 / -65504 mask could not tell adding from gating."""
+    D, N, C, stride = 8, 37, 45, 40
+    q, k, v, mask = _rand_tree_case(31 + H + L, H, Hk, D, N, C, L, stride, kv_dtype)
+    g = torch.Generator().manual_seed(77 + H)
+    bias = torch.rand((L, stride), generator=g) * 7.0 - 4.0          # U(-4, 3)
+    att = mask == 0.0
+    mask = torch.where(att, bias, mask)
+    mask[0, 1] = -1.0e30                                              # below -65504: masked too
+    mask[0, 0] = 2.5                                                  # row 0 keeps an attended key
+    scale = 0.37
+    got = oracle.tree_attention(q, k, v, mask, n_heads=H, n_kv_heads=Hk, head_dim=D, kv_seq_len=N,
+                                kv_capacity=C, scale=scale, q_l=L, mask_stride=stride, kv_dtype=kv_dtype)
+    fm = mask[:, :N].double()
+    fm = torch.where(fm <= W.MASKED, torch.tensor(-math.inf, dtype=torch.float64), fm)
+    qq = q.double().unsqueeze(0)
+    kk = k[:, :N].double().unsqueeze(0)
+    vv = v[:, :N].double().unsqueeze(0)
+    ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=fm.unsqueeze(0).unsqueeze(0), scale=scale,
+                                         enable_gqa=True)[0].permute(1, 0, 2).numpy()
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-12)
+    # and the bias matters: without it the result moves
+    plain = oracle.tree_attention(q, k, v, torch.where(mask > W.MASKED, torch.tensor(0.0), mask), n_heads=H,
+                                  n_kv_heads=Hk, head_dim=D, kv_seq_len=N, kv_capacity=C, scale=scale, q_l=L,
+                                  mask_stride=stride, kv_dtype=kv_dtype)
+    assert np.max(np.abs(plain - got)) > 1e-3
+
+
 def test_tree_oracle_row_subset_matches_full():
     H, Hk, D, N, C, L = 6, 2, 16, 50, 64, 4
     q, k, v, mask = _rand_tree_case(3, H, Hk, D, N, C, L, N, "f16")

@@ -91,3 +91,25 @@ def test_noalloc_rejects_requests_beyond_its_scratch(ta):
     st = ta.lib.tree_attn_fwd_noalloc(ctypes.byref(p), b, b, b, b, b, None)
     assert st == 4 and "static scratch" in ta.ta_last_error()
     assert ta.ta_launch_count() == before
+
+
+def test_noalloc_call_allocates_no_device_memory(ta):
+    """The defining claim: after a first call (which may load the module), a
+    call leaves the device's free memory unchanged.  Every tensor the calls use
+    exists before the first reading."""
+    wl = small_tree(H=24, Hk=4, D=256, N=1500, C=2048, L=32, kv_dtype="f16", nwg=8)
+    d = to_dev(W.make_tree_inputs(wl))
+    p = ta.tree_params(wl.n_heads, wl.n_kv_heads, wl.head_dim, wl.kv_seq_len, wl.kv_capacity,
+                       wl.scale, wl.q_l, wl.mask_stride, wl.nwg)
+    out = torch.empty((p.q_l, p.n_heads, p.head_dim), dtype=torch.float32, device="cuda")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    args = (ctypes.byref(p), ta.buf(d["q"]), ta.buf(d["k"]), ta.buf(d["v"]), ta.buf(d["mask"]), ta.buf(out),
+            stream)
+    assert ta.lib.tree_attn_fwd_noalloc(*args) == ta.TA_OK
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        assert ta.lib.tree_attn_fwd_noalloc(*args) == ta.TA_OK
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0

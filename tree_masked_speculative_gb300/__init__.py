@@ -19,14 +19,17 @@ from . import build as _build_mod
 __all__ = [
     "TA_OK", "TreeParams", "QuantParams", "TreeAttentionError", "lib", "library_path",
     "tree_attn_tmp_bytes", "tree_attn_num_splits", "tree_attn_workspace_bytes", "tree_attn_fwd",
-    "tree_attn_fwd_causal", "tree_attn_fwd_parents", "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
-    "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "ta_set_tree_path", "ta_set_quant_path",
-    "quant_sdpa_uses_tensor_cores", "tree_attention",
-    "quant_sdpa", "tree_params", "quant_params", "tree_mask_build",
+    "tree_attn_fwd_causal", "tree_attn_fwd_parents", "tree_attn_fwd_ex", "tree_attn_status_offset",
+    "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
+    "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "quant_sdpa_uses_tensor_cores",
+    "ta_test_quant_sdpa_fwd_wait_limit", "tree_attention", "quant_sdpa", "tree_params", "quant_params",
+    "tree_mask_build", "TreeOptions", "KERNEL_AUTO", "KERNEL_CUDA_CORES", "KERNEL_TENSOR_CORES",
 ]
 
 TA_OK = 0
 TA_F32, TA_F16, TA_BF16, TA_U32, TA_I32 = 0, 1, 2, 3, 4
+KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES = 0, 1, 2
+MASK_DENSE, MASK_CAUSAL, MASK_PARENTS = 0, 1, 2
 STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARGUMENT", 2: "TA_ERR_BUFFER_TOO_SMALL",
                 3: "TA_ERR_OVERFLOW", 4: "TA_ERR_UNSUPPORTED", 5: "TA_ERR_CUDA"}
 
@@ -54,7 +57,12 @@ class QuantParams(ctypes.Structure):
                 ("n_kv_heads", ctypes.c_uint32), ("dim", ctypes.c_uint32), ("tokens", ctypes.c_uint32),
                 ("bits", ctypes.c_uint32), ("group_size", ctypes.c_uint32),
                 ("has_sinks", ctypes.c_uint32), ("window_size", ctypes.c_uint32),
-                ("scale", ctypes.c_float), ("nwg", ctypes.c_uint32)]
+                ("scale", ctypes.c_float), ("nwg", ctypes.c_uint32), ("kernel", ctypes.c_uint32)]
+
+
+class TreeOptions(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("mask_kind", ctypes.c_int32), ("window_start", ctypes.c_uint32),
+                ("reserved", ctypes.c_int32)]
 
 
 def library_path() -> str:
@@ -83,6 +91,10 @@ def _load() -> ctypes.CDLL:
     L.tree_attn_fwd_causal.restype = ctypes.c_int
     L.tree_attn_fwd_parents.argtypes = [PT, B, B, B, B, B, B, P]
     L.tree_attn_fwd_parents.restype = ctypes.c_int
+    L.tree_attn_fwd_ex.argtypes = [PT, ctypes.POINTER(TreeOptions), B, B, B, B, B, B, P]
+    L.tree_attn_fwd_ex.restype = ctypes.c_int
+    L.tree_attn_status_offset.argtypes = [PT]
+    L.tree_attn_status_offset.restype = ctypes.c_size_t
     L.tree_attn_reduce.argtypes = [PT, B, B, P]
     L.tree_attn_reduce.restype = ctypes.c_int
     L.tree_attn_fwd_noalloc.argtypes = [PT, B, B, B, B, B, P]
@@ -97,10 +109,8 @@ def _load() -> ctypes.CDLL:
     L.ta_last_error.restype = ctypes.c_char_p
     L.ta_launch_count.argtypes = []
     L.ta_launch_count.restype = ctypes.c_uint64
-    L.ta_set_tree_path.argtypes = [ctypes.c_int]
-    L.ta_set_tree_path.restype = ctypes.c_int
-    L.ta_set_quant_path.argtypes = [ctypes.c_int]
-    L.ta_set_quant_path.restype = ctypes.c_int
+    L.ta_test_quant_sdpa_fwd_wait_limit.argtypes = [u32, PQ] + [B] * 12 + [P]
+    L.ta_test_quant_sdpa_fwd_wait_limit.restype = ctypes.c_int
     L.quant_sdpa_uses_tensor_cores.argtypes = [PQ]
     L.quant_sdpa_uses_tensor_cores.restype = ctypes.c_int
     L.tree_mask_build.argtypes = [PT, B, B, P]
@@ -156,14 +166,6 @@ def ta_launch_count() -> int:
     return int(lib.ta_launch_count())
 
 
-def ta_set_tree_path(path: int) -> int:
-    return int(lib.ta_set_tree_path(path))
-
-
-def ta_set_quant_path(path: int) -> int:
-    return int(lib.ta_set_quant_path(path))
-
-
 def quant_sdpa_uses_tensor_cores(p: QuantParams) -> int:
     return int(lib.quant_sdpa_uses_tensor_cores(ctypes.byref(p)))
 
@@ -175,9 +177,9 @@ def tree_params(n_heads, n_kv_heads, head_dim, kv_seq_len, kv_capacity, scale, q
 
 
 def quant_params(batch, n_q_heads, n_kv_heads, dim, tokens, bits, group_size, has_sinks,
-                 window_size, scale, nwg=0) -> QuantParams:
+                 window_size, scale, nwg=0, kernel=KERNEL_AUTO) -> QuantParams:
     return QuantParams(batch, n_q_heads, n_kv_heads, dim, tokens, bits, group_size, has_sinks,
-                       window_size, scale, nwg)
+                       window_size, scale, nwg, kernel)
 
 
 def tree_attn_tmp_bytes(n_heads: int, head_dim: int, q_l: int, nwg: int) -> int:
@@ -207,6 +209,20 @@ def tree_attn_fwd_causal(p: TreeParams, window_start: int, q, k, v, tmp, out, st
                                     buf(tmp), buf(out), _stream(stream)))
 
 
+def tree_attn_fwd_ex(p: TreeParams, kernel: int, mask_kind: int, window_start: int, q, k, v, mask, tmp, out,
+                     stream=None):
+    """Main pass with an explicit kernel family (KERNEL_*) and mask form (MASK_*:
+    `mask` is the dense mask, unused, or the int32 parent array)."""
+    o = TreeOptions(kernel, mask_kind, window_start, 0)
+    m = buf(mask, TA_I32) if mask_kind == MASK_PARENTS else (buf(mask) if mask_kind == MASK_DENSE else None)
+    _check(lib.tree_attn_fwd_ex(ctypes.byref(p), ctypes.byref(o), buf(q), buf(k), buf(v), m, buf(tmp), buf(out),
+                                _stream(stream)))
+
+
+def tree_attn_status_offset(p: TreeParams) -> int:
+    return int(lib.tree_attn_status_offset(ctypes.byref(p)))
+
+
 def tree_attn_reduce(p: TreeParams, tmp, out, stream=None):
     _check(lib.tree_attn_reduce(ctypes.byref(p), buf(tmp), buf(out), _stream(stream)))
 
@@ -226,12 +242,29 @@ def quant_sdpa_tmp_bytes(p: QuantParams) -> int:
     return int(lib.quant_sdpa_tmp_bytes(ctypes.byref(p)))
 
 
+def _quant_bufs(queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool,
+                mask_float, tmp, out):
+    return (buf(queries), buf(k_packed, TA_U32), buf(k_scales), buf(k_biases), buf(v_packed, TA_U32),
+            buf(v_scales), buf(v_biases), buf(sinks), buf(mask_bool, TA_U32) if mask_bool is not None else None,
+            buf(mask_float), buf(tmp), buf(out))
+
+
 def quant_sdpa_fwd(p: QuantParams, queries, k_packed, k_scales, k_biases, v_packed, v_scales,
                    v_biases, sinks, mask_bool, mask_float, tmp, out, stream=None):
-    _check(lib.quant_sdpa_fwd(ctypes.byref(p), buf(queries), buf(k_packed, TA_U32), buf(k_scales),
-                              buf(k_biases), buf(v_packed, TA_U32), buf(v_scales), buf(v_biases),
-                              buf(sinks), buf(mask_bool, TA_U32) if mask_bool is not None else None,
-                              buf(mask_float), buf(tmp), buf(out), _stream(stream)))
+    _check(lib.quant_sdpa_fwd(ctypes.byref(p), *_quant_bufs(queries, k_packed, k_scales, k_biases, v_packed,
+                                                            v_scales, v_biases, sinks, mask_bool, mask_float,
+                                                            tmp, out), _stream(stream)))
+
+
+def ta_test_quant_sdpa_fwd_wait_limit(first_wait_polls: int, p: QuantParams, queries, k_packed, k_scales,
+                                      k_biases, v_packed, v_scales, v_biases, sinks, mask_bool, mask_float, tmp,
+                                      out, stream=None):
+    """Test hook: quant_sdpa_fwd (CUDA-core kernel) whose first copy wait per CTA
+    gives up after `first_wait_polls` polls (0: at once)."""
+    _check(lib.ta_test_quant_sdpa_fwd_wait_limit(first_wait_polls, ctypes.byref(p),
+                                                 *_quant_bufs(queries, k_packed, k_scales, k_biases, v_packed,
+                                                              v_scales, v_biases, sinks, mask_bool, mask_float,
+                                                              tmp, out), _stream(stream)))
 
 
 # ------------------------------------------------------------- conveniences
@@ -239,11 +272,12 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
                    *, n_heads: int, n_kv_heads: int, kv_seq_len: int, scale: float,
                    mask_stride: Optional[int] = None, nwg: int = 0, window_start: int = 0,
                    tmp: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
-                   parents: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                   parents: Optional[torch.Tensor] = None, kernel: int = KERNEL_AUTO,
+                   stream=None) -> torch.Tensor:
     """One verify step (main pass + reduce) on device tensors.  mask=None uses the
     implicit causal mask starting at window_start, or, with `parents` (int32
-    [q_l] on the device), the tree mask of that parent array.  Returns out
-    [q_l, n_heads, D]."""
+    [q_l] on the device), the tree mask of that parent array.  `kernel` picks
+    the main pass's kernel family (KERNEL_*).  Returns out [q_l, n_heads, D]."""
     H, L, D = q.shape
     C = k.shape[1]
     stride = mask_stride if mask_stride is not None else (mask.shape[1] if mask is not None else kv_seq_len)
@@ -258,11 +292,11 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
     if parents is not None:
         if mask is not None:
             raise ValueError("give either a dense mask or a parent array, not both")
-        tree_attn_fwd_parents(p, parents, q, k, v, tmp, out, stream)
+        tree_attn_fwd_ex(p, kernel, MASK_PARENTS, 0, q, k, v, parents, tmp, out, stream)
     elif mask is None:
-        tree_attn_fwd_causal(p, window_start, q, k, v, tmp, out, stream)
+        tree_attn_fwd_ex(p, kernel, MASK_CAUSAL, window_start, q, k, v, None, tmp, out, stream)
     else:
-        tree_attn_fwd(p, q, k, v, mask, tmp, out, stream)
+        tree_attn_fwd_ex(p, kernel, MASK_DENSE, 0, q, k, v, mask, tmp, out, stream)
     tree_attn_reduce(p, tmp, out, stream)
     return out
 
@@ -270,10 +304,10 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
 def quant_sdpa(inputs: dict, *, batch: int, n_q_heads: int, n_kv_heads: int, dim: int, tokens: int,
                bits: int, group_size: int, has_sinks: int, window_size: int, scale: float,
                nwg: int = 0, out_dtype: Optional[torch.dtype] = None, tmp=None, out=None,
-               stream=None) -> torch.Tensor:
+               kernel: int = KERNEL_AUTO, stream=None) -> torch.Tensor:
     """Quantized-KV attention on device tensors (dict as made by workloads.make_quant_inputs)."""
     p = quant_params(batch, n_q_heads, n_kv_heads, dim, tokens, bits, group_size, has_sinks,
-                     window_size, scale, nwg)
+                     window_size, scale, nwg, kernel)
     dev = inputs["queries"].device
     if tmp is None:
         nb = quant_sdpa_tmp_bytes(p)

@@ -28,8 +28,6 @@ namespace {
 
 thread_local std::string g_err;
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_tree_path{0};
-std::atomic<int> g_quant_path{0};   // 0 auto, 1 CUDA cores, 2 tensor cores where the shape allows
 constexpr int kQuantTcMinRows = 16;  // automatic choice: tensor cores from this many rows per KV row
 
 ta_status fail(ta_status st, const char *fmt, ...) {
@@ -235,9 +233,11 @@ bool encode_map(CUtensorMap *m, bool bf16, void *ptr, int rank, const cuuint64_t
                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, const ta_buf *v,
+ta_status plan_tree(const ta_tree_params *p, int kernel, const ta_buf *q, const ta_buf *k, const ta_buf *v,
                     const ta_buf *mask, const ta_buf *tmp, const ta_buf *out, int window_start,
                     TreePlan *plan, const ta_buf *parents = nullptr) {
+    if (kernel < TA_KERNEL_AUTO || kernel > TA_KERNEL_TENSOR_CORES)
+        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: kernel must be 0 (auto), 1 or 2, got %d", kernel);
     TA_TRY(check_tree_params(p, mask != nullptr));
     if (parents) {
         TA_TRY(check_dtype(*parents, "parents", TA_I32));
@@ -317,8 +317,7 @@ ta_status plan_tree(const ta_tree_params *p, const ta_buf *q, const ta_buf *k, c
     plan->v = v->ptr;
     // Tensor cores when the K/V type is 16-bit and a KV head serves >= 16 query
     // rows (a dense contraction); otherwise the CUDA-core kernel.
-    const int path = g_tree_path.load(std::memory_order_relaxed);
-    plan->use_tc = path != 1 && plan->kv_type != kKvF32 && a.R >= 16;
+    plan->use_tc = kernel != TA_KERNEL_CUDA_CORES && plan->kv_type != kKvF32 && a.R >= 16;
     a.q16_type = plan->use_tc ? plan->kv_type : -1;
     // partial slots left for the merge pass (0 = the main pass writes the output)
     a.cluster_x = 1;
@@ -377,6 +376,8 @@ ta_status check_quant_params(const ta_quant_params *p) {
                     p->group_size);
     if (p->tokens == 0) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: tokens must be > 0");
     if (p->has_sinks > 1) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: has_sinks must be 0 or 1");
+    if (p->kernel > (uint32_t)TA_KERNEL_TENSOR_CORES)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: kernel must be 0 (auto), 1 or 2, got %u", p->kernel);
     if (!std::isfinite(p->scale)) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: scale is not finite");
     if (p->group_size % (4 * pf) != 0)
         return fail(TA_ERR_UNSUPPORTED,
@@ -417,13 +418,13 @@ struct QtcShape {
     int rr, rp, n_rb, cols;   // rows per CTA, MMA N (max(16, rr)), row blocks, TMEM columns
 };
 bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
-    const int path = g_quant_path.load(std::memory_order_relaxed);
-    if (path == 1) return false;
+    const int path = (int)p->kernel;
+    if (path == TA_KERNEL_CUDA_CORES) return false;
     if (p->dim != 64 && p->dim != 128 && p->dim != 256) return false;
     const int rep = (int)(p->n_q_heads / p->n_kv_heads);
     // automatic choice: the tensor-core kernel from 16 query rows per KV row
     // (draft-tree verification), where the CUDA-core kernel's per-row work dominates
-    if (path == 0 && rep < kQuantTcMinRows) return false;
+    if (path == TA_KERNEL_AUTO && rep < kQuantTcMinRows) return false;
     const int ng = (int)(p->dim / p->group_size);
     const int wpt = (int)(p->dim * p->bits / 32);
     if (wpt % 4 != 0 || p->group_size % 16 != 0) return false;
@@ -557,33 +558,64 @@ TA_EXPORT size_t tree_attn_workspace_bytes(const ta_tree_params *p) {
     return ws.total;
 }
 
+TA_EXPORT ta_status tree_attn_fwd_ex(const ta_tree_params *p, const ta_tree_options *o, const ta_buf *q,
+                                     const ta_buf *k, const ta_buf *v, const ta_buf *mask, const ta_buf *tmp,
+                                     const ta_buf *out, void *stream) {
+    if (o == nullptr) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: options is NULL");
+    if (o->reserved != 0) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: options.reserved must be 0");
+    TreePlan plan;
+    switch (o->mask_kind) {
+        case TA_MASK_DENSE:
+            if (absent(mask)) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: TA_MASK_DENSE needs a mask");
+            TA_TRY(plan_tree(p, o->kernel, &deref(q), &deref(k), &deref(v), mask, &deref(tmp), &deref(out), 0,
+                             &plan));
+            break;
+        case TA_MASK_CAUSAL:
+            if (o->window_start > (uint32_t)INT_MAX)
+                return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: window_start out of range");
+            TA_TRY(plan_tree(p, o->kernel, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out),
+                             (int)o->window_start, &plan));
+            break;
+        case TA_MASK_PARENTS:
+            if (absent(mask)) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: TA_MASK_PARENTS needs parents");
+            TA_TRY(plan_tree(p, o->kernel, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out), 0,
+                             &plan, mask));
+            break;
+        default:
+            return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: unknown mask_kind %d", o->mask_kind);
+    }
+    return run_tree(plan, static_cast<cudaStream_t>(stream));
+}
+
 TA_EXPORT ta_status tree_attn_fwd(const ta_tree_params *p, const ta_buf *q, const ta_buf *k,
                                   const ta_buf *v, const ta_buf *mask, const ta_buf *tmp,
                                   const ta_buf *out, void *stream) {
-    TreePlan plan;
-    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), absent(mask) ? nullptr : mask, &deref(tmp),
-                     &deref(out), 0, &plan));
-    return run_tree(plan, static_cast<cudaStream_t>(stream));
+    const ta_tree_options o = {TA_KERNEL_AUTO, absent(mask) ? TA_MASK_CAUSAL : TA_MASK_DENSE, 0, 0};
+    return tree_attn_fwd_ex(p, &o, q, k, v, mask, tmp, out, stream);
 }
 
 TA_EXPORT ta_status tree_attn_fwd_causal(const ta_tree_params *p, uint32_t window_start, const ta_buf *q,
                                          const ta_buf *k, const ta_buf *v, const ta_buf *tmp,
                                          const ta_buf *out, void *stream) {
-    if (window_start > (uint32_t)INT_MAX)
-        return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: window_start out of range");
-    TreePlan plan;
-    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out),
-                     (int)window_start, &plan));
-    return run_tree(plan, static_cast<cudaStream_t>(stream));
+    const ta_tree_options o = {TA_KERNEL_AUTO, TA_MASK_CAUSAL, window_start, 0};
+    return tree_attn_fwd_ex(p, &o, q, k, v, nullptr, tmp, out, stream);
 }
 
 TA_EXPORT ta_status tree_attn_fwd_parents(const ta_tree_params *p, const ta_buf *parents, const ta_buf *q,
                                           const ta_buf *k, const ta_buf *v, const ta_buf *tmp, const ta_buf *out,
                                           void *stream) {
-    TreePlan plan;
-    TA_TRY(plan_tree(p, &deref(q), &deref(k), &deref(v), nullptr, &deref(tmp), &deref(out), 0, &plan,
-                     &deref(parents)));
-    return run_tree(plan, static_cast<cudaStream_t>(stream));
+    if (absent(parents)) return fail(TA_ERR_INVALID_ARGUMENT, "tree_attention: parents is NULL");
+    const ta_tree_options o = {TA_KERNEL_AUTO, TA_MASK_PARENTS, 0, 0};
+    return tree_attn_fwd_ex(p, &o, q, k, v, parents, tmp, out, stream);
+}
+
+TA_EXPORT size_t tree_attn_status_offset(const ta_tree_params *p) {
+    if (check_tree_params(p, false) != TA_OK) return SIZE_MAX;
+    const uint32_t nwg = resolve_tree_nwg(p);
+    if (nwg == 0) return SIZE_MAX;
+    TreeWorkspace ws;
+    if (!tree_workspace(p, nwg, &ws)) return SIZE_MAX;
+    return ws.off_err;
 }
 
 TA_EXPORT ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp_d, const ta_buf *out_d,
@@ -652,11 +684,16 @@ TA_EXPORT size_t quant_sdpa_tmp_bytes(const ta_quant_params *p) {
     return (size_t)b;
 }
 
-TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries_d, const ta_buf *k_packed_d,
-                                   const ta_buf *k_scales_d, const ta_buf *k_biases_d, const ta_buf *v_packed_d,
-                                   const ta_buf *v_scales_d, const ta_buf *v_biases_d, const ta_buf *sinks_d,
-                                   const ta_buf *mask_bool_d, const ta_buf *mask_float_d, const ta_buf *tmp_d,
-                                   const ta_buf *out_d, void *stream) {
+namespace {
+
+// quant_sdpa_fwd; first_wait_polls bounds the first copy wait of every CTA of
+// the CUDA-core kernel (the normal bound for a regular call), and a call with
+// a shorter bound must take that kernel.
+ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, const ta_buf *k_packed_d,
+                         const ta_buf *k_scales_d, const ta_buf *k_biases_d, const ta_buf *v_packed_d,
+                         const ta_buf *v_scales_d, const ta_buf *v_biases_d, const ta_buf *sinks_d,
+                         const ta_buf *mask_bool_d, const ta_buf *mask_float_d, const ta_buf *tmp_d,
+                         const ta_buf *out_d, void *stream, uint32_t first_wait_polls, bool test_hook) {
     const ta_buf &queries = deref(queries_d), &k_packed = deref(k_packed_d), &k_scales = deref(k_scales_d);
     const ta_buf &k_biases = deref(k_biases_d), &v_packed = deref(v_packed_d), &v_scales = deref(v_scales_d);
     const ta_buf &v_biases = deref(v_biases_d), &sinks = deref(sinks_d), &mask_bool = deref(mask_bool_d);
@@ -760,7 +797,12 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     cudaError_t e;
     QtcShape sh;
     QtcPlan pl;
-    if (quant_tc_shape(p, &sh) && quant_tc_plan(p, sh, has_bool, has_float, &pl)) {
+    a.first_wait_polls = first_wait_polls;
+    const bool use_tc = quant_tc_shape(p, &sh) && quant_tc_plan(p, sh, has_bool, has_float, &pl);
+    if (test_hook && use_tc)
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: the wait-limit test hook takes the CUDA-core kernel only "
+                    "(set kernel = 1)");
+    if (use_tc) {
         uint32_t j_lo;
         a.ntile = (int)window_tiles(p, &j_lo);
         a.j_lo = (int)j_lo;
@@ -784,19 +826,31 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
     return TA_OK;
 }
 
+}  // namespace
+
+TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries, const ta_buf *k_packed,
+                                   const ta_buf *k_scales, const ta_buf *k_biases, const ta_buf *v_packed,
+                                   const ta_buf *v_scales, const ta_buf *v_biases, const ta_buf *sinks,
+                                   const ta_buf *mask_bool, const ta_buf *mask_float, const ta_buf *tmp,
+                                   const ta_buf *out, void *stream) {
+    return quant_fwd_impl(p, queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool,
+                          mask_float, tmp, out, stream, kQuantWaitPolls, false);
+}
+
+TA_EXPORT ta_status ta_test_quant_sdpa_fwd_wait_limit(uint32_t first_wait_polls, const ta_quant_params *p,
+                                                      const ta_buf *queries, const ta_buf *k_packed,
+                                                      const ta_buf *k_scales, const ta_buf *k_biases,
+                                                      const ta_buf *v_packed, const ta_buf *v_scales,
+                                                      const ta_buf *v_biases, const ta_buf *sinks,
+                                                      const ta_buf *mask_bool, const ta_buf *mask_float,
+                                                      const ta_buf *tmp, const ta_buf *out, void *stream) {
+    return quant_fwd_impl(p, queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool,
+                          mask_float, tmp, out, stream, first_wait_polls, true);
+}
+
 TA_EXPORT const char *ta_last_error(void) { return g_err.c_str(); }
 
 TA_EXPORT uint64_t ta_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
-
-TA_EXPORT int ta_set_tree_path(int path) {
-    if (path < 0 || path > 2) return -1;
-    return g_tree_path.exchange(path);
-}
-
-TA_EXPORT int ta_set_quant_path(int path) {
-    if (path < 0 || path > 2) return -1;
-    return g_quant_path.exchange(path);
-}
 
 TA_EXPORT int quant_sdpa_uses_tensor_cores(const ta_quant_params *p) {
     if (check_quant_params(p) != TA_OK) return -1;

@@ -9,14 +9,15 @@
 // file-scope device array instead of a caller-provided tmp buffer.
 //
 // The array is 16 MiB and is held on every GPU that loads the library until
-// the process exits.  Its device address is looked up once per device, on the
-// first call made with that device current; make that first call before any
+// the process exits.  Its device address belongs to the CUDA context, not to
+// the device number (a cudaDeviceReset, or another context made current on the
+// same device, reloads the module at a new address), so every call asks the
+// runtime for it (cudaGetSymbolAddress allocates nothing).  The first call in
+// a context also loads the module there; make that first call before any
 // stream capture.  Every call shares the one array and leaves the last call's
 // contents in it: nothing in it needs to start at zero (each call writes every
 // partial and class it later reads), but calls whose work overlaps on the GPU
 // (other streams, or graphs replayed concurrently) race on it.
-#include <mutex>
-
 #include "ta_internal.cuh"
 #include "tree_attn.h"
 
@@ -29,23 +30,14 @@ constexpr size_t kStaticScratchBytes = size_t(16) << 20;
 
 __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
 
-std::mutex g_scratch_mu;
-void *g_scratch_addr[64];   // per device; host code may not use the symbol itself
-
-// Device address of g_static_scratch on the current device (set up on first use).
+// Device address of g_static_scratch in the current context.  Host code may
+// not use the symbol itself: its host-side name is a stand-in, not a device
+// address.
 cudaError_t static_scratch_address(void **out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_scratch_mu);
-    if (g_scratch_addr[dev] == nullptr) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_static_scratch);
-        if (e != cudaSuccess) return e;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    *out = p;
     return cudaSuccess;
 }
 

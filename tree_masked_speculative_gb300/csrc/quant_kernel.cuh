@@ -45,7 +45,6 @@ using namespace ta::sm100;
 
 constexpr int REP = kQuantRowsPerCta;   // query rows of one row group
 constexpr int DPL = 16;                 // score pass: dimensions per lane (q regs = DPL * REP)
-constexpr uint32_t kWaitPolls = 1u << 22;   // bound of every mbarrier wait
 constexpr float kSlack = 8.0f;              // lazy-max slack (log2 units)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kTwo23 = 8388608.0f;   // 2^23: the float whose low mantissa bits hold a code
@@ -93,8 +92,8 @@ __device__ __forceinline__ void cp_arrive_noinc(uint64_t *bar) {
 }
 
 // Bounded wait of every lane on an mbarrier phase; the result is uniform.
-__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity) {
-    return __all_sync(0xffffffffu, mbar_wait(bar, parity, kWaitPolls));
+__device__ __forceinline__ bool wait_warp(uint64_t *bar, uint32_t parity, uint32_t polls = kQuantWaitPolls) {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, polls));
 }
 
 template <typename T>
@@ -350,7 +349,9 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     for (int i = 0; i < nc; ++i) {
         const int c = c_begin + i, b = i & 1;
         const uint32_t par = static_cast<uint32_t>(i >> 1) & 1u;
-        if (!wait_warp(&bars[b], par)) { ok = false; break; }   // group A of chunk c
+        // group A of chunk c (the first wait's bound is a parameter: a test
+        // makes it time out to exercise this failure path)
+        if (!wait_warp(&bars[b], par, i == 0 ? a.first_wait_polls : kQuantWaitPolls)) { ok = false; break; }
         ++a_done;
         __syncwarp();
         const unsigned char *st = smem + L.a0 + b * L.a_stage;

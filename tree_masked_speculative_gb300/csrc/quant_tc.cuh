@@ -461,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             auto issue_pv = [&](int t) -> bool {
                 if (!wait1(bars, &bars->p_full[t & 1], (static_cast<uint32_t>(t) >> 1) & 1u, err)) return false;
                 tc_fence_after();
-                const uint32_t pa = p_addr + (t & 1) * 2 * L.pkb;
+                const uint32_t pa = p_addr + (t & 1) * 4 * L.pkb;   // P_hi k-blocks, then P_lo
                 // O^T[128 dims][rows] += V^T P^T per 128-dimension block: its two
                 // 64-dimension chunks sit in adjacent ring slots (the V ring holds
                 // an even number of chunks and a tile part starts on an even one)
@@ -470,9 +470,14 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                     if (!take(1, &ca)) return false;
                     if (NCH > 1 && !take_next(1)) return false;
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ss(tm_o + static_cast<uint32_t>(mb * RP), sw128_desc_at(vmn, ca + kk * 2048),
-                                   sw128_desc_at(kmaj, pa + (kk >> 2) * L.pkb + (kk & 3) * 32), id_pv, (t | kk) != 0);
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint64_t vd = sw128_desc_at(vmn, ca + kk * 2048);
+                        const uint32_t pk = pa + (kk >> 2) * L.pkb + (kk & 3) * 32;
+                        mma_f16_ss(tm_o + static_cast<uint32_t>(mb * RP), vd, sw128_desc_at(kmaj, pk), id_pv,
+                                   (t | kk) != 0);
+                        mma_f16_ss(tm_o + static_cast<uint32_t>(mb * RP), vd, sw128_desc_at(kmaj, pk + 2 * L.pkb),
+                                   id_pv, 1u);
+                    }
                     give(1);
                     if (NCH > 1) give(1);
                 }
@@ -675,16 +680,26 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                     tmem_wait_st();
                 }
             }
-            unsigned char *pb = smem + L.p0 + sb * 2 * L.pkb + (tl >> 6) * L.pkb;
+            // P as two f16 terms, P_hi = rn(P) and P_lo = rn(P - P_hi) (the
+            // difference is exact in f32), in the P_hi and P_lo k-blocks of the
+            // buffer: one f16 P would move the output by up to 2^-11 of the
+            // spread of the attended V values, the pair by less than 2^-22.
+            // The row sums add P in f32.
+            unsigned char *pb = smem + L.p0 + sb * 4 * L.pkb + (tl >> 6) * L.pkb;
             const int tc = tl & 63;
 #pragma unroll
             for (int r = 0; r < RH; ++r) {
                 const int row = hr0 + r;
                 const float m = __shfl_sync(0xffffffffu, m_row, r);
-                const __half ph = __float2half_rn(ex2(lg[r] - (m == -INFINITY ? 0.0f : m)));
-                lsum[r] += __half2float(ph);
-                if (row < rows_here)
-                    *reinterpret_cast<__half *>(pb + row * 128 + (((tc >> 3) ^ (row & 7)) << 4) + (tc & 7) * 2) = ph;
+                const float pf = ex2(lg[r] - (m == -INFINITY ? 0.0f : m));
+                const __half ph = __float2half_rn(pf);
+                const __half pl = __float2half_rn(pf - __half2float(ph));
+                lsum[r] += pf;
+                if (row < rows_here) {
+                    const int off = row * 128 + (((tc >> 3) ^ (row & 7)) << 4) + (tc & 7) * 2;
+                    *reinterpret_cast<__half *>(pb + off) = ph;
+                    *reinterpret_cast<__half *>(pb + 2 * L.pkb + off) = pl;
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();

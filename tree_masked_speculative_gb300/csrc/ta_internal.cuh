@@ -168,6 +168,7 @@ struct QuantArgs {
     int al_mb;               // bool-mask chunks start on 16-byte boundaries
     int al_mf;               // float-mask chunks start on 16-byte boundaries
     int *err;                // error word (bit 0: a copy wait timed out), never cleared here
+    uint32_t first_wait_polls;   // CUDA-core kernel: bound of each CTA's first copy wait
     int t_is_bf16, out_f32;
     float scale;
     // tensor-core kernel only: rows per CTA (4, 8, 16 or 32), row blocks per KV row,
@@ -176,6 +177,8 @@ struct QuantArgs {
     int rp, n_rb, j_lo, ntile, tc_nd, tc_nk, tc_nv, tc_cols;
 };
 
+// Bound (polls) of every mbarrier wait of the CUDA-core quantized-KV kernel.
+constexpr uint32_t kQuantWaitPolls = 1u << 22;
 // Query rows served by one CTA of the quantized-KV kernel (a row group).
 constexpr int kQuantRowsPerCta = 4;
 // Dynamic shared-memory limit requested for the quantized-KV kernels.
@@ -228,7 +231,8 @@ __host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
 }
 // Shared-memory layout of the tensor-core quantized-KV kernel (byte offsets).
 // Two P buffers (the PV operand P^T: [rp rows][128 tokens] 16-bit, 128-byte
-// swizzled, two 64-token k-blocks of rp * 128 bytes; rows past the CTA's
+// swizzled, two 64-token k-blocks of rp * 128 bytes for P_hi, then two for
+// P_lo; rows past the CTA's
 // query rows are never written and only feed O^T columns that are never
 // read), the 16-bit Q operand ([rp][dim], 64-dimension blocks), the ring of
 // decoded 16 KB chunks ([128 tokens][64 dims] f16: K half, V half), the
@@ -252,7 +256,7 @@ __host__ __device__ inline QtcLayout qtc_layout(int rp, int dim, int wpt, int ng
     L.pkb = rp * 128;
     int o = 0;
     L.p0 = o;
-    o += 4 * L.pkb;
+    o += 8 * L.pkb;
     o = qtc_align(o, 1024);
     L.q0 = o;
     o += (dim / 64) * rp * 128;
@@ -306,8 +310,7 @@ struct TreeWorkspace {
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
 cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s);
-// Cluster shape of the tensor-core kernel: x = splits merged in-cluster, y = the
-// row tiles and O halves that share K/V through multicast.
+// Cluster shape of the tensor-core kernel: x = splits merged in-cluster (y = 1).
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);
 // Dense tree mask [q_l, stride] f32 from parents [q_l] (device pointers).

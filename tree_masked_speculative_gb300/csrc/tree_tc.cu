@@ -18,15 +18,24 @@
 //                (dead chunks are never loaded); empty slots and keys past
 //                kv_seq_len are loaded out of bounds, i.e. as zeros.
 //   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
-//                TMEM, double buffered) and O += P_t V_t (M 128, N 64 per V slab,
-//                P read from TMEM where the softmax left it over S_t, V MN-major);
-//                a buffer is released for S_t+2 when PV_t completes.
-//   warps 2..5 : one thread per row: mask + scale, online softmax with lazy
-//                rescaling (M only moves when a row max exceeds it by more
-//                than e^8, so O in TMEM is rarely touched), P as
-//                16-bit pairs back into TMEM, epilogue from TMEM.
+//                TMEM, double buffered) and O += P_t V_t (M 128, N = 64 per V
+//                slab, up to 256 over slabs in consecutive ring slots; P read
+//                from TMEM where the softmax left it over S_t, V MN-major); a
+//                buffer is released for S_t+2 when PV_t completes.
+//   warps 2..9 : two warps per TMEM lane quarter: mask + scale, online softmax
+//                with lazy rescaling (M only moves when a row max exceeds it by
+//                more than e^8, so O in TMEM is rarely touched), P back into
+//                TMEM as two 16-bit terms P = P_hi + P_lo, epilogue from TMEM.
+// P in two terms: the tensor core takes 16-bit operands, and a single 16-bit
+// P carries a relative rounding error of up to 2^-8 (bf16) or 2^-11 (f16),
+// which moves the output by up to that fraction of the spread of the attended
+// V rows - above the 2e-3 tolerance on a peaked softmax.  P_hi = rn16(P) and
+// P_lo = rn16(P - P_hi) (the difference is exact in f32) leave a relative
+// error below 2^-16 (bf16) or 2^-22 (f16); PV runs once per term.
 // Every mbarrier wait is bounded; on a timeout the CTA sets the workspace
 // error word, drains its outstanding copies and MMAs, frees TMEM and exits.
+// Every CTA loads its own K/V slabs (a row tile's second read of a slab is
+// usually an L2 hit).
 #include "sm100_ptx.cuh"
 #include "ta_internal.cuh"
 
@@ -48,7 +57,11 @@ struct TcCfg {
     static constexpr int DV = D < 256 ? D : 256;     // O columns per CTA
     static constexpr int NSK = D / 64;               // K slabs per key tile
     static constexpr int NSV = DV / 64;              // V slabs per key tile
-    static constexpr int STAGES = D == 512 ? 6 : (D == 256 ? 10 : 12);
+    // Ring depth.  Every key tile advances the ring by NSK + NSV slots and a V
+    // group starts NSK-aligned, so with these depths a tile's V slabs sit in
+    // runs of consecutive slots (D 128, 256: one run; D 512: slots 4, 5 | 0, 1)
+    // that one PV instruction covers (N = 64 x run length).
+    static constexpr int STAGES = D == 512 ? 6 : (D == 256 ? 8 : 12);
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = OFF_Q + NSK * kSlab;
     static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
@@ -187,26 +200,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
     const int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
-    // Cluster (cx x cy): along y, CTAs of one (split, KV head): 1, the row
-    // tiles of one O half (cy = n_rt), or the row tiles of both halves.  Each
-    // K slab is loaded once for the cluster and each V slab once for the row
-    // tiles of an O half, the shares multicast; along x, consecutive splits
-    // whose partials are merged in the cluster.
-    const int cx = static_cast<int>(cluster_nctaid_x()), cy = static_cast<int>(cluster_nctaid_y());
-    const int cxi = static_cast<int>(cluster_ctaid_x()), cyi = static_cast<int>(cluster_ctaid_y());
-    const int k_share = cy, k_idx = cyi;                            // K: every y of the cluster
-    const bool v_shared = n_rt > 1 && cy >= n_rt;                   // V: the row tiles of this O half
-    const int v_share = v_shared ? n_rt : 1, v_idx = v_shared ? rt : 0;
-    uint16_t k_mask = 0, v_mask = 0;
-    for (int y2 = 0; y2 < cy; ++y2) k_mask |= static_cast<uint16_t>(1u << (cxi + cx * y2));
-    if (v_shared) {
-        const int y0 = static_cast<int>(blockIdx.y) - cyi;          // first y of the cluster
-        for (int r2 = 0; r2 < n_rt; ++r2)
-            v_mask |= static_cast<uint16_t>(1u << (cxi + cx * (os * n_rt + r2 - y0)));
-    }
+    // Cluster (cx x 1): consecutive splits of one (row tile, O half, KV head)
+    // whose partials are merged in the cluster over DSMEM.
+    const int cx = static_cast<int>(cluster_nctaid_x());
+    const int cxi = static_cast<int>(cluster_ctaid_x());
 
     if (tid == 0) {
-        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], cy); }
+        for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], 1); }
         mbar_init(&bars->q_full, 1);
         for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 1); }
         mbar_init(&bars->p_full, 8);
@@ -221,7 +221,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         tmem_relinquish();
     }
     tc_fence_before();
-    cluster_sync();                                     // peers' mbarriers exist before any multicast
+    cluster_sync();                                     // peers exist before any DSMEM access
     tc_fence_after();
     pdl_wait();                                         // chunk classes and Q copy are ready
     const uint32_t tmem = bars->tmem_base;
@@ -238,15 +238,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads issued
-        // A slab's 4 chunks go as 32-key boxes split over the CTAs of the share
-        // group.  With D = 512, where chunks 0-1 and 2-3 are consecutive pairs,
-        // they go as two 64-key boxes instead (one per CTA with a share of 2,
-        // both with 1): half the boxes to issue for the twelve slabs of a key
-        // tile (measured faster there; with D <= 256 the 32-key boxes were).
+        // A slab's 4 chunks go as four 32-key boxes; with D = 512, where chunks
+        // 0-1 and 2-3 are consecutive pairs, as two 64-key boxes instead (half
+        // the boxes to issue for the twelve slabs of a key tile; with D <= 256
+        // the 32-key boxes measured faster).
         auto load_slabs = [&](const CUtensorMap *map, const CUtensorMap *map64, const int (&chunk)[4], int nslab,
-                              int x0, int share, int share_idx, uint16_t mask) -> bool {
-            const bool pairs = D == 512 && share <= 2 && chunk[0] >= 0 && chunk[1] == chunk[0] + 1 &&
-                               chunk[2] >= 0 && chunk[3] == chunk[2] + 1;
+                              int x0) -> bool {
+            const bool pairs = D == 512 && chunk[0] >= 0 && chunk[1] == chunk[0] + 1 && chunk[2] >= 0 &&
+                               chunk[3] == chunk[2] + 1;
             for (int s = 0; s < nslab; ++s) {
                 const int slot = issued % ST;
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
@@ -257,20 +256,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
                         unsigned char *dst = sRing + slot * kSlab;
                         if (pairs) {
-                            for (int c = 2 * share_idx; c < 4; c += 2 * share) {
-                                if (share > 1)
-                                    tma_load_3d_mc(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32,
-                                                   kh, mask);
-                                else
-                                    tma_load_3d(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32, kh);
-                            }
+                            for (int c = 0; c < 4; c += 2)
+                                tma_load_3d(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32, kh);
                         } else {
-                            for (int c = share_idx; c < 4; c += share) {
+                            for (int c = 0; c < 4; ++c) {
                                 const int y = chunk[c] >= 0 ? chunk[c] * 32 : n_pad;
-                                if (share > 1)
-                                    tma_load_3d_mc(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh, mask);
-                                else
-                                    tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
+                                tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
                             }
                         }
                     }
@@ -294,18 +285,17 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             }
             int cur[4], nxt[4], cl_unused;
             for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-            ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0, k_share, k_idx, k_mask);
+            ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0);
             for (int t = 0; t < T && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
                 if (t + 1 < T) {
                     for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-                    ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0, k_share, k_idx, k_mask);
+                    ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0);
                 }
-                if (ok) ok = load_slabs(&maps.v, &maps.v64, cur, NSV, os * DV, v_share, v_idx, v_mask);
+                if (ok) ok = load_slabs(&maps.v, &maps.v64, cur, NSV, os * DV);
             }
-            // Drain: every copy into this CTA's ring has landed, and every CTA
-            // of the cluster has released the last use of each slot, so no
-            // peer copy or release still targets this CTA's shared memory.
+            // Drain: every copy into this CTA's ring has landed and the MMAs
+            // have released the last use of each slot.
             if (lane == 0) {
                 if (!mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9);
                 const int first = issued > ST ? issued - ST : 0;
@@ -321,14 +311,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         // ---------------------------------------------------------- MMA issuer
         if (lane == 0 && T > 0) {
             constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
-            constexpr uint32_t id_pv = idesc_f16(128, 64, BF16 ? 1 : 0, 0, 1);
             const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
             int used = 0;                                   // ring loads consumed
-            // a slot is free once every CTA of the cluster has consumed it
-            auto release = [&](int slot) {
-                if (cy > 1) mma_commit_mc(&bars->empty[slot], k_mask);
-                else mma_commit(&bars->empty[slot]);
-            };
+            auto release = [&](int slot) { mma_commit(&bars->empty[slot]); };
             bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2);
             auto issue_s = [&](int t) -> bool {
                 const int sb = t & 1;
@@ -358,20 +343,32 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 ok = wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5);
                 if (!ok) break;
                 tc_fence_after();
-                for (int s = 0; s < NSV && ok; ++s) {
-                    const int slot = used % ST;
-                    ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 6);
+                // V slabs in runs of consecutive ring slots, one PV instruction
+                // per run and K step (N = 64 x run length).  P_t sits in TMEM
+                // over S_t: keys 64h + [0, 64) of the tile as P_hi in columns
+                // 64h + [0, 32) and P_lo in 64h + [32, 64), two 16-bit keys per
+                // column; each K step takes both terms.
+                for (int s = 0; s < NSV && ok;) {
+                    const int slot0 = used % ST;
+                    int len = 1;
+                    while (s + len < NSV && slot0 + len < ST) ++len;
+                    for (int j = 0; j < len && ok; ++j)
+                        ok = wait_or_abort(bars, &bars->full[slot0 + j], static_cast<uint32_t>((used + j) / ST) & 1u,
+                                           err, 6);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = ring_addr + slot * kSlab;
-                    // P_t sits in TMEM over S_t: keys 64h.. of the tile in columns
-                    // 64h + [0, 32) of the buffer, two 16-bit keys per column
+                    const uint32_t vb = ring_addr + slot0 * kSlab;
+                    const uint32_t id_pv = idesc_f16(128, 64 * len, BF16 ? 1 : 0, 0, 1);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_f16_ts(tm_o + s * 64, tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3),
-                                   sw128_desc(vb + kk * 2048, kSlab, 1024), id_pv, (t | kk) != 0);
-                    release(slot);
-                    ++used;
+                    for (int kk = 0; kk < 8; ++kk) {
+                        const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
+                        const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
+                        mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
+                        mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
+                    }
+                    for (int j = 0; j < len; ++j) release(slot0 + j);
+                    used += len;
+                    s += len;
                 }
                 mma_commit(&bars->o_done[t & 1]);
                 mma_commit(&bars->s_free[t & 1]);   // S_t / P_t buffer free once PV_t is done
@@ -391,9 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;              // row within the tile
         const int rg = rt * RT + r;                     // row within the KV group
-        const bool row_ok = r < rows_here;
         const int qi = rg % a.L;                        // query (tree node)
-        const int hj = kh * a.g + (rg / a.L);           // query head
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int last0 = a.N - a.L;
         const float *mrow = (IMPLICIT || a.mask == nullptr) ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
@@ -517,13 +512,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     tmem_wait_st();
                 }
             }
-            // pass 2: P = 2^(logit - M) rounded to the K/V type, written back into
-            // TMEM over this half's logits (columns 64 * half + [0, 32): two keys
-            // per column, the lower key in the low 16 bits), where PV reads it as
-            // the A operand.  The row sum adds the rounded values, the ones the
-            // tensor core uses.
+            // pass 2: P = 2^(logit - M) as two 16-bit terms of the K/V type,
+            // P_hi = rn(P) and P_lo = rn(P - P_hi), written back into TMEM over
+            // this half's logits (P_hi in columns 64 * half + [0, 32), P_lo in
+            // 64 * half + [32, 64); two keys per column, the lower key in the
+            // low 16 bits), where PV reads them as A operands.  The row sum adds
+            // P in f32 (P_hi + P_lo equals it to 2^-16 relative).
             float ps[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-            uint32_t pw[32];
+            uint32_t pw[32], pl[32];
 #pragma unroll
             for (int cc = 0; cc < 2; ++cc) {
                 uint32_t v[32];
@@ -540,12 +536,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     const float p1 = fast_exp2(__uint_as_float(v[2 * j + 1]) - m_use);
                     const uint32_t w = pack2(p0, p1, BF16);
                     pw[cc * 16 + j] = w;
-                    ps[(2 * j) & 7] += lo16(w, BF16);
-                    ps[(2 * j + 1) & 7] += hi16(w, BF16);
+                    pl[cc * 16 + j] = pack2(p0 - lo16(w, BF16), p1 - hi16(w, BF16), BF16);
+                    ps[(2 * j) & 7] += p0;
+                    ps[(2 * j + 1) & 7] += p1;
                 }
             }
             if (ok) {
                 tmem_st32(tm_s[sb] + lane_off + 64 * half, pw);
+                tmem_st32(tm_s[sb] + lane_off + 64 * half + 32, pl);
                 tmem_wait_st();
             }
             l_half += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
@@ -657,14 +655,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             // every remote load of the row is issued before any is used
             float2 ml = make_float2(0.0f, -FLT_MAX);
             float4 v[8][C4];
-            if (lane < cx) ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane + cx * cyi));
+            if (lane < cx) ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane));
 #pragma unroll
             for (int p = 0; p < 8; ++p) {
                 if (p >= cx) break;
 #pragma unroll
                 for (int j = 0; j < C4; ++j) {
                     const uint32_t off = stage_sa + (rr * SROW + 4 * (lane + 32 * j)) * 4;
-                    v[p][j] = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p + cx * cyi))
+                    v[p][j] = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p))
                                      : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * (lane + 32 * j));
                 }
             }
@@ -713,10 +711,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 // once (the kernel is shared-memory bound to one CTA per SM, equally for all
 // instantiations); cached per device.
 static int max_active_clusters(int size) {
-    static int cache[64][4];
+    static int cache[64][9];
     int dev = 0;
+    if (size < 1 || size > 8) return 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return 0; }
-    const int idx = size == 1 ? 0 : (size == 2 ? 1 : (size == 4 ? 2 : 3));
+    const int idx = size;
     int n = __atomic_load_n(&cache[dev][idx], __ATOMIC_ACQUIRE);
     if (n > 0) return n;
     auto kern = tree_tc_kernel<256, false, false>;
@@ -741,31 +740,20 @@ static int max_active_clusters(int size) {
 
 }  // namespace
 
-// Largest cluster whose clusters all fit on the device at once (one wave):
-// first the row tiles / O halves along y (multicast K/V); then all splits
-// along x when they fit in the cluster, so the merge completes inside it and
-// no partials are written (a partial in-cluster merge costs more in remote
-// loads than it saves in partial traffic); at most 8 CTAs.
+// Cluster shape: all splits of a (row tile, O half, KV head) along x when
+// they fit in one cluster (at most 8 CTAs) and every cluster of the grid fits
+// on the device at once, so the merge completes inside the cluster and no
+// partials are written (a partial in-cluster merge costs more in remote loads
+// than it saves in partial traffic); else clusters of one.  cy is always 1.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     const int n_rt = (a.R + 127) / 128;
     const int gy = n_rt * (a.D == 512 ? 2 : 1);
     const long total = static_cast<long>(a.nwg) * gy * a.Hk;
-    auto fits = [&](int size) {
-        const int n = size == 1 ? 1 << 30 : max_active_clusters(size);
-        return n > 0 && total / size <= n;
-    };
     *cx = 1;
     *cy = 1;
-    // With two O halves the cluster holds the row tiles of one half: K slabs
-    // are then shared by n_rt CTAs rather than by all of them, so a ring slot
-    // waits on fewer consumers (the other half reads K again from L2).
-    const int y_pref = (gy > n_rt && n_rt > 1) ? n_rt : gy;
-    const int y_choices[2] = {y_pref, 1};
-    for (int yc : y_choices) {
-        if (yc > 8 || (yc & (yc - 1)) != 0 || !fits(yc)) continue;
-        *cy = yc;
-        if (a.nwg > 1 && a.nwg * yc <= 8 && fits(a.nwg * yc)) *cx = a.nwg;
-        return;
+    if (a.nwg > 1 && a.nwg <= 8) {
+        const int n = max_active_clusters(a.nwg);
+        if (n > 0 && total / a.nwg <= n) *cx = a.nwg;
     }
 }
 
