@@ -135,7 +135,7 @@ uint32_t resolve_tree_nwg(const ta_tree_params *p) {
         // tensor-core kernel: one CTA per SM, CTAs = splits x row tiles x O halves x KV heads
         // and each split a run of whole 4-chunk key tiles (no split gets more tiles
         // than needed to cover the keys with at most one CTA per SM)
-        const uint64_t units = (uint64_t)p->n_kv_heads * ((R + 127) / 128) * (p->head_dim == 512 ? 2 : 1);
+        const uint64_t units = (uint64_t)p->n_kv_heads * (uint64_t)tree_tc_row_ctas((int)R) * (p->head_dim == 512 ? 2 : 1);
         const uint64_t tiles = (n_chunks + 3) / 4;
         uint64_t most = (uint64_t)sms / units;
         if (most < 1) most = 1;
@@ -327,6 +327,8 @@ ta_status plan_tree(const ta_tree_params *p, int kernel, const ta_buf *q, const 
         a.cluster_x = cx;
     }
     a.n_part = a.nwg / a.cluster_x == 1 ? 0 : a.nwg / a.cluster_x;
+    if (plan->use_tc && a.R > 128 && (uint64_t)a.nwg * (a.D == 512 ? 2u : 1u) > 65535u)
+        return fail(TA_ERR_UNSUPPORTED, "tree_attention: nwg (%d) too large for the tensor-core kernel's grid", a.nwg);
     if (plan->use_tc && !get_encoder())
         return fail(TA_ERR_CUDA, "tree_attention: cuTensorMapEncodeTiled is not available");
     return TA_OK;
@@ -342,12 +344,14 @@ ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
         const cuuint32_t qbox[2] = {64, 128};
         const cuuint64_t kdims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.N, (cuuint64_t)a.Hk};
         const cuuint64_t kstr[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.C * a.D * 2};
-        const cuuint32_t kbox[3] = {64, 32, 1}, kbox64[3] = {64, 64, 1};
+        const cuuint32_t kbox[3] = {64, 32, 1}, kbox64[3] = {64, 64, 1}, kbox128[3] = {64, 128, 1};
         if (!encode_map(&maps.q16, bf16, a.q16, 2, qdims, qstr, qbox) ||
             !encode_map(&maps.k, bf16, plan.k, 3, kdims, kstr, kbox) ||
             !encode_map(&maps.v, bf16, plan.v, 3, kdims, kstr, kbox) ||
             !encode_map(&maps.k64, bf16, plan.k, 3, kdims, kstr, kbox64) ||
-            !encode_map(&maps.v64, bf16, plan.v, 3, kdims, kstr, kbox64))
+            !encode_map(&maps.v64, bf16, plan.v, 3, kdims, kstr, kbox64) ||
+            !encode_map(&maps.k128, bf16, plan.k, 3, kdims, kstr, kbox128) ||
+            !encode_map(&maps.v128, bf16, plan.v, 3, kdims, kstr, kbox128))
             return fail(TA_ERR_CUDA, "tree_attention: TMA descriptor encoding failed");
     }
     cudaError_t e = launch_tree_classify(plan.a, s);

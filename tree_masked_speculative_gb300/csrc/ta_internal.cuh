@@ -147,6 +147,8 @@ struct TcMaps {
     CUtensorMap v;
     CUtensorMap k64;   // the same tensors, box {64, 64, 1}: two consecutive chunks
     CUtensorMap v64;
+    CUtensorMap k128;  // box {64, 128, 1}: four consecutive chunks
+    CUtensorMap v128;
 };
 
 struct QuantArgs {
@@ -310,6 +312,13 @@ struct TreeWorkspace {
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
 cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s);
+// Row tiles (CTAs along the rows of a KV head) of the tensor-core kernel: one
+// 128-row tile, or, above 128 rows, an even number of tiles served by CTA
+// pairs (two tiles per pair).
+__host__ __device__ inline int tree_tc_row_ctas(int R) {
+    const int n_rt = (R + 127) / 128;
+    return n_rt > 1 ? 2 * ((n_rt + 1) / 2) : 1;
+}
 // Cluster shape of the tensor-core kernel: x = splits merged in-cluster (y = 1).
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);
 cudaError_t launch_tree_reduce(const TreeArgs &a, cudaStream_t s);

@@ -20,8 +20,9 @@
 //   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
 //                TMEM, double buffered) and O += P_t V_t (M 128, N = 64 per V
 //                slab, up to 256 over slabs in consecutive ring slots; P read
-//                from TMEM where the softmax left it over S_t, V MN-major); a
-//                buffer is released for S_t+2 when PV_t completes.
+//                from TMEM where the softmax left it over S_t, V MN-major);
+//                S_t+2 is issued right after PV_t into the same buffer (the
+//                tensor core runs one thread's MMAs in order).
 //   warps 2..9 : two warps per TMEM lane quarter: mask + scale, online softmax
 //                with lazy rescaling (M only moves when a row max exceeds it by
 //                more than e^8, so O in TMEM is rarely touched), P back into
@@ -45,41 +46,52 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcThreads = 320;               // producer, MMA issuer, 8 softmax warps
+constexpr int kTcWarps = 11;                 // producer 0, MMA issuer, 8 softmax warps, producer 1
+constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kSlab = 16384;                 // [128 rows][64 x 16-bit], 128-byte swizzled
 constexpr uint32_t kWaitIters = 1u << 22;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleSlack2 = 8.0f * kLog2e;   // in log2 units: P <= e^8 = 2981 fits f16 and bf16
 
-template <int D>
+// PAIR = false: one CTA per 128-row tile (cta_group::1), ring slots of 16 KB
+// ([128 keys x 64 cols]).  PAIR = true: a CTA pair (cta_group::2) covers two
+// row tiles with M = 256 MMAs, and each CTA loads half of every operand tile:
+// 64 of a key tile's 128 keys for QK^T, half of the O columns of V for PV;
+// ring slots of 8 KB ([64 keys x 64 cols]).
+template <int D, bool PAIR>
 struct TcCfg {
-    static constexpr int DV = D < 256 ? D : 256;     // O columns per CTA
-    static constexpr int NSK = D / 64;               // K slabs per key tile
-    static constexpr int NSV = DV / 64;              // V slabs per key tile
+    static constexpr int DV = D < 256 ? D : 256;     // O columns per CTA (its rows' share of O)
+    static constexpr int NSK = D / 64;               // K slots per key tile
+    static constexpr int NSV = DV / 64;              // V slots per key tile
+    static constexpr int SLOT = PAIR ? 8192 : kSlab; // bytes of a ring slot
     // Ring depth.  Every key tile advances the ring by NSK + NSV slots and a V
-    // group starts NSK-aligned, so with these depths a tile's V slabs sit in
-    // runs of consecutive slots (D 128, 256: one run; D 512: slots 4, 5 | 0, 1)
-    // that one PV instruction covers (N = 64 x run length).
-    static constexpr int STAGES = D == 512 ? 6 : (D == 256 ? 8 : 12);
+    // group starts NSV-aligned, so with these depths a tile's V slots sit in
+    // runs of consecutive slots (single CTA: D 128, 256 one run, D 512 slots
+    // 4, 5 | 0, 1; pair: always one run) that one PV instruction covers.
+    static constexpr int STAGES = PAIR ? (D == 512 ? 12 : (D == 256 ? 16 : 24))
+                                       : (D == 512 ? 6 : (D == 256 ? 8 : 12));
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_RING = OFF_Q + NSK * kSlab;
-    static constexpr int OFF_BAR = OFF_RING + STAGES * kSlab;
+    static constexpr int OFF_BAR = OFF_RING + STAGES * SLOT;
     static constexpr int SMEM = OFF_BAR + 3072;      // the dynamic base must be 1024-aligned
     static_assert(SMEM <= 232448, "shared memory budget");
     static_assert(128 * (DV + 4) * 4 + 128 * 8 <= OFF_BAR, "epilogue staging fits below the barriers");
 };
 
+constexpr int kMaxStages = 24;
+
 struct Bars {
-    uint64_t full[12];
-    uint64_t empty[12];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t q_full;
     uint64_t s_full[2];
-    uint64_t s_free[2];
     uint64_t p_full;
     uint64_t o_done[2];   // PV of tiles t = b (mod 2) done
     uint64_t drain;
+    uint64_t peer_done[2];   // pair: the peer's producer p has published how far it issued
     uint32_t tmem_base;
+    uint32_t peer_issued[2]; // pair: 1 + index of the last ring load the peer's producer p issued
     volatile int abort_flag;
     float xrow[2][2][128];   // per-row values exchanged by the two warps of a TMEM quarter
 };
@@ -143,17 +155,32 @@ __device__ __forceinline__ float fast_exp2(float x) {
     return y;
 }
 
-__device__ __forceinline__ void note_abort(Bars *b, int *err, int code) {
+// Abort: flag this CTA (and, in a pair, the peer: peer_flag is the
+// shared::cluster address of its flag, 0 for none) and record the first code.
+__device__ __forceinline__ void note_abort(Bars *b, int *err, int code, uint32_t peer_flag) {
     b->abort_flag = 1;
+    if (peer_flag != 0u) st_dsmem_u32(peer_flag, 1u);
     atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code) {
+__device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code,
+                                              uint32_t peer_flag) {
     if (b->abort_flag) return false;
     // a waiting warp sleeps on the barrier (taking no issue slots from the
     // MMA issuer and the softmax) for at most 2^21 tries of 1 us
     if (mbar_try_wait(bar, parity) || mbar_wait_sleep(bar, parity, 1u << 21, 1000)) return true;
-    note_abort(b, err, code);
+    note_abort(b, err, code, peer_flag);
+    return false;
+}
+
+// As wait_or_abort, for a barrier that threads of the peer CTA arrive on
+// (acquire at cluster scope).
+__device__ __forceinline__ bool wait_or_abort_cluster(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code,
+                                                      uint32_t peer_flag) {
+    if (b->abort_flag) return false;
+    for (uint32_t i = 0; i < (1u << 21); ++i)
+        if (mbar_try_wait_cluster(bar, parity, 1000)) return true;
+    note_abort(b, err, code, peer_flag);
     return false;
 }
 
@@ -174,10 +201,11 @@ __device__ __forceinline__ float hi16(uint32_t u, bool bf16) {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(u >> 16)));
 }
 
-template <int D, bool BF16, bool IMPLICIT>
+template <int D, bool BF16, bool IMPLICIT, bool PAIR>
 __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a, const __grid_constant__ TcMaps maps) {
-    using Cfg = TcCfg<D>;
-    constexpr int DV = Cfg::DV, NSK = Cfg::NSK, NSV = Cfg::NSV, ST = Cfg::STAGES;
+    using Cfg = TcCfg<D, PAIR>;
+    constexpr int DV = Cfg::DV, NSK = Cfg::NSK, NSV = Cfg::NSV, ST = Cfg::STAGES, SLOT = Cfg::SLOT;
+    static_assert(ST <= kMaxStages, "ring depth");
     constexpr int SROW = DV + 4;                        // floats per staged O row
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 128-byte-swizzled TMA / MMA tiles need a 1024-byte-aligned base; every
@@ -193,35 +221,59 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     Bars *bars = reinterpret_cast<Bars *>(sm + Cfg::OFF_BAR);
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int split = blockIdx.x;
-    const int n_rt = (a.R + 127) / 128;
-    const int os = blockIdx.y / n_rt, rt = blockIdx.y % n_rt;   // y = O half * row tiles + row tile
+    // Grid.  Single CTA: x = split, y = O half * row tiles + row tile.  Pair:
+    // x = 2 * (pair of row tiles) + member, y = split * O halves + O half; the
+    // cluster is the pair (cluster ranks 2k, 2k + 1), member 0 the leader that
+    // issues the MMAs.  z = KV head.
+    constexpr int kHalves = D / DV;
+    const int n_ct = PAIR ? 2 * (((a.R + 127) / 128 + 1) / 2) : (a.R + 127) / 128;   // row tiles
+    const int member = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
+    const bool leader = member == 0;
+    const int split = PAIR ? static_cast<int>(blockIdx.y) / kHalves : static_cast<int>(blockIdx.x);
+    const int os = PAIR ? static_cast<int>(blockIdx.y) % kHalves : static_cast<int>(blockIdx.y) / n_ct;
+    const int rt = PAIR ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y) % n_ct;
     const int kh = blockIdx.z;
-    const int RT = (a.R + n_rt - 1) / n_rt;            // rows per tile
+    const int RT = (a.R + n_ct - 1) / n_ct;            // rows per tile
     const int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
-    // Cluster (cx x 1): consecutive splits of one (row tile, O half, KV head)
-    // whose partials are merged in the cluster over DSMEM.
-    const int cx = static_cast<int>(cluster_nctaid_x());
-    const int cxi = static_cast<int>(cluster_ctaid_x());
+    // Cluster (single CTA: cx x 1): consecutive splits of one (row tile, O
+    // half, KV head) whose partials are merged in the cluster over DSMEM.
+    // Pair: the cluster is the pair and splits are never merged in it.
+    const int cx = PAIR ? 1 : static_cast<int>(cluster_nctaid_x());
+    const int cxi = PAIR ? 0 : static_cast<int>(cluster_ctaid_x());
+    // shared::cluster addresses: the leader's barriers (pair), the peer's abort flag
+    const uint32_t lead_rank = PAIR ? (cluster_ctarank() & ~1u) : 0u;
+    const uint32_t peer_rank = PAIR ? (cluster_ctarank() ^ 1u) : 0u;
+    const uint32_t peer_flag =
+        PAIR ? mapa_shared(smem_u32(const_cast<int *>(&bars->abort_flag)), peer_rank) : 0u;
+    auto at_leader = [&](const void *p) -> uint32_t { return mapa_shared(smem_u32(p), lead_rank); };
+    auto at_peer = [&](const void *p) -> uint32_t { return mapa_shared(smem_u32(p), peer_rank); };
 
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], 1); }
         mbar_init(&bars->q_full, 1);
-        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 1); }
-        mbar_init(&bars->p_full, 8);
+        for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
+        mbar_init(&bars->p_full, PAIR ? 16 : 8);       // the softmax warps (of both CTAs of a pair)
         mbar_init(&bars->o_done[0], 1);
         mbar_init(&bars->o_done[1], 1);
         mbar_init(&bars->drain, 1);
+        mbar_init(&bars->peer_done[0], 1);
+        mbar_init(&bars->peer_done[1], 1);
+        bars->peer_issued[0] = bars->peer_issued[1] = 0u;
         bars->abort_flag = 0;
         fence_mbar_init();
     }
     if (warp == 1) {
-        tmem_alloc(&bars->tmem_base, 512);
-        tmem_relinquish();
+        if constexpr (PAIR) {
+            tmem_alloc_pair(&bars->tmem_base, 512);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(&bars->tmem_base, 512);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
-    cluster_sync();                                     // peers exist before any DSMEM access
+    cluster_sync();                                     // peers' barriers exist before any remote access
     tc_fence_after();
     pdl_wait();                                         // chunk classes and Q copy are ready
     const uint32_t tmem = bars->tmem_base;
@@ -233,151 +285,297 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const int T = count_tiles(a.cls, c_begin, c_end);
     const int n_pad = ((a.N + 31) / 32) * 32;          // a key row that is out of bounds
 
-    if (warp == 0) {
-        // ------------------------------------------------------------ producer
+    if (warp == 0 || warp == kTcWarps - 1) {
+        // ----------------------------------------------------------- producers
+        // Two producer warps issue alternate ring loads (global load index n:
+        // producer n % 2): one thread issuing copies back to back is limited
+        // by the issue time of each copy (about 0.2 us for an 8 KB box), two
+        // reach the rate HBM can feed an SM.  Both walk the whole sequence.
+        const int prod = warp == 0 ? 0 : 1;
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
-        int issued = 0;                                 // ring loads issued
-        // A slab's 4 chunks go as four 32-key boxes; with D = 512, where chunks
-        // 0-1 and 2-3 are consecutive pairs, as two 64-key boxes instead (half
-        // the boxes to issue for the twelve slabs of a key tile; with D <= 256
-        // the 32-key boxes measured faster).
-        auto load_slabs = [&](const CUtensorMap *map, const CUtensorMap *map64, const int (&chunk)[4], int nslab,
-                              int x0) -> bool {
-            const bool pairs = D == 512 && chunk[0] >= 0 && chunk[1] == chunk[0] + 1 && chunk[2] >= 0 &&
-                               chunk[3] == chunk[2] + 1;
-            for (int s = 0; s < nslab; ++s) {
+        int issued = 0;                                 // ring loads of the sequence so far (both producers)
+        int mine_end = 0;                               // 1 + index of the last load this producer issued
+        // Single CTA: a slab's 4 chunks as one 128-key box when they are
+        // consecutive, else as 64-key boxes for consecutive pairs and 32-key
+        // boxes otherwise (a missing chunk loads zeros from past kv_seq_len).
+        auto load_slabs = [&](const int (&chunk)[4], int nslab, int x0, bool is_v) -> bool {
+            const CUtensorMap *m32 = is_v ? &maps.v : &maps.k;
+            const CUtensorMap *m64 = is_v ? &maps.v64 : &maps.k64;
+            const CUtensorMap *m128 = is_v ? &maps.v128 : &maps.k128;
+            const bool p01 = chunk[0] >= 0 && chunk[1] == chunk[0] + 1;
+            const bool p23 = chunk[2] >= 0 && chunk[3] == chunk[2] + 1;
+            const bool all4 = p01 && p23 && chunk[2] == chunk[1] + 1;
+            for (int s = 0; s < nslab; ++s, ++issued) {
+                if ((issued & 1) != prod) continue;
                 const int slot = issued % ST;
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
                 bool ok = true;
                 if (lane == 0) {
-                    ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1);
+                    ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, 0u);
                     if (ok) {
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
-                        unsigned char *dst = sRing + slot * kSlab;
-                        if (pairs) {
-                            for (int c = 0; c < 4; c += 2)
-                                tma_load_3d(dst + c * 4096, map64, &bars->full[slot], x0 + s * 64, chunk[c] * 32, kh);
+                        unsigned char *dst = sRing + slot * SLOT;
+                        const int xx = x0 + s * 64;
+                        if (all4) {
+                            tma_load_3d(dst, m128, &bars->full[slot], xx, chunk[0] * 32, kh);
                         } else {
-                            for (int c = 0; c < 4; ++c) {
-                                const int y = chunk[c] >= 0 ? chunk[c] * 32 : n_pad;
-                                tma_load_3d(dst + c * 4096, map, &bars->full[slot], x0 + s * 64, y, kh);
+                            for (int h = 0; h < 2; ++h) {
+                                const int c0 = chunk[2 * h], c1 = chunk[2 * h + 1];
+                                if (h == 0 ? p01 : p23) {
+                                    tma_load_3d(dst + h * 8192, m64, &bars->full[slot], xx, c0 * 32, kh);
+                                } else {
+                                    tma_load_3d(dst + h * 8192, m32, &bars->full[slot], xx, c0 >= 0 ? c0 * 32 : n_pad, kh);
+                                    tma_load_3d(dst + h * 8192 + 4096, m32, &bars->full[slot], xx,
+                                                c1 >= 0 ? c1 * 32 : n_pad, kh);
+                                }
                             }
                         }
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) return false;
-                ++issued;
+                mine_end = issued + 1;
             }
+            return true;
+        };
+        // Pair: one slot = the 64 keys of chunks c0, c1 (one 64-key box when they
+        // are consecutive, else two 32-key boxes; a missing chunk loads zeros)
+        // x 64 columns from x0, into this CTA's slot; the copy completes on the
+        // leader's full barrier, which expects both CTAs' 8 KB.
+        auto load_unit = [&](const CUtensorMap *map, const CUtensorMap *map64, int c0, int c1, int x0) -> bool {
+            const int n = issued++;
+            if ((n & 1) != prod) return true;
+            const int slot = n % ST;
+            const uint32_t pass = static_cast<uint32_t>(n / ST);
+            bool ok = true;
+            if (lane == 0) {
+                ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, peer_flag);
+                if (ok) {
+                    if (leader) mbar_arrive_expect_tx(&bars->full[slot], 2 * SLOT);
+                    unsigned char *dst = sRing + slot * SLOT;
+                    const uint32_t fb = at_leader(&bars->full[slot]);
+                    if (c0 >= 0 && c1 == c0 + 1) {
+                        tma_load_3d_pair(dst, map64, fb, x0, c0 * 32, kh);
+                    } else {
+                        tma_load_3d_pair(dst, map, fb, x0, c0 >= 0 ? c0 * 32 : n_pad, kh);
+                        tma_load_3d_pair(dst + 4096, map, fb, x0, c1 >= 0 ? c1 * 32 : n_pad, kh);
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (ok) mine_end = n + 1;
+            return ok;
+        };
+        // Pair: K of a tile = NSK slots of this CTA's two chunks (its half of
+        // the key columns of S); V = NSV slots, sub-slab j of this CTA's half
+        // of the O columns in slots 2j (keys 0-63) and 2j + 1 (keys 64-127).
+        auto load_k_pair = [&](const int (&chunk)[4]) -> bool {
+            for (int s = 0; s < NSK; ++s)
+                if (!load_unit(&maps.k, &maps.k64, chunk[2 * member], chunk[2 * member + 1], s * 64)) return false;
+            return true;
+        };
+        auto load_v_pair = [&](const int (&chunk)[4]) -> bool {
+            const int x0 = os * DV + member * (DV / 2);
+            for (int j = 0; j < NSV; ++j)
+                if (!load_unit(&maps.v, &maps.v64, chunk[2 * (j & 1)], chunk[2 * (j & 1) + 1], x0 + (j >> 1) * 64))
+                    return false;
             return true;
         };
         bool ok = true;
         if (T > 0) {
-            if (lane == 0) {
+            if (lane == 0 && prod == 0) {
                 tma_prefetch_desc(&maps.k);
                 tma_prefetch_desc(&maps.v);
                 tma_prefetch_desc(&maps.k64);
                 tma_prefetch_desc(&maps.v64);
-                mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
-                for (int s = 0; s < NSK; ++s)
-                    tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
+                if constexpr (PAIR) {
+                    if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * NSK * kSlab);
+                    const uint32_t qb = at_leader(&bars->q_full);
+                    for (int s = 0; s < NSK; ++s)
+                        tma_load_2d_pair(sQ + s * kSlab, &maps.q16, qb, s * 64, kh * a.R + rt * RT);
+                } else {
+                    tma_prefetch_desc(&maps.k128);
+                    tma_prefetch_desc(&maps.v128);
+                    mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
+                    for (int s = 0; s < NSK; ++s)
+                        tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
+                }
             }
             int cur[4], nxt[4], cl_unused;
             for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-            ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0);
+            ok = PAIR ? load_k_pair(nxt) : load_slabs(nxt, NSK, 0, false);
             for (int t = 0; t < T && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
                 if (t + 1 < T) {
                     for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-                    ok = load_slabs(&maps.k, &maps.k64, nxt, NSK, 0);
+                    ok = PAIR ? load_k_pair(nxt) : load_slabs(nxt, NSK, 0, false);
                 }
-                if (ok) ok = load_slabs(&maps.v, &maps.v64, cur, NSV, os * DV);
+                if (ok) ok = PAIR ? load_v_pair(cur) : load_slabs(cur, NSV, os * DV, true);
             }
-            // Drain: every copy into this CTA's ring has landed and the MMAs
-            // have released the last use of each slot.
-            if (lane == 0) {
-                if (!mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9);
-                const int first = issued > ST ? issued - ST : 0;
-                for (int n = first; n < issued; ++n) {
-                    if (!mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
-                        note_abort(bars, err, 9);
-                    if (!mbar_wait(&bars->empty[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
-                        note_abort(bars, err, 9);
+        }
+        // Drain: every copy this producer issued into this CTA's ring has
+        // landed and the MMAs have released the last use of each of its slots,
+        // so nothing still targets this CTA's shared memory when it exits.  In
+        // a pair the copies complete on the leader's barriers: each peer
+        // producer publishes how far it issued and the leader's producer of the
+        // same parity waits for every slot of that parity either CTA filled
+        // (standing in, with complete_tx / expect_tx, for the bytes of a load
+        // only one of them issued after an abort); the final cluster barrier
+        // keeps the peer alive until then.
+        if (lane == 0 && T > 0) {
+            auto drain_from = [&](int end) { return end > ST ? end - ST : 0; };
+            if constexpr (PAIR) {
+                if (!leader) {
+                    st_dsmem_u32(at_leader(&bars->peer_issued[prod]), static_cast<uint32_t>(mine_end));
+                    mbar_arrive_cluster(at_leader(&bars->peer_done[prod]));
+                } else {
+                    int ip = mine_end;
+                    bool got = false;
+                    for (uint32_t i = 0; i < (1u << 21) && !got; ++i)
+                        got = mbar_try_wait_cluster(&bars->peer_done[prod], 0, 1000);
+                    if (got) ip = static_cast<int>(bars->peer_issued[prod]);
+                    else note_abort(bars, err, 12, peer_flag);
+                    if (prod == 0 && !mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9, peer_flag);
+                    const int hi = max(mine_end, ip);
+                    for (int n = drain_from(hi); n < hi; ++n) {
+                        if ((n & 1) != prod) continue;
+                        uint64_t *fb = &bars->full[n % ST];
+                        if (n < mine_end && n >= ip) mbar_complete_tx(fb, SLOT);         // the peer's part never comes
+                        if (n >= mine_end && n < ip) mbar_arrive_expect_tx(fb, SLOT);    // only the peer's part
+                        if (!mbar_wait(fb, static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
+                            note_abort(bars, err, 9, peer_flag);
+                    }
                 }
+            } else {
+                if (prod == 0 && !mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9, 0u);
+                for (int n = drain_from(mine_end); n < mine_end; ++n)
+                    if ((n & 1) == prod &&
+                        !mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
+                        note_abort(bars, err, 9, 0u);
             }
+            for (int n = drain_from(mine_end); n < mine_end; ++n)
+                if ((n & 1) == prod &&
+                    !mbar_wait(&bars->empty[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
+                    note_abort(bars, err, 9, PAIR ? peer_flag : 0u);
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------- MMA issuer
-        if (lane == 0 && T > 0) {
-            constexpr uint32_t id_qk = idesc_f16(128, 128, BF16 ? 1 : 0, 0, 0);
+        // (the leader of a pair issues for both CTAs; the peer's warp 1 only
+        // holds the TMEM allocation)
+        if (lane == 0 && T > 0 && leader) {
+            constexpr uint32_t id_qk = idesc_f16(PAIR ? 256 : 128, 128, BF16 ? 1 : 0, 0, 0);
             const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
             int used = 0;                                   // ring loads consumed
-            auto release = [&](int slot) { mma_commit(&bars->empty[slot]); };
-            bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2);
+            // a slot is free once its MMAs are done (in both CTAs of a pair)
+            auto release = [&](int slot) {
+                if constexpr (PAIR) {
+                    mma_commit_pair(smem_u32(&bars->empty[slot]));
+                    mma_commit_pair(at_peer(&bars->empty[slot]));
+                } else {
+                    mma_commit(&bars->empty[slot]);
+                }
+            };
+            auto commit_own = [&](uint64_t *bar) {
+                if constexpr (PAIR) mma_commit_pair(smem_u32(bar));
+                else mma_commit(bar);
+            };
+            auto commit_both = [&](uint64_t *bar) {
+                commit_own(bar);
+                if constexpr (PAIR) mma_commit_pair(at_peer(bar));
+            };
+            const uint32_t pf = PAIR ? peer_flag : 0u;
+            bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2, pf);
+            // S_t goes to TMEM buffer t % 2, over P_t-2.  It is issued right
+            // after PV_t-2 with no wait for PV_t-2 to complete: the tensor core
+            // executes one thread's MMAs in issue order, so PV_t-2 reads P_t-2
+            // before QK_t overwrites it, and the softmax of tile t-2 finished
+            // with S_t-2 before PV_t-2 was issued.  The tensor pipe then never
+            // waits for an MMA to drain between tiles.
             auto issue_s = [&](int t) -> bool {
                 const int sb = t & 1;
-                if (!wait_or_abort(bars, &bars->s_free[sb], ((static_cast<uint32_t>(t) >> 1) & 1u) ^ 1u, err, 3))
-                    return false;
                 tc_fence_after();
                 for (int s = 0; s < NSK; ++s) {
                     const int slot = used % ST;
-                    if (!wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 4))
+                    if (!wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 4, pf))
                         return false;
                     tc_fence_after();
-                    const uint32_t kb = ring_addr + slot * kSlab;
+                    const uint32_t kb = ring_addr + slot * SLOT;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_f16_ss(tm_s[sb], sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024),
-                                   sw128_desc(kb + kk * 32, 16, 1024), id_qk, (s | kk) != 0);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint64_t ad = sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024);
+                        const uint64_t bd = sw128_desc(kb + kk * 32, 16, 1024);
+                        if constexpr (PAIR) mma_f16_ss_pair(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
+                        else mma_f16_ss(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
+                    }
                     release(slot);
                     ++used;
                 }
-                mma_commit(&bars->s_full[sb]);
+                commit_both(&bars->s_full[sb]);
                 return true;
             };
             if (ok) ok = issue_s(0);
+            if (ok && T > 1) ok = issue_s(1);
             for (int t = 0; t < T && ok; ++t) {
-                if (t + 1 < T) ok = issue_s(t + 1);
-                if (!ok) break;
-                ok = wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5);
+                ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf)
+                          : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf);
                 if (!ok) break;
                 tc_fence_after();
-                // V slabs in runs of consecutive ring slots, one PV instruction
-                // per run and K step (N = 64 x run length).  P_t sits in TMEM
-                // over S_t: keys 64h + [0, 64) of the tile as P_hi in columns
-                // 64h + [0, 32) and P_lo in 64h + [32, 64), two 16-bit keys per
-                // column; each K step takes both terms.
+                // V slots in runs of consecutive ring slots, one PV instruction
+                // per run and K step (single CTA: N = 64 x run length; pair: the
+                // tile's whole V group, N = DV over both CTAs).  P_t sits in
+                // TMEM over S_t: keys 64h + [0, 64) of the tile as P_hi in
+                // columns 64h + [0, 32) and P_lo in 64h + [32, 64), two 16-bit
+                // keys per column; each K step takes both terms.
                 for (int s = 0; s < NSV && ok;) {
                     const int slot0 = used % ST;
                     int len = 1;
                     while (s + len < NSV && slot0 + len < ST) ++len;
+                    if (PAIR && len != NSV) {   // by construction a pair's V group never wraps
+                        note_abort(bars, err, 13, pf);
+                        ok = false;
+                        break;
+                    }
                     for (int j = 0; j < len && ok; ++j)
                         ok = wait_or_abort(bars, &bars->full[slot0 + j], static_cast<uint32_t>((used + j) / ST) & 1u,
-                                           err, 6);
+                                           err, 6, pf);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = ring_addr + slot0 * kSlab;
-                    const uint32_t id_pv = idesc_f16(128, 64 * len, BF16 ? 1 : 0, 0, 1);
+                    const uint32_t vb = ring_addr + slot0 * SLOT;
+                    if constexpr (PAIR) {
+                        // this CTA's half of the columns: sub-slab j (16 KB) in
+                        // slots 2j, 2j + 1; K step kk at kk * 2048 bytes
+                        const uint32_t id_pv = idesc_f16(256, DV, BF16 ? 1 : 0, 0, 1);
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk) {
-                        const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
-                        const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
-                        mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
-                        mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
+                            const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
+                            mma_f16_ts_pair(tm_o, pa, bd, id_pv, (t | kk) != 0);
+                            mma_f16_ts_pair(tm_o, pa + 32, bd, id_pv, 1u);
+                        }
+                    } else {
+                        const uint32_t id_pv = idesc_f16(128, 64 * len, BF16 ? 1 : 0, 0, 1);
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
+                            const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
+                            mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
+                            mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
+                        }
                     }
                     for (int j = 0; j < len; ++j) release(slot0 + j);
                     used += len;
                     s += len;
                 }
-                mma_commit(&bars->o_done[t & 1]);
-                mma_commit(&bars->s_free[t & 1]);   // S_t / P_t buffer free once PV_t is done
+                if (!ok) break;
+                commit_both(&bars->o_done[t & 1]);
+                if (t + 2 < T) ok = issue_s(t + 2);
             }
             // Drain: all MMAs issued by this thread have completed.
-            mma_commit(&bars->drain);
-            if (!mbar_wait(&bars->drain, 0, kWaitIters)) note_abort(bars, err, 10);
+            commit_own(&bars->drain);
+            if (!mbar_wait(&bars->drain, 0, kWaitIters)) note_abort(bars, err, 10, pf);
         }
-    } else {
+    } else if (warp >= 2) {
         // ---------------------------------------------- softmax and epilogue
         // Eight warps: warp w reads TMEM lanes 32*(w%4).. (its 32 rows) and owns
         // one 64-key half of each tile (chunks 2*half, 2*half+1) and one half of
@@ -404,7 +602,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         // collective), and the named barriers run in every iteration even after
         // a failed wait, so no softmax warp can be left at a barrier.
         auto wait_all = [&](uint64_t *bar, uint32_t parity, int code) -> bool {
-            const bool w = ok && wait_or_abort(bars, bar, parity, err, code);
+            const bool w = ok && wait_or_abort(bars, bar, parity, err, code, PAIR ? peer_flag : 0u);
             return __all_sync(0xffffffffu, w);
         };
         for (int t = 0; t < T; ++t) {
@@ -549,7 +747,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             l_half += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
             tc_fence_before();
             __syncwarp();
-            if (lane == 0 && ok) mbar_arrive(&bars->p_full);
+            if (lane == 0 && ok) {
+                if (PAIR && !leader) mbar_arrive_cluster(at_leader(&bars->p_full));
+                else mbar_arrive(&bars->p_full);
+            }
         }
         if (T > 0) {
             ok = wait_all(&bars->o_done[(T - 1) & 1], (static_cast<uint32_t>(T - 1) >> 1) & 1u, 8);
@@ -600,7 +801,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     tc_fence_before();
     __syncthreads();
     if (cx > 1) cluster_sync();   // the merge reads the peers' staged rows (cx is uniform in a cluster)
-    if (warp >= 2 && cx == 1) {
+    const bool epi_warp = warp >= 2 && warp < kTcWarps - 1;   // the softmax warps
+    if (epi_warp && cx == 1) {
         // No merge in the cluster: each staged row (final and normalized, or
         // partial slot `split` with its (S, M)) leaves by one bulk copy issued
         // by its own thread; a destination off a 16-byte boundary is written
@@ -638,7 +840,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
                 reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * nrows + rid2] = stage_ml[rr];
             }
-    } else if (warp >= 2) {
+    } else if (epi_warp) {
         const int sw = warp - 2;
         const int nrows = a.H * a.L;
         const bool final_out = a.n_part == 0;
@@ -699,11 +901,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     }
 
     __syncthreads();
-    cluster_sync();                                     // peers are done with this CTA's shared memory
+    tc_fence_before();
+    cluster_sync();                                     // peers are done with this CTA's shared memory and TMEM
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        if constexpr (PAIR) tmem_dealloc_pair(tmem, 512);
+        else tmem_dealloc(tmem, 512);
     }
 }
 
@@ -718,13 +922,13 @@ static int max_active_clusters(int size) {
     const int idx = size;
     int n = __atomic_load_n(&cache[dev][idx], __ATOMIC_ACQUIRE);
     if (n > 0) return n;
-    auto kern = tree_tc_kernel<256, false, false>;
+    auto kern = tree_tc_kernel<256, false, false, false>;
     static unsigned long long done = 0;
-    if (set_smem_limit_once(kern, TcCfg<256>::SMEM, &done) != cudaSuccess) { cudaGetLastError(); return 0; }
+    if (set_smem_limit_once(kern, TcCfg<256, false>::SMEM, &done) != cudaSuccess) { cudaGetLastError(); return 0; }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(kTcThreads);
-    cfg.dynamicSmemBytes = TcCfg<256>::SMEM;
+    cfg.dynamicSmemBytes = TcCfg<256, false>::SMEM;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = size;
@@ -740,17 +944,18 @@ static int max_active_clusters(int size) {
 
 }  // namespace
 
-// Cluster shape: all splits of a (row tile, O half, KV head) along x when
-// they fit in one cluster (at most 8 CTAs) and every cluster of the grid fits
-// on the device at once, so the merge completes inside the cluster and no
-// partials are written (a partial in-cluster merge costs more in remote loads
-// than it saves in partial traffic); else clusters of one.  cy is always 1.
+// Splits merged inside one cluster.  More than 128 rows per KV head take the
+// CTA-pair kernel, whose cluster is the pair: no in-cluster merge (1).
+// Otherwise all splits of a (row tile, O half, KV head) along x when they fit
+// in one cluster (at most 8 CTAs) and every cluster of the grid fits on the
+// device at once, so the merge completes inside the cluster and no partials
+// are written (a partial in-cluster merge costs more in remote loads than it
+// saves in partial traffic); else clusters of one.  cy is always 1.
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
-    const int n_rt = (a.R + 127) / 128;
-    const int gy = n_rt * (a.D == 512 ? 2 : 1);
-    const long total = static_cast<long>(a.nwg) * gy * a.Hk;
     *cx = 1;
     *cy = 1;
+    if (a.R > 128) return;
+    const long total = static_cast<long>(a.nwg) * (a.D == 512 ? 2 : 1) * a.Hk;
     if (a.nwg > 1 && a.nwg <= 8) {
         const int n = max_active_clusters(a.nwg);
         if (n > 0 && total / a.nwg <= n) *cx = a.nwg;
@@ -759,31 +964,45 @@ void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
 
 namespace {
 
-template <int D, bool BF16, bool IMPLICIT>
+template <int D, bool BF16, bool IMPLICIT, bool PAIR>
 cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
-    auto kern = tree_tc_kernel<D, BF16, IMPLICIT>;
+    using Cfg = TcCfg<D, PAIR>;
+    auto kern = tree_tc_kernel<D, BF16, IMPLICIT, PAIR>;
     static unsigned long long done = 0;
-    cudaError_t e = set_smem_limit_once(kern, TcCfg<D>::SMEM, &done);
+    cudaError_t e = set_smem_limit_once(kern, Cfg::SMEM, &done);
     if (e != cudaSuccess) return e;
-    const int n_rt = (a.R + 127) / 128;
-    const unsigned gy = static_cast<unsigned>(n_rt * (D / TcCfg<D>::DV));
-    int cx, cy;
-    tree_tc_cluster_shape(a, &cx, &cy);
-    dim3 grid(a.nwg, gy, a.Hk);
-    e = launch_pdl_cluster(kern, grid, dim3(kTcThreads), TcCfg<D>::SMEM, s, static_cast<unsigned>(cx),
-                           static_cast<unsigned>(cy), a, maps);
+    constexpr unsigned halves = D / Cfg::DV;
+    const unsigned n_ct = static_cast<unsigned>(tree_tc_row_ctas(a.R));
+    dim3 grid;
+    unsigned cx, cy = 1;
+    if (PAIR) {
+        grid = dim3(n_ct, static_cast<unsigned>(a.nwg) * halves, a.Hk);
+        cx = 2;
+    } else {
+        int mx, my;
+        tree_tc_cluster_shape(a, &mx, &my);
+        grid = dim3(a.nwg, n_ct * halves, a.Hk);
+        cx = static_cast<unsigned>(mx);
+    }
+    e = launch_pdl_cluster(kern, grid, dim3(kTcThreads), Cfg::SMEM, s, cx, cy, a, maps);
     count_launch();
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, bool BF16, bool IMPLICIT>
+cudaError_t launch_tc_rows(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
+    return a.R > 128 ? launch_tc_one<D, BF16, IMPLICIT, true>(a, maps, s)
+                     : launch_tc_one<D, BF16, IMPLICIT, false>(a, maps, s);
 }
 
 template <bool BF16>
 cudaError_t launch_tc_typed(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
     const bool imp = a.mask == nullptr && a.anc == nullptr;
     switch (a.D) {
-        case 128: return imp ? launch_tc_one<128, BF16, true>(a, maps, s) : launch_tc_one<128, BF16, false>(a, maps, s);
-        case 256: return imp ? launch_tc_one<256, BF16, true>(a, maps, s) : launch_tc_one<256, BF16, false>(a, maps, s);
-        case 512: return imp ? launch_tc_one<512, BF16, true>(a, maps, s) : launch_tc_one<512, BF16, false>(a, maps, s);
+        case 128: return imp ? launch_tc_rows<128, BF16, true>(a, maps, s) : launch_tc_rows<128, BF16, false>(a, maps, s);
+        case 256: return imp ? launch_tc_rows<256, BF16, true>(a, maps, s) : launch_tc_rows<256, BF16, false>(a, maps, s);
+        case 512: return imp ? launch_tc_rows<512, BF16, true>(a, maps, s) : launch_tc_rows<512, BF16, false>(a, maps, s);
         default: return cudaErrorInvalidValue;
     }
 }
