@@ -20,13 +20,14 @@
 //   warp 1     : TMEM owner and MMA issuer: S_t = Q K_t^T (M 128, N 128, f32 in
 //                TMEM, double buffered) and O += P_t V_t (M 128, N = 64 per V
 //                slab, up to 256 over slabs in consecutive ring slots; P read
-//                from TMEM where the softmax left it over S_t, V MN-major);
-//                S_t+2 is issued right after PV_t into the same buffer (the
-//                tensor core runs one thread's MMAs in order).
+//                from TMEM where the softmax left it over S_t, V MN-major); the
+//                QK^T and PV MMAs are issued by two threads (warps 1 and 11)
+//                and S_t+2 reuses the buffer of S_t once PV_t has completed.
 //   warps 2..9 : two warps per TMEM lane quarter: mask + scale, online softmax
 //                with lazy rescaling (M only moves when a row max exceeds it by
 //                more than e^8, so O in TMEM is rarely touched), P back into
 //                TMEM as two 16-bit terms P = P_hi + P_lo, epilogue from TMEM.
+//   warp 10    : second TMA producer (alternate ring loads).
 // P in two terms: the tensor core takes 16-bit operands, and a single 16-bit
 // P carries a relative rounding error of up to 2^-8 (bf16) or 2^-11 (f16),
 // which moves the output by up to that fraction of the spread of the attended
@@ -46,7 +47,11 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTcWarps = 11;                 // producer 0, MMA issuer, 8 softmax warps, producer 1
+// warp 0: producer 0, warp 1: QK issuer + TMEM owner, warps 2-9: softmax,
+// warp 10: producer 1, warp 11: PV issuer
+constexpr int kTcWarps = 12;
+constexpr int kPvWarp = 11;
+constexpr int kProd1Warp = 10;
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kSlab = 16384;                 // [128 rows][64 x 16-bit], 128-byte swizzled
 constexpr uint32_t kWaitIters = 1u << 22;
@@ -87,6 +92,8 @@ struct Bars {
     uint64_t q_full;
     uint64_t s_full[2];
     uint64_t p_full;
+    uint64_t s_free[2];   // PV of tiles t = b (mod 2) done: S buffer b may be overwritten
+    uint64_t drain_pv;
     uint64_t o_done[2];   // PV of tiles t = b (mod 2) done
     uint64_t drain;
     uint64_t peer_done[2];   // pair: the peer's producer p has published how far it issued
@@ -252,7 +259,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     if (tid == 0) {
         for (int i = 0; i < ST; ++i) { mbar_init(&bars->full[i], 1); mbar_init(&bars->empty[i], 1); }
         mbar_init(&bars->q_full, 1);
-        for (int i = 0; i < 2; ++i) mbar_init(&bars->s_full[i], 1);
+        for (int i = 0; i < 2; ++i) { mbar_init(&bars->s_full[i], 1); mbar_init(&bars->s_free[i], 1); }
+        mbar_init(&bars->drain_pv, 1);
         mbar_init(&bars->p_full, PAIR ? 16 : 8);       // the softmax warps (of both CTAs of a pair)
         mbar_init(&bars->o_done[0], 1);
         mbar_init(&bars->o_done[1], 1);
@@ -285,7 +293,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const int T = count_tiles(a.cls, c_begin, c_end);
     const int n_pad = ((a.N + 31) / 32) * 32;          // a key row that is out of bounds
 
-    if (warp == 0 || warp == kTcWarps - 1) {
+    if (warp == 0 || warp == kProd1Warp) {
         // ----------------------------------------------------------- producers
         // Two producer warps issue alternate ring loads (global load index n:
         // producer n % 2): one thread issuing copies back to back is limited
@@ -459,14 +467,18 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     !mbar_wait(&bars->empty[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
                     note_abort(bars, err, 9, PAIR ? peer_flag : 0u);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
-        // (the leader of a pair issues for both CTAs; the peer's warp 1 only
-        // holds the TMEM allocation)
+    } else if (warp == 1 || warp == kPvWarp) {
+        // ----------------------------------------------------------- MMA issue
+        // Two issuing threads (of the leader, for a pair): warp 1 issues the
+        // QK^T MMAs, warp kPvWarp the PV MMAs, so each one's waits and commits
+        // overlap the other's MMAs on the tensor pipe.  Ring positions follow
+        // the producers' order K_0, K_1, V_0, K_2, V_1, ..., V_T-1.  Warp 1 of
+        // every CTA owns the TMEM allocation.
+        const bool is_qk = warp == 1;
         if (lane == 0 && T > 0 && leader) {
-            constexpr uint32_t id_qk = idesc_f16(PAIR ? 256 : 128, 128, BF16 ? 1 : 0, 0, 0);
             const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
-            int used = 0;                                   // ring loads consumed
+            auto pos_k = [&](int t) { return t == 0 ? 0 : NSK + (t - 1) * (NSK + NSV); };
+            auto pos_v = [&](int t) { return t < T - 1 ? 2 * NSK + t * (NSK + NSV) : NSK + (T - 1) * (NSK + NSV); };
             // a slot is free once its MMAs are done (in both CTAs of a pair)
             auto release = [&](int slot) {
                 if constexpr (PAIR) {
@@ -485,95 +497,100 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 if constexpr (PAIR) mma_commit_pair(at_peer(bar));
             };
             const uint32_t pf = PAIR ? peer_flag : 0u;
-            bool ok = wait_or_abort(bars, &bars->q_full, 0, err, 2, pf);
-            // S_t goes to TMEM buffer t % 2, over P_t-2.  It is issued right
-            // after PV_t-2 with no wait for PV_t-2 to complete: the tensor core
-            // executes one thread's MMAs in issue order, so PV_t-2 reads P_t-2
-            // before QK_t overwrites it, and the softmax of tile t-2 finished
-            // with S_t-2 before PV_t-2 was issued.  The tensor pipe then never
-            // waits for an MMA to drain between tiles.
-            auto issue_s = [&](int t) -> bool {
-                const int sb = t & 1;
-                tc_fence_after();
-                for (int s = 0; s < NSK; ++s) {
-                    const int slot = used % ST;
-                    if (!wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(used / ST) & 1u, err, 4, pf))
-                        return false;
-                    tc_fence_after();
-                    const uint32_t kb = ring_addr + slot * SLOT;
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024);
-                        const uint64_t bd = sw128_desc(kb + kk * 32, 16, 1024);
-                        if constexpr (PAIR) mma_f16_ss_pair(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
-                        else mma_f16_ss(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
-                    }
-                    release(slot);
-                    ++used;
-                }
-                commit_both(&bars->s_full[sb]);
-                return true;
-            };
-            if (ok) ok = issue_s(0);
-            if (ok && T > 1) ok = issue_s(1);
-            for (int t = 0; t < T && ok; ++t) {
-                ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf)
-                          : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf);
-                if (!ok) break;
-                tc_fence_after();
-                // V slots in runs of consecutive ring slots, one PV instruction
-                // per run and K step (single CTA: N = 64 x run length; pair: the
-                // tile's whole V group, N = DV over both CTAs).  P_t sits in
-                // TMEM over S_t: keys 64h + [0, 64) of the tile as P_hi in
-                // columns 64h + [0, 32) and P_lo in 64h + [32, 64), two 16-bit
-                // keys per column; each K step takes both terms.
-                for (int s = 0; s < NSV && ok;) {
-                    const int slot0 = used % ST;
-                    int len = 1;
-                    while (s + len < NSV && slot0 + len < ST) ++len;
-                    if (PAIR && len != NSV) {   // by construction a pair's V group never wraps
-                        note_abort(bars, err, 13, pf);
-                        ok = false;
-                        break;
-                    }
-                    for (int j = 0; j < len && ok; ++j)
-                        ok = wait_or_abort(bars, &bars->full[slot0 + j], static_cast<uint32_t>((used + j) / ST) & 1u,
-                                           err, 6, pf);
+            bool ok = true;
+            if (is_qk) {
+                // S_t = Q K_t^T into TMEM buffer t % 2, over P_t-2: issued once
+                // PV_t-2 has completed (s_free), the softmax of tile t-2 having
+                // finished with S_t-2 before PV_t-2 was issued.
+                constexpr uint32_t id_qk = idesc_f16(PAIR ? 256 : 128, 128, BF16 ? 1 : 0, 0, 0);
+                ok = wait_or_abort(bars, &bars->q_full, 0, err, 2, pf);
+                for (int t = 0; t < T && ok; ++t) {
+                    const int sb = t & 1;
+                    if (t >= 2) ok = wait_or_abort(bars, &bars->s_free[sb], static_cast<uint32_t>((t - 2) >> 1) & 1u,
+                                                   err, 3, pf);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t vb = ring_addr + slot0 * SLOT;
-                    if constexpr (PAIR) {
-                        // this CTA's half of the columns: sub-slab j (16 KB) in
-                        // slots 2j, 2j + 1; K step kk at kk * 2048 bytes
-                        const uint32_t id_pv = idesc_f16(256, DV, BF16 ? 1 : 0, 0, 1);
+                    const int p0 = pos_k(t);
+                    for (int s = 0; s < NSK && ok; ++s) {
+                        const int pos = p0 + s, slot = pos % ST;
+                        ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(pos / ST) & 1u, err, 4, pf);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t kb = ring_addr + slot * SLOT;
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
-                            const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
-                            mma_f16_ts_pair(tm_o, pa, bd, id_pv, (t | kk) != 0);
-                            mma_f16_ts_pair(tm_o, pa + 32, bd, id_pv, 1u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sw128_desc(q_addr + s * kSlab + kk * 32, 16, 1024);
+                            const uint64_t bd = sw128_desc(kb + kk * 32, 16, 1024);
+                            if constexpr (PAIR) mma_f16_ss_pair(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
+                            else mma_f16_ss(tm_s[sb], ad, bd, id_qk, (s | kk) != 0);
                         }
-                    } else {
-                        const uint32_t id_pv = idesc_f16(128, 64 * len, BF16 ? 1 : 0, 0, 1);
-#pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
-                            const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
-                            mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
-                            mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
-                        }
+                        release(slot);
                     }
-                    for (int j = 0; j < len; ++j) release(slot0 + j);
-                    used += len;
-                    s += len;
+                    if (ok) commit_both(&bars->s_full[sb]);
                 }
-                if (!ok) break;
-                commit_both(&bars->o_done[t & 1]);
-                if (t + 2 < T) ok = issue_s(t + 2);
+            } else {
+                for (int t = 0; t < T && ok; ++t) {
+                    ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf)
+                              : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf);
+                    if (!ok) break;
+                    tc_fence_after();
+                    // V slots in runs of consecutive ring slots, one PV
+                    // instruction per run and K step (single CTA: N = 64 x run
+                    // length; pair: the tile's whole V group, N = DV over both
+                    // CTAs).  P_t sits in TMEM over S_t: keys 64h + [0, 64) of
+                    // the tile as P_hi in columns 64h + [0, 32) and P_lo in
+                    // 64h + [32, 64), two 16-bit keys per column; each K step
+                    // takes both terms.
+                    int used = pos_v(t);
+                    for (int s = 0; s < NSV && ok;) {
+                        const int slot0 = used % ST;
+                        int len = 1;
+                        while (s + len < NSV && slot0 + len < ST) ++len;
+                        if (PAIR && len != NSV) {   // by construction a pair's V group never wraps
+                            note_abort(bars, err, 13, pf);
+                            ok = false;
+                            break;
+                        }
+                        for (int j = 0; j < len && ok; ++j)
+                            ok = wait_or_abort(bars, &bars->full[slot0 + j],
+                                               static_cast<uint32_t>((used + j) / ST) & 1u, err, 6, pf);
+                        if (!ok) break;
+                        tc_fence_after();
+                        const uint32_t vb = ring_addr + slot0 * SLOT;
+                        if constexpr (PAIR) {
+                            // this CTA's half of the columns: sub-slab j (16 KB)
+                            // in slots 2j, 2j + 1; K step kk at kk * 2048 bytes
+                            const uint32_t id_pv = idesc_f16(256, DV, BF16 ? 1 : 0, 0, 1);
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
+                                const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
+                                mma_f16_ts_pair(tm_o, pa, bd, id_pv, (t | kk) != 0);
+                                mma_f16_ts_pair(tm_o, pa + 32, bd, id_pv, 1u);
+                            }
+                        } else {
+                            const uint32_t id_pv = idesc_f16(128, 64 * len, BF16 ? 1 : 0, 0, 1);
+#pragma unroll
+                            for (int kk = 0; kk < 8; ++kk) {
+                                const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
+                                const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
+                                mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
+                                mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
+                            }
+                        }
+                        for (int j = 0; j < len; ++j) release(slot0 + j);
+                        used += len;
+                        s += len;
+                    }
+                    if (!ok) break;
+                    commit_both(&bars->o_done[t & 1]);
+                    commit_own(&bars->s_free[t & 1]);   // S_t / P_t buffer free once PV_t is done
+                }
             }
             // Drain: all MMAs issued by this thread have completed.
-            commit_own(&bars->drain);
-            if (!mbar_wait(&bars->drain, 0, kWaitIters)) note_abort(bars, err, 10, pf);
+            uint64_t *dr = is_qk ? &bars->drain : &bars->drain_pv;
+            commit_own(dr);
+            if (!mbar_wait(dr, 0, kWaitIters)) note_abort(bars, err, 10, pf);
         }
     } else if (warp >= 2) {
         // ---------------------------------------------- softmax and epilogue
@@ -801,7 +818,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     tc_fence_before();
     __syncthreads();
     if (cx > 1) cluster_sync();   // the merge reads the peers' staged rows (cx is uniform in a cluster)
-    const bool epi_warp = warp >= 2 && warp < kTcWarps - 1;   // the softmax warps
+    const bool epi_warp = warp >= 2 && warp < kProd1Warp;   // the softmax warps
     if (epi_warp && cx == 1) {
         // No merge in the cluster: each staged row (final and normalized, or
         // partial slot `split` with its (S, M)) leaves by one bulk copy issued
