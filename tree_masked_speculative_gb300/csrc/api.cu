@@ -135,7 +135,7 @@ uint32_t resolve_tree_nwg(const ta_tree_params *p) {
         // tensor-core kernel: one CTA per SM, CTAs = splits x row tiles x O halves x KV heads
         // and each split a run of whole 4-chunk key tiles (no split gets more tiles
         // than needed to cover the keys with at most one CTA per SM)
-        const uint64_t units = (uint64_t)p->n_kv_heads * (uint64_t)tree_tc_row_ctas((int)R) * (p->head_dim == 512 ? 2 : 1);
+        const uint64_t units = (uint64_t)p->n_kv_heads * (uint64_t)tree_tc_row_ctas((int)R, (int)p->head_dim) * (p->head_dim == 512 ? 2 : 1);
         const uint64_t tiles = (n_chunks + 3) / 4;
         uint64_t most = (uint64_t)sms / units;
         if (most < 1) most = 1;
@@ -327,7 +327,7 @@ ta_status plan_tree(const ta_tree_params *p, int kernel, const ta_buf *q, const 
         a.cluster_x = cx;
     }
     a.n_part = a.nwg / a.cluster_x == 1 ? 0 : a.nwg / a.cluster_x;
-    if (plan->use_tc && a.R > 128 && (uint64_t)a.nwg * (a.D == 512 ? 2u : 1u) > 65535u)
+    if (plan->use_tc && tree_tc_pairs(a.R, a.D) && (uint64_t)a.nwg * 2u > 65535u)
         return fail(TA_ERR_UNSUPPORTED, "tree_attention: nwg (%d) too large for the tensor-core kernel's grid", a.nwg);
     if (plan->use_tc && !get_encoder())
         return fail(TA_ERR_CUDA, "tree_attention: cuTensorMapEncodeTiled is not available");

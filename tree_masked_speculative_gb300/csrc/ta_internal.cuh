@@ -312,12 +312,16 @@ struct TreeWorkspace {
 cudaError_t launch_tree_classify(const TreeArgs &a, cudaStream_t s);
 cudaError_t launch_tree_fma(const TreeArgs &a, int kv_type, cudaStream_t s);
 cudaError_t launch_tree_tc(const TreeArgs &a, const TcMaps &maps, int kv_type, cudaStream_t s);
-// Row tiles (CTAs along the rows of a KV head) of the tensor-core kernel: one
-// 128-row tile, or, above 128 rows, an even number of tiles served by CTA
-// pairs (two tiles per pair).
-__host__ __device__ inline int tree_tc_row_ctas(int R) {
+// Whether the tensor-core tree kernel runs as CTA pairs (cta_group::2): head
+// dimension 512 with more than 128 rows per KV head, where each CTA then
+// loads half of every key tile (measured faster there; with D <= 256 the
+// one-CTA form is).
+__host__ __device__ inline bool tree_tc_pairs(int R, int D) { return R > 128 && D == 512; }
+// Row tiles (CTAs along the rows of a KV head) of the tensor-core kernel:
+// ceil(R / 128), rounded up to an even count for CTA pairs.
+__host__ __device__ inline int tree_tc_row_ctas(int R, int D) {
     const int n_rt = (R + 127) / 128;
-    return n_rt > 1 ? 2 * ((n_rt + 1) / 2) : 1;
+    return tree_tc_pairs(R, D) ? 2 * ((n_rt + 1) / 2) : n_rt;
 }
 // Cluster shape of the tensor-core kernel: x = splits merged in-cluster (y = 1).
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);

@@ -170,12 +170,17 @@ __device__ __forceinline__ void note_abort(Bars *b, int *err, int code, uint32_t
     atomicCAS(err, 0, code);
 }
 
+// Suspend-time hint (ns) of the waits of the producers and MMA issuers, whose
+// wake-up latency is on the ring's critical path; the softmax warps use 1 us.
+constexpr uint32_t kPipeHintNs = 1000;
+
 __device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code,
-                                              uint32_t peer_flag) {
+                                              uint32_t peer_flag, uint32_t hint_ns = 1000) {
     if (b->abort_flag) return false;
     // a waiting warp sleeps on the barrier (taking no issue slots from the
-    // MMA issuer and the softmax) for at most 2^21 tries of 1 us
-    if (mbar_try_wait(bar, parity) || mbar_wait_sleep(bar, parity, 1u << 21, 1000)) return true;
+    // other warps), at most about 2 s in all
+    if (mbar_try_wait(bar, parity) || mbar_wait_sleep(bar, parity, (1u << 21) * (1000u / hint_ns), hint_ns))
+        return true;
     note_abort(b, err, code, peer_flag);
     return false;
 }
@@ -183,10 +188,10 @@ __device__ __forceinline__ bool wait_or_abort(Bars *b, uint64_t *bar, uint32_t p
 // As wait_or_abort, for a barrier that threads of the peer CTA arrive on
 // (acquire at cluster scope).
 __device__ __forceinline__ bool wait_or_abort_cluster(Bars *b, uint64_t *bar, uint32_t parity, int *err, int code,
-                                                      uint32_t peer_flag) {
+                                                      uint32_t peer_flag, uint32_t hint_ns = 1000) {
     if (b->abort_flag) return false;
-    for (uint32_t i = 0; i < (1u << 21); ++i)
-        if (mbar_try_wait_cluster(bar, parity, 1000)) return true;
+    for (uint32_t i = 0; i < (1u << 21) * (1000u / hint_ns); ++i)
+        if (mbar_try_wait_cluster(bar, parity, hint_ns)) return true;
     note_abort(b, err, code, peer_flag);
     return false;
 }
@@ -233,7 +238,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     // cluster is the pair (cluster ranks 2k, 2k + 1), member 0 the leader that
     // issues the MMAs.  z = KV head.
     constexpr int kHalves = D / DV;
-    const int n_ct = PAIR ? 2 * (((a.R + 127) / 128 + 1) / 2) : (a.R + 127) / 128;   // row tiles
+    const int n_ct = tree_tc_row_ctas(a.R, D);         // row tiles
     const int member = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
     const bool leader = member == 0;
     const int split = PAIR ? static_cast<int>(blockIdx.y) / kHalves : static_cast<int>(blockIdx.x);
@@ -320,7 +325,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
                 bool ok = true;
                 if (lane == 0) {
-                    ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, 0u);
+                    ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, 0u, kPipeHintNs);
                     if (ok) {
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
                         unsigned char *dst = sRing + slot * SLOT;
@@ -358,7 +363,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             const uint32_t pass = static_cast<uint32_t>(n / ST);
             bool ok = true;
             if (lane == 0) {
-                ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, peer_flag);
+                ok = wait_or_abort(bars, &bars->empty[slot], (pass & 1u) ^ 1u, err, 1, peer_flag, kPipeHintNs);
                 if (ok) {
                     if (leader) mbar_arrive_expect_tx(&bars->full[slot], 2 * SLOT);
                     unsigned char *dst = sRing + slot * SLOT;
@@ -507,13 +512,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 for (int t = 0; t < T && ok; ++t) {
                     const int sb = t & 1;
                     if (t >= 2) ok = wait_or_abort(bars, &bars->s_free[sb], static_cast<uint32_t>((t - 2) >> 1) & 1u,
-                                                   err, 3, pf);
+                                                   err, 3, pf, kPipeHintNs);
                     if (!ok) break;
                     tc_fence_after();
                     const int p0 = pos_k(t);
                     for (int s = 0; s < NSK && ok; ++s) {
                         const int pos = p0 + s, slot = pos % ST;
-                        ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(pos / ST) & 1u, err, 4, pf);
+                        ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(pos / ST) & 1u, err, 4, pf, kPipeHintNs);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t kb = ring_addr + slot * SLOT;
@@ -530,8 +535,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 }
             } else {
                 for (int t = 0; t < T && ok; ++t) {
-                    ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf)
-                              : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf);
+                    ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf,
+                                                      kPipeHintNs)
+                              : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf, kPipeHintNs);
                     if (!ok) break;
                     tc_fence_after();
                     // V slots in runs of consecutive ring slots, one PV
@@ -553,7 +559,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         }
                         for (int j = 0; j < len && ok; ++j)
                             ok = wait_or_abort(bars, &bars->full[slot0 + j],
-                                               static_cast<uint32_t>((used + j) / ST) & 1u, err, 6, pf);
+                                               static_cast<uint32_t>((used + j) / ST) & 1u, err, 6, pf, kPipeHintNs);
                         if (!ok) break;
                         tc_fence_after();
                         const uint32_t vb = ring_addr + slot0 * SLOT;
@@ -961,8 +967,8 @@ static int max_active_clusters(int size) {
 
 }  // namespace
 
-// Splits merged inside one cluster.  More than 128 rows per KV head take the
-// CTA-pair kernel, whose cluster is the pair: no in-cluster merge (1).
+// Splits merged inside one cluster.  The CTA-pair form's cluster is the pair:
+// no in-cluster merge (1).
 // Otherwise all splits of a (row tile, O half, KV head) along x when they fit
 // in one cluster (at most 8 CTAs) and every cluster of the grid fits on the
 // device at once, so the merge completes inside the cluster and no partials
@@ -971,7 +977,7 @@ static int max_active_clusters(int size) {
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     *cx = 1;
     *cy = 1;
-    if (a.R > 128) return;
+    if (tree_tc_pairs(a.R, a.D)) return;
     const long total = static_cast<long>(a.nwg) * (a.D == 512 ? 2 : 1) * a.Hk;
     if (a.nwg > 1 && a.nwg <= 8) {
         const int n = max_active_clusters(a.nwg);
@@ -989,7 +995,7 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
     cudaError_t e = set_smem_limit_once(kern, Cfg::SMEM, &done);
     if (e != cudaSuccess) return e;
     constexpr unsigned halves = D / Cfg::DV;
-    const unsigned n_ct = static_cast<unsigned>(tree_tc_row_ctas(a.R));
+    const unsigned n_ct = static_cast<unsigned>(tree_tc_row_ctas(a.R, D));
     dim3 grid;
     unsigned cx, cy = 1;
     if (PAIR) {
@@ -1009,8 +1015,10 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
 
 template <int D, bool BF16, bool IMPLICIT>
 cudaError_t launch_tc_rows(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
-    return a.R > 128 ? launch_tc_one<D, BF16, IMPLICIT, true>(a, maps, s)
-                     : launch_tc_one<D, BF16, IMPLICIT, false>(a, maps, s);
+    if constexpr (D == 512) {
+        if (tree_tc_pairs(a.R, D)) return launch_tc_one<D, BF16, IMPLICIT, true>(a, maps, s);
+    }
+    return launch_tc_one<D, BF16, IMPLICIT, false>(a, maps, s);
 }
 
 template <bool BF16>
