@@ -62,8 +62,8 @@ def parse():
                     help="kernel family of the main pass: 0 automatic, 1 CUDA cores, 2 tensor cores "
                          "where the shape allows them")
     ap.add_argument("--tree-mask", default="dense", choices=["dense", "parents"],
-                    help="tree workloads: the mask as the dense f32 array (tree_attn_fwd) or as the "
-                         "parent array (tree_attn_fwd_parents)")
+                    help="tree and draft-tree workloads: the mask as the dense array (tree_attn_fwd, "
+                         "quant_sdpa_fwd) or as the parent array (tree_attn_fwd_parents, quant_sdpa_fwd_tree)")
     ap.add_argument("--kv-sets", type=int, default=0,
                     help="K/V copies to rotate over (0 = enough to exceed 3x L2)")
     return ap.parse_args()
@@ -264,9 +264,15 @@ class TreeBench:
 
 # ------------------------------------------------------------ quant arm
 class QuantBench:
-    def __init__(self, ta, wl: W.QuantWorkload, dev, kv_sets=0, kernel=0):
+    def __init__(self, ta, wl: W.QuantWorkload, dev, kv_sets=0, kernel=0, tree_mask="dense"):
         self.ta, self.wl, self.dev = ta, wl, dev
         inp = W.make_quant_inputs(wl)
+        self.oracle_inputs = inp             # the same mask, dense, for the CPU baseline
+        # a draft-tree workload may take its tree mask as the parent array (no mask read)
+        self.tree = None
+        if tree_mask == "parents" and inp.get("tree_parents") is not None:
+            self.tree = torch.tensor(inp["tree_parents"], dtype=torch.int32, device=dev)
+            inp = dict(inp, mask_float=None)
         self.host = inp
         d = {k: (v.to(dev) if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
         self.d = d
@@ -288,15 +294,23 @@ class QuantBench:
         self.dtype = "u%d" % wl.bits
         self.tc = ta.quant_sdpa_uses_tensor_cores(self.p) == 1
         kern = "quant_tc_kernel (tensor cores)" if self.tc else "quant_kernel (CUDA cores)"
-        self.fwd_label = "main pass (%s) + split merge (quant_sdpa_fwd, one call)" % kern
+        call = "quant_sdpa_fwd_tree" if self.tree is not None else "quant_sdpa_fwd"
+        self.fwd_label = "main pass (%s) + split merge (%s, one call)" % (kern, call)
+
+    def _fwd(self, e, kv):
+        if self.tree is not None:
+            self.ta.quant_sdpa_fwd_tree(self.p, int(self.tree.numel()), self.tree, e["queries"], kv["k_packed"],
+                                        kv["k_scales"], kv["k_biases"], kv["v_packed"], kv["v_scales"],
+                                        kv["v_biases"], e["sinks"] if self.wl.has_sinks else None,
+                                        e.get("mask_bool"), self.tmp, self.out)
+        else:
+            self.ta.quant_sdpa_fwd(self.p, e["queries"], kv["k_packed"], kv["k_scales"], kv["k_biases"],
+                                   kv["v_packed"], kv["v_scales"], kv["v_biases"],
+                                   e["sinks"] if self.wl.has_sinks else None, e.get("mask_bool"),
+                                   e.get("mask_float"), self.tmp, self.out)
 
     def step(self, i, fwd_only=False):
-        s = self.sets[i % self.nsets]
-        d = self.d
-        self.ta.quant_sdpa_fwd(self.p, d["queries"], s["k_packed"], s["k_scales"], s["k_biases"],
-                               s["v_packed"], s["v_scales"], s["v_biases"],
-                               d["sinks"] if self.wl.has_sinks else None, d.get("mask_bool"),
-                               d.get("mask_float"), self.tmp, self.out)
+        self._fwd(self.d, self.sets[i % self.nsets])
 
     def config(self):
         wl = self.wl
@@ -304,6 +318,7 @@ class QuantBench:
                 "n_kv_heads": wl.n_kv_heads, "dim": wl.dim, "tokens": wl.tokens, "bits": wl.bits,
                 "group_size": wl.group_size, "window_size": wl.window_size, "splits": self.nwg,
                 "kernel": "tensor cores" if self.tc else "CUDA cores",
+                "tree_mask": "parent array" if self.tree is not None else None,
                 "l2": "rotating %d K/V sets, %.0f MB read per rotation (> 3x L2)" % (
                     self.nsets, self.nsets * self.bytes_per_step / 1e6)}
 
@@ -317,8 +332,10 @@ class QuantBench:
                 t = t[:, lo:]
             self.h[k] = t.contiguous().pin_memory()
         for k in ("mask_bool", "mask_float"):
-            if self.host.get(k) is not None:
+            if self.host.get(k) is not None and not (k == "mask_float" and self.tree is not None):
                 self.h[k] = self.host[k][:, lo:].contiguous().pin_memory()
+        if self.tree is not None:
+            self.h["tree_parents"] = self.tree.cpu().pin_memory()
         self.h_out = torch.empty_like(self.out, device="cpu").pin_memory()
         self.e2e_h2d = sum(t.numel() * t.element_size() for t in self.h.values())
         self.e2e_d2h = self.h_out.numel() * self.h_out.element_size()
@@ -340,13 +357,12 @@ class QuantBench:
         for k in ("mask_bool", "mask_float"):
             if k in self.h:
                 e[k][:, lo:].copy_(self.h[k], non_blocking=True)
+        if self.tree is not None:
+            self.tree.copy_(self.h["tree_parents"], non_blocking=True)
 
     def e2e_compute(self, i):
         e = self.e2e_sets[i % 2]
-        self.ta.quant_sdpa_fwd(self.p, e["queries"], e["k_packed"], e["k_scales"], e["k_biases"],
-                               e["v_packed"], e["v_scales"], e["v_biases"],
-                               e["sinks"] if self.wl.has_sinks else None, e.get("mask_bool"),
-                               e.get("mask_float"), self.tmp, self.out)
+        self._fwd(e, e)
         self.h_out.copy_(self.out, non_blocking=True)
 
     def status_word(self):
@@ -355,7 +371,7 @@ class QuantBench:
 
     def cpu_reference(self, rows, threads):
         import oracle
-        return oracle.quant_oracle_for(self.wl, self.host, rows=rows, threads=threads)
+        return oracle.quant_oracle_for(self.wl, self.oracle_inputs, rows=rows, threads=threads)
 
     def all_rows(self):
         return list(range(self.wl.rows))
@@ -365,7 +381,7 @@ def make_bench(ta, name, dev, kv_sets=0, tree_mask="dense", kernel=0):
     wl = WORKLOADS[name]
     if isinstance(wl, W.TreeWorkload):
         return TreeBench(ta, wl, dev, kv_sets, tree_mask, kernel)
-    return QuantBench(ta, wl, dev, kv_sets, kernel)
+    return QuantBench(ta, wl, dev, kv_sets, kernel, tree_mask)
 
 
 # ------------------------------------------------------------ timing

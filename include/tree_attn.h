@@ -331,6 +331,28 @@ ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queries, const 
                          const ta_buf *mask_bool, const ta_buf *mask_float, const ta_buf *tmp,
                          const ta_buf *out, void *stream);
 
+/*
+ * quant_sdpa_fwd for draft-tree verification on a quantized cache, with the
+ * tree mask given as a parent array instead of a dense [B*nQ, tokens] float
+ * mask (the tree semantics of [TA-M]'s header comment applied to the rows of
+ * [FQS]): the q_l draft nodes are the last q_l tokens of the cache, query row
+ * q is node q % q_l (rows ordered (batch, head, node), so n_q_heads counts
+ * heads x q_l), and row q attends every token before the tree plus the tree
+ * positions of its node's ancestors and of itself - the tokens an additive
+ * float mask of 0 there and -65504 on the other tree positions leaves, with no
+ * mask read from memory.  Window, bool mask and sinks apply as in
+ * quant_sdpa_fwd; there is no float mask.
+ *   q_l      1..32 nodes; n_q_heads must be a multiple of q_l; q_l <= tokens.
+ *   parents  [q_l] i32 on the device, the rule of tree_mask_build (a chain i,
+ *            parents[i], ... ends at a value outside [0, current node)).
+ * Other buffers and errors as quant_sdpa_fwd; q_l > 32 is TA_ERR_UNSUPPORTED.
+ */
+ta_status quant_sdpa_fwd_tree(const ta_quant_params *p, uint32_t q_l, const ta_buf *parents,
+                              const ta_buf *queries, const ta_buf *k_packed, const ta_buf *k_scales,
+                              const ta_buf *k_biases, const ta_buf *v_packed, const ta_buf *v_scales,
+                              const ta_buf *v_biases, const ta_buf *sinks, const ta_buf *mask_bool,
+                              const ta_buf *tmp, const ta_buf *out, void *stream);
+
 /* ----------------------------------------------------------------- misc */
 
 /* Message for the calling thread's last non-TA_OK status ("" if none). */

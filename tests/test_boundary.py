@@ -368,3 +368,27 @@ def test_quant_kernel_family_choice(ta):
     assert ta.quant_sdpa_uses_tensor_cores(p(256, G=16, nQ=256, bits=8, kernel=2)) == 0   # 16 groups x 32 rows
     assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1           # invalid params
     assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128, kernel=1)) == 0
+
+
+@pytest.mark.parametrize("q_l,nQ,tokens,pbytes,pdtype,st_want,frag", [
+    (0, 8, 100, 64, "I32", 1, "q_l must be > 0"),
+    (33, 66, 100, 33 * 4, "I32", 4, "<= 32"),
+    (8, 12, 100, 32, "I32", 1, "multiple of q_l"),
+    (8, 16, 5, 32, "I32", 1, "<= tokens"),
+    (8, 16, 100, 32, "U32", 1, "parents dtype"),
+    (8, 16, 100, 28, "I32", 2, "parents"),
+    (8, 16, 100, None, None, 1, "parents is NULL"),
+])
+def test_quant_tree_rejections(ta, q_l, nQ, tokens, pbytes, pdtype, st_want, frag):
+    """quant_sdpa_fwd_tree's own checks, before any launch."""
+    p = ta.quant_params(1, nQ, 2, 128, tokens, 4, 64, 0, 0, 0.1, 1, 1)
+    B = lambda n, c: ctypes.byref(_b(ta, n, c))
+    big = 1 << 30
+    code = {"I32": ta.TA_I32, "U32": ta.TA_U32}
+    par = B(pbytes, code[pdtype]) if pbytes is not None else None
+    before = ta.ta_launch_count()
+    st = ta.lib.quant_sdpa_fwd_tree(ctypes.byref(p), q_l, par, B(big, ta.TA_F16), B(big, ta.TA_U32),
+                                    B(big, ta.TA_F16), B(big, ta.TA_F16), B(big, ta.TA_U32), B(big, ta.TA_F16),
+                                    B(big, ta.TA_F16), None, None, B(big, ta.TA_F32), B(big, ta.TA_F16), None)
+    assert ta.ta_launch_count() == before
+    assert st == st_want and frag in ta.ta_last_error(), ta.ta_last_error()

@@ -230,3 +230,50 @@ def test_bounded_wait_timeout_sets_status_and_returns(ta):
     with pytest.raises(ta.TreeAttentionError, match="CUDA-core kernel only"):
         ta.ta_test_quant_sdpa_fwd_wait_limit(0, p2, *args[:-2], tmp2, out)
     assert ta.ta_launch_count() == before
+
+
+TREE_CASES = [
+    # q_l, bits, dtype, dim, G, N, window, bool fraction, sinks, heads per KV row
+    (8, 4, "f16", 128, 64, 700, 0, 0.0, 0, 4),      # 32 rows per KV row
+    (4, 8, "bf16", 128, 32, 333, 200, 0.1, 1, 2),   # window and bool mask
+    (16, 4, "bf16", 64, 32, 129, 0, 0.0, 1, 1),     # 16 rows
+    (32, 4, "f16", 128, 64, 500, 0, 0.0, 0, 1),     # the largest tree
+    (1, 8, "f16", 256, 64, 90, 0, 0.2, 1, 3),       # a single node
+    (8, 4, "f16", 128, 64, 1000, 0, 0.0, 0, 4),
+]
+
+
+@pytest.mark.parametrize("q_l,bits,dtype,dim,G,N,window,bfrac,sinks,hpk", TREE_CASES,
+                         ids=[str(i) for i in range(len(TREE_CASES))])
+def test_quant_tree_as_parent_array(ta, kern, q_l, bits, dtype, dim, G, N, window, bfrac, sinks, hpk):
+    """A draft tree verified on a quantized cache with the tree mask given as the
+    parent array of the last q_l tokens (no mask read): the same output, bit for
+    bit, as the dense additive mask that tree_mask_build's rule gives, and the
+    oracle on that dense mask."""
+    wl = qwl(B=2, nQ=2 * hpk * q_l, nKV=2, dim=dim, G=G, N=N, bits=bits, sinks=sinks, window=window,
+             dtype=dtype, fmask="tree%d" % q_l, bfrac=bfrac, seed=q_l * 7 + N)
+    inp = W.make_quant_inputs(wl)
+    ref = oracle.quant_oracle_for(wl, inp)
+    dense = run_quant(ta, wl, inp, out_dtype=torch.float32, kernel=kern)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    par = torch.tensor(inp["tree_parents"], dtype=torch.int32, device="cuda")
+    tree = ta.quant_sdpa(d, batch=wl.batch, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, dim=wl.dim,
+                         tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size, has_sinks=wl.has_sinks,
+                         window_size=wl.window_size, scale=wl.scale, out_dtype=torch.float32, kernel=kern,
+                         tree_parents=par)
+    torch.cuda.synchronize()
+    assert_close(tree.cpu().double().numpy(), ref, what="quant tree as parents")
+    assert torch.equal(tree, dense)
+
+
+def test_quant_tree_workload_as_parent_array(ta, kern):
+    wl = W.QUANT_TREE
+    inp = W.make_quant_inputs(wl)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+    par = torch.tensor(inp["tree_parents"], dtype=torch.int32, device="cuda")
+    got = ta.quant_sdpa(d, batch=wl.batch, n_q_heads=wl.n_q_heads, n_kv_heads=wl.n_kv_heads, dim=wl.dim,
+                        tokens=wl.tokens, bits=wl.bits, group_size=wl.group_size, has_sinks=wl.has_sinks,
+                        window_size=wl.window_size, scale=wl.scale, out_dtype=torch.float32, kernel=kern,
+                        tree_parents=par)
+    torch.cuda.synchronize()
+    assert_close(got.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp), what="quant tree workload, parents")

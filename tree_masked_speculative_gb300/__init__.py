@@ -22,7 +22,7 @@ __all__ = [
     "tree_attn_fwd_causal", "tree_attn_fwd_parents", "tree_attn_fwd_ex", "tree_attn_status_offset",
     "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
     "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "quant_sdpa_uses_tensor_cores",
-    "ta_test_quant_sdpa_fwd_wait_limit", "tree_attention", "quant_sdpa", "tree_params", "quant_params",
+    "ta_test_quant_sdpa_fwd_wait_limit", "quant_sdpa_fwd_tree", "tree_attention", "quant_sdpa", "tree_params", "quant_params",
     "tree_mask_build", "TreeOptions", "KERNEL_AUTO", "KERNEL_CUDA_CORES", "KERNEL_TENSOR_CORES",
 ]
 
@@ -109,6 +109,8 @@ def _load() -> ctypes.CDLL:
     L.ta_last_error.restype = ctypes.c_char_p
     L.ta_launch_count.argtypes = []
     L.ta_launch_count.restype = ctypes.c_uint64
+    L.quant_sdpa_fwd_tree.argtypes = [PQ, u32] + [B] * 12 + [P]
+    L.quant_sdpa_fwd_tree.restype = ctypes.c_int
     L.ta_test_quant_sdpa_fwd_wait_limit.argtypes = [u32, PQ] + [B] * 12 + [P]
     L.ta_test_quant_sdpa_fwd_wait_limit.restype = ctypes.c_int
     L.quant_sdpa_uses_tensor_cores.argtypes = [PQ]
@@ -256,6 +258,16 @@ def quant_sdpa_fwd(p: QuantParams, queries, k_packed, k_scales, k_biases, v_pack
                                                             tmp, out), _stream(stream)))
 
 
+def quant_sdpa_fwd_tree(p: QuantParams, q_l: int, parents, queries, k_packed, k_scales, k_biases, v_packed,
+                        v_scales, v_biases, sinks, mask_bool, tmp, out, stream=None):
+    """Quantized-KV attention of draft-tree rows (row q = node q % q_l) with the
+    tree mask as the int32 parent array of the last q_l tokens."""
+    b = _quant_bufs(queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool, None,
+                    tmp, out)
+    _check(lib.quant_sdpa_fwd_tree(ctypes.byref(p), q_l, buf(parents, TA_I32), *b[:9], b[10], b[11],
+                                   _stream(stream)))
+
+
 def ta_test_quant_sdpa_fwd_wait_limit(first_wait_polls: int, p: QuantParams, queries, k_packed, k_scales,
                                       k_biases, v_packed, v_scales, v_biases, sinks, mask_bool, mask_float, tmp,
                                       out, stream=None):
@@ -304,8 +316,12 @@ def tree_attention(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, mask: Opti
 def quant_sdpa(inputs: dict, *, batch: int, n_q_heads: int, n_kv_heads: int, dim: int, tokens: int,
                bits: int, group_size: int, has_sinks: int, window_size: int, scale: float,
                nwg: int = 0, out_dtype: Optional[torch.dtype] = None, tmp=None, out=None,
-               kernel: int = KERNEL_AUTO, stream=None) -> torch.Tensor:
-    """Quantized-KV attention on device tensors (dict as made by workloads.make_quant_inputs)."""
+               kernel: int = KERNEL_AUTO, tree_parents: Optional[torch.Tensor] = None,
+               stream=None) -> torch.Tensor:
+    """Quantized-KV attention on device tensors (dict as made by workloads.make_quant_inputs).
+    With `tree_parents` (int32 [q_l] on the device) the rows are draft-tree nodes
+    (row q = node q % q_l) masked by that tree over the last q_l tokens, and the
+    dict's float mask is not used."""
     p = quant_params(batch, n_q_heads, n_kv_heads, dim, tokens, bits, group_size, has_sinks,
                      window_size, scale, nwg, kernel)
     dev = inputs["queries"].device
@@ -317,6 +333,12 @@ def quant_sdpa(inputs: dict, *, batch: int, n_q_heads: int, n_kv_heads: int, dim
     if out is None:
         out = torch.empty((batch * n_q_heads, dim), dtype=out_dtype or inputs["queries"].dtype,
                           device=dev)
+    if tree_parents is not None:
+        quant_sdpa_fwd_tree(p, int(tree_parents.numel()), tree_parents, inputs["queries"], inputs["k_packed"],
+                            inputs["k_scales"], inputs["k_biases"], inputs["v_packed"], inputs["v_scales"],
+                            inputs["v_biases"], inputs["sinks"] if has_sinks else None, inputs.get("mask_bool"),
+                            tmp, out, stream)
+        return out
     quant_sdpa_fwd(p, inputs["queries"], inputs["k_packed"], inputs["k_scales"], inputs["k_biases"],
                    inputs["v_packed"], inputs["v_scales"], inputs["v_biases"],
                    inputs["sinks"] if has_sinks else None, inputs.get("mask_bool"),

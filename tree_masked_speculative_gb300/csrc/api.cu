@@ -697,7 +697,8 @@ ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, cons
                          const ta_buf *k_scales_d, const ta_buf *k_biases_d, const ta_buf *v_packed_d,
                          const ta_buf *v_scales_d, const ta_buf *v_biases_d, const ta_buf *sinks_d,
                          const ta_buf *mask_bool_d, const ta_buf *mask_float_d, const ta_buf *tmp_d,
-                         const ta_buf *out_d, void *stream, uint32_t first_wait_polls, bool test_hook) {
+                         const ta_buf *out_d, void *stream, uint32_t first_wait_polls, bool test_hook,
+                         uint32_t tree_ql = 0, const ta_buf *parents_d = nullptr) {
     const ta_buf &queries = deref(queries_d), &k_packed = deref(k_packed_d), &k_scales = deref(k_scales_d);
     const ta_buf &k_biases = deref(k_biases_d), &v_packed = deref(v_packed_d), &v_scales = deref(v_scales_d);
     const ta_buf &v_biases = deref(v_biases_d), &sinks = deref(sinks_d), &mask_bool = deref(mask_bool_d);
@@ -747,6 +748,21 @@ ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, cons
     TA_TRY(check_buf(v_scales, "quant_sdpa: v_scales", req_sb, 2));
     TA_TRY(check_buf(v_biases, "quant_sdpa: v_biases", req_sb, 2));
     if (p->has_sinks) TA_TRY(check_buf(sinks, "quant_sdpa: sinks", (uint64_t)p->n_q_heads * 4, 4));
+    if (tree_ql > 0) {
+        // a draft tree over the last tree_ql tokens, as a parent array
+        if (tree_ql > (uint32_t)kMaxQuantTreeNodes)
+            return fail(TA_ERR_UNSUPPORTED, "quant_sdpa_fwd_tree: q_l (%u) must be <= %d", tree_ql, kMaxQuantTreeNodes);
+        if (tree_ql > p->tokens)
+            return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa_fwd_tree: q_l (%u) must be <= tokens (%u)", tree_ql,
+                        p->tokens);
+        if (p->n_q_heads % tree_ql != 0)
+            return fail(TA_ERR_INVALID_ARGUMENT,
+                        "quant_sdpa_fwd_tree: n_q_heads (%u) must be a multiple of q_l (%u): rows are (head, node)",
+                        p->n_q_heads, tree_ql);
+        if (absent(parents_d)) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa_fwd_tree: parents is NULL");
+        if (parents_d->dtype != TA_I32) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa_fwd_tree: parents dtype must be I32");
+        TA_TRY(check_buf(*parents_d, "quant_sdpa_fwd_tree: parents", (uint64_t)tree_ql * 4, 4));
+    }
     if (has_bool) TA_TRY(check_buf(mask_bool, "quant_sdpa: mask_bool", req_mb, 4));
     if (has_float) TA_TRY(check_buf(mask_float, "quant_sdpa: mask_float", req_mf, 2));
     TA_TRY(check_buf(out, "quant_sdpa: out", req_out, out.dtype == TA_F32 ? 4 : 2));
@@ -802,6 +818,8 @@ ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, cons
     QtcShape sh;
     QtcPlan pl;
     a.first_wait_polls = first_wait_polls;
+    a.tree_ql = (int)tree_ql;
+    a.tree_parents = tree_ql > 0 ? static_cast<const int32_t *>(parents_d->ptr) : nullptr;
     const bool use_tc = quant_tc_shape(p, &sh) && quant_tc_plan(p, sh, has_bool, has_float, &pl);
     if (test_hook && use_tc)
         return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: the wait-limit test hook takes the CUDA-core kernel only "
@@ -839,6 +857,16 @@ TA_EXPORT ta_status quant_sdpa_fwd(const ta_quant_params *p, const ta_buf *queri
                                    const ta_buf *out, void *stream) {
     return quant_fwd_impl(p, queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool,
                           mask_float, tmp, out, stream, kQuantWaitPolls, false);
+}
+
+TA_EXPORT ta_status quant_sdpa_fwd_tree(const ta_quant_params *p, uint32_t q_l, const ta_buf *parents,
+                                        const ta_buf *queries, const ta_buf *k_packed, const ta_buf *k_scales,
+                                        const ta_buf *k_biases, const ta_buf *v_packed, const ta_buf *v_scales,
+                                        const ta_buf *v_biases, const ta_buf *sinks, const ta_buf *mask_bool,
+                                        const ta_buf *tmp, const ta_buf *out, void *stream) {
+    if (q_l == 0) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa_fwd_tree: q_l must be > 0");
+    return quant_fwd_impl(p, queries, k_packed, k_scales, k_biases, v_packed, v_scales, v_biases, sinks, mask_bool,
+                          nullptr, tmp, out, stream, kQuantWaitPolls, false, q_l, parents);
 }
 
 TA_EXPORT ta_status ta_test_quant_sdpa_fwd_wait_limit(uint32_t first_wait_polls, const ta_quant_params *p,

@@ -199,6 +199,14 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     const bool qk_live = d0 < dim;
     const int g_qk = qk_live ? d0 / G : 0;
     const int r_l = j % REP;   // row of the lane's reduced scores
+    // draft tree over the last tree_ql tokens: the ancestor bitset of the lane's
+    // row's node (lane i < tree_ql builds node i's, the row's node takes it)
+    const int tree_lo = N - a.tree_ql;
+    uint32_t tree_bits = 0u;
+    if (a.tree_ql > 0) {
+        const uint32_t mine = lane < a.tree_ql ? quant_tree_ancestors(a.tree_parents, a.tree_ql, lane) : 0u;
+        tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
+    }
     const int pb_l = j / REP;  // pass (within a batch) of the lane's reduced scores
     // value-pass roles: lane = (token in pass tv, word slot wl)
     const int tv = lane / S::LPV, wl = lane % S::LPV;
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
             const int t = t0 + tk[bb];
             bool g = r_l < nrow && t >= a.t_lo && t < N;
             if (g && a.mbool != nullptr) g = sMb[r_l * CH + tk[bb]] != 0u;
+            if (g && a.tree_ql > 0 && t >= tree_lo) g = (tree_bits >> (t - tree_lo)) & 1u;
             live[bb] = g;
             any |= g;
         }

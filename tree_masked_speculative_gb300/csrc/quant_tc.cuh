@@ -240,6 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     float *sMax = reinterpret_cast<float *>(smem + L.red);
     float *sSum = sMax + 512;
     float *sMrow = sSum + 256;
+    uint32_t *sTree = reinterpret_cast<uint32_t *>(sMrow + 32);   // [32] ancestor bitsets of a draft tree
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int split = blockIdx.x, rb = blockIdx.y % a.n_rb, kv = blockIdx.y / a.n_rb;
     const int q0 = kv * a.rep + rb * RR;
@@ -577,11 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                                                 (pos & 7) * 2) = __float2half_rn(x[i][e] * down);
                 }
             }
+            // draft tree over the last tree_ql tokens: node bitsets, by the first warp
+            if (sw == 0 && lane < a.tree_ql) sTree[lane] = quant_tree_ancestors(a.tree_parents, a.tree_ql, lane);
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->q_ready);
         }
-        bool ok = waitw(bars, &bars->q_ready, 0, err);      // every warp's rows (sF, sQG)
+        bool ok = waitw(bars, &bars->q_ready, 0, err);      // every warp's rows (sF, sQG, sTree)
+        const int tree_lo = N - a.tree_ql;
 
         float lsum[RH];
 #pragma unroll
@@ -632,6 +636,13 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
 #pragma unroll
                 for (int r = 0; r < RH; ++r)
                     if (hr0 + r < rows_here && mb[(hr0 + r) * 128] == 0u) lg[r] = -INFINITY;
+            }
+            if (a.tree_ql > 0 && tok >= tree_lo && tok < N) {
+                // a tree position: row q attends it if it is node q % tree_ql or one of its ancestors
+                const int jt = tok - tree_lo;
+#pragma unroll
+                for (int r = 0; r < RH; ++r)
+                    if (!((sTree[(q0 + hr0 + r) % a.tree_ql] >> jt) & 1u)) lg[r] = -INFINITY;
             }
             __syncwarp();
             if (lane == 0 && ok) mbar_arrive(&bars->vempty[vslot]);   // scales and masks read

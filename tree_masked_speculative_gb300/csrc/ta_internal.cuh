@@ -171,6 +171,8 @@ struct QuantArgs {
     int al_mf;               // float-mask chunks start on 16-byte boundaries
     int *err;                // error word (bit 0: a copy wait timed out), never cleared here
     uint32_t first_wait_polls;   // CUDA-core kernel: bound of each CTA's first copy wait
+    const int32_t *tree_parents; // [tree_ql] parent array of a draft tree over the last tree_ql tokens, or nullptr
+    int tree_ql;                 // 0: no tree mask; else row q is node q % tree_ql of that tree
     int t_is_bf16, out_f32;
     float scale;
     // tensor-core kernel only: rows per CTA (4, 8, 16 or 32), row blocks per KV row,
@@ -178,6 +180,23 @@ struct QuantArgs {
     // chunks, packed-K slots, packed-V slots) and TMEM columns
     int rp, n_rb, j_lo, ntile, tc_nd, tc_nk, tc_nv, tc_cols;
 };
+
+// Largest draft tree a quantized-KV call takes as a parent array (one 32-bit
+// ancestor bitset per node).
+constexpr int kMaxQuantTreeNodes = 32;
+
+// Ancestor bitset of node i (i itself and the chain i, parents[i], ... that a
+// value outside [0, current node) ends - the rule of tree_mask_build), i < L.
+__device__ __forceinline__ uint32_t quant_tree_ancestors(const int32_t *parents, int L, int i) {
+    uint32_t bits = 1u << i;
+    for (int node = i, steps = 0; steps < L; ++steps) {   // each step goes to a smaller node
+        const int up = __ldg(parents + node);
+        if (up < 0 || up >= node) break;
+        bits |= 1u << up;
+        node = up;
+    }
+    return bits;
+}
 
 // Bound (polls) of every mbarrier wait of the CUDA-core quantized-KV kernel.
 constexpr uint32_t kQuantWaitPolls = 1u << 22;

@@ -257,7 +257,9 @@ def make_quant_inputs(wl: QuantWorkload) -> dict:
     """Host tensors laid out as the quantized-SDPA page states:
     queries [B*nQ, dim] T; k/v_packed [B*nKV, N, dim*bits/32] u32 (int32 storage);
     k/v_scales and k/v_biases [B*nKV, N, dim/G] T; sinks [nQ] f32;
-    mask_bool [B*nQ, N] u32 (or None); mask_float [B*nQ, N] T (or None)."""
+    mask_bool [B*nQ, N] u32 (or None); mask_float [B*nQ, N] T (or None);
+    tree_parents: for a "tree<q_l>" float mask, the parent list of that draft
+    tree (row r is node r % q_l over the last q_l tokens), else None."""
     g = torch.Generator().manual_seed(wl.seed)
     T = DTYPES[wl.dtype]
     rows, kvr, N = wl.rows, wl.kv_rows, wl.tokens
@@ -288,16 +290,18 @@ def make_quant_inputs(wl: QuantWorkload) -> dict:
             idx = torch.randperm(N, generator=g)[:n_zero]
             mask_bool[r, idx] = 0
     mask_float = None
+    tree_parents = None
     if wl.float_mask == "alibi":
         mask_float = alibi_mask(rows, wl.n_q_heads, N, T)
     elif wl.float_mask.startswith("tree"):
         q_l = int(wl.float_mask[len("tree"):])
-        tm = tree_mask(fixed_tree_parents((4, 2, 2, 1, 1), q_l), N, N)      # [q_l, N]
+        tree_parents = fixed_tree_parents((4, 2, 2, 1, 1), q_l)
+        tm = tree_mask(tree_parents, N, N)      # [q_l, N]
         mask_float = tm.repeat(rows // q_l, 1).to(T)
     return {"queries": queries, "k_packed": k_packed, "k_scales": k_scales,
             "k_biases": k_biases, "v_packed": v_packed, "v_scales": v_scales,
             "v_biases": v_biases, "sinks": sinks, "mask_bool": mask_bool,
-            "mask_float": mask_float}
+            "mask_float": mask_float, "tree_parents": tree_parents}
 
 
 QUANT_B4 = QuantWorkload(
