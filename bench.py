@@ -188,6 +188,7 @@ class TreeBench:
         self.use_parents = tree_mask == "parents"
         self.fwd_label = ("ancestor bitsets + mask compaction + main pass (tree_attn_fwd_parents)"
                           if self.use_parents else "mask compaction + main pass (tree_attn_fwd)")
+        self.traffic_key = traffic_key(wl.name, self.use_parents, kernel)
         self.built_mask = None
 
     def mask_step(self, i):
@@ -296,6 +297,7 @@ class QuantBench:
         kern = "quant_tc_kernel (tensor cores)" if self.tc else "quant_kernel (CUDA cores)"
         call = "quant_sdpa_fwd_tree" if self.tree is not None else "quant_sdpa_fwd"
         self.fwd_label = "main pass (%s) + split merge (%s, one call)" % (kern, call)
+        self.traffic_key = traffic_key(wl.name, self.tree is not None, kernel)
 
     def _fwd(self, e, kv):
         if self.tree is not None:
@@ -534,7 +536,7 @@ def run_ours(args):
     us_step = ms * 1e3 / args.steps
     value = bench.bytes_per_step * args.steps / (ms * 1e-3) / 1e9
     achieved = bench.bytes_per_step * args.steps / (ms_fwd * 1e-3) / 1e9
-    traffic = committed_traffic(bench.name)
+    traffic = committed_traffic(bench.traffic_key)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -566,7 +568,13 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
-def committed_traffic(name):
+def traffic_key(name, parents, kernel):
+    """Entry of the committed DRAM-traffic table for a workload run: the mask
+    form and a forced kernel family select different kernels."""
+    return name + ("|parents" if parents else "") + ("|kernel%d" % kernel if kernel else "")
+
+
+def committed_traffic(key):
     """DRAM bytes per launch of the main kernel from the committed ncu summary,
     or None when absent or taken on an older version of the kernel sources."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -575,7 +583,7 @@ def committed_traffic(name):
     try:
         with open(path) as f:
             d = json.load(f)
-        ent = d.get(name)
+        ent = d.get(key)
         if not ent:
             return None
         import hashlib

@@ -32,6 +32,12 @@ def test_committed_traffic_follows_the_source_hash(tmp_path, monkeypatch):
     assert bench.committed_traffic("wl") is None                  # a listed source is gone
 
 
+def test_traffic_key_separates_mask_form_and_forced_kernel():
+    assert bench.traffic_key("wl", False, 0) == "wl"
+    keys = {bench.traffic_key("wl", p, k) for p in (False, True) for k in (0, 1, 2)}
+    assert len(keys) == 6
+
+
 def test_committed_traffic_without_a_capture_file(tmp_path, monkeypatch):
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     assert bench.committed_traffic("wl") is None
