@@ -344,14 +344,12 @@ ta_status run_tree(const TreePlan &plan, cudaStream_t s) {
         const cuuint32_t qbox[2] = {64, 128};
         const cuuint64_t kdims[3] = {(cuuint64_t)a.D, (cuuint64_t)a.N, (cuuint64_t)a.Hk};
         const cuuint64_t kstr[2] = {(cuuint64_t)a.D * 2, (cuuint64_t)a.C * a.D * 2};
-        const cuuint32_t kbox[3] = {64, 32, 1}, kbox64[3] = {64, 64, 1}, kbox128[3] = {64, 128, 1};
+        const cuuint32_t kbox[3] = {64, 32, 1}, kbox64[3] = {64, 64, 1};
         if (!encode_map(&maps.q16, bf16, a.q16, 2, qdims, qstr, qbox) ||
             !encode_map(&maps.k, bf16, plan.k, 3, kdims, kstr, kbox) ||
             !encode_map(&maps.v, bf16, plan.v, 3, kdims, kstr, kbox) ||
             !encode_map(&maps.k64, bf16, plan.k, 3, kdims, kstr, kbox64) ||
-            !encode_map(&maps.v64, bf16, plan.v, 3, kdims, kstr, kbox64) ||
-            !encode_map(&maps.k128, bf16, plan.k, 3, kdims, kstr, kbox128) ||
-            !encode_map(&maps.v128, bf16, plan.v, 3, kdims, kstr, kbox128))
+            !encode_map(&maps.v64, bf16, plan.v, 3, kdims, kstr, kbox64))
             return fail(TA_ERR_CUDA, "tree_attention: TMA descriptor encoding failed");
     }
     cudaError_t e = launch_tree_classify(plan.a, s);

@@ -145,10 +145,8 @@ struct TcMaps {
     CUtensorMap q16;   // 2D {D, H*L} 16-bit, box {64, 128}, 128-byte swizzle
     CUtensorMap k;     // 3D {D, kv_seq_len, Hk}, box {64, 32, 1}, 128-byte swizzle (one chunk)
     CUtensorMap v;
-    CUtensorMap k64;   // the same tensors, box {64, 64, 1}: two consecutive chunks
+    CUtensorMap k64;   // the same tensors, box {64, 64, 1}: two consecutive chunks (CTA pairs)
     CUtensorMap v64;
-    CUtensorMap k128;  // box {64, 128, 1}: four consecutive chunks
-    CUtensorMap v128;
 };
 
 struct QuantArgs {

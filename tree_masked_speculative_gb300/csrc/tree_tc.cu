@@ -27,7 +27,7 @@
 //                with lazy rescaling (M only moves when a row max exceeds it by
 //                more than e^8, so O in TMEM is rarely touched), P back into
 //                TMEM as two 16-bit terms P = P_hi + P_lo, epilogue from TMEM.
-//   warp 10    : second TMA producer (alternate ring loads).
+//   warp 10    : second TMA producer of a CTA pair (alternate ring loads).
 // P in two terms: the tensor core takes 16-bit operands, and a single 16-bit
 // P carries a relative rounding error of up to 2^-8 (bf16) or 2^-11 (f16),
 // which moves the output by up to that fraction of the spread of the attended
@@ -300,27 +300,24 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
 
     if (warp == 0 || warp == kProd1Warp) {
         // ----------------------------------------------------------- producers
-        // Two producer warps issue alternate ring loads (global load index n:
-        // producer n % 2): one thread issuing copies back to back is limited
-        // by the issue time of each copy (about 0.2 us for an 8 KB box), two
-        // reach the rate HBM can feed an SM.  Both walk the whole sequence.
+        // Pair: two producer warps issue alternate ring loads (global load
+        // index n: producer n % 2): one thread issuing 8 KB copies back to back
+        // is limited by the issue time of each copy, two reach the rate HBM can
+        // feed an SM.  Both walk the whole sequence.  Single CTA: warp 0 issues
+        // every load (measured faster there; warp kProd1Warp only idles).
         const int prod = warp == 0 ? 0 : 1;
+        auto mine = [&](int n) { return PAIR ? (n & 1) == prod : prod == 0; };
         ChunkWalk walk;
         walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads of the sequence so far (both producers)
         int mine_end = 0;                               // 1 + index of the last load this producer issued
-        // Single CTA: a slab's 4 chunks as one 128-key box when they are
-        // consecutive, else as 64-key boxes for consecutive pairs and 32-key
-        // boxes otherwise (a missing chunk loads zeros from past kv_seq_len).
+        // Single CTA: a slab's 4 chunks as four 32-key boxes (a missing chunk
+        // loads zeros from past kv_seq_len); one 128-key or two 64-key boxes
+        // for consecutive chunks measured slower here.
         auto load_slabs = [&](const int (&chunk)[4], int nslab, int x0, bool is_v) -> bool {
             const CUtensorMap *m32 = is_v ? &maps.v : &maps.k;
-            const CUtensorMap *m64 = is_v ? &maps.v64 : &maps.k64;
-            const CUtensorMap *m128 = is_v ? &maps.v128 : &maps.k128;
-            const bool p01 = chunk[0] >= 0 && chunk[1] == chunk[0] + 1;
-            const bool p23 = chunk[2] >= 0 && chunk[3] == chunk[2] + 1;
-            const bool all4 = p01 && p23 && chunk[2] == chunk[1] + 1;
             for (int s = 0; s < nslab; ++s, ++issued) {
-                if ((issued & 1) != prod) continue;
+                if (!mine(issued)) continue;
                 const int slot = issued % ST;
                 const uint32_t pass = static_cast<uint32_t>(issued / ST);
                 bool ok = true;
@@ -330,20 +327,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         mbar_arrive_expect_tx(&bars->full[slot], kSlab);
                         unsigned char *dst = sRing + slot * SLOT;
                         const int xx = x0 + s * 64;
-                        if (all4) {
-                            tma_load_3d(dst, m128, &bars->full[slot], xx, chunk[0] * 32, kh);
-                        } else {
-                            for (int h = 0; h < 2; ++h) {
-                                const int c0 = chunk[2 * h], c1 = chunk[2 * h + 1];
-                                if (h == 0 ? p01 : p23) {
-                                    tma_load_3d(dst + h * 8192, m64, &bars->full[slot], xx, c0 * 32, kh);
-                                } else {
-                                    tma_load_3d(dst + h * 8192, m32, &bars->full[slot], xx, c0 >= 0 ? c0 * 32 : n_pad, kh);
-                                    tma_load_3d(dst + h * 8192 + 4096, m32, &bars->full[slot], xx,
-                                                c1 >= 0 ? c1 * 32 : n_pad, kh);
-                                }
-                            }
-                        }
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_3d(dst + c * 4096, m32, &bars->full[slot], xx,
+                                        chunk[c] >= 0 ? chunk[c] * 32 : n_pad, kh);
                     }
                 }
                 ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -408,8 +394,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     for (int s = 0; s < NSK; ++s)
                         tma_load_2d_pair(sQ + s * kSlab, &maps.q16, qb, s * 64, kh * a.R + rt * RT);
                 } else {
-                    tma_prefetch_desc(&maps.k128);
-                    tma_prefetch_desc(&maps.v128);
                     mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
                     for (int s = 0; s < NSK; ++s)
                         tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
@@ -463,12 +447,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             } else {
                 if (prod == 0 && !mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9, 0u);
                 for (int n = drain_from(mine_end); n < mine_end; ++n)
-                    if ((n & 1) == prod &&
+                    if (mine(n) &&
                         !mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
                         note_abort(bars, err, 9, 0u);
             }
             for (int n = drain_from(mine_end); n < mine_end; ++n)
-                if ((n & 1) == prod &&
+                if (mine(n) &&
                     !mbar_wait(&bars->empty[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
                     note_abort(bars, err, 9, PAIR ? peer_flag : 0u);
         }
