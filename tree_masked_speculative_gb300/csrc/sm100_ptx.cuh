@@ -133,6 +133,13 @@ __device__ __forceinline__ void tma_load_3d_pair(void *dst, const CUtensorMap *m
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
 }
+// Arrive on a barrier of another CTA of the cluster with the default
+// (CTA-scope) semantics: enough where the waiter needs only the ordering of
+// tcgen05 operations, which the tcgen05 fences around the arrive and the wait
+// give; no ordinary memory written before it is published to the waiter.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster) : "memory");
+}
 // Complete `bytes` of this CTA's mbarrier's expected transaction count
 // without a copy (stands in for bytes that will never arrive).
 __device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes) {

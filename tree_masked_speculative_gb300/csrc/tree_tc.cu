@@ -755,7 +755,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             tc_fence_before();
             __syncwarp();
             if (lane == 0 && ok) {
-                if (PAIR && !leader) mbar_arrive_cluster(at_leader(&bars->p_full));
+                if (PAIR && !leader) mbar_arrive_remote(at_leader(&bars->p_full));
                 else mbar_arrive(&bars->p_full);
             }
         }
