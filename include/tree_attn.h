@@ -148,9 +148,14 @@ typedef struct {
 size_t tree_attn_tmp_bytes(uint32_t n_heads, uint32_t head_dim, uint32_t q_l, uint32_t nwg);
 
 /*
- * Number of KV splits tree_attn_fwd will use for these parameters on the
- * current device: p->nwg when non-zero, else a choice sized to the SM count.
- * Returns 0 when the parameters are invalid or no device is visible.
+ * Number of KV splits (partial slots per output row) tree_attn_fwd will use
+ * for these parameters on the current device: p->nwg when non-zero, else a
+ * choice sized to the SM count.  With head dim 512, more than 128 rows per KV
+ * head and p->nwg == 0 the tensor-core pass may spread the (KV head, key tile)
+ * work of all heads evenly over every SM; a row's keys are then cut at
+ * different points for different KV heads, and this count is the most slots
+ * any row uses (slots a row does not use hold S = 0 and add nothing to the
+ * merge).  Returns 0 when the parameters are invalid or no device is visible.
  */
 uint32_t tree_attn_num_splits(const ta_tree_params *p);
 
@@ -243,7 +248,8 @@ size_t tree_attn_status_offset(const ta_tree_params *p);
  * Second pass ([TA-R] tree_attention, reduce pass): merges the nwg partials
  * of every (query, head) row with a log-sum-exp rescale:
  *   M* = max_w M_w,  S* = sum_w S_w e^(M_w - M*),
- *   out = sum_w O_w e^(M_w - M*) / S*   (0 when S* == 0).
+ *   out = sum_w O_w e^(M_w - M*) / S*   (0 when S* == 0);
+ * a partial with S_w = 0 (no attended key) is skipped, its O_w not read.
  * `p` must equal the one given to the main pass; `tmp` is its tmp buffer.
  */
 ta_status tree_attn_reduce(const ta_tree_params *p, const ta_buf *tmp, const ta_buf *out,

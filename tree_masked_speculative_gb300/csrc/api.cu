@@ -124,8 +124,34 @@ ta_status check_tree_params(const ta_tree_params *p, bool need_mask_stride) {
 
 int rows_per_kv(const ta_tree_params *p) { return (int)(p->n_heads / p->n_kv_heads * p->q_l); }
 
+// CTA pairs: groups per O half of the flattened schedule (a group is one pair
+// for each O half), or 0 when the pairs are not used, the caller chose nwg,
+// or the uniform split count already fills every SM.
+int tree_flat_groups(const ta_tree_params *p) {
+    if (p->nwg != 0) return 0;
+    const int R = static_cast<int>(rows_per_kv(p)), D = static_cast<int>(p->head_dim);
+    if (R < 16 || !tree_tc_pairs(R, D)) return 0;
+    const int sms = sm_count();
+    if (sms <= 0) return 0;
+    const int G = sms / 4;
+    const int U = static_cast<int>(p->n_kv_heads) * (tree_tc_row_ctas(R, D) / 2);
+    const long long tpu = ((static_cast<long long>(p->kv_seq_len) + 31) / 32 + 3) / 4;
+    if (U > G || G % U == 0 || static_cast<long long>(U) * tpu < G) return 0;
+    return G;
+}
+
 uint32_t resolve_tree_nwg(const ta_tree_params *p) {
     if (p->nwg != 0) return p->nwg;
+    if (const int G = tree_flat_groups(p)) {
+        // partial slots: the most groups any unit's key tiles meet
+        const int R = static_cast<int>(rows_per_kv(p)), D = static_cast<int>(p->head_dim);
+        const int U = static_cast<int>(p->n_kv_heads) * (tree_tc_row_ctas(R, D) / 2);
+        const int tpu = static_cast<int>(((p->kv_seq_len + 31) / 32 + 3) / 4);
+        const long long W = static_cast<long long>(U) * tpu;
+        int most = 1;
+        for (int u = 0; u < U; ++u) most = std::max(most, flat_unit_slots(u, tpu, W, G));
+        return static_cast<uint32_t>(most);
+    }
     const int sms = sm_count();
     if (sms <= 0) return 0;
     const uint64_t n_chunks = (p->kv_seq_len + 31u) / 32u;
@@ -321,6 +347,7 @@ ta_status plan_tree(const ta_tree_params *p, int kernel, const ta_buf *q, const 
     a.q16_type = plan->use_tc ? plan->kv_type : -1;
     // partial slots left for the merge pass (0 = the main pass writes the output)
     a.cluster_x = 1;
+    a.flat_groups = plan->use_tc ? tree_flat_groups(p) : 0;
     if (plan->use_tc) {
         int cx, cy;
         tree_tc_cluster_shape(a, &cx, &cy);

@@ -101,6 +101,7 @@ struct TreeArgs {
     int q16_type;          // -1: no 16-bit Q copy, else kKvF16 / kKvBF16
     int n_part;            // partial slots the main pass leaves for the merge (0 = output final)
     int cluster_x;         // tensor-core kernel: splits merged inside one cluster
+    int flat_groups;       // CTA pairs: groups per O half of the flattened schedule (0 = uniform splits)
     float scale;
 };
 
@@ -339,6 +340,25 @@ __host__ __device__ inline bool tree_tc_pairs(int R, int D) { return R > 128 && 
 __host__ __device__ inline int tree_tc_row_ctas(int R, int D) {
     const int n_rt = (R + 127) / 128;
     return tree_tc_pairs(R, D) ? 2 * ((n_rt + 1) / 2) : n_rt;
+}
+// Flattened schedule of the CTA pairs.  Units are (KV head, pair of row
+// tiles), each with tpu key tiles of 4 chunks; the U x tpu (unit, tile)
+// positions are cut into G contiguous ranges of nearly equal length, one per
+// pair-group (per O half), so that every SM gets the same share of work when
+// the uniform split count would leave some idle.  A range meets at most two
+// units (G >= U); the part in one unit is a segment, which leaves one partial
+// slot for the merge: its group's index minus that of the unit's first group.
+__host__ __device__ inline long long flat_start(int g, long long W, int G) { return (long long)g * W / G; }
+// Group whose range holds position P (0 <= P < W).
+__host__ __device__ inline int flat_group_of(long long P, long long W, int G) {
+    int g = static_cast<int>(P * G / W);
+    while (g + 1 < G && flat_start(g + 1, W, G) <= P) ++g;
+    while (g > 0 && flat_start(g, W, G) > P) --g;
+    return g;
+}
+// Partial slots unit u uses.
+__host__ __device__ inline int flat_unit_slots(int u, int tpu, long long W, int G) {
+    return flat_group_of((long long)(u + 1) * tpu - 1, W, G) - flat_group_of((long long)u * tpu, W, G) + 1;
 }
 // Cluster shape of the tensor-core kernel: x = splits merged in-cluster (y = 1).
 void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy);

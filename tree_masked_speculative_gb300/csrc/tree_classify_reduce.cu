@@ -212,6 +212,9 @@ __global__ void __launch_bounds__(kReduceThreads) tree_reduce_kernel(const TreeA
     float m = -FLT_MAX, ssum = 0.0f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     auto merge = [&](float2 sm, float4 o) {
+        // a slot with no attended key (S = 0) adds nothing; its O is not read
+        // (slots that no split fills are marked this way and left unwritten)
+        if (sm.x == 0.0f) return;
         const float mn = fmaxf(m, sm.y);
         const float c = expf(m - mn), e = expf(sm.y - mn);
         m = mn;

@@ -236,17 +236,21 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     // Grid.  Single CTA: x = split, y = O half * row tiles + row tile.  Pair:
     // x = 2 * (pair of row tiles) + member, y = split * O halves + O half; the
     // cluster is the pair (cluster ranks 2k, 2k + 1), member 0 the leader that
-    // issues the MMAs.  z = KV head.
+    // issues the MMAs.  z = KV head.  Flattened pairs: x = member, y = group *
+    // O halves + O half, z = 0; the group's work segments name the KV head and
+    // row tiles.
     constexpr int kHalves = D / DV;
     const int n_ct = tree_tc_row_ctas(a.R, D);         // row tiles
     const int member = PAIR ? static_cast<int>(cluster_ctarank() & 1u) : 0;
     const bool leader = member == 0;
-    const int split = PAIR ? static_cast<int>(blockIdx.y) / kHalves : static_cast<int>(blockIdx.x);
+    const bool flat = PAIR && a.flat_groups > 0;
+    const int split = flat ? 0 : (PAIR ? static_cast<int>(blockIdx.y) / kHalves : static_cast<int>(blockIdx.x));
     const int os = PAIR ? static_cast<int>(blockIdx.y) % kHalves : static_cast<int>(blockIdx.y) / n_ct;
-    const int rt = PAIR ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y) % n_ct;
-    const int kh = blockIdx.z;
     const int RT = (a.R + n_ct - 1) / n_ct;            // rows per tile
-    const int rows_here = min(RT, a.R - rt * RT);
+    // the current work segment's KV head and row tile (set per segment below)
+    int kh = blockIdx.z;
+    int rt = PAIR ? static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.y) % n_ct;
+    int rows_here = min(RT, a.R - rt * RT);
     int *err = a.err;
     // Cluster (single CTA: cx x 1): consecutive splits of one (row tile, O
     // half, KV head) whose partials are merged in the cluster over DSMEM.
@@ -293,9 +297,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     const uint32_t tm_s[2] = {tmem, tmem + 128};
     const uint32_t tm_o = tmem + 256;
 
-    int c_begin, c_end;
-    split_range(a.n_chunks, a.nwg, split, &c_begin, &c_end);
-    const int T = count_tiles(a.cls, c_begin, c_end);
+    // Work segments of this CTA: (KV head, row tile, chunk range, partial
+    // slot, live tiles).  Uniform splits: one segment.  Flattened pairs: the
+    // group's range of (unit, key tile) positions, in at most two units; a
+    // segment ending its unit also marks the unit's unused slots empty.  The
+    // segments' tiles form one sequence through the ring and the barriers.
+    int nseg = 1;
+    int sg_kh[2], sg_rt[2], sg_cb[2], sg_ce[2], sg_slot[2], sg_T[2], sg_used[2];
+    bool sg_last[2];
+    if (flat) {
+        const int G = a.flat_groups, grp = static_cast<int>(blockIdx.y) / kHalves;
+        const int np = n_ct / 2, tpu = (a.n_chunks + 3) / 4;
+        const long long W = static_cast<long long>(a.Hk) * np * tpu;
+        const long long p1 = flat_start(grp + 1, W, G);
+        nseg = 0;
+        for (long long P = flat_start(grp, W, G); P < p1 && nseg < 2; ++nseg) {
+            const int u = static_cast<int>(P / tpu);
+            const long long ub = static_cast<long long>(u) * tpu, e = min(p1, ub + tpu);
+            sg_kh[nseg] = u / np;
+            sg_rt[nseg] = 2 * (u % np) + member;
+            sg_cb[nseg] = static_cast<int>(P - ub) * 4;
+            sg_ce[nseg] = min(a.n_chunks, static_cast<int>(e - ub) * 4);
+            sg_slot[nseg] = grp - flat_group_of(ub, W, G);
+            sg_used[nseg] = flat_unit_slots(u, tpu, W, G);
+            sg_last[nseg] = e == ub + tpu;
+            P = e;
+        }
+    } else {
+        sg_kh[0] = kh;
+        sg_rt[0] = rt;
+        split_range(a.n_chunks, a.nwg, split, &sg_cb[0], &sg_ce[0]);
+        sg_slot[0] = split;
+        sg_used[0] = a.nwg;
+        sg_last[0] = false;
+    }
+    int T = 0;                                          // tiles of all segments
+    for (int i = 0; i < nseg; ++i) {
+        sg_T[i] = count_tiles(a.cls, sg_cb[i], sg_ce[i]);
+        T += sg_T[i];
+    }
+    auto enter_segment = [&](int i) {
+        kh = sg_kh[i];
+        rt = sg_rt[i];
+        rows_here = min(RT, a.R - rt * RT);
+    };
+    enter_segment(0);
     const int n_pad = ((a.N + 31) / 32) * 32;          // a key row that is out of bounds
 
     if (warp == 0 || warp == kProd1Warp) {
@@ -308,7 +354,6 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int prod = warp == 0 ? 0 : 1;
         auto mine = [&](int n) { return PAIR ? (n & 1) == prod : prod == 0; };
         ChunkWalk walk;
-        walk.init(a.cls, c_begin, c_end);
         int issued = 0;                                 // ring loads of the sequence so far (both producers)
         int mine_end = 0;                               // 1 + index of the last load this producer issued
         // Single CTA: a slab's 4 chunks as four 32-key boxes (a missing chunk
@@ -382,34 +427,51 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             return true;
         };
         bool ok = true;
-        if (T > 0) {
+        int q_loads = 0, tg0 = 0;                       // Q tiles loaded; tiles of earlier segments
+        if (T > 0 && lane == 0 && prod == 0) {
+            tma_prefetch_desc(&maps.k);
+            tma_prefetch_desc(&maps.v);
+            tma_prefetch_desc(&maps.k64);
+            tma_prefetch_desc(&maps.v64);
+        }
+        for (int sgi = 0; sgi < nseg && ok; ++sgi) {
+            const int Ts = sg_T[sgi];
+            if (Ts == 0) continue;
+            enter_segment(sgi);
+            walk.init(a.cls, sg_cb[sgi], sg_ce[sgi]);
             if (lane == 0 && prod == 0) {
-                tma_prefetch_desc(&maps.k);
-                tma_prefetch_desc(&maps.v);
-                tma_prefetch_desc(&maps.k64);
-                tma_prefetch_desc(&maps.v64);
-                if constexpr (PAIR) {
-                    if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * NSK * kSlab);
-                    const uint32_t qb = at_leader(&bars->q_full);
-                    for (int s = 0; s < NSK; ++s)
-                        tma_load_2d_pair(sQ + s * kSlab, &maps.q16, qb, s * 64, kh * a.R + rt * RT);
-                } else {
-                    mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
-                    for (int s = 0; s < NSK; ++s)
-                        tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
+                // a later segment's Q tile replaces the earlier one once the
+                // last QK^T MMAs of the earlier segment are done
+                if (q_loads > 0)
+                    ok = wait_or_abort(bars, &bars->s_full[(tg0 - 1) & 1],
+                                       static_cast<uint32_t>((tg0 - 1) >> 1) & 1u, err, 14, peer_flag);
+                if (ok) {
+                    if constexpr (PAIR) {
+                        if (leader) mbar_arrive_expect_tx(&bars->q_full, 2 * NSK * kSlab);
+                        const uint32_t qb = at_leader(&bars->q_full);
+                        for (int s = 0; s < NSK; ++s)
+                            tma_load_2d_pair(sQ + s * kSlab, &maps.q16, qb, s * 64, kh * a.R + rt * RT);
+                    } else {
+                        mbar_arrive_expect_tx(&bars->q_full, NSK * kSlab);
+                        for (int s = 0; s < NSK; ++s)
+                            tma_load_2d(sQ + s * kSlab, &maps.q16, &bars->q_full, s * 64, kh * a.R + rt * RT);
+                    }
                 }
             }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            ++q_loads;
             int cur[4], nxt[4], cl_unused;
             for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
-            ok = PAIR ? load_k_pair(nxt) : load_slabs(nxt, NSK, 0, false);
-            for (int t = 0; t < T && ok; ++t) {
+            if (ok) ok = PAIR ? load_k_pair(nxt) : load_slabs(nxt, NSK, 0, false);
+            for (int t = 0; t < Ts && ok; ++t) {
                 for (int c = 0; c < 4; ++c) cur[c] = nxt[c];
-                if (t + 1 < T) {
+                if (t + 1 < Ts) {
                     for (int c = 0; c < 4; ++c) nxt[c] = walk.next(&cl_unused);
                     ok = PAIR ? load_k_pair(nxt) : load_slabs(nxt, NSK, 0, false);
                 }
                 if (ok) ok = PAIR ? load_v_pair(cur) : load_slabs(cur, NSV, os * DV, true);
             }
+            tg0 += Ts;
         }
         // Drain: every copy this producer issued into this CTA's ring has
         // landed and the MMAs have released the last use of each of its slots,
@@ -433,7 +495,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                         got = mbar_try_wait_cluster(&bars->peer_done[prod], 0, 1000);
                     if (got) ip = static_cast<int>(bars->peer_issued[prod]);
                     else note_abort(bars, err, 12, peer_flag);
-                    if (prod == 0 && !mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9, peer_flag);
+                    if (prod == 0 && q_loads > 0 &&
+                        !mbar_wait(&bars->q_full, static_cast<uint32_t>(q_loads - 1) & 1u, kWaitIters))
+                        note_abort(bars, err, 9, peer_flag);
                     const int hi = max(mine_end, ip);
                     for (int n = drain_from(hi); n < hi; ++n) {
                         if ((n & 1) != prod) continue;
@@ -445,7 +509,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     }
                 }
             } else {
-                if (prod == 0 && !mbar_wait(&bars->q_full, 0, kWaitIters)) note_abort(bars, err, 9, 0u);
+                if (prod == 0 && q_loads > 0 &&
+                    !mbar_wait(&bars->q_full, static_cast<uint32_t>(q_loads - 1) & 1u, kWaitIters))
+                    note_abort(bars, err, 9, 0u);
                 for (int n = drain_from(mine_end); n < mine_end; ++n)
                     if (mine(n) &&
                         !mbar_wait(&bars->full[n % ST], static_cast<uint32_t>(n / ST) & 1u, kWaitIters))
@@ -466,8 +532,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const bool is_qk = warp == 1;
         if (lane == 0 && T > 0 && leader) {
             const uint32_t q_addr = smem_u32(sQ), ring_addr = smem_u32(sRing);
+            // ring positions of tile t of a segment of Ts tiles (relative to
+            // the segment's first position; a segment takes Ts (NSK + NSV))
             auto pos_k = [&](int t) { return t == 0 ? 0 : NSK + (t - 1) * (NSK + NSV); };
-            auto pos_v = [&](int t) { return t < T - 1 ? 2 * NSK + t * (NSK + NSV) : NSK + (T - 1) * (NSK + NSV); };
+            auto pos_v = [&](int t, int Ts) {
+                return t < Ts - 1 ? 2 * NSK + t * (NSK + NSV) : NSK + (Ts - 1) * (NSK + NSV);
+            };
             // a slot is free once its MMAs are done (in both CTAs of a pair)
             auto release = [&](int slot) {
                 if constexpr (PAIR) {
@@ -492,14 +562,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 // PV_t-2 has completed (s_free), the softmax of tile t-2 having
                 // finished with S_t-2 before PV_t-2 was issued.
                 constexpr uint32_t id_qk = idesc_f16(PAIR ? 256 : 128, 128, BF16 ? 1 : 0, 0, 0);
-                ok = wait_or_abort(bars, &bars->q_full, 0, err, 2, pf);
-                for (int t = 0; t < T && ok; ++t) {
+                int tg = 0, pbase = 0, qn = 0;
+                for (int sgi = 0; sgi < nseg && ok; ++sgi) {
+                const int Ts = sg_T[sgi];
+                if (Ts == 0) continue;
+                ok = wait_or_abort(bars, &bars->q_full, static_cast<uint32_t>(qn++) & 1u, err, 2, pf);
+                for (int tl = 0; tl < Ts && ok; ++tl) {
+                    const int t = tg + tl;                  // tile of the whole sequence
                     const int sb = t & 1;
                     if (t >= 2) ok = wait_or_abort(bars, &bars->s_free[sb], static_cast<uint32_t>((t - 2) >> 1) & 1u,
                                                    err, 3, pf, kPipeHintNs);
                     if (!ok) break;
                     tc_fence_after();
-                    const int p0 = pos_k(t);
+                    const int p0 = pbase + pos_k(tl);
                     for (int s = 0; s < NSK && ok; ++s) {
                         const int pos = p0 + s, slot = pos % ST;
                         ok = wait_or_abort(bars, &bars->full[slot], static_cast<uint32_t>(pos / ST) & 1u, err, 4, pf, kPipeHintNs);
@@ -517,8 +592,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     }
                     if (ok) commit_both(&bars->s_full[sb]);
                 }
+                tg += Ts;
+                pbase += Ts * (NSK + NSV);
+                }
             } else {
-                for (int t = 0; t < T && ok; ++t) {
+                int tg = 0, pbase = 0;
+                for (int sgi = 0; sgi < nseg && ok; ++sgi) {
+                const int Ts = sg_T[sgi];
+                for (int tl = 0; tl < Ts && ok; ++tl) {
+                    const int t = tg + tl;                  // tile of the whole sequence
                     ok = PAIR ? wait_or_abort_cluster(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf,
                                                       kPipeHintNs)
                               : wait_or_abort(bars, &bars->p_full, static_cast<uint32_t>(t) & 1u, err, 5, pf, kPipeHintNs);
@@ -531,7 +613,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     // the tile as P_hi in columns 64h + [0, 32) and P_lo in
                     // 64h + [32, 64), two 16-bit keys per column; each K step
                     // takes both terms.
-                    int used = pos_v(t);
+                    int used = pbase + pos_v(tl, Ts);
                     for (int s = 0; s < NSV && ok;) {
                         const int slot0 = used % ST;
                         int len = 1;
@@ -555,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
                                 const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
-                                mma_f16_ts_pair(tm_o, pa, bd, id_pv, (t | kk) != 0);
+                                mma_f16_ts_pair(tm_o, pa, bd, id_pv, (tl | kk) != 0);
                                 mma_f16_ts_pair(tm_o, pa + 32, bd, id_pv, 1u);
                             }
                         } else {
@@ -564,7 +646,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                             for (int kk = 0; kk < 8; ++kk) {
                                 const uint32_t pa = tm_s[t & 1] + 64 * (kk >> 2) + 8 * (kk & 3);
                                 const uint64_t bd = sw128_desc(vb + kk * 2048, kSlab, 1024);
-                                mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (t | kk) != 0);
+                                mma_f16_ts(tm_o + s * 64, pa, bd, id_pv, (tl | kk) != 0);
                                 mma_f16_ts(tm_o + s * 64, pa + 32, bd, id_pv, 1u);
                             }
                         }
@@ -575,6 +657,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                     if (!ok) break;
                     commit_both(&bars->o_done[t & 1]);
                     commit_own(&bars->s_free[t & 1]);   // S_t / P_t buffer free once PV_t is done
+                }
+                tg += Ts;
+                pbase += Ts * (NSK + NSV);
                 }
             }
             // Drain: all MMAs issued by this thread have completed.
@@ -592,16 +677,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         const int half = sw >> 2;
         const int quarter = warp & 3;
         const int r = quarter * 32 + lane;              // row within the tile
-        const int rg = rt * RT + r;                     // row within the KV group
-        const int qi = rg % a.L;                        // query (tree node)
+        int rg = 0, qi = 0;                             // row within the KV group, query (tree node)
+        const float *mrow = nullptr;                    // its mask row
+        auto rows_of_segment = [&]() {
+            rg = rt * RT + r;
+            qi = rg % a.L;
+            mrow = (IMPLICIT || a.mask == nullptr) ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
+        };
         const uint32_t lane_off = static_cast<uint32_t>(quarter * 32) << 16;
         const int last0 = a.N - a.L;
-        const float *mrow = (IMPLICIT || a.mask == nullptr) ? nullptr : a.mask + static_cast<size_t>(qi) * a.stride;
         constexpr int DVH = DV / 2;                     // O columns of this warp
         auto pair_sync = [&]() { asm volatile("bar.sync %0, 64;" ::"r"(1 + quarter) : "memory"); };
 
         ChunkWalk walk;
-        walk.init(a.cls, c_begin, c_end);
         float m_run = -INFINITY, l_half = 0.0f;         // running max (log2 units), this half's sum
         bool ok = true;
         const float scale2 = a.scale * kLog2e;
@@ -612,7 +700,16 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             const bool w = ok && wait_or_abort(bars, bar, parity, err, code, PAIR ? peer_flag : 0u);
             return __all_sync(0xffffffffu, w);
         };
-        for (int t = 0; t < T; ++t) {
+        int tg = 0;                                     // tiles of earlier segments
+        for (int sgi = 0; sgi < nseg; ++sgi) {
+        const int Ts = sg_T[sgi];
+        enter_segment(sgi);
+        rows_of_segment();
+        walk.init(a.cls, sg_cb[sgi], sg_ce[sgi]);
+        m_run = -INFINITY;
+        l_half = 0.0f;
+        for (int tl = 0; tl < Ts; ++tl) {
+            const int t = tg + tl;                      // tile of the whole sequence
             int chunk[4], ccls[4];
             for (int c = 0; c < 4; ++c) chunk[c] = walk.next(&ccls[c]);
             const int ch0 = half ? chunk[2] : chunk[0], ch1 = half ? chunk[3] : chunk[1];
@@ -700,7 +797,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             // then; P_t has a TMEM buffer of its own).  Waiting for tile t-1 on
             // o_done[(t-1) % 2] is unambiguous: S_t was issued after PV_t-2 was
             // done, so that barrier's phase is the one of tile t-1.
-            if (t > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+            if (tl > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
                 ok = wait_all(&bars->o_done[(t - 1) & 1], (static_cast<uint32_t>(t - 1) >> 1) & 1u, 8);
                 tc_fence_after();
                 if (ok) {
@@ -759,6 +856,56 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 else mbar_arrive(&bars->p_full);
             }
         }
+        if (flat) {
+            // ---- end of a flattened segment: its partial (unnormalized O of
+            // this CTA's rows and O half, and (S, M)) goes from TMEM straight
+            // to its slot.  The next segment's first PV starts O over only
+            // after these warps signal P of that tile, i.e. after these loads.
+            const int tlast = tg + Ts - 1;
+            if (Ts > 0) {
+                ok = wait_all(&bars->o_done[tlast & 1], (static_cast<uint32_t>(tlast) >> 1) & 1u, 8);
+                tc_fence_after();
+            }
+            const int px = (tg + Ts) & 1;               // the exchange buffer of the next tile
+            bars->xrow[px][half][r] = l_half;
+            pair_sync();
+            const float l_run = l_half + bars->xrow[px][half ^ 1][r];
+            pair_sync();                                // both read it before the next tile writes it
+            const int nrows = a.H * a.L;
+            const size_t rid2 = static_cast<size_t>(qi) * a.H + kh * a.g + rg / a.L;
+            const bool row_ok = r < rows_here;
+            const size_t slot = static_cast<size_t>(sg_slot[sgi]);
+            if (Ts > 0 && ok) {
+#pragma unroll 1
+                for (int c = 0; c < DVH / 32; ++c) {
+                    uint32_t rr[32];
+                    tmem_ld32(tm_o + lane_off + half * DVH + c * 32, rr);
+                    tmem_wait_ld();
+                    if (row_ok) {
+                        float4 *dst = reinterpret_cast<float4 *>(a.part_o + (slot * nrows + rid2) * D + os * DV +
+                                                                 half * DVH + c * 32);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            dst[e] = make_float4(__uint_as_float(rr[4 * e]), __uint_as_float(rr[4 * e + 1]),
+                                                 __uint_as_float(rr[4 * e + 2]), __uint_as_float(rr[4 * e + 3]));
+                    }
+                }
+            }
+            if (os == 0 && half == 0 && row_ok) {
+                float2 *ml = reinterpret_cast<float2 *>(a.part_ml);
+                ml[slot * nrows + rid2] =
+                    make_float2(Ts > 0 ? l_run : 0.0f, m_run == -INFINITY ? kMInit : m_run * kLn2);
+                // the unit's slots no group fills hold no keys (S = 0: the merge skips them)
+                if (sg_last[sgi])
+                    for (int s2 = sg_used[sgi]; s2 < a.nwg; ++s2)
+                        ml[static_cast<size_t>(s2) * nrows + rid2] = make_float2(0.0f, kMInit);
+            }
+        }
+        tg += Ts;
+        }
+        if (flat) {
+            pdl_launch_dependents();
+        } else {
         if (T > 0) {
             ok = wait_all(&bars->o_done[(T - 1) & 1], (static_cast<uint32_t>(T - 1) >> 1) & 1u, 8);
             tc_fence_after();
@@ -796,6 +943,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             reinterpret_cast<float2 *>(stage + 128 * SROW)[r] =
                 make_float2(l_run, m_run == -INFINITY ? kMInit : m_run * kLn2);   // (S, M), natural log
         fence_proxy_async_smem();   // the staged rows may leave by bulk copy
+        }
     }
 
     // ------------------------------------------------------ store or merge
@@ -809,7 +957,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     __syncthreads();
     if (cx > 1) cluster_sync();   // the merge reads the peers' staged rows (cx is uniform in a cluster)
     const bool epi_warp = warp >= 2 && warp < kProd1Warp;   // the softmax warps
-    if (epi_warp && cx == 1) {
+    if (epi_warp && cx == 1 && !flat) {
         // No merge in the cluster: each staged row (final and normalized, or
         // partial slot `split` with its (S, M)) leaves by one bulk copy issued
         // by its own thread; a destination off a 16-byte boundary is written
@@ -847,7 +995,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
                 const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
                 reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * nrows + rid2] = stage_ml[rr];
             }
-    } else if (epi_warp) {
+    } else if (epi_warp && !flat) {
         const int sw = warp - 2;
         const int nrows = a.H * a.L;
         const bool final_out = a.n_part == 0;
@@ -983,7 +1131,8 @@ cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s)
     dim3 grid;
     unsigned cx, cy = 1;
     if (PAIR) {
-        grid = dim3(n_ct, static_cast<unsigned>(a.nwg) * halves, a.Hk);
+        grid = a.flat_groups > 0 ? dim3(2, static_cast<unsigned>(a.flat_groups) * halves, 1)
+                                 : dim3(n_ct, static_cast<unsigned>(a.nwg) * halves, a.Hk);
         cx = 2;
     } else {
         int mx, my;
