@@ -38,6 +38,7 @@ CASES = [
     (4, 2, 512, 100, 128, 3, "f32", 0),
     (16, 2, 512, 700, 700, 20, "bf16", 3),    # 160 rows: two row tiles per O half
     (20, 1, 512, 400, 416, 15, "f16", 2),     # 300 rows: three row tiles
+    (16, 2, 256, 3000, 3008, 8, "f16", 12),   # 12 splits merged in a 12-CTA cluster (two rounds of 8)
 ]
 
 

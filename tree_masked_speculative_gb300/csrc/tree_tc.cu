@@ -1009,20 +1009,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
         for (int rr = r0 + sw; rr < r1; rr += 8) {
             const int rg2 = rt * RT + rr;
             const size_t rid2 = static_cast<size_t>(rg2 % a.L) * a.H + kh * a.g + rg2 / a.L;
-            // every remote load of the row is issued before any is used
+            // up to 16 splits: lane p < cx holds split p's (S, M); the weighted
+            // rows are summed in rounds of 8, each round's remote loads all
+            // issued before any is used
             float2 ml = make_float2(0.0f, -FLT_MAX);
-            float4 v[8][C4];
             if (lane < cx) ml = ld_dsmem_f2(mapa_shared(ml_sa + rr * 8, lane));
-#pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                if (p >= cx) break;
-#pragma unroll
-                for (int j = 0; j < C4; ++j) {
-                    const uint32_t off = stage_sa + (rr * SROW + 4 * (lane + 32 * j)) * 4;
-                    v[p][j] = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p))
-                                     : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * (lane + 32 * j));
-                }
-            }
             const float mstar = warp_max(lane < cx ? ml.y : -FLT_MAX);
             const float wp = lane < cx ? expf(ml.y - mstar) : 0.0f;
             const float sstar = warp_sum(lane < cx ? ml.x * wp : 0.0f);
@@ -1030,14 +1021,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
             float4 acc[C4];
 #pragma unroll
             for (int j = 0; j < C4; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 1
+            for (int p0 = 0; p0 < cx; p0 += 8) {
+                float4 v[8][C4];
 #pragma unroll
-            for (int p = 0; p < 8; ++p) {
-                if (p >= cx) break;
-                const float w = __shfl_sync(0xffffffffu, wp, p);
+                for (int p = 0; p < 8; ++p) {
+                    if (p0 + p >= cx) break;
 #pragma unroll
-                for (int j = 0; j < C4; ++j) {
-                    acc[j].x += w * v[p][j].x; acc[j].y += w * v[p][j].y;
-                    acc[j].z += w * v[p][j].z; acc[j].w += w * v[p][j].w;
+                    for (int j = 0; j < C4; ++j) {
+                        const uint32_t off = stage_sa + (rr * SROW + 4 * (lane + 32 * j)) * 4;
+                        v[p][j] = cx > 1 ? ld_dsmem_f4(mapa_shared(off, p0 + p))
+                                         : *reinterpret_cast<const float4 *>(stage + rr * SROW + 4 * (lane + 32 * j));
+                    }
+                }
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    if (p0 + p >= cx) break;
+                    const float w = __shfl_sync(0xffffffffu, wp, p0 + p);
+#pragma unroll
+                    for (int j = 0; j < C4; ++j) {
+                        acc[j].x += w * v[p][j].x; acc[j].y += w * v[p][j].y;
+                        acc[j].z += w * v[p][j].z; acc[j].w += w * v[p][j].w;
+                    }
                 }
             }
             float *dst = final_out ? a.out + rid2 * D + os * DV
@@ -1066,13 +1071,26 @@ __global__ void __launch_bounds__(kTcThreads, 1) tree_tc_kernel(const TreeArgs a
     }
 }
 
-// Clusters of `size` CTAs of this kernel that the current device can hold at
-// once (the kernel is shared-memory bound to one CTA per SM, equally for all
-// instantiations); cached per device.
-static int max_active_clusters(int size) {
-    static int cache[64][9];
+// Clusters above 8 CTAs need the kernel's non-portable cluster size allowed.
+template <typename Kern>
+cudaError_t allow_big_clusters_once(Kern kern, unsigned long long *done_mask) {
     int dev = 0;
-    if (size < 1 || size > 8) return 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long bit = 1ull << (dev & 63);
+    if (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e == cudaSuccess) __atomic_fetch_or(done_mask, bit, __ATOMIC_ACQ_REL);
+    return e;
+}
+
+// Clusters of `size` (<= 16) CTAs of this kernel that the current device can
+// hold at once (the kernel is shared-memory bound to one CTA per SM, equally
+// for all instantiations); cached per device.
+static int max_active_clusters(int size) {
+    static int cache[64][17];
+    int dev = 0;
+    if (size < 1 || size > 16) return 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) { cudaGetLastError(); return 0; }
     const int idx = size;
     int n = __atomic_load_n(&cache[dev][idx], __ATOMIC_ACQUIRE);
@@ -1080,6 +1098,8 @@ static int max_active_clusters(int size) {
     auto kern = tree_tc_kernel<256, false, false, false>;
     static unsigned long long done = 0;
     if (set_smem_limit_once(kern, TcCfg<256, false>::SMEM, &done) != cudaSuccess) { cudaGetLastError(); return 0; }
+    static unsigned long long big = 0;
+    if (size > 8 && allow_big_clusters_once(kern, &big) != cudaSuccess) { cudaGetLastError(); return 0; }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(size, 1, 1);
     cfg.blockDim = dim3(kTcThreads);
@@ -1110,10 +1130,11 @@ void tree_tc_cluster_shape(const TreeArgs &a, int *cx, int *cy) {
     *cx = 1;
     *cy = 1;
     if (tree_tc_pairs(a.R, a.D)) return;
-    const long total = static_cast<long>(a.nwg) * (a.D == 512 ? 2 : 1) * a.Hk;
-    if (a.nwg > 1 && a.nwg <= 8) {
+    // every cluster resident at once: clusters = row tiles x O halves x KV heads
+    const long clusters = static_cast<long>(tree_tc_row_ctas(a.R, a.D)) * (a.D == 512 ? 2 : 1) * a.Hk;
+    if (a.nwg > 1 && a.nwg <= 16) {
         const int n = max_active_clusters(a.nwg);
-        if (n > 0 && total / a.nwg <= n) *cx = a.nwg;
+        if (n > 0 && clusters <= n) *cx = a.nwg;
     }
 }
 
@@ -1123,8 +1144,9 @@ template <int D, bool BF16, bool IMPLICIT, bool PAIR>
 cudaError_t launch_tc_one(const TreeArgs &a, const TcMaps &maps, cudaStream_t s) {
     using Cfg = TcCfg<D, PAIR>;
     auto kern = tree_tc_kernel<D, BF16, IMPLICIT, PAIR>;
-    static unsigned long long done = 0;
+    static unsigned long long done = 0, big = 0;
     cudaError_t e = set_smem_limit_once(kern, Cfg::SMEM, &done);
+    if (e == cudaSuccess && a.cluster_x > 8) e = allow_big_clusters_once(kern, &big);
     if (e != cudaSuccess) return e;
     constexpr unsigned halves = D / Cfg::DV;
     const unsigned n_ct = static_cast<unsigned>(tree_tc_row_ctas(a.R, D));
