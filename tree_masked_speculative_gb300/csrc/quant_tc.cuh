@@ -19,11 +19,12 @@
 //                 swizzled) in tile order: K as the exact integer codes (byte
 //                 permutes under the f16 exponent of 1024, minus 1024), V as
 //                 s * code + b rounded once to f16.
-//   warp 1      : TMEM owner and MMA issuer.  Scores transposed, tokens on the
-//                 M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M 128
-//                 tokens, N = max(16, RR) rows, one f32 accumulator per group,
-//                 double buffered); O += P V (M 128 with rows 0..RR-1 real, N 64
-//                 per V chunk, V MN-major, P from shared memory).
+//   warp 1      : TMEM owner and score MMA issuer.  Scores transposed, tokens
+//                 on the M side: S^T_g = Kcodes_g Q_g'^T per scale group g (M
+//                 128 tokens, N = max(16, RR) rows, one f32 accumulator per
+//                 group, double buffered).
+//   warp 18     : PV MMA issuer: O^T += V^T P^T (M 128 dimensions, N = max(16,
+//                 RR) rows, V MN-major, P as two f16 terms from shared memory).
 //   warps 10..17: softmax, one thread per (token, half of the rows): logit =
 //                 2^e_r * scale * log2(e) * (sum_g s_g S^T_g + b_g * 2^-e_r *
 //                 sum_{d in g} q_d) (+ log2(e) * float mask); row maxima by a
@@ -35,7 +36,7 @@
 // Q is staged once as f16 after scaling each row by a power of two (2^-e_r,
 // max |q'| in [2^14, 2^15)), exact for f16 and bf16 queries; K codes enter
 // the MMA exactly, so the scores carry only f32 accumulation error; V values
-// and P carry one f16 rounding each.  For 4-bit codes the decoded dimensions
+// carry one f16 rounding and P enters as two f16 terms (P_hi + P_lo).  For 4-bit codes the decoded dimensions
 // of every 8-dimension word sit in the order 0,4,1,5,2,6,3,7 (one mask-and-or
 // per pair); Q follows the same order and O columns are put back on output.
 // Every mbarrier wait is bounded; on a timeout the CTA sets bit 0 of the
@@ -55,7 +56,8 @@ using namespace ta::sm100;
 constexpr int kDecWarps = 8;      // decoders: four for K, four for V
 constexpr int kDecGroup = 4;
 constexpr int kSmWarps = 8;       // softmax: two per TMEM lane quarter, each half of the rows
-constexpr int kThreads = 32 * (2 + kDecWarps + kSmWarps);
+constexpr int kPvWarp = 2 + kDecWarps + kSmWarps;   // the PV MMA issuer, after the softmax warps
+constexpr int kThreads = 32 * (kPvWarp + 1);
 constexpr uint32_t kPolls = 1u << 21;     // bound of every wait: tries of up to kSleepNs each
 constexpr uint32_t kSleepNs = 1000;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -67,7 +69,7 @@ struct Bars {
     uint64_t vfull[kMaxRing], vempty[kMaxRing];
     uint64_t dfull[kMaxRing], dempty[kMaxRing];
     uint64_t s_full[2], s_free[2], p_full[2], p_free[2], o_done[2];   // per tile parity
-    uint64_t q_ready, drain;
+    uint64_t q_ready, drain, drain_pv;
     uint32_t tmem_base;
     volatile int abort_flag;
 };
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
         if (lane == 31) {
             mbar_init(&bars->q_ready, kSmWarps);
             mbar_init(&bars->drain, 1);
+            mbar_init(&bars->drain_pv, 1);
             bars->abort_flag = 0;
         }
         fence_mbar_init();
@@ -286,7 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     const int sw = warp - 2 - kDecWarps;                // softmax warp index (0..7 for those warps)
     const int E = DIM / 32;                             // Q elements per lane (2, 4 or 8)
     float qx[RPW][8];
-    if (sw >= 0) {
+    if (sw >= 0 && sw < kSmWarps) {
         const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
@@ -404,8 +407,12 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             for (int n = vn > NV ? vn - NV : 0; n < vn; ++n)
                 if (!mbar_wait_sleep(&bars->vfull[n % NV], static_cast<uint32_t>(n / NV) & 1u, kPolls, kSleepNs)) note_abort(bars, err);
         }
-    } else if (warp == 1) {
-        // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == kPvWarp) {
+        // --------------------------------------------------------- MMA issuers
+        // Warp 1 issues the score MMAs, warp kPvWarp the PV MMAs, so that one
+        // thread's waits (for decoded chunks, P, free buffers) overlap the
+        // other's MMAs; each takes chunks from its own decoded ring.
+        const bool is_s = warp == 1;
         if (lane == 0 && T > 0) {
             const uint32_t id_s = idesc_f16(128, RP, 0, 0, 0);
             const uint32_t id_pv = idesc_f16(128, RP, 0, 1, 0);   // A = V (MN-major), B = P (K-major)
@@ -486,16 +493,18 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 mma_commit(&bars->p_free[t & 1]);   // P_t buffer free once PV_t is done
                 return true;
             };
-            bool ok = wait1(bars, &bars->q_ready, 0, err);   // Q operand staged
-            tc_fence_after();
-            if (ok) ok = issue_s(0);
-            for (int t = 0; t < T && ok; ++t) {
-                if (t + 1 < T) ok = issue_s(t + 1);
-                if (ok) ok = issue_pv(t);
+            bool ok = true;
+            if (is_s) {
+                ok = wait1(bars, &bars->q_ready, 0, err);   // Q operand staged
+                tc_fence_after();
+                for (int t = 0; t < T && ok; ++t) ok = issue_s(t);
+            } else {
+                for (int t = 0; t < T && ok; ++t) ok = issue_pv(t);
             }
             // Drain: all MMAs issued by this thread have completed.
-            mma_commit(&bars->drain);
-            if (!mbar_wait_sleep(&bars->drain, 0, kPolls, kSleepNs)) note_abort(bars, err);
+            uint64_t *dr = is_s ? &bars->drain : &bars->drain_pv;
+            mma_commit(dr);
+            if (!mbar_wait_sleep(dr, 0, kPolls, kSleepNs)) note_abort(bars, err);
         }
     } else if (warp < 2 + kDecWarps) {
         // ------------------------------------------------------------ decoders
@@ -579,7 +588,10 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
                 }
             }
             // draft tree over the last tree_ql tokens: node bitsets, by the first warp
-            if (sw == 0 && lane < a.tree_ql) sTree[lane] = quant_tree_ancestors(a.tree_parents, a.tree_ql, lane);
+            if (sw == 0 && a.tree_ql > 0) {
+                const uint32_t anc = quant_tree_ancestors(a.tree_parents, a.tree_ql);
+                if (lane < a.tree_ql) sTree[lane] = anc;
+            }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bars->q_ready);
