@@ -204,7 +204,8 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     const int tree_lo = N - a.tree_ql;
     uint32_t tree_bits = 0u;
     if (a.tree_ql > 0) {
-        const uint32_t mine = quant_tree_ancestors(a.tree_parents, a.tree_ql);
+        const uint32_t mine =
+            quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
         tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
     }
     const int pb_l = j / REP;  // pass (within a batch) of the lane's reduced scores

@@ -289,6 +289,8 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
     const int sw = warp - 2 - kDecWarps;                // softmax warp index (0..7 for those warps)
     const int E = DIM / 32;                             // Q elements per lane (2, 4 or 8)
     float qx[RPW][8];
+    // the first softmax warp also fetches the draft tree's parent array now
+    const int tree_up = (sw == 0 && lane < a.tree_ql) ? __ldg(a.tree_parents + lane) : -1;
     if (sw >= 0 && sw < kSmWarps) {
         const uint16_t *qg = static_cast<const uint16_t *>(a.queries);
 #pragma unroll
@@ -589,7 +591,7 @@ __global__ void __launch_bounds__(kThreads, 1) quant_tc_kernel(const QuantArgs a
             }
             // draft tree over the last tree_ql tokens: node bitsets, by the first warp
             if (sw == 0 && a.tree_ql > 0) {
-                const uint32_t anc = quant_tree_ancestors(a.tree_parents, a.tree_ql);
+                const uint32_t anc = quant_tree_ancestors(tree_up, a.tree_ql);
                 if (lane < a.tree_ql) sTree[lane] = anc;
             }
             fence_proxy_async_smem();

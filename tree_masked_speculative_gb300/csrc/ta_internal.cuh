@@ -187,12 +187,12 @@ constexpr int kMaxQuantTreeNodes = 32;
 // Ancestor bitset of node `lane` (lane < L <= 32; 0 for the other lanes):
 // the node itself and the chain lane, parents[lane], ... that a value outside
 // [0, current node) ends (the rule of tree_mask_build).  Warp-collective: lane
-// i loads parents[i] once and the chains are followed by shuffles, one level
-// per step, so no chain waits on a dependent global load.
-__device__ __forceinline__ uint32_t quant_tree_ancestors(const int32_t *parents, int L) {
+// i holds parents[i] and the chains are followed by shuffles, one level per
+// step, so no chain waits on a dependent global load.
+// `up` is parents[lane] (any value for lane >= L), loaded by the caller.
+__device__ __forceinline__ uint32_t quant_tree_ancestors(int up, int L) {
     const int lane = static_cast<int>(threadIdx.x & 31u);
-    int up = lane < L ? __ldg(parents + lane) : -1;
-    if (up < 0 || up >= lane) up = -1;                     // the chain ends at this node
+    if (lane >= L || up < 0 || up >= lane) up = -1;        // the chain ends at this node
     uint32_t bits = lane < L ? 1u << lane : 0u;
     int node = lane < L ? up : -1;
     for (int step = 0; step < L; ++step) {                 // each step goes to a smaller node
