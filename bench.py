@@ -58,9 +58,9 @@ def parse():
                     help="run --warmup eager steps and exit (a short, graph-free run for a profiler)")
     ap.add_argument("--mask-build", action="store_true",
                     help="tree workloads: also time the device-side tree-mask build from the parent array")
-    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2],
-                    help="kernel family of the main pass: 0 automatic, 1 CUDA cores, 2 tensor cores "
-                         "where the shape allows them")
+    ap.add_argument("--kernel", type=int, default=0, choices=[0, 1, 2, 3],
+                    help="kernel family of the main pass: 0 automatic, 1 CUDA cores, 2 tcgen05 tensor cores "
+                         "where the shape allows them, 3 (quantized only) warp MMA where the shape allows it")
     ap.add_argument("--tree-mask", default="dense", choices=["dense", "parents"],
                     help="tree and draft-tree workloads: the mask as the dense array (tree_attn_fwd, "
                          "quant_sdpa_fwd) or as the parent array (tree_attn_fwd_parents, quant_sdpa_fwd_tree)")
@@ -293,8 +293,12 @@ class QuantBench:
         self.bytes_per_step = wl.kv_bytes
         self.name = wl.name
         self.dtype = "u%d" % wl.bits
-        self.tc = ta.quant_sdpa_uses_tensor_cores(self.p) == 1
-        kern = "quant_tc_kernel (tensor cores)" if self.tc else "quant_kernel (CUDA cores)"
+        self.family = ta.quant_sdpa_kernel_family(self.p)
+        self.tc = self.family != ta.KERNEL_CUDA_CORES
+        fam = {ta.KERNEL_TENSOR_CORES: ("quant_tc_kernel (tcgen05 tensor cores)", "tcgen05 tensor cores"),
+               ta.KERNEL_WARP_MMA: ("quant_mma_kernel (warp MMA tensor cores)", "warp MMA tensor cores"),
+               ta.KERNEL_CUDA_CORES: ("quant_kernel (CUDA cores)", "CUDA cores")}
+        kern, self.family_name = fam[self.family]
         call = "quant_sdpa_fwd_tree" if self.tree is not None else "quant_sdpa_fwd"
         self.fwd_label = "main pass (%s) + split merge (%s, one call)" % (kern, call)
         self.traffic_key = traffic_key(wl.name, self.tree is not None, kernel)
@@ -319,7 +323,7 @@ class QuantBench:
         return {"workload": wl.name, "batch": wl.batch, "n_q_heads": wl.n_q_heads,
                 "n_kv_heads": wl.n_kv_heads, "dim": wl.dim, "tokens": wl.tokens, "bits": wl.bits,
                 "group_size": wl.group_size, "window_size": wl.window_size, "splits": self.nwg,
-                "kernel": "tensor cores" if self.tc else "CUDA cores",
+                "kernel": self.family_name,
                 "tree_mask": "parent array" if self.tree is not None else None,
                 "l2": "rotating %d K/V sets, %.0f MB read per rotation (> 3x L2)" % (
                     self.nsets, self.nsets * self.bytes_per_step / 1e6)}
@@ -406,6 +410,11 @@ def timed_graph_steps(fn, steps, start):
     gr = capture(fn, rem, start) if rem else None
     if per_step is None:
         per_step = (ta.ta_launch_count() - c1) / max(rem, 1)
+    # one untimed replay of each graph first: a graph's first launch also
+    # uploads it to the device, which is not a cost of the steps
+    for gg in (g, gr):
+        if gg is not None:
+            gg.replay()
     torch.cuda.synchronize()
     s = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)

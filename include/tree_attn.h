@@ -64,7 +64,9 @@ typedef enum { TA_F32 = 0, TA_F16 = 1, TA_BF16 = 2, TA_U32 = 3, TA_I32 = 4 } ta_
 typedef enum {
     TA_KERNEL_AUTO = 0,         /* tensor cores where the shape makes a dense contraction */
     TA_KERNEL_CUDA_CORES = 1,   /* always the CUDA-core kernel */
-    TA_KERNEL_TENSOR_CORES = 2  /* the tensor-core kernel wherever its shape rules allow it */
+    TA_KERNEL_TENSOR_CORES = 2, /* the tensor-core kernel wherever its shape rules allow it */
+    TA_KERNEL_WARP_MMA = 3      /* quantized path only: the warp-MMA kernel wherever its
+                                   shape rules allow it (the tree path rejects it) */
 } ta_kernel;
 
 /* Borrowed device buffer. `bytes` is the usable size starting at `ptr`. */
@@ -368,9 +370,25 @@ const char *ta_last_error(void);
 uint64_t ta_launch_count(void);
 
 /*
- * 1 if quant_sdpa_fwd with these params (p->kernel included) takes the
- * tensor-core kernel, 0 if the CUDA-core kernel, -1 for invalid params.  No
- * device work.
+ * Kernel family quant_sdpa_fwd takes with these params (p->kernel included):
+ * TA_KERNEL_TENSOR_CORES (the tcgen05 kernel), TA_KERNEL_WARP_MMA or
+ * TA_KERNEL_CUDA_CORES; -1 for invalid params.  No device work.
+ *
+ * The warp-MMA kernel serves head dimensions 64, 128 and 256 with group size
+ * 32 or 64, four query rows per CTA.  With TA_KERNEL_AUTO it is chosen below
+ * 16 query rows per KV row (and wherever the tcgen05 kernel's rules fail): its
+ * scores multiply the exact K codes with Q scaled per row by a power of two
+ * into f16 (the group scales and biases are applied to the f32 sums), and P V
+ * takes V dequantized once to f16 (s * code + b, one rounding) and P as two
+ * f16 terms, as the tcgen05 kernel does; the same f16-range assumption on the
+ * dequantized V values applies.
+ */
+int quant_sdpa_kernel_family(const ta_quant_params *p);
+
+/*
+ * 1 if quant_sdpa_fwd with these params (p->kernel included) takes a
+ * tensor-core kernel (tcgen05 or warp MMA), 0 if the CUDA-core kernel, -1 for
+ * invalid params.  No device work.
  *
  * The tensor-core kernel serves head dimensions 64, 128 and 256 when TMEM
  * holds O (dim f32 columns) and two score buffers (dim / group_size groups x
@@ -386,8 +404,9 @@ uint64_t ta_launch_count(void);
 int quant_sdpa_uses_tensor_cores(const ta_quant_params *p);
 
 /*
- * Test hook, not for production use: quant_sdpa_fwd on the CUDA-core kernel
- * (p->kernel must resolve to it, else TA_ERR_UNSUPPORTED) with the first K/V
+ * Test hook, not for production use: quant_sdpa_fwd on the CUDA-core or the
+ * warp-MMA kernel (p->kernel must resolve to one of them, else
+ * TA_ERR_UNSUPPORTED) with the first K/V
  * copy wait of every CTA bounded by `first_wait_polls` polls instead of the
  * normal bound; 0 makes that wait give up at once.  It exercises the failure
  * path of the kernel's bounded waits without any fault: the CTA ORs 1 into the

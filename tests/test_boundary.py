@@ -310,7 +310,7 @@ def test_kernel_choice_is_per_call(ta):
     o = ta.TreeOptions(0, ta.MASK_DENSE, 0, 0)
     assert ta.lib.tree_attn_fwd_ex(ctypes.byref(p), ctypes.byref(o), b, b, b, None, b, b, None) == 1
     assert "needs a mask" in ta.ta_last_error()
-    q = ta.quant_params(1, 8, 2, 128, 100, 4, 64, 0, 0, 0.1, 0, 3)
+    q = ta.quant_params(1, 8, 2, 128, 100, 4, 64, 0, 0, 0.1, 0, 4)
     assert ta.quant_sdpa_uses_tensor_cores(q) == -1
     assert ta.quant_sdpa_tmp_bytes(q) == 2 ** 64 - 1
     assert ta.ta_launch_count() == before
@@ -356,18 +356,33 @@ def test_quant_kernel_family_choice(ta):
     """Which quantized kernel a shape takes (no device work)."""
     def p(dim, G=64, nQ=32, nKV=8, bits=4, kernel=0):
         return ta.quant_params(1, nQ, nKV, dim, 1000, bits, G, 0, 0, 0.1, 0, kernel)
-    assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 0            # 4 rows per KV row: CUDA cores
-    assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128)) == 1    # 16 rows per KV row
+    fam = ta.quant_sdpa_kernel_family
+    TC, MMA, CC = ta.KERNEL_TENSOR_CORES, ta.KERNEL_WARP_MMA, ta.KERNEL_CUDA_CORES
+    assert fam(p(128)) == MMA                 # 4 rows per KV row: warp MMA
+    assert fam(p(128, nQ=128)) == TC          # 16 rows per KV row: tcgen05
+    assert fam(p(512, nQ=256)) == CC          # neither tensor-core kernel takes dim 512
+    assert fam(p(96, G=32)) == CC             # warp MMA: dims 64, 128, 256 only
+    assert fam(p(128, G=128)) == CC           # warp MMA: group size 32 or 64 only
+    assert fam(p(256, bits=8)) == MMA
+    assert fam(p(256, bits=8, nQ=256)) == MMA  # tcgen05 rings exceed shared memory: warp MMA
+    assert fam(p(64, G=32, bits=8)) == MMA
+    assert fam(p(128, kernel=1)) == CC
+    assert fam(p(128, kernel=3)) == MMA
+    assert fam(p(128, nQ=128, kernel=3)) == MMA
+    assert fam(p(512, kernel=3)) == CC
+    assert fam(p(128, kernel=2)) == TC
+    assert fam(p(256, bits=4, kernel=2)) == TC
+    assert fam(p(256, bits=8, kernel=2)) == CC        # rings exceed shared memory
+    assert fam(p(64, G=32, kernel=2)) == TC
+    assert fam(p(512, kernel=2)) == CC                # O alone fills TMEM
+    assert fam(p(96, G=32, kernel=2)) == CC           # not a multiple of 64
+    assert fam(p(256, G=16, nQ=256, bits=8, kernel=2)) == CC   # 16 groups x 32 rows
+    assert fam(p(100)) == -1                  # invalid params
+    assert fam(p(128, kernel=4)) == -1        # no such family
+    assert ta.quant_sdpa_uses_tensor_cores(p(128)) == 1
+    assert ta.quant_sdpa_uses_tensor_cores(p(128, kernel=1)) == 0
     assert ta.quant_sdpa_uses_tensor_cores(p(512, nQ=256)) == 0
-    assert ta.quant_sdpa_uses_tensor_cores(p(128, kernel=2)) == 1
-    assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=4, kernel=2)) == 1
-    assert ta.quant_sdpa_uses_tensor_cores(p(256, bits=8, kernel=2)) == 0       # rings exceed shared memory
-    assert ta.quant_sdpa_uses_tensor_cores(p(64, G=32, kernel=2)) == 1
-    assert ta.quant_sdpa_uses_tensor_cores(p(512, kernel=2)) == 0            # O alone fills TMEM
-    assert ta.quant_sdpa_uses_tensor_cores(p(96, G=32, kernel=2)) == 0       # not a multiple of 64
-    assert ta.quant_sdpa_uses_tensor_cores(p(256, G=16, nQ=256, bits=8, kernel=2)) == 0   # 16 groups x 32 rows
-    assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1           # invalid params
-    assert ta.quant_sdpa_uses_tensor_cores(p(128, nQ=128, kernel=1)) == 0
+    assert ta.quant_sdpa_uses_tensor_cores(p(100)) == -1
 
 
 @pytest.mark.parametrize("q_l,nQ,tokens,pbytes,pdtype,st_want,frag", [

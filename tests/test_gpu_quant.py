@@ -19,10 +19,11 @@ def ta():
     return m
 
 
-@pytest.fixture(params=[2, 1], ids=["tensor_cores", "cuda_cores"])
+@pytest.fixture(params=[2, 1, 3], ids=["tensor_cores", "cuda_cores", "warp_mma"])
 def kern(request):
-    """Every test runs on both kernel families: the tensor-core kernel (where
-    the shape allows it; others fall back to CUDA cores) and the CUDA-core one."""
+    """Every test runs on the three kernel families: the tcgen05 kernel and the
+    warp-MMA kernel (each where its shape rules allow it; other shapes fall
+    back to CUDA cores) and the CUDA-core one."""
     return request.param
 
 
@@ -206,9 +207,9 @@ def test_bounded_wait_timeout_sets_status_and_returns(ta):
     wl = qwl(B=2, nQ=8, nKV=2, dim=128, N=2000, bits=4, G=64, sinks=1, dtype="f16")
     inp = W.make_quant_inputs(wl)
     d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
-    for nwg in (1, 0):
+    for nwg, kernel in ((1, 1), (0, 1), (1, 3), (0, 3)):
         p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits, wl.group_size,
-                            wl.has_sinks, wl.window_size, wl.scale, nwg, 1)
+                            wl.has_sinks, wl.window_size, wl.scale, nwg, kernel)
         nb = ta.quant_sdpa_tmp_bytes(p)
         tmp = torch.zeros((nb + 3) // 4, dtype=torch.float32, device="cuda")
         out = torch.zeros((wl.rows, wl.dim), dtype=torch.float32, device="cuda")
@@ -227,7 +228,7 @@ def test_bounded_wait_timeout_sets_status_and_returns(ta):
                          wl.has_sinks, wl.window_size, wl.scale, 0, 2)
     tmp2 = torch.zeros((ta.quant_sdpa_tmp_bytes(p2) + 3) // 4, dtype=torch.float32, device="cuda")
     before = ta.ta_launch_count()
-    with pytest.raises(ta.TreeAttentionError, match="CUDA-core kernel only"):
+    with pytest.raises(ta.TreeAttentionError, match="CUDA-core or warp-MMA kernel only"):
         ta.ta_test_quant_sdpa_fwd_wait_limit(0, p2, *args[:-2], tmp2, out)
     assert ta.ta_launch_count() == before
 

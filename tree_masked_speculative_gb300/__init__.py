@@ -22,13 +22,14 @@ __all__ = [
     "tree_attn_fwd_causal", "tree_attn_fwd_parents", "tree_attn_fwd_ex", "tree_attn_status_offset",
     "tree_attn_reduce", "tree_attn_fwd_noalloc", "quant_sdpa_num_splits", "quant_sdpa_tmp_bytes",
     "quant_sdpa_fwd", "ta_last_error", "ta_launch_count", "quant_sdpa_uses_tensor_cores",
+    "quant_sdpa_kernel_family", "KERNEL_WARP_MMA",
     "ta_test_quant_sdpa_fwd_wait_limit", "quant_sdpa_fwd_tree", "tree_attention", "quant_sdpa", "tree_params", "quant_params",
     "tree_mask_build", "TreeOptions", "KERNEL_AUTO", "KERNEL_CUDA_CORES", "KERNEL_TENSOR_CORES",
 ]
 
 TA_OK = 0
 TA_F32, TA_F16, TA_BF16, TA_U32, TA_I32 = 0, 1, 2, 3, 4
-KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES = 0, 1, 2
+KERNEL_AUTO, KERNEL_CUDA_CORES, KERNEL_TENSOR_CORES, KERNEL_WARP_MMA = 0, 1, 2, 3
 MASK_DENSE, MASK_CAUSAL, MASK_PARENTS = 0, 1, 2
 STATUS_NAMES = {0: "TA_OK", 1: "TA_ERR_INVALID_ARGUMENT", 2: "TA_ERR_BUFFER_TOO_SMALL",
                 3: "TA_ERR_OVERFLOW", 4: "TA_ERR_UNSUPPORTED", 5: "TA_ERR_CUDA"}
@@ -115,6 +116,8 @@ def _load() -> ctypes.CDLL:
     L.ta_test_quant_sdpa_fwd_wait_limit.restype = ctypes.c_int
     L.quant_sdpa_uses_tensor_cores.argtypes = [PQ]
     L.quant_sdpa_uses_tensor_cores.restype = ctypes.c_int
+    L.quant_sdpa_kernel_family.argtypes = [PQ]
+    L.quant_sdpa_kernel_family.restype = ctypes.c_int
     L.tree_mask_build.argtypes = [PT, B, B, P]
     L.tree_mask_build.restype = ctypes.c_int
     return L
@@ -170,6 +173,10 @@ def ta_launch_count() -> int:
 
 def quant_sdpa_uses_tensor_cores(p: QuantParams) -> int:
     return int(lib.quant_sdpa_uses_tensor_cores(ctypes.byref(p)))
+
+
+def quant_sdpa_kernel_family(p: QuantParams) -> int:
+    return int(lib.quant_sdpa_kernel_family(ctypes.byref(p)))
 
 
 def tree_params(n_heads, n_kv_heads, head_dim, kv_seq_len, kv_capacity, scale, q_l, mask_stride,

@@ -405,8 +405,8 @@ ta_status check_quant_params(const ta_quant_params *p) {
                     p->group_size);
     if (p->tokens == 0) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: tokens must be > 0");
     if (p->has_sinks > 1) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: has_sinks must be 0 or 1");
-    if (p->kernel > (uint32_t)TA_KERNEL_TENSOR_CORES)
-        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: kernel must be 0 (auto), 1 or 2, got %u", p->kernel);
+    if (p->kernel > (uint32_t)TA_KERNEL_WARP_MMA)
+        return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: kernel must be 0 (auto), 1, 2 or 3, got %u", p->kernel);
     if (!std::isfinite(p->scale)) return fail(TA_ERR_INVALID_ARGUMENT, "quant_sdpa: scale is not finite");
     if (p->group_size % (4 * pf) != 0)
         return fail(TA_ERR_UNSUPPORTED,
@@ -448,7 +448,7 @@ struct QtcShape {
 };
 bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
     const int path = (int)p->kernel;
-    if (path == TA_KERNEL_CUDA_CORES) return false;
+    if (path == TA_KERNEL_CUDA_CORES || path == TA_KERNEL_WARP_MMA) return false;
     if (p->dim != 64 && p->dim != 128 && p->dim != 256) return false;
     const int rep = (int)(p->n_q_heads / p->n_kv_heads);
     // automatic choice: the tensor-core kernel from 16 query rows per KV row
@@ -502,6 +502,22 @@ bool quant_tc_plan(const ta_quant_params *p, const QtcShape &sh, bool has_mb, bo
     return false;
 }
 
+// Kernel of a quantized call when the tcgen05 kernel does not take it: the
+// warp-MMA kernel where its shape rules allow (automatic choice or forced),
+// else the CUDA-core kernel.
+int quant_fallback_family(const ta_quant_params *p) {
+    const int path = (int)p->kernel;
+    if ((path == TA_KERNEL_AUTO || path == TA_KERNEL_WARP_MMA) &&
+        quant_mma_shape_ok((int)p->dim, (int)p->group_size))
+        return TA_KERNEL_WARP_MMA;
+    return TA_KERNEL_CUDA_CORES;
+}
+
+int quant_family(const ta_quant_params *p) {
+    QtcShape sh;
+    return quant_tc_shape(p, &sh) ? (int)TA_KERNEL_TENSOR_CORES : quant_fallback_family(p);
+}
+
 uint32_t window_tiles(const ta_quant_params *p, uint32_t *j_lo) {
     const uint32_t t_lo = p->tokens - window_tokens(p);
     *j_lo = t_lo / 128u;
@@ -527,7 +543,10 @@ uint32_t resolve_quant_nwg(const ta_quant_params *p) {
         if (nwg > 65535) nwg = 65535;
         return (uint32_t)nwg;
     }
-    const int per_sm = quant_ctas_per_sm((int)p->bits, (int)p->dim, (int)(p->dim / p->group_size));
+    const int ng = (int)(p->dim / p->group_size);
+    const int per_sm = quant_fallback_family(p) == TA_KERNEL_WARP_MMA
+                           ? quant_mma_ctas_per_sm((int)p->bits, (int)p->dim, ng)
+                           : quant_ctas_per_sm((int)p->bits, (int)p->dim, ng);
     if (per_sm <= 0) return 0;
     const uint64_t units = (uint64_t)p->batch * p->n_kv_heads * quant_row_groups(p);
     uint64_t nwg = ((uint64_t)sms * (uint64_t)per_sm) / units;
@@ -847,8 +866,8 @@ ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, cons
     a.tree_parents = tree_ql > 0 ? static_cast<const int32_t *>(parents_d->ptr) : nullptr;
     const bool use_tc = quant_tc_shape(p, &sh) && quant_tc_plan(p, sh, has_bool, has_float, &pl);
     if (test_hook && use_tc)
-        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: the wait-limit test hook takes the CUDA-core kernel only "
-                    "(set kernel = 1)");
+        return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: the wait-limit test hook takes the CUDA-core or warp-MMA "
+                    "kernel only (set kernel = 1 or 3)");
     if (use_tc) {
         uint32_t j_lo;
         a.ntile = (int)window_tiles(p, &j_lo);
@@ -862,6 +881,8 @@ ta_status quant_fwd_impl(const ta_quant_params *p, const ta_buf *queries_d, cons
         if ((uint64_t)kvr * (uint64_t)sh.n_rb > 65535u)
             return fail(TA_ERR_UNSUPPORTED, "quant_sdpa: too many KV rows x row blocks for one launch");
         e = launch_quant_tc(a, pl.smem, s);
+    } else if (quant_fallback_family(p) == TA_KERNEL_WARP_MMA) {
+        e = launch_quant_mma(a, s);
     } else {
         e = launch_quant_fma(a, s);
     }
@@ -909,8 +930,12 @@ TA_EXPORT const char *ta_last_error(void) { return g_err.c_str(); }
 
 TA_EXPORT uint64_t ta_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
+TA_EXPORT int quant_sdpa_kernel_family(const ta_quant_params *p) {
+    if (check_quant_params(p) != TA_OK) return -1;
+    return quant_family(p);
+}
+
 TA_EXPORT int quant_sdpa_uses_tensor_cores(const ta_quant_params *p) {
     if (check_quant_params(p) != TA_OK) return -1;
-    QtcShape sh;
-    return quant_tc_shape(p, &sh) ? 1 : 0;
+    return quant_family(p) == TA_KERNEL_CUDA_CORES ? 0 : 1;
 }

@@ -118,6 +118,24 @@ int quant_ctas_per_sm(int bits, int dim, int ng) {
     return 0;
 }
 
+bool quant_mma_shape_ok(int dim, int group_size) {
+    return (dim == 64 || dim == 128 || dim == 256) && (group_size == 32 || group_size == 64);
+}
+
+cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s) {
+    if (!quant_mma_shape_ok(a.dim, a.G)) return cudaErrorInvalidValue;
+    if (a.bits == 4) return launch_quant_mma_b4(a, s);
+    if (a.bits == 8) return launch_quant_mma_b8(a, s);
+    return cudaErrorInvalidValue;
+}
+
+int quant_mma_ctas_per_sm(int bits, int dim, int ng) {
+    if (ng <= 0 || !quant_mma_shape_ok(dim, dim / ng)) return 0;
+    if (bits == 4) return quant_mma_ctas_per_sm_b4(dim, ng);
+    if (bits == 8) return quant_mma_ctas_per_sm_b8(dim, ng);
+    return 0;
+}
+
 int quant_tc_ctas_per_sm(int bits, int rp, size_t smem) {
     if (bits == 4) return quant_tc_ctas_per_sm_b4(rp, smem);
     if (bits == 8) return quant_tc_ctas_per_sm_b8(rp, smem);

@@ -167,68 +167,22 @@ __device__ __forceinline__ void load_words(const uint32_t *p, uint32_t (&w)[WPL]
 // GC > 0: exact-shape instance (dim == DIMC, group size GC, both compile-time
 // so that shared-memory addressing folds into immediates); GC == 0: any
 // dim <= DIMC and group size, read at run time.
-template <int BITS, typename T, int DIMC, int GC>
-__global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const QuantArgs a) {
-    using S = Shape<BITS, DIMC>;
-    constexpr int CH = S::CH, NB = S::NB;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int lane = threadIdx.x;
-    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
-    const int q0 = kv * a.rep + rg * REP;
-    const int nrow = min(REP, a.rep - rg * REP);
-    const int N = a.N;
-    const int WPT = GC > 0 ? DIMC * BITS / 32 : a.wpt;
-    const int NG = GC > 0 ? DIMC / (GC > 0 ? GC : 1) : a.ng;
-    const int G = GC > 0 ? GC : a.G;
-    const int dim = GC > 0 ? DIMC : a.dim;
-    const QuantLayout L = quant_layout(WPT, NG, CH);
-    float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
-    float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
-    float2 *sP2 = reinterpret_cast<float2 *>(smem + L.p2);     // [token][row] {p, p}
-    float *sOBl = reinterpret_cast<float *>(smem + L.ob);      // [group][lane] sum_t p * b (lane's slots)
-    float *sQS = reinterpret_cast<float *>(smem + L.qs);       // [row][group] sum_{d in g} q'
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);   // A stage 0/1, B stage 0/1
+// Chunk staging shared by the quantized-KV kernels (one warp stages its own
+// chunks).  Group A of chunk c into stage b: lane 0 copies the K tile with one
+// bulk copy (mbarrier transaction bytes); the scale / bias runs and mask rows
+// are copied by all lanes with 16- or 4-byte cp.async that arrive on the same
+// mbarrier (count 1 + 32); tail chunks and unaligned rows are filled with
+// plain loads (zero beyond N).  Group B: lane 0 copies the V tile.
+template <int CH>
+struct QuantStager {
+    const QuantArgs &a;
+    const QuantLayout &L;
+    unsigned char *smem;
+    uint64_t *bars;   // A stages 0 .. ns-1, then B stages 0 .. ns-1
+    int WPT, NG, kv, q0, nrow, lane, ns;
 
-    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
-    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
-    const int nc = c_end - c_begin;
-
-    // score-pass roles: lane = (token in pass tp, dimension slice j)
-    const int tp = lane / S::LPT, j = lane % S::LPT;
-    const int d0 = j * DPL;
-    const bool qk_live = d0 < dim;
-    const int g_qk = qk_live ? d0 / G : 0;
-    const int r_l = j % REP;   // row of the lane's reduced scores
-    // draft tree over the last tree_ql tokens: the ancestor bitset of the lane's
-    // row's node (lane i < tree_ql builds node i's, the row's node takes it)
-    const int tree_lo = N - a.tree_ql;
-    uint32_t tree_bits = 0u;
-    if (a.tree_ql > 0) {
-        const uint32_t mine =
-            quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
-        tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
-    }
-    const int pb_l = j / REP;  // pass (within a batch) of the lane's reduced scores
-    // value-pass roles: lane = (token in pass tv, word slot wl)
-    const int tv = lane / S::LPV, wl = lane % S::LPV;
-    const bool pv_live = wl * S::WPL < WPT;
-    const int g_v = pv_live ? (wl * S::WPL * S::PF) / G : 0;
-
-    if (lane == 0) {
-        mbar_init(&bars[0], 33);   // group A: lane 0's expect-tx arrive + one cp.async arrive per lane
-        mbar_init(&bars[1], 33);
-        mbar_init(&bars[2], 1);    // group B: lane 0's expect-tx arrive
-        mbar_init(&bars[3], 1);
-        fence_mbar_init();
-    }
-    __syncwarp();
-
-    // ---- chunk staging.  Group A: lane 0 copies the K tile with one bulk copy
-    // (mbarrier transaction bytes); the scale / bias runs and mask rows are
-    // copied by all lanes with 16- or 4-byte cp.async that arrive on the same
-    // mbarrier (count 1 + 32); tail chunks and unaligned rows are filled with
-    // plain loads (zero beyond N).  Group B: lane 0 copies the V tile.
-    auto issue_a = [&](int c, int b) {
+    __device__ __forceinline__ void issue_a(int c, int b) const {
+        const int N = a.N;
         unsigned char *st = smem + L.a0 + b * L.a_stage;
         const int t0 = c * CH, tval = min(CH, N - t0);
         const bool full = tval == CH;
@@ -293,15 +247,78 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
             }
         }
         cp_arrive_noinc(&bars[b]);
-    };
-    auto issue_b = [&](int c, int b) {
+    }
+    __device__ __forceinline__ void issue_b(int c, int b) const {
+        const int N = a.N;
         if (lane == 0) {
             const int t0 = c * CH, tval = min(CH, N - t0);
             const uint32_t bytes = static_cast<uint32_t>(tval * WPT * 4);
-            mbar_arrive_expect_tx(&bars[2 + b], bytes);
-            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, bytes, &bars[2 + b]);
+            mbar_arrive_expect_tx(&bars[ns + b], bytes);
+            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, bytes,
+                      &bars[ns + b]);
         }
-    };
+    }
+};
+
+template <int BITS, typename T, int DIMC, int GC>
+__global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const QuantArgs a) {
+    using S = Shape<BITS, DIMC>;
+    constexpr int CH = S::CH, NB = S::NB;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x;
+    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
+    const int q0 = kv * a.rep + rg * REP;
+    const int nrow = min(REP, a.rep - rg * REP);
+    const int N = a.N;
+    const int WPT = GC > 0 ? DIMC * BITS / 32 : a.wpt;
+    const int NG = GC > 0 ? DIMC / (GC > 0 ? GC : 1) : a.ng;
+    const int G = GC > 0 ? GC : a.G;
+    const int dim = GC > 0 ? DIMC : a.dim;
+    const QuantLayout L = quant_layout(WPT, NG, CH);
+    float4 *sKS4 = reinterpret_cast<float4 *>(smem + L.ks4);   // {s, s, -2^23 s, -2^23 s}
+    float4 *sVS4 = reinterpret_cast<float4 *>(smem + L.vs4);
+    float2 *sP2 = reinterpret_cast<float2 *>(smem + L.p2);     // [token][row] {p, p}
+    float *sOBl = reinterpret_cast<float *>(smem + L.ob);      // [group][lane] sum_t p * b (lane's slots)
+    float *sQS = reinterpret_cast<float *>(smem + L.qs);       // [row][group] sum_{d in g} q'
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L.bars);   // A stage 0/1, B stage 0/1
+
+    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
+    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
+    const int nc = c_end - c_begin;
+
+    // score-pass roles: lane = (token in pass tp, dimension slice j)
+    const int tp = lane / S::LPT, j = lane % S::LPT;
+    const int d0 = j * DPL;
+    const bool qk_live = d0 < dim;
+    const int g_qk = qk_live ? d0 / G : 0;
+    const int r_l = j % REP;   // row of the lane's reduced scores
+    // draft tree over the last tree_ql tokens: the ancestor bitset of the lane's
+    // row's node (lane i < tree_ql builds node i's, the row's node takes it)
+    const int tree_lo = N - a.tree_ql;
+    uint32_t tree_bits = 0u;
+    if (a.tree_ql > 0) {
+        const uint32_t mine =
+            quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
+        tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
+    }
+    const int pb_l = j / REP;  // pass (within a batch) of the lane's reduced scores
+    // value-pass roles: lane = (token in pass tv, word slot wl)
+    const int tv = lane / S::LPV, wl = lane % S::LPV;
+    const bool pv_live = wl * S::WPL < WPT;
+    const int g_v = pv_live ? (wl * S::WPL * S::PF) / G : 0;
+
+    if (lane == 0) {
+        mbar_init(&bars[0], 33);   // group A: lane 0's expect-tx arrive + one cp.async arrive per lane
+        mbar_init(&bars[1], 33);
+        mbar_init(&bars[2], 1);    // group B: lane 0's expect-tx arrive
+        mbar_init(&bars[3], 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, 2};
+    auto issue_a = [&](int c, int b) { stg.issue_a(c, b); };
+    auto issue_b = [&](int c, int b) { stg.issue_b(c, b); };
     int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
     for (; a_issued < 2 && a_issued < nc; ++a_issued) issue_a(c_begin + a_issued, a_issued & 1);
     for (; b_issued < 2 && b_issued < nc; ++b_issued) issue_b(c_begin + b_issued, b_issued & 1);

@@ -1,0 +1,712 @@
+// Attention over an affine-quantized K/V cache with warp-level tensor-core
+// MMAs (mma.sync m16n8k16, f16 operands, f32 accumulation): the kernel for
+// fewer than 16 query rows per KV row.  Included by quant_mma_b4.cu and
+// quant_mma_b8.cu, which instantiate it.
+//
+// What it computes is the quantized-KV attention of quant_kernel.cuh
+// (metaltile-std flash_quantized_sdpa.rs: k = s * code + b per group, q
+// multiplied by `scale`, window / bool mask / float mask / sinks), with the
+// draft-tree gate of quant_sdpa_fwd_tree.
+//
+// Why MMAs with 4 query rows: on the CUDA cores every code costs a decode and
+// a multiply-add per query row, which for 4 rows keeps the FP32 pipe busier
+// than HBM.  Here the multiply-adds go to the tensor core, whose rate dwarfs
+// what 4 rows need, and a code costs about one integer instruction to decode.
+// One warp per CTA, the same work split and chunk staging as quant_kernel.cuh
+// (lane = quad gq = lane / 4 and position tq = lane % 4 in the MMA fragments):
+//  * scores S = Q K^T per chunk: A = Q (M = 16 rows: query row r of a
+//    dimension in scale group g sits in row 4 * (g % 4) + r, so one MMA keeps
+//    the partial sums of four groups apart), held as f16 scaled per row by a
+//    power of two (exact for f16 and bf16 queries); B = the K codes as exact
+//    f16 subnormals (code * 2^-24, one AND per two codes), each lane taking a
+//    quarter of its key's packed words; the group scales and the bias term
+//    sum_g b_g * sum_{d in g} q_d are applied to the f32 sums;
+//  * online softmax (log2 units, lazy running max) on the score fragments;
+//  * O^T = V^T P^T: A = V dequantized to f16 (s * code + b, one rounding:
+//    byte permutes pair two tokens' codes, a magic-exponent OR makes them
+//    f16, one subtract and one fused multiply-add per pair), B = P as two f16
+//    terms P_hi + P_lo in the 8 columns (4 rows x 2 terms).  The score
+//    accumulator fragments of two 8-key blocks are exactly the B fragment of a
+//    16-token block, so P never leaves the registers.
+#pragma once
+
+#include "quant_kernel.cuh"
+
+namespace ta {
+namespace quant {
+
+// D += A B, m16n8k16, f16 inputs, f32 accumulators (register fragments).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t h2_bits(__half2 h) { return *reinterpret_cast<uint32_t *>(&h); }
+__device__ __forceinline__ __half2 bits_h2(uint32_t u) { return *reinterpret_cast<__half2 *>(&u); }
+
+template <int BITS, int DIMC>
+struct MmaShape {
+    static constexpr int WPTC = DIMC * BITS / 32;          // packed words per token
+    static constexpr int CH = WPTC <= 32 ? 32 : 16;        // tokens per chunk (as quant_chunk_tokens)
+    static constexpr int KB = DIMC / 16;                   // score K-blocks = value M-blocks
+    static constexpr int NB = CH / 8;                      // score N-blocks (8 keys) per chunk
+    static constexpr int VB = CH / 16;                     // value K-blocks (16 tokens) per chunk
+    static constexpr int KW = WPTC / 4;                    // K words per lane per key (a quarter)
+    static constexpr int VW = WPTC / 8;                    // V words per lane per token (an eighth)
+    static_assert(KW >= 1 && VW >= 1 && CH % 16 == 0, "shape");
+};
+
+// Dimension and factor of score K-block v, lane position tq, k-slot j
+// (slots 0..3 = k 2tq, 2tq+1, 2tq+8, 2tq+9) for the K decode below.
+template <int BITS, int KW>
+__host__ __device__ inline int mma_k_dim(int v, int tq, int j, float *factor) {
+    if (BITS == 4) {
+        const int w = tq * KW + v / 2;
+        const int n = 4 * (v % 2) + (j == 0 ? 0 : j == 1 ? 2 : j == 2 ? 1 : 3);
+        *factor = j >= 2 ? 1.0f / 16.0f : 1.0f;   // high nibbles are decoded as 16 * code
+        return 8 * w + n;
+    }
+    const int w = tq * KW + v;
+    *factor = 1.0f;
+    return 4 * w + (j == 0 ? 0 : j == 1 ? 2 : j == 2 ? 1 : 3);
+}
+
+// Shared-memory layout: the two staging groups of quant_layout, then the
+// kernel's own arrays.
+struct QmmaLayout {
+    QuantLayout st;
+    int qa, qs, qf, ksf, kbias, vsb, bars, total;
+};
+__host__ __device__ inline QmmaLayout qmma_layout(int wpt, int ng, int ch, int dimc, int nacc, int ns) {
+    QmmaLayout M;
+    M.st = quant_layout(wpt, ng, ch, ns);
+    int o = M.st.v0 + ns * M.st.v_stage;
+    M.qa = quant_take(&o, nacc * (dimc / 16) * 32 * 16);   // Q A-fragments [acc][kblock][lane] uint4
+    M.qs = quant_take(&o, 4 * ng * 4 + 16);                // [row][group] scale*log2e * sum q, then 2^e per row
+    M.qf = quant_take(&o, 4 * dimc * 4);                   // q rows in f32 (setup)
+    M.ksf = quant_take(&o, ch * ng * 4);                   // [token][group] K scale, f32
+    M.kbias = quant_take(&o, ch * 4 * 4);                  // [token][row] score bias term
+    M.vsb = quant_take(&o, ng * (ch / 2) * 8);             // [group][token pair] {s, s}, {b, b} f16
+    M.bars = quant_take(&o, 2 * ns * 8);
+    M.total = o;
+    return M;
+}
+
+// Stages of each staging group (K words + scales + masks; V words).
+constexpr int kQmmaStages = 2;
+
+// Accumulator sets of the score MMA: four scale groups per set.
+__host__ __device__ inline int qmma_nacc(int ng) { return (ng + 3) / 4; }
+
+template <int BITS, typename T, int DIMC, int GC>
+__global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
+    using S = MmaShape<BITS, DIMC>;
+    constexpr int CH = S::CH, KB = S::KB, NB = S::NB, VB = S::VB, KW = S::KW, VW = S::VW;
+    constexpr int NG = DIMC / GC;
+    constexpr int NACC = (NG + 3) / 4;
+    constexpr int WPT = S::WPTC;
+    constexpr int NS = kQmmaStages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x, gq = lane >> 2, tq = lane & 3;
+    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
+    const int q0 = kv * a.rep + rg * REP;
+    const int nrow = min(REP, a.rep - rg * REP);
+    const int N = a.N;
+    const QmmaLayout M = qmma_layout(WPT, NG, CH, DIMC, NACC, NS);
+    const QuantLayout &L = M.st;
+    uint4 *sQA = reinterpret_cast<uint4 *>(smem + M.qa);
+    float *sQS = reinterpret_cast<float *>(smem + M.qs);
+    float *sQF = reinterpret_cast<float *>(smem + M.qf);
+    float *sKsf = reinterpret_cast<float *>(smem + M.ksf);
+    float *sKbias = reinterpret_cast<float *>(smem + M.kbias);
+    uint2 *sVSB = reinterpret_cast<uint2 *>(smem + M.vsb);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M.bars);
+
+    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
+    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
+    const int nc = c_end - c_begin;
+
+    // the 4 query rows, element lane + 32 k per lane, loaded before anything waits
+    constexpr int QPL = DIMC / 32;
+    uint16_t qraw[REP][QPL];
+    {
+        const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.queries);
+#pragma unroll
+        for (int r = 0; r < REP; ++r)
+#pragma unroll
+            for (int k = 0; k < QPL; ++k)
+                qraw[r][k] = r < nrow ? __ldg(qg + static_cast<size_t>(q0 + r) * DIMC + lane + 32 * k)
+                                      : static_cast<uint16_t>(0);
+    }
+
+    const int r_l = gq & 3;   // query row of the lane's score fragments
+    const int tree_lo = N - a.tree_ql;
+    uint32_t tree_bits = 0u;
+    if (a.tree_ql > 0) {
+        const uint32_t mine =
+            quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
+        tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
+    }
+
+    if (lane == 0) {
+        for (int k = 0; k < NS; ++k) {
+            mbar_init(&bars[k], 33);      // group A: lane 0's expect-tx arrive + one cp.async arrive per lane
+            mbar_init(&bars[NS + k], 1);  // group B: lane 0's expect-tx arrive
+        }
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, NS};
+    // Group A of a full chunk whose runs are 16-byte aligned, in a call with a
+    // mask: one bulk copy per run, each issued by a lane of its own in the same
+    // instruction - lane 0 the K words, lanes 1-4 the K / V scale and bias
+    // runs, then one lane per bool-mask and float-mask row - after lane 0 has
+    // posted the byte count on the group-A barrier; the lanes' cp.async
+    // arrivals then complete at once.  Other chunks (and calls without a mask,
+    // where the many small bulk copies measured slower than the lanes' 16-byte
+    // cp.async) take the staging of quant_kernel.cuh.
+    const bool bulk_a = (a.mbool != nullptr || a.mfloat != nullptr) && a.al_sb &&
+                        (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
+    const unsigned char *cp_src = nullptr;   // this lane's run at token 0
+    uint32_t cp_stride = 0, cp_bytes = 0, cp_dst = 0, tx_a = 0;
+    {
+        const size_t kv0 = static_cast<size_t>(kv) * N;
+        const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
+        if (lane == 0) {
+            cp_src = reinterpret_cast<const unsigned char *>(a.kp + kv0 * WPT);
+            cp_stride = WPT * 4;
+            cp_dst = L.k;
+        } else if (lane <= 4) {
+            const void *base = lane == 1 ? a.ks : lane == 2 ? a.kb : lane == 3 ? a.vs : a.vb;
+            cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(base) + kv0 * NG);
+            cp_stride = NG * 2;
+            cp_dst = lane == 1 ? L.ks : lane == 2 ? L.kb : lane == 3 ? L.vs : L.vb;
+        } else if (lane < 5 + nb_rows) {
+            const int r = lane - 5;
+            cp_src = reinterpret_cast<const unsigned char *>(a.mbool + static_cast<size_t>(q0 + r) * N);
+            cp_stride = 4;
+            cp_dst = L.mb + r * CH * 4;
+        } else if (lane < 5 + nb_rows + nf_rows) {
+            const int r = lane - 5 - nb_rows;
+            cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(a.mfloat) +
+                                                             static_cast<size_t>(q0 + r) * N);
+            cp_stride = 2;
+            cp_dst = L.mf + r * CH * 2;
+        }
+        cp_bytes = cp_stride * CH;
+        tx_a = CH * (WPT * 4 + 4 * NG * 2 + nb_rows * 4 + nf_rows * 2);
+    }
+    auto issue_a = [&](int c, int b) {
+        const int t0 = c * CH;
+        if (bulk_a && t0 + CH <= N) {
+            unsigned char *st = smem + L.a0 + b * L.a_stage;
+            if (lane == 0) mbar_arrive_expect_tx(&bars[b], tx_a);
+            __syncwarp();
+            if (cp_src != nullptr)
+                bulk_load(st + cp_dst, cp_src + static_cast<size_t>(t0) * cp_stride, cp_bytes, &bars[b]);
+            cp_arrive_noinc(&bars[b]);
+        } else {
+            stg.issue_a(c, b);
+        }
+    };
+    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
+    for (; a_issued < NS && a_issued < nc; ++a_issued) issue_a(c_begin + a_issued, a_issued % NS);
+    for (; b_issued < NS && b_issued < nc; ++b_issued) stg.issue_b(c_begin + b_issued, b_issued % NS);
+
+    // ---- queries: lane holds element lane + 32 k of each row (loaded above);
+    // per-row power-of-two scale 2^e (max |q| 2^e in [2^14, 2^15)), group sums
+    // (scale * log2(e) * sum_{d in g} q_d), the scaled rows in shared memory
+    // and from them the lane's score A-fragments
+    const float qscale = a.scale * kLog2e;
+    float *sE2 = sQS + REP * NG;   // 2^e per row
+#pragma unroll
+    for (int r = 0; r < REP; ++r) {
+        float qv[QPL];
+        float mx = 0.0f;
+#pragma unroll
+        for (int k = 0; k < QPL; ++k) {
+            qv[k] = t2f<T>(qraw[r][k]);
+            mx = fmaxf(mx, fabsf(qv[k]));
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+        int e = 0;
+        if (mx > 0.0f) e = 14 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127);
+        const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
+        if (lane == 0) sE2[r] = e2;
+#pragma unroll
+        for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = qv[k] * e2;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
+            float x = 0.0f;
+#pragma unroll
+            for (int k = 0; k < QPL; ++k)
+                if ((32 * k) / GC == g) x += qv[k];
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+            if (lane == 0) sQS[r * NG + g] = qscale * x;
+        }
+    }
+    __syncwarp();
+    // A-fragment of accumulator set acc, K-block v for this lane: a0a1 (row gq,
+    // slots 0, 1), a2a3 (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3)
+#pragma unroll
+    for (int acc = 0; acc < NACC; ++acc)
+#pragma unroll
+        for (int v = 0; v < KB; ++v) {
+            uint32_t reg[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h) {
+                const int m = gq + ((h & 1) ? 8 : 0);
+                float val[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int j = (h >> 1) * 2 + e;
+                    float f;
+                    const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
+                    const int g = d / GC;
+                    const bool here = g / 4 == acc && (m >> 2) == g % 4;
+                    val[e] = here ? sQF[(m & 3) * DIMC + d] * f : 0.0f;
+                }
+                reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
+            }
+            sQA[(acc * KB + v) * 32 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+        }
+    // group sums of the row of this lane's score-bias entries (row = lane % 4)
+    float qs_l[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) qs_l[g] = sQS[(lane & 3) * NG + g];
+    // score scale of row r: scale * log2(e) * 2^24 (subnormal codes) / 2^e
+    const float alpha_l = qscale * 16777216.0f / sE2[r_l];
+    // the lane's scale groups in the score fragments: c0/c1 rows gq, c2/c3 rows gq + 8
+    int grp_lo[NACC], grp_hi[NACC];
+#pragma unroll
+    for (int acc = 0; acc < NACC; ++acc) {
+        grp_lo[acc] = 4 * acc + (gq >> 2);
+        grp_hi[acc] = 4 * acc + 2 + (gq >> 2);
+    }
+    // the lane's V words: gq * VW .. + VW of each token; their scale groups
+    int vgrp[VW];
+#pragma unroll
+    for (int u = 0; u < VW; ++u) vgrp[u] = ((gq * VW + u) * (32 / BITS)) / GC;
+    __syncwarp();
+
+    float Mrow = -INFINITY, Ssum = 0.0f;   // online softmax of row r_l (log2 units)
+    float O[KB][4];
+#pragma unroll
+    for (int mb = 0; mb < KB; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) O[mb][e] = 0.0f;
+
+    bool ok = true;
+    for (int i = 0; i < nc; ++i) {
+        const int c = c_begin + i, b = i % NS;
+        const uint32_t par = static_cast<uint32_t>(i / NS) & 1u;
+        if (!wait_warp(&bars[b], par, i == 0 ? a.first_wait_polls : kQuantWaitPolls)) { ok = false; break; }
+        ++a_done;
+        __syncwarp();
+        const unsigned char *st = smem + L.a0 + b * L.a_stage;
+        const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
+        const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + L.ks);
+        const uint16_t *sKb = reinterpret_cast<const uint16_t *>(st + L.kb);
+        const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + L.vs);
+        const uint16_t *sVb = reinterpret_cast<const uint16_t *>(st + L.vb);
+        const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
+        const uint16_t *sMf = reinterpret_cast<const uint16_t *>(st + L.mf);
+        const uint32_t *sV = reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage);
+        const int t0 = c * CH;
+
+        // gates of the lane's (row r_l, key) score slots: key 8 nb + 2 tq + e
+        bool live[NB][2];
+        bool any = false;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                const int tk = 8 * nb + 2 * tq + e;
+                const int t = t0 + tk;
+                bool g = r_l < nrow && t >= a.t_lo && t < N;
+                if (g && a.mbool != nullptr) g = sMb[r_l * CH + tk] != 0u;
+                if (g && a.tree_ql > 0 && t >= tree_lo) g = (tree_bits >> (t - tree_lo)) & 1u;
+                live[nb][e] = g;
+                any |= g;
+            }
+        const bool chunk_live = __any_sync(0xffffffffu, any);
+
+        float lg[NB][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) lg[nb][0] = lg[nb][1] = -INFINITY;
+        if (chunk_live) {
+            // per-chunk tables, each lane filling fixed entries with every load
+            // issued before the first store: K scales in f32 [t][g], the score
+            // bias per (token, row) [t][r] (row = lane % 4), and the V scale /
+            // bias pairs of token pairs (2p, 2p + 1) in f16 [g][p]
+            {
+                constexpr int NKS = (CH * NG + 31) / 32, NKB = CH * REP / 32, NVP = (NG * (CH / 2) + 31) / 32;
+                uint16_t ksr[NKS], kbr[NKB][NG], vsr[NVP][2], vbr[NVP][2];
+#pragma unroll
+                for (int j = 0; j < NKS; ++j) {
+                    const int idx = lane + 32 * j;
+                    ksr[j] = idx < CH * NG ? sKs[idx] : static_cast<uint16_t>(0);
+                }
+#pragma unroll
+                for (int j = 0; j < NKB; ++j) {
+                    const int t = (lane + 32 * j) / REP;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) kbr[j][g] = sKb[t * NG + g];
+                }
+#pragma unroll
+                for (int j = 0; j < NVP; ++j) {
+                    const int idx = lane + 32 * j;
+                    const int g = idx / (CH / 2), p = idx % (CH / 2);
+                    const bool in = idx < NG * (CH / 2);
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        vsr[j][e] = in ? sVs[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
+                        vbr[j][e] = in ? sVb[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < NKS; ++j)
+                    if (lane + 32 * j < CH * NG) sKsf[lane + 32 * j] = t2f<T>(ksr[j]);
+#pragma unroll
+                for (int j = 0; j < NKB; ++j) {
+                    float x = 0.0f;
+#pragma unroll
+                    for (int g = 0; g < NG; ++g) x = fmaf(t2f<T>(kbr[j][g]), qs_l[g], x);
+                    sKbias[lane + 32 * j] = x;
+                }
+#pragma unroll
+                for (int j = 0; j < NVP; ++j)
+                    if (lane + 32 * j < NG * (CH / 2)) {
+                        const __half2 sp = __floats2half2_rn(t2f<T>(vsr[j][0]), t2f<T>(vsr[j][1]));
+                        const __half2 bp = __floats2half2_rn(t2f<T>(vbr[j][0]), t2f<T>(vbr[j][1]));
+                        sVSB[lane + 32 * j] = make_uint2(h2_bits(sp), h2_bits(bp));
+                    }
+            }
+            __syncwarp();
+
+            // ---- scores: the lane's quarter of key 8 nb + gq, all K-blocks
+            uint32_t kw[NB][KW];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                const uint32_t *src = sK + (8 * nb + gq) * WPT + tq * KW;
+                if constexpr (KW % 4 == 0) {
+#pragma unroll
+                    for (int u = 0; u < KW; u += 4) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
+                        kw[nb][u] = x.x; kw[nb][u + 1] = x.y; kw[nb][u + 2] = x.z; kw[nb][u + 3] = x.w;
+                    }
+                } else if constexpr (KW == 2) {
+                    const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                    kw[nb][0] = x.x; kw[nb][1] = x.y;
+                } else {
+#pragma unroll
+                    for (int u = 0; u < KW; ++u) kw[nb][u] = src[u];
+                }
+            }
+            float sacc[NB][NACC][4];
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int acc = 0; acc < NACC; ++acc)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) sacc[nb][acc][e] = 0.0f;
+#pragma unroll
+            for (int v = 0; v < KB; ++v) {
+                uint4 af[NACC];
+#pragma unroll
+                for (int acc = 0; acc < NACC; ++acc) af[acc] = sQA[(acc * KB + v) * 32 + lane];
+#pragma unroll
+                for (int nb = 0; nb < NB; ++nb) {
+                    uint32_t b0, b1;
+                    if constexpr (BITS == 4) {
+                        const uint32_t w = kw[nb][v / 2];
+                        // bytes (2, 3) or (0, 1) of the word into the two halves
+                        const uint32_t y = __byte_perm(w, 0u, (v & 1) ? 0x3322u : 0x1100u);
+                        b0 = y & 0x000F000Fu;   // nibbles 0, 2 of the pair: code * 2^-24
+                        b1 = y & 0x00F000F0u;   // nibbles 1, 3: 16 * code * 2^-24
+                    } else {
+                        const uint32_t w = kw[nb][v];
+                        b0 = w & 0x00FF00FFu;               // bytes 0, 2
+                        b1 = __byte_perm(w, 0u, 0x4341u);   // bytes 1, 3
+                    }
+#pragma unroll
+                    for (int acc = 0; acc < NACC; ++acc)
+                        mma16816(sacc[nb][acc], af[acc].x, af[acc].y, af[acc].z, af[acc].w, b0, b1);
+                }
+            }
+            // scale groups apart, then the two halves of the quad pair (lanes
+            // gq and gq ^ 4 hold the other groups of the same row)
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int tk = 8 * nb + 2 * tq + e;
+                    float x = 0.0f;
+#pragma unroll
+                    for (int acc = 0; acc < NACC; ++acc) {
+                        if (grp_lo[acc] < NG) x = fmaf(sKsf[tk * NG + grp_lo[acc]], sacc[nb][acc][e], x);
+                        if (grp_hi[acc] < NG) x = fmaf(sKsf[tk * NG + grp_hi[acc]], sacc[nb][acc][2 + e], x);
+                    }
+                    x += __shfl_xor_sync(0xffffffffu, x, 16);
+                    if (live[nb][e]) {
+                        float v = fmaf(alpha_l, x, sKbias[tk * REP + r_l]);
+                        if (a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l * CH + tk]), v);
+                        lg[nb][e] = v;
+                    }
+                }
+        }
+
+        // ---- online softmax of row r_l (log2 units), lazy running max: M only
+        // moves when a score exceeds it by more than kSlack
+        bool grow = false;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) grow |= lg[nb][0] > Mrow + kSlack || lg[nb][1] > Mrow + kSlack;
+        if (__any_sync(0xffffffffu, grow)) {
+            float cmax = -INFINITY;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) cmax = fmaxf(cmax, fmaxf(lg[nb][0], lg[nb][1]));
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
+            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
+            const float m_new = fmaxf(Mrow, cmax);
+            const float alpha = m_new == Mrow ? 1.0f : ex2(Mrow - m_new);   // 0 while M = -inf
+            Mrow = m_new;
+            Ssum *= alpha;
+            // O^T columns of this lane: n = 2 tq, 2 tq + 1 -> rows (2 tq) % 4, (2 tq + 1) % 4
+            const int r0 = (2 * tq) & 3;
+            const float al0 = __shfl_sync(0xffffffffu, alpha, 4 * r0);
+            const float al1 = __shfl_sync(0xffffffffu, alpha, 4 * (r0 + 1));
+#pragma unroll
+            for (int mb = 0; mb < KB; ++mb) {
+                O[mb][0] *= al0;
+                O[mb][1] *= al1;
+                O[mb][2] *= al0;
+                O[mb][3] *= al1;
+            }
+        }
+        uint32_t pf[VB][2];   // B fragments of P: lanes gq < 4 P_hi, gq >= 4 P_lo
+        if (chunk_live) {
+            const bool lo_term = gq >= 4;
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb) {
+                float p[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    p[e] = Mrow == -INFINITY ? 0.0f : ex2(lg[nb][e] - Mrow);
+                    Ssum += p[e];
+                }
+                const __half2 hi = __floats2half2_rn(p[0], p[1]);
+                uint32_t f = h2_bits(hi);
+                if (lo_term) {
+                    const float2 hf = __half22float2(hi);
+                    f = h2_bits(__floats2half2_rn(p[0] - hf.x, p[1] - hf.y));
+                }
+                pf[nb >> 1][nb & 1] = f;
+            }
+        }
+        __syncwarp();
+        if (a_issued < nc) { issue_a(c_begin + a_issued, a_issued % NS); ++a_issued; }   // stage b is free
+        if (!wait_warp(&bars[NS + b], par)) { ok = false; break; }   // group B of chunk c
+        ++b_done;
+        __syncwarp();
+
+        // ---- values: O^T += V^T P^T per 16-token block
+        if (chunk_live) {
+#pragma unroll
+            for (int kb = 0; kb < VB; ++kb) {
+                // tokens of the fragment: (T0, T1) = 16 kb + 2 tq + {0, 1}, (T2, T3) = + 8
+                const int tA = 16 * kb + 2 * tq, tB = tA + 8;
+                uint32_t w[4][VW];
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    const int t = (k < 2 ? tA : tB) + (k & 1);
+                    const uint32_t *src = sV + t * WPT + gq * VW;
+                    if constexpr (VW % 4 == 0) {
+#pragma unroll
+                        for (int u = 0; u < VW; u += 4) {
+                            const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
+                            w[k][u] = x.x; w[k][u + 1] = x.y; w[k][u + 2] = x.z; w[k][u + 3] = x.w;
+                        }
+                    } else if constexpr (VW == 2) {
+                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                        w[k][0] = x.x; w[k][1] = x.y;
+                    } else {
+                        w[k][0] = src[0];
+                    }
+                }
+                uint2 sbA[VW], sbB[VW];
+#pragma unroll
+                for (int u = 0; u < VW; ++u) {
+                    sbA[u] = sVSB[vgrp[u] * (CH / 2) + tA / 2];
+                    sbB[u] = sVSB[vgrp[u] * (CH / 2) + tB / 2];
+                }
+                const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
+#pragma unroll
+                for (int mb = 0; mb < KB; ++mb) {
+                    uint32_t ar[4];
+                    if constexpr (BITS == 4) {
+                        const int u = mb >> 2, bi = mb & 3;
+                        const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
+                            const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
+                            const uint2 sb = hb ? sbB[u] : sbA[u];
+                            const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
+                            const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
+                            ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
+                            ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // M row gq + 8
+                        }
+                    } else {
+                        const int u = mb >> 1, b0 = 2 * (mb & 1);
+#pragma unroll
+                        for (int hb = 0; hb < 2; ++hb) {
+                            const uint2 sb = hb ? sbB[u] : sbA[u];
+#pragma unroll
+                            for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
+                                const int bi = b0 + hr;
+                                const uint32_t sel =
+                                    static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
+                                const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
+                                const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
+                                ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
+                            }
+                        }
+                    }
+                    // A regs: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq, T2 T3), a6a7 (gq + 8, T2 T3)
+                    mma16816(O[mb], ar[0], ar[1], ar[2], ar[3], pf[kb][0], pf[kb][1]);
+                }
+            }
+        }
+        __syncwarp();
+        if (b_issued < nc) { stg.issue_b(c_begin + b_issued, b_issued % NS); ++b_issued; }
+    }
+    pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
+    if (!ok) {
+        if (lane == 0 && a.err != nullptr) atomicOr(a.err, 1);
+        for (; a_done < a_issued; ++a_done) wait_warp(&bars[a_done % NS], static_cast<uint32_t>(a_done / NS) & 1u);
+        for (; b_done < b_issued; ++b_done)
+            wait_warp(&bars[NS + b_done % NS], static_cast<uint32_t>(b_done / NS) & 1u);
+        return;
+    }
+
+    // ---- row sums over the quad's keys; O^T: P_hi + P_lo columns (tq, tq + 2)
+    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 1);
+    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 2);
+#pragma unroll
+    for (int mb = 0; mb < KB; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) O[mb][e] += __shfl_xor_sync(0xffffffffu, O[mb][e], 2);
+    // lanes tq 0, 1 hold rows 2 tq, 2 tq + 1: c0 / c2 row 2 tq, c1 / c3 row 2 tq + 1
+    float Mr[2], Sr[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r = (2 * tq + k) & 3;
+        Mr[k] = __shfl_sync(0xffffffffu, Mrow, 4 * r);
+        Sr[k] = __shfl_sync(0xffffffffu, Ssum, 4 * r);
+    }
+    if (tq < 2) {
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const int r = 2 * tq + k;
+            if (r >= nrow) continue;
+            const int q = q0 + r;
+            float f = 1.0f;
+            if (a.nwg == 1) {
+                float cs = 1.0f, sf = Sr[k];
+                if (a.has_sinks) {
+                    const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
+                    const float mf = fmaxf(Mr[k], sk);
+                    cs = Mr[k] == -INFINITY ? 0.0f : ex2(Mr[k] - mf);
+                    sf = Sr[k] * cs + ex2(sk - mf);
+                }
+                f = sf > 0.0f ? cs / sf : 0.0f;
+            }
+#pragma unroll
+            for (int mb = 0; mb < KB; ++mb) {
+                // M row gq of block mb: the low code of its byte, M row gq + 8 the next dimension
+                int d;
+                if constexpr (BITS == 4) d = 8 * (gq * VW + (mb >> 2)) + 2 * (mb & 3);
+                else d = 4 * (gq * VW + (mb >> 1)) + 2 * (mb & 1);
+                const float x0 = O[mb][k], x1 = O[mb][2 + k];
+                if (a.nwg == 1) {
+                    st_out<T>(a.out, static_cast<size_t>(q) * DIMC + d, x0 * f, a.out_f32);
+                    st_out<T>(a.out, static_cast<size_t>(q) * DIMC + d + 1, x1 * f, a.out_f32);
+                } else {
+                    *reinterpret_cast<float2 *>(a.part_o + (static_cast<size_t>(split) * a.rows + q) * DIMC + d) =
+                        make_float2(x0, x1);
+                }
+            }
+        }
+    }
+    const float s_row = __shfl_sync(0xffffffffu, Ssum, 4 * (lane & 3));
+    const float m_row = __shfl_sync(0xffffffffu, Mrow, 4 * (lane & 3));
+    if (a.nwg > 1 && lane < REP && lane < nrow)
+        reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] =
+            make_float2(s_row, m_row);
+}
+
+template <int BITS, int DIMC, int GC>
+inline size_t mma_smem_bytes() {
+    using S = MmaShape<BITS, DIMC>;
+    return static_cast<size_t>(qmma_layout(S::WPTC, DIMC / GC, S::CH, DIMC, qmma_nacc(DIMC / GC), kQmmaStages).total);
+}
+
+template <int BITS, typename T, int DIMC, int GC>
+cudaError_t mma_launch_one(const QuantArgs &a, cudaStream_t s) {
+    auto kern = quant_mma_kernel<BITS, T, DIMC, GC>;
+    static unsigned long long done = 0;
+    cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(a.nwg * a.n_rg, a.kv_rows), 32, mma_smem_bytes<BITS, DIMC, GC>(), s>>>(a);
+    count_launch();
+    return cudaGetLastError();
+}
+
+template <int BITS, typename T, int DIMC, int GC>
+int mma_occupancy_one() {
+    auto kern = quant_mma_kernel<BITS, T, DIMC, GC>;
+    static unsigned long long done = 0;
+    if (set_smem_limit_once(kern, kQuantMaxSmem, &done) != cudaSuccess) return 0;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, mma_smem_bytes<BITS, DIMC, GC>()) != cudaSuccess)
+        return 0;
+    return n;
+}
+
+// Instances: head dimension 64, 128 or 256 exactly, group size 32 or 64
+// (quant_mma_shape_ok); anything else is not launched.
+template <int BITS, typename T>
+cudaError_t mma_launch_t(const QuantArgs &a, cudaStream_t s) {
+    const bool g32 = a.G == 32;
+    if (a.dim == 64) return g32 ? mma_launch_one<BITS, T, 64, 32>(a, s) : mma_launch_one<BITS, T, 64, 64>(a, s);
+    if (a.dim == 128) return g32 ? mma_launch_one<BITS, T, 128, 32>(a, s) : mma_launch_one<BITS, T, 128, 64>(a, s);
+    return g32 ? mma_launch_one<BITS, T, 256, 32>(a, s) : mma_launch_one<BITS, T, 256, 64>(a, s);
+}
+
+template <int BITS>
+cudaError_t mma_launch_bits(const QuantArgs &a, cudaStream_t s) {
+    return a.t_is_bf16 ? mma_launch_t<BITS, __nv_bfloat16>(a, s) : mma_launch_t<BITS, __half>(a, s);
+}
+
+template <int BITS, typename T>
+int mma_occupancy_t(int dim, int G) {
+    const bool g32 = G == 32;
+    if (dim == 64) return g32 ? mma_occupancy_one<BITS, T, 64, 32>() : mma_occupancy_one<BITS, T, 64, 64>();
+    if (dim == 128) return g32 ? mma_occupancy_one<BITS, T, 128, 32>() : mma_occupancy_one<BITS, T, 128, 64>();
+    return g32 ? mma_occupancy_one<BITS, T, 256, 32>() : mma_occupancy_one<BITS, T, 256, 64>();
+}
+
+template <int BITS>
+int mma_occupancy_bits(int dim, int ng) {
+    const int G = dim / ng;
+    const int a = mma_occupancy_t<BITS, __half>(dim, G), b = mma_occupancy_t<BITS, __nv_bfloat16>(dim, G);
+    return a < b ? a : b;
+}
+
+}  // namespace quant
+}  // namespace ta

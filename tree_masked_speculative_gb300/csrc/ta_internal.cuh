@@ -230,7 +230,8 @@ __host__ __device__ inline int quant_take(int *o, int bytes) {
     *o += (bytes + 15) & ~15;
     return r;
 }
-__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
+// ns: stages of each group (the CUDA-core kernel uses two).
+__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch, int ns = 2) {
     constexpr int R = kQuantRowsPerCta;
     QuantLayout L;
     int o = 0;   // inside a group-A stage
@@ -243,9 +244,9 @@ __host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch) {
     L.mf = quant_take(&o, R * ch * 2);
     L.a_stage = o;
     o = 0;
-    L.a0 = quant_take(&o, 2 * L.a_stage);
+    L.a0 = quant_take(&o, ns * L.a_stage);
     L.v_stage = (ch * wpt * 4 + 15) & ~15;
-    L.v0 = quant_take(&o, 2 * L.v_stage);
+    L.v0 = quant_take(&o, ns * L.v_stage);
     L.ks4 = quant_take(&o, ch * ng * 16);
     L.vs4 = quant_take(&o, ch * ng * 16);
     L.p2 = quant_take(&o, (ch > 32 ? ch : 32) * R * 8);   // also holds [row][32] q sums
@@ -392,6 +393,15 @@ cudaError_t launch_quant_tc_b8(const QuantArgs &a, size_t smem, cudaStream_t s);
 int quant_tc_ctas_per_sm(int bits, int rp, size_t smem);
 int quant_tc_ctas_per_sm_b4(int rp, size_t smem);
 int quant_tc_ctas_per_sm_b8(int rp, size_t smem);
+// Warp-MMA quantized-KV kernel (mma.sync, one warp per CTA, 4 query rows):
+// head dimension 64, 128 or 256 exactly and group size 32 or 64.
+bool quant_mma_shape_ok(int dim, int group_size);
+cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_mma_b4(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_mma_b8(const QuantArgs &a, cudaStream_t s);
+int quant_mma_ctas_per_sm(int bits, int dim, int ng);
+int quant_mma_ctas_per_sm_b4(int dim, int ng);
+int quant_mma_ctas_per_sm_b8(int dim, int ng);
 
 // Rows of one CTA in the CUDA-core tree kernel.
 constexpr int kFmaRowsPerCta = 16;
