@@ -102,7 +102,9 @@ constexpr int kQmmaStages = 2;
 // Accumulator sets of the score MMA: four scale groups per set.
 __host__ __device__ inline int qmma_nacc(int ng) { return (ng + 3) / 4; }
 
-template <int BITS, typename T, int DIMC, int GC>
+// MASKED: the call passes a bool or a float mask (instances without one carry
+// no mask code and stage every chunk through the lanes' cp.async).
+template <int BITS, typename T, int DIMC, int GC, bool MASKED>
 __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
     using S = MmaShape<BITS, DIMC>;
     constexpr int CH = S::CH, KB = S::KB, NB = S::NB, VB = S::VB, KW = S::KW, VW = S::VW;
@@ -153,10 +155,9 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
     }
 
     if (lane == 0) {
-        for (int k = 0; k < NS; ++k) {
-            mbar_init(&bars[k], 33);      // group A: lane 0's expect-tx arrive + one cp.async arrive per lane
-            mbar_init(&bars[NS + k], 1);  // group B: lane 0's expect-tx arrive
-        }
+        // stage k: lane 0's expect-tx arrive + one cp.async arrive per lane; the
+        // V tile's bytes are posted on the same barrier
+        for (int k = 0; k < NS; ++k) mbar_init(&bars[k], 33);
         fence_mbar_init();
     }
     __syncwarp();
@@ -169,11 +170,10 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
     // arrivals then complete at once.  Other chunks (and calls without a mask,
     // where the many small bulk copies measured slower than the lanes' 16-byte
     // cp.async) take the staging of quant_kernel.cuh.
-    const bool bulk_a = (a.mbool != nullptr || a.mfloat != nullptr) && a.al_sb &&
-                        (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
+    const bool bulk_a = MASKED && a.al_sb && (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
     const unsigned char *cp_src = nullptr;   // this lane's run at token 0
     uint32_t cp_stride = 0, cp_bytes = 0, cp_dst = 0, tx_a = 0;
-    {
+    if constexpr (MASKED) {
         const size_t kv0 = static_cast<size_t>(kv) * N;
         const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
         if (lane == 0) {
@@ -202,7 +202,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
     }
     auto issue_a = [&](int c, int b) {
         const int t0 = c * CH;
-        if (bulk_a && t0 + CH <= N) {
+        if (MASKED && bulk_a && t0 + CH <= N) {
             unsigned char *st = smem + L.a0 + b * L.a_stage;
             if (lane == 0) mbar_arrive_expect_tx(&bars[b], tx_a);
             __syncwarp();
@@ -213,9 +213,20 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
             stg.issue_a(c, b);
         }
     };
-    int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
-    for (; a_issued < NS && a_issued < nc; ++a_issued) issue_a(c_begin + a_issued, a_issued % NS);
-    for (; b_issued < NS && b_issued < nc; ++b_issued) stg.issue_b(c_begin + b_issued, b_issued % NS);
+    // a whole chunk on one barrier: the V tile's bytes are posted (no arrival)
+    // before group A's arrivals, so the phase cannot complete without them
+    auto issue = [&](int c, int b) {
+        if (lane == 0) {
+            const int t0 = c * CH;
+            const uint32_t vbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
+            mbar_expect_tx(&bars[b], vbytes);
+            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, vbytes,
+                      &bars[b]);
+        }
+        issue_a(c, b);
+    };
+    int issued = 0, done = 0;
+    for (; issued < NS && issued < nc; ++issued) issue(c_begin + issued, issued % NS);
 
     // ---- queries: lane holds element lane + 32 k of each row (loaded above);
     // per-row power-of-two scale 2^e (max |q| 2^e in [2^14, 2^15)), group sums
@@ -253,10 +264,11 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
     }
     __syncwarp();
     // A-fragment of accumulator set acc, K-block v for this lane: a0a1 (row gq,
-    // slots 0, 1), a2a3 (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3)
-#pragma unroll
+    // slots 0, 1), a2a3 (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3).
+    // Setup code runs once per CTA: kept rolled (little code to fetch cold).
+#pragma unroll 1
     for (int acc = 0; acc < NACC; ++acc)
-#pragma unroll
+#pragma unroll 1
         for (int v = 0; v < KB; ++v) {
             uint32_t reg[4];
 #pragma unroll
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
         const int c = c_begin + i, b = i % NS;
         const uint32_t par = static_cast<uint32_t>(i / NS) & 1u;
         if (!wait_warp(&bars[b], par, i == 0 ? a.first_wait_polls : kQuantWaitPolls)) { ok = false; break; }
-        ++a_done;
+        ++done;
         __syncwarp();
         const unsigned char *st = smem + L.a0 + b * L.a_stage;
         const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
@@ -330,7 +342,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
                 const int tk = 8 * nb + 2 * tq + e;
                 const int t = t0 + tk;
                 bool g = r_l < nrow && t >= a.t_lo && t < N;
-                if (g && a.mbool != nullptr) g = sMb[r_l * CH + tk] != 0u;
+                if (MASKED && g && a.mbool != nullptr) g = sMb[r_l * CH + tk] != 0u;
                 if (g && a.tree_ql > 0 && t >= tree_lo) g = (tree_bits >> (t - tree_lo)) & 1u;
                 live[nb][e] = g;
                 any |= g;
@@ -456,7 +468,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
                     x += __shfl_xor_sync(0xffffffffu, x, 16);
                     if (live[nb][e]) {
                         float v = fmaf(alpha_l, x, sKbias[tk * REP + r_l]);
-                        if (a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l * CH + tk]), v);
+                        if (MASKED && a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l * CH + tk]), v);
                         lg[nb][e] = v;
                     }
                 }
@@ -509,11 +521,6 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
                 pf[nb >> 1][nb & 1] = f;
             }
         }
-        __syncwarp();
-        if (a_issued < nc) { issue_a(c_begin + a_issued, a_issued % NS); ++a_issued; }   // stage b is free
-        if (!wait_warp(&bars[NS + b], par)) { ok = false; break; }   // group B of chunk c
-        ++b_done;
-        __syncwarp();
 
         // ---- values: O^T += V^T P^T per 16-token block
         if (chunk_live) {
@@ -583,14 +590,12 @@ __global__ void __launch_bounds__(32, 12) quant_mma_kernel(const QuantArgs a) {
             }
         }
         __syncwarp();
-        if (b_issued < nc) { stg.issue_b(c_begin + b_issued, b_issued % NS); ++b_issued; }
+        if (issued < nc) { issue(c_begin + issued, issued % NS); ++issued; }   // stage b is free
     }
     pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
     if (!ok) {
         if (lane == 0 && a.err != nullptr) atomicOr(a.err, 1);
-        for (; a_done < a_issued; ++a_done) wait_warp(&bars[a_done % NS], static_cast<uint32_t>(a_done / NS) & 1u);
-        for (; b_done < b_issued; ++b_done)
-            wait_warp(&bars[NS + b_done % NS], static_cast<uint32_t>(b_done / NS) & 1u);
+        for (; done < issued; ++done) wait_warp(&bars[done % NS], static_cast<uint32_t>(done / NS) & 1u);
         return;
     }
 
@@ -656,9 +661,9 @@ inline size_t mma_smem_bytes() {
     return static_cast<size_t>(qmma_layout(S::WPTC, DIMC / GC, S::CH, DIMC, qmma_nacc(DIMC / GC), kQmmaStages).total);
 }
 
-template <int BITS, typename T, int DIMC, int GC>
-cudaError_t mma_launch_one(const QuantArgs &a, cudaStream_t s) {
-    auto kern = quant_mma_kernel<BITS, T, DIMC, GC>;
+template <int BITS, typename T, int DIMC, int GC, bool MASKED>
+cudaError_t mma_launch_masked(const QuantArgs &a, cudaStream_t s) {
+    auto kern = quant_mma_kernel<BITS, T, DIMC, GC, MASKED>;
     static unsigned long long done = 0;
     cudaError_t e = set_smem_limit_once(kern, kQuantMaxSmem, &done);
     if (e != cudaSuccess) return e;
@@ -668,14 +673,28 @@ cudaError_t mma_launch_one(const QuantArgs &a, cudaStream_t s) {
 }
 
 template <int BITS, typename T, int DIMC, int GC>
-int mma_occupancy_one() {
-    auto kern = quant_mma_kernel<BITS, T, DIMC, GC>;
+cudaError_t mma_launch_one(const QuantArgs &a, cudaStream_t s) {
+    if (a.mbool != nullptr || a.mfloat != nullptr) return mma_launch_masked<BITS, T, DIMC, GC, true>(a, s);
+    return mma_launch_masked<BITS, T, DIMC, GC, false>(a, s);
+}
+
+template <int BITS, typename T, int DIMC, int GC, bool MASKED>
+int mma_occupancy_masked() {
+    auto kern = quant_mma_kernel<BITS, T, DIMC, GC, MASKED>;
     static unsigned long long done = 0;
     if (set_smem_limit_once(kern, kQuantMaxSmem, &done) != cudaSuccess) return 0;
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 32, mma_smem_bytes<BITS, DIMC, GC>()) != cudaSuccess)
         return 0;
     return n;
+}
+
+// Resident CTAs per SM: the smaller of the two instances (the split count
+// does not depend on which masks a call passes).
+template <int BITS, typename T, int DIMC, int GC>
+int mma_occupancy_one() {
+    const int u = mma_occupancy_masked<BITS, T, DIMC, GC, false>(), m = mma_occupancy_masked<BITS, T, DIMC, GC, true>();
+    return u < m ? u : m;
 }
 
 // Instances: head dimension 64, 128 or 256 exactly, group size 32 or 64
