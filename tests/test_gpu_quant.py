@@ -50,6 +50,10 @@ QCASES = [
     dict(dim=128, G=32, bits=8, N=333, window=200, fmask="alibi", bfrac=0.1, sinks=1, dtype="bf16"),
     dict(nQ=6, nKV=2, N=64, nwg=1),                # 3 rows per KV row
     dict(N=31, window=500),
+    # both masks with 16-byte aligned rows (tokens a multiple of 8): the bulk-copy staging of masked chunks
+    dict(dim=256, bits=8, N=512, fmask="alibi", bfrac=0.1, dtype="bf16", sinks=0),
+    dict(dim=128, bits=4, N=256, window=100, fmask="alibi", bfrac=0.2, nwg=2),
+    dict(dim=64, G=32, bits=8, N=192, bfrac=0.3, nwg=1),
 ]
 
 

@@ -180,6 +180,7 @@ struct QuantStager {
     unsigned char *smem;
     uint64_t *bars;   // A stages 0 .. ns-1, then B stages 0 .. ns-1
     int WPT, NG, kv, q0, nrow, lane, ns;
+    bool with_k;      // issue_a also copies the K tile (else another warp does)
 
     __device__ __forceinline__ void issue_a(int c, int b) const {
         const int N = a.N;
@@ -187,7 +188,7 @@ struct QuantStager {
         const int t0 = c * CH, tval = min(CH, N - t0);
         const bool full = tval == CH;
         const size_t tok0 = static_cast<size_t>(kv) * N + t0;
-        if (lane == 0) {
+        if (lane == 0 && with_k) {
             const uint32_t kbytes = static_cast<uint32_t>(tval * WPT * 4);
             mbar_arrive_expect_tx(&bars[b], kbytes);
             bulk_load(st + L.k, a.kp + tok0 * WPT, kbytes, &bars[b]);
@@ -316,7 +317,7 @@ __global__ void __launch_bounds__(32, (DIMC >= 512 ? 8 : 12)) quant_kernel(const
     }
     __syncwarp();
 
-    const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, 2};
+    const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, 2, true};
     auto issue_a = [&](int c, int b) { stg.issue_a(c, b); };
     auto issue_b = [&](int c, int b) { stg.issue_b(c, b); };
     int a_issued = 0, b_issued = 0, a_done = 0, b_done = 0;
