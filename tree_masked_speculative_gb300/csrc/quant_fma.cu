@@ -131,9 +131,14 @@ cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s) {
 
 int quant_mma_ctas_per_sm(int bits, int dim, int ng) {
     if (ng <= 0 || !quant_mma_shape_ok(dim, dim / ng)) return 0;
-    if (bits == 4) return quant_mma_ctas_per_sm_b4(dim, ng);
-    if (bits == 8) return quant_mma_ctas_per_sm_b8(dim, ng);
-    return 0;
+    int n = 0;
+    if (bits == 4) n = quant_mma_ctas_per_sm_b4(dim, ng);
+    if (bits == 8) n = quant_mma_ctas_per_sm_b8(dim, ng);
+    // the two-warp form (more than 16 packed words per token) measured fastest
+    // with its splits sized for 6 CTAs per SM (8-bit workload: 47.0 us at 6,
+    // 48.7 at 7)
+    if (dim * bits / 32 > 16 && n > kQmmaTwoWarpCtasPerSm) n = kQmmaTwoWarpCtasPerSm;
+    return n;
 }
 
 int quant_tc_ctas_per_sm(int bits, int rp, size_t smem) {

@@ -97,7 +97,7 @@ __host__ __device__ inline QmmaLayout qmma_layout(int wpt, int ng, int ch, int d
     int o = M.st.v0 + ns * M.st.v_stage;
     M.qa = quant_take(&o, nacc * (dimc / 16) * 32 * 16);   // Q A-fragments [acc][kblock][lane] uint4
     M.qs = quant_take(&o, 4 * ng * 4 + 16);                // [row][group] scale*log2e * sum q, then 2^e per row
-    M.qf = quant_take(&o, 4 * dimc * 4);                   // q rows in f32 (setup)
+    M.qf = quant_take(&o, 4 * dimc * 2);                   // q rows scaled by 2^e, f16 (setup)
     M.ksf = quant_take(&o, ch * ng * 4);                   // [token][group] K scale, f32
     M.kbias = quant_take(&o, ch * 4 * 4);                  // [token][row] score bias term
     M.vsb = quant_take(&o, ng * (ch / 2) * 8);             // [group][token pair] {s, s}, {b, b} f16
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
     const QuantLayout &L = M.st;
     uint4 *sQA = reinterpret_cast<uint4 *>(smem + M.qa);
     float *sQS = reinterpret_cast<float *>(smem + M.qs);
-    float *sQF = reinterpret_cast<float *>(smem + M.qf);
+    __half *sQF = reinterpret_cast<__half *>(smem + M.qf);   // q * 2^e, exact in f16
     float *sKsf = reinterpret_cast<float *>(smem + M.ksf);
     float *sKbias = reinterpret_cast<float *>(smem + M.kbias);
     uint2 *sVSB = reinterpret_cast<uint2 *>(smem + M.vsb);
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
         const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
         if (lane == 0) sE2[r] = e2;
 #pragma unroll
-        for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = qv[k] * e2;
+        for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = __float2half_rn(qv[k] * e2);
 #pragma unroll
         for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
             float x = 0.0f;
@@ -302,7 +302,7 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
                     const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
                     const int g = d / GC;
                     const bool here = g / 4 == acc && (m >> 2) == g % 4;
-                    val[e] = here ? sQF[(m & 3) * DIMC + d] * f : 0.0f;
+                    val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
                 }
                 reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
             }
@@ -706,7 +706,7 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
     const QuantLayout &L = M.st;
     uint4 *sQA = reinterpret_cast<uint4 *>(smem + M.qa);
     float *sQS = reinterpret_cast<float *>(smem + M.qs);
-    float *sQF = reinterpret_cast<float *>(smem + M.qf);
+    __half *sQF = reinterpret_cast<__half *>(smem + M.qf);   // q * 2^e, exact in f16
     float *sKsf = reinterpret_cast<float *>(smem + M.ksf);
     float *sKbias = reinterpret_cast<float *>(smem + M.kbias);
     uint2 *sVSB = reinterpret_cast<uint2 *>(smem + M.vsb);
@@ -1000,7 +1000,7 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
             const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
             if (lane == 0) sE2[r] = e2;
 #pragma unroll
-            for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = qv[k] * e2;
+            for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = __float2half_rn(qv[k] * e2);
 #pragma unroll
             for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
                 float x = 0.0f;
@@ -1031,7 +1031,7 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
                         const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
                         const int g = d / GC;
                         const bool here = g / 4 == acc && (m >> 2) == g % 4;
-                        val[e] = here ? sQF[(m & 3) * DIMC + d] * f : 0.0f;
+                        val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
                     }
                     reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
                 }

@@ -396,6 +396,8 @@ int quant_tc_ctas_per_sm_b8(int rp, size_t smem);
 // Warp-MMA quantized-KV kernel (mma.sync, one warp per CTA, 4 query rows):
 // head dimension 64, 128 or 256 exactly and group size 32 or 64.
 bool quant_mma_shape_ok(int dim, int group_size);
+// CTAs per SM the two-warp form's split count is sized for (at most).
+constexpr int kQmmaTwoWarpCtasPerSm = 6;
 cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_mma_b4(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_mma_b8(const QuantArgs &a, cudaStream_t s);
