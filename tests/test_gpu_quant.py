@@ -54,6 +54,10 @@ QCASES = [
     dict(dim=256, bits=8, N=512, fmask="alibi", bfrac=0.1, dtype="bf16", sinks=0),
     dict(dim=128, bits=4, N=256, window=100, fmask="alibi", bfrac=0.2, nwg=2),
     dict(dim=64, G=32, bits=8, N=192, bfrac=0.3, nwg=1),
+    # eight scale groups per token (two accumulator sets of the warp-MMA scores)
+    dict(dim=256, G=32, bits=4, N=300, nwg=3),
+    dict(dim=256, G=32, bits=8, N=256, fmask="alibi", bfrac=0.1, dtype="bf16"),
+    dict(dim=128, G=32, bits=8, nQ=12, nKV=2, N=320, window=150),   # 6 rows per KV row: a partial row group
 ]
 
 
