@@ -121,41 +121,32 @@ struct QmmaForm {
 // Accumulator sets of the score MMA: four scale groups per set.
 __host__ __device__ inline int qmma_nacc(int ng) { return (ng + 3) / 4; }
 
-// One-warp form (shapes of up to 16 packed words per token, where it measured
-// faster than the two-warp form): the same scores, softmax and values, one warp
-// doing every step of a chunk in turn and issuing every copy itself.
+// The phases of a warp-MMA chunk, shared by the one-warp and the two-warp
+// forms (each a warp's view: lane = quad gq, position tq).  MASKED: the call
+// passes a bool or a float mask (instances without one carry no mask code and
+// stage every chunk through the lanes' cp.async).
 template <int BITS, typename T, int DIMC, int GC, bool MASKED>
-__global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
+struct QmmaPhases {
     using S = MmaShape<BITS, DIMC>;
-    constexpr int CH = S::CH, KB = S::KB, NB = S::NB, VB = S::VB, KW = S::KW, VW = S::VW;
-    constexpr int NG = DIMC / GC;
-    constexpr int NACC = (NG + 3) / 4;
-    constexpr int WPT = S::WPTC;
-    constexpr int NS = 2;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int lane = threadIdx.x, gq = lane >> 2, tq = lane & 3;
-    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
-    const int q0 = kv * a.rep + rg * REP;
-    const int nrow = min(REP, a.rep - rg * REP);
-    const int N = a.N;
-    const QmmaLayout M = qmma_layout(WPT, NG, CH, DIMC, NACC, NS, false);
-    const QuantLayout &L = M.st;
-    uint4 *sQA = reinterpret_cast<uint4 *>(smem + M.qa);
-    float *sQS = reinterpret_cast<float *>(smem + M.qs);
-    __half *sQF = reinterpret_cast<__half *>(smem + M.qf);   // q * 2^e, exact in f16
-    float *sKsf = reinterpret_cast<float *>(smem + M.ksf);
-    float *sKbias = reinterpret_cast<float *>(smem + M.kbias);
-    uint2 *sVSB = reinterpret_cast<uint2 *>(smem + M.vsb);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M.bars);
+    static constexpr int CH = S::CH, KB = S::KB, NB = S::NB, VB = S::VB, KW = S::KW, VW = S::VW;
+    static constexpr int NG = DIMC / GC;
+    static constexpr int NACC = (NG + 3) / 4;
+    static constexpr int WPT = S::WPTC;
+    static constexpr int QPL = DIMC / 32;   // query elements per lane per row
 
-    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
-    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
-    const int nc = c_end - c_begin;
+    const QuantArgs &a;
+    const QuantLayout &L;
+    uint4 *sQA;
+    float *sQS;
+    __half *sQF;
+    float *sKsf, *sKbias;
+    uint2 *sVSB;
+    int lane, gq, tq, q0, nrow, N;
 
-    // the 4 query rows, element lane + 32 k per lane, loaded before anything waits
-    constexpr int QPL = DIMC / 32;
-    uint16_t qraw[REP][QPL];
-    {
+    __device__ __forceinline__ int r_l() const { return gq & 3; }   // query row of the score fragments
+
+    // The 4 query rows, element lane + 32 k per lane (issued before anything waits).
+    __device__ __forceinline__ void load_q(uint16_t (&qraw)[REP][QPL]) const {
         const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.queries);
 #pragma unroll
         for (int r = 0; r < REP; ++r)
@@ -165,195 +156,90 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
                                       : static_cast<uint16_t>(0);
     }
 
-    const int r_l = gq & 3;   // query row of the lane's score fragments
-    const int tree_lo = N - a.tree_ql;
-    uint32_t tree_bits = 0u;
-    if (a.tree_ql > 0) {
-        const uint32_t mine =
-            quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
-        tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
+    // Ancestor bitset of the lane's row's node for a parent-array draft tree (0 without one).
+    __device__ __forceinline__ uint32_t tree_bits() const {
+        if (a.tree_ql <= 0) return 0u;
+        const uint32_t mine = quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
+        return __shfl_sync(0xffffffffu, mine, (q0 + r_l()) % a.tree_ql);
     }
 
-    if (lane == 0) {
-        // stage k: lane 0's expect-tx arrive + one cp.async arrive per lane; the
-        // V tile's bytes are posted on the same barrier
-        for (int k = 0; k < NS; ++k) mbar_init(&bars[k], 33);
-        fence_mbar_init();
-    }
-    __syncwarp();
-    const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, NS, true};
-    // Group A of a full chunk whose runs are 16-byte aligned, in a call with a
-    // mask: one bulk copy per run, each issued by a lane of its own in the same
-    // instruction - lane 0 the K words, lanes 1-4 the K / V scale and bias
-    // runs, then one lane per bool-mask and float-mask row - after lane 0 has
-    // posted the byte count on the group-A barrier; the lanes' cp.async
-    // arrivals then complete at once.  Other chunks (and calls without a mask,
-    // where the many small bulk copies measured slower than the lanes' 16-byte
-    // cp.async) take the staging of quant_kernel.cuh.
-    const bool bulk_a = MASKED && a.al_sb && (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
-    const unsigned char *cp_src = nullptr;   // this lane's run at token 0
-    uint32_t cp_stride = 0, cp_bytes = 0, cp_dst = 0, tx_a = 0;
-    if constexpr (MASKED) {
-        const size_t kv0 = static_cast<size_t>(kv) * N;
-        const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
-        if (lane == 0) {
-            cp_src = reinterpret_cast<const unsigned char *>(a.kp + kv0 * WPT);
-            cp_stride = WPT * 4;
-            cp_dst = L.k;
-        } else if (lane <= 4) {
-            const void *base = lane == 1 ? a.ks : lane == 2 ? a.kb : lane == 3 ? a.vs : a.vb;
-            cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(base) + kv0 * NG);
-            cp_stride = NG * 2;
-            cp_dst = lane == 1 ? L.ks : lane == 2 ? L.kb : lane == 3 ? L.vs : L.vb;
-        } else if (lane < 5 + nb_rows) {
-            const int r = lane - 5;
-            cp_src = reinterpret_cast<const unsigned char *>(a.mbool + static_cast<size_t>(q0 + r) * N);
-            cp_stride = 4;
-            cp_dst = L.mb + r * CH * 4;
-        } else if (lane < 5 + nb_rows + nf_rows) {
-            const int r = lane - 5 - nb_rows;
-            cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(a.mfloat) +
-                                                             static_cast<size_t>(q0 + r) * N);
-            cp_stride = 2;
-            cp_dst = L.mf + r * CH * 2;
-        }
-        cp_bytes = cp_stride * CH;
-        tx_a = CH * (WPT * 4 + 4 * NG * 2 + nb_rows * 4 + nf_rows * 2);
-    }
-    auto issue_a = [&](int c, int b) {
-        const int t0 = c * CH;
-        if (MASKED && bulk_a && t0 + CH <= N) {
-            unsigned char *st = smem + L.a0 + b * L.a_stage;
-            if (lane == 0) mbar_arrive_expect_tx(&bars[b], tx_a);
-            __syncwarp();
-            if (cp_src != nullptr)
-                bulk_load(st + cp_dst, cp_src + static_cast<size_t>(t0) * cp_stride, cp_bytes, &bars[b]);
-            cp_arrive_noinc(&bars[b]);
-        } else {
-            stg.issue_a(c, b);
-        }
-    };
-    // a whole chunk on one barrier: the V tile's bytes are posted (no arrival)
-    // before group A's arrivals, so the phase cannot complete without them
-    auto issue = [&](int c, int b) {
-        if (lane == 0) {
-            const int t0 = c * CH;
-            const uint32_t vbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
-            mbar_expect_tx(&bars[b], vbytes);
-            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, vbytes,
-                      &bars[b]);
-        }
-        issue_a(c, b);
-    };
-    int issued = 0, done = 0;
-    for (; issued < NS && issued < nc; ++issued) issue(c_begin + issued, issued % NS);
-
-    // ---- queries: lane holds element lane + 32 k of each row (loaded above);
-    // per-row power-of-two scale 2^e (max |q| 2^e in [2^14, 2^15)), group sums
-    // (scale * log2(e) * sum_{d in g} q_d), the scaled rows in shared memory
-    // and from them the lane's score A-fragments
-    const float qscale = a.scale * kLog2e;
-    float *sE2 = sQS + REP * NG;   // 2^e per row
+    // Per-row power-of-two scale 2^e (max |q| 2^e in [2^14, 2^15)), group sums
+    // (scale * log2(e) * sum_{d in g} q_d), the scaled rows in shared memory and
+    // from them the lane's score A-fragments: a0a1 (row gq, slots 0, 1), a2a3
+    // (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3) of accumulator set
+    // acc and K-block v.  Returns the score scale of the lane's row,
+    // scale * log2(e) * 2^24 (subnormal codes) / 2^e.
+    __device__ __forceinline__ float setup_scores(const uint16_t (&qraw)[REP][QPL]) const {
+        const float qscale = a.scale * kLog2e;
+        float *sE2 = sQS + REP * NG;   // 2^e per row
 #pragma unroll
-    for (int r = 0; r < REP; ++r) {
-        float qv[QPL];
-        float mx = 0.0f;
+        for (int r = 0; r < REP; ++r) {
+            float qv[QPL];
+            float mx = 0.0f;
 #pragma unroll
-        for (int k = 0; k < QPL; ++k) {
-            qv[k] = t2f<T>(qraw[r][k]);
-            mx = fmaxf(mx, fabsf(qv[k]));
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-        int e = 0;
-        if (mx > 0.0f) e = 14 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127);
-        const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
-        if (lane == 0) sE2[r] = e2;
-#pragma unroll
-        for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = __float2half_rn(qv[k] * e2);
-#pragma unroll
-        for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
-            float x = 0.0f;
-#pragma unroll
-            for (int k = 0; k < QPL; ++k)
-                if ((32 * k) / GC == g) x += qv[k];
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-            if (lane == 0) sQS[r * NG + g] = qscale * x;
-        }
-    }
-    __syncwarp();
-    // A-fragment of accumulator set acc, K-block v for this lane: a0a1 (row gq,
-    // slots 0, 1), a2a3 (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3).
-    // Setup code runs once per CTA: kept rolled (little code to fetch cold).
-#pragma unroll 1
-    for (int acc = 0; acc < NACC; ++acc)
-#pragma unroll 1
-        for (int v = 0; v < KB; ++v) {
-            uint32_t reg[4];
-#pragma unroll
-            for (int h = 0; h < 4; ++h) {
-                const int m = gq + ((h & 1) ? 8 : 0);
-                float val[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int j = (h >> 1) * 2 + e;
-                    float f;
-                    const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
-                    const int g = d / GC;
-                    const bool here = g / 4 == acc && (m >> 2) == g % 4;
-                    val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
-                }
-                reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
+            for (int k = 0; k < QPL; ++k) {
+                qv[k] = t2f<T>(qraw[r][k]);
+                mx = fmaxf(mx, fabsf(qv[k]));
             }
-            sQA[(acc * KB + v) * 32 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+#pragma unroll
+            for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            int e = 0;
+            if (mx > 0.0f) e = 14 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127);
+            const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
+            if (lane == 0) sE2[r] = e2;
+#pragma unroll
+            for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = __float2half_rn(qv[k] * e2);
+#pragma unroll
+            for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
+                float x = 0.0f;
+#pragma unroll
+                for (int k = 0; k < QPL; ++k)
+                    if ((32 * k) / GC == g) x += qv[k];
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+                if (lane == 0) sQS[r * NG + g] = qscale * x;
+            }
         }
-    // group sums of the row of this lane's score-bias entries (row = lane % 4)
-    float qs_l[NG];
-#pragma unroll
-    for (int g = 0; g < NG; ++g) qs_l[g] = sQS[(lane & 3) * NG + g];
-    // score scale of row r: scale * log2(e) * 2^24 (subnormal codes) / 2^e
-    const float alpha_l = qscale * 16777216.0f / sE2[r_l];
-    // the lane's scale groups in the score fragments: c0/c1 rows gq, c2/c3 rows gq + 8
-    int grp_lo[NACC], grp_hi[NACC];
-#pragma unroll
-    for (int acc = 0; acc < NACC; ++acc) {
-        grp_lo[acc] = 4 * acc + (gq >> 2);
-        grp_hi[acc] = 4 * acc + 2 + (gq >> 2);
-    }
-    // the lane's V words: gq * VW .. + VW of each token; their scale groups
-    int vgrp[VW];
-#pragma unroll
-    for (int u = 0; u < VW; ++u) vgrp[u] = ((gq * VW + u) * (32 / BITS)) / GC;
-    __syncwarp();
-
-    float Mrow = -INFINITY, Ssum = 0.0f;   // online softmax of row r_l (log2 units)
-    float O[KB][4];
-#pragma unroll
-    for (int mb = 0; mb < KB; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) O[mb][e] = 0.0f;
-
-    bool ok = true;
-    for (int i = 0; i < nc; ++i) {
-        const int c = c_begin + i, b = i % NS;
-        const uint32_t par = static_cast<uint32_t>(i / NS) & 1u;
-        if (!wait_warp(&bars[b], par, i == 0 ? a.first_wait_polls : kQuantWaitPolls)) { ok = false; break; }
-        ++done;
         __syncwarp();
-        const unsigned char *st = smem + L.a0 + b * L.a_stage;
-        const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
-        const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + L.ks);
-        const uint16_t *sKb = reinterpret_cast<const uint16_t *>(st + L.kb);
-        const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + L.vs);
-        const uint16_t *sVb = reinterpret_cast<const uint16_t *>(st + L.vb);
-        const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
-        const uint16_t *sMf = reinterpret_cast<const uint16_t *>(st + L.mf);
-        const uint32_t *sV = reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage);
-        const int t0 = c * CH;
+        // setup code runs once per CTA: kept rolled (little code to fetch cold)
+#pragma unroll 1
+        for (int acc = 0; acc < NACC; ++acc)
+#pragma unroll 1
+            for (int v = 0; v < KB; ++v) {
+                uint32_t reg[4];
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const int m = gq + ((h & 1) ? 8 : 0);
+                    float val[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int j = (h >> 1) * 2 + e;
+                        float f;
+                        const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
+                        const int g = d / GC;
+                        const bool here = g / 4 == acc && (m >> 2) == g % 4;
+                        val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
+                    }
+                    reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
+                }
+                sQA[(acc * KB + v) * 32 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
+            }
+        __syncwarp();
+        return qscale * 16777216.0f / sE2[r_l()];
+    }
 
-        // gates of the lane's (row r_l, key) score slots: key 8 nb + 2 tq + e
-        bool live[NB][2];
+    // Group sums of the row of this lane's score-bias entries (row = lane % 4).
+    __device__ __forceinline__ void bias_sums(float (&qs_l)[NG]) const {
+#pragma unroll
+        for (int g = 0; g < NG; ++g) qs_l[g] = sQS[(lane & 3) * NG + g];
+    }
+
+    // Gates of the lane's (row r_l, key) score slots, key 8 nb + 2 tq + e of the
+    // chunk at token t0; returns whether any slot of the warp is live.
+    __device__ __forceinline__ bool gates(const unsigned char *st, int t0, uint32_t tree_bits,
+                                          bool (&live)[NB][2]) const {
+        const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
+        const int tree_lo = N - a.tree_ql;
         bool any = false;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb)
@@ -361,280 +247,297 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
             for (int e = 0; e < 2; ++e) {
                 const int tk = 8 * nb + 2 * tq + e;
                 const int t = t0 + tk;
-                bool g = r_l < nrow && t >= a.t_lo && t < N;
-                if (MASKED && g && a.mbool != nullptr) g = sMb[r_l * CH + tk] != 0u;
+                bool g = r_l() < nrow && t >= a.t_lo && t < N;
+                if (MASKED && g && a.mbool != nullptr) g = sMb[r_l() * CH + tk] != 0u;
                 if (g && a.tree_ql > 0 && t >= tree_lo) g = (tree_bits >> (t - tree_lo)) & 1u;
                 live[nb][e] = g;
                 any |= g;
             }
-        const bool chunk_live = __any_sync(0xffffffffu, any);
+        return __any_sync(0xffffffffu, any);
+    }
 
-        float lg[NB][2];
+    // Per-chunk tables, each lane filling fixed entries: K scales in f32 [t][g],
+    // the score bias per (token, row) [t][r] (row = lane % 4), and the V scale /
+    // bias pairs of token pairs (2p, 2p + 1) in f16 [g][p].  Each is loaded
+    // (k_load, v_load) before any is stored (k_store, v_store), so the loads
+    // of a warp doing both are all in flight at once.
+    static constexpr int NKS = (CH * NG + 31) / 32, NKB = CH * REP / 32, NVP = (NG * (CH / 2) + 31) / 32;
+    struct KRaw {
+        uint16_t ks[NKS], kb[NKB][NG];
+    };
+    struct VRaw {
+        uint16_t vs[NVP][2], vb[NVP][2];
+    };
+    __device__ __forceinline__ void k_load(const unsigned char *st, KRaw &r) const {
+        const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + L.ks);
+        const uint16_t *sKb = reinterpret_cast<const uint16_t *>(st + L.kb);
 #pragma unroll
-        for (int nb = 0; nb < NB; ++nb) lg[nb][0] = lg[nb][1] = -INFINITY;
-        if (chunk_live) {
-            // per-chunk tables, each lane filling fixed entries with every load
-            // issued before the first store: K scales in f32 [t][g], the score
-            // bias per (token, row) [t][r] (row = lane % 4), and the V scale /
-            // bias pairs of token pairs (2p, 2p + 1) in f16 [g][p]
-            {
-                constexpr int NKS = (CH * NG + 31) / 32, NKB = CH * REP / 32, NVP = (NG * (CH / 2) + 31) / 32;
-                uint16_t ksr[NKS], kbr[NKB][NG], vsr[NVP][2], vbr[NVP][2];
+        for (int j = 0; j < NKS; ++j) {
+            const int idx = lane + 32 * j;
+            r.ks[j] = idx < CH * NG ? sKs[idx] : static_cast<uint16_t>(0);
+        }
 #pragma unroll
-                for (int j = 0; j < NKS; ++j) {
-                    const int idx = lane + 32 * j;
-                    ksr[j] = idx < CH * NG ? sKs[idx] : static_cast<uint16_t>(0);
-                }
+        for (int j = 0; j < NKB; ++j) {
+            const int t = (lane + 32 * j) / REP;
 #pragma unroll
-                for (int j = 0; j < NKB; ++j) {
-                    const int t = (lane + 32 * j) / REP;
+            for (int g = 0; g < NG; ++g) r.kb[j][g] = sKb[t * NG + g];
+        }
+    }
+    __device__ __forceinline__ void k_store(const KRaw &r, const float (&qs_l)[NG]) const {
 #pragma unroll
-                    for (int g = 0; g < NG; ++g) kbr[j][g] = sKb[t * NG + g];
-                }
+        for (int j = 0; j < NKS; ++j)
+            if (lane + 32 * j < CH * NG) sKsf[lane + 32 * j] = t2f<T>(r.ks[j]);
 #pragma unroll
-                for (int j = 0; j < NVP; ++j) {
-                    const int idx = lane + 32 * j;
-                    const int g = idx / (CH / 2), p = idx % (CH / 2);
-                    const bool in = idx < NG * (CH / 2);
+        for (int j = 0; j < NKB; ++j) {
+            float x = 0.0f;
 #pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        vsr[j][e] = in ? sVs[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
-                        vbr[j][e] = in ? sVb[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
-                    }
-                }
+            for (int g = 0; g < NG; ++g) x = fmaf(t2f<T>(r.kb[j][g]), qs_l[g], x);
+            sKbias[lane + 32 * j] = x;
+        }
+    }
+    __device__ __forceinline__ void v_load(const unsigned char *st, VRaw &r) const {
+        const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + L.vs);
+        const uint16_t *sVb = reinterpret_cast<const uint16_t *>(st + L.vb);
 #pragma unroll
-                for (int j = 0; j < NKS; ++j)
-                    if (lane + 32 * j < CH * NG) sKsf[lane + 32 * j] = t2f<T>(ksr[j]);
+        for (int j = 0; j < NVP; ++j) {
+            const int idx = lane + 32 * j;
+            const int g = idx / (CH / 2), p = idx % (CH / 2);
+            const bool in = idx < NG * (CH / 2);
 #pragma unroll
-                for (int j = 0; j < NKB; ++j) {
-                    float x = 0.0f;
-#pragma unroll
-                    for (int g = 0; g < NG; ++g) x = fmaf(t2f<T>(kbr[j][g]), qs_l[g], x);
-                    sKbias[lane + 32 * j] = x;
-                }
-#pragma unroll
-                for (int j = 0; j < NVP; ++j)
-                    if (lane + 32 * j < NG * (CH / 2)) {
-                        const __half2 sp = __floats2half2_rn(t2f<T>(vsr[j][0]), t2f<T>(vsr[j][1]));
-                        const __half2 bp = __floats2half2_rn(t2f<T>(vbr[j][0]), t2f<T>(vbr[j][1]));
-                        sVSB[lane + 32 * j] = make_uint2(h2_bits(sp), h2_bits(bp));
-                    }
+            for (int e = 0; e < 2; ++e) {
+                r.vs[j][e] = in ? sVs[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
+                r.vb[j][e] = in ? sVb[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
             }
-            __syncwarp();
+        }
+    }
+    __device__ __forceinline__ void v_store(const VRaw &r) const {
+#pragma unroll
+        for (int j = 0; j < NVP; ++j)
+            if (lane + 32 * j < NG * (CH / 2)) {
+                const __half2 sp = __floats2half2_rn(t2f<T>(r.vs[j][0]), t2f<T>(r.vs[j][1]));
+                const __half2 bp = __floats2half2_rn(t2f<T>(r.vb[j][0]), t2f<T>(r.vb[j][1]));
+                sVSB[lane + 32 * j] = make_uint2(h2_bits(sp), h2_bits(bp));
+            }
+    }
 
-            // ---- scores: the lane's quarter of key 8 nb + gq, all K-blocks
-            uint32_t kw[NB][KW];
+    // Scores of the chunk in stage st: the lane's quarter of key 8 nb + gq, all
+    // K-blocks, S = Q K^T per accumulator set; then the scale groups apart and
+    // the two halves of the quad pair (lanes gq and gq ^ 4 hold the other
+    // groups of the same row); live slots get scale * sum + bias (+ float mask)
+    // in log2 units.
+    __device__ __forceinline__ void scores(const unsigned char *st, float alpha_l, const bool (&live)[NB][2],
+                                           float (&lg)[NB][2]) const {
+        const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
+        const uint16_t *sMf = reinterpret_cast<const uint16_t *>(st + L.mf);
+        uint32_t kw[NB][KW];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            const uint32_t *src = sK + (8 * nb + gq) * WPT + tq * KW;
+            if constexpr (KW % 4 == 0) {
+#pragma unroll
+                for (int u = 0; u < KW; u += 4) {
+                    const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
+                    kw[nb][u] = x.x; kw[nb][u + 1] = x.y; kw[nb][u + 2] = x.z; kw[nb][u + 3] = x.w;
+                }
+            } else if constexpr (KW == 2) {
+                const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                kw[nb][0] = x.x; kw[nb][1] = x.y;
+            } else {
+#pragma unroll
+                for (int u = 0; u < KW; ++u) kw[nb][u] = src[u];
+            }
+        }
+        float sacc[NB][NACC][4];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+            for (int acc = 0; acc < NACC; ++acc)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) sacc[nb][acc][e] = 0.0f;
+#pragma unroll
+        for (int v = 0; v < KB; ++v) {
+            uint4 af[NACC];
+#pragma unroll
+            for (int acc = 0; acc < NACC; ++acc) af[acc] = sQA[(acc * KB + v) * 32 + lane];
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) {
-                const uint32_t *src = sK + (8 * nb + gq) * WPT + tq * KW;
-                if constexpr (KW % 4 == 0) {
-#pragma unroll
-                    for (int u = 0; u < KW; u += 4) {
-                        const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
-                        kw[nb][u] = x.x; kw[nb][u + 1] = x.y; kw[nb][u + 2] = x.z; kw[nb][u + 3] = x.w;
-                    }
-                } else if constexpr (KW == 2) {
-                    const uint2 x = *reinterpret_cast<const uint2 *>(src);
-                    kw[nb][0] = x.x; kw[nb][1] = x.y;
+                uint32_t b0, b1;
+                if constexpr (BITS == 4) {
+                    // bytes (2, 3) or (0, 1) of the word into the two halves
+                    const uint32_t w = kw[nb][v / 2];
+                    const uint32_t y = __byte_perm(w, 0u, (v & 1) ? 0x3322u : 0x1100u);
+                    b0 = y & 0x000F000Fu;   // nibbles 0, 2 of the pair: code * 2^-24
+                    b1 = y & 0x00F000F0u;   // nibbles 1, 3: 16 * code * 2^-24
                 } else {
-#pragma unroll
-                    for (int u = 0; u < KW; ++u) kw[nb][u] = src[u];
+                    const uint32_t w = kw[nb][v];
+                    b0 = w & 0x00FF00FFu;               // bytes 0, 2
+                    b1 = __byte_perm(w, 0u, 0x4341u);   // bytes 1, 3
                 }
-            }
-            float sacc[NB][NACC][4];
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
                 for (int acc = 0; acc < NACC; ++acc)
+                    mma16816(sacc[nb][acc], af[acc].x, af[acc].y, af[acc].z, af[acc].w, b0, b1);
+            }
+        }
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) sacc[nb][acc][e] = 0.0f;
+        for (int nb = 0; nb < NB; ++nb)
 #pragma unroll
-            for (int v = 0; v < KB; ++v) {
-                uint4 af[NACC];
+            for (int e = 0; e < 2; ++e) {
+                const int tk = 8 * nb + 2 * tq + e;
+                float x = 0.0f;
 #pragma unroll
-                for (int acc = 0; acc < NACC; ++acc) af[acc] = sQA[(acc * KB + v) * 32 + lane];
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                    uint32_t b0, b1;
-                    if constexpr (BITS == 4) {
-                        const uint32_t w = kw[nb][v / 2];
-                        // bytes (2, 3) or (0, 1) of the word into the two halves
-                        const uint32_t y = __byte_perm(w, 0u, (v & 1) ? 0x3322u : 0x1100u);
-                        b0 = y & 0x000F000Fu;   // nibbles 0, 2 of the pair: code * 2^-24
-                        b1 = y & 0x00F000F0u;   // nibbles 1, 3: 16 * code * 2^-24
-                    } else {
-                        const uint32_t w = kw[nb][v];
-                        b0 = w & 0x00FF00FFu;               // bytes 0, 2
-                        b1 = __byte_perm(w, 0u, 0x4341u);   // bytes 1, 3
-                    }
-#pragma unroll
-                    for (int acc = 0; acc < NACC; ++acc)
-                        mma16816(sacc[nb][acc], af[acc].x, af[acc].y, af[acc].z, af[acc].w, b0, b1);
+                for (int acc = 0; acc < NACC; ++acc) {
+                    const int glo = 4 * acc + (gq >> 2), ghi = 4 * acc + 2 + (gq >> 2);   // c0/c1, c2/c3 rows
+                    if (glo < NG) x = fmaf(sKsf[tk * NG + glo], sacc[nb][acc][e], x);
+                    if (NG > 2 && ghi < NG) x = fmaf(sKsf[tk * NG + ghi], sacc[nb][acc][2 + e], x);
+                }
+                x += __shfl_xor_sync(0xffffffffu, x, 16);
+                if (live[nb][e]) {
+                    float v = fmaf(alpha_l, x, sKbias[tk * REP + r_l()]);
+                    if (MASKED && a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l() * CH + tk]), v);
+                    lg[nb][e] = v;
                 }
             }
-            // scale groups apart, then the two halves of the quad pair (lanes
-            // gq and gq ^ 4 hold the other groups of the same row)
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tk = 8 * nb + 2 * tq + e;
-                    float x = 0.0f;
-#pragma unroll
-                    for (int acc = 0; acc < NACC; ++acc) {
-                        if (grp_lo[acc] < NG) x = fmaf(sKsf[tk * NG + grp_lo[acc]], sacc[nb][acc][e], x);
-                        if (grp_hi[acc] < NG) x = fmaf(sKsf[tk * NG + grp_hi[acc]], sacc[nb][acc][2 + e], x);
-                    }
-                    x += __shfl_xor_sync(0xffffffffu, x, 16);
-                    if (live[nb][e]) {
-                        float v = fmaf(alpha_l, x, sKbias[tk * REP + r_l]);
-                        if (MASKED && a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l * CH + tk]), v);
-                        lg[nb][e] = v;
-                    }
-                }
-        }
+    }
 
-        // ---- online softmax of row r_l (log2 units), lazy running max: M only
-        // moves when a score exceeds it by more than kSlack
+    // Online softmax of row r_l (log2 units), lazy running max: M only moves
+    // when a score exceeds it by more than kSlack.  Returns whether any row's
+    // max moved (warp-uniform); alpha is then the factor the lane's row's O
+    // (and S, rescaled here) is multiplied by, else 1.
+    __device__ __forceinline__ bool update_max(const float (&lg)[NB][2], float &Mrow, float &Ssum,
+                                               float &alpha) const {
+        alpha = 1.0f;
         bool grow = false;
 #pragma unroll
         for (int nb = 0; nb < NB; ++nb) grow |= lg[nb][0] > Mrow + kSlack || lg[nb][1] > Mrow + kSlack;
-        if (__any_sync(0xffffffffu, grow)) {
-            float cmax = -INFINITY;
+        if (!__any_sync(0xffffffffu, grow)) return false;
+        float cmax = -INFINITY;
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) cmax = fmaxf(cmax, fmaxf(lg[nb][0], lg[nb][1]));
-            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
-            cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
-            const float m_new = fmaxf(Mrow, cmax);
-            const float alpha = m_new == Mrow ? 1.0f : ex2(Mrow - m_new);   // 0 while M = -inf
-            Mrow = m_new;
-            Ssum *= alpha;
-            // O^T columns of this lane: n = 2 tq, 2 tq + 1 -> rows (2 tq) % 4, (2 tq + 1) % 4
-            const int r0 = (2 * tq) & 3;
-            const float al0 = __shfl_sync(0xffffffffu, alpha, 4 * r0);
-            const float al1 = __shfl_sync(0xffffffffu, alpha, 4 * (r0 + 1));
+        for (int nb = 0; nb < NB; ++nb) cmax = fmaxf(cmax, fmaxf(lg[nb][0], lg[nb][1]));
+        cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
+        cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
+        const float m_new = fmaxf(Mrow, cmax);
+        alpha = m_new == Mrow ? 1.0f : ex2(Mrow - m_new);   // 0 while M = -inf
+        Mrow = m_new;
+        Ssum *= alpha;
+        return true;
+    }
+
+    // B fragments of P (lanes gq < 4 P_hi, gq >= 4 P_lo) and the row sums.
+    __device__ __forceinline__ void p_frags(const float (&lg)[NB][2], float Mrow, float &Ssum,
+                                            uint32_t (&pf)[VB][2]) const {
+        const bool lo_term = gq >= 4;
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) {
+            float p[2];
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                p[e] = Mrow == -INFINITY ? 0.0f : ex2(lg[nb][e] - Mrow);
+                Ssum += p[e];
+            }
+            const __half2 hi = __floats2half2_rn(p[0], p[1]);
+            uint32_t f = h2_bits(hi);
+            if (lo_term) {
+                const float2 hf = __half22float2(hi);
+                f = h2_bits(__floats2half2_rn(p[0] - hf.x, p[1] - hf.y));
+            }
+            pf[nb >> 1][nb & 1] = f;
+        }
+    }
+
+    // O^T columns of this lane: n = 2 tq, 2 tq + 1 -> rows (2 tq) % 4, (2 tq) % 4 + 1.
+    __device__ __forceinline__ static void rescale_o(float (&O)[KB][4], float al0, float al1) {
+#pragma unroll
+        for (int mb = 0; mb < KB; ++mb) {
+            O[mb][0] *= al0;
+            O[mb][1] *= al1;
+            O[mb][2] *= al0;
+            O[mb][3] *= al1;
+        }
+    }
+
+    // O^T += V^T P^T per 16-token block of the chunk whose V words are at sV
+    // (the V table of the chunk stored).
+    __device__ __forceinline__ void pv(const uint32_t *sV, const uint32_t (&pf)[VB][2], float (&O)[KB][4]) const {
+        int vgrp[VW];   // scale groups of the lane's V words gq * VW .. + VW
+#pragma unroll
+        for (int u = 0; u < VW; ++u) vgrp[u] = ((gq * VW + u) * (32 / BITS)) / GC;
+#pragma unroll
+        for (int kb = 0; kb < VB; ++kb) {
+            // tokens of the fragment: (T0, T1) = 16 kb + 2 tq + {0, 1}, (T2, T3) = + 8
+            const int tA = 16 * kb + 2 * tq, tB = tA + 8;
+            uint32_t w[4][VW];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int t = (k < 2 ? tA : tB) + (k & 1);
+                const uint32_t *src = sV + t * WPT + gq * VW;
+                if constexpr (VW % 4 == 0) {
+#pragma unroll
+                    for (int u = 0; u < VW; u += 4) {
+                        const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
+                        w[k][u] = x.x; w[k][u + 1] = x.y; w[k][u + 2] = x.z; w[k][u + 3] = x.w;
+                    }
+                } else if constexpr (VW == 2) {
+                    const uint2 x = *reinterpret_cast<const uint2 *>(src);
+                    w[k][0] = x.x; w[k][1] = x.y;
+                } else {
+                    w[k][0] = src[0];
+                }
+            }
+            uint2 sbA[VW], sbB[VW];
+#pragma unroll
+            for (int u = 0; u < VW; ++u) {
+                sbA[u] = sVSB[vgrp[u] * (CH / 2) + tA / 2];
+                sbB[u] = sVSB[vgrp[u] * (CH / 2) + tB / 2];
+            }
+            const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
 #pragma unroll
             for (int mb = 0; mb < KB; ++mb) {
-                O[mb][0] *= al0;
-                O[mb][1] *= al1;
-                O[mb][2] *= al0;
-                O[mb][3] *= al1;
-            }
-        }
-        uint32_t pf[VB][2];   // B fragments of P: lanes gq < 4 P_hi, gq >= 4 P_lo
-        if (chunk_live) {
-            const bool lo_term = gq >= 4;
+                uint32_t ar[4];
+                if constexpr (BITS == 4) {
+                    const int u = mb >> 2, bi = mb & 3;
+                    const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
 #pragma unroll
-            for (int nb = 0; nb < NB; ++nb) {
-                float p[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    p[e] = Mrow == -INFINITY ? 0.0f : ex2(lg[nb][e] - Mrow);
-                    Ssum += p[e];
-                }
-                const __half2 hi = __floats2half2_rn(p[0], p[1]);
-                uint32_t f = h2_bits(hi);
-                if (lo_term) {
-                    const float2 hf = __half22float2(hi);
-                    f = h2_bits(__floats2half2_rn(p[0] - hf.x, p[1] - hf.y));
-                }
-                pf[nb >> 1][nb & 1] = f;
-            }
-        }
-
-        // ---- values: O^T += V^T P^T per 16-token block
-        if (chunk_live) {
-#pragma unroll
-            for (int kb = 0; kb < VB; ++kb) {
-                // tokens of the fragment: (T0, T1) = 16 kb + 2 tq + {0, 1}, (T2, T3) = + 8
-                const int tA = 16 * kb + 2 * tq, tB = tA + 8;
-                uint32_t w[4][VW];
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    const int t = (k < 2 ? tA : tB) + (k & 1);
-                    const uint32_t *src = sV + t * WPT + gq * VW;
-                    if constexpr (VW % 4 == 0) {
-#pragma unroll
-                        for (int u = 0; u < VW; u += 4) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
-                            w[k][u] = x.x; w[k][u + 1] = x.y; w[k][u + 2] = x.z; w[k][u + 3] = x.w;
-                        }
-                    } else if constexpr (VW == 2) {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
-                        w[k][0] = x.x; w[k][1] = x.y;
-                    } else {
-                        w[k][0] = src[0];
+                    for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
+                        const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
+                        const uint2 sb = hb ? sbB[u] : sbA[u];
+                        const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
+                        const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
+                        ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
+                        ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // M row gq + 8
                     }
-                }
-                uint2 sbA[VW], sbB[VW];
+                } else {
+                    const int u = mb >> 1, b0 = 2 * (mb & 1);
 #pragma unroll
-                for (int u = 0; u < VW; ++u) {
-                    sbA[u] = sVSB[vgrp[u] * (CH / 2) + tA / 2];
-                    sbB[u] = sVSB[vgrp[u] * (CH / 2) + tB / 2];
-                }
-                const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
+                    for (int hb = 0; hb < 2; ++hb) {
+                        const uint2 sb = hb ? sbB[u] : sbA[u];
 #pragma unroll
-                for (int mb = 0; mb < KB; ++mb) {
-                    uint32_t ar[4];
-                    if constexpr (BITS == 4) {
-                        const int u = mb >> 2, bi = mb & 3;
-                        const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-#pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
+                        for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
+                            const int bi = b0 + hr;
+                            const uint32_t sel =
+                                static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
                             const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                            const uint2 sb = hb ? sbB[u] : sbA[u];
-                            const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
-                            const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
-                            ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
-                            ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // M row gq + 8
-                        }
-                    } else {
-                        const int u = mb >> 1, b0 = 2 * (mb & 1);
-#pragma unroll
-                        for (int hb = 0; hb < 2; ++hb) {
-                            const uint2 sb = hb ? sbB[u] : sbA[u];
-#pragma unroll
-                            for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
-                                const int bi = b0 + hr;
-                                const uint32_t sel =
-                                    static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-                                const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                                const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
-                                ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
-                            }
+                            const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
+                            ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
                         }
                     }
-                    // A regs: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq, T2 T3), a6a7 (gq + 8, T2 T3)
-                    mma16816(O[mb], ar[0], ar[1], ar[2], ar[3], pf[kb][0], pf[kb][1]);
                 }
+                // A regs: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq, T2 T3), a6a7 (gq + 8, T2 T3)
+                mma16816(O[mb], ar[0], ar[1], ar[2], ar[3], pf[kb][0], pf[kb][1]);
             }
         }
-        __syncwarp();
-        if (issued < nc) { issue(c_begin + issued, issued % NS); ++issued; }   // stage b is free
-    }
-    pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
-    if (!ok) {
-        if (lane == 0 && a.err != nullptr) atomicOr(a.err, 1);
-        for (; done < issued; ++done) wait_warp(&bars[done % NS], static_cast<uint32_t>(done / NS) & 1u);
-        return;
     }
 
-    // ---- row sums over the quad's keys; O^T: P_hi + P_lo columns (tq, tq + 2)
-    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 1);
-    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 2);
+    // Output of the rows: O^T columns P_hi + P_lo (tq, tq + 2) added; lanes tq 0
+    // and 1 hold rows 2 tq, 2 tq + 1 (c0 / c2 row 2 tq, c1 / c3 row 2 tq + 1).
+    // Mr / Sr: the rows' final running max and sum.  One split: out = O / S
+    // with the sink; else the split's partial O.
+    __device__ __forceinline__ void write_out(float (&O)[KB][4], const float (&Mr)[2], const float (&Sr)[2],
+                                              int split) const {
 #pragma unroll
-    for (int mb = 0; mb < KB; ++mb)
+        for (int mb = 0; mb < KB; ++mb)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) O[mb][e] += __shfl_xor_sync(0xffffffffu, O[mb][e], 2);
-    // lanes tq 0, 1 hold rows 2 tq, 2 tq + 1: c0 / c2 row 2 tq, c1 / c3 row 2 tq + 1
-    float Mr[2], Sr[2];
-#pragma unroll
-    for (int k = 0; k < 2; ++k) {
-        const int r = (2 * tq + k) & 3;
-        Mr[k] = __shfl_sync(0xffffffffu, Mrow, 4 * r);
-        Sr[k] = __shfl_sync(0xffffffffu, Ssum, 4 * r);
-    }
-    if (tq < 2) {
+            for (int e = 0; e < 4; ++e) O[mb][e] += __shfl_xor_sync(0xffffffffu, O[mb][e], 2);
+        if (tq >= 2) return;
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int r = 2 * tq + k;
@@ -668,54 +571,240 @@ __global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
             }
         }
     }
+
+    // Copies of a chunk's runs.  A full chunk whose runs are 16-byte aligned,
+    // in a call with a mask: one bulk copy per run, each issued by a lane of its
+    // own in the same instruction - lane 0 the K words (when this warp copies
+    // them), lanes 1-4 the K / V scale and bias runs, then one lane per
+    // bool-mask and float-mask row - after lane 0 has posted the byte count;
+    // the lanes' cp.async arrivals then complete at once.  Other chunks (and
+    // calls without a mask, where the many small bulk copies measured slower
+    // than the lanes' 16-byte cp.async) take the staging of quant_kernel.cuh.
+    struct CopyPlan {
+        const unsigned char *src;   // this lane's run at token 0 (nullptr: none)
+        uint32_t stride, bytes, dst, tx;
+        bool bulk, with_k;
+    };
+    __device__ __forceinline__ CopyPlan copy_plan(int kv, bool with_k) const {
+        CopyPlan cp{nullptr, 0u, 0u, 0u, 0u, false, with_k};
+        if constexpr (MASKED) {
+            cp.bulk = a.al_sb && (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
+            const size_t kv0 = static_cast<size_t>(kv) * N;
+            const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
+            if (lane == 0) {
+                if (with_k) {
+                    cp.src = reinterpret_cast<const unsigned char *>(a.kp + kv0 * WPT);
+                    cp.stride = WPT * 4;
+                    cp.dst = L.k;
+                }
+            } else if (lane <= 4) {
+                const void *base = lane == 1 ? a.ks : lane == 2 ? a.kb : lane == 3 ? a.vs : a.vb;
+                cp.src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(base) + kv0 * NG);
+                cp.stride = NG * 2;
+                cp.dst = lane == 1 ? L.ks : lane == 2 ? L.kb : lane == 3 ? L.vs : L.vb;
+            } else if (lane < 5 + nb_rows) {   // bool-mask rows 0 .. nrow - 1
+                const int r = lane - 5;
+                cp.src = reinterpret_cast<const unsigned char *>(a.mbool + static_cast<size_t>(q0 + r) * N);
+                cp.stride = 4;
+                cp.dst = L.mb + r * CH * 4;
+            } else if (lane < 5 + nb_rows + nf_rows) {   // float-mask rows
+                const int r = lane - 5 - nb_rows;
+                cp.src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(a.mfloat) +
+                                                                 static_cast<size_t>(q0 + r) * N);
+                cp.stride = 2;
+                cp.dst = L.mf + r * CH * 2;
+            }
+            cp.bytes = cp.stride * CH;
+            cp.tx = CH * ((with_k ? WPT * 4 : 0) + 4 * NG * 2 + nb_rows * 4 + nf_rows * 2);
+        }
+        return cp;
+    }
+    // Group A of chunk c into stage b (the K tile only when the plan has it).
+    __device__ __forceinline__ void issue_runs(const CopyPlan &cp, const QuantStager<CH> &stg, unsigned char *smem,
+                                               uint64_t *bars, int c, int b) const {
+        const int t0 = c * CH;
+        if (MASKED && cp.bulk && t0 + CH <= N) {
+            unsigned char *st = smem + L.a0 + b * L.a_stage;
+            if (lane == 0) {
+                if (cp.with_k) mbar_arrive_expect_tx(&bars[b], cp.tx);
+                else mbar_expect_tx(&bars[b], cp.tx);
+            }
+            __syncwarp();
+            if (cp.src != nullptr)
+                bulk_load(st + cp.dst, cp.src + static_cast<size_t>(t0) * cp.stride, cp.bytes, &bars[b]);
+            cp_arrive_noinc(&bars[b]);
+        } else {
+            stg.issue_a(c, b);
+        }
+    }
+    // The V tile of chunk c into stage b: its bytes posted (no arrival) before
+    // group A's arrivals, so the phase cannot complete without them.
+    __device__ __forceinline__ void issue_v(unsigned char *smem, uint64_t *bars, int kv, int c, int b) const {
+        if (lane == 0) {
+            const int t0 = c * CH;
+            const uint32_t vbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
+            mbar_expect_tx(&bars[b], vbytes);
+            bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, vbytes, &bars[b]);
+        }
+    }
+    // The K tile of chunk c into stage b (the expect-tx arrive is one of the
+    // stage barrier's 33): the two-warp form's score warp.
+    __device__ __forceinline__ void issue_k(unsigned char *smem, uint64_t *bars, int kv, int c, int b) const {
+        if (lane == 0) {
+            const int t0 = c * CH;
+            const uint32_t kbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
+            mbar_arrive_expect_tx(&bars[b], kbytes);
+            bulk_load(smem + L.a0 + b * L.a_stage + L.k, a.kp + (static_cast<size_t>(kv) * N + t0) * WPT, kbytes,
+                      &bars[b]);
+        }
+    }
+};
+
+// One-warp form (shapes of up to 16 packed words per token, where it measured
+// faster than the two-warp form): one warp per CTA does every phase of a chunk
+// in turn and issues every copy itself.
+template <int BITS, typename T, int DIMC, int GC, bool MASKED>
+__global__ void __launch_bounds__(32, 12) quant_mma1_kernel(const QuantArgs a) {
+    using P = QmmaPhases<BITS, T, DIMC, GC, MASKED>;
+    constexpr int CH = P::CH, NB = P::NB, VB = P::VB, KB = P::KB, NG = P::NG, NS = kQmmaStages;
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int lane = threadIdx.x, tq = lane & 3;
+    const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
+    const int q0 = kv * a.rep + rg * REP;
+    const int nrow = min(REP, a.rep - rg * REP);
+    const QmmaLayout M = qmma_layout(P::WPT, NG, CH, DIMC, P::NACC, NS, false);
+    const QuantLayout &L = M.st;
+    const P ph{a, L, reinterpret_cast<uint4 *>(smem + M.qa), reinterpret_cast<float *>(smem + M.qs),
+               reinterpret_cast<__half *>(smem + M.qf), reinterpret_cast<float *>(smem + M.ksf),
+               reinterpret_cast<float *>(smem + M.kbias), reinterpret_cast<uint2 *>(smem + M.vsb),
+               lane, lane >> 2, tq, q0, nrow, a.N};
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M.bars);
+    const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
+    const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
+    const int nc = c_end - c_begin;
+
+    uint16_t qraw[REP][P::QPL];
+    ph.load_q(qraw);
+    const uint32_t tree_bits = ph.tree_bits();
+    if (lane == 0) {
+        // stage k: lane 0's expect-tx arrive + one cp.async arrive per lane; the
+        // V tile's bytes are posted on the same barrier
+        for (int k = 0; k < NS; ++k) mbar_init(&bars[k], 33);
+        fence_mbar_init();
+    }
+    __syncwarp();
+    const QuantStager<CH> stg{a, L, smem, bars, P::WPT, NG, kv, q0, nrow, lane, NS, true};
+    const typename P::CopyPlan cp = ph.copy_plan(kv, true);
+    auto issue = [&](int c, int b) {
+        ph.issue_v(smem, bars, kv, c, b);
+        ph.issue_runs(cp, stg, smem, bars, c, b);
+    };
+    int issued = 0, done = 0;
+    for (; issued < NS && issued < nc; ++issued) issue(c_begin + issued, issued % NS);
+    const float alpha_l = ph.setup_scores(qraw);
+    float qs_l[NG];
+    ph.bias_sums(qs_l);
+
+    float Mrow = -INFINITY, Ssum = 0.0f;   // online softmax of row r_l (log2 units)
+    float O[KB][4];
+#pragma unroll
+    for (int mb = 0; mb < KB; ++mb)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) O[mb][e] = 0.0f;
+
+    bool ok = true;
+    for (int i = 0; i < nc; ++i) {
+        const int c = c_begin + i, b = i % NS;
+        if (!wait_warp(&bars[b], static_cast<uint32_t>(i / NS) & 1u, i == 0 ? a.first_wait_polls : kQuantWaitPolls)) {
+            ok = false;
+            break;
+        }
+        ++done;
+        __syncwarp();
+        const unsigned char *st = smem + L.a0 + b * L.a_stage;
+        bool live[NB][2];
+        const bool chunk_live = ph.gates(st, c * CH, tree_bits, live);
+        float lg[NB][2];
+#pragma unroll
+        for (int nb = 0; nb < NB; ++nb) lg[nb][0] = lg[nb][1] = -INFINITY;
+        if (chunk_live) {
+            typename P::KRaw kr;
+            typename P::VRaw vr;
+            ph.k_load(st, kr);
+            ph.v_load(st, vr);
+            ph.k_store(kr, qs_l);
+            ph.v_store(vr);
+            __syncwarp();
+            ph.scores(st, alpha_l, live, lg);
+        }
+        float alpha;
+        if (ph.update_max(lg, Mrow, Ssum, alpha)) {   // a row's running max moved
+            const int r0 = (2 * tq) & 3;
+            P::rescale_o(O, __shfl_sync(0xffffffffu, alpha, 4 * r0), __shfl_sync(0xffffffffu, alpha, 4 * (r0 + 1)));
+        }
+        if (chunk_live) {
+            uint32_t pf[VB][2];
+            ph.p_frags(lg, Mrow, Ssum, pf);
+            ph.pv(reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage), pf, O);
+        }
+        __syncwarp();
+        if (issued < nc) { issue(c_begin + issued, issued % NS); ++issued; }   // stage b is free
+    }
+    pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
+    if (!ok) {
+        // a copy never completed: report it, let the issued copies land (bounded) and leave
+        if (lane == 0 && a.err != nullptr) atomicOr(a.err, 1);
+        for (; done < issued; ++done) wait_warp(&bars[done % NS], static_cast<uint32_t>(done / NS) & 1u);
+        return;
+    }
+    // row sums over the quad's keys; the rows' statistics from lanes 4 r
+    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 1);
+    Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 2);
+    float Mr[2], Sr[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int r = (2 * tq + k) & 3;
+        Mr[k] = __shfl_sync(0xffffffffu, Mrow, 4 * r);
+        Sr[k] = __shfl_sync(0xffffffffu, Ssum, 4 * r);
+    }
     const float s_row = __shfl_sync(0xffffffffu, Ssum, 4 * (lane & 3));
     const float m_row = __shfl_sync(0xffffffffu, Mrow, 4 * (lane & 3));
-    if (a.nwg > 1 && lane < REP && lane < nrow)
+    ph.write_out(O, Mr, Sr, split);
+    if (a.nwg > 1 && lane < nrow)
         reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] =
             make_float2(s_row, m_row);
 }
 
-// MASKED: the call passes a bool or a float mask (instances without one carry
-// no mask code and stage every chunk through the lanes' cp.async).
-//
-// Two warps per CTA, one (KV row, row group, token split) each:
+// Two-warp form (wider tokens), one (KV row, row group, token split) per CTA:
 //  * warp 0 (scores): gates, the K tables, S = Q K^T, the online softmax and
 //    the B fragments of P, handed to warp 1 through a double-buffered slot in
-//    shared memory (P, the per-row rescale factors of O, the chunk's liveness);
+//    shared memory (P, the per-row rescale factors of O, the chunk's
+//    liveness); it issues the chunks' K tiles;
 //  * warp 1 (values): issues the copies of a chunk's scale / bias runs, masks
-//    and V (warp 0 issues its K tile; all on one barrier, NS chunks ahead),
-//    rescales O, builds the V table and accumulates O^T += V^T P^T; it also
-//    writes the output.
+//    and V tile (all on the stage's barrier, NS chunks ahead), rescales O,
+//    builds the V table, accumulates O^T += V^T P^T and writes the output.
 // The two work on different chunks at the same time.
 template <int BITS, typename T, int DIMC, int GC, bool MASKED>
 __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
-    using S = MmaShape<BITS, DIMC>;
-    constexpr int CH = S::CH, KB = S::KB, NB = S::NB, VB = S::VB, KW = S::KW, VW = S::VW;
-    constexpr int NG = DIMC / GC;
-    constexpr int NACC = (NG + 3) / 4;
-    constexpr int WPT = S::WPTC;
-    constexpr int NS = kQmmaStages;
+    using P = QmmaPhases<BITS, T, DIMC, GC, MASKED>;
+    constexpr int CH = P::CH, NB = P::NB, VB = P::VB, KB = P::KB, NG = P::NG, NS = kQmmaStages;
     extern __shared__ __align__(128) unsigned char smem[];
     const int warp = static_cast<int>(threadIdx.x) >> 5, lane = static_cast<int>(threadIdx.x) & 31;
-    const int gq = lane >> 2, tq = lane & 3;
+    const int tq = lane & 3;
     const int rg = blockIdx.x % a.n_rg, split = blockIdx.x / a.n_rg, kv = blockIdx.y;
     const int q0 = kv * a.rep + rg * REP;
     const int nrow = min(REP, a.rep - rg * REP);
-    const int N = a.N;
-    const QmmaLayout M = qmma_layout(WPT, NG, CH, DIMC, NACC, NS, true);
+    const QmmaLayout M = qmma_layout(P::WPT, NG, CH, DIMC, P::NACC, NS, true);
     const QuantLayout &L = M.st;
-    uint4 *sQA = reinterpret_cast<uint4 *>(smem + M.qa);
-    float *sQS = reinterpret_cast<float *>(smem + M.qs);
-    __half *sQF = reinterpret_cast<__half *>(smem + M.qf);   // q * 2^e, exact in f16
-    float *sKsf = reinterpret_cast<float *>(smem + M.ksf);
-    float *sKbias = reinterpret_cast<float *>(smem + M.kbias);
-    uint2 *sVSB = reinterpret_cast<uint2 *>(smem + M.vsb);
+    const P ph{a, L, reinterpret_cast<uint4 *>(smem + M.qa), reinterpret_cast<float *>(smem + M.qs),
+               reinterpret_cast<__half *>(smem + M.qf), reinterpret_cast<float *>(smem + M.ksf),
+               reinterpret_cast<float *>(smem + M.kbias), reinterpret_cast<uint2 *>(smem + M.vsb),
+               lane, lane >> 2, tq, q0, nrow, a.N};
     QmmaPSlot *sPS = reinterpret_cast<QmmaPSlot *>(smem + M.pslot);
     float *sML = reinterpret_cast<float *>(smem + M.ml);   // [row] M, then [row] S
     volatile int *sAbort = reinterpret_cast<volatile int *>(smem + M.ml + 8 * 4);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + M.bars);
     uint64_t *p_full = bars + NS, *p_empty = bars + NS + 2;
-
     const int c_begin = a.c_lo + static_cast<int>((static_cast<long long>(split) * a.nch) / a.nwg);
     const int c_end = a.c_lo + static_cast<int>((static_cast<long long>(split + 1) * a.nch) / a.nwg);
     const int nc = c_end - c_begin;
@@ -734,7 +823,6 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
     }
     __syncthreads();
     bool ok = true;
-    const uint32_t first_polls = a.first_wait_polls;
     float O[KB][4];   // warp 1: O^T fragments (M rows = dimensions, columns = rows x {P_hi, P_lo})
 #pragma unroll
     for (int mb = 0; mb < KB; ++mb)
@@ -743,80 +831,19 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
 
     if (warp == 1) {
         // ================================================================ values
-        const QuantStager<CH> stg{a, L, smem, bars, WPT, NG, kv, q0, nrow, lane, NS, false};
-        // The runs of a full chunk whose runs are 16-byte aligned, in a call with
-        // a mask: one bulk copy per run, each issued by a lane of its own in the
-        // same instruction - lanes 1-4 the K / V scale and bias runs, then one
-        // lane per bool-mask and float-mask row - after lane 0 has posted the
-        // byte count; the lanes' cp.async arrivals then complete at once.  Other
-        // chunks (and calls without a mask, where the many small bulk copies
-        // measured slower than the lanes' 16-byte cp.async) take the staging of
-        // quant_kernel.cuh without its K tile (warp 0 copies that).
-        const bool bulk_a =
-            MASKED && a.al_sb && (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
-        const unsigned char *cp_src = nullptr;   // this lane's run at token 0
-        uint32_t cp_stride = 0, cp_bytes = 0, cp_dst = 0, tx_a = 0;
-        if constexpr (MASKED) {
-            const size_t kv0 = static_cast<size_t>(kv) * N;
-            const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
-            // lane 0 copies nothing here (it posts the byte count); lanes 1-4 the
-            // scale / bias runs; lanes 5 .. 5 + nb_rows - 1 the bool-mask rows and
-            // the next nf_rows lanes the float-mask rows (rows 0 .. nrow - 1)
-            if (lane == 0) {
-                cp_src = nullptr;
-            } else if (lane <= 4) {
-                const void *base = lane == 1 ? a.ks : lane == 2 ? a.kb : lane == 3 ? a.vs : a.vb;
-                cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(base) + kv0 * NG);
-                cp_stride = NG * 2;
-                cp_dst = lane == 1 ? L.ks : lane == 2 ? L.kb : lane == 3 ? L.vs : L.vb;
-            } else if (lane < 5 + nb_rows) {
-                const int r = lane - 5;
-                cp_src = reinterpret_cast<const unsigned char *>(a.mbool + static_cast<size_t>(q0 + r) * N);
-                cp_stride = 4;
-                cp_dst = L.mb + r * CH * 4;
-            } else if (lane < 5 + nb_rows + nf_rows) {
-                const int r = lane - 5 - nb_rows;
-                cp_src = reinterpret_cast<const unsigned char *>(static_cast<const uint16_t *>(a.mfloat) +
-                                                                 static_cast<size_t>(q0 + r) * N);
-                cp_stride = 2;
-                cp_dst = L.mf + r * CH * 2;
-            }
-            cp_bytes = cp_stride * CH;
-            tx_a = CH * (4 * NG * 2 + nb_rows * 4 + nf_rows * 2);
-        }
-        // a whole chunk on one barrier: the V tile's bytes are posted (no
-        // arrival) before group A's arrivals, so the phase cannot complete
-        // without them
+        const QuantStager<CH> stg{a, L, smem, bars, P::WPT, NG, kv, q0, nrow, lane, NS, false};
+        const typename P::CopyPlan cp = ph.copy_plan(kv, false);
         auto issue = [&](int c, int b) {
-            const int t0 = c * CH;
-            if (lane == 0) {
-                const uint32_t vbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
-                mbar_expect_tx(&bars[b], vbytes);
-                bulk_load(smem + L.v0 + b * L.v_stage, a.vp + (static_cast<size_t>(kv) * N + t0) * WPT, vbytes,
-                          &bars[b]);
-            }
-            if (MASKED && bulk_a && t0 + CH <= N) {
-                unsigned char *st = smem + L.a0 + b * L.a_stage;
-                if (lane == 0) mbar_expect_tx(&bars[b], tx_a);
-                __syncwarp();
-                if (cp_src != nullptr)
-                    bulk_load(st + cp_dst, cp_src + static_cast<size_t>(t0) * cp_stride, cp_bytes, &bars[b]);
-                cp_arrive_noinc(&bars[b]);
-            } else {
-                stg.issue_a(c, b);
-            }
+            ph.issue_v(smem, bars, kv, c, b);
+            ph.issue_runs(cp, stg, smem, bars, c, b);
         };
         int issued = 0, done = 0;
         for (; issued < NS && issued < nc; ++issued) issue(c_begin + issued, issued % NS);
-        // the lane's V words: gq * VW .. + VW of each token; their scale groups
-        int vgrp[VW];
-#pragma unroll
-        for (int u = 0; u < VW; ++u) vgrp[u] = ((gq * VW + u) * (32 / BITS)) / GC;
         const int r0 = (2 * tq) & 3;   // rows of this lane's O^T columns: r0, r0 + 1
-
         for (int i = 0; i < nc && ok; ++i) {
             const int b = i % NS, slot = i & 1;
-            if (!wait_warp(&bars[b], static_cast<uint32_t>(i / NS) & 1u, i == 0 ? first_polls : kQuantWaitPolls) ||
+            if (!wait_warp(&bars[b], static_cast<uint32_t>(i / NS) & 1u,
+                           i == 0 ? a.first_wait_polls : kQuantWaitPolls) ||
                 !wait_warp(&p_full[slot], static_cast<uint32_t>(i >> 1) & 1u)) {
                 ok = false;
                 break;
@@ -824,112 +851,19 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
             ++done;
             const QmmaPSlot &ps = sPS[slot];
             const float al0 = ps.alpha[r0], al1 = ps.alpha[r0 + 1];
-            if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) {
-#pragma unroll
-                for (int mb = 0; mb < KB; ++mb) {
-                    O[mb][0] *= al0;
-                    O[mb][1] *= al1;
-                    O[mb][2] *= al0;
-                    O[mb][3] *= al1;
-                }
-            }
+            if (__any_sync(0xffffffffu, al0 != 1.0f || al1 != 1.0f)) P::rescale_o(O, al0, al1);
             if (ps.live) {
-                const unsigned char *st = smem + L.a0 + b * L.a_stage;
-                const uint16_t *sVs = reinterpret_cast<const uint16_t *>(st + L.vs);
-                const uint16_t *sVb = reinterpret_cast<const uint16_t *>(st + L.vb);
-                const uint32_t *sV = reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage);
-                // V scale / bias pairs of token pairs (2p, 2p + 1) in f16 [g][p],
-                // every load issued before the first store
-                {
-                    constexpr int NVP = (NG * (CH / 2) + 31) / 32;
-                    uint16_t vsr[NVP][2], vbr[NVP][2];
-#pragma unroll
-                    for (int j = 0; j < NVP; ++j) {
-                        const int idx = lane + 32 * j;
-                        const int g = idx / (CH / 2), p = idx % (CH / 2);
-                        const bool in = idx < NG * (CH / 2);
-#pragma unroll
-                        for (int e = 0; e < 2; ++e) {
-                            vsr[j][e] = in ? sVs[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
-                            vbr[j][e] = in ? sVb[(2 * p + e) * NG + g] : static_cast<uint16_t>(0);
-                        }
-                    }
-#pragma unroll
-                    for (int j = 0; j < NVP; ++j)
-                        if (lane + 32 * j < NG * (CH / 2)) {
-                            const __half2 sp = __floats2half2_rn(t2f<T>(vsr[j][0]), t2f<T>(vsr[j][1]));
-                            const __half2 bp = __floats2half2_rn(t2f<T>(vbr[j][0]), t2f<T>(vbr[j][1]));
-                            sVSB[lane + 32 * j] = make_uint2(h2_bits(sp), h2_bits(bp));
-                        }
-                }
+                typename P::VRaw vr;
+                ph.v_load(smem + L.a0 + b * L.a_stage, vr);
+                ph.v_store(vr);
                 __syncwarp();
-                // ---- O^T += V^T P^T per 16-token block
+                uint32_t pf[VB][2];
 #pragma unroll
                 for (int kb = 0; kb < VB; ++kb) {
-                    const uint32_t pf0 = ps.pf[kb][0][lane], pf1 = ps.pf[kb][1][lane];
-                    // tokens of the fragment: (T0, T1) = 16 kb + 2 tq + {0, 1}, (T2, T3) = + 8
-                    const int tA = 16 * kb + 2 * tq, tB = tA + 8;
-                    uint32_t w[4][VW];
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const int t = (k < 2 ? tA : tB) + (k & 1);
-                        const uint32_t *src = sV + t * WPT + gq * VW;
-                        if constexpr (VW % 4 == 0) {
-#pragma unroll
-                            for (int u = 0; u < VW; u += 4) {
-                                const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
-                                w[k][u] = x.x; w[k][u + 1] = x.y; w[k][u + 2] = x.z; w[k][u + 3] = x.w;
-                            }
-                        } else if constexpr (VW == 2) {
-                            const uint2 x = *reinterpret_cast<const uint2 *>(src);
-                            w[k][0] = x.x; w[k][1] = x.y;
-                        } else {
-                            w[k][0] = src[0];
-                        }
-                    }
-                    uint2 sbA[VW], sbB[VW];
-#pragma unroll
-                    for (int u = 0; u < VW; ++u) {
-                        sbA[u] = sVSB[vgrp[u] * (CH / 2) + tA / 2];
-                        sbB[u] = sVSB[vgrp[u] * (CH / 2) + tB / 2];
-                    }
-                    const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
-#pragma unroll
-                    for (int mb = 0; mb < KB; ++mb) {
-                        uint32_t ar[4];
-                        if constexpr (BITS == 4) {
-                            const int u = mb >> 2, bi = mb & 3;
-                            const uint32_t sel =
-                                static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-#pragma unroll
-                            for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
-                                const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                                const uint2 sb = hb ? sbB[u] : sbA[u];
-                                const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
-                                const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
-                                ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
-                                ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // gq + 8
-                            }
-                        } else {
-                            const int u = mb >> 1, b0 = 2 * (mb & 1);
-#pragma unroll
-                            for (int hb = 0; hb < 2; ++hb) {
-                                const uint2 sb = hb ? sbB[u] : sbA[u];
-#pragma unroll
-                                for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
-                                    const int bi = b0 + hr;
-                                    const uint32_t sel =
-                                        static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-                                    const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                                    const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
-                                    ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
-                                }
-                            }
-                        }
-                        // A regs: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq, T2 T3), a6a7 (gq + 8, T2 T3)
-                        mma16816(O[mb], ar[0], ar[1], ar[2], ar[3], pf0, pf1);
-                    }
+                    pf[kb][0] = ps.pf[kb][0][lane];
+                    pf[kb][1] = ps.pf[kb][1][lane];
                 }
+                ph.pv(reinterpret_cast<const uint32_t *>(smem + L.v0 + b * L.v_stage), pf, O);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_empty[slot]);   // the slot and the stage's reads are done
@@ -945,292 +879,48 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
         }
     } else {
         // ================================================================ scores
-        // the 4 query rows, element lane + 32 k per lane, loaded before anything waits
-        constexpr int QPL = DIMC / 32;
-        uint16_t qraw[REP][QPL];
-        {
-            const uint16_t *qg = reinterpret_cast<const uint16_t *>(a.queries);
-#pragma unroll
-            for (int r = 0; r < REP; ++r)
-#pragma unroll
-                for (int k = 0; k < QPL; ++k)
-                    qraw[r][k] = r < nrow ? __ldg(qg + static_cast<size_t>(q0 + r) * DIMC + lane + 32 * k)
-                                          : static_cast<uint16_t>(0);
-        }
-        // the K tiles: chunk c into stage b (the expect-tx arrive is one of the
-        // stage barrier's 33), NS chunks ahead, each once this warp is done
-        // with the stage's K tile
-        auto issue_k = [&](int c, int b) {
-            if (lane == 0) {
-                const int t0 = c * CH;
-                const uint32_t kbytes = static_cast<uint32_t>(min(CH, N - t0) * WPT * 4);
-                mbar_arrive_expect_tx(&bars[b], kbytes);
-                bulk_load(smem + L.a0 + b * L.a_stage + L.k, a.kp + (static_cast<size_t>(kv) * N + t0) * WPT,
-                          kbytes, &bars[b]);
-            }
-        };
+        uint16_t qraw[REP][P::QPL];
+        ph.load_q(qraw);
+        // the K tiles, NS chunks ahead, each once this warp is done with the stage's K tile
         int k_issued = 0;
-        for (; k_issued < NS && k_issued < nc; ++k_issued) issue_k(c_begin + k_issued, k_issued % NS);
-        const int r_l = gq & 3;   // query row of the lane's score fragments
-        const int tree_lo = N - a.tree_ql;
-        uint32_t tree_bits = 0u;
-        if (a.tree_ql > 0) {
-            const uint32_t mine =
-                quant_tree_ancestors(lane < a.tree_ql ? __ldg(a.tree_parents + lane) : -1, a.tree_ql);
-            tree_bits = __shfl_sync(0xffffffffu, mine, (q0 + r_l) % a.tree_ql);
-        }
-        // per-row power-of-two scale 2^e (max |q| 2^e in [2^14, 2^15)), group sums
-        // (scale * log2(e) * sum_{d in g} q_d), the scaled rows in shared memory
-        // and from them the lane's score A-fragments
-        const float qscale = a.scale * kLog2e;
-        float *sE2 = sQS + REP * NG;   // 2^e per row
-#pragma unroll
-        for (int r = 0; r < REP; ++r) {
-            float qv[QPL];
-            float mx = 0.0f;
-#pragma unroll
-            for (int k = 0; k < QPL; ++k) {
-                qv[k] = t2f<T>(qraw[r][k]);
-                mx = fmaxf(mx, fabsf(qv[k]));
-            }
-#pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-            int e = 0;
-            if (mx > 0.0f) e = 14 - (static_cast<int>((__float_as_uint(mx) >> 23) & 0xffu) - 127);
-            const float e2 = ldexpf(1.0f, max(-100, min(100, e)));
-            if (lane == 0) sE2[r] = e2;
-#pragma unroll
-            for (int k = 0; k < QPL; ++k) sQF[r * DIMC + lane + 32 * k] = __float2half_rn(qv[k] * e2);
-#pragma unroll
-            for (int g = 0; g < NG; ++g) {   // element k is in group 32 k / GC
-                float x = 0.0f;
-#pragma unroll
-                for (int k = 0; k < QPL; ++k)
-                    if ((32 * k) / GC == g) x += qv[k];
-#pragma unroll
-                for (int m = 16; m >= 1; m >>= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-                if (lane == 0) sQS[r * NG + g] = qscale * x;
-            }
-        }
-        __syncwarp();
-        // A-fragment of accumulator set acc, K-block v for this lane: a0a1 (row
-        // gq, slots 0, 1), a2a3 (gq + 8, 0, 1), a4a5 (gq, 2, 3), a6a7 (gq + 8, 2, 3)
-#pragma unroll 1
-        for (int acc = 0; acc < NACC; ++acc)
-#pragma unroll 1
-            for (int v = 0; v < KB; ++v) {
-                uint32_t reg[4];
-#pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int m = gq + ((h & 1) ? 8 : 0);
-                    float val[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = (h >> 1) * 2 + e;
-                        float f;
-                        const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
-                        const int g = d / GC;
-                        const bool here = g / 4 == acc && (m >> 2) == g % 4;
-                        val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
-                    }
-                    reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
-                }
-                sQA[(acc * KB + v) * 32 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
-            }
-        __syncwarp();
-        // group sums of the row of this lane's score-bias entries (row = lane % 4)
+        for (; k_issued < NS && k_issued < nc; ++k_issued) ph.issue_k(smem, bars, kv, c_begin + k_issued, k_issued % NS);
+        const uint32_t tree_bits = ph.tree_bits();
+        const float alpha_l = ph.setup_scores(qraw);
         float qs_l[NG];
-#pragma unroll
-        for (int g = 0; g < NG; ++g) qs_l[g] = sQS[(lane & 3) * NG + g];
-        // score scale of row r: scale * log2(e) * 2^24 (subnormal codes) / 2^e
-        const float alpha_l = qscale * 16777216.0f / sE2[r_l];
-        // the lane's scale groups in the score fragments: c0/c1 rows gq, c2/c3 rows gq + 8
-        int grp_lo[NACC], grp_hi[NACC];
-#pragma unroll
-        for (int acc = 0; acc < NACC; ++acc) {
-            grp_lo[acc] = 4 * acc + (gq >> 2);
-            grp_hi[acc] = 4 * acc + 2 + (gq >> 2);
-        }
+        ph.bias_sums(qs_l);
 
         float Mrow = -INFINITY, Ssum = 0.0f;   // online softmax of row r_l (log2 units)
         for (int i = 0; i < nc && ok; ++i) {
             const int c = c_begin + i, b = i % NS, slot = i & 1;
-            if (!wait_warp(&bars[b], static_cast<uint32_t>(i / NS) & 1u, i == 0 ? first_polls : kQuantWaitPolls)) {
+            if (!wait_warp(&bars[b], static_cast<uint32_t>(i / NS) & 1u,
+                           i == 0 ? a.first_wait_polls : kQuantWaitPolls)) {
                 ok = false;
                 break;
             }
             const unsigned char *st = smem + L.a0 + b * L.a_stage;
-            const uint32_t *sK = reinterpret_cast<const uint32_t *>(st + L.k);
-            const uint16_t *sKs = reinterpret_cast<const uint16_t *>(st + L.ks);
-            const uint16_t *sKb = reinterpret_cast<const uint16_t *>(st + L.kb);
-            const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
-            const uint16_t *sMf = reinterpret_cast<const uint16_t *>(st + L.mf);
-            const int t0 = c * CH;
-            // gates of the lane's (row r_l, key) score slots: key 8 nb + 2 tq + e
             bool live[NB][2];
-            bool any = false;
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int tk = 8 * nb + 2 * tq + e;
-                    const int t = t0 + tk;
-                    bool g = r_l < nrow && t >= a.t_lo && t < N;
-                    if (MASKED && g && a.mbool != nullptr) g = sMb[r_l * CH + tk] != 0u;
-                    if (g && a.tree_ql > 0 && t >= tree_lo) g = (tree_bits >> (t - tree_lo)) & 1u;
-                    live[nb][e] = g;
-                    any |= g;
-                }
-            const bool chunk_live = __any_sync(0xffffffffu, any);
-
+            const bool chunk_live = ph.gates(st, c * CH, tree_bits, live);
             float lg[NB][2];
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb) lg[nb][0] = lg[nb][1] = -INFINITY;
             if (chunk_live) {
-                // K tables, each lane filling fixed entries with every load issued
-                // before the first store: scales in f32 [t][g], the score bias per
-                // (token, row) [t][r] (row = lane % 4)
-                {
-                    constexpr int NKS = (CH * NG + 31) / 32, NKB = CH * REP / 32;
-                    uint16_t ksr[NKS], kbr[NKB][NG];
-#pragma unroll
-                    for (int j = 0; j < NKS; ++j) {
-                        const int idx = lane + 32 * j;
-                        ksr[j] = idx < CH * NG ? sKs[idx] : static_cast<uint16_t>(0);
-                    }
-#pragma unroll
-                    for (int j = 0; j < NKB; ++j) {
-                        const int t = (lane + 32 * j) / REP;
-#pragma unroll
-                        for (int g = 0; g < NG; ++g) kbr[j][g] = sKb[t * NG + g];
-                    }
-#pragma unroll
-                    for (int j = 0; j < NKS; ++j)
-                        if (lane + 32 * j < CH * NG) sKsf[lane + 32 * j] = t2f<T>(ksr[j]);
-#pragma unroll
-                    for (int j = 0; j < NKB; ++j) {
-                        float x = 0.0f;
-#pragma unroll
-                        for (int g = 0; g < NG; ++g) x = fmaf(t2f<T>(kbr[j][g]), qs_l[g], x);
-                        sKbias[lane + 32 * j] = x;
-                    }
-                }
+                typename P::KRaw kr;
+                ph.k_load(st, kr);
+                ph.k_store(kr, qs_l);
                 __syncwarp();
-
-                // ---- scores: the lane's quarter of key 8 nb + gq, all K-blocks
-                uint32_t kw[NB][KW];
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                    const uint32_t *src = sK + (8 * nb + gq) * WPT + tq * KW;
-                    if constexpr (KW % 4 == 0) {
-#pragma unroll
-                        for (int u = 0; u < KW; u += 4) {
-                            const uint4 x = *reinterpret_cast<const uint4 *>(src + u);
-                            kw[nb][u] = x.x; kw[nb][u + 1] = x.y; kw[nb][u + 2] = x.z; kw[nb][u + 3] = x.w;
-                        }
-                    } else if constexpr (KW == 2) {
-                        const uint2 x = *reinterpret_cast<const uint2 *>(src);
-                        kw[nb][0] = x.x; kw[nb][1] = x.y;
-                    } else {
-#pragma unroll
-                        for (int u = 0; u < KW; ++u) kw[nb][u] = src[u];
-                    }
-                }
-                float sacc[NB][NACC][4];
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int acc = 0; acc < NACC; ++acc)
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) sacc[nb][acc][e] = 0.0f;
-#pragma unroll
-                for (int v = 0; v < KB; ++v) {
-                    uint4 af[NACC];
-#pragma unroll
-                    for (int acc = 0; acc < NACC; ++acc) af[acc] = sQA[(acc * KB + v) * 32 + lane];
-#pragma unroll
-                    for (int nb = 0; nb < NB; ++nb) {
-                        uint32_t b0, b1;
-                        if constexpr (BITS == 4) {
-                            // bytes (2, 3) or (0, 1) of the word into the two halves
-                            const uint32_t w = kw[nb][v / 2];
-                            const uint32_t y = __byte_perm(w, 0u, (v & 1) ? 0x3322u : 0x1100u);
-                            b0 = y & 0x000F000Fu;   // nibbles 0, 2 of the pair: code * 2^-24
-                            b1 = y & 0x00F000F0u;   // nibbles 1, 3: 16 * code * 2^-24
-                        } else {
-                            const uint32_t w = kw[nb][v];
-                            b0 = w & 0x00FF00FFu;               // bytes 0, 2
-                            b1 = __byte_perm(w, 0u, 0x4341u);   // bytes 1, 3
-                        }
-#pragma unroll
-                        for (int acc = 0; acc < NACC; ++acc)
-                            mma16816(sacc[nb][acc], af[acc].x, af[acc].y, af[acc].z, af[acc].w, b0, b1);
-                    }
-                }
-                // scale groups apart, then the two halves of the quad pair (lanes
-                // gq and gq ^ 4 hold the other groups of the same row)
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb)
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int tk = 8 * nb + 2 * tq + e;
-                        float x = 0.0f;
-#pragma unroll
-                        for (int acc = 0; acc < NACC; ++acc) {
-                            if (grp_lo[acc] < NG) x = fmaf(sKsf[tk * NG + grp_lo[acc]], sacc[nb][acc][e], x);
-                            if (NG > 2 && grp_hi[acc] < NG)
-                                x = fmaf(sKsf[tk * NG + grp_hi[acc]], sacc[nb][acc][2 + e], x);
-                        }
-                        x += __shfl_xor_sync(0xffffffffu, x, 16);
-                        if (live[nb][e]) {
-                            float v = fmaf(alpha_l, x, sKbias[tk * REP + r_l]);
-                            if (MASKED && a.mfloat != nullptr) v = fmaf(kLog2e, t2f<T>(sMf[r_l * CH + tk]), v);
-                            lg[nb][e] = v;
-                        }
-                    }
+                ph.scores(st, alpha_l, live, lg);
             }
             __syncwarp();
-            if (k_issued < nc) { issue_k(c_begin + k_issued, k_issued % NS); ++k_issued; }   // K tile read
-
-            // ---- online softmax of row r_l (log2 units), lazy running max: M
-            // only moves when a score exceeds it by more than kSlack
-            float alpha = 1.0f;
-            bool grow = false;
-#pragma unroll
-            for (int nb = 0; nb < NB; ++nb) grow |= lg[nb][0] > Mrow + kSlack || lg[nb][1] > Mrow + kSlack;
-            if (__any_sync(0xffffffffu, grow)) {
-                float cmax = -INFINITY;
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) cmax = fmaxf(cmax, fmaxf(lg[nb][0], lg[nb][1]));
-                cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 1));
-                cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, 2));
-                const float m_new = fmaxf(Mrow, cmax);
-                alpha = m_new == Mrow ? 1.0f : ex2(Mrow - m_new);   // 0 while M = -inf
-                Mrow = m_new;
-                Ssum *= alpha;
+            if (k_issued < nc) {   // this chunk's K tile is read
+                ph.issue_k(smem, bars, kv, c_begin + k_issued, k_issued % NS);
+                ++k_issued;
             }
-            uint32_t pf[VB][2];   // B fragments of P: lanes gq < 4 P_hi, gq >= 4 P_lo
+            float alpha;
+            ph.update_max(lg, Mrow, Ssum, alpha);
+            uint32_t pf[VB][2];
 #pragma unroll
             for (int kb = 0; kb < VB; ++kb) pf[kb][0] = pf[kb][1] = 0u;
-            if (chunk_live) {
-                const bool lo_term = gq >= 4;
-#pragma unroll
-                for (int nb = 0; nb < NB; ++nb) {
-                    float p[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        p[e] = Mrow == -INFINITY ? 0.0f : ex2(lg[nb][e] - Mrow);
-                        Ssum += p[e];
-                    }
-                    const __half2 hi = __floats2half2_rn(p[0], p[1]);
-                    uint32_t f = h2_bits(hi);
-                    if (lo_term) {
-                        const float2 hf = __half22float2(hi);
-                        f = h2_bits(__floats2half2_rn(p[0] - hf.x, p[1] - hf.y));
-                    }
-                    pf[nb >> 1][nb & 1] = f;
-                }
-            }
+            if (chunk_live) ph.p_frags(lg, Mrow, Ssum, pf);
             // hand P, the rescale factors and the liveness to warp 1
             if (!wait_warp(&p_empty[slot], (static_cast<uint32_t>(i >> 1) & 1u) ^ 1u)) {
                 ok = false;
@@ -1242,7 +932,7 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
                 ps.pf[kb][0][lane] = pf[kb][0];
                 ps.pf[kb][1][lane] = pf[kb][1];
             }
-            if (tq == 0 && gq < 4) ps.alpha[gq] = alpha;
+            if (tq == 0 && (lane >> 2) < 4) ps.alpha[lane >> 2] = alpha;
             if (lane == 0) ps.live = chunk_live ? 1 : 0;
             __syncwarp();
             if (lane == 0) mbar_arrive(&p_full[slot]);
@@ -1254,62 +944,28 @@ __global__ void __launch_bounds__(64, 8) quant_mma_kernel(const QuantArgs a) {
         // row statistics for the epilogue: S summed over the quad's keys
         Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 1);
         Ssum += __shfl_xor_sync(0xffffffffu, Ssum, 2);
-        if (tq == 0 && gq < 4) {
-            sML[gq] = Mrow;
-            sML[4 + gq] = Ssum;
+        if (tq == 0 && (lane >> 2) < 4) {
+            sML[lane >> 2] = Mrow;
+            sML[4 + (lane >> 2)] = Ssum;
         }
     }
     pdl_launch_dependents();   // the merge may start launching; it waits for this grid to finish
     __syncthreads();
     if (*sAbort != 0) return;
-
     if (warp == 0) {
         if (a.nwg > 1 && lane < nrow)
             reinterpret_cast<float2 *>(a.part_ml)[static_cast<size_t>(split) * a.rows + q0 + lane] =
                 make_float2(sML[4 + lane], sML[lane]);
         return;
     }
-    // ---- warp 1: O^T columns P_hi + P_lo (tq, tq + 2); lanes tq 0, 1 hold rows
-    // 2 tq, 2 tq + 1: c0 / c2 row 2 tq, c1 / c3 row 2 tq + 1
+    float Mr[2], Sr[2];
 #pragma unroll
-    for (int mb = 0; mb < KB; ++mb)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) O[mb][e] += __shfl_xor_sync(0xffffffffu, O[mb][e], 2);
-    if (tq < 2) {
-#pragma unroll
-        for (int k = 0; k < 2; ++k) {
-            const int r = 2 * tq + k;
-            if (r >= nrow) continue;
-            const int q = q0 + r;
-            const float Mr = sML[r], Sr = sML[4 + r];
-            float f = 1.0f;
-            if (a.nwg == 1) {
-                float cs = 1.0f, sf = Sr;
-                if (a.has_sinks) {
-                    const float sk = kLog2e * __ldg(a.sinks + (q % a.nQ));
-                    const float mf = fmaxf(Mr, sk);
-                    cs = Mr == -INFINITY ? 0.0f : ex2(Mr - mf);
-                    sf = Sr * cs + ex2(sk - mf);
-                }
-                f = sf > 0.0f ? cs / sf : 0.0f;
-            }
-#pragma unroll
-            for (int mb = 0; mb < KB; ++mb) {
-                // M row gq of block mb: the low code of its byte, M row gq + 8 the next dimension
-                int d;
-                if constexpr (BITS == 4) d = 8 * (gq * VW + (mb >> 2)) + 2 * (mb & 3);
-                else d = 4 * (gq * VW + (mb >> 1)) + 2 * (mb & 1);
-                const float x0 = O[mb][k], x1 = O[mb][2 + k];
-                if (a.nwg == 1) {
-                    st_out<T>(a.out, static_cast<size_t>(q) * DIMC + d, x0 * f, a.out_f32);
-                    st_out<T>(a.out, static_cast<size_t>(q) * DIMC + d + 1, x1 * f, a.out_f32);
-                } else {
-                    *reinterpret_cast<float2 *>(a.part_o + (static_cast<size_t>(split) * a.rows + q) * DIMC + d) =
-                        make_float2(x0, x1);
-                }
-            }
-        }
+    for (int k = 0; k < 2; ++k) {
+        const int r = (2 * tq + k) & 3;
+        Mr[k] = sML[r];
+        Sr[k] = sML[4 + r];
     }
+    ph.write_out(O, Mr, Sr, split);
 }
 
 template <int BITS, int DIMC, int GC>
