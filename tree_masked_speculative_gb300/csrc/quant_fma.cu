@@ -134,10 +134,10 @@ int quant_mma_ctas_per_sm(int bits, int dim, int ng) {
     int n = 0;
     if (bits == 4) n = quant_mma_ctas_per_sm_b4(dim, ng);
     if (bits == 8) n = quant_mma_ctas_per_sm_b8(dim, ng);
-    // the two-warp form (more than 16 packed words per token) measured fastest
+    // the two-warp form (more than 32 packed words per token) measured fastest
     // with its splits sized for 6 CTAs per SM (8-bit workload: 47.0 us at 6,
     // 48.7 at 7)
-    if (dim * bits / 32 > 16 && n > kQmmaTwoWarpCtasPerSm) n = kQmmaTwoWarpCtasPerSm;
+    if (dim * bits / 32 > 32 && n > kQmmaTwoWarpCtasPerSm) n = kQmmaTwoWarpCtasPerSm;
     return n;
 }
 

@@ -110,11 +110,14 @@ __host__ __device__ inline QmmaLayout qmma_layout(int wpt, int ng, int ch, int d
 
 // Staged chunks in flight (each chunk's K, scale / bias runs, masks and V).
 constexpr int kQmmaStages = 2;
-// Kernel form of a shape: one warp per CTA up to 16 packed words per token
-// (quant_mma1_kernel), else two (quant_mma_kernel); each measured faster there.
+// Kernel form of a shape: one warp per CTA up to 32 packed words per token
+// (quant_mma1_kernel), else two (quant_mma_kernel); each measured faster there
+// (at 32 words the one-warp form took 34.8 against 39.2 us on an 8-bit dim-128
+// workload, 54.7 against 55.8 on a 4-bit dim-256 one, and 26.9 against 26.2
+// with both masks; at 64 words the two-warp form wins).
 template <int WPTC>
 struct QmmaForm {
-    static constexpr bool one_warp = WPTC <= 16;
+    static constexpr bool one_warp = WPTC <= 32;
     static constexpr int threads = one_warp ? 32 : 64;
 };
 
@@ -660,7 +663,7 @@ struct QmmaPhases {
     }
 };
 
-// One-warp form (shapes of up to 16 packed words per token, where it measured
+// One-warp form (shapes of up to 32 packed words per token, where it measured
 // faster than the two-warp form): one warp per CTA does every phase of a chunk
 // in turn and issues every copy itself.
 template <int BITS, typename T, int DIMC, int GC, bool MASKED>
