@@ -12,8 +12,11 @@
 // a multiply-add per query row, which for 4 rows keeps the FP32 pipe busier
 // than HBM.  Here the multiply-adds go to the tensor core, whose rate dwarfs
 // what 4 rows need, and a code costs about one integer instruction to decode.
-// One warp per CTA, the same work split and chunk staging as quant_kernel.cuh
-// (lane = quad gq = lane / 4 and position tq = lane % 4 in the MMA fragments):
+// The same work split (a CTA per KV row, row group of 4 query rows and token
+// split) and chunk staging as quant_kernel.cuh, in two forms: one warp doing
+// every phase (up to 32 packed words per token) or a score warp handing P to a
+// value warp (wider tokens).  In the MMA fragments lane = quad gq = lane / 4
+// and position tq = lane % 4:
 //  * scores S = Q K^T per chunk: A = Q (M = 16 rows: query row r of a
 //    dimension in scale group g sits in row 4 * (g % 4) + r, so one MMA keeps
 //    the partial sums of four groups apart), held as f16 scaled per row by a
