@@ -241,6 +241,34 @@ def test_bounded_wait_timeout_sets_status_and_returns(ta):
     assert ta.ta_launch_count() == before
 
 
+def test_bounded_wait_timeout_two_warp_form(ta):
+    """The same failure path on the warp-MMA kernel's two-warp form (64 packed
+    words per token; with and without masks): both warps give up at their
+    first wait, the value warp lets every copy it issued land, and the CTA
+    leaves through its final barrier with the status set."""
+    assert ta.quant_sdpa_kernel_family(ta.quant_params(1, 8, 2, 256, 640, 8, 64, 0, 0, 0.1, 0, 3)) == \
+        ta.KERNEL_WARP_MMA
+    for fmask, bfrac in (("none", 0.0), ("alibi", 0.1)):
+        wl = qwl(B=2, nQ=8, nKV=2, dim=256, N=640, bits=8, G=64, sinks=0, dtype="bf16", fmask=fmask, bfrac=bfrac)
+        inp = W.make_quant_inputs(wl)
+        d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        for nwg in (1, 0):
+            p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits, wl.group_size,
+                                wl.has_sinks, wl.window_size, wl.scale, nwg, 3)
+            tmp = torch.zeros((ta.quant_sdpa_tmp_bytes(p) + 3) // 4, dtype=torch.float32, device="cuda")
+            out = torch.zeros((wl.rows, wl.dim), dtype=torch.float32, device="cuda")
+            args = (d["queries"], d["k_packed"], d["k_scales"], d["k_biases"], d["v_packed"], d["v_scales"],
+                    d["v_biases"], None, d.get("mask_bool"), d.get("mask_float"), tmp, out)
+            ta.ta_test_quant_sdpa_fwd_wait_limit(0, p, *args)
+            torch.cuda.synchronize()
+            assert int(tmp[:1].view(torch.int32).item()) & 1 == 1
+            tmp.zero_()
+            ta.quant_sdpa_fwd(p, *args)
+            torch.cuda.synchronize()
+            assert int(tmp[:1].view(torch.int32).item()) == 0
+            assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp), what="two-warp, after a timeout")
+
+
 TREE_CASES = [
     # q_l, bits, dtype, dim, G, N, window, bool fraction, sinks, heads per KV row
     (8, 4, "f16", 128, 64, 700, 0, 0.0, 0, 4),      # 32 rows per KV row
