@@ -129,8 +129,7 @@ __host__ __device__ inline int qmma_nacc(int ng) { return (ng + 3) / 4; }
 
 // The phases of a warp-MMA chunk, shared by the one-warp and the two-warp
 // forms (each a warp's view: lane = quad gq, position tq).  MASKED: the call
-// passes a bool or a float mask (instances without one carry no mask code and
-// stage every chunk through the lanes' cp.async).
+// passes a bool or a float mask (instances without one carry no mask code).
 template <int BITS, typename T, int DIMC, int GC, bool MASKED>
 struct QmmaPhases {
     using S = MmaShape<BITS, DIMC>;
@@ -578,14 +577,15 @@ struct QmmaPhases {
         }
     }
 
-    // Copies of a chunk's runs.  A full chunk whose runs are 16-byte aligned,
-    // in a call with a mask: one bulk copy per run, each issued by a lane of its
-    // own in the same instruction - lane 0 the K words (when this warp copies
-    // them), lanes 1-4 the K / V scale and bias runs, then one lane per
-    // bool-mask and float-mask row - after lane 0 has posted the byte count;
-    // the lanes' cp.async arrivals then complete at once.  Other chunks (and
-    // calls without a mask, where the many small bulk copies measured slower
-    // than the lanes' 16-byte cp.async) take the staging of quant_kernel.cuh.
+    // Copies of a chunk's runs.  A full chunk whose runs are 16-byte aligned:
+    // one bulk copy per run, each issued by a lane of its own in the same
+    // instruction - lane 0 the K words (when this warp copies them), lanes 1-4
+    // the K / V scale and bias runs, then one lane per bool-mask and float-mask
+    // row - after lane 0 has posted the byte count; the lanes' cp.async
+    // arrivals then complete at once (measured against the lanes' 16-byte
+    // cp.async of the runs: 28.4 against 28.3 us on the 4-bit dim-128 workload,
+    // 34.0 against 34.7 on an 8-bit dim-128 one, 52.6 against 54.6 on a 4-bit
+    // dim-256 one).  Other chunks take the staging of quant_kernel.cuh.
     struct CopyPlan {
         const unsigned char *src;   // this lane's run at token 0 (nullptr: none)
         uint32_t stride, bytes, dst, tx;
@@ -593,7 +593,7 @@ struct QmmaPhases {
     };
     __device__ __forceinline__ CopyPlan copy_plan(int kv, bool with_k) const {
         CopyPlan cp{nullptr, 0u, 0u, 0u, 0u, false, with_k};
-        if constexpr (MASKED) {
+        {
             cp.bulk = a.al_sb && (a.mbool == nullptr || a.al_mb) && (a.mfloat == nullptr || a.al_mf);
             const size_t kv0 = static_cast<size_t>(kv) * N;
             const int nb_rows = a.mbool != nullptr ? nrow : 0, nf_rows = a.mfloat != nullptr ? nrow : 0;
@@ -629,7 +629,7 @@ struct QmmaPhases {
     __device__ __forceinline__ void issue_runs(const CopyPlan &cp, const QuantStager<CH> &stg, unsigned char *smem,
                                                uint64_t *bars, int c, int b) const {
         const int t0 = c * CH;
-        if (MASKED && cp.bulk && t0 + CH <= N) {
+        if (cp.bulk && t0 + CH <= N) {
             unsigned char *st = smem + L.a0 + b * L.a_stage;
             if (lane == 0) {
                 if (cp.with_k) mbar_arrive_expect_tx(&bars[b], cp.tx);
