@@ -63,21 +63,6 @@ struct MmaShape {
     static_assert(KW >= 1 && VW >= 1 && CH % 16 == 0, "shape");
 };
 
-// Dimension and factor of score K-block v, lane position tq, k-slot j
-// (slots 0..3 = k 2tq, 2tq+1, 2tq+8, 2tq+9) for the K decode below.
-template <int BITS, int KW>
-__host__ __device__ inline int mma_k_dim(int v, int tq, int j, float *factor) {
-    if (BITS == 4) {
-        const int w = tq * KW + v / 2;
-        const int n = 4 * (v % 2) + (j == 0 ? 0 : j == 1 ? 2 : j == 2 ? 1 : 3);
-        *factor = j >= 2 ? 1.0f / 16.0f : 1.0f;   // high nibbles are decoded as 16 * code
-        return 8 * w + n;
-    }
-    const int w = tq * KW + v;
-    *factor = 1.0f;
-    return 4 * w + (j == 0 ? 0 : j == 1 ? 2 : j == 2 ? 1 : 3);
-}
-
 // Shared-memory layout: the two staging groups of quant_layout, then the
 // kernel's own arrays.
 struct QmmaLayout {
@@ -206,26 +191,35 @@ struct QmmaPhases {
             }
         }
         __syncwarp();
-        // setup code runs once per CTA: kept rolled (little code to fetch cold)
+        // The lane's k-slots of K-block v (k = 2 tq, 2 tq + 1, 2 tq + 8,
+        // 2 tq + 9) are four consecutive dimensions d0 .. d0 + 3 of one scale
+        // group, the codes the K decode puts there (4-bit: nibbles 4 (v % 2) ..
+        // of word tq KW + v / 2; 8-bit: word tq KW + v): slots 0, 1 = d0,
+        // d0 + 2 and slots 2, 3 = d0 + 1, d0 + 3 (for 4-bit codes the high
+        // nibbles, decoded as 16 * code, so q / 16 there).  One 8-byte load per
+        // M row.  Setup code runs once per CTA: the acc loop stays rolled
+        // (little code to fetch cold).
+        constexpr float fhi = BITS == 4 ? 1.0f / 16.0f : 1.0f;
 #pragma unroll 1
         for (int acc = 0; acc < NACC; ++acc)
-#pragma unroll 1
+#pragma unroll 4
             for (int v = 0; v < KB; ++v) {
+                const int d0 = BITS == 4 ? 8 * (tq * KW + v / 2) + 4 * (v % 2) : 4 * (tq * KW + v);
+                const int g = d0 / GC;
                 uint32_t reg[4];
 #pragma unroll
-                for (int h = 0; h < 4; ++h) {
-                    const int m = gq + ((h & 1) ? 8 : 0);
-                    float val[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int j = (h >> 1) * 2 + e;
-                        float f;
-                        const int d = mma_k_dim<BITS, KW>(v, tq, j, &f);
-                        const int g = d / GC;
-                        const bool here = g / 4 == acc && (m >> 2) == g % 4;
-                        val[e] = here ? __half2float(sQF[(m & 3) * DIMC + d]) * f : 0.0f;
+                for (int hr = 0; hr < 2; ++hr) {   // M row gq, then gq + 8
+                    const int m = gq + 8 * hr;
+                    uint2 x = make_uint2(0u, 0u);
+                    if (g / 4 == acc && (m >> 2) == g % 4)
+                        x = *reinterpret_cast<const uint2 *>(sQF + (m & 3) * DIMC + d0);
+                    reg[hr] = __byte_perm(x.x, x.y, 0x5410u);   // (d0, d0 + 2)
+                    if constexpr (BITS == 4) {
+                        const float2 lo = __half22float2(bits_h2(x.x)), hi = __half22float2(bits_h2(x.y));
+                        reg[2 + hr] = h2_bits(__floats2half2_rn(lo.y * fhi, hi.y * fhi));   // (d0 + 1, d0 + 3) / 16
+                    } else {
+                        reg[2 + hr] = __byte_perm(x.x, x.y, 0x7632u);   // (d0 + 1, d0 + 3)
                     }
-                    reg[h] = h2_bits(__floats2half2_rn(val[0], val[1]));
                 }
                 sQA[(acc * KB + v) * 32 + lane] = make_uint4(reg[0], reg[1], reg[2], reg[3]);
             }
