@@ -299,6 +299,9 @@ class QuantBench:
                ta.KERNEL_WARP_MMA: ("quant_mma_kernel (warp MMA tensor cores)", "warp MMA tensor cores"),
                ta.KERNEL_CUDA_CORES: ("quant_kernel (CUDA cores)", "CUDA cores")}
         kern, self.family_name = fam[self.family]
+        rep = wl.n_q_heads // wl.n_kv_heads
+        if self.family == ta.KERNEL_WARP_MMA and rep >= 16 and wl.dim in (64, 128) and wl.group_size in (32, 64):
+            kern = "quant_mma16_kernel (warp MMA tensor cores, 16 rows per warp)"
         call = "quant_sdpa_fwd_tree" if self.tree is not None else "quant_sdpa_fwd"
         self.fwd_label = "main pass (%s) + split merge (%s, one call)" % (kern, call)
         self.traffic_key = traffic_key(wl.name, self.tree is not None, kernel)

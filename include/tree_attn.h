@@ -375,8 +375,11 @@ uint64_t ta_launch_count(void);
  * TA_KERNEL_CUDA_CORES; -1 for invalid params.  No device work.
  *
  * The warp-MMA kernel serves head dimensions 64, 128 and 256 with group size
- * 32 or 64, four query rows per CTA.  With TA_KERNEL_AUTO it is chosen below
- * 16 query rows per KV row (and wherever the tcgen05 kernel's rules fail): its
+ * 32 or 64, four query rows per CTA; from 16 query rows per KV row, with head
+ * dimension 64 or 128, it runs 16 query rows per CTA instead (its wide form,
+ * each score MMA within one scale group).  With TA_KERNEL_AUTO it is chosen
+ * below 16 query rows per KV row, from 16 rows where the wide form takes the
+ * shape, and wherever the tcgen05 kernel's rules fail: its
  * scores multiply the exact K codes with Q scaled per row by a power of two
  * into f16 (the group scales and biases are applied to the f32 sums), and P V
  * takes V dequantized once to f16 (s * code + b, one rounding) and P as two
@@ -394,7 +397,8 @@ int quant_sdpa_kernel_family(const ta_quant_params *p);
  * holds O (dim f32 columns) and two score buffers (dim / group_size groups x
  * 16 or 32 query rows each) and its shared-memory layout fits.  With
  * TA_KERNEL_AUTO it is chosen from 16 query rows per KV row (e.g. draft-tree
- * nodes as rows).  It feeds the tensor core the exact integer codes of K (the
+ * nodes as rows) for the shapes the warp-MMA kernel's wide form does not take
+ * (head dimension 256, group size other than 32 or 64).  It feeds the tensor core the exact integer codes of K (the
  * per-group scales and biases are applied to the f32 scores), V dequantized
  * once to f16 (s * code + b, one rounding) and the weights P as two f16 terms
  * (P_hi + P_lo); Q is scaled per row by a power of two into f16 (exact for

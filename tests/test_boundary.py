@@ -359,7 +359,10 @@ def test_quant_kernel_family_choice(ta):
     fam = ta.quant_sdpa_kernel_family
     TC, MMA, CC = ta.KERNEL_TENSOR_CORES, ta.KERNEL_WARP_MMA, ta.KERNEL_CUDA_CORES
     assert fam(p(128)) == MMA                 # 4 rows per KV row: warp MMA
-    assert fam(p(128, nQ=128)) == TC          # 16 rows per KV row: tcgen05
+    assert fam(p(128, nQ=128)) == MMA         # 16 rows per KV row, dim 128: the warp-MMA wide form
+    assert fam(p(64, G=32, nQ=256)) == MMA    # 32 rows per KV row, dim 64
+    assert fam(p(256, nQ=128)) == TC          # 16 rows per KV row, dim 256: tcgen05
+    assert fam(p(128, G=128, nQ=128)) == TC   # group size 128: tcgen05
     assert fam(p(512, nQ=256)) == CC          # neither tensor-core kernel takes dim 512
     assert fam(p(96, G=32)) == CC             # warp MMA: dims 64, 128, 256 only
     assert fam(p(128, G=128)) == CC           # warp MMA: group size 32 or 64 only

@@ -58,6 +58,12 @@ QCASES = [
     dict(dim=256, G=32, bits=4, N=300, nwg=3),
     dict(dim=256, G=32, bits=8, N=256, fmask="alibi", bfrac=0.1, dtype="bf16"),
     dict(dim=128, G=32, bits=8, nQ=12, nKV=2, N=320, window=150),   # 6 rows per KV row: a partial row group
+    # 16 or more query rows per KV row: the warp-MMA kernel's wide form (16 rows per warp)
+    dict(nQ=40, nKV=2, N=300, window=120),                                  # 20 rows: a partial 16-row group
+    dict(nQ=32, nKV=2, N=256, dim=64, G=64, fmask="alibi"),                 # 16 float-mask rows by bulk copies
+    dict(nQ=32, nKV=1, N=512, bits=8, G=32, dtype="bf16", bfrac=0.2),       # 32 rows, bool-mask rows by bulk copies
+    dict(nQ=32, nKV=2, N=512, bits=8, fmask="alibi", bfrac=0.1, nwg=1),     # both masks (32 rows): lanes' cp.async
+    dict(nQ=64, nKV=2, N=190, dim=64, G=32, bits=8, sinks=1, nwg=2),        # 32 rows, ragged last chunk
 ]
 
 
@@ -267,6 +273,31 @@ def test_bounded_wait_timeout_two_warp_form(ta):
             torch.cuda.synchronize()
             assert int(tmp[:1].view(torch.int32).item()) == 0
             assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp), what="two-warp, after a timeout")
+
+
+def test_bounded_wait_timeout_wide_form(ta):
+    """The same failure path on the warp-MMA kernel's wide form (16 query rows
+    per warp), with its copies by bulk copies (float mask) and by the lanes'
+    cp.async (both masks on 16 rows)."""
+    for fmask, bfrac in (("none", 0.0), ("alibi", 0.0), ("alibi", 0.2)):
+        wl = qwl(B=2, nQ=32, nKV=2, dim=128, N=1024, bits=4, G=64, sinks=1, dtype="f16", fmask=fmask, bfrac=bfrac)
+        inp = W.make_quant_inputs(wl)
+        d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in inp.items()}
+        for nwg in (1, 0):
+            p = ta.quant_params(wl.batch, wl.n_q_heads, wl.n_kv_heads, wl.dim, wl.tokens, wl.bits, wl.group_size,
+                                wl.has_sinks, wl.window_size, wl.scale, nwg, 3)
+            tmp = torch.zeros((ta.quant_sdpa_tmp_bytes(p) + 3) // 4, dtype=torch.float32, device="cuda")
+            out = torch.zeros((wl.rows, wl.dim), dtype=torch.float32, device="cuda")
+            args = (d["queries"], d["k_packed"], d["k_scales"], d["k_biases"], d["v_packed"], d["v_scales"],
+                    d["v_biases"], d["sinks"], d.get("mask_bool"), d.get("mask_float"), tmp, out)
+            ta.ta_test_quant_sdpa_fwd_wait_limit(0, p, *args)
+            torch.cuda.synchronize()
+            assert int(tmp[:1].view(torch.int32).item()) & 1 == 1
+            tmp.zero_()
+            ta.quant_sdpa_fwd(p, *args)
+            torch.cuda.synchronize()
+            assert int(tmp[:1].view(torch.int32).item()) == 0
+            assert_close(out.cpu().double().numpy(), oracle.quant_oracle_for(wl, inp), what="wide form, after a timeout")
 
 
 TREE_CASES = [

@@ -433,9 +433,16 @@ uint32_t quant_chunks(const ta_quant_params *p) {
     return (p->tokens + c - 1u) / c - t_lo / c;
 }
 
+int quant_fallback_family(const ta_quant_params *p);
+
+// Row groups per KV row of the CUDA-core or warp-MMA kernel (whichever the
+// call runs when the tcgen05 kernel does not take it).
 uint32_t quant_row_groups(const ta_quant_params *p) {
     const uint32_t rep = p->n_q_heads / p->n_kv_heads;
-    return (rep + (uint32_t)kQuantRowsPerCta - 1) / (uint32_t)kQuantRowsPerCta;
+    const uint32_t rows = quant_fallback_family(p) == TA_KERNEL_WARP_MMA
+                              ? (uint32_t)quant_mma_rows((int)rep, (int)p->dim, (int)p->group_size)
+                              : (uint32_t)kQuantRowsPerCta;
+    return (rep + rows - 1) / rows;
 }
 
 // Tensor-core quantized kernel: shape rules (params only, so that the split
@@ -452,8 +459,12 @@ bool quant_tc_shape(const ta_quant_params *p, QtcShape *sh) {
     if (p->dim != 64 && p->dim != 128 && p->dim != 256) return false;
     const int rep = (int)(p->n_q_heads / p->n_kv_heads);
     // automatic choice: the tensor-core kernel from 16 query rows per KV row
-    // (draft-tree verification), where the CUDA-core kernel's per-row work dominates
+    // (draft-tree verification), where the CUDA-core kernel's per-row work
+    // dominates, unless the warp-MMA kernel's wide form (16 rows per warp) takes
+    // the shape: it measured faster there (4-bit draft tree of 256 rows on 8 KV
+    // heads, dim 128: 29.4 against 41.4 us; 8-bit: 35.0 against 49.7)
     if (path == TA_KERNEL_AUTO && rep < kQuantTcMinRows) return false;
+    if (path == TA_KERNEL_AUTO && quant_mma_wide(rep, (int)p->dim, (int)p->group_size)) return false;
     const int ng = (int)(p->dim / p->group_size);
     const int wpt = (int)(p->dim * p->bits / 32);
     if (wpt % 4 != 0 || p->group_size % 16 != 0) return false;
@@ -545,7 +556,8 @@ uint32_t resolve_quant_nwg(const ta_quant_params *p) {
     }
     const int ng = (int)(p->dim / p->group_size);
     const int per_sm = quant_fallback_family(p) == TA_KERNEL_WARP_MMA
-                           ? quant_mma_ctas_per_sm((int)p->bits, (int)p->dim, ng)
+                           ? quant_mma_ctas_per_sm((int)p->bits, (int)p->dim, ng,
+                                                   (int)(p->n_q_heads / p->n_kv_heads))
                            : quant_ctas_per_sm((int)p->bits, (int)p->dim, ng);
     if (per_sm <= 0) return 0;
     const uint64_t units = (uint64_t)p->batch * p->n_kv_heads * quant_row_groups(p);

@@ -122,15 +122,31 @@ bool quant_mma_shape_ok(int dim, int group_size) {
     return (dim == 64 || dim == 128 || dim == 256) && (group_size == 32 || group_size == 64);
 }
 
+bool quant_mma_wide(int rep, int dim, int group_size) {
+    return rep >= 16 && (dim == 64 || dim == 128) && (group_size == 32 || group_size == 64);
+}
+
+int quant_mma_rows(int rep, int dim, int group_size) { return quant_mma_wide(rep, dim, group_size) ? 16 : 4; }
+
 cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s) {
     if (!quant_mma_shape_ok(a.dim, a.G)) return cudaErrorInvalidValue;
+    if (quant_mma_wide(a.rep, a.dim, a.G)) {
+        if (a.bits == 4) return launch_quant_mma16_b4(a, s);
+        if (a.bits == 8) return launch_quant_mma16_b8(a, s);
+        return cudaErrorInvalidValue;
+    }
     if (a.bits == 4) return launch_quant_mma_b4(a, s);
     if (a.bits == 8) return launch_quant_mma_b8(a, s);
     return cudaErrorInvalidValue;
 }
 
-int quant_mma_ctas_per_sm(int bits, int dim, int ng) {
+int quant_mma_ctas_per_sm(int bits, int dim, int ng, int rep) {
     if (ng <= 0 || !quant_mma_shape_ok(dim, dim / ng)) return 0;
+    if (quant_mma_wide(rep, dim, dim / ng)) {
+        if (bits == 4) return quant_mma16_ctas_per_sm_b4(dim, ng);
+        if (bits == 8) return quant_mma16_ctas_per_sm_b8(dim, ng);
+        return 0;
+    }
     int n = 0;
     if (bits == 4) n = quant_mma_ctas_per_sm_b4(dim, ng);
     if (bits == 8) n = quant_mma_ctas_per_sm_b8(dim, ng);

@@ -63,6 +63,48 @@ struct MmaShape {
     static_assert(KW >= 1 && VW >= 1 && CH % 16 == 0, "shape");
 };
 
+// A fragment of V^T for value M-block mb (16 dimensions) and one 16-token
+// block: w[k][u] are the lane's V words u of the block's tokens T0, T1 (k 0,
+// 1) and T2, T3 (k 2, 3); sbA[u] / sbB[u] the f16 {s, s} / {b, b} pairs of
+// (T0, T1) / (T2, T3) in word u's scale group.  Each register pairs two
+// tokens' codes of one dimension (a byte permute), made f16 by an OR under the
+// exponent of 1024 (low nibble or byte) or 64 (high nibble), then s * c + b
+// rounded once.  ar: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq,
+// T2 T3), a6a7 (gq + 8, T2 T3); row gq is the lower code of its byte (4-bit)
+// or byte 2 (mb % 2) (8-bit), row gq + 8 the next dimension.
+template <int BITS, int VW>
+__device__ __forceinline__ void qmma_v_frag(const uint32_t (&w)[4][VW], const uint2 (&sbA)[VW],
+                                            const uint2 (&sbB)[VW], int mb, uint32_t (&ar)[4]) {
+    const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
+    if constexpr (BITS == 4) {
+        const int u = mb >> 2, bi = mb & 3;
+        const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
+            const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
+            const uint2 sb = hb ? sbB[u] : sbA[u];
+            const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
+            const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
+            ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
+            ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // M row gq + 8
+        }
+    } else {
+        const int u = mb >> 1, b0 = 2 * (mb & 1);
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+            const uint2 sb = hb ? sbB[u] : sbA[u];
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
+                const int bi = b0 + hr;
+                const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
+                const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
+                const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
+                ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
+            }
+        }
+    }
+}
+
 // Shared-memory layout: the two staging groups of quant_layout, then the
 // kernel's own arrays.
 struct QmmaLayout {
@@ -488,38 +530,10 @@ struct QmmaPhases {
                 sbA[u] = sVSB[vgrp[u] * (CH / 2) + tA / 2];
                 sbB[u] = sVSB[vgrp[u] * (CH / 2) + tB / 2];
             }
-            const __half2 k1024 = __float2half2_rn(1024.0f), k64 = __float2half2_rn(64.0f);
 #pragma unroll
             for (int mb = 0; mb < KB; ++mb) {
                 uint32_t ar[4];
-                if constexpr (BITS == 4) {
-                    const int u = mb >> 2, bi = mb & 3;
-                    const uint32_t sel = static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {   // tokens (T0, T1), then (T2, T3)
-                        const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                        const uint2 sb = hb ? sbB[u] : sbA[u];
-                        const __half2 clo = __hsub2(bits_h2((y & 0x000F000Fu) | 0x64006400u), k1024);
-                        const __half2 chi = __hsub2(bits_h2((y & 0x00F000F0u) | 0x54005400u), k64);
-                        ar[2 * hb] = h2_bits(__hfma2(clo, bits_h2(sb.x), bits_h2(sb.y)));       // M row gq
-                        ar[2 * hb + 1] = h2_bits(__hfma2(chi, bits_h2(sb.x), bits_h2(sb.y)));   // M row gq + 8
-                    }
-                } else {
-                    const int u = mb >> 1, b0 = 2 * (mb & 1);
-#pragma unroll
-                    for (int hb = 0; hb < 2; ++hb) {
-                        const uint2 sb = hb ? sbB[u] : sbA[u];
-#pragma unroll
-                        for (int hr = 0; hr < 2; ++hr) {   // byte b0 -> M row gq, b0 + 1 -> gq + 8
-                            const int bi = b0 + hr;
-                            const uint32_t sel =
-                                static_cast<uint32_t>(bi | (bi << 4) | ((4 + bi) << 8) | ((4 + bi) << 12));
-                            const uint32_t y = __byte_perm(w[2 * hb][u], w[2 * hb + 1][u], sel);
-                            const __half2 cc = __hsub2(bits_h2((y & 0x00FF00FFu) | 0x64006400u), k1024);
-                            ar[2 * hb + hr] = h2_bits(__hfma2(cc, bits_h2(sb.x), bits_h2(sb.y)));
-                        }
-                    }
-                }
+                qmma_v_frag<BITS, VW>(w, sbA, sbB, mb, ar);
                 // A regs: a0a1 (row gq, T0 T1), a2a3 (gq + 8, T0 T1), a4a5 (gq, T2 T3), a6a7 (gq + 8, T2 T3)
                 mma16816(O[mb], ar[0], ar[1], ar[2], ar[3], pf[kb][0], pf[kb][1]);
             }

@@ -230,9 +230,11 @@ __host__ __device__ inline int quant_take(int *o, int bytes) {
     *o += (bytes + 15) & ~15;
     return r;
 }
-// ns: stages of each group (the CUDA-core kernel uses two).
-__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch, int ns = 2) {
-    constexpr int R = kQuantRowsPerCta;
+// ns: stages of each group (the CUDA-core kernel uses two); rows: query rows
+// whose mask rows a stage holds.
+__host__ __device__ inline QuantLayout quant_layout(int wpt, int ng, int ch, int ns = 2,
+                                                    int rows = kQuantRowsPerCta) {
+    const int R = rows;
     QuantLayout L;
     int o = 0;   // inside a group-A stage
     L.k = quant_take(&o, ch * wpt * 4);
@@ -396,14 +398,23 @@ int quant_tc_ctas_per_sm_b8(int rp, size_t smem);
 // Warp-MMA quantized-KV kernel (mma.sync, one warp per CTA, 4 query rows):
 // head dimension 64, 128 or 256 exactly and group size 32 or 64.
 bool quant_mma_shape_ok(int dim, int group_size);
+// Its wide form (16 query rows per warp, quant_mma16.cuh): from 16 query rows
+// per KV row, head dimension 64 or 128, group size 32 or 64.
+bool quant_mma_wide(int rep, int dim, int group_size);
+// Query rows of one warp-MMA CTA for rep rows per KV row (4, or 16 in the wide form).
+int quant_mma_rows(int rep, int dim, int group_size);
 // CTAs per SM the two-warp form's split count is sized for (at most).
 constexpr int kQmmaTwoWarpCtasPerSm = 6;
 cudaError_t launch_quant_mma(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_mma_b4(const QuantArgs &a, cudaStream_t s);
 cudaError_t launch_quant_mma_b8(const QuantArgs &a, cudaStream_t s);
-int quant_mma_ctas_per_sm(int bits, int dim, int ng);
+cudaError_t launch_quant_mma16_b4(const QuantArgs &a, cudaStream_t s);
+cudaError_t launch_quant_mma16_b8(const QuantArgs &a, cudaStream_t s);
+int quant_mma_ctas_per_sm(int bits, int dim, int ng, int rep);
 int quant_mma_ctas_per_sm_b4(int dim, int ng);
 int quant_mma_ctas_per_sm_b8(int dim, int ng);
+int quant_mma16_ctas_per_sm_b4(int dim, int ng);
+int quant_mma16_ctas_per_sm_b8(int dim, int ng);
 
 // Rows of one CTA in the CUDA-core tree kernel.
 constexpr int kFmaRowsPerCta = 16;
