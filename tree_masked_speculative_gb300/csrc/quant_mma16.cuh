@@ -296,7 +296,17 @@ __global__ void __launch_bounds__(32, 8) quant_mma16_kernel(const QuantArgs a) {
         // gates of the lane's slots: [nb][e] = (row gq + 8 (e >> 1), key 8 nb + 2 tq + (e & 1))
         bool live[NB][4];
         bool any = false;
-        {
+        // a chunk inside the window, before the draft-tree positions and without a
+        // bool mask keeps every key of the CTA's rows (the common case)
+        const bool plain = !(MASKED && a.mbool != nullptr) && t0 >= a.t_lo && t0 + CH <= N &&
+                           (a.tree_ql <= 0 || t0 + CH <= tree_lo);
+        if (plain) {
+#pragma unroll
+            for (int nb = 0; nb < NB; ++nb)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) live[nb][e] = gq + 8 * (e >> 1) < nrow;
+            any = true;   // row 0 exists
+        } else {
             const uint32_t *sMb = reinterpret_cast<const uint32_t *>(st + L.mb);
 #pragma unroll
             for (int nb = 0; nb < NB; ++nb)
